@@ -1,0 +1,173 @@
+"""fp64 CPU oracle of the Mamba selective-scan layer -- TEST INFRASTRUCTURE.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The library under
+``selective_state_space_118_b300`` never imports it, and it imports nothing
+from the library: the two share no code.
+
+The arithmetic lives in ``mamba_oracle.c`` (plain sequential fp64 loops; see
+its header for the definition and the page sections it follows).  This module
+only compiles that file with gcc, converts arrays to contiguous fp64 and calls
+it through ctypes.
+
+Functions
+---------
+scan(...)          sequential scan over a whole sequence (prefill)
+scan_chunked(...)  the same scan evaluated chunk by chunk with a carried,
+                   decayed chunk state (checks the chunked decomposition)
+step(...)          one decode token, state updated in place
+build()            compile ``liboracle.so`` next to this file
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mamba_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+_P = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False) -> str:
+    """Compile mamba_oracle.c into liboracle.so (gcc, -O2, OpenMP)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99",
+           "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    i = ctypes.c_int
+    lib.oracle_scan_f64.argtypes = [i, i, i, i, i] + [_P] * 14 + [i]
+    lib.oracle_scan_f64.restype = None
+    lib.oracle_scan_chunked_f64.argtypes = [i, i, i, i, i, i] + [_P] * 14
+    lib.oracle_scan_chunked_f64.restype = None
+    lib.oracle_step_f64.argtypes = [i, i, i, i] + [_P] * 12
+    lib.oracle_step_f64.restype = None
+    return lib
+
+
+def _load(lib=None):
+    """The default oracle library, or `lib` when given (a path or a handle):
+    the tests load deliberately mutated copies this way."""
+    global _lib
+    if lib is not None:
+        return _bind(lib) if isinstance(lib, str) else lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(build())
+    return _lib
+
+
+def compile_variant(src_text: str, out_path: str) -> str:
+    """Compile C source text (e.g. a mutated copy of mamba_oracle.c, for the
+    tests that check the pins catch planted mistakes) into out_path."""
+    c_path = out_path + ".c"
+    with open(c_path, "w") as f:
+        f.write(src_text)
+    subprocess.run(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99", "-o",
+                    out_path, c_path, "-lm"], check=True)
+    return out_path
+
+
+def source() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+def f64(a) -> np.ndarray:
+    """Contiguous fp64 numpy copy of a numpy array or a (CPU/CUDA) torch tensor.
+
+    bf16 and fp32 values convert to fp64 exactly, so the oracle sees the very
+    values the GPU receives.
+    """
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor
+        import torch
+        a = a.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(_P)
+
+
+def scan(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=None,
+         conv_state0=None, n_threads: int = 0, lib=None):
+    """Sequential fp64 scan.  Shapes: x, z, dt_raw (B,L,D); Bm, Cm (B,L,N);
+    A_log (D,N); Dskip (D,); conv_w (D,K); conv_b (D,) or None;
+    h0 (B,D,N) or None; conv_state0 (B,K-1,D) or None.
+    Returns (y (B,L,D), final_h (B,D,N), final_conv_state (B,K-1,D))."""
+    lib = _load(lib)
+    x, z, dt_raw, Bm, Cm = map(f64, (x, z, dt_raw, Bm, Cm))
+    A_log, Dskip, conv_w, conv_b, h0, conv_state0 = map(
+        f64, (A_log, Dskip, conv_w, conv_b, h0, conv_state0))
+    B, L, D = x.shape
+    N = A_log.shape[1]
+    K = conv_w.shape[1]
+    y = np.zeros((B, L, D))
+    fh = np.zeros((B, D, N))
+    fcs = np.zeros((B, max(K - 1, 0), D))
+    lib.oracle_scan_f64(B, L, D, N, K, _ptr(x), _ptr(z), _ptr(dt_raw), _ptr(Bm),
+                        _ptr(Cm), _ptr(A_log), _ptr(Dskip), _ptr(conv_w),
+                        _ptr(conv_b), _ptr(h0), _ptr(conv_state0), _ptr(y),
+                        _ptr(fh), _ptr(fcs), int(n_threads))
+    return y, fh, fcs
+
+
+def scan_chunked(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None,
+                 h0=None, conv_state0=None, chunk: int = 64, lib=None):
+    """The scan evaluated chunk by chunk (see mamba_oracle.c); same outputs."""
+    lib = _load(lib)
+    x, z, dt_raw, Bm, Cm = map(f64, (x, z, dt_raw, Bm, Cm))
+    A_log, Dskip, conv_w, conv_b, h0, conv_state0 = map(
+        f64, (A_log, Dskip, conv_w, conv_b, h0, conv_state0))
+    B, L, D = x.shape
+    N = A_log.shape[1]
+    K = conv_w.shape[1]
+    y = np.zeros((B, L, D))
+    fh = np.zeros((B, D, N))
+    fcs = np.zeros((B, max(K - 1, 0), D))
+    lib.oracle_scan_chunked_f64(B, L, D, N, K, int(chunk), _ptr(x), _ptr(z),
+                                _ptr(dt_raw), _ptr(Bm), _ptr(Cm), _ptr(A_log),
+                                _ptr(Dskip), _ptr(conv_w), _ptr(conv_b),
+                                _ptr(h0), _ptr(conv_state0), _ptr(y), _ptr(fh),
+                                _ptr(fcs))
+    return y, fh, fcs
+
+
+def step(h, conv_state, x_t, z_t, dt_raw_t, B_t, C_t, A_log, Dskip, conv_w,
+         conv_b=None, lib=None):
+    """One fp64 decode token.  h (B,D,N) and conv_state (B,K-1,D) are taken
+    as fp64 copies, updated and returned: (y_t (B,D), h, conv_state)."""
+    lib = _load(lib)
+    h = f64(h).copy()
+    conv_state = f64(conv_state).copy()
+    x_t, z_t, dt_raw_t, B_t, C_t = map(f64, (x_t, z_t, dt_raw_t, B_t, C_t))
+    A_log, Dskip, conv_w, conv_b = map(f64, (A_log, Dskip, conv_w, conv_b))
+    B, D = x_t.shape
+    N = A_log.shape[1]
+    K = conv_w.shape[1]
+    y = np.zeros((B, D))
+    lib.oracle_step_f64(B, D, N, K, _ptr(h), _ptr(conv_state), _ptr(x_t),
+                        _ptr(z_t), _ptr(dt_raw_t), _ptr(B_t), _ptr(C_t),
+                        _ptr(A_log), _ptr(Dskip), _ptr(conv_w), _ptr(conv_b),
+                        _ptr(y))
+    return y, h, conv_state
