@@ -1,0 +1,452 @@
+#!/usr/bin/env python
+"""Benchmark of the selective-scan library on synthetic Jamba-shaped inputs.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload NAME] [--no-decode] [--no-e2e] [--no-cpu-baseline]
+
+A step is one prefill pass of the layer (conv, SiLU, softplus, discretised
+scan, D skip, SiLU(z) gate; final h and conv state) over the workload's whole
+batch, through the C ABI, inputs resident in HBM (larger than L2).  Prints
+one JSON line on rank 0.  Under torchrun every rank runs an independent
+replica (the scan has no cross-device exchange): value = elements all ranks
+processed / max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle (the definition the library is
+checked against) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selective_state_space_118_b300 import inputs  # noqa: E402
+
+METRIC = "selective-scan elements/s (B*L*d_inner), HBM GB/s vs B300 peak; decode steps/s"
+UNIT = "elements/s"
+D_STATE, D_CONV = 16, 4
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0) if torch.cuda.is_available() else None
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], device="cuda", dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class _Nvml:
+    """Minimal read-only NVML access through the driver's libnvidia-ml (ctypes):
+    SM clock, max SM clock and the active clock-event reasons."""
+
+    def __init__(self, device_index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        self._check(self.lib.nvmlInit_v2())
+        props = torch.cuda.get_device_properties(device_index)
+        self.h = ctypes.c_void_p()
+        uuid = str(getattr(props, "uuid", ""))
+        rc = 1
+        if uuid:
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            rc = self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h))
+        if rc != 0:
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+            self._check(self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)))
+
+    @staticmethod
+    def _check(rc):
+        if rc != 0:
+            raise RuntimeError(f"NVML error {rc}")
+
+    def sm_clock(self):
+        v = self.ct.c_uint()
+        self._check(self.lib.nvmlDeviceGetClockInfo(self.h, 1, self.ct.byref(v)))  # NVML_CLOCK_SM
+        return v.value
+
+    def max_sm_clock(self):
+        v = self.ct.c_uint()
+        self._check(self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, self.ct.byref(v)))
+        return v.value
+
+    def reasons(self):
+        v = self.ct.c_ulonglong()
+        self._check(self.lib.nvmlDeviceGetCurrentClocksEventReasons(self.h, self.ct.byref(v)))
+        return v.value
+
+
+class ClockSampler:
+    """Polls NVML (read-only) every millisecond while the timed region runs."""
+
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting"}
+
+    def __init__(self, device_index: int, period_s: float = 0.001):
+        self.samples, self.reasons, self.max_mhz, self.error = [], 0, None, None
+        self.period = period_s
+        self._stop = threading.Event()
+        self.nv = None
+        try:
+            self.nv = _Nvml(device_index)
+            self.max_mhz = self.nv.max_sm_clock()
+        except Exception as e:  # report, do not guess
+            self.nv, self.error = None, f"{type(e).__name__}: {e}"
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.sm_clock())
+                self.reasons |= int(self.nv.reasons())
+            except Exception as e:
+                self.error = f"{type(e).__name__}: {e}"
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.nv is not None:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self.nv is not None:
+            self.t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"],
+                    "samples": 0, "error": self.error}
+        reasons = [n for bit, n in self.REASONS.items() if self.reasons & bit]
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- byte counts
+def scan_algorithmic_bytes(B, L, D, es):
+    """Minimum HBM bytes of one prefill call: x, z, dt_raw read and y written
+    once; B, C rows; parameters; final h (fp32) and final conv state."""
+    act = 4 * B * L * D * es
+    bc = 2 * B * L * D_STATE * es
+    params = D * (D_STATE + 1 + D_CONV + 1) * 4
+    state = B * D * D_STATE * 4 + B * (D_CONV - 1) * D * es
+    return act + bc + params + state
+
+
+def decode_algorithmic_bytes(B, D, es):
+    """Minimum HBM bytes of one decode step of one layer: h read and written
+    (fp32), x_t, z_t, dt_raw_t read and y_t written, the conv state's 3
+    values read and one written, B_t and C_t."""
+    return B * D * (2 * D_STATE * 4 + 4 * es + 4 * es) + 2 * B * D_STATE * es
+
+
+# ---------------------------------------------------------------- our arm
+def scan_call(ops, inp, out, ws, stream):
+    ops.mamba_scan_fwd(inp["x"], inp["z"], inp["dt_raw"], inp["Bm"], inp["Cm"], inp["A_log"],
+                       inp["Dskip"], inp["conv_w"], inp["conv_b"], None, None, y=out["y"],
+                       final_h=out["fh"], final_conv_state=out["fcs"], workspace=ws,
+                       stream=stream)
+
+
+def bench_prefill(w, steps, warmup, world, local):
+    from selective_state_space_118_b300 import ops
+    dev = torch.device("cuda", local)
+    inp = inputs.workload_inputs(w, device=dev)
+    B, L, D = w.batch, w.seqlen, w.d_inner
+    es = 2 if w.io == "bf16" else 4
+    out = {"y": torch.empty_like(inp["x"]),
+           "fh": torch.empty(B, D, D_STATE, device=dev),
+           "fcs": torch.empty(B, D_CONV - 1, D, device=dev, dtype=inp["x"].dtype)}
+    nbytes = ops.mamba_scan_workspace_size(B, L, D, 0)
+    ws = torch.empty(max(nbytes, 1), device=dev, dtype=torch.uint8) if nbytes else None
+    n_chunks = ops.mamba_scan_default_chunks(B, L, D)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        scan_call(ops, inp, out, ws, stream)
+    torch.cuda.synchronize(dev)
+    assert ops.mamba_last_error(stream) == ops.MAMBA_OK
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with ClockSampler(dev.index) as clk:
+        ev[0].record(stream)
+        for i in range(steps):
+            scan_call(ops, inp, out, ws, stream)
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    assert ops.mamba_last_error(stream) == ops.MAMBA_OK
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    t_total_ms = ev[0].elapsed_time(ev[steps])
+    t_max_ms = max_over_ranks(t_total_ms, world)
+    elems = B * L * D
+    alg = scan_algorithmic_bytes(B, L, D, es)
+    res = dict(elems=elems, t_ms=t_max_ms, per_launch_ms=statistics.mean(per),
+               per_launch_min_ms=min(per), alg_bytes=alg, n_chunks=n_chunks,
+               launches_per_step=1 if n_chunks == 1 else 2, clocks=clk.summary(),
+               in_bytes=sum(inp[k].numel() * inp[k].element_size()
+                            for k in ("x", "z", "dt_raw", "Bm", "Cm")),
+               out_bytes=out["y"].numel() * out["y"].element_size())
+    return res, inp, out, ws
+
+
+def bench_e2e(w, inp, out, ws, steps, local):
+    """Same metric through the C ABI with the inputs in pinned HOST memory:
+    every step copies x, z, dt_raw, B, C host->device, scans, and copies y
+    device->host, all inside the timed region."""
+    from selective_state_space_118_b300 import ops
+    dev = torch.device("cuda", local)
+    host = {k: torch.empty(inp[k].shape, dtype=inp[k].dtype, pin_memory=True)
+            for k in ("x", "z", "dt_raw", "Bm", "Cm")}
+    for k in host:
+        host[k].copy_(inp[k])
+    y_host = torch.empty(out["y"].shape, dtype=out["y"].dtype, pin_memory=True)
+    dbuf = {k: torch.empty_like(inp[k]) for k in host}
+    dinp = dict(inp, **dbuf)
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        for k in host:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        scan_call(ops, dinp, out, ws, stream)
+        y_host.copy_(out["y"], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t = e0.elapsed_time(e1) / 1e3
+    bi = sum(h.numel() * h.element_size() for h in host.values())
+    bo = y_host.numel() * y_host.element_size()
+    return {"t": t, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "steps": steps, "ms_per_step": t * 1e3 / steps}
+
+
+def bench_decode(w, local, replays=3):
+    """28 layers x 256 tokens, one mamba_step per layer and token, replayed
+    from one CUDA graph.  decode steps/s = tokens (for all 64 sequences
+    through all layers) per second."""
+    from selective_state_space_118_b300 import ops
+    dev = torch.device("cuda", local)
+    states = [inputs.decode_layer_state(w, l, device=dev) for l in range(w.layers)]
+    toks = [inputs.decode_token_inputs(w, l, w.steps, device=dev) for l in range(w.layers)]
+    ys = [torch.empty(w.batch, w.d_inner, device=dev, dtype=inputs.torch_dtype(w.io))
+          for _ in range(w.layers)]
+    stream = torch.cuda.Stream(dev)
+
+    def run_all():
+        for t in range(w.steps):
+            for l in range(w.layers):
+                st, tk = states[l], toks[l]
+                ops.mamba_step(st["h"], st["conv_state"], tk["x_t"][t], tk["z_t"][t],
+                               tk["dt_raw_t"][t], tk["B_t"][t], tk["C_t"][t], st["A_log"],
+                               st["Dskip"], st["conv_w"], st["conv_b"], y_t=ys[l], stream=stream)
+
+    with torch.cuda.stream(stream):
+        run_all()  # warm-up, outside the graph
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run_all()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk, torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()  # replays on the current stream, i.e. `stream`
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    t = e0.elapsed_time(e1) / 1e3 / replays
+    launches = w.layers * w.steps
+    es = 2 if w.io == "bf16" else 4
+    alg = decode_algorithmic_bytes(w.batch, w.d_inner, es)
+    hbm, src = peaks()
+    per_launch = t / launches
+    return {"metric": "decode steps/s", "value": w.steps / t, "unit": "steps/s",
+            "config": {"workload": w.name, "layers": w.layers, "batch": w.batch,
+                       "d_inner": w.d_inner, "tokens": w.steps, "cuda_graph": True},
+            "ms_per_token": t * 1e3 / w.steps,
+            "roofline": {"bound": "hbm", "achieved": alg / per_launch / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": alg / per_launch / 1e9 / hbm,
+                         "traffic": None, "peak_source": src,
+                         "note": "per-launch time = graph replay time / launches (gaps included)"},
+            "gpu_launches": launches * replays, "clocks": clk.summary()}
+
+
+# ---------------------------------------------------------------- oracle arm
+def oracle_sample_rate(w, target_s: float, max_channels: int = 2048):
+    """Times the fp64 oracle on an evenly strided subset of channels of the
+    workload (exact per channel: channels are independent) for about
+    target_s seconds of CPU work; returns elements/s and a description."""
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    L = w.seqlen
+    inp = inputs.workload_inputs(inputs.ScanWorkload(w.name, w.batch, L, 16, w.io, w.seed, w.bc_std),
+                                 device="cpu")
+    t0 = time.perf_counter()
+    oracle.scan(inp["x"][:, :, :1], inp["z"][:, :, :1], inp["dt_raw"][:, :, :1], inp["Bm"],
+                inp["Cm"], inp["A_log"][:1], inp["Dskip"][:1], inp["conv_w"][:1], inp["conv_b"][:1],
+                n_threads=1)
+    per_row = max(time.perf_counter() - t0, 1e-4)
+    rows = int(target_s * threads / per_row)
+    ch = int(min(max(rows // w.batch, min(threads, w.d_inner)), w.d_inner, max_channels))
+    ch = max(ch, 1)
+    inp = inputs.workload_inputs(inputs.ScanWorkload(w.name, w.batch, L, ch, w.io, w.seed, w.bc_std),
+                                 device="cpu")
+    t0 = time.perf_counter()
+    oracle.scan(inp["x"], inp["z"], inp["dt_raw"], inp["Bm"], inp["Cm"], inp["A_log"],
+                inp["Dskip"], inp["conv_w"], inp["conv_b"], n_threads=threads)
+    t = time.perf_counter() - t0
+    elems = w.batch * L * ch
+    return elems / t, {"kind": "oracle", "cores": threads,
+                       "sample": f"{ch} of {w.d_inner} channels x all {L} tokens x batch {w.batch} "
+                                 f"({elems} elements, {t:.1f} s); elements/s extrapolate exactly "
+                                 f"since channels are independent"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = workload_of(args)
+    vals = []
+    desc = None
+    for i in range(args.warmup + args.steps):
+        v, desc = oracle_sample_rate(w, target_s=2.0, max_channels=256)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": w.batch * w.seqlen * w.d_inner / value * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w, None),
+            "cpu_baseline": dict(desc, value=value, unit=UNIT),
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_of(args):
+    w = inputs.SCAN_WORKLOADS[args.workload]
+    if args.seqlen:
+        w = inputs.ScanWorkload(f"{w.name}@L{args.seqlen}", w.batch, args.seqlen, w.d_inner, w.io,
+                                w.seed, w.bc_std)
+    return w
+
+
+def config_of(w, n_chunks):
+    return {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "d_inner": w.d_inner,
+            "d_state": D_STATE, "d_conv": D_CONV, "io": w.io, "n_chunks": n_chunks,
+            "l2": "inputs larger than L2 (no flush needed)", "parallelism": "replicas"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=inputs.JAMBA_PREFILL.name, choices=list(inputs.SCAN_WORKLOADS))
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seqlen", type=int, default=0,
+                    help="override the workload's sequence length (smaller cases for profiling)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    from selective_state_space_118_b300 import build, ops
+    if rank == 0 and not os.path.exists(ops.LIB_PATH):
+        build.build()
+    barrier(world)
+    w = workload_of(args)
+    res, inp, out, ws = bench_prefill(w, args.steps, args.warmup, world, local)
+    elems_all = res["elems"] * args.steps * world
+    value = elems_all / (res["t_ms"] / 1e3)
+    hbm, src = peaks()
+    achieved = res["alg_bytes"] / (res["per_launch_ms"] / 1e3) / 1e9
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["t_ms"] / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.io,
+            "data": "synthetic", "config": config_of(w, res["n_chunks"]),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": None, "peak_source": src,
+                         "kernel": "scan_fwd_kernel",
+                         "algorithmic_bytes_per_launch": res["alg_bytes"]},
+            "gpu_launches": res["launches_per_step"] * args.steps,
+            "clocks": res["clocks"]}
+    if not args.no_e2e:
+        e2e = bench_e2e(w, inp, out, ws, max(2, min(args.steps, 5)), local)
+        t = max_over_ranks(e2e.pop("t"), world)
+        e2e = dict(value=res["elems"] * e2e["steps"] * world / t, **e2e)
+        line["e2e"] = e2e
+    del inp, out, ws
+    torch.cuda.empty_cache()
+    if not args.no_decode:
+        line["decode"] = bench_decode(inputs.DECODE, local)
+        torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        v, desc = oracle_sample_rate(w, target_s=10.0)
+        line["cpu_baseline"] = dict(desc, value=v, unit=UNIT)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

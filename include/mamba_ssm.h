@@ -1,0 +1,169 @@
+/*
+ * mamba_ssm.h -- C ABI of the B300 (sm_103a) Mamba selective-scan library
+ * (libmamba_ssm.so).
+ *
+ * The operation.  A Mamba layer's selective state-space scan, as built in
+ * "【大模型】- Jamba 混合 SSM-Transformer" (sxl-space.tk), section
+ * "实现 > Mamba 层" (MambaBlock.forward and MambaBlock.ssm), with the
+ * read-out y_t = C h_t of the lesson "Jamba -- SSM-Transformer Hibrido"
+ * (ai-engineering.academy), section "Um SSM em uma pagina".  For every batch
+ * row b and channel c, with A_n = -exp(A_log[c,n]) and t = 0..L-1:
+ *
+ *   u    = silu(conv_b[c] + sum_{k=0..3} conv_w[c,k] * x[b,t-3+k,c])
+ *          (causal depthwise conv, d_conv = 4; inputs before t = 0 come from
+ *           conv_state0, or are zero)
+ *   dt   = softplus(dt_raw[b,t,c])          (beta 1, threshold 20)
+ *   h_n  = exp(dt*A_n) * h_n + dt*B[b,t,n]*u  (n = 0..15; h starts at h0 or 0)
+ *   y    = (sum_n C[b,t,n]*h_n + D[c]*u) * silu(z[b,t,c])
+ *
+ * The projections around the scan (in_proj producing x and z, x_proj
+ * producing B, C and the dt input, dt_proj, out_proj) are not part of this
+ * library: the caller passes their results.
+ *
+ * Conventions for every call below.
+ *  - All tensor pointers are DEVICE pointers (CUDA global memory), row-major
+ *    and contiguous, 16-byte aligned, owned by the caller.  The library never
+ *    allocates, frees or keeps them.
+ *  - `io` tensors (activations) are fp32 or bf16 as chosen by `io`;
+ *    parameters and the SSM state h are always fp32.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and never synchronise.  Argument errors are reported
+ *    before anything is launched; a launch failure returns MAMBA_ERR_CUDA.
+ *  - d_state must be 16 and d_conv 4 (the layer's defaults); d_inner must be
+ *    a multiple of 16.
+ *  - A device-side wait that gives up (it cannot, in a healthy run) sets a
+ *    sticky error word that mamba_last_error() reports.
+ */
+#ifndef MAMBA_SSM_H
+#define MAMBA_SSM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MAMBA_OK = 0,
+    MAMBA_ERR_INVALID_ARG = 1,   /* null required pointer, bad size, misalignment */
+    MAMBA_ERR_UNSUPPORTED = 2,   /* d_state != 16, d_conv != 4, d_inner % 16, dtype */
+    MAMBA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+    MAMBA_ERR_TIMEOUT = 4,       /* a device-side wait gave up (sticky, see below) */
+    MAMBA_ERR_WORKSPACE = 5      /* workspace missing or smaller than required */
+} mamba_status;
+
+typedef enum { MAMBA_F32 = 0, MAMBA_BF16 = 1 } mamba_dtype;
+
+#define MAMBA_D_STATE 16
+#define MAMBA_D_CONV 4
+
+/* Test switch for mamba_scan_args.flags: the kernel skips issuing its first
+ * input copy and so waits on a barrier that never completes; the wait gives
+ * up after wait_timeout_ns and the call reports MAMBA_ERR_TIMEOUT through
+ * mamba_last_error().  Never set in normal use. */
+#define MAMBA_FLAG_TEST_STALL_FIRST_LOAD 0x1u
+
+/*
+ * Prefill: the scan over a whole sequence (MambaBlock.forward minus the
+ * projections).
+ *
+ *   x, z, dt_raw      (B, L, D) io        inputs (read once)
+ *   Bm, Cm            (B, L, 16) io       per-token B and C rows
+ *   A_log             (D, 16) fp32        A = -exp(A_log)
+ *   Dskip             (D) fp32            D, the skip weight
+ *   conv_w            (D, 4) fp32         conv taps; conv_w[c,3] multiplies x_t
+ *   conv_b            (D) fp32 or NULL    conv bias (NULL: zero)
+ *   h0                (B, D, 16) fp32 or NULL     initial state (NULL: zero)
+ *   conv_state0       (B, 3, D) io or NULL        the 3 inputs before t = 0,
+ *                                                 oldest first (NULL: zero)
+ *   y                 (B, L, D) io        output (written once)
+ *   final_h           (B, D, 16) fp32 or NULL     state after the last token;
+ *                                                 may alias h0
+ *   final_conv_state  (B, 3, D) io or NULL        last 3 inputs; may alias
+ *                                                 conv_state0
+ *   workspace         device scratch of at least mamba_scan_workspace_size()
+ *                     bytes, 256-byte aligned (B and C widened to fp32,
+ *                     B*L*128 bytes, plus the chunk carries in chunked mode);
+ *                     its contents need not be initialised and are not kept
+ *   n_chunks          0: the library picks; 1: one sequential pass over L;
+ *                     k > 1: L is cut into k chunks (a multiple of 64 tokens
+ *                     each, the last one shorter) that run in parallel, each
+ *                     chunk's carried-in state being the decayed end states of
+ *                     the chunks before it (two passes; results agree with the
+ *                     sequential pass to rounding)
+ *   flags             0, or MAMBA_FLAG_TEST_* (tests only)
+ *   wait_timeout_ns   limit of every device-side wait (0: 1 second)
+ *
+ * seqlen may be 0 (then only final_h/final_conv_state are written: copies of
+ * h0/conv_state0, or zeros).  batch and d_inner must be > 0.
+ */
+typedef struct mamba_scan_args {
+    int batch, seqlen, d_inner, d_state, d_conv;
+    mamba_dtype io;
+    const void *x, *z, *dt_raw;
+    const void *Bm, *Cm;
+    const float *A_log, *Dskip, *conv_w, *conv_b;
+    const float *h0;
+    const void *conv_state0;
+    void *y;
+    float *final_h;
+    void *final_conv_state;
+    void *workspace;
+    size_t workspace_bytes;
+    int n_chunks;
+    uint32_t flags;
+    uint64_t wait_timeout_ns;
+} mamba_scan_args;
+
+/* Bytes of workspace mamba_scan_fwd needs for these sizes and n_chunks
+ * (0 = the library's choice); 0 only for invalid sizes or seqlen 0. */
+size_t mamba_scan_workspace_size(int batch, int seqlen, int d_inner, int n_chunks);
+
+/* The number of chunks mamba_scan_fwd uses when n_chunks = 0. */
+int mamba_scan_default_chunks(int batch, int seqlen, int d_inner);
+
+mamba_status mamba_scan_fwd(const mamba_scan_args *args, void *stream);
+
+/*
+ * Decode: one token through the layer, state updated in place -- the
+ * constant-memory recurrence of "Um SSM em uma pagina" (y_t needs only
+ * h_{t-1} and x_t).  Bit for bit the same arithmetic as one token of
+ * mamba_scan_fwd with n_chunks = 1.
+ *
+ *   h                 (B, D, 16) fp32     in/out, in place
+ *   conv_state        (B, 3, D) io        in/out, in place (shifts by one)
+ *   x_t, z_t, dt_raw_t  (B, D) io
+ *   B_t, C_t          (B, 16) io
+ *   A_log, Dskip, conv_w, conv_b   as for the scan
+ *   y_t               (B, D) io           output
+ */
+typedef struct mamba_step_args {
+    int batch, d_inner, d_state, d_conv;
+    mamba_dtype io;
+    float *h;
+    void *conv_state;
+    const void *x_t, *z_t, *dt_raw_t;
+    const void *B_t, *C_t;
+    const float *A_log, *Dskip, *conv_w, *conv_b;
+    void *y_t;
+} mamba_step_args;
+
+mamba_status mamba_step(const mamba_step_args *args, void *stream);
+
+/* Synchronises `stream`, then reads and clears the sticky device error word
+ * of the current device: MAMBA_OK, or MAMBA_ERR_TIMEOUT if a device-side
+ * wait gave up since the last call. */
+mamba_status mamba_last_error(void *stream);
+
+/* A static, human-readable name of a status code. */
+const char *mamba_status_string(mamba_status s);
+
+/* Library ABI version (major * 100 + minor). */
+int mamba_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAMBA_SSM_H */

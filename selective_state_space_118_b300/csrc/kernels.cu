@@ -1,0 +1,87 @@
+// kernels.cu -- the one translation unit holding the device code (prefill,
+// chunk summary, decode step and the sticky error word) and its launchers.
+#include <cuda_bf16.h>
+
+#include "launch.h"
+#include "scan_fwd.cuh"
+#include "step.cuh"
+
+namespace mamba {
+
+size_t scan_smem_bytes(IoType io) {
+  return (io == IoType::BF16 ? sizeof(ScanSmem<__nv_bfloat16>) : sizeof(ScanSmem<float>)) + 128;
+}
+
+size_t summary_smem_bytes(IoType io) {
+  return (io == IoType::BF16 ? sizeof(SummarySmem<__nv_bfloat16>) : sizeof(SummarySmem<float>)) + 128;
+}
+
+template <typename IO>
+static cudaError_t launch_scan_t(const CUtensorMap* m, const ScanParams& p, dim3 grid, cudaStream_t s) {
+  const size_t smem = sizeof(ScanSmem<IO>) + 128;
+  cudaError_t e = cudaFuncSetAttribute(scan_fwd_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  scan_fwd_kernel<IO><<<grid, kScanThreads, smem, s>>>(m[0], m[1], m[2], m[3], m[4], p);
+  return cudaGetLastError();
+}
+
+template <typename IO>
+static cudaError_t launch_summary_t(const CUtensorMap* m, const ScanParams& p, dim3 grid, cudaStream_t s) {
+  const size_t smem = sizeof(SummarySmem<IO>) + 128;
+  cudaError_t e = cudaFuncSetAttribute(scan_chunk_summary_kernel<IO>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  scan_chunk_summary_kernel<IO><<<grid, kScanThreads, smem, s>>>(m[0], m[1], m[2], p);
+  return cudaGetLastError();
+}
+
+template <typename IO>
+static cudaError_t launch_widen_t(const void* Bm, const void* Cm, float* bc, long rows, cudaStream_t s) {
+  const long n = rows * 8;
+  long blocks = (n + 255) / 256;
+  if (blocks > 148L * 16) blocks = 148L * 16;
+  if (blocks < 1) blocks = 1;
+  bc_widen_kernel<IO><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const IO*>(Bm), static_cast<const IO*>(Cm),
+                                                        bc, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bc_widen(IoType io, const void* Bm, const void* Cm, float* bc, long rows,
+                            cudaStream_t stream) {
+  return io == IoType::BF16 ? launch_widen_t<__nv_bfloat16>(Bm, Cm, bc, rows, stream)
+                            : launch_widen_t<float>(Bm, Cm, bc, rows, stream);
+}
+
+cudaError_t launch_scan(IoType io, const CUtensorMap maps[5], const ScanParams& p, dim3 grid,
+                        cudaStream_t stream) {
+  return io == IoType::BF16 ? launch_scan_t<__nv_bfloat16>(maps, p, grid, stream)
+                            : launch_scan_t<float>(maps, p, grid, stream);
+}
+
+cudaError_t launch_summary(IoType io, const CUtensorMap maps[3], const ScanParams& p, dim3 grid,
+                           cudaStream_t stream) {
+  return io == IoType::BF16 ? launch_summary_t<__nv_bfloat16>(maps, p, grid, stream)
+                            : launch_summary_t<float>(maps, p, grid, stream);
+}
+
+cudaError_t launch_step(IoType io, const StepParams& p, cudaStream_t stream) {
+  const long threads = (long)p.batch * p.d_inner * 4;
+  const unsigned blocks = (unsigned)((threads + kStepThreads - 1) / kStepThreads);
+  if (io == IoType::BF16)
+    step_kernel<__nv_bfloat16><<<blocks, kStepThreads, 0, stream>>>(p);
+  else
+    step_kernel<float><<<blocks, kStepThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t take_device_error(unsigned* code, cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(code, g_mamba_error, sizeof(unsigned));
+  if (e != cudaSuccess) return e;
+  const unsigned zero = 0;
+  return cudaMemcpyToSymbol(g_mamba_error, &zero, sizeof(unsigned));
+}
+
+}  // namespace mamba

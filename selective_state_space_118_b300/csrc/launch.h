@@ -1,0 +1,35 @@
+// launch.h -- host-side launchers of the kernels (defined in kernels.cu),
+// called by the C ABI in api.cpp.  Internal; not part of the public header.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "params.h"
+
+namespace mamba {
+
+enum class IoType { F32, BF16 };
+
+// Dynamic shared memory of the prefill kernels for an I/O type.
+size_t scan_smem_bytes(IoType io);
+size_t summary_smem_bytes(IoType io);
+
+// B (rows, 16), C (rows, 16) in the I/O dtype -> bc (rows, 32) fp32.
+cudaError_t launch_bc_widen(IoType io, const void* Bm, const void* Cm, float* bc, long rows,
+                            cudaStream_t stream);
+// maps: x, z, dt_raw, bc, y (3-D tiled tensor maps).
+cudaError_t launch_scan(IoType io, const CUtensorMap maps[5], const ScanParams& p, dim3 grid,
+                        cudaStream_t stream);
+// maps: x, dt_raw, bc.
+cudaError_t launch_summary(IoType io, const CUtensorMap maps[3], const ScanParams& p, dim3 grid,
+                           cudaStream_t stream);
+cudaError_t launch_step(IoType io, const StepParams& p, cudaStream_t stream);
+
+// Reads and clears the sticky device error word of the current device
+// (synchronises the stream first).
+cudaError_t take_device_error(unsigned* code, cudaStream_t stream);
+
+}  // namespace mamba

@@ -1,0 +1,191 @@
+"""ctypes binding of libmamba_ssm.so: argument marshalling only.
+
+Every function here packs torch tensors' device pointers into the C structs
+of ``include/mamba_ssm.h`` and calls the C ABI; all arithmetic runs in the
+library's CUDA kernels.  Output and workspace tensors the caller does not
+pass are allocated with torch (device memory is torch's job; the library
+never allocates).  If the library is missing the first call raises -- there
+is no other implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmamba_ssm.so")
+
+MAMBA_OK, MAMBA_ERR_INVALID_ARG, MAMBA_ERR_UNSUPPORTED, MAMBA_ERR_CUDA, MAMBA_ERR_TIMEOUT, \
+    MAMBA_ERR_WORKSPACE = range(6)
+MAMBA_F32, MAMBA_BF16 = 0, 1
+MAMBA_FLAG_TEST_STALL_FIRST_LOAD = 0x1
+D_STATE, D_CONV = 16, 4
+
+# the functions the public header declares (checked by the tests)
+EXPORTED = ("mamba_scan_workspace_size", "mamba_scan_default_chunks", "mamba_scan_fwd",
+            "mamba_step", "mamba_last_error", "mamba_status_string", "mamba_abi_version")
+
+_vp = ctypes.c_void_p
+
+
+class ScanArgs(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("seqlen", ctypes.c_int), ("d_inner", ctypes.c_int),
+                ("d_state", ctypes.c_int), ("d_conv", ctypes.c_int), ("io", ctypes.c_int),
+                ("x", _vp), ("z", _vp), ("dt_raw", _vp), ("Bm", _vp), ("Cm", _vp),
+                ("A_log", _vp), ("Dskip", _vp), ("conv_w", _vp), ("conv_b", _vp),
+                ("h0", _vp), ("conv_state0", _vp), ("y", _vp), ("final_h", _vp),
+                ("final_conv_state", _vp), ("workspace", _vp),
+                ("workspace_bytes", ctypes.c_size_t), ("n_chunks", ctypes.c_int),
+                ("flags", ctypes.c_uint32), ("wait_timeout_ns", ctypes.c_uint64)]
+
+
+class StepArgs(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("d_inner", ctypes.c_int), ("d_state", ctypes.c_int),
+                ("d_conv", ctypes.c_int), ("io", ctypes.c_int),
+                ("h", _vp), ("conv_state", _vp), ("x_t", _vp), ("z_t", _vp), ("dt_raw_t", _vp),
+                ("B_t", _vp), ("C_t", _vp), ("A_log", _vp), ("Dskip", _vp), ("conv_w", _vp),
+                ("conv_b", _vp), ("y_t", _vp)]
+
+
+class MambaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads (once) and returns the C library with its signatures declared."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m selective_state_space_118_b300.build`")
+        lib = ctypes.CDLL(path)
+        lib.mamba_scan_workspace_size.argtypes = [ctypes.c_int] * 4
+        lib.mamba_scan_workspace_size.restype = ctypes.c_size_t
+        lib.mamba_scan_default_chunks.argtypes = [ctypes.c_int] * 3
+        lib.mamba_scan_default_chunks.restype = ctypes.c_int
+        lib.mamba_scan_fwd.argtypes = [ctypes.POINTER(ScanArgs), _vp]
+        lib.mamba_scan_fwd.restype = ctypes.c_int
+        lib.mamba_step.argtypes = [ctypes.POINTER(StepArgs), _vp]
+        lib.mamba_step.restype = ctypes.c_int
+        lib.mamba_last_error.argtypes = [_vp]
+        lib.mamba_last_error.restype = ctypes.c_int
+        lib.mamba_status_string.argtypes = [ctypes.c_int]
+        lib.mamba_status_string.restype = ctypes.c_char_p
+        lib.mamba_abi_version.argtypes = []
+        lib.mamba_abi_version.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().mamba_status_string(int(status)).decode()
+
+
+def _io_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return MAMBA_BF16
+    if t.dtype == torch.float32:
+        return MAMBA_F32
+    raise TypeError(f"I/O tensors must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def mamba_scan_workspace_size(batch: int, seqlen: int, d_inner: int, n_chunks: int = 0) -> int:
+    return int(load_library().mamba_scan_workspace_size(batch, seqlen, d_inner, n_chunks))
+
+
+def mamba_scan_default_chunks(batch: int, seqlen: int, d_inner: int) -> int:
+    return int(load_library().mamba_scan_default_chunks(batch, seqlen, d_inner))
+
+
+def mamba_scan_fwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=None,
+                   conv_state0=None, *, y=None, final_h=None, final_conv_state=None,
+                   workspace=None, n_chunks: int = 0, flags: int = 0,
+                   wait_timeout_ns: int = 0, return_state: bool = True, stream=None):
+    """Prefill scan (C ABI ``mamba_scan_fwd``).  x, z, dt_raw (B,L,D) and
+    Bm, Cm (B,L,16) in fp32 or bf16; A_log (D,16), Dskip (D), conv_w (D,4),
+    conv_b (D) fp32; h0 (B,D,16) fp32; conv_state0 (B,3,D) in the I/O dtype.
+    Returns (y, final_h, final_conv_state) (the last two None when
+    return_state is False and they were not passed)."""
+    lib = load_library()
+    B, L, D = x.shape
+    dev = x.device
+    if y is None:
+        y = torch.empty_like(x)
+    if return_state:
+        if final_h is None:
+            final_h = torch.empty((B, D, D_STATE), device=dev, dtype=torch.float32)
+        if final_conv_state is None:
+            final_conv_state = torch.empty((B, D_CONV - 1, D), device=dev, dtype=x.dtype)
+    ws_bytes = mamba_scan_workspace_size(B, L, D, n_chunks)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+    a = ScanArgs(batch=B, seqlen=L, d_inner=D, d_state=A_log.shape[-1], d_conv=conv_w.shape[-1],
+                 io=_io_code(x), x=_ptr(x), z=_ptr(z), dt_raw=_ptr(dt_raw), Bm=_ptr(Bm),
+                 Cm=_ptr(Cm), A_log=_ptr(A_log), Dskip=_ptr(Dskip), conv_w=_ptr(conv_w),
+                 conv_b=_ptr(conv_b), h0=_ptr(h0), conv_state0=_ptr(conv_state0), y=_ptr(y),
+                 final_h=_ptr(final_h), final_conv_state=_ptr(final_conv_state),
+                 workspace=_ptr(workspace),
+                 workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
+                 n_chunks=n_chunks, flags=flags, wait_timeout_ns=wait_timeout_ns)
+    for t in (z, dt_raw, Bm, Cm, conv_state0, y, final_conv_state):
+        if t is not None and t.dtype != x.dtype:
+            raise TypeError("x, z, dt_raw, Bm, Cm, conv_state0, y and final_conv_state share one dtype")
+    st = lib.mamba_scan_fwd(ctypes.byref(a), _stream(stream))
+    if st != MAMBA_OK:
+        raise MambaError(st, "mamba_scan_fwd")
+    return y, final_h, final_conv_state
+
+
+def mamba_step(h, conv_state, x_t, z_t, dt_raw_t, B_t, C_t, A_log, Dskip, conv_w, conv_b=None,
+               *, y_t=None, stream=None):
+    """One decode token (C ABI ``mamba_step``): h (B,D,16) fp32 and
+    conv_state (B,3,D) are updated in place; returns y_t (B,D)."""
+    lib = load_library()
+    B, D = x_t.shape
+    if y_t is None:
+        y_t = torch.empty_like(x_t)
+    a = StepArgs(batch=B, d_inner=D, d_state=A_log.shape[-1], d_conv=conv_w.shape[-1],
+                 io=_io_code(x_t), h=_ptr(h), conv_state=_ptr(conv_state), x_t=_ptr(x_t),
+                 z_t=_ptr(z_t), dt_raw_t=_ptr(dt_raw_t), B_t=_ptr(B_t), C_t=_ptr(C_t),
+                 A_log=_ptr(A_log), Dskip=_ptr(Dskip), conv_w=_ptr(conv_w), conv_b=_ptr(conv_b),
+                 y_t=_ptr(y_t))
+    st = lib.mamba_step(ctypes.byref(a), _stream(stream))
+    if st != MAMBA_OK:
+        raise MambaError(st, "mamba_step")
+    return y_t
+
+
+def mamba_last_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the sticky device
+    error code: MAMBA_OK or MAMBA_ERR_TIMEOUT."""
+    return int(load_library().mamba_last_error(_stream(stream)))
+
+
+def mamba_abi_version() -> int:
+    return int(load_library().mamba_abi_version())

@@ -1,0 +1,129 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/mamba_ssm.h declares, the ctypes structs match the C layout,
+and host-side argument checks return the documented status codes without
+launching anything."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from selective_state_space_118_b300 import build, ops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mamba_ssm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ops.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mamba_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_functions():
+    assert declared_functions() == sorted(ops.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", ops.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (mamba_\w+)$", out, flags=re.M))
+    missing = set(declared_functions()) - exported
+    assert not missing, f"declared but not exported: {missing}"
+    for name in declared_functions():
+        assert hasattr(lib, name)
+
+
+def _c_layout(tmp_path, struct, fields):
+    src = tmp_path / "layout.c"
+    body = "\n".join(f'printf("{f} %zu\\n", offsetof({struct}, {f}));' for f in fields)
+    src.write_text(f'#include <stdio.h>\n#include <stddef.h>\n#include "mamba_ssm.h"\n'
+                   f'int main(void) {{ printf("sizeof %zu\\n", sizeof({struct}));\n{body}\nreturn 0; }}\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.dirname(HEADER), "-o", str(exe), str(src)],
+                   check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout
+    return dict((k, int(v)) for k, v in (line.split() for line in out.splitlines()))
+
+
+@pytest.mark.parametrize("struct,cls", [("mamba_scan_args", ops.ScanArgs),
+                                        ("mamba_step_args", ops.StepArgs)])
+def test_ctypes_structs_match_c_layout(tmp_path, struct, cls):
+    fields = [f for f, _ in cls._fields_]
+    c = _c_layout(tmp_path, struct, fields)
+    assert c["sizeof"] == ctypes.sizeof(cls)
+    for f in fields:
+        assert c[f] == getattr(cls, f).offset, f
+
+
+def test_status_strings_and_version(lib):
+    assert ops.mamba_abi_version() == 100
+    for code in range(6):
+        assert ops.status_string(code)
+    assert "timed out" in ops.status_string(ops.MAMBA_ERR_TIMEOUT)
+
+
+def _args(**kw):
+    base = dict(batch=1, seqlen=8, d_inner=16, d_state=16, d_conv=4, io=ops.MAMBA_BF16)
+    base.update(kw)
+    return ops.ScanArgs(**base)
+
+
+FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced: checks fail first
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d_state=8), ops.MAMBA_ERR_UNSUPPORTED),
+    (dict(d_conv=3), ops.MAMBA_ERR_UNSUPPORTED),
+    (dict(d_inner=24), ops.MAMBA_ERR_UNSUPPORTED),
+    (dict(io=7), ops.MAMBA_ERR_UNSUPPORTED),
+    (dict(batch=0), ops.MAMBA_ERR_INVALID_ARG),
+    (dict(seqlen=-1), ops.MAMBA_ERR_INVALID_ARG),
+    (dict(), ops.MAMBA_ERR_INVALID_ARG),  # A_log, Dskip, conv_w missing
+    (dict(A_log=FAKE, Dskip=FAKE, conv_w=FAKE), ops.MAMBA_ERR_INVALID_ARG),  # x... missing
+    (dict(A_log=FAKE, Dskip=FAKE, conv_w=FAKE + 4, x=FAKE, z=FAKE, dt_raw=FAKE, Bm=FAKE, Cm=FAKE,
+          y=FAKE), ops.MAMBA_ERR_INVALID_ARG),  # misaligned conv_w
+    (dict(A_log=FAKE, Dskip=FAKE, conv_w=FAKE, x=FAKE + 2, z=FAKE, dt_raw=FAKE, Bm=FAKE, Cm=FAKE,
+          y=FAKE), ops.MAMBA_ERR_INVALID_ARG),  # misaligned x
+    (dict(batch=1, seqlen=4096, d_inner=16, n_chunks=4, A_log=FAKE, Dskip=FAKE, conv_w=FAKE, x=FAKE,
+          z=FAKE, dt_raw=FAKE, Bm=FAKE, Cm=FAKE, y=FAKE), ops.MAMBA_ERR_WORKSPACE),
+])
+def test_scan_argument_checks(lib, kw, status):
+    a = _args(**kw)
+    assert lib.mamba_scan_fwd(ctypes.byref(a), None) == status
+    assert lib.mamba_scan_fwd(None, None) == ops.MAMBA_ERR_INVALID_ARG
+
+
+def test_step_argument_checks(lib):
+    a = ops.StepArgs(batch=1, d_inner=16, d_state=16, d_conv=4, io=ops.MAMBA_BF16)
+    assert lib.mamba_step(ctypes.byref(a), None) == ops.MAMBA_ERR_INVALID_ARG
+    a.d_state = 32
+    assert lib.mamba_step(ctypes.byref(a), None) == ops.MAMBA_ERR_UNSUPPORTED
+    assert lib.mamba_step(None, None) == ops.MAMBA_ERR_INVALID_ARG
+
+
+def test_workspace_plan(lib):
+    def r256(v):
+        return (v + 255) // 256 * 256
+    # one sequential pass: only B and C widened to fp32, (B, L, 32)
+    assert ops.mamba_scan_workspace_size(1, 32768, 8192, 1) == r256(32768 * 32 * 4)
+    assert ops.mamba_scan_workspace_size(2, 2048, 1024, 1) == r256(2 * 2048 * 32 * 4)
+    assert ops.mamba_scan_workspace_size(2, 0, 1024, 1) == 0
+    # chunked: plus carries for every chunk, summaries for all but the last, counters
+    B, L, D, n = 2, 4096, 64, 4
+    ws = ops.mamba_scan_workspace_size(B, L, D, n)
+    need = (B * L * 32 * 4 + B * n * D * 16 * 4 + B * (n - 1) * D * 16 * 4 + B * (n - 1) * D * 4
+            + B * (D // 16) * 4)
+    assert need <= ws <= need + 5 * 256
+    # a chunk count larger than the number of 64-token tiles is clamped
+    assert ops.mamba_scan_workspace_size(1, 100, 16, 50) == ops.mamba_scan_workspace_size(1, 100, 16, 2)
+    assert ops.mamba_scan_default_chunks(1, 64, 16) == 1
+    assert ops.mamba_scan_default_chunks(1, 32768, 8192) == 1
+    assert ops.mamba_scan_default_chunks(1, 32768, 16) > 1

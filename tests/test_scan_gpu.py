@@ -1,0 +1,152 @@
+"""Prefill scan on the GPU (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from parity import assert_close, io_name, oracle_scan, to_device
+from selective_state_space_118_b300 import inputs, ops
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(inp, **kw):
+    return ops.mamba_scan_fwd(inp["x"], inp["z"], inp["dt_raw"], inp["Bm"], inp["Cm"],
+                              inp["A_log"], inp["Dskip"], inp["conv_w"], inp.get("conv_b"),
+                              inp.get("h0"), inp.get("conv_state0"), **kw)
+
+
+def check_against_oracle(inp, outs, what=""):
+    y, fh, fcs = outs
+    torch.cuda.synchronize()
+    yr, fhr, fcsr = oracle_scan(inp)
+    io = io_name(inp["x"])
+    assert_close(y, yr, io, f"{what} y")
+    assert_close(fh, fhr, io, f"{what} final_h", fp32_output=True)
+    np.testing.assert_array_equal(fcs.double().cpu().numpy(), fcsr)
+
+
+def test_tiny_f32_workload():
+    w = inputs.TINY_F32
+    inp = inputs.workload_inputs(w, device="cuda")
+    check_against_oracle(inp, run_gpu(inp), w.name)
+
+
+@pytest.mark.parametrize("n_chunks", [0, 1, 4])
+def test_small_bf16_workload(n_chunks):
+    w = inputs.SMALL_BF16
+    inp = inputs.workload_inputs(w, device="cuda")
+    check_against_oracle(inp, run_gpu(inp, n_chunks=n_chunks), f"{w.name} n_chunks={n_chunks}")
+
+
+EDGE = [
+    # (B, L, D, io, with_state, conv_b, n_chunks)
+    (1, 1, 16, "f32", False, True, 1),
+    (1, 2, 16, "bf16", True, True, 1),
+    (2, 3, 32, "f32", True, False, 1),
+    (1, 5, 16, "bf16", False, True, 1),
+    (3, 63, 48, "f32", True, True, 1),
+    (1, 64, 16, "bf16", True, True, 1),
+    (2, 65, 32, "bf16", True, False, 1),
+    (1, 130, 16, "f32", True, True, 1),
+    (2, 257, 48, "bf16", True, True, 1),
+    (1, 337, 16, "f32", True, True, 2),
+    (2, 337, 32, "bf16", True, True, 3),
+    (1, 337, 16, "bf16", False, False, 6),
+    (3, 1000, 64, "f32", True, True, 5),
+    (1, 4096, 16, "bf16", True, True, 0),
+]
+
+
+@pytest.mark.parametrize("B,L,D,io,with_state,conv_b,n_chunks", EDGE)
+def test_edge_shapes(B, L, D, io, with_state, conv_b, n_chunks):
+    inp = inputs.scan_inputs(B, L, D, io, seed=100 + L + D, bc_std=1.0, device="cuda",
+                             with_state=with_state)
+    if not conv_b:
+        inp["conv_b"] = None
+    else:
+        inp["conv_b"] = torch.randn(D, device="cuda") * 0.1
+    check_against_oracle(inp, run_gpu(inp, n_chunks=n_chunks), f"B{B} L{L} D{D} {io} nc{n_chunks}")
+
+
+def test_seqlen_zero_returns_initial_state():
+    inp = inputs.scan_inputs(2, 0, 32, "bf16", seed=5, device="cuda", with_state=True)
+    y, fh, fcs = run_gpu(inp)
+    torch.cuda.synchronize()
+    assert y.numel() == 0
+    assert torch.equal(fh, inp["h0"])
+    assert torch.equal(fcs, inp["conv_state0"])
+    del inp["h0"], inp["conv_state0"]
+    y, fh, fcs = run_gpu(inp)
+    torch.cuda.synchronize()
+    assert torch.all(fh == 0) and torch.all(fcs == 0)
+
+
+@pytest.mark.parametrize("n_chunks", [1, 3])
+def test_final_state_may_alias_initial_state(n_chunks):
+    inp = inputs.scan_inputs(2, 300, 32, "bf16", seed=7, device="cuda", with_state=True)
+    ref = [t.clone() for t in run_gpu(inp, n_chunks=n_chunks)]
+    h, cs = inp["h0"].clone(), inp["conv_state0"].clone()
+    inp2 = dict(inp, h0=h, conv_state0=cs)
+    y, fh, fcs = run_gpu(inp2, final_h=h, final_conv_state=cs, n_chunks=n_chunks)
+    torch.cuda.synchronize()
+    assert torch.equal(y, ref[0]) and torch.equal(h, ref[1]) and torch.equal(cs, ref[2])
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_host_split_calls_equal_one_call_bitwise(io):
+    """One sequential pass == the same sequence fed as several calls that carry
+    (final_h, final_conv_state) into (h0, conv_state0) -- bit for bit."""
+    inp = inputs.scan_inputs(1, 1024, 64, io, seed=11, device="cuda", with_state=True)
+    y, fh, fcs = run_gpu(inp, n_chunks=1)
+    h, cs, ys = inp["h0"], inp["conv_state0"], []
+    for t0, t1 in [(0, 64), (64, 65), (65, 300), (300, 1024)]:
+        part = dict(inp, h0=h, conv_state0=cs)
+        for k in ("x", "z", "dt_raw", "Bm", "Cm"):
+            part[k] = inp[k][:, t0:t1].contiguous()
+        yp, h, cs = run_gpu(part, n_chunks=1)
+        ys.append(yp)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(ys, 1), y)
+    assert torch.equal(h, fh) and torch.equal(cs, fcs)
+
+
+def test_chunked_matches_sequential_within_tolerance():
+    inp = inputs.scan_inputs(1, 64 * 40 + 7, 32, "f32", seed=13, device="cuda", with_state=True)
+    y1, fh1, fcs1 = [t.clone() for t in run_gpu(inp, n_chunks=1)]
+    for nc in (2, 7, 40):
+        y, fh, fcs = run_gpu(inp, n_chunks=nc)
+        torch.cuda.synchronize()
+        assert_close(y, oracle_like(y1), "f32", f"nc={nc} y")
+        assert_close(fh, oracle_like(fh1), "f32", f"nc={nc} h", fp32_output=True)
+        assert torch.equal(fcs, fcs1)
+
+
+def oracle_like(t):
+    return t.double().cpu().numpy()
+
+
+def test_timeout_is_reported_and_gpu_stays_usable():
+    inp = inputs.scan_inputs(1, 256, 16, "bf16", seed=17, device="cuda")
+    assert ops.mamba_last_error() == ops.MAMBA_OK
+    run_gpu(inp, flags=ops.MAMBA_FLAG_TEST_STALL_FIRST_LOAD, wait_timeout_ns=20_000_000)
+    assert ops.mamba_last_error() == ops.MAMBA_ERR_TIMEOUT
+    assert ops.mamba_last_error() == ops.MAMBA_OK  # cleared by the read
+    check_against_oracle(inp, run_gpu(inp), "after timeout")
+    assert ops.mamba_last_error() == ops.MAMBA_OK
+
+
+def test_rejects_bad_arguments_on_device():
+    inp = inputs.scan_inputs(1, 64, 24, "bf16", seed=19, device="cuda")
+    with pytest.raises(ops.MambaError) as e:
+        run_gpu(inp)
+    assert e.value.status == ops.MAMBA_ERR_UNSUPPORTED
+    inp = inputs.scan_inputs(1, 64, 32, "bf16", seed=19, device="cuda")
+    x = torch.empty(inp["x"].numel() * 2 + 8, dtype=torch.bfloat16, device="cuda")[1:1 + inp["x"].numel()]
+    x = x.view(inp["x"].shape)
+    with pytest.raises(ops.MambaError) as e:
+        run_gpu(dict(inp, x=x))
+    assert e.value.status == ops.MAMBA_ERR_INVALID_ARG
+    inp = inputs.scan_inputs(1, 4096, 16, "bf16", seed=19, device="cuda")
+    with pytest.raises(ops.MambaError) as e:
+        run_gpu(inp, n_chunks=4, workspace=torch.empty(256, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == ops.MAMBA_ERR_WORKSPACE
