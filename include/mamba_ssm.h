@@ -126,6 +126,32 @@ int mamba_scan_default_chunks(int batch, int seqlen, int d_inner);
 mamba_status mamba_scan_fwd(const mamba_scan_args *args, void *stream);
 
 /*
+ * Prefill without any allocation.  The pages have no counterpart of this
+ * call: it exists for callers that cannot call cudaMalloc -- for instance a
+ * plugin whose host framework owns all device memory through its own pool
+ * and forbids allocations from outside it, or a latency-critical path where
+ * cudaMalloc's implicit synchronisation is not acceptable.  It runs exactly
+ * mamba_scan_fwd, with `workspace` and `workspace_bytes` ignored: the scratch
+ * is a fixed array of MAMBA_NOALLOC_SCRATCH_BYTES (32 MiB) that the library
+ * holds in every GPU that loads it, until the process exits.
+ *
+ *  - Calls whose mamba_scan_workspace_size() exceeds that size are rejected
+ *    with MAMBA_ERR_WORKSPACE before anything runs (one sequential pass fits
+ *    up to batch * seqlen = 262,144 tokens).
+ *  - The first call on a device looks the array's device address up (once,
+ *    with that device current); make that first call before any stream
+ *    capture.
+ *  - All calls share the one array: calls that may overlap on the GPU (two
+ *    streams, or two threads) race and corrupt each other's results; order
+ *    them on one stream.  The array keeps the last call's contents; every
+ *    call writes or clears everything it reads before reading it (the
+ *    chunk counters are cleared at the start of each call).
+ */
+#define MAMBA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+mamba_status mamba_scan_fwd_noalloc(const mamba_scan_args *args, void *stream);
+
+/*
  * Decode: one token through the layer, state updated in place -- the
  * constant-memory recurrence of "Um SSM em uma pagina" (y_t needs only
  * h_{t-1} and x_t).  Bit for bit the same arithmetic as one token of

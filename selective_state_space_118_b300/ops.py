@@ -26,7 +26,9 @@ D_STATE, D_CONV = 16, 4
 
 # the functions the public header declares (checked by the tests)
 EXPORTED = ("mamba_scan_workspace_size", "mamba_scan_default_chunks", "mamba_scan_fwd",
-            "mamba_step", "mamba_last_error", "mamba_status_string", "mamba_abi_version")
+            "mamba_step", "mamba_last_error", "mamba_status_string", "mamba_abi_version",
+            "mamba_scan_fwd_noalloc")
+MAMBA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _vp = ctypes.c_void_p
 
@@ -84,6 +86,8 @@ def load_library(path: str = LIB_PATH):
         lib.mamba_status_string.restype = ctypes.c_char_p
         lib.mamba_abi_version.argtypes = []
         lib.mamba_abi_version.restype = ctypes.c_int
+        lib.mamba_scan_fwd_noalloc.argtypes = [ctypes.POINTER(ScanArgs), _vp]
+        lib.mamba_scan_fwd_noalloc.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -189,3 +193,26 @@ def mamba_last_error(stream=None) -> int:
 
 def mamba_abi_version() -> int:
     return int(load_library().mamba_abi_version())
+
+
+def mamba_scan_fwd_noalloc(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=None,
+                           conv_state0=None, *, y, final_h=None, final_conv_state=None,
+                           n_chunks: int = 0, stream=None):
+    """Prefill scan through ``mamba_scan_fwd_noalloc``: the same computation
+    as mamba_scan_fwd for callers that cannot allocate device memory -- the
+    library uses its own fixed scratch array (MAMBA_NOALLOC_SCRATCH_BYTES per
+    GPU) instead of a workspace, so the caller passes only inputs and outputs
+    (y, and optionally final_h / final_conv_state) and nothing here allocates.
+    Calls that may overlap on the GPU share that scratch and race."""
+    lib = load_library()
+    B, L, D = x.shape
+    a = ScanArgs(batch=B, seqlen=L, d_inner=D, d_state=A_log.shape[-1], d_conv=conv_w.shape[-1],
+                 io=_io_code(x), x=_ptr(x), z=_ptr(z), dt_raw=_ptr(dt_raw), Bm=_ptr(Bm),
+                 Cm=_ptr(Cm), A_log=_ptr(A_log), Dskip=_ptr(Dskip), conv_w=_ptr(conv_w),
+                 conv_b=_ptr(conv_b), h0=_ptr(h0), conv_state0=_ptr(conv_state0), y=_ptr(y),
+                 final_h=_ptr(final_h), final_conv_state=_ptr(final_conv_state),
+                 workspace=None, workspace_bytes=0, n_chunks=n_chunks, flags=0, wait_timeout_ns=0)
+    st = lib.mamba_scan_fwd_noalloc(ctypes.byref(a), _stream(stream))
+    if st != MAMBA_OK:
+        raise MambaError(st, "mamba_scan_fwd_noalloc")
+    return y, final_h, final_conv_state
