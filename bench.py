@@ -182,14 +182,14 @@ def decode_algorithmic_bytes(B, D, es):
 
 
 # ---------------------------------------------------------------- our arm
-def scan_call(ops, inp, out, ws, stream):
+def scan_call(ops, inp, out, ws, stream, n_chunks=0):
     ops.mamba_scan_fwd(inp["x"], inp["z"], inp["dt_raw"], inp["Bm"], inp["Cm"], inp["A_log"],
                        inp["Dskip"], inp["conv_w"], inp["conv_b"], None, None, y=out["y"],
                        final_h=out["fh"], final_conv_state=out["fcs"], workspace=ws,
-                       stream=stream)
+                       n_chunks=n_chunks, stream=stream)
 
 
-def bench_prefill(w, steps, warmup, world, local):
+def bench_prefill(w, steps, warmup, world, local, n_chunks_req=0):
     from selective_state_space_118_b300 import ops
     dev = torch.device("cuda", local)
     inp = inputs.workload_inputs(w, device=dev)
@@ -198,12 +198,13 @@ def bench_prefill(w, steps, warmup, world, local):
     out = {"y": torch.empty_like(inp["x"]),
            "fh": torch.empty(B, D, D_STATE, device=dev),
            "fcs": torch.empty(B, D_CONV - 1, D, device=dev, dtype=inp["x"].dtype)}
-    nbytes = ops.mamba_scan_workspace_size(B, L, D, 0)
+    nbytes = ops.mamba_scan_workspace_size(B, L, D, n_chunks_req)
     ws = torch.empty(max(nbytes, 1), device=dev, dtype=torch.uint8) if nbytes else None
-    n_chunks = ops.mamba_scan_default_chunks(B, L, D)
+    plan = ops.mamba_scan_plan(B, L, D, n_chunks_req)
+    n_chunks = plan["n_chunks"]
     stream = torch.cuda.current_stream(dev)
     for _ in range(warmup):
-        scan_call(ops, inp, out, ws, stream)
+        scan_call(ops, inp, out, ws, stream, n_chunks_req)
     torch.cuda.synchronize(dev)
     assert ops.mamba_last_error(stream) == ops.MAMBA_OK
     barrier(world)
@@ -212,7 +213,7 @@ def bench_prefill(w, steps, warmup, world, local):
     with ClockSampler(dev.index) as clk:
         ev[0].record(stream)
         for i in range(steps):
-            scan_call(ops, inp, out, ws, stream)
+            scan_call(ops, inp, out, ws, stream, n_chunks_req)
             ev[i + 1].record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
@@ -223,8 +224,8 @@ def bench_prefill(w, steps, warmup, world, local):
     elems = B * L * D
     alg = scan_algorithmic_bytes(B, L, D, es)
     res = dict(elems=elems, t_ms=t_max_ms, per_launch_ms=statistics.mean(per),
-               per_launch_min_ms=min(per), alg_bytes=alg, n_chunks=n_chunks,
-               launches_per_step=1 if n_chunks == 1 else 2, clocks=clk.summary(),
+               per_launch_min_ms=min(per), alg_bytes=alg, n_chunks=n_chunks, plan=plan,
+               launches_per_step=2 if n_chunks == 1 else 3, clocks=clk.summary(),
                in_bytes=sum(inp[k].numel() * inp[k].element_size()
                             for k in ("x", "z", "dt_raw", "Bm", "Cm")),
                out_bytes=out["y"].numel() * out["y"].element_size())
@@ -398,6 +399,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--n-chunks", type=int, default=0,
+                    help="chunk count passed to the library (0: its own plan)")
     ap.add_argument("--seqlen", type=int, default=0,
                     help="override the workload's sequence length (smaller cases for profiling)")
     args = ap.parse_args()
@@ -413,7 +416,7 @@ def main():
         build.build()
     barrier(world)
     w = workload_of(args)
-    res, inp, out, ws = bench_prefill(w, args.steps, args.warmup, world, local)
+    res, inp, out, ws = bench_prefill(w, args.steps, args.warmup, world, local, args.n_chunks)
     elems_all = res["elems"] * args.steps * world
     value = elems_all / (res["t_ms"] / 1e3)
     hbm, src = peaks()
@@ -421,10 +424,10 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": res["t_ms"] / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.io,
-            "data": "synthetic", "config": config_of(w, res["n_chunks"]),
+            "data": "synthetic", "config": dict(config_of(w, res["n_chunks"]), plan=res["plan"]),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": None, "peak_source": src,
-                         "kernel": "scan_fwd_kernel",
+                         "kernel": "mamba_scan_fwd: bc_widen + scan_piece_summary + scan_fwd (one call)",
                          "algorithmic_bytes_per_launch": res["alg_bytes"]},
             "gpu_launches": res["launches_per_step"] * args.steps,
             "clocks": res["clocks"]}

@@ -87,11 +87,12 @@ typedef enum { MAMBA_F32 = 0, MAMBA_BF16 = 1 } mamba_dtype;
  *                     B*L*128 bytes, plus the chunk carries in chunked mode);
  *                     its contents need not be initialised and are not kept
  *   n_chunks          0: the library picks; 1: one sequential pass over L;
- *                     k > 1: L is cut into k chunks (a multiple of 64 tokens
+ *                     k > 1: L is cut into k chunks (a multiple of 16 tokens
  *                     each, the last one shorter) that run in parallel, each
  *                     chunk's carried-in state being the decayed end states of
- *                     the chunks before it (two passes; results agree with the
- *                     sequential pass to rounding)
+ *                     the chunks before it, computed by a first pass over the
+ *                     earlier chunks cut into pieces (two passes; results
+ *                     agree with the sequential pass to rounding)
  *   flags             0, or MAMBA_FLAG_TEST_* (tests only)
  *   wait_timeout_ns   limit of every device-side wait (0: 1 second)
  *
@@ -122,6 +123,12 @@ size_t mamba_scan_workspace_size(int batch, int seqlen, int d_inner, int n_chunk
 
 /* The number of chunks mamba_scan_fwd uses when n_chunks = 0. */
 int mamba_scan_default_chunks(int batch, int seqlen, int d_inner);
+
+/* The work plan mamba_scan_fwd follows for these sizes and n_chunks:
+ * out[0] = chunks, out[1] = tokens per chunk (the last chunk may be shorter),
+ * out[2] = summary pieces per chunk and out[3] = tokens per piece (both 0 for
+ * one pass).  MAMBA_ERR_INVALID_ARG / _UNSUPPORTED as for the scan. */
+mamba_status mamba_scan_plan(int batch, int seqlen, int d_inner, int n_chunks, int out[4]);
 
 mamba_status mamba_scan_fwd(const mamba_scan_args *args, void *stream);
 

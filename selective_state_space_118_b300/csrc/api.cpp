@@ -15,8 +15,8 @@ using mamba::IoType;
 
 namespace {
 
-constexpr int kT = 64;   // tokens per tile (multiple of every chunk)
-constexpr int kCT = 16;  // channels per CTA
+constexpr int kT = mamba::kTileTokens;  // tokens per tile (every chunk and piece is whole tiles)
+constexpr int kLanes = 32;  // channels per CTA (one warp)
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -51,31 +51,94 @@ size_t esize(mamba_dtype io) { return io == MAMBA_BF16 ? 2 : 4; }
 
 size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// The chunking plan: how many chunks of how many tokens.
+// The chunking plan: n_chunks chunks of chunk_tiles tiles (the last one may
+// be shorter), and, in chunked mode, every chunk but the last cut into
+// `pieces` summary pieces of piece_tiles tiles (the last piece may be shorter).
 struct Plan {
   int n_chunks;
-  int chunk_len;
+  int chunk_tiles;
+  int pieces;
+  int piece_tiles;
 };
 
-Plan make_plan(int batch, int seqlen, int d_inner, int n_chunks_req) {
-  Plan pl{1, seqlen};
-  if (seqlen <= 0) return pl;
-  const int tiles = (seqlen + kT - 1) / kT;
-  int n = n_chunks_req;
-  if (n <= 0) {
-    // Enough CTAs for ~4 per SM; each chunk keeps at least 4 tiles.
-    const long ctas = (long)batch * (d_inner / kCT);
-    const long target = 4L * sm_count();
-    n = ctas >= (3 * target) / 4 ? 1 : (int)((target + ctas - 1) / ctas);
-    const int max_by_len = tiles / 4 > 0 ? tiles / 4 : 1;
-    if (n > max_by_len) n = max_by_len;
+// The machine as the plan sees it: SM count and resident one-warp CTAs per SM
+// of each prefill kernel with bf16 I/O (from the occupancy calculator;
+// typical B300 values when no device answers, e.g. in a build without a GPU).
+struct Machine {
+  int sms;
+  int main_per_sm;
+  int summary_per_sm;
+};
+
+Machine machine() {
+  Machine m{sm_count(), 16, 20};
+  int a = 0, b = 0;
+  mamba::scan_occupancy(IoType::BF16, &a, &b);
+  if (a > 0) m.main_per_sm = a;
+  if (b > 0) m.summary_per_sm = b;
+  return m;
+}
+
+// Modelled time of a kernel pass that runs `items` one-warp CTAs of `tiles`
+// tiles each at `cost` per tile.  The busiest of the 4 * SM schedulers runs
+// ceil(items / (4 SMs)) of them; how fast depends on how many warps share a
+// scheduler (a lone warp issues about every other cycle, four or more keep it
+// busy), so the rate is the issue efficiency at the resident warp count; each
+// CTA pays a fixed set-up of about half a tile.
+double pass_time(long items, int tiles, double cost, int sms, int per_sm) {
+  const long units = 4L * sms;
+  const long resident = items < (long)sms * per_sm ? items : (long)sms * per_sm;
+  const double w = (double)resident / units;
+  double ipc = 0.25 + 0.2 * w;
+  if (ipc > 0.95) ipc = 0.95;
+  const long per_unit = (items + units - 1) / units;
+  return (double)per_unit * (tiles + 0.5) * cost / ipc;
+}
+
+// For a chunk length, the summary piece count with the least modelled time.
+void choose_pieces(long groups, int n_chunks, int chunk_tiles, const Machine& mc, int* pieces, int* piece_tiles,
+                   double* time) {
+  *pieces = 1;
+  *piece_tiles = chunk_tiles;
+  *time = 0.0;
+  if (n_chunks <= 1) return;
+  double best = -1.0;
+  for (int m = 1; m <= 16 && m <= chunk_tiles; ++m) {
+    const int P = (chunk_tiles + m - 1) / m;
+    const int m_eff = (chunk_tiles + P - 1) / P;
+    const double t = pass_time(groups * (n_chunks - 1) * m_eff, P, 0.7, mc.sms, mc.summary_per_sm);
+    if (best < 0.0 || t < best - 1e-9) {
+      best = t;
+      *pieces = m_eff;
+      *piece_tiles = P;
+    }
   }
-  if (n > tiles) n = tiles;
-  if (n < 1) n = 1;
-  const int tiles_per_chunk = (tiles + n - 1) / n;
-  pl.chunk_len = tiles_per_chunk * kT;
-  pl.n_chunks = (tiles + tiles_per_chunk - 1) / tiles_per_chunk;
-  if (pl.n_chunks == 1) pl.chunk_len = seqlen;
+  *time = best;
+}
+
+// The plan depends only on the sizes (not on the I/O dtype), so that the
+// workspace queries, which take no dtype, agree with the call.
+Plan make_plan(int batch, int seqlen, int d_inner, int n_chunks_req) {
+  const int tiles = (seqlen + kT - 1) / kT;
+  Plan pl{1, tiles, 1, tiles};
+  if (tiles <= 1 || n_chunks_req == 1) return pl;
+  const long groups = (long)batch * ((d_inner + kLanes - 1) / kLanes);
+  const Machine mc = machine();
+  int lo = 1, hi = tiles < 64 ? tiles : 64;
+  if (n_chunks_req > 1) lo = hi = n_chunks_req < tiles ? n_chunks_req : tiles;
+  double best = -1.0;
+  for (int n = lo; n <= hi; ++n) {
+    const int C = (tiles + n - 1) / n;
+    const int n_eff = (tiles + C - 1) / C;
+    int m = 1, P = C;
+    double t_sum = 0.0;
+    choose_pieces(groups, n_eff, C, mc, &m, &P, &t_sum);
+    const double t = pass_time(groups * n_eff, C, 1.0, mc.sms, mc.main_per_sm) + t_sum;
+    if (best < 0.0 || t < best - 1e-9) {
+      best = t;
+      pl = Plan{n_eff, C, m, P};
+    }
+  }
   return pl;
 }
 
@@ -84,24 +147,25 @@ struct Workspace {
 };
 
 // bc: B and C widened to fp32 and interleaved, (B, L, 32); then, in chunked
-// mode only, the carries, chunk summaries and arrival counters.
+// mode only, the carries, piece summaries and arrival counters.
 Workspace workspace_layout(int batch, int seqlen, int d_inner, const Plan& pl) {
   Workspace w{0, 0, 0, 0, 0, 0};
   const size_t B = batch, L = seqlen, D = d_inner, n = pl.n_chunks;
+  const size_t np = (n - 1) * (size_t)pl.pieces;
+  const size_t G = (D + kLanes - 1) / kLanes;
   w.bc = 0;
   w.total = round256(B * L * 32 * sizeof(float));
   if (pl.n_chunks <= 1) return w;
   w.carry = w.total;
   w.hloc = round256(w.carry + B * n * D * 16 * sizeof(float));
-  w.sum_dt = round256(w.hloc + B * (n - 1) * D * 16 * sizeof(float));
-  w.counters = round256(w.sum_dt + B * (n - 1) * D * sizeof(float));
-  w.total = round256(w.counters + B * (D / kCT) * sizeof(unsigned));
+  w.sum_dt = round256(w.hloc + B * np * D * 16 * sizeof(float));
+  w.counters = round256(w.sum_dt + B * np * D * sizeof(float));
+  w.total = round256(w.counters + B * G * sizeof(unsigned));
   return w;
 }
 
-// 3-D tiled map over a (B, L, inner) row-major tensor: box (box_inner, 64, 1).
-bool encode3d(CUtensorMap* m, const void* base, mamba_dtype io, int inner, int L, int B,
-              int box_inner = 16) {
+// 3-D tiled map over a (B, L, inner) row-major tensor: box (box_inner, kT, 1).
+bool encode3d(CUtensorMap* m, const void* base, mamba_dtype io, int inner, int L, int B, int box_inner) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const size_t es = esize(io);
@@ -120,7 +184,7 @@ mamba_status check_common(int batch, int d_inner, int d_state, int d_conv, mamba
   if (batch <= 0 || d_inner <= 0) return MAMBA_ERR_INVALID_ARG;
   if (io != MAMBA_F32 && io != MAMBA_BF16) return MAMBA_ERR_UNSUPPORTED;
   if (d_state != MAMBA_D_STATE || d_conv != MAMBA_D_CONV) return MAMBA_ERR_UNSUPPORTED;
-  if (d_inner % kCT != 0) return MAMBA_ERR_UNSUPPORTED;
+  if (d_inner % 16 != 0) return MAMBA_ERR_UNSUPPORTED;
   return MAMBA_OK;
 }
 
@@ -143,12 +207,23 @@ const char* mamba_status_string(mamba_status s) {
 }
 
 int mamba_scan_default_chunks(int batch, int seqlen, int d_inner) {
-  if (batch <= 0 || seqlen <= 0 || d_inner <= 0 || d_inner % kCT) return 1;
+  if (batch <= 0 || seqlen <= 0 || d_inner <= 0 || d_inner % 16) return 1;
   return make_plan(batch, seqlen, d_inner, 0).n_chunks;
 }
 
+mamba_status mamba_scan_plan(int batch, int seqlen, int d_inner, int n_chunks, int out[4]) {
+  if (!out || batch <= 0 || seqlen <= 0 || d_inner <= 0 || n_chunks < 0) return MAMBA_ERR_INVALID_ARG;
+  if (d_inner % 16) return MAMBA_ERR_UNSUPPORTED;
+  const Plan pl = make_plan(batch, seqlen, d_inner, n_chunks);
+  out[0] = pl.n_chunks;
+  out[1] = pl.chunk_tiles * kT;
+  out[2] = pl.n_chunks > 1 ? pl.pieces : 0;
+  out[3] = pl.n_chunks > 1 ? pl.piece_tiles * kT : 0;
+  return MAMBA_OK;
+}
+
 size_t mamba_scan_workspace_size(int batch, int seqlen, int d_inner, int n_chunks) {
-  if (batch <= 0 || seqlen <= 0 || d_inner <= 0 || d_inner % kCT) return 0;
+  if (batch <= 0 || seqlen <= 0 || d_inner <= 0 || d_inner % 16 || n_chunks < 0) return 0;
   return workspace_layout(batch, seqlen, d_inner, make_plan(batch, seqlen, d_inner, n_chunks)).total;
 }
 
@@ -195,23 +270,25 @@ mamba_status mamba_scan_fwd(const mamba_scan_args* a, void* stream_v) {
   char* wsp = static_cast<char*>(a->workspace);
   float* bc = reinterpret_cast<float*>(wsp + ws.bc);
 
-  // x, z, dt_raw, bc, y
+  // x, z, dt_raw, bc (both rows), bc (the B row only, for the summary pass)
   CUtensorMap maps[5];
-  const void* bases[5] = {a->x, a->z, a->dt_raw, bc, a->y};
-  for (int i = 0; i < 5; ++i) {
-    const bool is_bc = i == 3;
-    if (!encode3d(&maps[i], bases[i], is_bc ? MAMBA_F32 : a->io, is_bc ? 32 : a->d_inner, a->seqlen,
-                  a->batch, is_bc ? 32 : 16))
-      return MAMBA_ERR_CUDA;
-  }
+  if (!encode3d(&maps[0], a->x, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
+      !encode3d(&maps[1], a->z, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
+      !encode3d(&maps[2], a->dt_raw, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
+      !encode3d(&maps[3], bc, MAMBA_F32, 32, a->seqlen, a->batch, 32) ||
+      !encode3d(&maps[4], bc, MAMBA_F32, 32, a->seqlen, a->batch, 16))
+    return MAMBA_ERR_CUDA;
 
   mamba::ScanParams p;
   std::memset(&p, 0, sizeof(p));
   p.batch = a->batch;
   p.seqlen = a->seqlen;
   p.d_inner = a->d_inner;
-  p.chunk_len = pl.chunk_len;
+  p.n_groups = (a->d_inner + kLanes - 1) / kLanes;
+  p.chunk_tiles = pl.chunk_tiles;
   p.n_chunks = pl.n_chunks;
+  p.piece_tiles = pl.piece_tiles;
+  p.pieces = pl.pieces;
   p.A_log = a->A_log;
   p.Dskip = a->Dskip;
   p.conv_w = a->conv_w;
@@ -219,6 +296,7 @@ mamba_status mamba_scan_fwd(const mamba_scan_args* a, void* stream_v) {
   p.h0 = a->h0;
   p.conv_state0 = a->conv_state0;
   p.x = a->x;
+  p.y = a->y;
   p.final_h = a->final_h;
   p.final_conv_state = a->final_conv_state;
   p.flags = a->flags;
@@ -232,13 +310,13 @@ mamba_status mamba_scan_fwd(const mamba_scan_args* a, void* stream_v) {
     p.hloc = reinterpret_cast<float*>(wsp + ws.hloc);
     p.sum_dt = reinterpret_cast<float*>(wsp + ws.sum_dt);
     p.counters = reinterpret_cast<unsigned*>(wsp + ws.counters);
-    if (cudaMemsetAsync(p.counters, 0, B * (D / kCT) * sizeof(unsigned), stream) != cudaSuccess)
+    if (cudaMemsetAsync(p.counters, 0, B * (size_t)p.n_groups * sizeof(unsigned), stream) != cudaSuccess)
       return MAMBA_ERR_CUDA;
-    const CUtensorMap smaps[3] = {maps[0], maps[2], maps[3]};  // x, dt_raw, bc
-    dim3 g1((unsigned)(D / kCT), (unsigned)B, (unsigned)(pl.n_chunks - 1));
+    const CUtensorMap smaps[3] = {maps[0], maps[2], maps[4]};  // x, dt_raw, B rows
+    dim3 g1((unsigned)p.n_groups, (unsigned)B, (unsigned)((pl.n_chunks - 1) * pl.pieces));
     if (mamba::launch_summary(io, smaps, p, g1, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
   }
-  dim3 g2((unsigned)(D / kCT), (unsigned)B, (unsigned)pl.n_chunks);
+  dim3 g2((unsigned)p.n_groups, (unsigned)B, (unsigned)pl.n_chunks);
   if (mamba::launch_scan(io, maps, p, g2, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
   return MAMBA_OK;
 }

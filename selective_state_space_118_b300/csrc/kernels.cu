@@ -1,5 +1,5 @@
 // kernels.cu -- the one translation unit holding the device code (prefill,
-// chunk summary, decode step and the sticky error word) and its launchers.
+// piece summaries, decode step and the sticky error word) and its launchers.
 #include <cuda_bf16.h>
 
 #include "launch.h"
@@ -9,7 +9,7 @@
 namespace mamba {
 
 size_t scan_smem_bytes(IoType io) {
-  return (io == IoType::BF16 ? sizeof(ScanSmem<__nv_bfloat16>) : sizeof(ScanSmem<float>)) + 128;
+  return (io == IoType::BF16 ? sizeof(MainSmem<__nv_bfloat16>) : sizeof(MainSmem<float>)) + 128;
 }
 
 size_t summary_smem_bytes(IoType io) {
@@ -18,21 +18,21 @@ size_t summary_smem_bytes(IoType io) {
 
 template <typename IO>
 static cudaError_t launch_scan_t(const CUtensorMap* m, const ScanParams& p, dim3 grid, cudaStream_t s) {
-  const size_t smem = sizeof(ScanSmem<IO>) + 128;
+  const size_t smem = sizeof(MainSmem<IO>) + 128;
   cudaError_t e = cudaFuncSetAttribute(scan_fwd_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  scan_fwd_kernel<IO><<<grid, kScanThreads, smem, s>>>(m[0], m[1], m[2], m[3], m[4], p);
+  scan_fwd_kernel<IO><<<grid, kLanes, smem, s>>>(m[0], m[1], m[2], m[3], p);
   return cudaGetLastError();
 }
 
 template <typename IO>
 static cudaError_t launch_summary_t(const CUtensorMap* m, const ScanParams& p, dim3 grid, cudaStream_t s) {
   const size_t smem = sizeof(SummarySmem<IO>) + 128;
-  cudaError_t e = cudaFuncSetAttribute(scan_chunk_summary_kernel<IO>,
+  cudaError_t e = cudaFuncSetAttribute(scan_piece_summary_kernel<IO>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  scan_chunk_summary_kernel<IO><<<grid, kScanThreads, smem, s>>>(m[0], m[1], m[2], p);
+  scan_piece_summary_kernel<IO><<<grid, kLanes, smem, s>>>(m[0], m[1], m[2], p);
   return cudaGetLastError();
 }
 
@@ -53,7 +53,7 @@ cudaError_t launch_bc_widen(IoType io, const void* Bm, const void* Cm, float* bc
                             : launch_widen_t<float>(Bm, Cm, bc, rows, stream);
 }
 
-cudaError_t launch_scan(IoType io, const CUtensorMap maps[5], const ScanParams& p, dim3 grid,
+cudaError_t launch_scan(IoType io, const CUtensorMap maps[4], const ScanParams& p, dim3 grid,
                         cudaStream_t stream) {
   return io == IoType::BF16 ? launch_scan_t<__nv_bfloat16>(maps, p, grid, stream)
                             : launch_scan_t<float>(maps, p, grid, stream);
@@ -66,13 +66,29 @@ cudaError_t launch_summary(IoType io, const CUtensorMap maps[3], const ScanParam
 }
 
 cudaError_t launch_step(IoType io, const StepParams& p, cudaStream_t stream) {
-  const long threads = (long)p.batch * p.d_inner * 4;
-  const unsigned blocks = (unsigned)((threads + kStepThreads - 1) / kStepThreads);
+  const dim3 grid((unsigned)((p.d_inner + kStepThreads - 1) / kStepThreads), (unsigned)p.batch);
   if (io == IoType::BF16)
-    step_kernel<__nv_bfloat16><<<blocks, kStepThreads, 0, stream>>>(p);
+    step_kernel<__nv_bfloat16><<<grid, kStepThreads, 0, stream>>>(p);
   else
-    step_kernel<float><<<blocks, kStepThreads, 0, stream>>>(p);
+    step_kernel<float><<<grid, kStepThreads, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+void scan_occupancy(IoType io, int* main_per_sm, int* summary_per_sm) {
+  int a = 0, b = 0;
+  if (io == IoType::BF16) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, scan_fwd_kernel<__nv_bfloat16>, kLanes,
+                                                      sizeof(MainSmem<__nv_bfloat16>) + 128) != cudaSuccess) a = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, scan_piece_summary_kernel<__nv_bfloat16>, kLanes,
+                                                      sizeof(SummarySmem<__nv_bfloat16>) + 128) != cudaSuccess) b = 0;
+  } else {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, scan_fwd_kernel<float>, kLanes,
+                                                      sizeof(MainSmem<float>) + 128) != cudaSuccess) a = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, scan_piece_summary_kernel<float>, kLanes,
+                                                      sizeof(SummarySmem<float>) + 128) != cudaSuccess) b = 0;
+  }
+  *main_per_sm = a;
+  *summary_per_sm = b;
 }
 
 cudaError_t take_device_error(unsigned* code, cudaStream_t stream) {

@@ -20,13 +20,18 @@ size_t summary_smem_bytes(IoType io);
 // B (rows, 16), C (rows, 16) in the I/O dtype -> bc (rows, 32) fp32.
 cudaError_t launch_bc_widen(IoType io, const void* Bm, const void* Cm, float* bc, long rows,
                             cudaStream_t stream);
-// maps: x, z, dt_raw, bc, y (3-D tiled tensor maps).
-cudaError_t launch_scan(IoType io, const CUtensorMap maps[5], const ScanParams& p, dim3 grid,
+// maps: x, z, dt_raw, bc (3-D tiled tensor maps).
+cudaError_t launch_scan(IoType io, const CUtensorMap maps[4], const ScanParams& p, dim3 grid,
                         cudaStream_t stream);
-// maps: x, dt_raw, bc.
+// maps: x, dt_raw, and the B half of bc.
 cudaError_t launch_summary(IoType io, const CUtensorMap maps[3], const ScanParams& p, dim3 grid,
                            cudaStream_t stream);
 cudaError_t launch_step(IoType io, const StepParams& p, cudaStream_t stream);
+
+// Resident CTAs per SM of the main and summary kernels (0 when no device
+// answers); the dynamic shared memory has to be allowed first (launch_* do
+// that; scan_occupancy sets the same attribute).
+void scan_occupancy(IoType io, int* main_per_sm, int* summary_per_sm);
 
 // Reads and clears the sticky device error word of the current device
 // (synchronises the stream first).

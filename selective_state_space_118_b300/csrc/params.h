@@ -6,23 +6,30 @@
 
 namespace mamba {
 
+// Tokens per tile: the unit of the TMA ring and of every chunk and piece.
+constexpr int kTileTokens = 16;
+
 struct ScanParams {
   int batch, seqlen, d_inner;
-  int chunk_len;  // tokens per chunk, a multiple of kT
-  int n_chunks;
+  int n_groups;     // ceil(d_inner / 32): one CTA (warp) per group of 32 channels
+  int chunk_tiles;  // tiles of kTileTokens tokens per chunk
+  int n_chunks;     // chunks of the sequence run in parallel (1: one pass)
+  int piece_tiles;  // tiles per summary piece (chunked mode)
+  int pieces;       // pieces per chunk = ceil(chunk_tiles / piece_tiles)
   const float* A_log;
   const float* Dskip;
   const float* conv_w;
   const float* conv_b;       // may be null
   const float* h0;           // may be null
   const void* conv_state0;   // may be null
-  const void* x;             // plain pointer to x, for the conv halo at chunk starts
+  const void* x;             // plain pointer to x, for the conv inputs before a chunk
+  void* y;
   float* final_h;            // may be null
   void* final_conv_state;    // may be null
-  float* carry;              // chunked: (B, n_chunks, D, 16) carried-in states
-  float* hloc;               // chunked: (B, n_chunks-1, D, 16) chunk end states from zero
-  float* sum_dt;             // chunked: (B, n_chunks-1, D)
-  unsigned* counters;        // chunked: (B, D/16) arrival counters, zero between calls
+  float* carry;              // chunked: (B, n_chunks, D, 16) carried-in states (entry 0 unused)
+  float* hloc;               // chunked: (B, (n_chunks-1)*pieces, D, 16) piece end states from zero
+  float* sum_dt;             // chunked: (B, (n_chunks-1)*pieces, D)
+  unsigned* counters;        // chunked: (B, n_groups) arrival counters, zero between calls
   uint32_t flags;
   uint64_t timeout_ns;
 };

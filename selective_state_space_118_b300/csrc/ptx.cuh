@@ -2,6 +2,8 @@
 // mbarriers with bounded waits, async-proxy fences and the MUFU approximations.
 #pragma once
 #include <cuda.h>
+#include <cuda_bf16.h>
+
 #include <cstdint>
 
 namespace mamba {
@@ -99,6 +101,30 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------- global stores
+// Stores to global memory written as st.global: the compiler then knows they
+// cannot touch shared memory and may move later shared-memory loads above
+// them.  Ordered by their data only; kernels end, or fence, before anything
+// reads what they wrote.
+__device__ __forceinline__ void st_global(float* p, float v) {
+  asm volatile("st.global.f32 [%0], %1;" ::"l"(p), "f"(v));
+}
+
+__device__ __forceinline__ void st_global(__nv_bfloat16* p, __nv_bfloat16 v) {
+  asm volatile("st.global.b16 [%0], %1;" ::"l"(p), "h"(__bfloat16_as_ushort(v)));
+}
+
+// The same, predicated on `pred` (no branch).
+__device__ __forceinline__ void st_global_if(bool pred, float* p, float v) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.global.f32 [%0], %1;\n\t}" ::"l"(p), "f"(v),
+               "r"((unsigned)pred));
+}
+
+__device__ __forceinline__ void st_global_if(bool pred, __nv_bfloat16* p, __nv_bfloat16 v) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.global.b16 [%0], %1;\n\t}" ::"l"(p),
+               "h"(__bfloat16_as_ushort(v)), "r"((unsigned)pred));
 }
 
 // ---------------------------------------------------------------- MUFU

@@ -1,40 +1,33 @@
 // scan_fwd.cuh -- prefill kernels of the selective scan.
 //
-// Work decomposition.  A CTA of 64 threads owns one tile of 16 channels of one
-// batch row and one chunk of the sequence (the whole sequence when n_chunks is
-// 1), and walks it in tiles of 64 tokens.  Each tile of x, z, dt_raw
-// (64 tokens x 16 channels, I/O dtype) and of the token rows of B and C
-// (64 x 32 fp32, widened and interleaved beforehand by bc_widen_kernel) is
-// brought into shared memory by TMA bulk-tensor copies through a ring of
-// three mbarrier-tracked stages, so every input byte is read from HBM once.
+// Work decomposition.  A CTA is one warp.  Lane i owns channel c0 + i of a
+// group of 32 channels of one batch row, with all 16 of its fp32 states in
+// registers, and walks one chunk of the sequence in tiles of 32 tokens.  Each
+// tile of x, z, dt_raw (32 tokens x 32 channels, I/O dtype) and of the token
+// rows of B and C (32 x 32 fp32, widened and interleaved beforehand by
+// bc_widen_kernel) is brought into shared memory by TMA bulk-tensor copies
+// through a ring of two mbarrier-tracked stages, so every input byte is read
+// from HBM once.  B and C are the same for every channel: all lanes read the
+// same row, so their 128-bit shared loads are broadcasts.  Nothing is
+// exchanged between lanes; the only serial dependence is each state's
+// recurrence, and a lane has 16 independent ones plus all the per-token
+// exponentials, which do not depend on the state, to overlap with it.
 //
-// Lanes.  Thread (ci = tid >> 2, g = tid & 3) owns states 4g..4g+3 of
-// channel ci in registers (fp32).  Tokens go eight at a time; in each step
-// lane g first runs the per-token prologue (causal conv, SiLU, softplus,
-// silu(z)) of its own two tokens t0+g and t0+4+g, shares (dt, dt*u) with the
-// three other lanes of its channel through an 8-entry warp-private buffer,
-// advances its four states through the eight tokens, combines the four
-// lanes' read-out partials (shuffle reduce-scatter) and finishes its two
-// tokens, y = (C.h + D u) silu(z), u and silu(z) still in its registers.  All
-// exponentials and products of a step are independent of the state, so they
-// are issued ahead of the eight dependent state updates.
+// The conv's three earlier inputs travel in registers from token to token
+// (loaded from x, or conv_state0, at the chunk start).  y is stored straight
+// from registers (a warp writes 32 consecutive channels of one token).
 //
-// The ring is refilled one tile late (the stage of tile k-1 after tile k is
-// done), so the previous tile's x rows are still resident and give the conv
-// its three earlier inputs; before the first tile those rows of the spare
-// stage hold conv_state0 (or the inputs before the chunk).  y leaves through
-// a double-buffered shared tile and a TMA store, which clips rows past the end
-// of the sequence.  Padding tokens past the end carry dt = dt*u = 0, which
-// leaves the state bit-for-bit unchanged (2^0 = 1, fma(1, h, 0) = h).
-//
-// Chunked mode (n_chunks > 1, chunks a multiple of 64 tokens) is two passes:
-// scan_chunk_summary_kernel computes, for every chunk but the last, the end
-// state hloc_j of the chunk started from zero and S_j = sum of dt over the
-// chunk; the last CTA to finish for a (channel tile, batch row) folds them in
-// chunk order into the carried-in state of every chunk,
-//   carry_0 = h0,   carry_{j+1} = 2^(A2 S_j) * carry_j + hloc_j,
-// and scan_fwd_kernel then runs each chunk from its carry (the "chunked scan
-// equals the sequential scan" identity of the oracle).
+// Chunked mode.  At batch 1 the groups alone cannot fill the GPU, so the
+// sequence is cut into n_chunks chunks that run in parallel, each starting
+// from its carried-in state.  Those carries come from a first pass,
+// scan_piece_summary_kernel: every chunk but the last is cut into pieces; for
+// each piece it computes the end state hloc of the piece started from zero and
+// S = sum of dt over the piece; the last CTA to finish for a (group, batch
+// row) folds the pieces in order,
+//   carry <- h0;   for each piece: carry <- 2^(A2 S) carry + hloc
+// writing the carry at every chunk boundary (the "chunked scan equals the
+// sequential scan" identity of the oracle).  The fold order is fixed, so the
+// result does not depend on timing.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -47,12 +40,10 @@
 
 namespace mamba {
 
-constexpr int kScanThreads = 64;
-constexpr int kT = 64;       // tokens per tile
-constexpr int kCT = 16;      // channels per CTA
-constexpr int kN = 16;       // d_state
+constexpr int kLanes = 32;   // channels per CTA (one warp)
+constexpr int kT = kTileTokens;
 constexpr int kBC = 2 * kN;  // widened B and C per token
-constexpr int kStages = 3;   // TMA ring depth
+constexpr int kStages = 2;   // TMA ring depth
 
 // Sticky device error word (MAMBA_ERR_* code of the first failure).
 __device__ unsigned int g_mamba_error;
@@ -68,16 +59,16 @@ __device__ __forceinline__ uint32_t smem_pad128(const void* base) {
 // Raw input of channel c at token tau of batch row b (tau < 0: conv_state0,
 // or zero).
 template <typename IO>
-__device__ __forceinline__ IO input_raw(const ScanParams& p, int b, long tau, int c) {
-  if (tau >= 0) return reinterpret_cast<const IO*>(p.x)[((size_t)b * p.seqlen + tau) * p.d_inner + c];
-  if (p.conv_state0 == nullptr) return from_f32<IO>(0.0f);
-  return reinterpret_cast<const IO*>(p.conv_state0)[((size_t)b * 3 + (3 + tau)) * p.d_inner + c];
+__device__ __forceinline__ float input_at(const ScanParams& p, int b, long tau, int c) {
+  if (tau >= 0) return to_f32(reinterpret_cast<const IO*>(p.x)[((size_t)b * p.seqlen + tau) * p.d_inner + c]);
+  if (p.conv_state0 == nullptr) return 0.0f;
+  return to_f32(reinterpret_cast<const IO*>(p.conv_state0)[((size_t)b * 3 + (3 + tau)) * p.d_inner + c]);
 }
 
 // ---------------------------------------------------------------- B, C widening
 // bc[row][0..15] = B[row][:], bc[row][16..31] = C[row][:] in fp32, for the
-// B*L token rows (64 bytes per token read in bf16), so that the scan's TMA
-// brings both rows in one box and the lanes read fp32 directly.
+// B*L token rows (64 bytes per token read in bf16), so that one TMA box
+// carries both rows and the lanes read fp32 directly.
 template <typename IO>
 __global__ void __launch_bounds__(256) bc_widen_kernel(const IO* __restrict__ Bm, const IO* __restrict__ Cm,
                                                        float* __restrict__ bc, long rows) {
@@ -93,369 +84,339 @@ __global__ void __launch_bounds__(256) bc_widen_kernel(const IO* __restrict__ Bm
 
 // ---------------------------------------------------------------- shared layout
 template <typename IO>
-struct ScanStage {
-  IO x[kT][kCT];
-  IO z[kT][kCT];
-  IO dt[kT][kCT];
+struct MainStage {
+  IO x[kT][kLanes];
+  IO z[kT][kLanes];
+  IO dt[kT][kLanes];
   float bc[kT][kBC];
 };
 
 template <typename IO>
-struct ScanSmem {
-  ScanStage<IO> stage[kStages];
-  IO y[2][kT][kCT];
-  float2 dtb[2][kCT][8];  // (dt, dt*u) of a step's 8 tokens per channel, double-buffered
+struct MainSmem {
+  MainStage<IO> stage[kStages];
   uint64_t full[kStages];
 };
 
-// Issues the copies of one tile; with_z = false skips z (the summary pass).
-template <typename IO, bool kWithZ>
-__device__ __forceinline__ void issue_tile(ScanStage<IO>& S, uint64_t* bar_ptr, const CUtensorMap* tx,
-                                           const CUtensorMap* tz, const CUtensorMap* tdt,
-                                           const CUtensorMap* tbc, int c0, int tt, int b) {
-  constexpr uint32_t kBytes =
-      (kWithZ ? 3 : 2) * kT * kCT * sizeof(IO) + kT * kBC * sizeof(float);
-  const uint32_t bar = smem_u32(bar_ptr);
-  mbar_arrive_expect_tx(bar, kBytes);
-  tma_load_3d(smem_u32(&S.x[0][0]), tx, c0, tt, b, bar);
-  if (kWithZ) tma_load_3d(smem_u32(&S.z[0][0]), tz, c0, tt, b, bar);
-  tma_load_3d(smem_u32(&S.dt[0][0]), tdt, c0, tt, b, bar);
-  tma_load_3d(smem_u32(&S.bc[0][0]), tbc, 0, tt, b, bar);
-}
-
-// x of channel ci at tile row r in [-3, 63]: rows < 0 are the previous tile's
-// rows 61..63, still resident in the previous stage.
 template <typename IO>
-__device__ __forceinline__ float x_at(const ScanStage<IO>& S, const ScanStage<IO>& P, int r, int ci) {
-  const IO* row = r >= 0 ? &S.x[r][0] : &P.x[kT + r][0];
-  return to_f32(row[ci]);
-}
+struct SummaryStage {
+  IO x[kT][kLanes];
+  IO dt[kT][kLanes];
+  float b[kT][kN];
+};
 
-// Conv + SiLU of the token at tile row r of channel ci.
 template <typename IO>
-__device__ __forceinline__ float conv_silu_at(const ScanStage<IO>& S, const ScanStage<IO>& P, int r,
-                                              int ci, float4 w, float bias) {
-  return silu(conv4(w, bias, x_at<IO>(S, P, r - 3, ci), x_at<IO>(S, P, r - 2, ci),
-                    x_at<IO>(S, P, r - 1, ci), x_at<IO>(S, P, r, ci)));
+struct SummarySmem {
+  SummaryStage<IO> stage[kStages];
+  uint64_t full[kStages];
+  int last;
+};
+
+__device__ __forceinline__ void load_bc4(const float* row, float4 (&v)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) v[q] = *reinterpret_cast<const float4*>(row + 4 * q);
 }
 
-// softplus of two dt_raw values; the warp takes the small-dt formula alone
-// when all its values allow it (the same formula softplus() selects there).
-__device__ __forceinline__ void softplus2(float v0, float v1, float& d0, float& d1) {
-  const float e0 = softplus_e(v0), e1 = softplus_e(v1);
-  const bool small = (e0 < kSoftplusSmallE) && (e1 < kSoftplusSmallE);
-  if (__all_sync(0xffffffffu, small)) {
-    d0 = softplus_small(e0);
-    d1 = softplus_small(e1);
-  } else {
-    d0 = e0 < kSoftplusSmallE ? softplus_small(e0) : softplus_large(v0, e0);
-    d1 = e1 < kSoftplusSmallE ? softplus_small(e1) : softplus_large(v1, e1);
+// Lets the copies already issued land (bounded) before shared memory goes away.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int k, int n_tiles, uint64_t timeout_ns) {
+  for (int kk = k; kk < n_tiles && kk < k + kStages; ++kk)
+    (void)mbar_wait_bounded(smem_u32(&full[kk % kStages]), (kk / kStages) & 1, timeout_ns);
+}
+
+// True when every dt_raw of the tile's first `rows` rows (over the active
+// lanes) lies in softplus's small-e region, checked on the raw value.
+template <typename IO>
+__device__ __forceinline__ bool small_dt_tile(const IO (&dt)[kT][kLanes], int rows, int lane, bool active) {
+  float m = -3.0e38f;
+#pragma unroll 8
+  for (int r = 0; r < rows; ++r) m = fmaxf(m, to_f32(dt[r][lane]));
+  return __all_sync(0xffffffffu, !active || m < kSoftplusSmallRaw);
+}
+
+template <bool kSmall>
+__device__ __forceinline__ float softplus_sel(float v) {
+  return kSmall ? softplus_small_raw(v) : softplus(v);
+}
+
+// One tile of the main pass, `rows` tokens, straight-line per token.
+template <typename IO, bool kSmall>
+__device__ __forceinline__ void main_tile(const MainStage<IO>& S, int rows, int lane, bool active,
+                                          const Channel& ch, State16& st, float& xm3, float& xm2, float& xm1,
+                                          IO* ytile, int D) {
+#pragma unroll 4
+  for (int r = 0; r < rows; ++r) {
+    const float xv = to_f32(S.x[r][lane]);
+    const float u = silu(conv4(ch.w, ch.bias, xm3, xm2, xm1, xv));
+    xm3 = xm2;
+    xm2 = xm1;
+    xm1 = xv;
+    const float dt = softplus_sel<kSmall>(to_f32(S.dt[r][lane]));
+    const float gz = silu(to_f32(S.z[r][lane]));
+    float4 Bv[4], Cv[4];
+    load_bc4(&S.bc[r][0], Bv);
+    load_bc4(&S.bc[r][kN], Cv);
+    state16_advance(st, ch.a2, dt, __fmul_rn(dt, u), Bv);
+    const float yv = gate_out(state16_readout(st, Cv), ch.Dc, u, gz);
+    st_global_if(active, ytile + (size_t)r * D, from_f32<IO>(yv));
   }
 }
 
-// Writes the raw inputs of tokens t_begin-3 .. t_begin-1 into rows 61..63 of
-// the spare stage (the conv's earlier inputs for the first tile) and, from
-// chunk 0 only, final_conv_state = the last three inputs of the sequence.
-// Chunk 0 is the one CTA of these channels that reads conv_state0, so the
-// final state may alias it: everything is read before the barrier.
-template <typename IO>
-__device__ __forceinline__ void init_halo(const ScanParams& p, ScanStage<IO>& spare, int b, int c0,
-                                          int t_begin, bool write_final) {
-  const int tid = threadIdx.x;
-  const int k = tid >> 4, cc = tid & 15;  // tid < 48: k = 0..2
-  IO fv = from_f32<IO>(0.0f);
-  const bool fin = write_final && p.final_conv_state != nullptr && tid < 48;
-  if (tid < 48) {
-    spare.x[kT - 3 + k][cc] = input_raw<IO>(p, b, (long)t_begin - 3 + k, c0 + cc);
-    if (fin) fv = input_raw<IO>(p, b, (long)p.seqlen - 3 + k, c0 + cc);
-    fence_proxy_async_smem();  // these rows are later overwritten by TMA
+// One full tile of the summary pass.
+template <typename IO, bool kSmall>
+__device__ __forceinline__ void summary_tile(const SummaryStage<IO>& S, int lane, const Channel& ch, State16& st,
+                                             float& sdt, float& xm3, float& xm2, float& xm1) {
+#pragma unroll 4
+  for (int r = 0; r < kT; ++r) {
+    const float xv = to_f32(S.x[r][lane]);
+    const float u = silu(conv4(ch.w, ch.bias, xm3, xm2, xm1, xv));
+    xm3 = xm2;
+    xm2 = xm1;
+    xm1 = xv;
+    const float dt = softplus_sel<kSmall>(to_f32(S.dt[r][lane]));
+    float4 Bv[4];
+    load_bc4(&S.b[r][0], Bv);
+    state16_advance(st, ch.a2, dt, __fmul_rn(dt, u), Bv);
+    sdt = __fadd_rn(sdt, dt);
   }
-  __syncthreads();
-  if (fin) reinterpret_cast<IO*>(p.final_conv_state)[((size_t)b * 3 + k) * p.d_inner + c0 + cc] = fv;
 }
 
+// ---------------------------------------------------------------- main pass
+// grid (n_groups, batch, n_chunks), 32 threads.
 template <typename IO>
-__global__ void __launch_bounds__(kScanThreads)
+__global__ void __launch_bounds__(kLanes)
     scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
                     const __grid_constant__ CUtensorMap tm_dt, const __grid_constant__ CUtensorMap tm_bc,
-                    const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ ScanParams p) {
+                    const __grid_constant__ ScanParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  ScanSmem<IO>& sm = *reinterpret_cast<ScanSmem<IO>*>(smem_raw + smem_pad128(smem_raw));
+  MainSmem<IO>& sm = *reinterpret_cast<MainSmem<IO>*>(smem_raw + smem_pad128(smem_raw));
 
-  const int tid = threadIdx.x;
-  const int c0 = blockIdx.x * kCT;
+  const int lane = threadIdx.x;
+  const int c0 = blockIdx.x * kLanes;
   const int b = blockIdx.y;
   const int j = blockIdx.z;
   const int D = p.d_inner;
-  const int t_begin = j * p.chunk_len;
-  const int t_end = min(t_begin + p.chunk_len, p.seqlen);
+  const int c = c0 + lane;
+  const bool active = c < D;
+  const int cl = active ? c : D - 1;  // channel whose parameters an idle lane reads
+  const int t_begin = j * p.chunk_tiles * kT;
+  const int t_end = min(t_begin + p.chunk_tiles * kT, p.seqlen);
   const int n_tiles = (t_end - t_begin + kT - 1) / kT;
-  const int ci = tid >> 2, g = tid & 3;
-  const int c = c0 + ci;
 
-  if (tid == 0) {
+  if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&sm.full[s]), 1);
     fence_mbar_init();
     prefetch_tensormap(&tm_x);
     prefetch_tensormap(&tm_z);
     prefetch_tensormap(&tm_dt);
     prefetch_tensormap(&tm_bc);
-    prefetch_tensormap(&tm_y);
   }
+  __syncwarp();
 
-  // ---- per-thread parameters and initial state
-  const float4 w = *reinterpret_cast<const float4*>(p.conv_w + (size_t)c * 4);
-  const float bias = p.conv_b ? p.conv_b[c] : 0.0f;
-  const float Dc = p.Dskip[c];
-  const float4 al = *reinterpret_cast<const float4*>(p.A_log + (size_t)c * kN + 4 * g);
-  const float2 a01 = make_float2(a2_from_log(al.x), a2_from_log(al.y));
-  const float2 a23 = make_float2(a2_from_log(al.z), a2_from_log(al.w));
-  State4 st;
-  {
-    const float* src = nullptr;
-    if (p.n_chunks > 1)
-      src = p.carry + (((size_t)b * p.n_chunks + j) * D + c) * kN + 4 * g;
-    else if (p.h0)
-      src = p.h0 + ((size_t)b * D + c) * kN + 4 * g;
-    const float4 h = src ? *reinterpret_cast<const float4*>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
-    st.h01 = make_float2(h.x, h.y);
-    st.h23 = make_float2(h.z, h.w);
-  }
-  init_halo<IO>(p, sm.stage[kStages - 1], b, c0, t_begin, j == 0);
-
-  // ---- fill the ring (the last stage is refilled after tile 0)
   const bool stall_test = (p.flags & 1u) != 0;
-  if (tid == 0) {
-    for (int k = 0; k < kStages - 1 && k < n_tiles; ++k) {
+  if (lane == 0) {
+    constexpr uint32_t kBytes = 3 * kT * kLanes * sizeof(IO) + kT * kBC * sizeof(float);
+    for (int k = 0; k < kStages && k < n_tiles; ++k) {
       if (stall_test && k == 0) continue;  // test switch: this stage never completes
-      issue_tile<IO, true>(sm.stage[k], &sm.full[k], &tm_x, &tm_z, &tm_dt, &tm_bc, c0, t_begin + k * kT, b);
+      const uint32_t bar = smem_u32(&sm.full[k]);
+      const int tt = t_begin + k * kT;
+      mbar_arrive_expect_tx(bar, kBytes);
+      tma_load_3d(smem_u32(&sm.stage[k].x[0][0]), &tm_x, c0, tt, b, bar);
+      tma_load_3d(smem_u32(&sm.stage[k].z[0][0]), &tm_z, c0, tt, b, bar);
+      tma_load_3d(smem_u32(&sm.stage[k].dt[0][0]), &tm_dt, c0, tt, b, bar);
+      tma_load_3d(smem_u32(&sm.stage[k].bc[0][0]), &tm_bc, 0, tt, b, bar);
     }
   }
 
+  Channel ch;
+  load_channel(ch, p.A_log, p.conv_w, p.conv_b, p.Dskip, cl);
+  State16 st;
+  if (j > 0)
+    state16_load(st, p.carry + (((size_t)b * p.n_chunks + j) * D + cl) * kN);
+  else if (p.h0)
+    state16_load(st, p.h0 + ((size_t)b * D + cl) * kN);
+  else
+    state16_zero(st);
+
+  // the conv's earlier inputs; chunk 0 also writes the final conv state (it
+  // is the one CTA of these channels that reads conv_state0, which the final
+  // state may alias: everything is read before anything is written)
+  float xm3 = input_at<IO>(p, b, (long)t_begin - 3, cl);
+  float xm2 = input_at<IO>(p, b, (long)t_begin - 2, cl);
+  float xm1 = input_at<IO>(p, b, (long)t_begin - 1, cl);
+  if (j == 0 && p.final_conv_state != nullptr) {
+    const float f0 = input_at<IO>(p, b, (long)p.seqlen - 3, cl);
+    const float f1 = input_at<IO>(p, b, (long)p.seqlen - 2, cl);
+    const float f2 = input_at<IO>(p, b, (long)p.seqlen - 1, cl);
+    __syncwarp();
+    if (active) {
+      IO* fcs = reinterpret_cast<IO*>(p.final_conv_state) + (size_t)b * 3 * D + c;
+      fcs[0] = from_f32<IO>(f0);
+      fcs[D] = from_f32<IO>(f1);
+      fcs[2 * (size_t)D] = from_f32<IO>(f2);
+    }
+  }
+
+  IO* yrow = reinterpret_cast<IO*>(p.y) + ((size_t)b * p.seqlen + t_begin) * D + cl;
   bool ok = true;
   int k = 0;
   for (; k < n_tiles; ++k) {
     const int s = k % kStages;
-    const int sp = (k + kStages - 1) % kStages;
-    const ScanStage<IO>& S = sm.stage[s];
-    const ScanStage<IO>& P = sm.stage[sp];
-    const int tile_t0 = t_begin + k * kT;
-    const int t_valid = min(kT, t_end - tile_t0);
-    IO(*ytile)[kCT] = sm.y[k & 1];
-
+    const MainStage<IO>& S = sm.stage[s];
+    const int t_valid = min(kT, t_end - (t_begin + k * kT));
     bool mine = mbar_wait_bounded(smem_u32(&sm.full[s]), (k / kStages) & 1, p.timeout_ns);
-    mine = __all_sync(0xffffffffu, mine);
-    if (mine) {
-      const int n_steps = (t_valid + 7) >> 3;
-#pragma unroll 1
-      for (int oc = 0; oc < n_steps; ++oc) {
-        const int t0 = oc * 8;
-        const int ra = t0 + g, rb = t0 + 4 + g;
-        // prologue of this lane's two tokens
-        float da, db;
-        softplus2(to_f32(S.dt[ra][ci]), to_f32(S.dt[rb][ci]), da, db);
-        const float ua = conv_silu_at<IO>(S, P, ra, ci, w, bias);
-        const float ub = conv_silu_at<IO>(S, P, rb, ci, w, bias);
-        const float gza = silu(to_f32(S.z[ra][ci]));
-        const float gzb = silu(to_f32(S.z[rb][ci]));
-        if (ra >= t_valid) da = 0.0f;
-        if (rb >= t_valid) db = 0.0f;
-        float2(*dtb)[8] = sm.dtb[oc & 1];
-        dtb[ci][g] = make_float2(da, __fmul_rn(da, ua));
-        dtb[ci][4 + g] = make_float2(db, __fmul_rn(db, ub));
-        __syncwarp();
-        float dts[8], dtus[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 v = *reinterpret_cast<const float4*>(&dtb[ci][2 * i]);
-          dts[2 * i] = v.x;
-          dtus[2 * i] = v.y;
-          dts[2 * i + 1] = v.z;
-          dtus[2 * i + 1] = v.w;
-        }
-        // eight tokens through this lane's four states
-        float part[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 Bv = *reinterpret_cast<const float4*>(&S.bc[t0 + q][4 * g]);
-          const float4 Cv = *reinterpret_cast<const float4*>(&S.bc[t0 + q][kN + 4 * g]);
-          part[q] = state4_step(st, a01, a23, dts[q], dtus[q], Bv, Cv);
-        }
-        const float Sa = group4_reduce_scatter(part, g);
-        const float Sb = group4_reduce_scatter(part + 4, g);
-        ytile[ra][ci] = from_f32<IO>(gate_out(Sa, Dc, ua, gza));
-        ytile[rb][ci] = from_f32<IO>(gate_out(Sb, Dc, ub, gzb));
-      }
-      fence_proxy_async_smem();  // y tile -> TMA store
-    }
-    if (tid == 0) bulk_wait_read<0>();  // tile k-1's store has read the buffer tile k+1 reuses
-    ok = __syncthreads_and(mine) != 0;
+    ok = __all_sync(0xffffffffu, mine);
     if (!ok) break;
-    if (tid == 0) {
-      tma_store_3d(&tm_y, c0, tile_t0, b, smem_u32(&ytile[0][0]));
-      bulk_commit();
-      const int kn = k + kStages - 1;  // refill the previous tile's stage
-      if (kn < n_tiles)
-        issue_tile<IO, true>(sm.stage[sp], &sm.full[sp], &tm_x, &tm_z, &tm_dt, &tm_bc, c0, t_begin + kn * kT, b);
+    if (small_dt_tile<IO>(S.dt, t_valid, lane, active))
+      main_tile<IO, true>(S, t_valid, lane, active, ch, st, xm3, xm2, xm1, yrow + (size_t)k * kT * D, D);
+    else
+      main_tile<IO, false>(S, t_valid, lane, active, ch, st, xm3, xm2, xm1, yrow + (size_t)k * kT * D, D);
+    __syncwarp();  // every lane is done with stage s
+    if (lane == 0 && k + kStages < n_tiles) {
+      constexpr uint32_t kBytes = 3 * kT * kLanes * sizeof(IO) + kT * kBC * sizeof(float);
+      const uint32_t bar = smem_u32(&sm.full[s]);
+      const int tt = t_begin + (k + kStages) * kT;
+      mbar_arrive_expect_tx(bar, kBytes);
+      tma_load_3d(smem_u32(&sm.stage[s].x[0][0]), &tm_x, c0, tt, b, bar);
+      tma_load_3d(smem_u32(&sm.stage[s].z[0][0]), &tm_z, c0, tt, b, bar);
+      tma_load_3d(smem_u32(&sm.stage[s].dt[0][0]), &tm_dt, c0, tt, b, bar);
+      tma_load_3d(smem_u32(&sm.stage[s].bc[0][0]), &tm_bc, 0, tt, b, bar);
     }
   }
 
   if (!ok) {
-    if (tid == 0) {
+    if (lane == 0) {
       report_error(4u);  // MAMBA_ERR_TIMEOUT
-      // let the copies already issued land (bounded) before shared memory goes away
-      for (int kk = k; kk < n_tiles && kk < k + kStages - 1; ++kk)
-        (void)mbar_wait_bounded(smem_u32(&sm.full[kk % kStages]), (kk / kStages) & 1, p.timeout_ns);
-      bulk_wait_all();
+      drain_ring(sm.full, k, n_tiles, p.timeout_ns);
     }
     return;
   }
-  if (tid == 0) bulk_wait_all();
-
-  if (j == p.n_chunks - 1 && p.final_h) {
-    float* dst = p.final_h + ((size_t)b * D + c) * kN + 4 * g;
-    *reinterpret_cast<float4*>(dst) = make_float4(st.h01.x, st.h01.y, st.h23.x, st.h23.y);
-  }
+  if (j == p.n_chunks - 1 && p.final_h && active) state16_store(st, p.final_h + ((size_t)b * D + c) * kN);
 }
 
-// ---------------------------------------------------------------- chunk summary
-// For chunk j < n_chunks-1: the chunk's end state from h = 0 (hloc_j) and the
-// sum of its dt (S_j); then the fold of all chunks by the last CTA to finish.
+// ---------------------------------------------------------------- piece summaries
+// grid (n_groups, batch, (n_chunks - 1) * pieces), 32 threads.  Piece q of
+// chunk jc covers tiles [jc*C + q*P, min(jc*C + (q+1)*P, (jc+1)*C)).
 template <typename IO>
-struct SummarySmem {
-  ScanStage<IO> stage[kStages];  // z unused
-  float2 dtb[2][kCT][8];
-  uint64_t full[kStages];
-  int last;
-};
-
-template <typename IO>
-__global__ void __launch_bounds__(kScanThreads)
-    scan_chunk_summary_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dt,
-                              const __grid_constant__ CUtensorMap tm_bc, const __grid_constant__ ScanParams p) {
+__global__ void __launch_bounds__(kLanes)
+    scan_piece_summary_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dt,
+                              const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ ScanParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SummarySmem<IO>& sm = *reinterpret_cast<SummarySmem<IO>*>(smem_raw + smem_pad128(smem_raw));
 
-  const int tid = threadIdx.x;
-  const int c0 = blockIdx.x * kCT;
+  const int lane = threadIdx.x;
+  const int c0 = blockIdx.x * kLanes;
   const int b = blockIdx.y;
-  const int j = blockIdx.z;  // 0 .. n_chunks-2: always full chunks
+  const int piece = blockIdx.z;  // 0 .. (n_chunks-1)*pieces - 1
+  const int jc = piece / p.pieces;
+  const int q = piece - jc * p.pieces;
   const int D = p.d_inner;
-  const int t_begin = j * p.chunk_len;
-  const int n_tiles = p.chunk_len / kT;
-  const int ci = tid >> 2, g = tid & 3;
-  const int c = c0 + ci;
+  const int c = c0 + lane;
+  const bool active = c < D;
+  const int cl = active ? c : D - 1;
+  const int tile0 = jc * p.chunk_tiles + q * p.piece_tiles;
+  const int tile1 = min(tile0 + p.piece_tiles, (jc + 1) * p.chunk_tiles);
+  const int t_begin = tile0 * kT;
+  const int n_tiles = tile1 - tile0;  // >= 1: chunks before the last are full
 
-  if (tid == 0) {
+  if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&sm.full[s]), 1);
     fence_mbar_init();
     prefetch_tensormap(&tm_x);
     prefetch_tensormap(&tm_dt);
-    prefetch_tensormap(&tm_bc);
+    prefetch_tensormap(&tm_b);
   }
-  const float4 w = *reinterpret_cast<const float4*>(p.conv_w + (size_t)c * 4);
-  const float bias = p.conv_b ? p.conv_b[c] : 0.0f;
-  const float4 al = *reinterpret_cast<const float4*>(p.A_log + (size_t)c * kN + 4 * g);
-  const float2 a01 = make_float2(a2_from_log(al.x), a2_from_log(al.y));
-  const float2 a23 = make_float2(a2_from_log(al.z), a2_from_log(al.w));
-  State4 st;
-  st.h01 = make_float2(0.f, 0.f);
-  st.h23 = make_float2(0.f, 0.f);
-  float sdt = 0.0f;
-  init_halo<IO>(p, sm.stage[kStages - 1], b, c0, t_begin, false);
+  __syncwarp();
+  constexpr uint32_t kBytes = 2 * kT * kLanes * sizeof(IO) + kT * kN * sizeof(float);
+  if (lane == 0) {
+    for (int k = 0; k < kStages && k < n_tiles; ++k) {
+      const uint32_t bar = smem_u32(&sm.full[k]);
+      const int tt = t_begin + k * kT;
+      mbar_arrive_expect_tx(bar, kBytes);
+      tma_load_3d(smem_u32(&sm.stage[k].x[0][0]), &tm_x, c0, tt, b, bar);
+      tma_load_3d(smem_u32(&sm.stage[k].dt[0][0]), &tm_dt, c0, tt, b, bar);
+      tma_load_3d(smem_u32(&sm.stage[k].b[0][0]), &tm_b, 0, tt, b, bar);
+    }
+  }
 
-  if (tid == 0) {
-    for (int k = 0; k < kStages - 1 && k < n_tiles; ++k)
-      issue_tile<IO, false>(sm.stage[k], &sm.full[k], &tm_x, nullptr, &tm_dt, &tm_bc, c0, t_begin + k * kT, b);
-  }
+  Channel ch;
+  load_channel(ch, p.A_log, p.conv_w, p.conv_b, p.Dskip, cl);
+  State16 st;
+  state16_zero(st);
+  float sdt = 0.0f;
+  float xm3 = input_at<IO>(p, b, (long)t_begin - 3, cl);
+  float xm2 = input_at<IO>(p, b, (long)t_begin - 2, cl);
+  float xm1 = input_at<IO>(p, b, (long)t_begin - 1, cl);
 
   bool ok = true;
   int k = 0;
   for (; k < n_tiles; ++k) {
     const int s = k % kStages;
-    const int sp = (k + kStages - 1) % kStages;
-    const ScanStage<IO>& S = sm.stage[s];
-    const ScanStage<IO>& P = sm.stage[sp];
+    const SummaryStage<IO>& S = sm.stage[s];
     bool mine = mbar_wait_bounded(smem_u32(&sm.full[s]), (k / kStages) & 1, p.timeout_ns);
-    mine = __all_sync(0xffffffffu, mine);
-    if (mine) {
-#pragma unroll 1
-      for (int oc = 0; oc < kT / 8; ++oc) {
-        const int t0 = oc * 8;
-        const int ra = t0 + g, rb = t0 + 4 + g;
-        float da, db;
-        softplus2(to_f32(S.dt[ra][ci]), to_f32(S.dt[rb][ci]), da, db);
-        const float ua = conv_silu_at<IO>(S, P, ra, ci, w, bias);
-        const float ub = conv_silu_at<IO>(S, P, rb, ci, w, bias);
-        float2(*dtb)[8] = sm.dtb[oc & 1];
-        dtb[ci][g] = make_float2(da, __fmul_rn(da, ua));
-        dtb[ci][4 + g] = make_float2(db, __fmul_rn(db, ub));
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 v = *reinterpret_cast<const float4*>(&dtb[ci][2 * i]);
-          const float4 B0 = *reinterpret_cast<const float4*>(&S.bc[t0 + 2 * i][4 * g]);
-          const float4 B1 = *reinterpret_cast<const float4*>(&S.bc[t0 + 2 * i + 1][4 * g]);
-          state4_advance(st, a01, a23, v.x, v.y, B0);
-          state4_advance(st, a01, a23, v.z, v.w, B1);
-          sdt = __fadd_rn(__fadd_rn(sdt, v.x), v.z);
-        }
-      }
-    }
-    ok = __syncthreads_and(mine) != 0;
+    ok = __all_sync(0xffffffffu, mine);
     if (!ok) break;
-    if (tid == 0) {
-      const int kn = k + kStages - 1;
-      if (kn < n_tiles)
-        issue_tile<IO, false>(sm.stage[sp], &sm.full[sp], &tm_x, nullptr, &tm_dt, &tm_bc, c0,
-                              t_begin + kn * kT, b);
+    if (small_dt_tile<IO>(S.dt, kT, lane, active))
+      summary_tile<IO, true>(S, lane, ch, st, sdt, xm3, xm2, xm1);
+    else
+      summary_tile<IO, false>(S, lane, ch, st, sdt, xm3, xm2, xm1);
+    __syncwarp();
+    if (lane == 0 && k + kStages < n_tiles) {
+      const uint32_t bar = smem_u32(&sm.full[s]);
+      const int tt = t_begin + (k + kStages) * kT;
+      mbar_arrive_expect_tx(bar, kBytes);
+      tma_load_3d(smem_u32(&sm.stage[s].x[0][0]), &tm_x, c0, tt, b, bar);
+      tma_load_3d(smem_u32(&sm.stage[s].dt[0][0]), &tm_dt, c0, tt, b, bar);
+      tma_load_3d(smem_u32(&sm.stage[s].b[0][0]), &tm_b, 0, tt, b, bar);
     }
   }
   if (!ok) {
-    if (tid == 0) {
+    if (lane == 0) {
       report_error(4u);
-      for (int kk = k; kk < n_tiles && kk < k + kStages - 1; ++kk)
-        (void)mbar_wait_bounded(smem_u32(&sm.full[kk % kStages]), (kk / kStages) & 1, p.timeout_ns);
+      drain_ring(sm.full, k, n_tiles, p.timeout_ns);
     }
     return;
   }
 
-  // ---- publish this chunk's summary
-  const int nsum = p.n_chunks - 1;
-  {
-    const size_t o = ((size_t)b * nsum + j) * D + c;
-    *reinterpret_cast<float4*>(p.hloc + o * kN + 4 * g) = make_float4(st.h01.x, st.h01.y, st.h23.x, st.h23.y);
-    if (g == 0) p.sum_dt[o] = sdt;
+  // ---- publish this piece's summary
+  const int npieces = (p.n_chunks - 1) * p.pieces;
+  const size_t o = ((size_t)b * npieces + piece) * D + cl;
+  if (active) {
+    state16_store(st, p.hloc + o * kN);
+    p.sum_dt[o] = sdt;
   }
   __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    unsigned* cnt = p.counters + (size_t)b * (D / kCT) + blockIdx.x;
+  __syncwarp();
+  if (lane == 0) {
+    unsigned* cnt = p.counters + (size_t)b * p.n_groups + blockIdx.x;
     const unsigned prev = atomicAdd(cnt, 1u);
-    sm.last = (prev == (unsigned)(nsum - 1));
-    if (sm.last) *cnt = 0u;  // every chunk of this tile has arrived: reset for the next call
+    sm.last = (prev == (unsigned)(npieces - 1));
+    if (sm.last) *cnt = 0u;  // every piece of this group has arrived: reset for the next call
   }
-  __syncthreads();
+  __syncwarp();
   if (!sm.last) return;
   __threadfence();
 
-  // ---- fold in chunk order: carry_0 = h0, carry_{j+1} = 2^(A2 S_j) carry_j + hloc_j
-  float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (p.h0) h = *reinterpret_cast<const float4*>(p.h0 + ((size_t)b * D + c) * kN + 4 * g);
-  float* carry = p.carry + ((size_t)b * p.n_chunks * D + c) * kN + 4 * g;
-  const size_t cstride = (size_t)D * kN;
-  *reinterpret_cast<float4*>(carry) = h;
-  for (int jj = 0; jj < nsum; ++jj) {
-    const size_t o = ((size_t)b * nsum + jj) * D + c;
-    const float4 hl = __ldcg(reinterpret_cast<const float4*>(p.hloc + o * kN + 4 * g));
-    const float S = __ldcg(p.sum_dt + o);
-    const float2 S2 = make_float2(S, S);
-    const float2 x01 = __fmul2_rn(S2, a01), x23 = __fmul2_rn(S2, a23);
-    h.x = __fmaf_rn(ex2_approx(x01.x), h.x, hl.x);
-    h.y = __fmaf_rn(ex2_approx(x01.y), h.y, hl.y);
-    h.z = __fmaf_rn(ex2_approx(x23.x), h.z, hl.z);
-    h.w = __fmaf_rn(ex2_approx(x23.y), h.w, hl.w);
-    *reinterpret_cast<float4*>(carry + (size_t)(jj + 1) * cstride) = h;
+  // ---- fold in piece order; the carry at the end of chunk jc is chunk jc+1's start
+  if (!active) return;
+  State16 h;
+  if (p.h0)
+    state16_load(h, p.h0 + ((size_t)b * D + c) * kN);
+  else
+    state16_zero(h);
+  for (int pc = 0; pc < npieces; ++pc) {
+    const size_t oo = ((size_t)b * npieces + pc) * D + c;
+    State16 hl;
+    const float4* src = reinterpret_cast<const float4*>(p.hloc + oo * kN);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const float4 v = __ldcg(src + kk);
+      hl.h[2 * kk] = make_float2(v.x, v.y);
+      hl.h[2 * kk + 1] = make_float2(v.z, v.w);
+    }
+    state16_fold(h, ch.a2, __ldcg(p.sum_dt + oo), hl);
+    if ((pc + 1) % p.pieces == 0) {
+      const int jn = (pc + 1) / p.pieces;  // the chunk this carry starts
+      state16_store(h, p.carry + (((size_t)b * p.n_chunks + jn) * D + c) * kN);
+    }
   }
 }
 

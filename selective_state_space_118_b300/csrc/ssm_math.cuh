@@ -10,9 +10,10 @@
 //   u   = silu(pre);   dt = softplus(dt_raw);   dtu = dt * u
 //   h_n = 2^(dt * A2_n) * h_n + dtu * B_n,      A2_n = -exp(A_log_n) * log2(e)
 //   y   = (sum_n C_n h_n + D u) * silu(z)
-// The 16 states of a channel are split over 4 lanes (4 states each, lanes
-// g = lane & 3); the read-out sum is ((p0 + p2) + (p1 + p3)) over the lanes'
-// partial sums p_g.
+// One lane owns one channel and all 16 of its states, held as 8 float2 pairs
+// (h[k] = states 2k, 2k+1) and advanced with packed f32x2 arithmetic.  The
+// read-out sum is fixed: p0 collects pairs 0,2,4,6 and p1 pairs 1,3,5,7, then
+// (p0.x + p1.x) + (p0.y + p1.y).
 #pragma once
 #include <cuda_bf16.h>
 
@@ -20,6 +21,7 @@
 
 namespace mamba {
 
+constexpr int kN = 16;  // d_state
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -52,9 +54,10 @@ __device__ __forceinline__ float silu(float v) {
 //             log2(1 + e) would lose it, and needs no reciprocal.
 //   e >= 1/8: log2(1 + e) ln 2, with 1 + e >= 1.125, where the approximate
 //             log2's absolute error stays ~1e-6 relative to the result.
-// softplus() evaluates both and selects (straight-line code); the scan calls
-// softplus_small() directly when a whole warp's values lie in the first
-// region -- the same formula, hence the same bits.
+// softplus() selects per value.  The scan kernels check a whole tile first
+// and, when every value lies below kSoftplusSmallRaw (so that e < 1/8 for
+// sure: 2^(-2.08 log2 e) = 0.12493), take softplus_small(softplus_e(v))
+// directly -- the formula softplus() selects there, hence the same bits.
 __device__ __forceinline__ float softplus_e(float v) { return ex2_approx(__fmul_rn(v, kLog2e)); }
 
 __device__ __forceinline__ float softplus_small(float e) {
@@ -78,6 +81,11 @@ __device__ __forceinline__ float softplus(float v) {
   return e < kSoftplusSmallE ? softplus_small(e) : softplus_large(v, e);
 }
 
+constexpr float kSoftplusSmallRaw = -2.08f;
+
+// softplus(v) for v < kSoftplusSmallRaw (the caller guarantees it).
+__device__ __forceinline__ float softplus_small_raw(float v) { return softplus_small(softplus_e(v)); }
+
 // ---------------------------------------------------------------- conv
 // Causal depthwise cross-correlation of width 4: w.w multiplies the current
 // input (PyTorch Conv1d with padding 3, first L outputs kept).
@@ -89,69 +97,123 @@ __device__ __forceinline__ float conv4(float4 w, float bias, float xm3, float xm
   return __fmaf_rn(w.w, x0, a);
 }
 
-// A2 = A * log2(e) with A = -exp(A_log): the state decay exponent in base 2.
-__device__ __forceinline__ float a2_from_log(float a_log) { return __fmul_rn(-expf(a_log), kLog2e); }
+// ---------------------------------------------------------------- parameters
+// A2 = A * log2(e) with A = -exp(A_log) = -2^(A_log log2 e): the state decay
+// exponent in base 2.
+__device__ __forceinline__ float a2_from_log(float a_log) {
+  return __fmul_rn(-ex2_approx(__fmul_rn(a_log, kLog2e)), kLog2e);
+}
 
-// ---------------------------------------------------------------- state
-// Four states of one channel (h01 = states 4g, 4g+1; h23 = 4g+2, 4g+3).
-struct State4 {
-  float2 h01, h23;
+// The per-channel constants one lane keeps in registers.
+struct Channel {
+  float2 a2[8];  // A2 of states (2k, 2k+1)
+  float4 w;      // conv taps
+  float bias;    // conv bias
+  float Dc;      // skip weight
 };
 
-// One token on four states; returns this lane's read-out partial
-// (C0 h0 + C2 h2) + (C1 h1 + C3 h3).
-__device__ __forceinline__ float state4_step(State4& s, float2 a01, float2 a23, float dt, float dtu,
-                                             float4 B, float4 C) {
-  const float2 dt2 = make_float2(dt, dt);
-  const float2 x01 = __fmul2_rn(dt2, a01);
-  const float2 x23 = __fmul2_rn(dt2, a23);
-  const float2 dA01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
-  const float2 dA23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+__device__ __forceinline__ void load_channel(Channel& ch, const float* __restrict__ A_log,
+                                             const float* __restrict__ conv_w,
+                                             const float* __restrict__ conv_b,
+                                             const float* __restrict__ Dskip, int c) {
+  const float4* al = reinterpret_cast<const float4*>(A_log + (size_t)c * kN);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 v = __ldg(al + q);
+    ch.a2[2 * q] = make_float2(a2_from_log(v.x), a2_from_log(v.y));
+    ch.a2[2 * q + 1] = make_float2(a2_from_log(v.z), a2_from_log(v.w));
+  }
+  ch.w = __ldg(reinterpret_cast<const float4*>(conv_w + (size_t)c * 4));
+  ch.bias = conv_b ? __ldg(conv_b + c) : 0.0f;
+  ch.Dc = __ldg(Dskip + c);
+}
+
+// ---------------------------------------------------------------- state
+struct State16 {
+  float2 h[8];  // states (2k, 2k+1)
+};
+
+__device__ __forceinline__ void state16_zero(State16& s) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) s.h[k] = make_float2(0.0f, 0.0f);
+}
+
+__device__ __forceinline__ void state16_load(State16& s, const float* p) {
+  const float4* q = reinterpret_cast<const float4*>(p);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float4 v = q[k];
+    s.h[2 * k] = make_float2(v.x, v.y);
+    s.h[2 * k + 1] = make_float2(v.z, v.w);
+  }
+}
+
+__device__ __forceinline__ void state16_store(const State16& s, float* p) {
+  float4* q = reinterpret_cast<float4*>(p);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    q[k] = make_float4(s.h[2 * k].x, s.h[2 * k].y, s.h[2 * k + 1].x, s.h[2 * k + 1].y);
+}
+
+// The state-independent half of one token's update: the decays 2^(dt A2) and
+// the inputs dtu B of all 16 states (B[q] holds states 4q..4q+3).
+struct Drive16 {
+  float2 dA[8];
+  float2 bu[8];
+};
+
+__device__ __forceinline__ void drive16(Drive16& d, const float2 (&a2)[8], float dt, float dtu,
+                                        const float4 (&B)[4]) {
+  const float2 d2 = make_float2(dt, dt);
   const float2 u2 = make_float2(dtu, dtu);
-  const float2 b01 = __fmul2_rn(u2, make_float2(B.x, B.y));
-  const float2 b23 = __fmul2_rn(u2, make_float2(B.z, B.w));
-  s.h01 = __ffma2_rn(dA01, s.h01, b01);
-  s.h23 = __ffma2_rn(dA23, s.h23, b23);
-  float2 p = __fmul2_rn(make_float2(C.x, C.y), s.h01);
-  p = __ffma2_rn(make_float2(C.z, C.w), s.h23, p);
-  return __fadd_rn(p.x, p.y);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 x0 = __fmul2_rn(d2, a2[2 * q]);
+    const float2 x1 = __fmul2_rn(d2, a2[2 * q + 1]);
+    d.dA[2 * q] = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+    d.dA[2 * q + 1] = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+    d.bu[2 * q] = __fmul2_rn(u2, make_float2(B[q].x, B[q].y));
+    d.bu[2 * q + 1] = __fmul2_rn(u2, make_float2(B[q].z, B[q].w));
+  }
 }
 
-// State update without the read-out (the chunk-summary pass).
-__device__ __forceinline__ void state4_advance(State4& s, float2 a01, float2 a23, float dt, float dtu,
-                                               float4 B) {
-  const float2 dt2 = make_float2(dt, dt);
-  const float2 x01 = __fmul2_rn(dt2, a01);
-  const float2 x23 = __fmul2_rn(dt2, a23);
-  const float2 dA01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
-  const float2 dA23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
-  const float2 u2 = make_float2(dtu, dtu);
-  s.h01 = __ffma2_rn(dA01, s.h01, __fmul2_rn(u2, make_float2(B.x, B.y)));
-  s.h23 = __ffma2_rn(dA23, s.h23, __fmul2_rn(u2, make_float2(B.z, B.w)));
+// The state-dependent half: h <- dA h + bu.
+__device__ __forceinline__ void state16_apply(State16& s, const Drive16& d) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) s.h[k] = __ffma2_rn(d.dA[k], s.h[k], d.bu[k]);
 }
 
-// Sum of the four lanes' partials of one channel, ((p0 + p2) + (p1 + p3)),
-// returned on all four lanes.
-__device__ __forceinline__ float group4_sum(float p) {
-  p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, 2));
-  return __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, 1));
+// h <- 2^(dt A2) h + dtu B on all 16 states (drive16 then state16_apply: the
+// same operations).
+__device__ __forceinline__ void state16_advance(State16& s, const float2 (&a2)[8], float dt, float dtu,
+                                                const float4 (&B)[4]) {
+  Drive16 d;
+  drive16(d, a2, dt, dtu, B);
+  state16_apply(s, d);
 }
 
-// Four tokens at once: lane g holds its partials p[0..3] of tokens t0..t0+3
-// and receives the full sum of token t0 + g, in the same association as
-// group4_sum.
-__device__ __forceinline__ float group4_reduce_scatter(const float p[4], int g) {
-  const bool hi = (g & 2) != 0;
-  const float send0 = hi ? p[0] : p[2];
-  const float send1 = hi ? p[1] : p[3];
-  const float keep0 = hi ? p[2] : p[0];
-  const float keep1 = hi ? p[3] : p[1];
-  const float q0 = __fadd_rn(keep0, __shfl_xor_sync(0xffffffffu, send0, 2));
-  const float q1 = __fadd_rn(keep1, __shfl_xor_sync(0xffffffffu, send1, 2));
-  const bool lo = (g & 1) != 0;
-  const float keep = lo ? q1 : q0;
-  const float send = lo ? q0 : q1;
-  return __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+// sum_n C_n h_n in the fixed order described at the top of the file.
+__device__ __forceinline__ float state16_readout(const State16& s, const float4 (&C)[4]) {
+  float2 p0 = __fmul2_rn(make_float2(C[0].x, C[0].y), s.h[0]);
+  float2 p1 = __fmul2_rn(make_float2(C[0].z, C[0].w), s.h[1]);
+#pragma unroll
+  for (int q = 1; q < 4; ++q) {
+    p0 = __ffma2_rn(make_float2(C[q].x, C[q].y), s.h[2 * q], p0);
+    p1 = __ffma2_rn(make_float2(C[q].z, C[q].w), s.h[2 * q + 1], p1);
+  }
+  return __fadd_rn(__fadd_rn(p0.x, p1.x), __fadd_rn(p0.y, p1.y));
+}
+
+// Carry fold: h <- 2^(A2 S) h + hl, S the summed dt of a span of tokens and
+// hl that span's end state from zero.
+__device__ __forceinline__ void state16_fold(State16& s, const float2 (&a2)[8], float S,
+                                             const State16& hl) {
+  const float2 S2 = make_float2(S, S);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float2 x = __fmul2_rn(S2, a2[k]);
+    s.h[k] = __ffma2_rn(make_float2(ex2_approx(x.x), ex2_approx(x.y)), s.h[k], hl.h[k]);
+  }
 }
 
 // y = (S + D u) * gz with gz = silu(z)

@@ -25,7 +25,7 @@ MAMBA_FLAG_TEST_STALL_FIRST_LOAD = 0x1
 D_STATE, D_CONV = 16, 4
 
 # the functions the public header declares (checked by the tests)
-EXPORTED = ("mamba_scan_workspace_size", "mamba_scan_default_chunks", "mamba_scan_fwd",
+EXPORTED = ("mamba_scan_workspace_size", "mamba_scan_default_chunks", "mamba_scan_plan", "mamba_scan_fwd",
             "mamba_step", "mamba_last_error", "mamba_status_string", "mamba_abi_version",
             "mamba_scan_fwd_noalloc")
 MAMBA_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -76,6 +76,8 @@ def load_library(path: str = LIB_PATH):
         lib.mamba_scan_workspace_size.restype = ctypes.c_size_t
         lib.mamba_scan_default_chunks.argtypes = [ctypes.c_int] * 3
         lib.mamba_scan_default_chunks.restype = ctypes.c_int
+        lib.mamba_scan_plan.argtypes = [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_int)]
+        lib.mamba_scan_plan.restype = ctypes.c_int
         lib.mamba_scan_fwd.argtypes = [ctypes.POINTER(ScanArgs), _vp]
         lib.mamba_scan_fwd.restype = ctypes.c_int
         lib.mamba_step.argtypes = [ctypes.POINTER(StepArgs), _vp]
@@ -125,6 +127,16 @@ def mamba_scan_workspace_size(batch: int, seqlen: int, d_inner: int, n_chunks: i
 
 def mamba_scan_default_chunks(batch: int, seqlen: int, d_inner: int) -> int:
     return int(load_library().mamba_scan_default_chunks(batch, seqlen, d_inner))
+
+
+def mamba_scan_plan(batch: int, seqlen: int, d_inner: int, n_chunks: int = 0) -> dict:
+    """The work plan of mamba_scan_fwd for these sizes: chunks, tokens per
+    chunk, summary pieces per chunk and tokens per piece (0, 0 for one pass)."""
+    out = (ctypes.c_int * 4)()
+    st = load_library().mamba_scan_plan(batch, seqlen, d_inner, n_chunks, out)
+    if st != MAMBA_OK:
+        raise MambaError(st, "mamba_scan_plan")
+    return dict(n_chunks=out[0], chunk_len=out[1], pieces=out[2], piece_len=out[3])
 
 
 def mamba_scan_fwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=None,

@@ -116,14 +116,26 @@ def test_workspace_plan(lib):
     assert ops.mamba_scan_workspace_size(1, 32768, 8192, 1) == r256(32768 * 32 * 4)
     assert ops.mamba_scan_workspace_size(2, 2048, 1024, 1) == r256(2 * 2048 * 32 * 4)
     assert ops.mamba_scan_workspace_size(2, 0, 1024, 1) == 0
-    # chunked: plus carries for every chunk, summaries for all but the last, counters
+    assert ops.mamba_scan_plan(2, 2048, 1024, 1) == dict(n_chunks=1, chunk_len=2048, pieces=0, piece_len=0)
+    # chunked: plus carries for every chunk, piece summaries for all but the last chunk, counters
     B, L, D, n = 2, 4096, 64, 4
+    pl = ops.mamba_scan_plan(B, L, D, n)
+    assert pl["n_chunks"] == n and pl["chunk_len"] == L // n
+    m = pl["pieces"]
+    assert m >= 1 and pl["piece_len"] % 16 == 0 and (m - 1) * pl["piece_len"] < pl["chunk_len"] <= m * pl["piece_len"]
     ws = ops.mamba_scan_workspace_size(B, L, D, n)
-    need = (B * L * 32 * 4 + B * n * D * 16 * 4 + B * (n - 1) * D * 16 * 4 + B * (n - 1) * D * 4
-            + B * (D // 16) * 4)
+    need = (B * L * 32 * 4 + B * n * D * 16 * 4 + B * (n - 1) * m * D * 16 * 4 + B * (n - 1) * m * D * 4
+            + B * (D // 32) * 4)
     assert need <= ws <= need + 5 * 256
-    # a chunk count larger than the number of 64-token tiles is clamped
-    assert ops.mamba_scan_workspace_size(1, 100, 16, 50) == ops.mamba_scan_workspace_size(1, 100, 16, 2)
-    assert ops.mamba_scan_default_chunks(1, 64, 16) == 1
-    assert ops.mamba_scan_default_chunks(1, 32768, 8192) == 1
-    assert ops.mamba_scan_default_chunks(1, 32768, 16) > 1
+    # chunks are whole 16-token tiles; a chunk count above the tile count is clamped
+    assert ops.mamba_scan_plan(1, 100, 16, 50)["n_chunks"] == 7
+    p3 = ops.mamba_scan_plan(1, 100, 16, 3)
+    assert p3["n_chunks"] == 3 and p3["chunk_len"] == 48
+    p4 = ops.mamba_scan_plan(1, 100, 16, 4)
+    assert p4["n_chunks"] == 4 and p4["chunk_len"] == 32
+    assert ops.mamba_scan_default_chunks(1, 16, 16) == 1
+    # batch 1 at the Jamba shape cannot fill the GPU with channel groups alone: chunked
+    big = ops.mamba_scan_plan(1, 32768, 8192, 0)
+    assert big["n_chunks"] > 1 and big["chunk_len"] * big["n_chunks"] >= 32768
+    # many sequences fill it: one pass
+    assert ops.mamba_scan_default_chunks(64, 4096, 8192) == 1

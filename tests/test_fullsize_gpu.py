@@ -39,26 +39,37 @@ def test_jamba_prefill_full_size():
 def test_prefill_256k_host_chunks_equal_one_pass():
     w = inputs.PREFILL_256K
     inp = inputs.workload_inputs(w, device="cuda")
-    y, fh, fcs = run_gpu(inp)
-    assert ops.mamba_scan_default_chunks(w.batch, w.seqlen, w.d_inner) == 1
-    # the same sequence as 64 calls of 4096 tokens, state carried between them
     step = w.seqlen // w.host_chunks
-    ys = torch.empty_like(y)
-    h, cs = None, None
-    for i in range(w.host_chunks):
-        part = dict(inp, h0=h, conv_state0=cs)
-        for k in ("x", "z", "dt_raw", "Bm", "Cm"):
-            part[k] = inp[k][:, i * step:(i + 1) * step]
-        _, h, cs = run_gpu(part, y=ys[:, i * step:(i + 1) * step])
+
+    def split_calls(n_chunks):
+        ys = torch.empty_like(inp["x"])
+        h, cs = None, None
+        for i in range(w.host_chunks):
+            part = dict(inp, h0=h, conv_state0=cs)
+            for k in ("x", "z", "dt_raw", "Bm", "Cm"):
+                part[k] = inp[k][:, i * step:(i + 1) * step]
+            _, h, cs = run_gpu(part, y=ys[:, i * step:(i + 1) * step], n_chunks=n_chunks)
+        return ys, h, cs
+
+    # one sequential pass == the same sequence as 64 calls of 4096 tokens with
+    # the state carried between them, bit for bit
+    y, fh, fcs = run_gpu(inp, n_chunks=1)
+    ys, h, cs = split_calls(1)
     torch.cuda.synchronize()
     assert torch.equal(ys, y)
     assert torch.equal(h, fh) and torch.equal(cs, fcs)
     del ys
-    check_sampled(inp, (y, fh, fcs), sample_channels(w.d_inner, 12), w.io, w.name)
-    # the kernel's own chunked mode (64 chunks in parallel) agrees within tolerance
-    yc, fhc, fcsc = run_gpu(inp, n_chunks=64)
+    cs12 = sample_channels(w.d_inner, 12)
+    check_sampled(inp, (y, fh, fcs), cs12, w.io, w.name)
+    del y
+    # the default (chunked) plan, in one call and in 64 carried calls
+    outs = run_gpu(inp)
     torch.cuda.synchronize()
-    check_sampled(inp, (yc, fhc, fcsc), sample_channels(w.d_inner, 12), w.io, w.name + " chunked")
+    check_sampled(inp, outs, cs12, w.io, w.name + " default plan")
+    del outs
+    outs = split_calls(0)
+    torch.cuda.synchronize()
+    check_sampled(inp, outs, cs12, w.io, w.name + " default plan, 64 carried calls")
 
 
 def test_decode_28_layers_full_size():
