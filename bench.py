@@ -163,6 +163,34 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.samples)}
 
 
+# ---------------------------------------------------------------- ncu traffic record
+def sources_digest() -> str:
+    """sha256 over the CUDA/C++ sources of the library: a DRAM-traffic figure
+    measured by ncu is reported only for the sources it was measured on."""
+    import hashlib
+    csrc = os.path.join(ROOT, "selective_state_space_118_b300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".cpp", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(key: str):
+    """DRAM bytes per call from profiles/dram_traffic.json (written from an ncu
+    capture, see the profiles' command lines), or None when absent or taken on
+    other sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            rec = json.load(f)
+        if rec.get("sources_sha256") != sources_digest():
+            return None
+        return rec["per_call_bytes"].get(key)
+    except Exception:
+        return None
+
+
 # ---------------------------------------------------------------- byte counts
 def scan_algorithmic_bytes(B, L, D, es):
     """Minimum HBM bytes of one prefill call: x, z, dt_raw read and y written
@@ -268,11 +296,15 @@ def bench_e2e(w, inp, out, ws, steps, local):
             "steps": steps, "ms_per_step": t * 1e3 / steps}
 
 
-def bench_decode(w, local, replays=3):
+def bench_decode(w, local, replays=3, layers=None, tokens=None):
     """28 layers x 256 tokens, one mamba_step per layer and token, replayed
     from one CUDA graph.  decode steps/s = tokens (for all 64 sequences
     through all layers) per second."""
     from selective_state_space_118_b300 import ops
+    import dataclasses
+    if layers or tokens:  # a smaller block of the same workload (profiling)
+        w = dataclasses.replace(w, name=f"{w.name}@{layers or w.layers}x{tokens or w.steps}",
+                                layers=layers or w.layers, steps=tokens or w.steps)
     dev = torch.device("cuda", local)
     states = [inputs.decode_layer_state(w, l, device=dev) for l in range(w.layers)]
     toks = [inputs.decode_token_inputs(w, l, w.steps, device=dev) for l in range(w.layers)]
@@ -397,6 +429,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=inputs.JAMBA_PREFILL.name, choices=list(inputs.SCAN_WORKLOADS))
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="decode block only (profiling)")
+    ap.add_argument("--decode-layers", type=int, default=0, help="fewer decode layers (profiling)")
+    ap.add_argument("--decode-tokens", type=int, default=0, help="fewer decode tokens (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--n-chunks", type=int, default=0,
@@ -415,6 +450,11 @@ def main():
     if rank == 0 and not os.path.exists(ops.LIB_PATH):
         build.build()
     barrier(world)
+    if args.no_prefill:
+        d = bench_decode(inputs.DECODE, local, layers=args.decode_layers, tokens=args.decode_tokens)
+        if rank == 0:
+            print(json.dumps(d), flush=True)
+        return
     w = workload_of(args)
     res, inp, out, ws = bench_prefill(w, args.steps, args.warmup, world, local, args.n_chunks)
     elems_all = res["elems"] * args.steps * world
@@ -426,7 +466,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.io,
             "data": "synthetic", "config": dict(config_of(w, res["n_chunks"]), plan=res["plan"]),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": None, "peak_source": src,
+                         "frac": achieved / hbm, "traffic": measured_traffic(w.name), "peak_source": src,
                          "kernel": "mamba_scan_fwd: bc_widen + scan_piece_summary + scan_fwd (one call)",
                          "algorithmic_bytes_per_launch": res["alg_bytes"]},
             "gpu_launches": res["launches_per_step"] * args.steps,
@@ -439,10 +479,11 @@ def main():
     del inp, out, ws
     torch.cuda.empty_cache()
     if not args.no_decode:
-        line["decode"] = bench_decode(inputs.DECODE, local)
+        line["decode"] = bench_decode(inputs.DECODE, local, layers=args.decode_layers,
+                                      tokens=args.decode_tokens)
         torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        v, desc = oracle_sample_rate(w, target_s=10.0)
+        v, desc = oracle_sample_rate(w, target_s=10.0, max_channels=w.d_inner)
         line["cpu_baseline"] = dict(desc, value=v, unit=UNIT)
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -164,10 +164,12 @@ mamba_status mamba_scan_fwd_noalloc(const mamba_scan_args *args, void *stream);
  * h_{t-1} and x_t).  Bit for bit the same arithmetic as one token of
  * mamba_scan_fwd with n_chunks = 1.
  *
- *   h                 (B, D, 16) fp32     in/out, in place
+ *   h                 (B, D, 16) fp32     in/out, in place; 32-byte aligned
+ *                                         (it is read and written in
+ *                                         32-byte pieces)
  *   conv_state        (B, 3, D) io        in/out, in place (shifts by one)
  *   x_t, z_t, dt_raw_t  (B, D) io
- *   B_t, C_t          (B, 16) io
+ *   B_t, C_t          (B, 16) io          (16-byte aligned, like h)
  *   A_log, Dskip, conv_w, conv_b   as for the scan
  *   y_t               (B, D) io           output
  */

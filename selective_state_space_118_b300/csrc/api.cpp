@@ -330,9 +330,10 @@ mamba_status mamba_step(const mamba_step_args* a, void* stream_v) {
                        a->A_log, a->Dskip, a->conv_w, a->y_t};
   for (const void* p : req)
     if (!p) return MAMBA_ERR_INVALID_ARG;
-  const void* al[] = {a->h, a->A_log, a->conv_w, a->conv_b};
+  const void* al[] = {a->h, a->A_log, a->conv_w, a->conv_b, a->B_t, a->C_t};
   for (const void* p : al)
     if (p && !aligned16(p)) return MAMBA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(a->h) & 31u) != 0) return MAMBA_ERR_INVALID_ARG;  // 32-byte accesses
   mamba::StepParams p;
   p.batch = a->batch;
   p.d_inner = a->d_inner;

@@ -65,13 +65,23 @@ cudaError_t launch_summary(IoType io, const CUtensorMap maps[3], const ScanParam
                             : launch_summary_t<float>(maps, p, grid, stream);
 }
 
+// Launched with programmatic stream serialization: the kernel may be
+// scheduled while the previous kernel in the stream finishes, and waits for
+// it (griddepcontrol.wait) before touching memory.
 cudaError_t launch_step(IoType io, const StepParams& p, cudaStream_t stream) {
-  const dim3 grid((unsigned)((p.d_inner + kStepThreads - 1) / kStepThreads), (unsigned)p.batch);
-  if (io == IoType::BF16)
-    step_kernel<__nv_bfloat16><<<grid, kStepThreads, 0, stream>>>(p);
-  else
-    step_kernel<float><<<grid, kStepThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((p.d_inner + kStepChannels - 1) / kStepChannels),
+                     (unsigned)p.batch);
+  cfg.blockDim = dim3(kStepThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (io == IoType::BF16) return cudaLaunchKernelEx(&cfg, step_kernel<__nv_bfloat16>, p);
+  return cudaLaunchKernelEx(&cfg, step_kernel<float>, p);
 }
 
 void scan_occupancy(IoType io, int* main_per_sm, int* summary_per_sm) {

@@ -103,6 +103,18 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream drains;
+// griddep_wait() blocks until that kernel has completed and its writes are
+// visible (a no-op when the launch had no such dependency), and
+// griddep_launch_dependents() lets the next such kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- global stores
 // Stores to global memory written as st.global: the compiler then knows they
 // cannot touch shared memory and may move later shared-memory loads above

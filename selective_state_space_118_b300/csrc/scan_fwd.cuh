@@ -44,6 +44,7 @@ constexpr int kLanes = 32;   // channels per CTA (one warp)
 constexpr int kT = kTileTokens;
 constexpr int kBC = 2 * kN;  // widened B and C per token
 constexpr int kStages = 2;   // TMA ring depth
+constexpr int kScanUnroll = 4;  // tokens unrolled in the tile loops
 
 // Sticky device error word (MAMBA_ERR_* code of the first failure).
 __device__ unsigned int g_mamba_error;
@@ -142,7 +143,7 @@ template <typename IO, bool kSmall>
 __device__ __forceinline__ void main_tile(const MainStage<IO>& S, int rows, int lane, bool active,
                                           const Channel& ch, State16& st, float& xm3, float& xm2, float& xm1,
                                           IO* ytile, int D) {
-#pragma unroll 4
+#pragma unroll(kScanUnroll)
   for (int r = 0; r < rows; ++r) {
     const float xv = to_f32(S.x[r][lane]);
     const float u = silu(conv4(ch.w, ch.bias, xm3, xm2, xm1, xv));
@@ -164,7 +165,7 @@ __device__ __forceinline__ void main_tile(const MainStage<IO>& S, int rows, int 
 template <typename IO, bool kSmall>
 __device__ __forceinline__ void summary_tile(const SummaryStage<IO>& S, int lane, const Channel& ch, State16& st,
                                              float& sdt, float& xm3, float& xm2, float& xm1) {
-#pragma unroll 4
+#pragma unroll(kScanUnroll)
   for (int r = 0; r < kT; ++r) {
     const float xv = to_f32(S.x[r][lane]);
     const float u = silu(conv4(ch.w, ch.bias, xm3, xm2, xm1, xv));

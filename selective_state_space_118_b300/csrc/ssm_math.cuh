@@ -10,10 +10,13 @@
 //   u   = silu(pre);   dt = softplus(dt_raw);   dtu = dt * u
 //   h_n = 2^(dt * A2_n) * h_n + dtu * B_n,      A2_n = -exp(A_log_n) * log2(e)
 //   y   = (sum_n C_n h_n + D u) * silu(z)
-// One lane owns one channel and all 16 of its states, held as 8 float2 pairs
-// (h[k] = states 2k, 2k+1) and advanced with packed f32x2 arithmetic.  The
-// read-out sum is fixed: p0 collects pairs 0,2,4,6 and p1 pairs 1,3,5,7, then
-// (p0.x + p1.x) + (p0.y + p1.y).
+// The prefill kernels keep all 16 states of a channel in one lane, as 8
+// float2 pairs (h[k] = states 2k, 2k+1) advanced with packed f32x2
+// arithmetic; the decode kernel splits them over 2 or 4 lanes.  The read-out
+// sum is fixed so that every layout produces the same bits: for each group
+// q of 4 states, p = (C_4q h_4q, C_4q+1 h_4q+1) + (C_4q+2 h_4q+2,
+// C_4q+3 h_4q+3) (one packed multiply, one packed fma) and g_q = p.x + p.y;
+// then sum_n C_n h_n = (g_0 + g_1) + (g_2 + g_3).
 #pragma once
 #include <cuda_bf16.h>
 
@@ -192,16 +195,20 @@ __device__ __forceinline__ void state16_advance(State16& s, const float2 (&a2)[8
   state16_apply(s, d);
 }
 
+// g of one group of 4 states: h0, h1 the group's two pairs, C its 4 values.
+__device__ __forceinline__ float readout4(float2 h0, float2 h1, float4 C) {
+  float2 p = __fmul2_rn(make_float2(C.x, C.y), h0);
+  p = __ffma2_rn(make_float2(C.z, C.w), h1, p);
+  return __fadd_rn(p.x, p.y);
+}
+
 // sum_n C_n h_n in the fixed order described at the top of the file.
 __device__ __forceinline__ float state16_readout(const State16& s, const float4 (&C)[4]) {
-  float2 p0 = __fmul2_rn(make_float2(C[0].x, C[0].y), s.h[0]);
-  float2 p1 = __fmul2_rn(make_float2(C[0].z, C[0].w), s.h[1]);
-#pragma unroll
-  for (int q = 1; q < 4; ++q) {
-    p0 = __ffma2_rn(make_float2(C[q].x, C[q].y), s.h[2 * q], p0);
-    p1 = __ffma2_rn(make_float2(C[q].z, C[q].w), s.h[2 * q + 1], p1);
-  }
-  return __fadd_rn(__fadd_rn(p0.x, p1.x), __fadd_rn(p0.y, p1.y));
+  const float g0 = readout4(s.h[0], s.h[1], C[0]);
+  const float g1 = readout4(s.h[2], s.h[3], C[1]);
+  const float g2 = readout4(s.h[4], s.h[5], C[2]);
+  const float g3 = readout4(s.h[6], s.h[7], C[3]);
+  return __fadd_rn(__fadd_rn(g0, g1), __fadd_rn(g2, g3));
 }
 
 // Carry fold: h <- 2^(A2 S) h + hl, S the summed dt of a span of tokens and

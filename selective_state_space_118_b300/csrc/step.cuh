@@ -1,63 +1,149 @@
 // step.cuh -- decode: one token through the layer, state updated in place.
 //
 // The constant-memory recurrence of the lesson's "Um SSM em uma pagina":
-// y_t needs only h_{t-1}, the last three inputs and x_t.  One thread serves
-// one (batch row, channel) and holds its 16 fp32 states in registers: it reads
-// and writes its 64 bytes of h as four 16-byte accesses (a warp moves 32
-// channels x 64 B contiguously).  The per-token arithmetic is ssm_math.cuh's,
-// in the same order as one token of scan_fwd_kernel, so a sequence of steps
-// reproduces a single-pass scan bit for bit.  The step is HBM-bound: h is 128
-// of the ~144 bytes moved per channel.
+// y_t needs only h_{t-1}, the last three inputs and x_t.  kLPC lanes (2 or 4)
+// serve one (batch row, channel), lane q holding states 16/kLPC * q onwards,
+// each reading and writing its part of h with one 32- or 16-byte access, so
+// that a warp instruction moves a contiguous 1 KB or 512 B of h (a
+// lane-per-channel layout touches 16 cache lines per instruction and
+// throttles the load/store unit).  The lanes of a channel all compute its
+// conv, SiLU, softplus and gate (cheap: the step is HBM-bound, not
+// arithmetic-bound); their read-out groups meet through shuffles in the
+// fixed order of state16_readout.  The arithmetic is ssm_math.cuh's, in the
+// same order as one token of scan_fwd_kernel, so a sequence of steps
+// reproduces a single-pass scan bit for bit.  h is 128 of the ~144 bytes
+// moved per channel and row; many small threads (one row each) keep more
+// bytes in flight per SM than fewer threads with several rows.
 #pragma once
 #include <cuda_bf16.h>
 
 #include "params.h"
+#include "ptx.cuh"
 #include "ssm_math.cuh"
 
 namespace mamba {
 
 constexpr int kStepThreads = 128;
+constexpr int kLPC = 2;                       // lanes per (row, channel): 2 or 4
+constexpr int kLS = kN / kLPC;                // states per lane: 8 or 4
+constexpr int kStepChannels = kStepThreads / kLPC;
+static_assert(kLPC == 2 || kLPC == 4, "2 or 4 lanes per channel");
 
-template <typename IO>
-__device__ __forceinline__ void load16_io(const IO* p, float4 (&v)[4]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    v[q] = make_float4(to_f32(p[4 * q]), to_f32(p[4 * q + 1]), to_f32(p[4 * q + 2]), to_f32(p[4 * q + 3]));
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// kLS consecutive fp32 values of h.
+__device__ __forceinline__ void load_h(const float* p, float4 (&v)[kLS / 4]) {
+  if constexpr (kLS == 8) {
+    asm volatile("ld.global.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=f"(v[0].x), "=f"(v[0].y), "=f"(v[0].z), "=f"(v[0].w), "=f"(v[1].x), "=f"(v[1].y),
+                   "=f"(v[1].z), "=f"(v[1].w)
+                 : "l"(p));
+  } else {
+    v[0] = *reinterpret_cast<const float4*>(p);
+  }
 }
 
-// grid (ceil(D / 128), batch), 128 threads: thread = channel of one batch row.
+__device__ __forceinline__ void store_h(float* p, const float4 (&v)[kLS / 4]) {
+  if constexpr (kLS == 8) {
+    asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v[0].x), "f"(v[0].y),
+                 "f"(v[0].z), "f"(v[0].w), "f"(v[1].x), "f"(v[1].y), "f"(v[1].z), "f"(v[1].w)
+                 : "memory");
+  } else {
+    *reinterpret_cast<float4*>(p) = v[0];
+  }
+}
+
+// kLS consecutive I/O values (part of a B or C row) as fp32.
+__device__ __forceinline__ void load_part(const float* p, float4 (&v)[kLS / 4]) {
+#pragma unroll
+  for (int q = 0; q < kLS / 4; ++q) v[q] = __ldg(reinterpret_cast<const float4*>(p) + q);
+}
+
+__device__ __forceinline__ void load_part(const __nv_bfloat16* p, float4 (&v)[kLS / 4]) {
+  if constexpr (kLS == 8) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+    v[0] = make_float4(bf16_lo(a.x), bf16_hi(a.x), bf16_lo(a.y), bf16_hi(a.y));
+    v[1] = make_float4(bf16_lo(a.z), bf16_hi(a.z), bf16_lo(a.w), bf16_hi(a.w));
+  } else {
+    const uint2 a = __ldg(reinterpret_cast<const uint2*>(p));
+    v[0] = make_float4(bf16_lo(a.x), bf16_hi(a.x), bf16_lo(a.y), bf16_hi(a.y));
+  }
+}
+
+// (mine + other) for the lower lane of an exchanged pair, (other + mine) for
+// the upper: both lanes get the same bits, in the order lower + upper.
+__device__ __forceinline__ float pair_sum(float mine, int lane_bit, int upper) {
+  const float other = __shfl_xor_sync(0xffffffffu, mine, lane_bit);
+  return upper ? __fadd_rn(other, mine) : __fadd_rn(mine, other);
+}
+
+// grid (ceil(D / kStepChannels), batch), kStepThreads threads: kLPC
+// consecutive threads = one channel of one batch row.
 template <typename IO>
 __global__ void __launch_bounds__(kStepThreads) step_kernel(const __grid_constant__ StepParams p) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int D = p.d_inner;
-  const int c = blockIdx.x * kStepThreads + threadIdx.x;
+  const int q = threadIdx.x % kLPC;
+  const int c = blockIdx.x * kStepChannels + threadIdx.x / kLPC;
   const int b = blockIdx.y;
-  if (c >= D) return;
-  const size_t ch = (size_t)b * D + c;
+  const bool valid = c < D;  // the lanes of a channel share it
+  const int cl = valid ? c : D - 1;
+  const size_t ch = (size_t)b * D + cl;
 
-  float* hp = p.h + ch * kN;
-  State16 st;
-  state16_load(st, hp);
-  IO* cs = reinterpret_cast<IO*>(p.conv_state) + (size_t)b * 3 * D + c;
+  float4 hv[kLS / 4], Bv[kLS / 4], Cv[kLS / 4];
+  load_h(p.h + ch * kN + kLS * q, hv);
+  const IO* cs = reinterpret_cast<const IO*>(p.conv_state) + (size_t)b * 3 * D + cl;
   const IO r0 = cs[0], r1 = cs[D], r2 = cs[2 * (size_t)D];
-  const IO rx = reinterpret_cast<const IO*>(p.x_t)[ch];
-  const float zv = to_f32(reinterpret_cast<const IO*>(p.z_t)[ch]);
-  const float dr = to_f32(reinterpret_cast<const IO*>(p.dt_raw_t)[ch]);
-  float4 Bv[4], Cv[4];
-  load16_io(reinterpret_cast<const IO*>(p.B_t) + (size_t)b * kN, Bv);
-  load16_io(reinterpret_cast<const IO*>(p.C_t) + (size_t)b * kN, Cv);
-  Channel chn;
-  load_channel(chn, p.A_log, p.conv_w, p.conv_b, p.Dskip, c);
+  const IO rx = __ldg(reinterpret_cast<const IO*>(p.x_t) + ch);
+  const float zv = to_f32(__ldg(reinterpret_cast<const IO*>(p.z_t) + ch));
+  const float dr = to_f32(__ldg(reinterpret_cast<const IO*>(p.dt_raw_t) + ch));
+  load_part(reinterpret_cast<const IO*>(p.B_t) + (size_t)b * kN + kLS * q, Bv);
+  load_part(reinterpret_cast<const IO*>(p.C_t) + (size_t)b * kN + kLS * q, Cv);
+  float4 al[kLS / 4];
+  load_part(p.A_log + (size_t)cl * kN + kLS * q, al);
+  const float4 w = __ldg(reinterpret_cast<const float4*>(p.conv_w + (size_t)cl * 4));
+  const float bias = p.conv_b ? __ldg(p.conv_b + cl) : 0.0f;
+  const float Dc = __ldg(p.Dskip + cl);
 
-  const float u = silu(conv4(chn.w, chn.bias, to_f32(r0), to_f32(r1), to_f32(r2), to_f32(rx)));
+  const float u = silu(conv4(w, bias, to_f32(r0), to_f32(r1), to_f32(r2), to_f32(rx)));
   const float dt = softplus(dr);
   const float gz = silu(zv);
-  state16_advance(st, chn.a2, dt, __fmul_rn(dt, u), Bv);
-  const float yv = gate_out(state16_readout(st, Cv), chn.Dc, u, gz);
-  state16_store(st, hp);
-  reinterpret_cast<IO*>(p.y_t)[ch] = from_f32<IO>(yv);
-  cs[0] = r1;
-  cs[D] = r2;
-  cs[2 * (size_t)D] = rx;
+  const float2 d2 = make_float2(dt, dt);
+  const float dtu = __fmul_rn(dt, u);
+  const float2 u2 = make_float2(dtu, dtu);
+  float g[kLS / 4];
+#pragma unroll
+  for (int k = 0; k < kLS / 4; ++k) {  // one group of 4 states: pairs h01, h23
+    const float2 a01 = make_float2(a2_from_log(al[k].x), a2_from_log(al[k].y));
+    const float2 a23 = make_float2(a2_from_log(al[k].z), a2_from_log(al[k].w));
+    const float2 x01 = __fmul2_rn(d2, a01), x23 = __fmul2_rn(d2, a23);
+    const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+    const float2 e23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+    float2 h01 = make_float2(hv[k].x, hv[k].y), h23 = make_float2(hv[k].z, hv[k].w);
+    h01 = __ffma2_rn(e01, h01, __fmul2_rn(u2, make_float2(Bv[k].x, Bv[k].y)));
+    h23 = __ffma2_rn(e23, h23, __fmul2_rn(u2, make_float2(Bv[k].z, Bv[k].w)));
+    hv[k] = make_float4(h01.x, h01.y, h23.x, h23.y);
+    g[k] = readout4(h01, h23, Cv[k]);
+  }
+  // (g0 + g1) + (g2 + g3) over the channel's lanes
+  float ss;
+  if constexpr (kLPC == 2) {
+    ss = pair_sum(__fadd_rn(g[0], g[1]), 1, q);
+  } else {
+    ss = pair_sum(pair_sum(g[0], 1, q & 1), 2, q >> 1);
+  }
+  if (valid) {
+    store_h(p.h + ch * kN + kLS * q, hv);
+    if (q == 0) {
+      reinterpret_cast<IO*>(p.y_t)[ch] = from_f32<IO>(gate_out(ss, Dc, u, gz));
+      IO* csw = reinterpret_cast<IO*>(p.conv_state) + (size_t)b * 3 * D + c;
+      csw[0] = r1;
+      csw[D] = r2;
+      csw[2 * (size_t)D] = rx;
+    }
+  }
 }
 
 }  // namespace mamba

@@ -104,6 +104,12 @@ def test_scan_argument_checks(lib, kw, status):
 def test_step_argument_checks(lib):
     a = ops.StepArgs(batch=1, d_inner=16, d_state=16, d_conv=4, io=ops.MAMBA_BF16)
     assert lib.mamba_step(ctypes.byref(a), None) == ops.MAMBA_ERR_INVALID_ARG
+    full = dict(batch=1, d_inner=16, d_state=16, d_conv=4, io=ops.MAMBA_BF16, h=FAKE, conv_state=FAKE,
+                x_t=FAKE, z_t=FAKE, dt_raw_t=FAKE, B_t=FAKE, C_t=FAKE, A_log=FAKE, Dskip=FAKE,
+                conv_w=FAKE, y_t=FAKE)
+    for k, off in (("h", 16), ("B_t", 8), ("A_log", 4)):  # h needs 32 bytes, the others 16
+        a = ops.StepArgs(**dict(full, **{k: FAKE + off}))
+        assert lib.mamba_step(ctypes.byref(a), None) == ops.MAMBA_ERR_INVALID_ARG, k
     a.d_state = 32
     assert lib.mamba_step(ctypes.byref(a), None) == ops.MAMBA_ERR_UNSUPPORTED
     assert lib.mamba_step(None, None) == ops.MAMBA_ERR_INVALID_ARG
