@@ -95,26 +95,15 @@ double pass_time(long items, int tiles, double cost, int sms, int per_sm) {
   return (double)per_unit * (tiles + 0.5) * cost / ipc;
 }
 
-// For a chunk length, the summary piece count with the least modelled time.
-void choose_pieces(long groups, int n_chunks, int chunk_tiles, const Machine& mc, int* pieces, int* piece_tiles,
-                   double* time) {
-  *pieces = 1;
-  *piece_tiles = chunk_tiles;
-  *time = 0.0;
-  if (n_chunks <= 1) return;
-  double best = -1.0;
-  for (int m = 1; m <= 16 && m <= chunk_tiles; ++m) {
-    const int P = (chunk_tiles + m - 1) / m;
-    const int m_eff = (chunk_tiles + P - 1) / P;
-    const double t = pass_time(groups * (n_chunks - 1) * m_eff, P, 0.7, mc.sms, mc.summary_per_sm);
-    if (best < 0.0 || t < best - 1e-9) {
-      best = t;
-      *pieces = m_eff;
-      *piece_tiles = P;
-    }
-  }
-  *time = best;
-}
+// Carry pieces: 16 tiles (256 tokens).  A boundary's walk stops at a piece
+// boundary, so shorter pieces waste less past the point where the decay makes
+// earlier tokens negligible; longer ones keep the TMA ring flowing.
+constexpr int kPieceTiles = 16;
+
+// Expected tiles walked per chunk boundary when the inputs decay fast (the
+// walk stops after the decay reaches 2^-32; ~1,000 tokens for dt ~ 0.02,
+// A = -1): used only to size the plan.
+constexpr int kCarryTilesEstimate = 64;
 
 // The plan depends only on the sizes (not on the I/O dtype), so that the
 // workspace queries, which take no dtype, agree with the call.
@@ -130,37 +119,37 @@ Plan make_plan(int batch, int seqlen, int d_inner, int n_chunks_req) {
   for (int n = lo; n <= hi; ++n) {
     const int C = (tiles + n - 1) / n;
     const int n_eff = (tiles + C - 1) / C;
-    int m = 1, P = C;
-    double t_sum = 0.0;
-    choose_pieces(groups, n_eff, C, mc, &m, &P, &t_sum);
-    const double t = pass_time(groups * n_eff, C, 1.0, mc.sms, mc.main_per_sm) + t_sum;
+    const int P = C < kPieceTiles ? C : kPieceTiles;
+    const int m = (C + P - 1) / P;
+    const int walk = C < kCarryTilesEstimate ? C : kCarryTilesEstimate;
+    const double t_carry = n_eff > 1 ? pass_time(groups * (n_eff - 1), walk, 0.7, mc.sms, mc.summary_per_sm) : 0.0;
+    const double t = pass_time(groups * n_eff, C, 1.0, mc.sms, mc.main_per_sm) + t_carry;
     if (best < 0.0 || t < best - 1e-9) {
       best = t;
-      pl = Plan{n_eff, C, m, P};
+      pl = Plan{n_eff, C, n_eff > 1 ? m : 1, n_eff > 1 ? P : C};
     }
   }
   return pl;
 }
 
 struct Workspace {
-  size_t bc, carry, hloc, sum_dt, counters, total;
+  size_t bc, carry, counters, counters_bytes, total;
 };
 
-// bc: B and C widened to fp32 and interleaved, (B, L, 32); then, in chunked
-// mode only, the carries, piece summaries and arrival counters.
+// bc: B and C widened to fp32 in pair quads, (B, L, 32); then, in chunked
+// mode only, the carries (B, n_chunks, D, 16) and the counters: a ticket
+// counter and (B, groups, n_chunks) ready flags.
 Workspace workspace_layout(int batch, int seqlen, int d_inner, const Plan& pl) {
-  Workspace w{0, 0, 0, 0, 0, 0};
+  Workspace w{0, 0, 0, 0, 0};
   const size_t B = batch, L = seqlen, D = d_inner, n = pl.n_chunks;
-  const size_t np = (n - 1) * (size_t)pl.pieces;
   const size_t G = (D + kLanes - 1) / kLanes;
   w.bc = 0;
   w.total = round256(B * L * 32 * sizeof(float));
   if (pl.n_chunks <= 1) return w;
   w.carry = w.total;
-  w.hloc = round256(w.carry + B * n * D * 16 * sizeof(float));
-  w.sum_dt = round256(w.hloc + B * np * D * 16 * sizeof(float));
-  w.counters = round256(w.sum_dt + B * np * D * sizeof(float));
-  w.total = round256(w.counters + B * G * sizeof(unsigned));
+  w.counters = round256(w.carry + B * n * D * 16 * sizeof(float));
+  w.counters_bytes = (1 + B * G * n) * sizeof(unsigned);
+  w.total = round256(w.counters + w.counters_bytes);
   return w;
 }
 
@@ -270,13 +259,13 @@ mamba_status mamba_scan_fwd(const mamba_scan_args* a, void* stream_v) {
   char* wsp = static_cast<char*>(a->workspace);
   float* bc = reinterpret_cast<float*>(wsp + ws.bc);
 
-  // x, z, dt_raw, bc (both rows), bc (the B row only, for the summary pass)
+  // x, z, dt_raw, bc (main pass), bc (summary pass)
   CUtensorMap maps[5];
   if (!encode3d(&maps[0], a->x, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
       !encode3d(&maps[1], a->z, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
       !encode3d(&maps[2], a->dt_raw, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
       !encode3d(&maps[3], bc, MAMBA_F32, 32, a->seqlen, a->batch, 32) ||
-      !encode3d(&maps[4], bc, MAMBA_F32, 32, a->seqlen, a->batch, 16))
+      !encode3d(&maps[4], bc, MAMBA_F32, 32, a->seqlen, a->batch, 32))
     return MAMBA_ERR_CUDA;
 
   mamba::ScanParams p;
@@ -307,13 +296,10 @@ mamba_status mamba_scan_fwd(const mamba_scan_args* a, void* stream_v) {
     return MAMBA_ERR_CUDA;
   if (pl.n_chunks > 1) {
     p.carry = reinterpret_cast<float*>(wsp + ws.carry);
-    p.hloc = reinterpret_cast<float*>(wsp + ws.hloc);
-    p.sum_dt = reinterpret_cast<float*>(wsp + ws.sum_dt);
     p.counters = reinterpret_cast<unsigned*>(wsp + ws.counters);
-    if (cudaMemsetAsync(p.counters, 0, B * (size_t)p.n_groups * sizeof(unsigned), stream) != cudaSuccess)
-      return MAMBA_ERR_CUDA;
-    const CUtensorMap smaps[3] = {maps[0], maps[2], maps[4]};  // x, dt_raw, B rows
-    dim3 g1((unsigned)p.n_groups, (unsigned)B, (unsigned)((pl.n_chunks - 1) * pl.pieces));
+    if (cudaMemsetAsync(p.counters, 0, ws.counters_bytes, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+    const CUtensorMap smaps[3] = {maps[0], maps[2], maps[4]};  // x, dt_raw, B/C rows
+    dim3 g1((unsigned)((size_t)(pl.n_chunks - 1) * p.n_groups * B));
     if (mamba::launch_summary(io, smaps, p, g1, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
   }
   dim3 g2((unsigned)p.n_groups, (unsigned)B, (unsigned)pl.n_chunks);

@@ -3,7 +3,8 @@ softplus for small e (so that softplus(v) = e * P(e), e = exp(v), needs no
 reciprocal).  Method: linear least squares in the monomial basis on 4000
 Chebyshev nodes of the interval, in fp64, rounded to fp32.  Running it
 prints the coefficients (constant term first) that ssm_math.cuh holds, and
-the maximum relative error of e * P(e) evaluated in fp32 by Horner's rule.
+the maximum relative error of e * P(e) evaluated in fp32 the way the kernels
+do (Estrin's scheme, fused multiply-adds).
 """
 import numpy as np
 
@@ -20,12 +21,25 @@ def fit(degree: int = DEGREE, nodes: int = 4000):
     return c.astype(np.float32)
 
 
+def _fma32(a, b, c):
+    """fp32 fused multiply-add: the exact a*b+c (fp64 holds it for fp32 inputs
+    up to the last bits that matter here) rounded once to fp32."""
+    return (a.astype(np.float64) * b.astype(np.float64) + c.astype(np.float64)).astype(np.float32)
+
+
+def estrin32(c32, e):
+    """P(e) = (c0 + c1 e) + e^2 ((c2 + c3 e) + e^2 (c4 + c5 e)) in fp32."""
+    c = [np.full_like(e, v) for v in c32]
+    e2 = (e * e).astype(np.float32)
+    q0 = _fma32(e, c[1], c[0])
+    q1 = _fma32(e, c[3], c[2])
+    q2 = _fma32(e, c[5], c[4])
+    return _fma32(_fma32(q2, e2, q1), e2, q0)
+
+
 def max_rel_error(c32) -> float:
     e = np.linspace(LO, HI, 200001).astype(np.float32)[1:]
-    p = np.float32(c32[-1])
-    for ci in c32[-2::-1]:
-        p = (p * e + ci).astype(np.float32)
-    r = (e * p).astype(np.float32)
+    r = (e * estrin32(c32, e)).astype(np.float32)
     ref = np.log1p(e.astype(np.float64))
     return float(np.max(np.abs(r - ref) / ref))
 

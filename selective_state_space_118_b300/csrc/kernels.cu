@@ -1,5 +1,5 @@
 // kernels.cu -- the one translation unit holding the device code (prefill,
-// piece summaries, decode step and the sticky error word) and its launchers.
+// chunk carries, decode step and the sticky error word) and its launchers.
 #include <cuda_bf16.h>
 
 #include "launch.h"
@@ -13,7 +13,7 @@ size_t scan_smem_bytes(IoType io) {
 }
 
 size_t summary_smem_bytes(IoType io) {
-  return (io == IoType::BF16 ? sizeof(SummarySmem<__nv_bfloat16>) : sizeof(SummarySmem<float>)) + 128;
+  return (io == IoType::BF16 ? sizeof(CarrySmem<__nv_bfloat16>) : sizeof(CarrySmem<float>)) + 128;
 }
 
 template <typename IO>
@@ -28,11 +28,11 @@ static cudaError_t launch_scan_t(const CUtensorMap* m, const ScanParams& p, dim3
 
 template <typename IO>
 static cudaError_t launch_summary_t(const CUtensorMap* m, const ScanParams& p, dim3 grid, cudaStream_t s) {
-  const size_t smem = sizeof(SummarySmem<IO>) + 128;
-  cudaError_t e = cudaFuncSetAttribute(scan_piece_summary_kernel<IO>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = sizeof(CarrySmem<IO>) + 128;
+  cudaError_t e = cudaFuncSetAttribute(scan_carry_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
   if (e != cudaSuccess) return e;
-  scan_piece_summary_kernel<IO><<<grid, kLanes, smem, s>>>(m[0], m[1], m[2], p);
+  scan_carry_kernel<IO><<<grid, kLanes, smem, s>>>(m[0], m[1], m[2], p);
   return cudaGetLastError();
 }
 
@@ -89,13 +89,13 @@ void scan_occupancy(IoType io, int* main_per_sm, int* summary_per_sm) {
   if (io == IoType::BF16) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, scan_fwd_kernel<__nv_bfloat16>, kLanes,
                                                       sizeof(MainSmem<__nv_bfloat16>) + 128) != cudaSuccess) a = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, scan_piece_summary_kernel<__nv_bfloat16>, kLanes,
-                                                      sizeof(SummarySmem<__nv_bfloat16>) + 128) != cudaSuccess) b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, scan_carry_kernel<__nv_bfloat16>, kLanes,
+                                                      sizeof(CarrySmem<__nv_bfloat16>) + 128) != cudaSuccess) b = 0;
   } else {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, scan_fwd_kernel<float>, kLanes,
                                                       sizeof(MainSmem<float>) + 128) != cudaSuccess) a = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, scan_piece_summary_kernel<float>, kLanes,
-                                                      sizeof(SummarySmem<float>) + 128) != cudaSuccess) b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, scan_carry_kernel<float>, kLanes,
+                                                      sizeof(CarrySmem<float>) + 128) != cudaSuccess) b = 0;
   }
   *main_per_sm = a;
   *summary_per_sm = b;

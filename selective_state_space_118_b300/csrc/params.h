@@ -14,7 +14,7 @@ struct ScanParams {
   int n_groups;     // ceil(d_inner / 32): one CTA (warp) per group of 32 channels
   int chunk_tiles;  // tiles of kTileTokens tokens per chunk
   int n_chunks;     // chunks of the sequence run in parallel (1: one pass)
-  int piece_tiles;  // tiles per summary piece (chunked mode)
+  int piece_tiles;  // tiles per carry piece (chunked mode)
   int pieces;       // pieces per chunk = ceil(chunk_tiles / piece_tiles)
   const float* A_log;
   const float* Dskip;
@@ -27,9 +27,8 @@ struct ScanParams {
   float* final_h;            // may be null
   void* final_conv_state;    // may be null
   float* carry;              // chunked: (B, n_chunks, D, 16) carried-in states (entry 0 unused)
-  float* hloc;               // chunked: (B, (n_chunks-1)*pieces, D, 16) piece end states from zero
-  float* sum_dt;             // chunked: (B, (n_chunks-1)*pieces, D)
-  unsigned* counters;        // chunked: (B, n_groups) arrival counters, zero between calls
+  unsigned* counters;        // chunked: [0] ticket counter, then (B, n_groups, n_chunks) ready
+                             // flags; zeroed before every call
   uint32_t flags;
   uint64_t timeout_ns;
 };

@@ -19,15 +19,11 @@
 //
 // Chunked mode.  At batch 1 the groups alone cannot fill the GPU, so the
 // sequence is cut into n_chunks chunks that run in parallel, each starting
-// from its carried-in state.  Those carries come from a first pass,
-// scan_piece_summary_kernel: every chunk but the last is cut into pieces; for
-// each piece it computes the end state hloc of the piece started from zero and
-// S = sum of dt over the piece; the last CTA to finish for a (group, batch
-// row) folds the pieces in order,
-//   carry <- h0;   for each piece: carry <- 2^(A2 S) carry + hloc
-// writing the carry at every chunk boundary (the "chunked scan equals the
-// sequential scan" identity of the oracle).  The fold order is fixed, so the
-// result does not depend on timing.
+// from its carried-in state.  Those carries come from a first kernel,
+// scan_carry_kernel (described with it below): one warp per chunk boundary
+// and channel group walks the previous chunk backwards in pieces and stops
+// where the decay to the boundary makes earlier tokens negligible (below
+// 2^-32 for every state), or else chains onto the previous boundary's carry.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -67,19 +63,22 @@ __device__ __forceinline__ float input_at(const ScanParams& p, int b, long tau, 
 }
 
 // ---------------------------------------------------------------- B, C widening
-// bc[row][0..15] = B[row][:], bc[row][16..31] = C[row][:] in fp32, for the
-// B*L token rows (64 bytes per token read in bf16), so that one TMA box
-// carries both rows and the lanes read fp32 directly.
+// B and C rows widened to fp32 in pair-quad layout: bc[row][4k .. 4k+3] =
+// (B_2k, B_2k+1, C_2k, C_2k+1) for the state pairs k = 0..7, for the B*L
+// token rows (64 bytes per token read in bf16).  One TMA box carries both
+// rows; one 128-bit shared load gives a lane the B and C values of one state
+// pair as two aligned register pairs.
 template <typename IO>
 __global__ void __launch_bounds__(256) bc_widen_kernel(const IO* __restrict__ Bm, const IO* __restrict__ Cm,
                                                        float* __restrict__ bc, long rows) {
-  const long n = rows * 8;  // 8 groups of 4 values per row (4 of B, then 4 of C)
+  const long n = rows * 8;  // 8 pair quads per row
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
     const long r = i >> 3;
-    const int q = (int)(i & 7);
-    const IO* src = (q < 4 ? Bm : Cm) + r * kN + (q & 3) * 4;
-    const float4 v = make_float4(to_f32(src[0]), to_f32(src[1]), to_f32(src[2]), to_f32(src[3]));
-    *reinterpret_cast<float4*>(bc + r * kBC + q * 4) = v;
+    const int k = (int)(i & 7);
+    const IO* b = Bm + r * kN + 2 * k;
+    const IO* c = Cm + r * kN + 2 * k;
+    *reinterpret_cast<float4*>(bc + r * kBC + 4 * k) =
+        make_float4(to_f32(b[0]), to_f32(b[1]), to_f32(c[0]), to_f32(c[1]));
   }
 }
 
@@ -102,19 +101,13 @@ template <typename IO>
 struct SummaryStage {
   IO x[kT][kLanes];
   IO dt[kT][kLanes];
-  float b[kT][kN];
+  float bc[kT][kBC];  // B and C (only B is used: the quads interleave them)
 };
 
-template <typename IO>
-struct SummarySmem {
-  SummaryStage<IO> stage[kStages];
-  uint64_t full[kStages];
-  int last;
-};
 
-__device__ __forceinline__ void load_bc4(const float* row, float4 (&v)[4]) {
+__device__ __forceinline__ void load_quads(const float* row, float4 (&Q)[8]) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) v[q] = *reinterpret_cast<const float4*>(row + 4 * q);
+  for (int k = 0; k < 8; ++k) Q[k] = *reinterpret_cast<const float4*>(row + 4 * k);
 }
 
 // Lets the copies already issued land (bounded) before shared memory goes away.
@@ -139,11 +132,13 @@ __device__ __forceinline__ float softplus_sel(float v) {
 }
 
 // One tile of the main pass, `rows` tokens, straight-line per token.
-template <typename IO, bool kSmall>
+// kFull: rows == kT, the loop is unrolled completely.
+template <typename IO, bool kSmall, bool kFull>
 __device__ __forceinline__ void main_tile(const MainStage<IO>& S, int rows, int lane, bool active,
                                           const Channel& ch, State16& st, float& xm3, float& xm2, float& xm1,
                                           IO* ytile, int D) {
-#pragma unroll(kScanUnroll)
+  if (kFull) rows = kT;
+#pragma unroll(kFull ? kT : kScanUnroll)
   for (int r = 0; r < rows; ++r) {
     const float xv = to_f32(S.x[r][lane]);
     const float u = silu(conv4(ch.w, ch.bias, xm3, xm2, xm1, xv));
@@ -152,16 +147,17 @@ __device__ __forceinline__ void main_tile(const MainStage<IO>& S, int rows, int 
     xm1 = xv;
     const float dt = softplus_sel<kSmall>(to_f32(S.dt[r][lane]));
     const float gz = silu(to_f32(S.z[r][lane]));
-    float4 Bv[4], Cv[4];
-    load_bc4(&S.bc[r][0], Bv);
-    load_bc4(&S.bc[r][kN], Cv);
-    state16_advance(st, ch.a2, dt, __fmul_rn(dt, u), Bv);
-    const float yv = gate_out(state16_readout(st, Cv), ch.Dc, u, gz);
+    float4 Q[8];
+    load_quads(&S.bc[r][0], Q);
+    Drive16 d;
+    drive16_q(d, ch.a2, dt, __fmul_rn(dt, u), Q);
+    state16_apply(st, d);
+    const float yv = gate_out(state16_readout_q(st, Q), ch.Dc, u, gz);
     st_global_if(active, ytile + (size_t)r * D, from_f32<IO>(yv));
   }
 }
 
-// One full tile of the summary pass.
+// One full tile of a carry piece (state and dt sum only).
 template <typename IO, bool kSmall>
 __device__ __forceinline__ void summary_tile(const SummaryStage<IO>& S, int lane, const Channel& ch, State16& st,
                                              float& sdt, float& xm3, float& xm2, float& xm1) {
@@ -173,9 +169,11 @@ __device__ __forceinline__ void summary_tile(const SummaryStage<IO>& S, int lane
     xm2 = xm1;
     xm1 = xv;
     const float dt = softplus_sel<kSmall>(to_f32(S.dt[r][lane]));
-    float4 Bv[4];
-    load_bc4(&S.b[r][0], Bv);
-    state16_advance(st, ch.a2, dt, __fmul_rn(dt, u), Bv);
+    float4 Q[8];
+    load_quads(&S.bc[r][0], Q);
+    Drive16 d;
+    drive16_q(d, ch.a2, dt, __fmul_rn(dt, u), Q);
+    state16_apply(st, d);
     sdt = __fadd_rn(sdt, dt);
   }
 }
@@ -266,10 +264,15 @@ __global__ void __launch_bounds__(kLanes)
     bool mine = mbar_wait_bounded(smem_u32(&sm.full[s]), (k / kStages) & 1, p.timeout_ns);
     ok = __all_sync(0xffffffffu, mine);
     if (!ok) break;
-    if (small_dt_tile<IO>(S.dt, t_valid, lane, active))
-      main_tile<IO, true>(S, t_valid, lane, active, ch, st, xm3, xm2, xm1, yrow + (size_t)k * kT * D, D);
-    else
-      main_tile<IO, false>(S, t_valid, lane, active, ch, st, xm3, xm2, xm1, yrow + (size_t)k * kT * D, D);
+    IO* ytile = yrow + (size_t)k * kT * D;
+    if (small_dt_tile<IO>(S.dt, t_valid, lane, active)) {
+      if (t_valid == kT)
+        main_tile<IO, true, true>(S, kT, lane, active, ch, st, xm3, xm2, xm1, ytile, D);
+      else
+        main_tile<IO, true, false>(S, t_valid, lane, active, ch, st, xm3, xm2, xm1, ytile, D);
+    } else {
+      main_tile<IO, false, false>(S, t_valid, lane, active, ch, st, xm3, xm2, xm1, ytile, D);
+    }
     __syncwarp();  // every lane is done with stage s
     if (lane == 0 && k + kStages < n_tiles) {
       constexpr uint32_t kBytes = 3 * kT * kLanes * sizeof(IO) + kT * kBC * sizeof(float);
@@ -293,62 +296,129 @@ __global__ void __launch_bounds__(kLanes)
   if (j == p.n_chunks - 1 && p.final_h && active) state16_store(st, p.final_h + ((size_t)b * D + c) * kN);
 }
 
-// ---------------------------------------------------------------- piece summaries
-// grid (n_groups, batch, (n_chunks - 1) * pieces), 32 threads.  Piece q of
-// chunk jc covers tiles [jc*C + q*P, min(jc*C + (q+1)*P, (jc+1)*C)).
+// ---------------------------------------------------------------- chunk carries
+// One warp per (chunk boundary j = 1..n_chunks-1, channel group, batch row),
+// assigned in launch order from a ticket counter, so that the warp of
+// boundary j-1 of the same group always started earlier.  It computes
+// carry_j, the state entering chunk j, from the tokens of chunk j-1, walking
+// that chunk's pieces backwards, each scanned forward from zero: with hloc_q
+// and S_q the end state and dt sum of piece q, and W_q = 2^(A2 * (sum of S
+// over the pieces after q)) the decay from the end of piece q to the boundary,
+//   carry_j = sum_q W_q hloc_q + W_start carry_{j-1}      (per state)
+// where W_start is the decay over the whole chunk.  The walk stops early once
+// every state of every lane has decayed below 2^-32 from the start of the
+// current piece to the boundary: the terms left out (earlier pieces and
+// carry_{j-1}) then enter with weights below 2^-32 and are dropped.
+// Otherwise, after the chunk's first piece, the warp waits (bounded) for
+// carry_{j-1}, published by boundary j-1's warp, and folds it in.  Fast
+// decay, the common case, costs a few pieces per boundary; no decay at all
+// costs one pass over the earlier chunks and a chain of waits, no more than a
+// full two-pass scan.
+constexpr float kCarryDropLog2 = -32.0f;
+
+template <typename IO>
+struct CarrySmem {
+  SummaryStage<IO> stage[kStages];
+  uint64_t full[kStages];
+  unsigned ticket;
+};
+
+// Tiles of chunk jc's pieces in walk order (last piece first, each forward):
+// piece q covers chunk tiles [q*P, min((q+1)*P, C)).
+struct PieceWalk {
+  int first_tile;  // chunk's first tile
+  int C, P, m;     // chunk tiles, piece tiles, pieces
+  int len_last;    // tiles of the last piece
+  __device__ __forceinline__ int piece_of(int i) const {
+    return i < len_last ? m - 1 : m - 2 - (i - len_last) / P;
+  }
+  __device__ __forceinline__ int tile_of(int i) const {
+    if (i < len_last) return first_tile + (m - 1) * P + i;
+    const int r = i - len_last;
+    return first_tile + (m - 2 - r / P) * P + r % P;
+  }
+  __device__ __forceinline__ int piece_len(int q) const { return q == m - 1 ? len_last : P; }
+};
+
+template <typename IO>
+__device__ __forceinline__ void issue_carry_tile(CarrySmem<IO>& sm, int s, const CUtensorMap* tx,
+                                                 const CUtensorMap* tdt, const CUtensorMap* tbc, int c0, int tile,
+                                                 int b) {
+  constexpr uint32_t kBytes = 2 * kT * kLanes * sizeof(IO) + kT * kBC * sizeof(float);
+  const uint32_t bar = smem_u32(&sm.full[s]);
+  const int tt = tile * kT;
+  mbar_arrive_expect_tx(bar, kBytes);
+  tma_load_3d(smem_u32(&sm.stage[s].x[0][0]), tx, c0, tt, b, bar);
+  tma_load_3d(smem_u32(&sm.stage[s].dt[0][0]), tdt, c0, tt, b, bar);
+  tma_load_3d(smem_u32(&sm.stage[s].bc[0][0]), tbc, 0, tt, b, bar);
+}
+
+// grid ((n_chunks - 1) * n_groups * batch), 32 threads.
 template <typename IO>
 __global__ void __launch_bounds__(kLanes)
-    scan_piece_summary_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dt,
-                              const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ ScanParams p) {
+    scan_carry_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dt,
+                      const __grid_constant__ CUtensorMap tm_bc, const __grid_constant__ ScanParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  SummarySmem<IO>& sm = *reinterpret_cast<SummarySmem<IO>*>(smem_raw + smem_pad128(smem_raw));
+  CarrySmem<IO>& sm = *reinterpret_cast<CarrySmem<IO>*>(smem_raw + smem_pad128(smem_raw));
 
   const int lane = threadIdx.x;
-  const int c0 = blockIdx.x * kLanes;
-  const int b = blockIdx.y;
-  const int piece = blockIdx.z;  // 0 .. (n_chunks-1)*pieces - 1
-  const int jc = piece / p.pieces;
-  const int q = piece - jc * p.pieces;
-  const int D = p.d_inner;
-  const int c = c0 + lane;
-  const bool active = c < D;
-  const int cl = active ? c : D - 1;
-  const int tile0 = jc * p.chunk_tiles + q * p.piece_tiles;
-  const int tile1 = min(tile0 + p.piece_tiles, (jc + 1) * p.chunk_tiles);
-  const int t_begin = tile0 * kT;
-  const int n_tiles = tile1 - tile0;  // >= 1: chunks before the last are full
-
   if (lane == 0) {
+    sm.ticket = atomicAdd(p.counters, 1u);
     for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&sm.full[s]), 1);
     fence_mbar_init();
     prefetch_tensormap(&tm_x);
     prefetch_tensormap(&tm_dt);
-    prefetch_tensormap(&tm_b);
+    prefetch_tensormap(&tm_bc);
   }
   __syncwarp();
-  constexpr uint32_t kBytes = 2 * kT * kLanes * sizeof(IO) + kT * kN * sizeof(float);
-  if (lane == 0) {
-    for (int k = 0; k < kStages && k < n_tiles; ++k) {
-      const uint32_t bar = smem_u32(&sm.full[k]);
-      const int tt = t_begin + k * kT;
-      mbar_arrive_expect_tx(bar, kBytes);
-      tma_load_3d(smem_u32(&sm.stage[k].x[0][0]), &tm_x, c0, tt, b, bar);
-      tma_load_3d(smem_u32(&sm.stage[k].dt[0][0]), &tm_dt, c0, tt, b, bar);
-      tma_load_3d(smem_u32(&sm.stage[k].b[0][0]), &tm_b, 0, tt, b, bar);
-    }
-  }
+  const int per = p.n_chunks - 1;
+  const unsigned ticket = sm.ticket;
+  const int j = (int)(ticket % per) + 1;  // boundary: carry into chunk j
+  const int gb = (int)(ticket / per);
+  const int g = gb % p.n_groups;
+  const int b = gb / p.n_groups;
+  const int D = p.d_inner;
+  const int c0 = g * kLanes;
+  const int c = c0 + lane;
+  const bool active = c < D;
+  const int cl = active ? c : D - 1;
+  unsigned* ready = p.counters + 1 + (size_t)b * p.n_groups * p.n_chunks + (size_t)g * p.n_chunks;
+
+  PieceWalk wk;
+  wk.first_tile = (j - 1) * p.chunk_tiles;
+  wk.C = p.chunk_tiles;
+  wk.P = p.piece_tiles;
+  wk.m = p.pieces;
+  wk.len_last = p.chunk_tiles - (p.pieces - 1) * p.piece_tiles;
+  const int n_tiles = wk.C;
+
+  if (lane == 0)
+    for (int k = 0; k < kStages && k < n_tiles; ++k)
+      issue_carry_tile<IO>(sm, k, &tm_x, &tm_dt, &tm_bc, c0, wk.tile_of(k), b);
 
   Channel ch;
   load_channel(ch, p.A_log, p.conv_w, p.conv_b, p.Dskip, cl);
-  State16 st;
-  state16_zero(st);
-  float sdt = 0.0f;
-  float xm3 = input_at<IO>(p, b, (long)t_begin - 3, cl);
-  float xm2 = input_at<IO>(p, b, (long)t_begin - 2, cl);
-  float xm1 = input_at<IO>(p, b, (long)t_begin - 1, cl);
+  float a2max = ch.a2[0].x;  // the slowest decay of this channel
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a2max = fmaxf(a2max, fmaxf(ch.a2[k].x, ch.a2[k].y));
+  State16 acc, wgt, st;
+  state16_zero(acc);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) wgt.h[k] = make_float2(1.0f, 1.0f);
+  float s_after = 0.0f;  // dt summed from the current piece's end to the boundary
 
-  bool ok = true;
+  bool ok = true, done = false;
   int k = 0;
+  int q = wk.piece_of(0);
+  int left = wk.piece_len(q);  // tiles left in the current piece
+  float sdt = 0.0f, xm3 = 0.0f, xm2 = 0.0f, xm1 = 0.0f;
+  state16_zero(st);
+  {
+    const long t0 = (long)wk.tile_of(0) * kT;
+    xm3 = input_at<IO>(p, b, t0 - 3, cl);
+    xm2 = input_at<IO>(p, b, t0 - 2, cl);
+    xm1 = input_at<IO>(p, b, t0 - 1, cl);
+  }
   for (; k < n_tiles; ++k) {
     const int s = k % kStages;
     const SummaryStage<IO>& S = sm.stage[s];
@@ -360,65 +430,81 @@ __global__ void __launch_bounds__(kLanes)
     else
       summary_tile<IO, false>(S, lane, ch, st, sdt, xm3, xm2, xm1);
     __syncwarp();
-    if (lane == 0 && k + kStages < n_tiles) {
-      const uint32_t bar = smem_u32(&sm.full[s]);
-      const int tt = t_begin + (k + kStages) * kT;
-      mbar_arrive_expect_tx(bar, kBytes);
-      tma_load_3d(smem_u32(&sm.stage[s].x[0][0]), &tm_x, c0, tt, b, bar);
-      tma_load_3d(smem_u32(&sm.stage[s].dt[0][0]), &tm_dt, c0, tt, b, bar);
-      tma_load_3d(smem_u32(&sm.stage[s].b[0][0]), &tm_b, 0, tt, b, bar);
-    }
-  }
-  if (!ok) {
-    if (lane == 0) {
-      report_error(4u);
-      drain_ring(sm.full, k, n_tiles, p.timeout_ns);
-    }
-    return;
-  }
-
-  // ---- publish this piece's summary
-  const int npieces = (p.n_chunks - 1) * p.pieces;
-  const size_t o = ((size_t)b * npieces + piece) * D + cl;
-  if (active) {
-    state16_store(st, p.hloc + o * kN);
-    p.sum_dt[o] = sdt;
-  }
-  __threadfence();
-  __syncwarp();
-  if (lane == 0) {
-    unsigned* cnt = p.counters + (size_t)b * p.n_groups + blockIdx.x;
-    const unsigned prev = atomicAdd(cnt, 1u);
-    sm.last = (prev == (unsigned)(npieces - 1));
-    if (sm.last) *cnt = 0u;  // every piece of this group has arrived: reset for the next call
-  }
-  __syncwarp();
-  if (!sm.last) return;
-  __threadfence();
-
-  // ---- fold in piece order; the carry at the end of chunk jc is chunk jc+1's start
-  if (!active) return;
-  State16 h;
-  if (p.h0)
-    state16_load(h, p.h0 + ((size_t)b * D + c) * kN);
-  else
-    state16_zero(h);
-  for (int pc = 0; pc < npieces; ++pc) {
-    const size_t oo = ((size_t)b * npieces + pc) * D + c;
-    State16 hl;
-    const float4* src = reinterpret_cast<const float4*>(p.hloc + oo * kN);
+    if (lane == 0 && k + kStages < n_tiles)
+      issue_carry_tile<IO>(sm, s, &tm_x, &tm_dt, &tm_bc, c0, wk.tile_of(k + kStages), b);
+    if (--left == 0) {  // piece q done: acc += wgt hloc_q, then wgt decays over piece q
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const float4 v = __ldcg(src + kk);
-      hl.h[2 * kk] = make_float2(v.x, v.y);
-      hl.h[2 * kk + 1] = make_float2(v.z, v.w);
-    }
-    state16_fold(h, ch.a2, __ldcg(p.sum_dt + oo), hl);
-    if ((pc + 1) % p.pieces == 0) {
-      const int jn = (pc + 1) / p.pieces;  // the chunk this carry starts
-      state16_store(h, p.carry + (((size_t)b * p.n_chunks + jn) * D + c) * kN);
+      for (int kk = 0; kk < 8; ++kk) acc.h[kk] = __ffma2_rn(wgt.h[kk], st.h[kk], acc.h[kk]);
+      State16 zero;
+      state16_zero(zero);
+      state16_fold(wgt, ch.a2, sdt, zero);
+      s_after = __fadd_rn(s_after, sdt);
+      if (__all_sync(0xffffffffu, !active || __fmul_rn(a2max, s_after) < kCarryDropLog2)) {
+        done = true;
+        ++k;
+        break;
+      }
+      if (k + 1 < n_tiles) {  // next (earlier) piece: restart from zero
+        q = wk.piece_of(k + 1);
+        left = wk.piece_len(q);
+        state16_zero(st);
+        sdt = 0.0f;
+        const long t0 = (long)wk.tile_of(k + 1) * kT;
+        xm3 = input_at<IO>(p, b, t0 - 3, cl);
+        xm2 = input_at<IO>(p, b, t0 - 2, cl);
+        xm1 = input_at<IO>(p, b, t0 - 1, cl);
+      }
     }
   }
+  if (lane == 0) {  // copies still in flight land before shared memory goes away
+    for (int kk = k; kk < n_tiles && kk < k + kStages; ++kk)
+      (void)mbar_wait_bounded(smem_u32(&sm.full[kk % kStages]), (kk / kStages) & 1, p.timeout_ns);
+  }
+  if (!ok && lane == 0) report_error(4u);  // MAMBA_ERR_TIMEOUT
+
+  if (ok && !done) {  // the whole chunk matters: fold in the carry entering it
+    State16 prev;
+    bool have = true;
+    if (j - 1 == 0) {
+      if (p.h0)
+        state16_load(prev, p.h0 + ((size_t)b * D + cl) * kN);
+      else
+        state16_zero(prev);
+    } else {
+      if (lane == 0) {
+        const uint64_t t_start = globaltimer_ns();
+        while (atomicAdd(ready + (j - 1), 0u) == 0u) {
+          if (globaltimer_ns() - t_start > p.timeout_ns) {
+            have = false;
+            break;
+          }
+        }
+      }
+      have = __shfl_sync(0xffffffffu, have, 0);
+      __threadfence();
+      if (!have) {
+        if (lane == 0) report_error(4u);
+        state16_zero(prev);
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(
+            p.carry + (((size_t)b * p.n_chunks + (j - 1)) * D + cl) * kN);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float4 v = __ldcg(src + kk);
+          prev.h[2 * kk] = make_float2(v.x, v.y);
+          prev.h[2 * kk + 1] = make_float2(v.z, v.w);
+        }
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) acc.h[kk] = __ffma2_rn(wgt.h[kk], prev.h[kk], acc.h[kk]);
+  }
+
+  // publish carry_j (also after a failure, so that no later boundary waits in vain)
+  if (active) state16_store(acc, p.carry + (((size_t)b * p.n_chunks + j) * D + c) * kN);
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) atomicExch(ready + j, 1u);
 }
 
 }  // namespace mamba

@@ -12,11 +12,11 @@
 //   y   = (sum_n C_n h_n + D u) * silu(z)
 // The prefill kernels keep all 16 states of a channel in one lane, as 8
 // float2 pairs (h[k] = states 2k, 2k+1) advanced with packed f32x2
-// arithmetic; the decode kernel splits them over 2 or 4 lanes.  The read-out
-// sum is fixed so that every layout produces the same bits: for each group
-// q of 4 states, p = (C_4q h_4q, C_4q+1 h_4q+1) + (C_4q+2 h_4q+2,
-// C_4q+3 h_4q+3) (one packed multiply, one packed fma) and g_q = p.x + p.y;
-// then sum_n C_n h_n = (g_0 + g_1) + (g_2 + g_3).
+// arithmetic; other kernels split them over 2 or 8 lanes.  The read-out sum
+// is fixed so that every layout produces the same bits: with the packed
+// products s_k = (C_2k h_2k, C_2k+1 h_2k+1) of the 8 pairs,
+//   T_lo = (s0 + s2) + (s1 + s3),  T_hi = (s4 + s6) + (s5 + s7)  (packed adds)
+//   v = T_lo + T_hi,  sum_n C_n h_n = v.x + v.y.
 #pragma once
 #include <cuda_bf16.h>
 
@@ -52,7 +52,7 @@ __device__ __forceinline__ float silu(float v) {
 // Two regions of e = e^v:
 //   e < 1/8:  log1p(e) = e * P(e), P a degree-5 polynomial fitted to
 //             log1p(e)/e on [0, 1/8] by least squares (fit_log1p.py; max
-//             relative error 9e-8 evaluated in fp32).  This keeps full
+//             relative error 1.2e-7 evaluated in fp32).  This keeps full
 //             relative accuracy for the small dt of the layer, where
 //             log2(1 + e) would lose it, and needs no reciprocal.
 //   e >= 1/8: log2(1 + e) ln 2, with 1 + e >= 1.125, where the approximate
@@ -63,12 +63,14 @@ __device__ __forceinline__ float silu(float v) {
 // directly -- the formula softplus() selects there, hence the same bits.
 __device__ __forceinline__ float softplus_e(float v) { return ex2_approx(__fmul_rn(v, kLog2e)); }
 
+// P evaluated in Estrin's scheme (depth 4 instead of Horner's 6):
+// P = (1 + a1 e) + e^2 ((a2 + a3 e) + e^2 (a4 + a5 e)).
 __device__ __forceinline__ float softplus_small(float e) {
-  float p = __fmaf_rn(e, -0.12255968898534775f, 0.19420583546161652f);
-  p = __fmaf_rn(e, p, -0.24963703751564026f);
-  p = __fmaf_rn(e, p, 0.3333229124546051f);
-  p = __fmaf_rn(e, p, -0.49999988079071045f);
-  p = __fmaf_rn(e, p, 1.0f);
+  const float e2 = __fmul_rn(e, e);
+  const float q0 = __fmaf_rn(e, -0.49999988079071045f, 1.0f);
+  const float q1 = __fmaf_rn(e, -0.24963703751564026f, 0.3333229124546051f);
+  const float q2 = __fmaf_rn(e, -0.12255968898534775f, 0.19420583546161652f);
+  const float p = __fmaf_rn(__fmaf_rn(q2, e2, q1), e2, q0);
   return __fmul_rn(e, p);
 }
 
@@ -180,6 +182,20 @@ __device__ __forceinline__ void drive16(Drive16& d, const float2 (&a2)[8], float
   }
 }
 
+// The same from widened B/C rows in pair-quad layout: Q[k] = (B_2k, B_2k+1,
+// C_2k, C_2k+1); only the B halves are used here.
+__device__ __forceinline__ void drive16_q(Drive16& d, const float2 (&a2)[8], float dt, float dtu,
+                                          const float4 (&Q)[8]) {
+  const float2 d2 = make_float2(dt, dt);
+  const float2 u2 = make_float2(dtu, dtu);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float2 x = __fmul2_rn(d2, a2[k]);
+    d.dA[k] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    d.bu[k] = __fmul2_rn(u2, make_float2(Q[k].x, Q[k].y));
+  }
+}
+
 // The state-dependent half: h <- dA h + bu.
 __device__ __forceinline__ void state16_apply(State16& s, const Drive16& d) {
 #pragma unroll
@@ -195,20 +211,38 @@ __device__ __forceinline__ void state16_advance(State16& s, const float2 (&a2)[8
   state16_apply(s, d);
 }
 
-// g of one group of 4 states: h0, h1 the group's two pairs, C its 4 values.
-__device__ __forceinline__ float readout4(float2 h0, float2 h1, float4 C) {
-  float2 p = __fmul2_rn(make_float2(C.x, C.y), h0);
-  p = __ffma2_rn(make_float2(C.z, C.w), h1, p);
-  return __fadd_rn(p.x, p.y);
+// Half of the read-out: the 8 states of pairs h[0..3] (C values C[0..1]),
+// T = (s0 + s2) + (s1 + s3) with s_k = C_pair_k * h_pair_k (packed).
+__device__ __forceinline__ float2 readout_half(const float2* h, const float4* C) {
+  const float2 s0 = __fmul2_rn(make_float2(C[0].x, C[0].y), h[0]);
+  const float2 s1 = __fmul2_rn(make_float2(C[0].z, C[0].w), h[1]);
+  const float2 s2 = __fmul2_rn(make_float2(C[1].x, C[1].y), h[2]);
+  const float2 s3 = __fmul2_rn(make_float2(C[1].z, C[1].w), h[3]);
+  return __fadd2_rn(__fadd2_rn(s0, s2), __fadd2_rn(s1, s3));
+}
+
+// The two halves combined: v = T_lo + T_hi, sum_n C_n h_n = v.x + v.y.
+__device__ __forceinline__ float readout_join(float2 lo, float2 hi) {
+  const float2 v = __fadd2_rn(lo, hi);
+  return __fadd_rn(v.x, v.y);
 }
 
 // sum_n C_n h_n in the fixed order described at the top of the file.
 __device__ __forceinline__ float state16_readout(const State16& s, const float4 (&C)[4]) {
-  const float g0 = readout4(s.h[0], s.h[1], C[0]);
-  const float g1 = readout4(s.h[2], s.h[3], C[1]);
-  const float g2 = readout4(s.h[4], s.h[5], C[2]);
-  const float g3 = readout4(s.h[6], s.h[7], C[3]);
-  return __fadd_rn(__fadd_rn(g0, g1), __fadd_rn(g2, g3));
+  return readout_join(readout_half(&s.h[0], &C[0]), readout_half(&s.h[4], &C[2]));
+}
+
+// The same with C taken from pair quads (the C halves of Q[k]).
+__device__ __forceinline__ float2 readout_half_q(const float2* h, const float4* Q) {
+  const float2 s0 = __fmul2_rn(make_float2(Q[0].z, Q[0].w), h[0]);
+  const float2 s1 = __fmul2_rn(make_float2(Q[1].z, Q[1].w), h[1]);
+  const float2 s2 = __fmul2_rn(make_float2(Q[2].z, Q[2].w), h[2]);
+  const float2 s3 = __fmul2_rn(make_float2(Q[3].z, Q[3].w), h[3]);
+  return __fadd2_rn(__fadd2_rn(s0, s2), __fadd2_rn(s1, s3));
+}
+
+__device__ __forceinline__ float state16_readout_q(const State16& s, const float4 (&Q)[8]) {
+  return readout_join(readout_half_q(&s.h[0], &Q[0]), readout_half_q(&s.h[4], &Q[4]));
 }
 
 // Carry fold: h <- 2^(A2 S) h + hl, S the summed dt of a span of tokens and

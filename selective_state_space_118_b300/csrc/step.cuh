@@ -1,15 +1,15 @@
 // step.cuh -- decode: one token through the layer, state updated in place.
 //
 // The constant-memory recurrence of the lesson's "Um SSM em uma pagina":
-// y_t needs only h_{t-1}, the last three inputs and x_t.  kLPC lanes (2 or 4)
-// serve one (batch row, channel), lane q holding states 16/kLPC * q onwards,
-// each reading and writing its part of h with one 32- or 16-byte access, so
-// that a warp instruction moves a contiguous 1 KB or 512 B of h (a
-// lane-per-channel layout touches 16 cache lines per instruction and
-// throttles the load/store unit).  The lanes of a channel all compute its
+// y_t needs only h_{t-1}, the last three inputs and x_t.  Two lanes serve one
+// (batch row, channel), lane q holding states 8q..8q+7, each reading and
+// writing its half of h with one 32-byte access, so that a warp instruction
+// moves a contiguous 1 KB of h (a lane-per-channel layout touches 16 cache
+// lines per instruction and throttles the load/store unit; four lanes per
+// channel issue more instructions and measured slower).  The lanes of a channel all compute its
 // conv, SiLU, softplus and gate (cheap: the step is HBM-bound, not
-// arithmetic-bound); their read-out groups meet through shuffles in the
-// fixed order of state16_readout.  The arithmetic is ssm_math.cuh's, in the
+// arithmetic-bound); their read-out halves (T_lo on lane 0, T_hi on lane 1)
+// meet through one exchange in the fixed order of state16_readout.  The arithmetic is ssm_math.cuh's, in the
 // same order as one token of scan_fwd_kernel, so a sequence of steps
 // reproduces a single-pass scan bit for bit.  h is 128 of the ~144 bytes
 // moved per channel and row; many small threads (one row each) keep more
@@ -24,10 +24,9 @@
 namespace mamba {
 
 constexpr int kStepThreads = 128;
-constexpr int kLPC = 2;                       // lanes per (row, channel): 2 or 4
-constexpr int kLS = kN / kLPC;                // states per lane: 8 or 4
+constexpr int kLPC = 2;                       // lanes per (row, channel)
+constexpr int kLS = kN / kLPC;                // states per lane: 8
 constexpr int kStepChannels = kStepThreads / kLPC;
-static_assert(kLPC == 2 || kLPC == 4, "2 or 4 lanes per channel");
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -71,13 +70,6 @@ __device__ __forceinline__ void load_part(const __nv_bfloat16* p, float4 (&v)[kL
   }
 }
 
-// (mine + other) for the lower lane of an exchanged pair, (other + mine) for
-// the upper: both lanes get the same bits, in the order lower + upper.
-__device__ __forceinline__ float pair_sum(float mine, int lane_bit, int upper) {
-  const float other = __shfl_xor_sync(0xffffffffu, mine, lane_bit);
-  return upper ? __fadd_rn(other, mine) : __fadd_rn(mine, other);
-}
-
 // grid (ceil(D / kStepChannels), batch), kStepThreads threads: kLPC
 // consecutive threads = one channel of one batch row.
 template <typename IO>
@@ -113,7 +105,7 @@ __global__ void __launch_bounds__(kStepThreads) step_kernel(const __grid_constan
   const float2 d2 = make_float2(dt, dt);
   const float dtu = __fmul_rn(dt, u);
   const float2 u2 = make_float2(dtu, dtu);
-  float g[kLS / 4];
+  float2 hp[kLS / 2];
 #pragma unroll
   for (int k = 0; k < kLS / 4; ++k) {  // one group of 4 states: pairs h01, h23
     const float2 a01 = make_float2(a2_from_log(al[k].x), a2_from_log(al[k].y));
@@ -125,15 +117,13 @@ __global__ void __launch_bounds__(kStepThreads) step_kernel(const __grid_constan
     h01 = __ffma2_rn(e01, h01, __fmul2_rn(u2, make_float2(Bv[k].x, Bv[k].y)));
     h23 = __ffma2_rn(e23, h23, __fmul2_rn(u2, make_float2(Bv[k].z, Bv[k].w)));
     hv[k] = make_float4(h01.x, h01.y, h23.x, h23.y);
-    g[k] = readout4(h01, h23, Cv[k]);
+    hp[2 * k] = h01;
+    hp[2 * k + 1] = h23;
   }
-  // (g0 + g1) + (g2 + g3) over the channel's lanes
-  float ss;
-  if constexpr (kLPC == 2) {
-    ss = pair_sum(__fadd_rn(g[0], g[1]), 1, q);
-  } else {
-    ss = pair_sum(pair_sum(g[0], 1, q & 1), 2, q >> 1);
-  }
+  // this lane's half of the read-out, then T_lo + T_hi
+  const float2 pr = readout_half(hp, Cv);
+  const float2 po = make_float2(__shfl_xor_sync(0xffffffffu, pr.x, 1), __shfl_xor_sync(0xffffffffu, pr.y, 1));
+  const float ss = q == 0 ? readout_join(pr, po) : readout_join(po, pr);
   if (valid) {
     store_h(p.h + ch * kN + kLS * q, hv);
     if (q == 0) {

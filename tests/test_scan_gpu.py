@@ -150,3 +150,36 @@ def test_rejects_bad_arguments_on_device():
     with pytest.raises(ops.MambaError) as e:
         run_gpu(inp, n_chunks=4, workspace=torch.empty(256, dtype=torch.uint8, device="cuda"))
     assert e.value.status == ops.MAMBA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("case", ["fast_decay", "slow_decay", "mixed", "very_slow_bf16"])
+def test_chunk_carries_against_oracle(case):
+    """The chunk-carry walk: with fast decay it stops after a few pieces (the
+    carried state from far back is below 2^-32 of its size); with slow decay
+    it must chain every boundary onto the previous one; a warp mixing both
+    follows its slowest channel.  Each case is checked against the oracle and
+    against the GPU's own one-pass scan (same fp32 arithmetic but for the
+    carry sums).  A very slow leak (A = -0.0025, ~1/20000 per token) is
+    checked in bf16: there the fp32 rounding of dA = 2^(dt A2) near 1 alone
+    misstates the leak rate by ~0.1 %, beyond the fp32-I/O bound for any fp32
+    recurrence, one pass included."""
+    B, L, D = 1, 8192, 64
+    io = "bf16" if case == "very_slow_bf16" else "f32"
+    inp = inputs.scan_inputs(B, L, D, io, seed=23, device="cuda", with_state=True)
+    if case == "slow_decay":
+        inp["A_log"] = torch.full_like(inp["A_log"], -1.5)  # A = -0.22: no 2^-32 decay within a chunk
+    elif case == "mixed":
+        inp["A_log"][5] = -1.5
+        inp["A_log"][40, :4] = -1.0
+    elif case == "very_slow_bf16":
+        inp["A_log"] = torch.full_like(inp["A_log"], -6.0)
+    plan = ops.mamba_scan_plan(B, L, D, 4)
+    assert plan["n_chunks"] == 4 and plan["pieces"] > 1
+    outs = [t.clone() for t in run_gpu(inp, n_chunks=4)]
+    check_against_oracle(inp, outs, f"carries {case}")
+    y1, fh1, fcs1 = run_gpu(inp, n_chunks=1)
+    torch.cuda.synchronize()
+    if io == "f32":  # bf16 outputs of the two may round one ulp apart
+        assert_close(outs[0], oracle_like(y1), "f32", f"{case}: chunked vs one pass, y")
+    assert_close(outs[1], oracle_like(fh1), "f32", f"{case}: chunked vs one pass, h", fp32_output=True)
+    assert torch.equal(outs[2], fcs1)
