@@ -121,8 +121,13 @@ Plan make_plan(int batch, int seqlen, int d_inner, int n_chunks_req) {
     const int n_eff = (tiles + C - 1) / C;
     const int P = C < kPieceTiles ? C : kPieceTiles;
     const int m = (C + P - 1) / P;
-    const int walk = C < kCarryTilesEstimate ? C : kCarryTilesEstimate;
-    const double t_carry = n_eff > 1 ? pass_time(groups * (n_eff - 1), walk, 0.7, mc.sms, mc.summary_per_sm) : 0.0;
+    // Chunks shorter than the expected walk make every boundary wait for the
+    // previous one: the carries of a group then form one serial chain.
+    double t_carry = 0.0;
+    if (n_eff > 1)
+      t_carry = C >= kCarryTilesEstimate
+                    ? pass_time(groups * (n_eff - 1), kCarryTilesEstimate, 0.7, mc.sms, mc.summary_per_sm)
+                    : pass_time(groups, (n_eff - 1) * C, 0.7, mc.sms, mc.summary_per_sm);
     const double t = pass_time(groups * n_eff, C, 1.0, mc.sms, mc.main_per_sm) + t_carry;
     if (best < 0.0 || t < best - 1e-9) {
       best = t;
