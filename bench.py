@@ -47,14 +47,21 @@ def peaks():
 
 
 # ---------------------------------------------------------------- distributed
-def dist_setup(n_gpus: int):
+# The scan has no cross-device exchange: N ranks run N independent replicas
+# (one per GPU); only the timing is combined (a barrier on both sides of the
+# timed region and the maximum time over ranks).
+def dist_setup(n_gpus: int, backend: str | None = None):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        backend = backend or ("nccl" if torch.cuda.is_available() else "gloo")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
     else:
         torch.cuda.set_device(0) if torch.cuda.is_available() else None
     return world, rank, local
@@ -70,9 +77,15 @@ def max_over_ranks(v: float, world: int) -> float:
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], device="cuda", dtype=torch.float64)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], device=dev, dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(units_per_rank_step: int, steps: int, world: int, t_max_ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed / the slowest rank's time."""
+    return units_per_rank_step * steps * world / (t_max_ms / 1e3)
 
 
 # ---------------------------------------------------------------- clocks
@@ -474,8 +487,7 @@ def main():
         return
     w = workload_of(args)
     res, inp, out, ws = bench_prefill(w, args.steps, args.warmup, world, local, args.n_chunks)
-    elems_all = res["elems"] * args.steps * world
-    value = elems_all / (res["t_ms"] / 1e3)
+    value = job_value(res["elems"], args.steps, world, res["t_ms"])
     hbm, src = peaks()
     achieved = res["alg_bytes"] / (res["per_launch_ms"] / 1e3) / 1e9
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

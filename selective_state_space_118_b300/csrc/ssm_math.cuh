@@ -12,11 +12,11 @@
 //   y   = (sum_n C_n h_n + D u) * silu(z)
 // The prefill kernels keep all 16 states of a channel in one lane, as 8
 // float2 pairs (h[k] = states 2k, 2k+1) advanced with packed f32x2
-// arithmetic; other kernels split them over 2 or 8 lanes.  The read-out sum
-// is fixed so that every layout produces the same bits: with the packed
-// products s_k = (C_2k h_2k, C_2k+1 h_2k+1) of the 8 pairs,
-//   T_lo = (s0 + s2) + (s1 + s3),  T_hi = (s4 + s6) + (s5 + s7)  (packed adds)
-//   v = T_lo + T_hi,  sum_n C_n h_n = v.x + v.y.
+// arithmetic; the decode kernel splits them over two lanes.  The read-out
+// sum is fixed so that both layouts produce the same bits: two packed
+// accumulation chains, p_lo over the pairs of states 0-7 and p_hi over those
+// of states 8-15 (each one packed multiply, then three packed fmas in pair
+// order), v = p_lo + p_hi (packed), and sum_n C_n h_n = v.x + v.y.
 #pragma once
 #include <cuda_bf16.h>
 
@@ -211,17 +211,16 @@ __device__ __forceinline__ void state16_advance(State16& s, const float2 (&a2)[8
   state16_apply(s, d);
 }
 
-// Half of the read-out: the 8 states of pairs h[0..3] (C values C[0..1]),
-// T = (s0 + s2) + (s1 + s3) with s_k = C_pair_k * h_pair_k (packed).
+// Half of the read-out: the 8 states of pairs h[0..3] (C values C[0..1]) as
+// one packed chain, p = C01 h01; p += C23 h23; p += C45 h45; p += C67 h67.
 __device__ __forceinline__ float2 readout_half(const float2* h, const float4* C) {
-  const float2 s0 = __fmul2_rn(make_float2(C[0].x, C[0].y), h[0]);
-  const float2 s1 = __fmul2_rn(make_float2(C[0].z, C[0].w), h[1]);
-  const float2 s2 = __fmul2_rn(make_float2(C[1].x, C[1].y), h[2]);
-  const float2 s3 = __fmul2_rn(make_float2(C[1].z, C[1].w), h[3]);
-  return __fadd2_rn(__fadd2_rn(s0, s2), __fadd2_rn(s1, s3));
+  float2 p = __fmul2_rn(make_float2(C[0].x, C[0].y), h[0]);
+  p = __ffma2_rn(make_float2(C[0].z, C[0].w), h[1], p);
+  p = __ffma2_rn(make_float2(C[1].x, C[1].y), h[2], p);
+  return __ffma2_rn(make_float2(C[1].z, C[1].w), h[3], p);
 }
 
-// The two halves combined: v = T_lo + T_hi, sum_n C_n h_n = v.x + v.y.
+// The two halves combined: v = p_lo + p_hi, sum_n C_n h_n = v.x + v.y.
 __device__ __forceinline__ float readout_join(float2 lo, float2 hi) {
   const float2 v = __fadd2_rn(lo, hi);
   return __fadd_rn(v.x, v.y);
@@ -234,11 +233,10 @@ __device__ __forceinline__ float state16_readout(const State16& s, const float4 
 
 // The same with C taken from pair quads (the C halves of Q[k]).
 __device__ __forceinline__ float2 readout_half_q(const float2* h, const float4* Q) {
-  const float2 s0 = __fmul2_rn(make_float2(Q[0].z, Q[0].w), h[0]);
-  const float2 s1 = __fmul2_rn(make_float2(Q[1].z, Q[1].w), h[1]);
-  const float2 s2 = __fmul2_rn(make_float2(Q[2].z, Q[2].w), h[2]);
-  const float2 s3 = __fmul2_rn(make_float2(Q[3].z, Q[3].w), h[3]);
-  return __fadd2_rn(__fadd2_rn(s0, s2), __fadd2_rn(s1, s3));
+  float2 p = __fmul2_rn(make_float2(Q[0].z, Q[0].w), h[0]);
+  p = __ffma2_rn(make_float2(Q[1].z, Q[1].w), h[1], p);
+  p = __ffma2_rn(make_float2(Q[2].z, Q[2].w), h[2], p);
+  return __ffma2_rn(make_float2(Q[3].z, Q[3].w), h[3], p);
 }
 
 __device__ __forceinline__ float state16_readout_q(const State16& s, const float4 (&Q)[8]) {

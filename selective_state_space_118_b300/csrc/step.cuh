@@ -8,7 +8,7 @@
 // lines per instruction and throttles the load/store unit; four lanes per
 // channel issue more instructions and measured slower).  The lanes of a channel all compute its
 // conv, SiLU, softplus and gate (cheap: the step is HBM-bound, not
-// arithmetic-bound); their read-out halves (T_lo on lane 0, T_hi on lane 1)
+// arithmetic-bound); their read-out chains (p_lo on lane 0, p_hi on lane 1)
 // meet through one exchange in the fixed order of state16_readout.  The arithmetic is ssm_math.cuh's, in the
 // same order as one token of scan_fwd_kernel, so a sequence of steps
 // reproduces a single-pass scan bit for bit.  h is 128 of the ~144 bytes
