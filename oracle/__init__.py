@@ -16,6 +16,8 @@ scan(...)          sequential scan over a whole sequence (prefill)
 scan_chunked(...)  the same scan evaluated chunk by chunk with a carried,
                    decayed chunk state (checks the chunked decomposition)
 step(...)          one decode token, state updated in place
+scan_bwd(...)      gradients of sum(y*dy) (+ final-state terms) w.r.t. every
+                   input of scan(...)
 build()            compile ``liboracle.so`` next to this file
 """
 from __future__ import annotations
@@ -58,6 +60,8 @@ def _bind(path: str):
     lib.oracle_scan_chunked_f64.restype = None
     lib.oracle_step_f64.argtypes = [i, i, i, i] + [_P] * 12
     lib.oracle_step_f64.restype = None
+    lib.oracle_scan_bwd_f64.argtypes = [i, i, i, i, i] + [_P] * 25
+    lib.oracle_scan_bwd_f64.restype = None
     return lib
 
 
@@ -171,3 +175,33 @@ def step(h, conv_state, x_t, z_t, dt_raw_t, B_t, C_t, A_log, Dskip, conv_w,
                         _ptr(A_log), _ptr(Dskip), _ptr(conv_w), _ptr(conv_b),
                         _ptr(y))
     return y, h, conv_state
+
+
+BWD_NAMES = ("dx", "dz", "ddt_raw", "dB", "dC", "dA_log", "dD", "dconv_w", "dconv_b", "dh0",
+             "dconv_state0")
+
+
+def scan_bwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=None,
+             conv_state0=None, dy=None, dfinal_h=None, dfinal_conv_state=None, lib=None):
+    """Gradients of loss = sum(y*dy) + sum(final_h*dfinal_h)
+    + sum(final_conv_state*dfinal_conv_state) with respect to every input of
+    scan(...).  Returns a dict keyed by BWD_NAMES (dconv_b is zero when conv_b
+    is None; dh0 and dconv_state0 are returned whether or not h0 / conv_state0
+    were given, as the gradients at those zero defaults)."""
+    lib = _load(lib)
+    x, z, dt_raw, Bm, Cm, dy = map(f64, (x, z, dt_raw, Bm, Cm, dy))
+    A_log, Dskip, conv_w, conv_b, h0, conv_state0 = map(
+        f64, (A_log, Dskip, conv_w, conv_b, h0, conv_state0))
+    dfinal_h, dfinal_conv_state = f64(dfinal_h), f64(dfinal_conv_state)
+    B, L, D = x.shape
+    N = A_log.shape[1]
+    K = conv_w.shape[1]
+    out = {"dx": np.zeros((B, L, D)), "dz": np.zeros((B, L, D)), "ddt_raw": np.zeros((B, L, D)),
+           "dB": np.zeros((B, L, N)), "dC": np.zeros((B, L, N)), "dA_log": np.zeros((D, N)),
+           "dD": np.zeros(D), "dconv_w": np.zeros((D, K)), "dconv_b": np.zeros(D),
+           "dh0": np.zeros((B, D, N)), "dconv_state0": np.zeros((B, max(K - 1, 0), D))}
+    lib.oracle_scan_bwd_f64(B, L, D, N, K, _ptr(x), _ptr(z), _ptr(dt_raw), _ptr(Bm), _ptr(Cm),
+                            _ptr(A_log), _ptr(Dskip), _ptr(conv_w), _ptr(conv_b), _ptr(h0),
+                            _ptr(conv_state0), _ptr(dy), _ptr(dfinal_h), _ptr(dfinal_conv_state),
+                            *[_ptr(out[k]) for k in BWD_NAMES])
+    return out

@@ -261,3 +261,148 @@ void oracle_scan_chunked_f64(int batch, int seqlen, int d_inner, int d_state, in
         }
     free(H); free(h); free(s); free(P);
 }
+
+/* ------------------------------------------------------------------ backward
+ *
+ * Reverse-mode gradient of the scan above (the next step for training; the
+ * pages train the layer end to end, "【大模型】- Jamba 混合 SSM-Transformer",
+ * section "训练" / Jamba.forward's cross-entropy loss, but print no backward:
+ * this is the chain rule applied to the forward definition, written out).
+ * For the scalar
+ *   loss = sum y*dy + sum final_h*dfinal_h + sum final_conv_state*dfinal_conv_state
+ * it returns the gradients with respect to every input.  Per (b, c) row the
+ * forward pass is run first, keeping every state; then t runs backwards with
+ * lam = d loss / d h_t:
+ *   dyss = dy*silu(z);   dz = dy*yss*silu'(z)
+ *   lam += C_t*dyss;     dC_t += dyss*h_t;     du = dyss*D;   dD += dyss*u
+ *   for each n:  g = lam*h_{t-1};  ddt += g*dA*A + lam*B*u;
+ *                dA_log += g*dA*dt*A   (A = -exp(A_log), dA = exp(dt*A));
+ *                dB_t += lam*dt*u;  du += lam*dt*B;  lam *= dA
+ *   ddt_raw = ddt * softplus'(dt_raw)    (sigmoid, or 1 above the threshold)
+ *   dpre = du*silu'(pre);  dconv_b += dpre;  dconv_w[k] += dpre*in(t-K+1+k);
+ *   d in(t-K+1+k) += dpre*w[k]
+ * and at the end dh0 = lam; inputs before t = 0 send their gradient to
+ * dconv_state0.  silu'(v) = s(1 + v(1 - s)), s = sigmoid(v).
+ *
+ * All gradient outputs are overwritten (zeroed first).  dfinal_h and
+ * dfinal_conv_state may be NULL (zero).  Single-threaded: the B and C
+ * gradients sum over channels.
+ */
+static double sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
+
+static double dsilu(double v)
+{
+    double s = sigmoid(v);
+    return s * (1.0 + v * (1.0 - s));
+}
+
+static double dsoftplus(double v) { return v > 20.0 ? 1.0 : sigmoid(v); }
+
+void oracle_scan_bwd_f64(int batch, int seqlen, int d_inner, int d_state, int d_conv,
+                         const double *x, const double *z, const double *dt_raw,
+                         const double *Bm, const double *Cm,
+                         const double *A_log, const double *Dskip,
+                         const double *conv_w, const double *conv_b,
+                         const double *h0, const double *conv_state0,
+                         const double *dy, const double *dfinal_h,
+                         const double *dfinal_conv_state,
+                         double *dx, double *dz, double *ddt_raw,
+                         double *dB, double *dC, double *dA_log, double *dD,
+                         double *dconv_w, double *dconv_b, double *dh0,
+                         double *dconv_state0)
+{
+    int L = seqlen, D = d_inner, N = d_state, K = d_conv, B = batch;
+    size_t nLD = (size_t)B * L * D, nLN = (size_t)B * L * N;
+    memset(dx, 0, nLD * sizeof(double));
+    memset(dz, 0, nLD * sizeof(double));
+    memset(ddt_raw, 0, nLD * sizeof(double));
+    memset(dB, 0, nLN * sizeof(double));
+    memset(dC, 0, nLN * sizeof(double));
+    memset(dA_log, 0, (size_t)D * N * sizeof(double));
+    memset(dD, 0, (size_t)D * sizeof(double));
+    memset(dconv_w, 0, (size_t)D * K * sizeof(double));
+    memset(dconv_b, 0, (size_t)D * sizeof(double));
+    memset(dh0, 0, (size_t)B * D * N * sizeof(double));
+    if (K > 1) memset(dconv_state0, 0, (size_t)B * (K - 1) * D * sizeof(double));
+
+    double *hs = (double *)malloc((size_t)(L + 1) * N * sizeof(double)); /* hs[t+1] = h after t */
+    double *u = (double *)malloc((size_t)(L > 0 ? L : 1) * sizeof(double));
+    double *pre = (double *)malloc((size_t)(L > 0 ? L : 1) * sizeof(double));
+    double *dt = (double *)malloc((size_t)(L > 0 ? L : 1) * sizeof(double));
+    double *yss = (double *)malloc((size_t)(L > 0 ? L : 1) * sizeof(double));
+    double *din = (double *)malloc((size_t)(L + K) * sizeof(double)); /* d in(tau), tau = -(K-1) .. L-1 */
+    double *lam = (double *)malloc((size_t)N * sizeof(double));
+
+    for (int b = 0; b < B; ++b)
+        for (int c = 0; c < D; ++c) {
+            const double *Al = A_log + (size_t)c * N;
+            const double *w = conv_w + (size_t)c * K;
+            double bias = conv_b ? conv_b[c] : 0.0;
+            /* forward, keeping every state */
+            for (int n = 0; n < N; ++n) hs[n] = h0 ? h0[((size_t)b * D + c) * N + n] : 0.0;
+            for (int t = 0; t < L; ++t) {
+                size_t e = ((size_t)b * L + t) * D + c, r = ((size_t)b * L + t) * N;
+                double p = bias;
+                for (int k = 0; k < K; ++k)
+                    p += w[k] * input_at(b, c, (long)t - (K - 1) + k, L, D, K, x, conv_state0);
+                pre[t] = p;
+                u[t] = silu(p);
+                dt[t] = softplus(dt_raw[e]);
+                double acc = 0.0;
+                for (int n = 0; n < N; ++n) {
+                    double A = -exp(Al[n]);
+                    double hn = exp(dt[t] * A) * hs[(size_t)t * N + n] + dt[t] * Bm[r + n] * u[t];
+                    hs[(size_t)(t + 1) * N + n] = hn;
+                    acc += Cm[r + n] * hn;
+                }
+                yss[t] = acc + Dskip[c] * u[t];
+            }
+            /* backward */
+            for (int i = 0; i < L + K; ++i) din[i] = 0.0;
+            if (dfinal_conv_state)
+                for (int k = 0; k < K - 1; ++k)
+                    din[(L - (K - 1) + k) + (K - 1)] +=
+                        dfinal_conv_state[((size_t)b * (K - 1) + k) * D + c];
+            for (int n = 0; n < N; ++n)
+                lam[n] = dfinal_h ? dfinal_h[((size_t)b * D + c) * N + n] : 0.0;
+            for (int t = L - 1; t >= 0; --t) {
+                size_t e = ((size_t)b * L + t) * D + c, r = ((size_t)b * L + t) * N;
+                double g = silu(z[e]);
+                double dyss = dy[e] * g;
+                dz[e] = dy[e] * yss[t] * dsilu(z[e]);
+                double du = dyss * Dskip[c];
+                dD[c] += dyss * u[t];
+                double ddt = 0.0;
+                for (int n = 0; n < N; ++n) {
+                    lam[n] += Cm[r + n] * dyss;
+                    dC[r + n] += dyss * hs[(size_t)(t + 1) * N + n];
+                    double A = -exp(Al[n]);
+                    double dA = exp(dt[t] * A);
+                    double gA = lam[n] * hs[(size_t)t * N + n];
+                    ddt += gA * dA * A + lam[n] * Bm[r + n] * u[t];
+                    dA_log[(size_t)c * N + n] += gA * dA * dt[t] * A;
+                    dB[r + n] += lam[n] * dt[t] * u[t];
+                    du += lam[n] * dt[t] * Bm[r + n];
+                    lam[n] *= dA;
+                }
+                ddt_raw[e] = ddt * dsoftplus(dt_raw[e]);
+                double dpre = du * dsilu(pre[t]);
+                if (conv_b) dconv_b[c] += dpre;
+                for (int k = 0; k < K; ++k) {
+                    long tau = (long)t - (K - 1) + k;
+                    dconv_w[(size_t)c * K + k] +=
+                        dpre * input_at(b, c, tau, L, D, K, x, conv_state0);
+                    din[tau + (K - 1)] += dpre * w[k];
+                }
+            }
+            for (int n = 0; n < N; ++n) dh0[((size_t)b * D + c) * N + n] = lam[n];
+            for (long tau = -(K - 1); tau < L; ++tau) {
+                double v = din[tau + (K - 1)];
+                if (tau >= 0)
+                    dx[((size_t)b * L + (size_t)tau) * D + c] = v;
+                else
+                    dconv_state0[((size_t)b * (K - 1) + (size_t)(tau + (K - 1))) * D + c] = v;
+            }
+        }
+    free(hs); free(u); free(pre); free(dt); free(yss); free(din); free(lam);
+}
