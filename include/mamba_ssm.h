@@ -159,6 +159,78 @@ mamba_status mamba_scan_fwd(const mamba_scan_args *args, void *stream);
 mamba_status mamba_scan_fwd_noalloc(const mamba_scan_args *args, void *stream);
 
 /*
+ * Backward of the prefill: the gradients of a scalar loss l with respect to
+ * every input of mamba_scan_fwd, given dy = dl/dy and optionally
+ * dl/dfinal_h and dl/dfinal_conv_state -- the chain rule through the
+ * recurrence stated at the top of this file (for training the layer of
+ * "实现 > Mamba 层"; the pages train it end to end but print no backward, so
+ * this is the plain reverse-mode derivative of that forward).  The forward
+ * pass is recomputed inside the call (it stores the state entering every
+ * 16-token tile in the workspace); nothing from an earlier forward call is
+ * needed.
+ *
+ *   x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b, h0, conv_state0
+ *                     the forward's inputs, as for mamba_scan_fwd
+ *   dy                (B, L, D) io        dl/dy
+ *   dfinal_h          (B, D, 16) fp32 or NULL     dl/dfinal_h (NULL: zero)
+ *   dfinal_conv_state (B, 3, D) io or NULL        dl/dfinal_conv_state
+ *   dx, dz, ddt_raw   (B, L, D) io        outputs: dl/dx, dl/dz, dl/ddt_raw
+ *   dB, dC            (B, L, 16) fp32     outputs: dl/dBm, dl/dCm (sums over
+ *                                         the D channels, kept in fp32)
+ *   dA_log            (D, 16) fp32        output
+ *   dDskip            (D) fp32            output
+ *   dconv_w           (D, 4) fp32         output
+ *   dconv_b           (D) fp32 or NULL    output (NULL: not written; the
+ *                                         bias may still be given)
+ *   dh0               (B, D, 16) fp32 or NULL     output: dl/dh0 (the
+ *                                         gradient at h0, or at zero)
+ *   dconv_state0      (B, 3, D) fp32 or NULL      output: dl/dconv_state0
+ *   workspace         at least mamba_scan_bwd_workspace_size() bytes,
+ *                     256-byte aligned, contents need not be initialised:
+ *                     the forward's workspace, the tile states (B*L*D*4
+ *                     bytes, rounded up to whole tiles), the per-32-channel
+ *                     sums of dB and dC (B*L*D*4 bytes) and smaller buffers
+ *   n_chunks          as for mamba_scan_fwd (the same plan is used); in
+ *                     chunked mode the adjoint entering each chunk from the
+ *                     right is computed first, the way the forward computes
+ *                     its carries, with time reversed
+ *   wait_timeout_ns   limit of every device-side wait (0: 1 second)
+ *
+ * Every output is overwritten.  Results are deterministic (fixed summation
+ * orders, no atomics).  seqlen may be 0: then dh0 = dfinal_h,
+ * dconv_state0 = dfinal_conv_state (or zeros) and the parameter gradients
+ * are zero.
+ */
+typedef struct mamba_scan_bwd_args {
+    int batch, seqlen, d_inner, d_state, d_conv;
+    mamba_dtype io;
+    const void *x, *z, *dt_raw;
+    const void *Bm, *Cm;
+    const float *A_log, *Dskip, *conv_w, *conv_b;
+    const float *h0;
+    const void *conv_state0;
+    const void *dy;
+    const float *dfinal_h;
+    const void *dfinal_conv_state;
+    void *dx, *dz, *ddt_raw;
+    float *dB, *dC;
+    float *dA_log, *dDskip, *dconv_w, *dconv_b;
+    float *dh0;
+    float *dconv_state0;
+    void *workspace;
+    size_t workspace_bytes;
+    int n_chunks;
+    uint32_t flags;
+    uint64_t wait_timeout_ns;
+} mamba_scan_bwd_args;
+
+/* Bytes of workspace mamba_scan_bwd needs (0 only for invalid sizes or
+ * seqlen 0). */
+size_t mamba_scan_bwd_workspace_size(int batch, int seqlen, int d_inner, int n_chunks);
+
+mamba_status mamba_scan_bwd(const mamba_scan_bwd_args *args, void *stream);
+
+/*
  * Decode: one token through the layer, state updated in place -- the
  * constant-memory recurrence of "Um SSM em uma pagina" (y_t needs only
  * h_{t-1} and x_t).  Bit for bit the same arithmetic as one token of

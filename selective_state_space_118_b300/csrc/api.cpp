@@ -158,6 +158,48 @@ Workspace workspace_layout(int batch, int seqlen, int d_inner, const Plan& pl) {
   return w;
 }
 
+// The backward's workspace: the forward's (at offset 0; the checkpointing
+// forward pass uses it), then the states entering every tile (B, tiles, D,
+// 16), in chunked mode the adjoint carries (B, n_chunks, D, 16) and their
+// counters, the per-group dB | dC sums (groups, B * L, 32), the per-chunk
+// parameter partials (B * n_chunks, D, 24) and, in chunked mode, the edge
+// buffers of the conv (B, n_chunks, 3, D) twice.
+struct BwdWorkspace {
+  Workspace fwd;
+  size_t ckpt, acarry, counters, counters_bytes, part_bc, part_param, edge_dx, edge_dpre, total;
+};
+
+BwdWorkspace bwd_workspace_layout(int batch, int seqlen, int d_inner, const Plan& pl) {
+  BwdWorkspace w;
+  std::memset(&w, 0, sizeof(w));
+  w.fwd = workspace_layout(batch, seqlen, d_inner, pl);
+  const size_t B = batch, L = seqlen, D = d_inner, n = pl.n_chunks;
+  const size_t G = (D + kLanes - 1) / kLanes;
+  const size_t tiles = (L + kT - 1) / kT;
+  size_t o = w.fwd.total;
+  w.ckpt = o;
+  o = round256(o + B * tiles * D * 16 * sizeof(float));
+  if (n > 1) {
+    w.acarry = o;
+    o = round256(o + B * n * D * 16 * sizeof(float));
+    w.counters = o;
+    w.counters_bytes = (1 + B * G * n) * sizeof(unsigned);
+    o = round256(o + w.counters_bytes);
+  }
+  w.part_bc = o;
+  o = round256(o + G * B * L * 32 * sizeof(float));
+  w.part_param = o;
+  o = round256(o + B * n * D * 24 * sizeof(float));
+  if (n > 1) {
+    w.edge_dx = o;
+    o = round256(o + B * n * 3 * D * sizeof(float));
+    w.edge_dpre = o;
+    o = round256(o + B * n * 3 * D * sizeof(float));
+  }
+  w.total = o;
+  return w;
+}
+
 // 3-D tiled map over a (B, L, inner) row-major tensor: box (box_inner, kT, 1).
 bool encode3d(CUtensorMap* m, const void* base, mamba_dtype io, int inner, int L, int B, int box_inner) {
   EncodeTiledFn fn = encode_fn();
@@ -179,6 +221,65 @@ mamba_status check_common(int batch, int d_inner, int d_state, int d_conv, mamba
   if (io != MAMBA_F32 && io != MAMBA_BF16) return MAMBA_ERR_UNSUPPORTED;
   if (d_state != MAMBA_D_STATE || d_conv != MAMBA_D_CONV) return MAMBA_ERR_UNSUPPORTED;
   if (d_inner % 16 != 0) return MAMBA_ERR_UNSUPPORTED;
+  return MAMBA_OK;
+}
+
+// The forward kernels for checked arguments and a workspace of the plan's
+// layout: B/C widening, chunk carries (chunked mode) and the main pass.
+// ckpt (may be null): the state entering every tile is stored there.
+mamba_status launch_forward(const mamba_scan_args* a, const Plan& pl, const Workspace& ws, float* ckpt,
+                            cudaStream_t stream) {
+  const size_t B = a->batch;
+  char* wsp = static_cast<char*>(a->workspace);
+  float* bc = reinterpret_cast<float*>(wsp + ws.bc);
+
+  // x, z, dt_raw, bc (main pass), bc (summary pass)
+  CUtensorMap maps[5];
+  if (!encode3d(&maps[0], a->x, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
+      !encode3d(&maps[1], a->z, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
+      !encode3d(&maps[2], a->dt_raw, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
+      !encode3d(&maps[3], bc, MAMBA_F32, 32, a->seqlen, a->batch, 32) ||
+      !encode3d(&maps[4], bc, MAMBA_F32, 32, a->seqlen, a->batch, 32))
+    return MAMBA_ERR_CUDA;
+
+  mamba::ScanParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.ckpt = ckpt;
+  p.seq_tiles = (a->seqlen + kT - 1) / kT;
+  p.batch = a->batch;
+  p.seqlen = a->seqlen;
+  p.d_inner = a->d_inner;
+  p.n_groups = (a->d_inner + kLanes - 1) / kLanes;
+  p.chunk_tiles = pl.chunk_tiles;
+  p.n_chunks = pl.n_chunks;
+  p.piece_tiles = pl.piece_tiles;
+  p.pieces = pl.pieces;
+  p.A_log = a->A_log;
+  p.Dskip = a->Dskip;
+  p.conv_w = a->conv_w;
+  p.conv_b = a->conv_b;
+  p.h0 = a->h0;
+  p.conv_state0 = a->conv_state0;
+  p.x = a->x;
+  p.y = a->y;
+  p.final_h = a->final_h;
+  p.final_conv_state = a->final_conv_state;
+  p.flags = a->flags;
+  p.timeout_ns = a->wait_timeout_ns ? a->wait_timeout_ns : kDefaultTimeoutNs;
+  const IoType io = a->io == MAMBA_BF16 ? IoType::BF16 : IoType::F32;
+
+  if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, stream) != cudaSuccess)
+    return MAMBA_ERR_CUDA;
+  if (pl.n_chunks > 1) {
+    p.carry = reinterpret_cast<float*>(wsp + ws.carry);
+    p.counters = reinterpret_cast<unsigned*>(wsp + ws.counters);
+    if (cudaMemsetAsync(p.counters, 0, ws.counters_bytes, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+    const CUtensorMap smaps[3] = {maps[0], maps[2], maps[4]};  // x, dt_raw, B/C rows
+    dim3 g1((unsigned)((size_t)(pl.n_chunks - 1) * p.n_groups * B));
+    if (mamba::launch_summary(io, smaps, p, g1, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+  }
+  dim3 g2((unsigned)p.n_groups, (unsigned)B, (unsigned)pl.n_chunks);
+  if (mamba::launch_scan(io, maps, p, g2, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
   return MAMBA_OK;
 }
 
@@ -261,19 +362,102 @@ mamba_status mamba_scan_fwd(const mamba_scan_args* a, void* stream_v) {
 
   if (!a->workspace || a->workspace_bytes < ws.total) return MAMBA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return MAMBA_ERR_INVALID_ARG;
-  char* wsp = static_cast<char*>(a->workspace);
-  float* bc = reinterpret_cast<float*>(wsp + ws.bc);
+  return launch_forward(a, pl, ws, nullptr, stream);
+}
 
-  // x, z, dt_raw, bc (main pass), bc (summary pass)
-  CUtensorMap maps[5];
+size_t mamba_scan_bwd_workspace_size(int batch, int seqlen, int d_inner, int n_chunks) {
+  if (batch <= 0 || seqlen <= 0 || d_inner <= 0 || d_inner % 16 || n_chunks < 0) return 0;
+  return bwd_workspace_layout(batch, seqlen, d_inner, make_plan(batch, seqlen, d_inner, n_chunks)).total;
+}
+
+mamba_status mamba_scan_bwd(const mamba_scan_bwd_args* a, void* stream_v) {
+  if (!a) return MAMBA_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
+  mamba_status st = check_common(a->batch, a->d_inner, a->d_state, a->d_conv, a->io);
+  if (st != MAMBA_OK) return st;
+  if (a->seqlen < 0 || a->n_chunks < 0) return MAMBA_ERR_INVALID_ARG;
+  if (!a->A_log || !a->Dskip || !a->conv_w || !a->dA_log || !a->dDskip || !a->dconv_w)
+    return MAMBA_ERR_INVALID_ARG;
+  const void* aligned_ptrs[] = {a->A_log, a->Dskip, a->conv_w, a->conv_b, a->h0, a->conv_state0,
+                                a->dfinal_h, a->dfinal_conv_state, a->dA_log, a->dDskip, a->dconv_w,
+                                a->dconv_b, a->dh0, a->dconv_state0};
+  for (const void* p : aligned_ptrs)
+    if (p && !aligned16(p)) return MAMBA_ERR_INVALID_ARG;
+  const size_t B = a->batch, D = a->d_inner;
+  const IoType io = a->io == MAMBA_BF16 ? IoType::BF16 : IoType::F32;
+
+  if (a->seqlen == 0) {
+    // final_h = h0 and final_conv_state = conv_state0; the parameters are unused
+    if (cudaMemsetAsync(a->dA_log, 0, D * 16 * sizeof(float), stream) != cudaSuccess ||
+        cudaMemsetAsync(a->dDskip, 0, D * sizeof(float), stream) != cudaSuccess ||
+        cudaMemsetAsync(a->dconv_w, 0, D * 4 * sizeof(float), stream) != cudaSuccess ||
+        (a->dconv_b && cudaMemsetAsync(a->dconv_b, 0, D * sizeof(float), stream) != cudaSuccess))
+      return MAMBA_ERR_CUDA;
+    if (a->dh0) {
+      cudaError_t e = a->dfinal_h ? cudaMemcpyAsync(a->dh0, a->dfinal_h, B * D * 16 * sizeof(float),
+                                                    cudaMemcpyDeviceToDevice, stream)
+                                  : cudaMemsetAsync(a->dh0, 0, B * D * 16 * sizeof(float), stream);
+      if (e != cudaSuccess) return MAMBA_ERR_CUDA;
+    }
+    if (a->dconv_state0) {
+      cudaError_t e = a->dfinal_conv_state
+                          ? mamba::launch_io_to_f32(io, a->dfinal_conv_state, a->dconv_state0, (long)(B * 3 * D), stream)
+                          : cudaMemsetAsync(a->dconv_state0, 0, B * 3 * D * sizeof(float), stream);
+      if (e != cudaSuccess) return MAMBA_ERR_CUDA;
+    }
+    return MAMBA_OK;
+  }
+
+  const void* io_ptrs[] = {a->x, a->z, a->dt_raw, a->Bm, a->Cm, a->dy, a->dx, a->dz, a->ddt_raw, a->dB, a->dC};
+  for (const void* p : io_ptrs)
+    if (!p || !aligned16(p)) return MAMBA_ERR_INVALID_ARG;
+  if ((long long)a->seqlen * (long long)D > (1LL << 40)) return MAMBA_ERR_UNSUPPORTED;
+
+  const Plan pl = make_plan(a->batch, a->seqlen, a->d_inner, a->n_chunks);
+  const BwdWorkspace ws = bwd_workspace_layout(a->batch, a->seqlen, a->d_inner, pl);
+  if (!a->workspace || a->workspace_bytes < ws.total) return MAMBA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return MAMBA_ERR_INVALID_ARG;
+  char* wsp = static_cast<char*>(a->workspace);
+  float* ckpt = reinterpret_cast<float*>(wsp + ws.ckpt);
+  const uint64_t timeout = a->wait_timeout_ns ? a->wait_timeout_ns : kDefaultTimeoutNs;
+
+  // 1. the forward pass again, storing the state entering every tile (no y)
+  mamba_scan_args fa;
+  std::memset(&fa, 0, sizeof(fa));
+  fa.batch = a->batch;
+  fa.seqlen = a->seqlen;
+  fa.d_inner = a->d_inner;
+  fa.d_state = a->d_state;
+  fa.d_conv = a->d_conv;
+  fa.io = a->io;
+  fa.x = a->x;
+  fa.z = a->z;
+  fa.dt_raw = a->dt_raw;
+  fa.Bm = a->Bm;
+  fa.Cm = a->Cm;
+  fa.A_log = a->A_log;
+  fa.Dskip = a->Dskip;
+  fa.conv_w = a->conv_w;
+  fa.conv_b = a->conv_b;
+  fa.h0 = a->h0;
+  fa.conv_state0 = a->conv_state0;
+  fa.workspace = a->workspace;
+  fa.workspace_bytes = a->workspace_bytes;
+  fa.wait_timeout_ns = timeout;
+  st = launch_forward(&fa, pl, ws.fwd, ckpt, stream);
+  if (st != MAMBA_OK) return st;
+
+  // 2. adjoint carries (chunked mode), 3. reverse sweep, 4. sums
+  float* bc = reinterpret_cast<float*>(wsp + ws.fwd.bc);
+  CUtensorMap maps[5];  // x, z, dt_raw, dy, bc
   if (!encode3d(&maps[0], a->x, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
       !encode3d(&maps[1], a->z, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
       !encode3d(&maps[2], a->dt_raw, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
-      !encode3d(&maps[3], bc, MAMBA_F32, 32, a->seqlen, a->batch, 32) ||
+      !encode3d(&maps[3], a->dy, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
       !encode3d(&maps[4], bc, MAMBA_F32, 32, a->seqlen, a->batch, 32))
     return MAMBA_ERR_CUDA;
 
-  mamba::ScanParams p;
+  mamba::BwdParams p;
   std::memset(&p, 0, sizeof(p));
   p.batch = a->batch;
   p.seqlen = a->seqlen;
@@ -283,32 +467,39 @@ mamba_status mamba_scan_fwd(const mamba_scan_args* a, void* stream_v) {
   p.n_chunks = pl.n_chunks;
   p.piece_tiles = pl.piece_tiles;
   p.pieces = pl.pieces;
+  p.seq_tiles = (a->seqlen + kT - 1) / kT;
   p.A_log = a->A_log;
   p.Dskip = a->Dskip;
   p.conv_w = a->conv_w;
   p.conv_b = a->conv_b;
-  p.h0 = a->h0;
   p.conv_state0 = a->conv_state0;
   p.x = a->x;
-  p.y = a->y;
-  p.final_h = a->final_h;
-  p.final_conv_state = a->final_conv_state;
-  p.flags = a->flags;
-  p.timeout_ns = a->wait_timeout_ns ? a->wait_timeout_ns : kDefaultTimeoutNs;
-  const IoType io = a->io == MAMBA_BF16 ? IoType::BF16 : IoType::F32;
-
-  if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, stream) != cudaSuccess)
-    return MAMBA_ERR_CUDA;
+  p.ckpt = ckpt;
+  p.dfinal_h = a->dfinal_h;
+  p.dfinal_conv_state = a->dfinal_conv_state;
+  p.dx = a->dx;
+  p.dz = a->dz;
+  p.ddt_raw = a->ddt_raw;
+  p.part_bc = reinterpret_cast<float*>(wsp + ws.part_bc);
+  p.part_param = reinterpret_cast<float*>(wsp + ws.part_param);
+  p.dh0 = a->dh0;
+  p.dconv_state0 = a->dconv_state0;
+  p.timeout_ns = timeout;
   if (pl.n_chunks > 1) {
-    p.carry = reinterpret_cast<float*>(wsp + ws.carry);
+    p.acarry = reinterpret_cast<float*>(wsp + ws.acarry);
     p.counters = reinterpret_cast<unsigned*>(wsp + ws.counters);
+    p.edge_dx = reinterpret_cast<float*>(wsp + ws.edge_dx);
+    p.edge_dpre = reinterpret_cast<float*>(wsp + ws.edge_dpre);
     if (cudaMemsetAsync(p.counters, 0, ws.counters_bytes, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
-    const CUtensorMap smaps[3] = {maps[0], maps[2], maps[4]};  // x, dt_raw, B/C rows
+    const CUtensorMap amaps[4] = {maps[1], maps[2], maps[3], maps[4]};
     dim3 g1((unsigned)((size_t)(pl.n_chunks - 1) * p.n_groups * B));
-    if (mamba::launch_summary(io, smaps, p, g1, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+    if (mamba::launch_acarry(io, amaps, p, g1, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
   }
   dim3 g2((unsigned)p.n_groups, (unsigned)B, (unsigned)pl.n_chunks);
-  if (mamba::launch_scan(io, maps, p, g2, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+  if (mamba::launch_bwd(io, maps, p, g2, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+  if (mamba::launch_bwd_finish(io, p, a->dB, a->dC, a->dA_log, a->dDskip, a->dconv_w, a->dconv_b, stream) !=
+      cudaSuccess)
+    return MAMBA_ERR_CUDA;
   return MAMBA_OK;
 }
 

@@ -3,6 +3,7 @@
 #include <cuda_bf16.h>
 
 #include "launch.h"
+#include "scan_bwd.cuh"
 #include "scan_fwd.cuh"
 #include "step.cuh"
 
@@ -99,6 +100,72 @@ void scan_occupancy(IoType io, int* main_per_sm, int* summary_per_sm) {
   }
   *main_per_sm = a;
   *summary_per_sm = b;
+}
+
+template <typename IO>
+static cudaError_t launch_bwd_t(const CUtensorMap* m, const BwdParams& p, dim3 grid, cudaStream_t s) {
+  const size_t smem = sizeof(BwdSmem<IO>) + 128;
+  cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  scan_bwd_kernel<IO><<<grid, kLanes, smem, s>>>(m[0], m[1], m[2], m[3], m[4], p);
+  return cudaGetLastError();
+}
+
+template <typename IO>
+static cudaError_t launch_acarry_t(const CUtensorMap* m, const BwdParams& p, dim3 grid, cudaStream_t s) {
+  const size_t smem = sizeof(ACarrySmem<IO>) + 128;
+  cudaError_t e =
+      cudaFuncSetAttribute(scan_acarry_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  scan_acarry_kernel<IO><<<grid, kLanes, smem, s>>>(m[0], m[1], m[2], m[3], p);
+  return cudaGetLastError();
+}
+
+static unsigned grid_for(long n, int threads) {
+  long blocks = (n + threads - 1) / threads;
+  if (blocks > 148L * 16) blocks = 148L * 16;
+  if (blocks < 1) blocks = 1;
+  return (unsigned)blocks;
+}
+
+cudaError_t launch_bwd(IoType io, const CUtensorMap maps[5], const BwdParams& p, dim3 grid, cudaStream_t stream) {
+  return io == IoType::BF16 ? launch_bwd_t<__nv_bfloat16>(maps, p, grid, stream)
+                            : launch_bwd_t<float>(maps, p, grid, stream);
+}
+
+cudaError_t launch_acarry(IoType io, const CUtensorMap maps[4], const BwdParams& p, dim3 grid,
+                          cudaStream_t stream) {
+  return io == IoType::BF16 ? launch_acarry_t<__nv_bfloat16>(maps, p, grid, stream)
+                            : launch_acarry_t<float>(maps, p, grid, stream);
+}
+
+cudaError_t launch_bwd_finish(IoType io, const BwdParams& p, float* dB, float* dC, float* dA_log, float* dD,
+                              float* dconv_w, float* dconv_b, cudaStream_t stream) {
+  if (p.n_chunks > 1) {
+    const long n = (long)p.batch * (p.n_chunks - 1) * p.d_inner;
+    if (io == IoType::BF16)
+      bwd_edges_kernel<__nv_bfloat16><<<grid_for(n, 256), 256, 0, stream>>>(p);
+    else
+      bwd_edges_kernel<float><<<grid_for(n, 256), 256, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const long rows = (long)p.batch * p.seqlen;
+  bwd_reduce_bc_kernel<<<grid_for(rows * 8, 256), 256, 0, stream>>>(p.part_bc, p.n_groups, rows, dB, dC);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_reduce_param_kernel<<<grid_for((long)p.d_inner * 22, 256), 256, 0, stream>>>(
+      p.part_param, p.batch * p.n_chunks, p.d_inner, dA_log, dD, dconv_w, dconv_b);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_io_to_f32(IoType io, const void* src, float* dst, long n, cudaStream_t stream) {
+  if (io == IoType::BF16)
+    io_to_f32_kernel<__nv_bfloat16><<<grid_for(n, 256), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(src), dst, n);
+  else
+    io_to_f32_kernel<float><<<grid_for(n, 256), 256, 0, stream>>>(static_cast<const float*>(src), dst, n);
+  return cudaGetLastError();
 }
 
 cudaError_t take_device_error(unsigned* code, cudaStream_t stream) {

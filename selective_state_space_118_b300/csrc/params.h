@@ -29,7 +29,38 @@ struct ScanParams {
   float* carry;              // chunked: (B, n_chunks, D, 16) carried-in states (entry 0 unused)
   unsigned* counters;        // chunked: [0] ticket counter, then (B, n_groups, n_chunks) ready
                              // flags; zeroed before every call
+  float* ckpt;               // may be null: (B, seq_tiles, D, 16) state entering every tile
+  int seq_tiles;             // tiles of the whole sequence (rows of ckpt)
   uint32_t flags;
+  uint64_t timeout_ns;
+};
+
+// The backward pass (scan_bwd.cuh).  Sizes and plan as in ScanParams; the
+// forward states entering every tile come from a checkpointing forward pass.
+struct BwdParams {
+  int batch, seqlen, d_inner;
+  int n_groups, chunk_tiles, n_chunks, piece_tiles, pieces, seq_tiles;
+  const float* A_log;
+  const float* Dskip;
+  const float* conv_w;
+  const float* conv_b;              // may be null
+  const void* conv_state0;          // may be null
+  const void* x;                    // plain pointer to x (conv inputs before a tile)
+  const float* ckpt;                // (B, seq_tiles, D, 16)
+  const float* dfinal_h;            // (B, D, 16) or null
+  const void* dfinal_conv_state;    // (B, 3, D) I/O dtype, or null
+  float* acarry;                    // chunked: (B, n_chunks, D, 16) adjoint entering chunk j
+                                    // from its right (j < n_chunks - 1)
+  unsigned* counters;               // chunked: ticket counter, then (B, n_groups, n_chunks) flags
+  void* dx;                         // (B, L, D) I/O dtype
+  void* dz;
+  void* ddt_raw;
+  float* part_bc;                   // (n_groups, B * L, 32): per group sums of dB | dC
+  float* part_param;                // (B * n_chunks, D, 24): dA_log(16), dD, dconv_w(4), dconv_b
+  float* edge_dx;                   // (B, n_chunks, 3, D): dx of a chunk's last 3 tokens, partial
+  float* edge_dpre;                 // (B, n_chunks, 3, D): d(conv output) of its first 3 tokens
+  float* dh0;                       // (B, D, 16) or null
+  float* dconv_state0;              // (B, 3, D) fp32 or null
   uint64_t timeout_ns;
 };
 

@@ -131,10 +131,10 @@ __device__ __forceinline__ float softplus_sel(float v) {
   return kSmall ? softplus_small_raw(v) : softplus(v);
 }
 
-// One tile of the main pass, `rows` tokens, straight-line per token.
-// kFull: rows == kT, the loop is unrolled completely.
+// One tile of the main pass, `rows` tokens, straight-line per token; y is
+// stored where wy holds.  kFull: rows == kT, the loop is unrolled completely.
 template <typename IO, bool kSmall, bool kFull>
-__device__ __forceinline__ void main_tile(const MainStage<IO>& S, int rows, int lane, bool active,
+__device__ __forceinline__ void main_tile(const MainStage<IO>& S, int rows, int lane, bool wy,
                                           const Channel& ch, State16& st, float& xm3, float& xm2, float& xm1,
                                           IO* ytile, int D) {
   if (kFull) rows = kT;
@@ -153,7 +153,7 @@ __device__ __forceinline__ void main_tile(const MainStage<IO>& S, int rows, int 
     drive16_q(d, ch.a2, dt, __fmul_rn(dt, u), Q);
     state16_apply(st, d);
     const float yv = gate_out(state16_readout_q(st, Q), ch.Dc, u, gz);
-    st_global_if(active, ytile + (size_t)r * D, from_f32<IO>(yv));
+    st_global_if(wy, ytile + (size_t)r * D, from_f32<IO>(yv));
   }
 }
 
@@ -254,6 +254,8 @@ __global__ void __launch_bounds__(kLanes)
     }
   }
 
+  // y may be null (a checkpointing pass for the backward needs only the states)
+  const bool wy = active && p.y != nullptr;
   IO* yrow = reinterpret_cast<IO*>(p.y) + ((size_t)b * p.seqlen + t_begin) * D + cl;
   bool ok = true;
   int k = 0;
@@ -261,17 +263,19 @@ __global__ void __launch_bounds__(kLanes)
     const int s = k % kStages;
     const MainStage<IO>& S = sm.stage[s];
     const int t_valid = min(kT, t_end - (t_begin + k * kT));
+    if (p.ckpt != nullptr && active)
+      state16_store(st, p.ckpt + (((size_t)b * p.seq_tiles + (t_begin / kT + k)) * D + c) * kN);
     bool mine = mbar_wait_bounded(smem_u32(&sm.full[s]), (k / kStages) & 1, p.timeout_ns);
     ok = __all_sync(0xffffffffu, mine);
     if (!ok) break;
     IO* ytile = yrow + (size_t)k * kT * D;
     if (small_dt_tile<IO>(S.dt, t_valid, lane, active)) {
       if (t_valid == kT)
-        main_tile<IO, true, true>(S, kT, lane, active, ch, st, xm3, xm2, xm1, ytile, D);
+        main_tile<IO, true, true>(S, kT, lane, wy, ch, st, xm3, xm2, xm1, ytile, D);
       else
-        main_tile<IO, true, false>(S, t_valid, lane, active, ch, st, xm3, xm2, xm1, ytile, D);
+        main_tile<IO, true, false>(S, t_valid, lane, wy, ch, st, xm3, xm2, xm1, ytile, D);
     } else {
-      main_tile<IO, false, false>(S, t_valid, lane, active, ch, st, xm3, xm2, xm1, ytile, D);
+      main_tile<IO, false, false>(S, t_valid, lane, wy, ch, st, xm3, xm2, xm1, ytile, D);
     }
     __syncwarp();  // every lane is done with stage s
     if (lane == 0 && k + kStages < n_tiles) {

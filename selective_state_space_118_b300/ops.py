@@ -27,7 +27,7 @@ D_STATE, D_CONV = 16, 4
 # the functions the public header declares (checked by the tests)
 EXPORTED = ("mamba_scan_workspace_size", "mamba_scan_default_chunks", "mamba_scan_plan", "mamba_scan_fwd",
             "mamba_step", "mamba_last_error", "mamba_status_string", "mamba_abi_version",
-            "mamba_scan_fwd_noalloc")
+            "mamba_scan_fwd_noalloc", "mamba_scan_bwd_workspace_size", "mamba_scan_bwd")
 MAMBA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _vp = ctypes.c_void_p
@@ -40,6 +40,19 @@ class ScanArgs(ctypes.Structure):
                 ("A_log", _vp), ("Dskip", _vp), ("conv_w", _vp), ("conv_b", _vp),
                 ("h0", _vp), ("conv_state0", _vp), ("y", _vp), ("final_h", _vp),
                 ("final_conv_state", _vp), ("workspace", _vp),
+                ("workspace_bytes", ctypes.c_size_t), ("n_chunks", ctypes.c_int),
+                ("flags", ctypes.c_uint32), ("wait_timeout_ns", ctypes.c_uint64)]
+
+
+class BwdArgs(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("seqlen", ctypes.c_int), ("d_inner", ctypes.c_int),
+                ("d_state", ctypes.c_int), ("d_conv", ctypes.c_int), ("io", ctypes.c_int),
+                ("x", _vp), ("z", _vp), ("dt_raw", _vp), ("Bm", _vp), ("Cm", _vp),
+                ("A_log", _vp), ("Dskip", _vp), ("conv_w", _vp), ("conv_b", _vp),
+                ("h0", _vp), ("conv_state0", _vp), ("dy", _vp), ("dfinal_h", _vp),
+                ("dfinal_conv_state", _vp), ("dx", _vp), ("dz", _vp), ("ddt_raw", _vp),
+                ("dB", _vp), ("dC", _vp), ("dA_log", _vp), ("dDskip", _vp), ("dconv_w", _vp),
+                ("dconv_b", _vp), ("dh0", _vp), ("dconv_state0", _vp), ("workspace", _vp),
                 ("workspace_bytes", ctypes.c_size_t), ("n_chunks", ctypes.c_int),
                 ("flags", ctypes.c_uint32), ("wait_timeout_ns", ctypes.c_uint64)]
 
@@ -90,6 +103,10 @@ def load_library(path: str = LIB_PATH):
         lib.mamba_abi_version.restype = ctypes.c_int
         lib.mamba_scan_fwd_noalloc.argtypes = [ctypes.POINTER(ScanArgs), _vp]
         lib.mamba_scan_fwd_noalloc.restype = ctypes.c_int
+        lib.mamba_scan_bwd_workspace_size.argtypes = [ctypes.c_int] * 4
+        lib.mamba_scan_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.mamba_scan_bwd.argtypes = [ctypes.POINTER(BwdArgs), _vp]
+        lib.mamba_scan_bwd.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -176,6 +193,61 @@ def mamba_scan_fwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=N
     if st != MAMBA_OK:
         raise MambaError(st, "mamba_scan_fwd")
     return y, final_h, final_conv_state
+
+
+def mamba_scan_bwd_workspace_size(batch: int, seqlen: int, d_inner: int, n_chunks: int = 0) -> int:
+    return int(load_library().mamba_scan_bwd_workspace_size(batch, seqlen, d_inner, n_chunks))
+
+
+BWD_OUTPUTS = ("dx", "dz", "ddt_raw", "dB", "dC", "dA_log", "dDskip", "dconv_w", "dconv_b", "dh0",
+               "dconv_state0")
+
+
+def mamba_scan_bwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=None,
+                   conv_state0=None, *, dy, dfinal_h=None, dfinal_conv_state=None,
+                   out=None, workspace=None, n_chunks: int = 0, wait_timeout_ns: int = 0,
+                   stream=None) -> dict:
+    """Backward of the prefill scan (C ABI ``mamba_scan_bwd``): the gradients
+    of l given dy = dl/dy (B,L,D) and optionally dl/dfinal_h (B,D,16) fp32 and
+    dl/dfinal_conv_state (B,3,D).  Returns a dict keyed by BWD_OUTPUTS: dx,
+    dz, ddt_raw in the I/O dtype, everything else fp32 (dconv_b only when
+    conv_b is given).  `out` may hold preallocated outputs by the same keys."""
+    lib = load_library()
+    B, L, D = x.shape
+    dev = x.device
+    f32 = torch.float32
+    shapes = {"dx": ((B, L, D), x.dtype), "dz": ((B, L, D), x.dtype), "ddt_raw": ((B, L, D), x.dtype),
+              "dB": ((B, L, D_STATE), f32), "dC": ((B, L, D_STATE), f32),
+              "dA_log": ((D, D_STATE), f32), "dDskip": ((D,), f32), "dconv_w": ((D, D_CONV), f32),
+              "dconv_b": ((D,), f32), "dh0": ((B, D, D_STATE), f32),
+              "dconv_state0": ((B, D_CONV - 1, D), f32)}
+    g = dict(out or {})
+    for k, (shape, dtype) in shapes.items():
+        if k == "dconv_b" and conv_b is None:
+            g.setdefault(k, None)
+            continue
+        if g.get(k) is None:
+            g[k] = torch.empty(shape, device=dev, dtype=dtype)
+    for t in (z, dt_raw, Bm, Cm, conv_state0, dy, dfinal_conv_state, g["dx"], g["dz"], g["ddt_raw"]):
+        if t is not None and t.dtype != x.dtype:
+            raise TypeError("x, z, dt_raw, Bm, Cm, conv_state0, dy, dfinal_conv_state, dx, dz and "
+                            "ddt_raw share one dtype")
+    ws_bytes = mamba_scan_bwd_workspace_size(B, L, D, n_chunks)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+    a = BwdArgs(batch=B, seqlen=L, d_inner=D, d_state=A_log.shape[-1], d_conv=conv_w.shape[-1],
+                io=_io_code(x), x=_ptr(x), z=_ptr(z), dt_raw=_ptr(dt_raw), Bm=_ptr(Bm), Cm=_ptr(Cm),
+                A_log=_ptr(A_log), Dskip=_ptr(Dskip), conv_w=_ptr(conv_w), conv_b=_ptr(conv_b),
+                h0=_ptr(h0), conv_state0=_ptr(conv_state0), dy=_ptr(dy), dfinal_h=_ptr(dfinal_h),
+                dfinal_conv_state=_ptr(dfinal_conv_state),
+                **{k: _ptr(g[k]) for k in BWD_OUTPUTS},
+                workspace=_ptr(workspace),
+                workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
+                n_chunks=n_chunks, flags=0, wait_timeout_ns=wait_timeout_ns)
+    st = lib.mamba_scan_bwd(ctypes.byref(a), _stream(stream))
+    if st != MAMBA_OK:
+        raise MambaError(st, "mamba_scan_bwd")
+    return g
 
 
 def mamba_step(h, conv_state, x_t, z_t, dt_raw_t, B_t, C_t, A_log, Dskip, conv_w, conv_b=None,

@@ -54,7 +54,8 @@ def _c_layout(tmp_path, struct, fields):
 
 
 @pytest.mark.parametrize("struct,cls", [("mamba_scan_args", ops.ScanArgs),
-                                        ("mamba_step_args", ops.StepArgs)])
+                                        ("mamba_step_args", ops.StepArgs),
+                                        ("mamba_scan_bwd_args", ops.BwdArgs)])
 def test_ctypes_structs_match_c_layout(tmp_path, struct, cls):
     fields = [f for f, _ in cls._fields_]
     c = _c_layout(tmp_path, struct, fields)
@@ -113,6 +114,46 @@ def test_step_argument_checks(lib):
     a.d_state = 32
     assert lib.mamba_step(ctypes.byref(a), None) == ops.MAMBA_ERR_UNSUPPORTED
     assert lib.mamba_step(None, None) == ops.MAMBA_ERR_INVALID_ARG
+
+
+def test_bwd_argument_checks(lib):
+    base = dict(batch=1, seqlen=8, d_inner=16, d_state=16, d_conv=4, io=ops.MAMBA_BF16)
+    a = ops.BwdArgs(**base)
+    assert lib.mamba_scan_bwd(ctypes.byref(a), None) == ops.MAMBA_ERR_INVALID_ARG  # params missing
+    full = dict(base, A_log=FAKE, Dskip=FAKE, conv_w=FAKE, dA_log=FAKE, dDskip=FAKE, dconv_w=FAKE,
+                x=FAKE, z=FAKE, dt_raw=FAKE, Bm=FAKE, Cm=FAKE, dy=FAKE, dx=FAKE, dz=FAKE, ddt_raw=FAKE,
+                dB=FAKE, dC=FAKE)
+    for k in ("dA_log", "dy", "dB"):
+        assert lib.mamba_scan_bwd(ctypes.byref(ops.BwdArgs(**dict(full, **{k: 0}))), None) == \
+            ops.MAMBA_ERR_INVALID_ARG, k
+    for k in ("dconv_w", "dx", "dfinal_h"):
+        assert lib.mamba_scan_bwd(ctypes.byref(ops.BwdArgs(**dict(full, **{k: FAKE + 4}))), None) == \
+            ops.MAMBA_ERR_INVALID_ARG, k
+    assert lib.mamba_scan_bwd(ctypes.byref(ops.BwdArgs(**dict(full, d_inner=24))), None) == \
+        ops.MAMBA_ERR_UNSUPPORTED
+    assert lib.mamba_scan_bwd(ctypes.byref(ops.BwdArgs(**full)), None) == ops.MAMBA_ERR_WORKSPACE
+    assert lib.mamba_scan_bwd(None, None) == ops.MAMBA_ERR_INVALID_ARG
+
+
+def test_bwd_workspace(lib):
+    def r256(v):
+        return (v + 255) // 256 * 256
+    # one pass: the forward's B/C rows, the state entering every 16-token tile,
+    # the per-group dB | dC sums and the per-chunk parameter partials
+    B, L, D = 1, 32768, 8192
+    assert ops.mamba_scan_bwd_workspace_size(B, L, D, 1) == (
+        r256(B * L * 32 * 4) + r256(B * (L // 16) * D * 16 * 4) + r256((D // 32) * B * L * 32 * 4)
+        + r256(B * D * 24 * 4))
+    assert ops.mamba_scan_bwd_workspace_size(1, 0, 64, 1) == 0
+    # chunked: plus the forward's carries, the adjoint carries, their counters
+    # and the conv edge buffers
+    B, L, D, n = 2, 4096, 64, 4
+    ws = ops.mamba_scan_bwd_workspace_size(B, L, D, n)
+    G = D // 32
+    need = (B * L * 32 * 4 + B * n * D * 16 * 4 + (1 + B * G * n) * 4  # forward
+            + B * (L // 16) * D * 16 * 4 + B * n * D * 16 * 4 + (1 + B * G * n) * 4
+            + G * B * L * 32 * 4 + B * n * D * 24 * 4 + 2 * B * n * 3 * D * 4)
+    assert need <= ws <= need + 9 * 256
 
 
 def test_workspace_plan(lib):
