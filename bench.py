@@ -215,6 +215,16 @@ def scan_algorithmic_bytes(B, L, D, es):
     return act + bc + params + state
 
 
+def bwd_algorithmic_bytes(B, L, D, es):
+    """Minimum HBM bytes of one backward call: x, z, dt_raw, dy read and dx,
+    dz, ddt_raw written once; B, C rows read and dB, dC (fp32) written; the
+    parameters read and their gradients written."""
+    act = 7 * B * L * D * es
+    bc = 2 * B * L * D_STATE * es + 2 * B * L * D_STATE * 4
+    params = 2 * D * (D_STATE + 1 + D_CONV + 1) * 4
+    return act + bc + params
+
+
 def decode_algorithmic_bytes(B, D, es):
     """Minimum HBM bytes of one decode step of one layer: h read and written
     (fp32), x_t, z_t, dt_raw_t read and y_t written, the conv state's 3
@@ -324,6 +334,85 @@ def bench_e2e(w, inp, out, ws, steps, local):
     return {"t": t, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "steps": steps, "ms_per_step": t * 1e3 / steps,
             "pipelining": "uploads / scan / downloads on three streams, two buffer sets"}
+
+
+def bench_backward(w, steps, warmup, local, n_chunks_req=0):
+    """The backward of the prefill (mamba_scan_bwd: it recomputes the forward
+    with tile checkpoints, then the reverse sweep) on the same workload, with
+    a seeded random dy; elements/s over B * L * D, like the forward."""
+    from selective_state_space_118_b300 import ops
+    dev = torch.device("cuda", local)
+    inp = inputs.workload_inputs(w, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 1000)
+    dy = torch.randn(inp["x"].shape, generator=g, device=dev).to(inp["x"].dtype)
+    B, L, D = w.batch, w.seqlen, w.d_inner
+    ws = torch.empty(ops.mamba_scan_bwd_workspace_size(B, L, D, n_chunks_req), device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+    out = None
+
+    def call():
+        return ops.mamba_scan_bwd(inp["x"], inp["z"], inp["dt_raw"], inp["Bm"], inp["Cm"], inp["A_log"],
+                                  inp["Dskip"], inp["conv_w"], inp["conv_b"], dy=dy, out=out, workspace=ws,
+                                  n_chunks=n_chunks_req, stream=stream)
+
+    out = call()
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    assert ops.mamba_last_error(stream) == ops.MAMBA_OK
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with ClockSampler(dev.index) as clk:
+        ev[0].record(stream)
+        for i in range(steps):
+            call()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+    assert ops.mamba_last_error(stream) == ops.MAMBA_OK
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    t = ev[0].elapsed_time(ev[steps]) / 1e3 / steps
+    es = 2 if w.io == "bf16" else 4
+    alg = bwd_algorithmic_bytes(B, L, D, es)
+    hbm, src = peaks()
+    n_chunks = ops.mamba_scan_plan(B, L, D, n_chunks_req)["n_chunks"]
+    launches = 7 if n_chunks > 1 else 5
+    res = {"metric": "backward elements/s", "value": B * L * D / t, "unit": UNIT,
+           "config": {"workload": w.name, "batch": B, "seqlen": L, "d_inner": D, "n_chunks": n_chunks,
+                      "dy": "seeded N(0,1) in the I/O dtype"},
+           "ms_per_call": t * 1e3, "ms_per_call_min": min(per),
+           "roofline": {"bound": "issue", "hbm_achieved": alg / t / 1e9, "hbm_peak": hbm, "unit": "GB/s",
+                        "hbm_frac": alg / t / 1e9 / hbm, "peak_source": src,
+                        "algorithmic_bytes_per_call": alg,
+                        "note": "instruction-issue bound (forward recomputed from tile checkpoints, "
+                                "then the reverse sweep); the HBM fraction is context"},
+           "gpu_launches": launches * steps, "clocks": clk.summary()}
+    del inp, dy, ws, out
+    return res
+
+
+def oracle_bwd_sample_rate(w, target_s: float):
+    """The fp64 backward oracle on a few channels of the workload (every token
+    and batch row): elements/s, extrapolated per channel."""
+    import oracle
+    oracle.build()
+    L = w.seqlen
+
+    def run(ch):
+        sub = inputs.ScanWorkload(w.name, w.batch, L, ch, w.io, w.seed, w.bc_std)
+        inp = inputs.workload_inputs(sub, device="cpu")
+        dy = torch.randn(inp["x"].shape, generator=torch.Generator().manual_seed(1)).to(inp["x"].dtype)
+        t0 = time.perf_counter()
+        oracle.scan_bwd(inp["x"], inp["z"], inp["dt_raw"], inp["Bm"], inp["Cm"], inp["A_log"],
+                        inp["Dskip"], inp["conv_w"], inp["conv_b"], dy=dy)
+        return time.perf_counter() - t0
+
+    t1 = max(run(1), 1e-3)
+    ch = int(max(1, min(w.d_inner, target_s / t1)))
+    t = run(ch)
+    elems = w.batch * L * ch
+    return elems / t, {"kind": "oracle", "cores": 1,
+                       "sample": f"{ch} of {w.d_inner} channels x all {L} tokens x batch {w.batch} "
+                                 f"({elems} elements, {t:.1f} s, one thread: dB and dC sum over channels)"}
 
 
 def bench_decode(w, local, replays=3, layers=None, tokens=None):
@@ -463,6 +552,7 @@ def main():
     ap.add_argument("--decode-layers", type=int, default=0, help="fewer decode layers (profiling)")
     ap.add_argument("--decode-tokens", type=int, default=0, help="fewer decode tokens (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--n-chunks", type=int, default=0,
                     help="chunk count passed to the library (0: its own plan)")
@@ -496,7 +586,7 @@ def main():
             "data": "synthetic", "config": dict(config_of(w, res["n_chunks"]), plan=res["plan"]),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": measured_traffic(w.name), "peak_source": src,
-                         "kernel": "mamba_scan_fwd: bc_widen + scan_piece_summary + scan_fwd (one call)",
+                         "kernel": "mamba_scan_fwd: bc_widen + scan_carry + scan_fwd (one call)",
                          "algorithmic_bytes_per_launch": res["alg_bytes"]},
             "gpu_launches": res["launches_per_step"] * args.steps,
             "clocks": res["clocks"]}
@@ -511,6 +601,12 @@ def main():
         line["decode"] = bench_decode(inputs.DECODE, local, layers=args.decode_layers,
                                       tokens=args.decode_tokens)
         torch.cuda.empty_cache()
+    if not args.no_backward:
+        line["backward"] = bench_backward(w, max(3, min(args.steps, 20)), 3, local, args.n_chunks)
+        torch.cuda.empty_cache()
+        if rank == 0 and not args.no_cpu_baseline and world == 1:
+            v, desc = oracle_bwd_sample_rate(w, target_s=4.0)
+            line["backward"]["cpu_baseline"] = dict(desc, value=v, unit=UNIT)
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         v, desc = oracle_sample_rate(w, target_s=10.0, max_channels=w.d_inner)
         line["cpu_baseline"] = dict(desc, value=v, unit=UNIT)

@@ -224,28 +224,13 @@ mamba_status check_common(int batch, int d_inner, int d_state, int d_conv, mamba
   return MAMBA_OK;
 }
 
-// The forward kernels for checked arguments and a workspace of the plan's
-// layout: B/C widening, chunk carries (chunked mode) and the main pass.
-// ckpt (may be null): the state entering every tile is stored there.
-mamba_status launch_forward(const mamba_scan_args* a, const Plan& pl, const Workspace& ws, float* ckpt,
-                            cudaStream_t stream) {
-  const size_t B = a->batch;
+// The forward's parameter block for checked arguments and a workspace of the
+// plan's layout.  ckpt (may be null): the state entering every tile is
+// stored there.
+mamba::ScanParams fwd_params(const mamba_scan_args* a, const Plan& pl, const Workspace& ws, float* ckpt) {
   char* wsp = static_cast<char*>(a->workspace);
-  float* bc = reinterpret_cast<float*>(wsp + ws.bc);
-
-  // x, z, dt_raw, bc (main pass), bc (summary pass)
-  CUtensorMap maps[5];
-  if (!encode3d(&maps[0], a->x, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
-      !encode3d(&maps[1], a->z, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
-      !encode3d(&maps[2], a->dt_raw, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
-      !encode3d(&maps[3], bc, MAMBA_F32, 32, a->seqlen, a->batch, 32) ||
-      !encode3d(&maps[4], bc, MAMBA_F32, 32, a->seqlen, a->batch, 32))
-    return MAMBA_ERR_CUDA;
-
   mamba::ScanParams p;
   std::memset(&p, 0, sizeof(p));
-  p.ckpt = ckpt;
-  p.seq_tiles = (a->seqlen + kT - 1) / kT;
   p.batch = a->batch;
   p.seqlen = a->seqlen;
   p.d_inner = a->d_inner;
@@ -264,15 +249,37 @@ mamba_status launch_forward(const mamba_scan_args* a, const Plan& pl, const Work
   p.y = a->y;
   p.final_h = a->final_h;
   p.final_conv_state = a->final_conv_state;
+  p.ckpt = ckpt;
+  p.seq_tiles = (a->seqlen + kT - 1) / kT;
   p.flags = a->flags;
   p.timeout_ns = a->wait_timeout_ns ? a->wait_timeout_ns : kDefaultTimeoutNs;
+  if (pl.n_chunks > 1) {
+    p.carry = reinterpret_cast<float*>(wsp + ws.carry);
+    p.counters = reinterpret_cast<unsigned*>(wsp + ws.counters);
+  }
+  return p;
+}
+
+// The forward kernels: B/C widening, chunk carries (chunked mode), main pass.
+mamba_status launch_forward(const mamba_scan_args* a, const Plan& pl, const Workspace& ws, cudaStream_t stream) {
+  const size_t B = a->batch;
+  float* bc = reinterpret_cast<float*>(static_cast<char*>(a->workspace) + ws.bc);
+
+  // x, z, dt_raw, bc (main pass), bc (summary pass)
+  CUtensorMap maps[5];
+  if (!encode3d(&maps[0], a->x, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
+      !encode3d(&maps[1], a->z, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
+      !encode3d(&maps[2], a->dt_raw, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
+      !encode3d(&maps[3], bc, MAMBA_F32, 32, a->seqlen, a->batch, 32) ||
+      !encode3d(&maps[4], bc, MAMBA_F32, 32, a->seqlen, a->batch, 32))
+    return MAMBA_ERR_CUDA;
+
+  const mamba::ScanParams p = fwd_params(a, pl, ws, nullptr);
   const IoType io = a->io == MAMBA_BF16 ? IoType::BF16 : IoType::F32;
 
   if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, stream) != cudaSuccess)
     return MAMBA_ERR_CUDA;
   if (pl.n_chunks > 1) {
-    p.carry = reinterpret_cast<float*>(wsp + ws.carry);
-    p.counters = reinterpret_cast<unsigned*>(wsp + ws.counters);
     if (cudaMemsetAsync(p.counters, 0, ws.counters_bytes, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
     const CUtensorMap smaps[3] = {maps[0], maps[2], maps[4]};  // x, dt_raw, B/C rows
     dim3 g1((unsigned)((size_t)(pl.n_chunks - 1) * p.n_groups * B));
@@ -362,7 +369,7 @@ mamba_status mamba_scan_fwd(const mamba_scan_args* a, void* stream_v) {
 
   if (!a->workspace || a->workspace_bytes < ws.total) return MAMBA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return MAMBA_ERR_INVALID_ARG;
-  return launch_forward(a, pl, ws, nullptr, stream);
+  return launch_forward(a, pl, ws, stream);
 }
 
 size_t mamba_scan_bwd_workspace_size(int batch, int seqlen, int d_inner, int n_chunks) {
@@ -421,7 +428,7 @@ mamba_status mamba_scan_bwd(const mamba_scan_bwd_args* a, void* stream_v) {
   float* ckpt = reinterpret_cast<float*>(wsp + ws.ckpt);
   const uint64_t timeout = a->wait_timeout_ns ? a->wait_timeout_ns : kDefaultTimeoutNs;
 
-  // 1. the forward pass again, storing the state entering every tile (no y)
+  // The forward pass again, storing the state entering every tile (no y).
   mamba_scan_args fa;
   std::memset(&fa, 0, sizeof(fa));
   fa.batch = a->batch;
@@ -444,10 +451,8 @@ mamba_status mamba_scan_bwd(const mamba_scan_bwd_args* a, void* stream_v) {
   fa.workspace = a->workspace;
   fa.workspace_bytes = a->workspace_bytes;
   fa.wait_timeout_ns = timeout;
-  st = launch_forward(&fa, pl, ws.fwd, ckpt, stream);
-  if (st != MAMBA_OK) return st;
+  const mamba::ScanParams fp = fwd_params(&fa, pl, ws.fwd, ckpt);
 
-  // 2. adjoint carries (chunked mode), 3. reverse sweep, 4. sums
   float* bc = reinterpret_cast<float*>(wsp + ws.fwd.bc);
   CUtensorMap maps[5];  // x, z, dt_raw, dy, bc
   if (!encode3d(&maps[0], a->x, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
@@ -485,18 +490,27 @@ mamba_status mamba_scan_bwd(const mamba_scan_bwd_args* a, void* stream_v) {
   p.dh0 = a->dh0;
   p.dconv_state0 = a->dconv_state0;
   p.timeout_ns = timeout;
+
+  // 1. B/C rows widened; 2. chunked mode: the forward's chunk carries and the
+  // adjoint carries (one launch); 3. the states-only forward pass; 4. the
+  // reverse sweep; 5. the edge fix-up and the fixed-order sums
+  if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, stream) != cudaSuccess)
+    return MAMBA_ERR_CUDA;
   if (pl.n_chunks > 1) {
     p.acarry = reinterpret_cast<float*>(wsp + ws.acarry);
     p.counters = reinterpret_cast<unsigned*>(wsp + ws.counters);
     p.edge_dx = reinterpret_cast<float*>(wsp + ws.edge_dx);
     p.edge_dpre = reinterpret_cast<float*>(wsp + ws.edge_dpre);
-    if (cudaMemsetAsync(p.counters, 0, ws.counters_bytes, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
-    const CUtensorMap amaps[4] = {maps[1], maps[2], maps[3], maps[4]};
-    dim3 g1((unsigned)((size_t)(pl.n_chunks - 1) * p.n_groups * B));
-    if (mamba::launch_acarry(io, amaps, p, g1, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+    if (cudaMemsetAsync(fp.counters, 0, ws.fwd.counters_bytes, stream) != cudaSuccess ||
+        cudaMemsetAsync(p.counters, 0, ws.counters_bytes, stream) != cudaSuccess)
+      return MAMBA_ERR_CUDA;
+    const unsigned n_each = (unsigned)((size_t)(pl.n_chunks - 1) * p.n_groups * B);
+    if (mamba::launch_carries(io, maps, fp, p, n_each, n_each, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
   }
-  dim3 g2((unsigned)p.n_groups, (unsigned)B, (unsigned)pl.n_chunks);
-  if (mamba::launch_bwd(io, maps, p, g2, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+  const CUtensorMap fmaps[4] = {maps[0], maps[1], maps[2], maps[4]};  // x, z (unused), dt_raw, bc
+  dim3 grid((unsigned)p.n_groups, (unsigned)B, (unsigned)pl.n_chunks);
+  if (mamba::launch_scan(io, fmaps, fp, grid, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+  if (mamba::launch_bwd(io, maps, p, grid, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
   if (mamba::launch_bwd_finish(io, p, a->dB, a->dC, a->dA_log, a->dDskip, a->dconv_w, a->dconv_b, stream) !=
       cudaSuccess)
     return MAMBA_ERR_CUDA;

@@ -17,14 +17,20 @@ size_t summary_smem_bytes(IoType io) {
   return (io == IoType::BF16 ? sizeof(CarrySmem<__nv_bfloat16>) : sizeof(CarrySmem<float>)) + 128;
 }
 
-template <typename IO>
-static cudaError_t launch_scan_t(const CUtensorMap* m, const ScanParams& p, dim3 grid, cudaStream_t s) {
+template <typename IO, bool kY>
+static cudaError_t launch_scan_y(const CUtensorMap* m, const ScanParams& p, dim3 grid, cudaStream_t s) {
   const size_t smem = sizeof(MainSmem<IO>) + 128;
-  cudaError_t e = cudaFuncSetAttribute(scan_fwd_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(scan_fwd_kernel<IO, kY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  scan_fwd_kernel<IO><<<grid, kLanes, smem, s>>>(m[0], m[1], m[2], m[3], p);
+  scan_fwd_kernel<IO, kY><<<grid, kLanes, smem, s>>>(m[0], m[1], m[2], m[3], p);
   return cudaGetLastError();
+}
+
+// y null: the states-only pass (for the backward's checkpoints)
+template <typename IO>
+static cudaError_t launch_scan_t(const CUtensorMap* m, const ScanParams& p, dim3 grid, cudaStream_t s) {
+  return p.y != nullptr ? launch_scan_y<IO, true>(m, p, grid, s) : launch_scan_y<IO, false>(m, p, grid, s);
 }
 
 template <typename IO>
@@ -88,12 +94,12 @@ cudaError_t launch_step(IoType io, const StepParams& p, cudaStream_t stream) {
 void scan_occupancy(IoType io, int* main_per_sm, int* summary_per_sm) {
   int a = 0, b = 0;
   if (io == IoType::BF16) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, scan_fwd_kernel<__nv_bfloat16>, kLanes,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, scan_fwd_kernel<__nv_bfloat16, true>, kLanes,
                                                       sizeof(MainSmem<__nv_bfloat16>) + 128) != cudaSuccess) a = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, scan_carry_kernel<__nv_bfloat16>, kLanes,
                                                       sizeof(CarrySmem<__nv_bfloat16>) + 128) != cudaSuccess) b = 0;
   } else {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, scan_fwd_kernel<float>, kLanes,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, scan_fwd_kernel<float, true>, kLanes,
                                                       sizeof(MainSmem<float>) + 128) != cudaSuccess) a = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, scan_carry_kernel<float>, kLanes,
                                                       sizeof(CarrySmem<float>) + 128) != cudaSuccess) b = 0;
@@ -112,12 +118,13 @@ static cudaError_t launch_bwd_t(const CUtensorMap* m, const BwdParams& p, dim3 g
 }
 
 template <typename IO>
-static cudaError_t launch_acarry_t(const CUtensorMap* m, const BwdParams& p, dim3 grid, cudaStream_t s) {
-  const size_t smem = sizeof(ACarrySmem<IO>) + 128;
+static cudaError_t launch_carries_t(const CUtensorMap* m, const ScanParams& fp, const BwdParams& bp,
+                                   unsigned n_fwd, unsigned n_adj, cudaStream_t s) {
+  const size_t smem = sizeof(CarriesSmem<IO>) + 128;
   cudaError_t e =
-      cudaFuncSetAttribute(scan_acarry_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      cudaFuncSetAttribute(scan_carries_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  scan_acarry_kernel<IO><<<grid, kLanes, smem, s>>>(m[0], m[1], m[2], m[3], p);
+  scan_carries_kernel<IO><<<n_fwd + n_adj, kLanes, smem, s>>>(m[0], m[1], m[2], m[3], m[4], fp, bp, n_fwd);
   return cudaGetLastError();
 }
 
@@ -133,10 +140,10 @@ cudaError_t launch_bwd(IoType io, const CUtensorMap maps[5], const BwdParams& p,
                             : launch_bwd_t<float>(maps, p, grid, stream);
 }
 
-cudaError_t launch_acarry(IoType io, const CUtensorMap maps[4], const BwdParams& p, dim3 grid,
-                          cudaStream_t stream) {
-  return io == IoType::BF16 ? launch_acarry_t<__nv_bfloat16>(maps, p, grid, stream)
-                            : launch_acarry_t<float>(maps, p, grid, stream);
+cudaError_t launch_carries(IoType io, const CUtensorMap maps[5], const ScanParams& fp, const BwdParams& bp,
+                           unsigned n_fwd, unsigned n_adj, cudaStream_t stream) {
+  return io == IoType::BF16 ? launch_carries_t<__nv_bfloat16>(maps, fp, bp, n_fwd, n_adj, stream)
+                            : launch_carries_t<float>(maps, fp, bp, n_fwd, n_adj, stream);
 }
 
 cudaError_t launch_bwd_finish(IoType io, const BwdParams& p, float* dB, float* dC, float* dA_log, float* dD,

@@ -28,12 +28,13 @@ cudaError_t launch_summary(IoType io, const CUtensorMap maps[3], const ScanParam
                            cudaStream_t stream);
 cudaError_t launch_step(IoType io, const StepParams& p, cudaStream_t stream);
 
-// Backward.  maps: x, z, dt_raw, dy, bc (reverse sweep); z, dt_raw, dy, bc
-// (adjoint carries).  launch_bwd_finish runs the edge dx fix-up (chunked
-// mode) and the fixed-order sums of the dB | dC and parameter partials.
+// Backward.  maps: x, z, dt_raw, dy, bc.  launch_carries runs the forward's
+// chunk carries (n_fwd warps) and the adjoint carries (n_adj warps) in one
+// launch; launch_bwd_finish runs the edge dx fix-up (chunked mode) and the
+// fixed-order sums of the dB | dC and parameter partials.
 cudaError_t launch_bwd(IoType io, const CUtensorMap maps[5], const BwdParams& p, dim3 grid, cudaStream_t stream);
-cudaError_t launch_acarry(IoType io, const CUtensorMap maps[4], const BwdParams& p, dim3 grid,
-                          cudaStream_t stream);
+cudaError_t launch_carries(IoType io, const CUtensorMap maps[5], const ScanParams& fp, const BwdParams& bp,
+                           unsigned n_fwd, unsigned n_adj, cudaStream_t stream);
 cudaError_t launch_bwd_finish(IoType io, const BwdParams& p, float* dB, float* dC, float* dA_log, float* dD,
                               float* dconv_w, float* dconv_b, cudaStream_t stream);
 cudaError_t launch_io_to_f32(IoType io, const void* src, float* dst, long n, cudaStream_t stream);

@@ -37,7 +37,7 @@
 // its last token from the tokens after it.  That adjoint obeys the same kind
 // of linear recurrence as the state, run backwards:
 //   R_{t-1} = dA_t (C_t dyss_t + R_t),        R_{L-1} = dl/dfinal_h
-// (dyss does not depend on the state), so scan_acarry_kernel computes the
+// (dyss does not depend on the state), so the adjoint-carry warps compute the
 // carries like the forward's scan_carry_kernel with time reversed: one warp
 // per boundary walks the next chunk forwards in pieces, each piece scanned
 // backwards from zero, and stops once the decay from the boundary makes the
@@ -51,8 +51,8 @@ namespace mamba {
 
 constexpr int kSub = 4;             // tokens per register sub-tile
 constexpr int kSubs = kT / kSub;    // sub-tiles per tile
-constexpr int kRedStride = 36;      // floats per row of the dB | dC transpose buffer
 constexpr int kParamStride = 24;    // floats per channel of the parameter partials
+constexpr int kBwdMinBlocks = 1;    // resident reverse-sweep CTAs per SM the register budget must allow
 
 template <typename IO>
 struct BwdStage {
@@ -67,7 +67,7 @@ template <typename IO>
 struct BwdSmem {
   BwdStage<IO> stage[kStages];
   float4 sub[kSubs - 1][4][kLanes];  // states entering sub-tiles 1..3 of the current tile
-  float red[kLanes][kRedStride];     // dB | dC of one token, one row per lane
+  float4 red[2][kLanes][8];          // dB | dC of two tokens, one swizzled row per lane each
   uint64_t full[kStages];
 };
 
@@ -127,39 +127,62 @@ __device__ __forceinline__ void state16_load_f4(State16& s, const float4 (&src)[
   }
 }
 
-// Sums dB | dC of one token over the warp's 32 channels and stores the 32
-// sums (128 bytes) at dst.  Each lane writes its row; lane (rg, cg) adds rows
-// 8 rg .. 8 rg + 7 of columns 4 cg .. 4 cg + 3 in row order, then the four row
-// groups are combined by two exchanges (xor 8, then xor 16).  Row stride 36
-// keeps both the row writes and the column reads free of bank conflicts.
-__device__ __forceinline__ void reduce_bc_store(float (&red)[kLanes][kRedStride], const float2 (&dB)[8],
-                                                const float2 (&dC)[8], int lane, float* dst) {
-  float4* row = reinterpret_cast<float4*>(&red[lane][0]);
+// dB | dC of one token summed over the warp's 32 channels, in two steps:
+// every lane writes its channel's 32 values as one row of a buffer
+// (write_bc_row), then, for up to two tokens at once (reduce_bc_pair), lane
+// (rg, cg) adds rows 8 rg .. 8 rg + 7 of columns 4 cg .. 4 cg + 3 in row
+// order and the four row groups are combined by two exchanges (xor 8, then
+// xor 16); lanes 0-7 store the first token's 32 sums (128 bytes), lanes 8-15
+// the second's.  Row r keeps quad q at position q ^ (r % 8), so that both the
+// row writes and the column reads of 8 consecutive lanes touch 8 different
+// 16-byte bank groups.  Batching two tokens halves the warp barriers, which
+// also fence the compiler's scheduling of shared-memory accesses.
+__device__ __forceinline__ void write_bc_row(float4 (&red)[kLanes][8], const float2 (&dB)[8],
+                                             const float2 (&dC)[8], int lane) {
+  const int sw = lane & 7;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    row[q] = make_float4(dB[2 * q].x, dB[2 * q].y, dB[2 * q + 1].x, dB[2 * q + 1].y);
-    row[4 + q] = make_float4(dC[2 * q].x, dC[2 * q].y, dC[2 * q + 1].x, dC[2 * q + 1].y);
+    red[lane][q ^ sw] = make_float4(dB[2 * q].x, dB[2 * q].y, dB[2 * q + 1].x, dB[2 * q + 1].y);
+    red[lane][(4 + q) ^ sw] = make_float4(dC[2 * q].x, dC[2 * q].y, dC[2 * q + 1].x, dC[2 * q + 1].y);
   }
-  __syncwarp();
+}
+
+__device__ __forceinline__ void column_sums(const float4 (&red)[kLanes][8], int lane, float2& s0, float2& s1) {
   const int cg = lane & 7, rg = lane >> 3;
-  float4 s = *reinterpret_cast<const float4*>(&red[rg * 8][4 * cg]);
+  float4 v = red[rg * 8][cg];
+  s0 = make_float2(v.x, v.y);
+  s1 = make_float2(v.z, v.w);
 #pragma unroll
   for (int m = 1; m < 8; ++m) {
-    const float4 v = *reinterpret_cast<const float4*>(&red[rg * 8 + m][4 * cg]);
-    s.x = __fadd_rn(s.x, v.x);
-    s.y = __fadd_rn(s.y, v.y);
-    s.z = __fadd_rn(s.z, v.z);
-    s.w = __fadd_rn(s.w, v.w);
+    v = red[rg * 8 + m][cg ^ m];
+    s0 = __fadd2_rn(s0, make_float2(v.x, v.y));
+    s1 = __fadd2_rn(s1, make_float2(v.z, v.w));
   }
-  __syncwarp();  // every row read: the buffer is free for the next token
+}
+
+__device__ __forceinline__ void rowgroup_sums(float2& s0, float2& s1) {
 #pragma unroll
   for (int m = 8; m <= 16; m <<= 1) {
-    s.x = __fadd_rn(s.x, __shfl_xor_sync(0xffffffffu, s.x, m));
-    s.y = __fadd_rn(s.y, __shfl_xor_sync(0xffffffffu, s.y, m));
-    s.z = __fadd_rn(s.z, __shfl_xor_sync(0xffffffffu, s.z, m));
-    s.w = __fadd_rn(s.w, __shfl_xor_sync(0xffffffffu, s.w, m));
+    const float2 o0 = make_float2(__shfl_xor_sync(0xffffffffu, s0.x, m), __shfl_xor_sync(0xffffffffu, s0.y, m));
+    const float2 o1 = make_float2(__shfl_xor_sync(0xffffffffu, s1.x, m), __shfl_xor_sync(0xffffffffu, s1.y, m));
+    s0 = __fadd2_rn(s0, o0);
+    s1 = __fadd2_rn(s1, o1);
   }
-  if (lane < 8) *reinterpret_cast<float4*>(dst + 4 * lane) = s;
+}
+
+// Rows of token A in red[a], of token B (if two) in red[a ^ 1]; sums to dstA, dstB.
+__device__ __forceinline__ void reduce_bc_pair(float4 (&red)[2][kLanes][8], int a, bool two, int lane,
+                                               float* dstA, float* dstB) {
+  __syncwarp();  // every row written
+  float2 a0, a1, b0 = make_float2(0.0f, 0.0f), b1 = make_float2(0.0f, 0.0f);
+  column_sums(red[a], lane, a0, a1);
+  if (two) column_sums(red[a ^ 1], lane, b0, b1);
+  __syncwarp();  // every row read: the buffers are free again
+  rowgroup_sums(a0, a1);
+  if (two) rowgroup_sums(b0, b1);
+  if (lane < 8) *reinterpret_cast<float4*>(dstA + 4 * lane) = make_float4(a0.x, a0.y, a1.x, a1.y);
+  if (two && lane >= 8 && lane < 16)
+    *reinterpret_cast<float4*>(dstB + 4 * (lane - 8)) = make_float4(b0.x, b0.y, b1.x, b1.y);
 }
 
 // The forward quantities of one token kept for its reverse step.
@@ -179,7 +202,8 @@ struct BwdLane {
 // One sub-tile: `rq` tokens (1..4) starting at tile row r0, entering state
 // hh[0].  xw[0..2] are the three inputs before row r0.
 template <typename IO>
-__device__ __forceinline__ void bwd_subtile(const BwdParams& p, const BwdStage<IO>& S, float (&red)[kLanes][kRedStride],
+__device__ __forceinline__ void bwd_subtile(const BwdParams& p, const BwdStage<IO>& S,
+                                            float4 (&red)[2][kLanes][8],
                                             int lane, bool active, int c, int b, int g, int t0, int r0, int rq,
                                             int edge_from, const Channel& ch, State16 (&hh)[kSub + 1],
                                             float (&xw)[kSub + 3], BwdLane& ln, size_t BL) {
@@ -268,7 +292,12 @@ __device__ __forceinline__ void bwd_subtile(const BwdParams& p, const BwdStage<I
         else
           reinterpret_cast<IO*>(p.dx)[o] = from_f32<IO>(dxv);
       }
-      reduce_bc_store(red, dBv, dCv, lane, p.part_bc + ((size_t)g * BL + (size_t)b * p.seqlen + t) * 32);
+      // tokens 3, 2 and 1, 0 of the sub-tile share one reduction
+      write_bc_row(red[i & 1], dBv, dCv, lane);
+      if ((i & 1) == 0) {
+        float* dst = p.part_bc + ((size_t)g * BL + (size_t)b * p.seqlen + t) * 32;
+        reduce_bc_pair(red, 0, i + 1 < rq, lane, dst, dst + 32);
+      }
     }
   }
 }
@@ -316,7 +345,7 @@ __device__ __forceinline__ void issue_bwd_tile(BwdSmem<IO>& sm, int s, const CUt
 // ---------------------------------------------------------------- reverse sweep
 // grid (n_groups, batch, n_chunks), 32 threads.
 template <typename IO>
-__global__ void __launch_bounds__(kLanes)
+__global__ void __launch_bounds__(kLanes, kBwdMinBlocks)
     scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
                     const __grid_constant__ CUtensorMap tm_dt, const __grid_constant__ CUtensorMap tm_dy,
                     const __grid_constant__ CUtensorMap tm_bc, const __grid_constant__ BwdParams p) {
@@ -504,15 +533,9 @@ struct RevPieceWalk {
   }
 };
 
-// grid ((n_chunks - 1) * n_groups * batch), 32 threads.
 template <typename IO>
-__global__ void __launch_bounds__(kLanes)
-    scan_acarry_kernel(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_dt,
-                       const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_bc,
-                       const __grid_constant__ BwdParams p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  ACarrySmem<IO>& sm = *reinterpret_cast<ACarrySmem<IO>*>(smem_raw + smem_pad128(smem_raw));
-
+__device__ __forceinline__ void acarry_warp(const CUtensorMap& tm_z, const CUtensorMap& tm_dt, const CUtensorMap& tm_dy,
+                                            const CUtensorMap& tm_bc, const BwdParams& p, ACarrySmem<IO>& sm) {
   const int lane = threadIdx.x;
   if (lane == 0) {
     sm.ticket = atomicAdd(p.counters, 1u);
@@ -658,6 +681,31 @@ __global__ void __launch_bounds__(kLanes)
   __threadfence();
   __syncwarp();
   if (lane == 0) atomicExch(ready + j, 1u);
+}
+
+// Both carry passes of the backward in one launch (they are independent, and
+// each alone leaves most of the GPU idle): CTAs [0, n_fwd) run the forward's
+// chunk carries, the rest the adjoint carries.  Each kind takes its tickets
+// from its own counter and waits only on earlier tickets of its own kind, so
+// every awaited warp has started.  grid (n_fwd + n_adj), 32 threads.
+template <typename IO>
+union CarriesSmem {
+  CarrySmem<IO> fwd;
+  ACarrySmem<IO> adj;
+};
+
+template <typename IO>
+__global__ void __launch_bounds__(kLanes)
+    scan_carries_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
+                        const __grid_constant__ CUtensorMap tm_dt, const __grid_constant__ CUtensorMap tm_dy,
+                        const __grid_constant__ CUtensorMap tm_bc, const __grid_constant__ ScanParams fp,
+                        const __grid_constant__ BwdParams bp, unsigned n_fwd) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  CarriesSmem<IO>& sm = *reinterpret_cast<CarriesSmem<IO>*>(smem_raw + smem_pad128(smem_raw));
+  if (blockIdx.x < n_fwd)
+    carry_warp<IO>(tm_x, tm_dt, tm_bc, fp, sm.fwd);
+  else
+    acarry_warp<IO>(tm_z, tm_dt, tm_dy, tm_bc, bp, sm.adj);
 }
 
 // ---------------------------------------------------------------- finishing

@@ -133,7 +133,8 @@ __device__ __forceinline__ float softplus_sel(float v) {
 
 // One tile of the main pass, `rows` tokens, straight-line per token; y is
 // stored where wy holds.  kFull: rows == kT, the loop is unrolled completely.
-template <typename IO, bool kSmall, bool kFull>
+// kY false: the states alone (z, the read-out and y are skipped).
+template <typename IO, bool kSmall, bool kFull, bool kY>
 __device__ __forceinline__ void main_tile(const MainStage<IO>& S, int rows, int lane, bool wy,
                                           const Channel& ch, State16& st, float& xm3, float& xm2, float& xm1,
                                           IO* ytile, int D) {
@@ -146,14 +147,16 @@ __device__ __forceinline__ void main_tile(const MainStage<IO>& S, int rows, int 
     xm2 = xm1;
     xm1 = xv;
     const float dt = softplus_sel<kSmall>(to_f32(S.dt[r][lane]));
-    const float gz = silu(to_f32(S.z[r][lane]));
     float4 Q[8];
     load_quads(&S.bc[r][0], Q);
     Drive16 d;
     drive16_q(d, ch.a2, dt, __fmul_rn(dt, u), Q);
     state16_apply(st, d);
-    const float yv = gate_out(state16_readout_q(st, Q), ch.Dc, u, gz);
-    st_global_if(wy, ytile + (size_t)r * D, from_f32<IO>(yv));
+    if (kY) {
+      const float gz = silu(to_f32(S.z[r][lane]));
+      const float yv = gate_out(state16_readout_q(st, Q), ch.Dc, u, gz);
+      st_global_if(wy, ytile + (size_t)r * D, from_f32<IO>(yv));
+    }
   }
 }
 
@@ -179,8 +182,10 @@ __device__ __forceinline__ void summary_tile(const SummaryStage<IO>& S, int lane
 }
 
 // ---------------------------------------------------------------- main pass
-// grid (n_groups, batch, n_chunks), 32 threads.
-template <typename IO>
+// grid (n_groups, batch, n_chunks), 32 threads.  kY false: no y (and no z):
+// the pass only stores the states entering every tile (p.ckpt), for the
+// backward.
+template <typename IO, bool kY>
 __global__ void __launch_bounds__(kLanes)
     scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
                     const __grid_constant__ CUtensorMap tm_dt, const __grid_constant__ CUtensorMap tm_bc,
@@ -211,15 +216,15 @@ __global__ void __launch_bounds__(kLanes)
   __syncwarp();
 
   const bool stall_test = (p.flags & 1u) != 0;
+  constexpr uint32_t kBytes = (kY ? 3 : 2) * kT * kLanes * sizeof(IO) + kT * kBC * sizeof(float);
   if (lane == 0) {
-    constexpr uint32_t kBytes = 3 * kT * kLanes * sizeof(IO) + kT * kBC * sizeof(float);
     for (int k = 0; k < kStages && k < n_tiles; ++k) {
       if (stall_test && k == 0) continue;  // test switch: this stage never completes
       const uint32_t bar = smem_u32(&sm.full[k]);
       const int tt = t_begin + k * kT;
       mbar_arrive_expect_tx(bar, kBytes);
       tma_load_3d(smem_u32(&sm.stage[k].x[0][0]), &tm_x, c0, tt, b, bar);
-      tma_load_3d(smem_u32(&sm.stage[k].z[0][0]), &tm_z, c0, tt, b, bar);
+      if (kY) tma_load_3d(smem_u32(&sm.stage[k].z[0][0]), &tm_z, c0, tt, b, bar);
       tma_load_3d(smem_u32(&sm.stage[k].dt[0][0]), &tm_dt, c0, tt, b, bar);
       tma_load_3d(smem_u32(&sm.stage[k].bc[0][0]), &tm_bc, 0, tt, b, bar);
     }
@@ -271,20 +276,19 @@ __global__ void __launch_bounds__(kLanes)
     IO* ytile = yrow + (size_t)k * kT * D;
     if (small_dt_tile<IO>(S.dt, t_valid, lane, active)) {
       if (t_valid == kT)
-        main_tile<IO, true, true>(S, kT, lane, wy, ch, st, xm3, xm2, xm1, ytile, D);
+        main_tile<IO, true, true, kY>(S, kT, lane, wy, ch, st, xm3, xm2, xm1, ytile, D);
       else
-        main_tile<IO, true, false>(S, t_valid, lane, wy, ch, st, xm3, xm2, xm1, ytile, D);
+        main_tile<IO, true, false, kY>(S, t_valid, lane, wy, ch, st, xm3, xm2, xm1, ytile, D);
     } else {
-      main_tile<IO, false, false>(S, t_valid, lane, wy, ch, st, xm3, xm2, xm1, ytile, D);
+      main_tile<IO, false, false, kY>(S, t_valid, lane, wy, ch, st, xm3, xm2, xm1, ytile, D);
     }
     __syncwarp();  // every lane is done with stage s
     if (lane == 0 && k + kStages < n_tiles) {
-      constexpr uint32_t kBytes = 3 * kT * kLanes * sizeof(IO) + kT * kBC * sizeof(float);
       const uint32_t bar = smem_u32(&sm.full[s]);
       const int tt = t_begin + (k + kStages) * kT;
       mbar_arrive_expect_tx(bar, kBytes);
       tma_load_3d(smem_u32(&sm.stage[s].x[0][0]), &tm_x, c0, tt, b, bar);
-      tma_load_3d(smem_u32(&sm.stage[s].z[0][0]), &tm_z, c0, tt, b, bar);
+      if (kY) tma_load_3d(smem_u32(&sm.stage[s].z[0][0]), &tm_z, c0, tt, b, bar);
       tma_load_3d(smem_u32(&sm.stage[s].dt[0][0]), &tm_dt, c0, tt, b, bar);
       tma_load_3d(smem_u32(&sm.stage[s].bc[0][0]), &tm_bc, 0, tt, b, bar);
     }
@@ -357,14 +361,11 @@ __device__ __forceinline__ void issue_carry_tile(CarrySmem<IO>& sm, int s, const
   tma_load_3d(smem_u32(&sm.stage[s].bc[0][0]), tbc, 0, tt, b, bar);
 }
 
-// grid ((n_chunks - 1) * n_groups * batch), 32 threads.
+// One warp of the carry pass (the kernel below, or the backward's launch
+// that runs it beside the adjoint carries).
 template <typename IO>
-__global__ void __launch_bounds__(kLanes)
-    scan_carry_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dt,
-                      const __grid_constant__ CUtensorMap tm_bc, const __grid_constant__ ScanParams p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  CarrySmem<IO>& sm = *reinterpret_cast<CarrySmem<IO>*>(smem_raw + smem_pad128(smem_raw));
-
+__device__ __forceinline__ void carry_warp(const CUtensorMap& tm_x, const CUtensorMap& tm_dt, const CUtensorMap& tm_bc,
+                                           const ScanParams& p, CarrySmem<IO>& sm) {
   const int lane = threadIdx.x;
   if (lane == 0) {
     sm.ticket = atomicAdd(p.counters, 1u);
@@ -509,6 +510,15 @@ __global__ void __launch_bounds__(kLanes)
   __threadfence();
   __syncwarp();
   if (lane == 0) atomicExch(ready + j, 1u);
+}
+
+// grid ((n_chunks - 1) * n_groups * batch), 32 threads.
+template <typename IO>
+__global__ void __launch_bounds__(kLanes)
+    scan_carry_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dt,
+                      const __grid_constant__ CUtensorMap tm_bc, const __grid_constant__ ScanParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  carry_warp<IO>(tm_x, tm_dt, tm_bc, p, *reinterpret_cast<CarrySmem<IO>*>(smem_raw + smem_pad128(smem_raw)));
 }
 
 }  // namespace mamba

@@ -3,15 +3,16 @@ fp64 backward oracle.
 
 Tolerance: the forward's bounds (parity.py: max error / rms of the oracle,
 1e-4 for fp32 I/O, 1e-2 for bf16 I/O, bf16 outputs first allowed their own
-rounding), applied channel by channel to every gradient that has a channel
-axis.  Channels are independent recurrences whose gradients can differ in
-scale by large factors (a slowly decaying channel accumulates a larger
-state and adjoint), and a channel's rounding error scales with its own
-magnitude: measured against the rms of the whole tensor, one large channel
-among small ones would look worse than it is, and a small channel's errors
-would be drowned.  Each channel's rms is floored at 1e-3 of the tensor's, so
-that a channel with next to no gradient is held to the tensor's scale.  dB
-and dC sum over all channels and are measured against the whole tensor.
+rounding).  The per-token gradients (dx, dz, ddt_raw) and the state
+gradients (dh0, dconv_state0) are measured channel by channel: channels are
+independent recurrences whose gradients can differ in scale by large
+factors (a slowly decaying channel accumulates a larger state and adjoint),
+and a channel's rounding error scales with its own magnitude, so against
+the rms of the whole tensor one large channel among small ones would look
+worse than it is and a small channel's errors would be drowned.  Each
+channel's rms is floored at 1e-3 of the tensor's.  The parameter gradients
+(one sum over all tokens per element, which may cancel to near zero) and dB,
+dC (sums over all channels) are measured against the whole tensor.
 """
 import numpy as np
 import pytest
@@ -28,8 +29,8 @@ NAMES = {"dx": "dx", "dz": "dz", "ddt_raw": "ddt_raw", "dB": "dB", "dC": "dC", "
          "dDskip": "dD", "dconv_w": "dconv_w", "dconv_b": "dconv_b", "dh0": "dh0",
          "dconv_state0": "dconv_state0"}
 IO_OUTPUTS = ("dx", "dz", "ddt_raw")
-CHANNEL_AXIS = {"dx": 2, "dz": 2, "ddt_raw": 2, "dA_log": 0, "dDskip": 0, "dconv_w": 0, "dconv_b": 0,
-                "dh0": 1, "dconv_state0": 2}
+CHANNEL_AXIS = {"dx": 2, "dz": 2, "ddt_raw": 2, "dh0": 1, "dconv_state0": 2}
+PARAM_AXIS = {"dA_log": 0, "dDskip": 0, "dconv_w": 0, "dconv_b": 0}
 
 
 def assert_close_per_channel(gpu, ref, axis, io, what, rounded_bf16):
@@ -97,10 +98,10 @@ def check(inp, g, what, channels=None, skip=()):
         if k in skip or g.get(k) is None:
             continue
         t = g[k]
+        axis = CHANNEL_AXIS.get(k, PARAM_AXIS.get(k))
+        if channels is not None and axis is not None:
+            t = torch.index_select(t, axis, torch.as_tensor(channels, device=t.device))
         if k in CHANNEL_AXIS:
-            axis = CHANNEL_AXIS[k]
-            if channels is not None:
-                t = torch.index_select(t, axis, torch.as_tensor(channels, device=t.device))
             worst[k] = assert_close_per_channel(t, ref[rk], axis, io, f"{what} {k}",
                                                 rounded_bf16=io == "bf16" and k in IO_OUTPUTS)
         else:
