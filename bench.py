@@ -553,6 +553,7 @@ def main():
     ap.add_argument("--decode-tokens", type=int, default=0, help="fewer decode tokens (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--backward-only", action="store_true", help="the backward block alone (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--n-chunks", type=int, default=0,
                     help="chunk count passed to the library (0: its own plan)")
@@ -576,6 +577,11 @@ def main():
             print(json.dumps(d), flush=True)
         return
     w = workload_of(args)
+    if args.backward_only:
+        b = bench_backward(w, args.steps, args.warmup, local, args.n_chunks)
+        if rank == 0:
+            print(json.dumps(b), flush=True)
+        return
     res, inp, out, ws = bench_prefill(w, args.steps, args.warmup, world, local, args.n_chunks)
     value = job_value(res["elems"], args.steps, world, res["t_ms"])
     hbm, src = peaks()

@@ -147,17 +147,31 @@ __device__ __forceinline__ void write_bc_row(float4 (&red)[kLanes][8], const flo
   }
 }
 
+// Column sums of 8 rows as two interleaved chains (even and odd rows), added
+// at the end: half the dependent latency of one chain, still a fixed order.
 __device__ __forceinline__ void column_sums(const float4 (&red)[kLanes][8], int lane, float2& s0, float2& s1) {
   const int cg = lane & 7, rg = lane >> 3;
-  float4 v = red[rg * 8][cg];
-  s0 = make_float2(v.x, v.y);
-  s1 = make_float2(v.z, v.w);
+  float2 e0, e1, o0, o1;
 #pragma unroll
-  for (int m = 1; m < 8; ++m) {
-    v = red[rg * 8 + m][cg ^ m];
-    s0 = __fadd2_rn(s0, make_float2(v.x, v.y));
-    s1 = __fadd2_rn(s1, make_float2(v.z, v.w));
+  for (int m = 0; m < 8; ++m) {
+    const float4 v = red[rg * 8 + m][cg ^ m];
+    const float2 lo = make_float2(v.x, v.y), hi = make_float2(v.z, v.w);
+    if (m == 0) {
+      e0 = lo;
+      e1 = hi;
+    } else if (m == 1) {
+      o0 = lo;
+      o1 = hi;
+    } else if (m & 1) {
+      o0 = __fadd2_rn(o0, lo);
+      o1 = __fadd2_rn(o1, hi);
+    } else {
+      e0 = __fadd2_rn(e0, lo);
+      e1 = __fadd2_rn(e1, hi);
+    }
   }
+  s0 = __fadd2_rn(e0, o0);
+  s1 = __fadd2_rn(e1, o1);
 }
 
 __device__ __forceinline__ void rowgroup_sums(float2& s0, float2& s1) {
@@ -227,7 +241,11 @@ __device__ __forceinline__ void bwd_subtile(const BwdParams& p, const BwdStage<I
       state16_apply(hh[i + 1], d);
     }
   }
-  // reverse
+  // reverse; row0: element (b, t0 + r0, c) of the (B, L, D) outputs; part0:
+  // row (g, b, t0 + r0) of the dB | dC sums
+  const size_t row0 = ((size_t)b * p.seqlen + t0 + r0) * D + c;
+  float* part0 = p.part_bc + ((size_t)g * BL + (size_t)b * p.seqlen + t0 + r0) * 32;
+  const int cl = active ? c : D - 1;
 #pragma unroll
   for (int i = kSub - 1; i >= 0; --i) {
     if (i < rq) {
@@ -246,7 +264,9 @@ __device__ __forceinline__ void bwd_subtile(const BwdParams& p, const BwdStage<I
       ln.dD = __fmaf_rn(dyss, u, ln.dD);
       const float dtu = __fmul_rn(dt, u);
       const float2 dyss2 = make_float2(dyss, dyss), dtu2 = make_float2(dtu, dtu), dt2 = make_float2(dt, dt);
-      float2 lamB = make_float2(0.0f, 0.0f), ddtA = make_float2(0.0f, 0.0f);
+      // sum_n lam_n B_n and sum_n A2_n w_n as two chains each (pairs 0-3, 4-7)
+      float2 lamB[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+      float2 ddtA[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
       float2 dBv[8], dCv[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -254,17 +274,18 @@ __device__ __forceinline__ void bwd_subtile(const BwdParams& p, const BwdStage<I
         float2 lam = __ffma2_rn(Ck, dyss2, ln.lam.h[k]);
         dCv[k] = __fmul2_rn(hh[i + 1].h[k], dyss2);
         dBv[k] = __fmul2_rn(lam, dtu2);
-        lamB = __ffma2_rn(lam, Bk, lamB);
+        lamB[k >> 2] = __ffma2_rn(lam, Bk, lamB[k >> 2]);
         const float2 xa = __fmul2_rn(dt2, ch.a2[k]);
         const float2 dA = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
         lam = __fmul2_rn(lam, dA);
         const float2 w = __fmul2_rn(lam, hh[i].h[k]);
-        ddtA = __ffma2_rn(ch.a2[k], w, ddtA);
+        ddtA[k >> 2] = __ffma2_rn(ch.a2[k], w, ddtA[k >> 2]);
         ln.Sw.h[k] = __ffma2_rn(dt2, w, ln.Sw.h[k]);
         ln.lam.h[k] = lam;
       }
-      const float sB = __fadd_rn(lamB.x, lamB.y);
-      const float sA = __fadd_rn(ddtA.x, ddtA.y);
+      const float2 lB = __fadd2_rn(lamB[0], lamB[1]), dA2 = __fadd2_rn(ddtA[0], ddtA[1]);
+      const float sB = __fadd_rn(lB.x, lB.y);
+      const float sA = __fadd_rn(dA2.x, dA2.y);
       const float ddt = __fmaf_rn(sA, kLn2, __fmul_rn(sB, u));
       const float du = __fmaf_rn(dyss, ch.Dc, __fmul_rn(sB, dt));
       const float dpre = __fmul_rn(du, f[i].dsil);
@@ -280,22 +301,21 @@ __device__ __forceinline__ void bwd_subtile(const BwdParams& p, const BwdStage<I
       ln.dp3 = ln.dp2;
       ln.dp2 = ln.dp1;
       ln.dp1 = dpre;
-      if (p.dfinal_conv_state != nullptr && t >= p.seqlen - 3 && active)
+      if (p.dfinal_conv_state != nullptr && t >= p.seqlen - 3)  // the same for every lane
         dxv = __fadd_rn(dxv, to_f32(reinterpret_cast<const IO*>(p.dfinal_conv_state)
-                                        [((size_t)b * 3 + (t - (p.seqlen - 3))) * D + c]));
-      const size_t o = ((size_t)b * p.seqlen + t) * D + c;
-      if (active) {
-        reinterpret_cast<IO*>(p.dz)[o] = from_f32<IO>(dzv);
-        reinterpret_cast<IO*>(p.ddt_raw)[o] = from_f32<IO>(__fmul_rn(ddt, f[i].dsig));
-        if (t >= edge_from)
-          p.edge_dx[(((size_t)b * p.n_chunks + blockIdx.z) * 3 + (t - edge_from)) * D + c] = dxv;
-        else
-          reinterpret_cast<IO*>(p.dx)[o] = from_f32<IO>(dxv);
-      }
+                                        [((size_t)b * 3 + (t - (p.seqlen - 3))) * D + cl]));
+      const size_t o = row0 + (size_t)i * D;
+      st_global_if(active, reinterpret_cast<IO*>(p.dz) + o, from_f32<IO>(dzv));
+      st_global_if(active, reinterpret_cast<IO*>(p.ddt_raw) + o, from_f32<IO>(__fmul_rn(ddt, f[i].dsig)));
+      if (t >= edge_from)  // the same for every lane: a chunk's last three tokens
+        st_global_if(active, p.edge_dx + (((size_t)b * p.n_chunks + blockIdx.z) * 3 + (t - edge_from)) * D + c,
+                     dxv);
+      else
+        st_global_if(active, reinterpret_cast<IO*>(p.dx) + o, from_f32<IO>(dxv));
       // tokens 3, 2 and 1, 0 of the sub-tile share one reduction
       write_bc_row(red[i & 1], dBv, dCv, lane);
       if ((i & 1) == 0) {
-        float* dst = p.part_bc + ((size_t)g * BL + (size_t)b * p.seqlen + t) * 32;
+        float* dst = part0 + (size_t)i * 32;
         reduce_bc_pair(red, 0, i + 1 < rq, lane, dst, dst + 32);
       }
     }
