@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import sys
@@ -415,6 +416,83 @@ def oracle_bwd_sample_rate(w, target_s: float):
                                  f"({elems} elements, {t:.1f} s, one thread: dB and dC sum over channels)"}
 
 
+def bf16_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1800.0, 1400.0, "fallback"
+
+
+def layer_weights(B, L, H, D, R, dev, seed):
+    """Seeded layer weights and input: N(0, 1/fan_in) projections (bf16),
+    the scan's parameters as in the workload recipe, dt_proj's bias chosen
+    so that softplus(bias) is log-uniform in [1e-3, 1e-1]."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    bf = torch.bfloat16
+
+    def n(shape, std):
+        return (torch.randn(shape, generator=g, device=dev) * std).to(bf)
+    dt = torch.exp(math.log(1e-3) + torch.rand(D, generator=g, device=dev) * (math.log(1e-1) - math.log(1e-3)))
+    return dict(hidden=n((B, L, H), 1.0), W_in=n((2 * D, H), H ** -0.5),
+                conv_w=torch.rand((D, D_CONV), generator=g, device=dev) - 0.5,
+                conv_b=torch.zeros(D, device=dev), W_x=n((R + 32, D), D ** -0.5), W_dt=n((D, R), R ** -0.5),
+                b_dt=torch.log(torch.expm1(dt)).to(bf),
+                A_log=torch.log(torch.arange(1, D_STATE + 1, device=dev, dtype=torch.float32)).expand(D, D_STATE)
+                .contiguous(),
+                Dskip=torch.ones(D, device=dev), W_out=n((H, D), D ** -0.5))
+
+
+def bench_layer(w, steps, warmup, local, n_chunks_req=0, d_model=4096, dt_rank=256):
+    """The whole Mamba layer (mamba_layer_fwd): in_proj, conv + SiLU, x_proj,
+    dt_proj, the scan and out_proj, at the workload's batch, length and
+    d_inner with d_model = d_inner / 2 (expand 2) and dt_rank = d_model / 16."""
+    from selective_state_space_118_b300 import ops
+    dev = torch.device("cuda", local)
+    B, L, D, H, R = w.batch, w.seqlen, w.d_inner, d_model, dt_rank
+    p = layer_weights(B, L, H, D, R, dev, w.seed + 2000)
+    ws = torch.empty(ops.mamba_layer_workspace_size(B, L, H, D, R, n_chunks_req), device=dev, dtype=torch.uint8)
+    out = torch.empty(B, L, H, device=dev, dtype=torch.bfloat16)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        ops.mamba_layer_fwd(p["hidden"], p["W_in"], p["conv_w"], p["conv_b"], p["W_x"], p["W_dt"], p["b_dt"],
+                            p["A_log"], p["Dskip"], p["W_out"], out=out, workspace=ws, n_chunks=n_chunks_req,
+                            stream=stream)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    assert ops.mamba_last_error(stream) == ops.MAMBA_OK
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with ClockSampler(dev.index) as clk:
+        ev[0].record(stream)
+        for i in range(steps):
+            call()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    t = ev[0].elapsed_time(ev[steps]) / 1e3 / steps
+    flops = 2 * B * L * (H * 2 * D + D * (R + 32) + R * D + D * H)
+    burst, sustained, src = bf16_peaks()
+    n_chunks = ops.mamba_scan_plan(B, L, D, n_chunks_req)["n_chunks"]
+    res = {"metric": "layer tokens/s", "value": B * L / t, "unit": "tokens/s",
+           "config": {"workload": f"mamba_layer_bf16_b{B}_l{L}_h{H}_d{D}_r{R}", "batch": B, "seqlen": L,
+                      "d_model": H, "d_inner": D, "dt_rank": R, "n_chunks": n_chunks,
+                      "weights": "seeded N(0, 1/fan_in), bf16"},
+           "ms_per_call": t * 1e3, "ms_per_call_min": min(per),
+           "roofline": {"bound": "tensor", "achieved": flops / t / 1e12, "peak": sustained, "unit": "TFLOP/s",
+                        "frac": flops / t / 1e12 / sustained, "peak_source": f"{src} (sustained: a long step)",
+                        "flops_per_call": flops,
+                        "note": "projection FLOPs over the whole layer call (the scan and conv included in "
+                                "the time); the GEMMs are cuBLASLt"},
+           "gpu_launches": (2 if n_chunks == 1 else 3) + 1, "library_gemms_per_call": 5, "clocks": clk.summary()}
+    del p, ws, out
+    return res
+
+
 def bench_decode(w, local, replays=3, layers=None, tokens=None):
     """28 layers x 256 tokens, one mamba_step per layer and token, replayed
     from one CUDA graph.  decode steps/s = tokens (for all 64 sequences
@@ -554,6 +632,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--backward-only", action="store_true", help="the backward block alone (profiling)")
+    ap.add_argument("--no-layer", action="store_true")
+    ap.add_argument("--layer-only", action="store_true", help="the layer block alone (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--n-chunks", type=int, default=0,
                     help="chunk count passed to the library (0: its own plan)")
@@ -582,6 +662,11 @@ def main():
         if rank == 0:
             print(json.dumps(b), flush=True)
         return
+    if args.layer_only:
+        b = bench_layer(w, args.steps, args.warmup, local, args.n_chunks)
+        if rank == 0:
+            print(json.dumps(b), flush=True)
+        return
     res, inp, out, ws = bench_prefill(w, args.steps, args.warmup, world, local, args.n_chunks)
     value = job_value(res["elems"], args.steps, world, res["t_ms"])
     hbm, src = peaks()
@@ -606,6 +691,9 @@ def main():
     if not args.no_decode:
         line["decode"] = bench_decode(inputs.DECODE, local, layers=args.decode_layers,
                                       tokens=args.decode_tokens)
+        torch.cuda.empty_cache()
+    if not args.no_layer:
+        line["layer"] = bench_layer(w, max(3, min(args.steps, 20)), 3, local, args.n_chunks)
         torch.cuda.empty_cache()
     if not args.no_backward:
         line["backward"] = bench_backward(w, max(3, min(args.steps, 20)), 3, local, args.n_chunks)

@@ -231,6 +231,72 @@ size_t mamba_scan_bwd_workspace_size(int batch, int seqlen, int d_inner, int n_c
 mamba_status mamba_scan_bwd(const mamba_scan_bwd_args *args, void *stream);
 
 /*
+ * The whole Mamba layer of "实现 › Mamba 层" (MambaBlock.forward): the
+ * projections around the scan as bf16 tensor-core GEMMs, then the scan.
+ * For hidden (B, L, d_model):
+ *
+ *   x | z   = hidden W_in^T            (in_proj: W_in (2D, d_model); rows
+ *                                        0..D-1 give x, D..2D-1 give z)
+ *   u       = silu(conv(x))            (causal depthwise conv as for the scan;
+ *                                        zero inputs before t = 0)
+ *   dt_in | B | C = u W_x^T            (x_proj: W_x (dt_rank + 32, D); per
+ *                                        token dt_rank values, then B's 16,
+ *                                        then C's 16)
+ *   dt_raw  = dt_in W_dt^T + b_dt      (dt_proj: W_dt (D, dt_rank))
+ *   y       = the scan (mamba_scan_fwd) of x, z, dt_raw, B, C
+ *   out     = y W_out^T                (out_proj: W_out (d_model, D))
+ *
+ * Every stored intermediate (x, z, u, the x_proj output, dt_raw, y) and out
+ * is bf16; the GEMMs accumulate in fp32 (cuBLASLt, the one part of the
+ * library not written here), the scan as for mamba_scan_fwd.  The pages'
+ * x_proj yields no C; here it yields dt input, B and C, as in the layer the
+ * pages describe in prose.
+ *
+ *   io                MAMBA_BF16 only
+ *   hidden            (B, L, d_model) bf16
+ *   W_in, W_x, W_dt, W_out   bf16, the nn.Linear weight layouts above
+ *   b_dt              (D) bf16 or NULL (the dt_proj bias)
+ *   conv_w, conv_b, A_log, Dskip   fp32, as for the scan
+ *   out               (B, L, d_model) bf16 output
+ *   u_out             (B, L, D) bf16 or NULL: u, for a caller that needs it
+ *                     (e.g. to keep for the backward of x_proj)
+ *   final_h, final_conv_state   as for the scan (may be NULL)
+ *   workspace         at least mamba_layer_workspace_size() bytes, 256-byte
+ *                     aligned: the intermediates, the scan's workspace and
+ *                     32 MiB of GEMM scratch
+ *   n_chunks          the scan's, as for mamba_scan_fwd
+ *
+ * d_model and dt_rank must be multiples of 8, d_inner of 16.  The first call
+ * creates one cuBLASLt handle for the process (kept until exit); GEMM
+ * algorithms are chosen once per shape.  MAMBA_ERR_CUDA if cuBLASLt refuses
+ * a GEMM.
+ */
+typedef struct mamba_layer_args {
+    int batch, seqlen, d_model, d_inner, dt_rank, d_state, d_conv;
+    mamba_dtype io;
+    const void *hidden;
+    const void *W_in;
+    const float *conv_w, *conv_b;
+    const void *W_x, *W_dt, *b_dt;
+    const float *A_log, *Dskip;
+    const void *W_out;
+    void *out;
+    void *u_out;
+    float *final_h;
+    void *final_conv_state;
+    void *workspace;
+    size_t workspace_bytes;
+    int n_chunks;
+} mamba_layer_args;
+
+/* Bytes of workspace mamba_layer_fwd needs (with_u_out: whether u_out will
+ * be given; without it u lives in the workspace). */
+size_t mamba_layer_workspace_size(int batch, int seqlen, int d_model, int d_inner, int dt_rank, int n_chunks,
+                                  int with_u_out);
+
+mamba_status mamba_layer_fwd(const mamba_layer_args *args, void *stream);
+
+/*
  * Decode: one token through the layer, state updated in place -- the
  * constant-memory recurrence of "Um SSM em uma pagina" (y_t needs only
  * h_{t-1} and x_t).  Bit for bit the same arithmetic as one token of

@@ -18,6 +18,9 @@ scan_chunked(...)  the same scan evaluated chunk by chunk with a carried,
 step(...)          one decode token, state updated in place
 scan_bwd(...)      gradients of sum(y*dy) (+ final-state terms) w.r.t. every
                    input of scan(...)
+layer(...)         the whole Mamba layer: the projections (numpy matmuls in
+                   fp64) around scan(...), with every stored intermediate
+                   rounded to bf16 where the library stores it
 build()            compile ``liboracle.so`` next to this file
 """
 from __future__ import annotations
@@ -205,3 +208,50 @@ def scan_bwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=None,
                             _ptr(conv_state0), _ptr(dy), _ptr(dfinal_h), _ptr(dfinal_conv_state),
                             *[_ptr(out[k]) for k in BWD_NAMES])
     return out
+
+
+def bf16_round(a) -> np.ndarray:
+    """fp64 values rounded to bf16 the way the GPU stores an fp32 result: to
+    fp32 (nearest), then to the upper 16 bits (nearest, ties to even);
+    returned as fp64.  Finite values only."""
+    f = np.ascontiguousarray(np.asarray(a, dtype=np.float64).astype(np.float32))
+    bits = f.view(np.uint32).astype(np.uint64)
+    bits = (bits + 0x7FFF + ((bits >> 16) & 1)) & 0xFFFF0000
+    return bits.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def layer(hidden, W_in, conv_w, conv_b, W_x, W_dt, b_dt, A_log, Dskip, W_out, lib=None):
+    """The Mamba layer of "【大模型】- Jamba 混合 SSM-Transformer", section
+    "实现 > Mamba 层" (MambaBlock.forward), in fp64:
+      x | z = hidden W_in^T (in_proj, rows 0..D-1 then D..2D-1 of W_in)
+      u = silu(conv(x)) (causal depthwise conv, zero inputs before t = 0)
+      dt_in | B | C = u W_x^T (x_proj; per token dt_rank, 16 and 16 values:
+                      the blog's x_proj omits C, the layer it describes has it)
+      dt_raw = dt_in W_dt^T + b_dt (dt_proj with its bias)
+      y = scan(x, z, dt_raw, B, C, ...) (the C oracle above)
+      out = y W_out^T (out_proj)
+    Every quantity the library stores in bf16 (x, z, u, the x_proj output,
+    dt_raw, y, out) is rounded to bf16 here at the same point, so that both
+    sides feed each stage the same kind of values.  Returns a dict with out
+    and the intermediates."""
+    h = f64(hidden)
+    Bsz, L, _ = h.shape
+    Win = f64(W_in)
+    D = Win.shape[0] // 2
+    x = bf16_round(h @ Win[:D].T)
+    z = bf16_round(h @ Win[D:].T)
+    cw = f64(conv_w)
+    cb = np.zeros(D) if conv_b is None else f64(conv_b)
+    xp = np.concatenate([np.zeros((Bsz, 3, D)), x], axis=1)
+    pre = cb + cw[:, 0] * xp[:, 0:L] + cw[:, 1] * xp[:, 1:L + 1] + cw[:, 2] * xp[:, 2:L + 2] + cw[:, 3] * xp[:, 3:L + 3]
+    u = bf16_round(pre / (1.0 + np.exp(-pre)))
+    xdbl = bf16_round(u @ f64(W_x).T)
+    R = f64(W_dt).shape[1]
+    dt_in, Bm, Cm = xdbl[..., :R], xdbl[..., R:R + 16], xdbl[..., R + 16:R + 32]
+    bias = 0.0 if b_dt is None else f64(b_dt)
+    dt_raw = bf16_round(dt_in @ f64(W_dt).T + bias)
+    y, fh, fcs = scan(x, z, dt_raw, np.ascontiguousarray(Bm), np.ascontiguousarray(Cm), A_log, Dskip, conv_w,
+                      conv_b, lib=lib)
+    y = bf16_round(y)
+    out = bf16_round(y @ f64(W_out).T)
+    return dict(out=out, x=x, z=z, u=u, xdbl=xdbl, dt_raw=dt_raw, y=y, final_h=fh, final_conv_state=fcs)

@@ -10,14 +10,15 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmamba_ssm.so")
-SOURCES = ["kernels.cu", "api.cpp", "noalloc.cu"]
-HEADERS = ["ptx.cuh", "ssm_math.cuh", "scan_fwd.cuh", "scan_bwd.cuh", "step.cuh", "params.h", "launch.h"]
+SOURCES = ["kernels.cu", "api.cpp", "noalloc.cu", "gemm.cpp"]
+HEADERS = ["ptx.cuh", "ssm_math.cuh", "scan_fwd.cuh", "scan_bwd.cuh", "step.cuh", "params.h", "launch.h", "gemm.h"]
 PUBLIC_HEADER = os.path.join(os.path.dirname(HERE), "include", "mamba_ssm.h")
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-cudart", "shared",
          "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
+LIBS = ["-lcublasLt"]
 
 
 def _stale() -> bool:
@@ -35,7 +36,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     cmd = [NVCC, *ARCH, *FLAGS, "-shared", "-o", tmp]
     if verbose:
         cmd += ["-Xptxas", "-v"]
-    cmd += [os.path.join(CSRC, f) for f in SOURCES]
+    cmd += [os.path.join(CSRC, f) for f in SOURCES] + LIBS
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed ({r.returncode}):\n{r.stderr}")

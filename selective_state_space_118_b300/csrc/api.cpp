@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "../../include/mamba_ssm.h"
+#include "gemm.h"
 #include "launch.h"
 
 using mamba::IoType;
@@ -200,6 +201,44 @@ BwdWorkspace bwd_workspace_layout(int batch, int seqlen, int d_inner, const Plan
   return w;
 }
 
+// The layer's workspace: x, z, u (unless the caller takes u), the x_proj
+// output (B, L, dt_rank + 32), dt_raw and y, then the scan's workspace, then
+// cuBLASLt's scratch.
+struct LayerWorkspace {
+  size_t x, z, u, xdbl, dt_raw, y, scan, gemm, total;
+  Workspace scan_ws;
+};
+
+LayerWorkspace layer_workspace_layout(int batch, int seqlen, int d_inner, int dt_rank, const Plan& pl,
+                                      bool need_u) {
+  LayerWorkspace w;
+  std::memset(&w, 0, sizeof(w));
+  const size_t rows = (size_t)batch * seqlen, D = d_inner, R = dt_rank;
+  size_t o = 0;
+  const size_t act = round256(rows * D * 2);
+  w.x = o;
+  o += act;
+  w.z = o;
+  o += act;
+  if (need_u) {
+    w.u = o;
+    o += act;
+  }
+  w.xdbl = o;
+  o += round256(rows * (R + 32) * 2);
+  w.dt_raw = o;
+  o += act;
+  w.y = o;
+  o += act;
+  w.scan = o;
+  w.scan_ws = workspace_layout(batch, seqlen, d_inner, pl);
+  o += w.scan_ws.total;
+  w.gemm = o;
+  o += mamba::kGemmWorkspace;
+  w.total = o;
+  return w;
+}
+
 // 3-D tiled map over a (B, L, inner) row-major tensor: box (box_inner, kT, 1).
 bool encode3d(CUtensorMap* m, const void* base, mamba_dtype io, int inner, int L, int B, int box_inner) {
   EncodeTiledFn fn = encode_fn();
@@ -261,7 +300,9 @@ mamba::ScanParams fwd_params(const mamba_scan_args* a, const Plan& pl, const Wor
 }
 
 // The forward kernels: B/C widening, chunk carries (chunked mode), main pass.
-mamba_status launch_forward(const mamba_scan_args* a, const Plan& pl, const Workspace& ws, cudaStream_t stream) {
+// bc_ld: elements from one token's B (and C) row to the next.
+mamba_status launch_forward(const mamba_scan_args* a, const Plan& pl, const Workspace& ws, cudaStream_t stream,
+                            int bc_ld = 16) {
   const size_t B = a->batch;
   float* bc = reinterpret_cast<float*>(static_cast<char*>(a->workspace) + ws.bc);
 
@@ -277,7 +318,7 @@ mamba_status launch_forward(const mamba_scan_args* a, const Plan& pl, const Work
   const mamba::ScanParams p = fwd_params(a, pl, ws, nullptr);
   const IoType io = a->io == MAMBA_BF16 ? IoType::BF16 : IoType::F32;
 
-  if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, stream) != cudaSuccess)
+  if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, bc_ld, stream) != cudaSuccess)
     return MAMBA_ERR_CUDA;
   if (pl.n_chunks > 1) {
     if (cudaMemsetAsync(p.counters, 0, ws.counters_bytes, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
@@ -494,7 +535,7 @@ mamba_status mamba_scan_bwd(const mamba_scan_bwd_args* a, void* stream_v) {
   // 1. B/C rows widened; 2. chunked mode: the forward's chunk carries and the
   // adjoint carries (one launch); 3. the states-only forward pass; 4. the
   // reverse sweep; 5. the edge fix-up and the fixed-order sums
-  if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, stream) != cudaSuccess)
+  if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, 16, stream) != cudaSuccess)
     return MAMBA_ERR_CUDA;
   if (pl.n_chunks > 1) {
     p.acarry = reinterpret_cast<float*>(wsp + ws.acarry);
@@ -513,6 +554,94 @@ mamba_status mamba_scan_bwd(const mamba_scan_bwd_args* a, void* stream_v) {
   if (mamba::launch_bwd(io, maps, p, grid, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
   if (mamba::launch_bwd_finish(io, p, a->dB, a->dC, a->dA_log, a->dDskip, a->dconv_w, a->dconv_b, stream) !=
       cudaSuccess)
+    return MAMBA_ERR_CUDA;
+  return MAMBA_OK;
+}
+
+size_t mamba_layer_workspace_size(int batch, int seqlen, int d_model, int d_inner, int dt_rank, int n_chunks,
+                                  int with_u_out) {
+  if (batch <= 0 || seqlen <= 0 || d_model <= 0 || d_inner <= 0 || d_inner % 16 || dt_rank <= 0 ||
+      n_chunks < 0)
+    return 0;
+  return layer_workspace_layout(batch, seqlen, d_inner, dt_rank, make_plan(batch, seqlen, d_inner, n_chunks),
+                                with_u_out == 0)
+      .total;
+}
+
+mamba_status mamba_layer_fwd(const mamba_layer_args* a, void* stream_v) {
+  if (!a) return MAMBA_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
+  mamba_status st = check_common(a->batch, a->d_inner, a->d_state, a->d_conv, a->io);
+  if (st != MAMBA_OK) return st;
+  if (a->io != MAMBA_BF16) return MAMBA_ERR_UNSUPPORTED;
+  if (a->seqlen <= 0 || a->d_model <= 0 || a->dt_rank <= 0 || a->n_chunks < 0) return MAMBA_ERR_INVALID_ARG;
+  // 16-byte rows for the tensor-core GEMMs
+  if (a->d_model % 8 || a->dt_rank % 8) return MAMBA_ERR_UNSUPPORTED;
+  const void* req[] = {a->hidden, a->W_in, a->conv_w, a->W_x, a->W_dt, a->A_log, a->Dskip, a->W_out, a->out};
+  for (const void* p : req)
+    if (!p || !aligned16(p)) return MAMBA_ERR_INVALID_ARG;
+  const void* opt[] = {a->conv_b, a->b_dt, a->u_out, a->final_h, a->final_conv_state};
+  for (const void* p : opt)
+    if (p && !aligned16(p)) return MAMBA_ERR_INVALID_ARG;
+  if ((long long)a->seqlen * (long long)a->d_inner > (1LL << 40)) return MAMBA_ERR_UNSUPPORTED;
+
+  const Plan pl = make_plan(a->batch, a->seqlen, a->d_inner, a->n_chunks);
+  const LayerWorkspace ws = layer_workspace_layout(a->batch, a->seqlen, a->d_inner, a->dt_rank, pl, !a->u_out);
+  if (!a->workspace || a->workspace_bytes < ws.total) return MAMBA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return MAMBA_ERR_INVALID_ARG;
+  char* wsp = static_cast<char*>(a->workspace);
+  const long M = (long)a->batch * a->seqlen;
+  const int H = a->d_model, D = a->d_inner, R = a->dt_rank, XD = a->dt_rank + 32;
+  void* x = wsp + ws.x;
+  void* z = wsp + ws.z;
+  void* u = a->u_out ? a->u_out : static_cast<void*>(wsp + ws.u);
+  char* xdbl = wsp + ws.xdbl;
+  void* dt_raw = wsp + ws.dt_raw;
+  void* y = wsp + ws.y;
+  void* gws = wsp + ws.gemm;
+  const char* W_in = static_cast<const char*>(a->W_in);
+
+  // in_proj (two halves: x and z, each contiguous), conv + SiLU, x_proj
+  // (dt input | B | C per token), dt_proj with its bias
+  if (!mamba::gemm_bf16(a->hidden, H, W_in, nullptr, x, D, M, D, H, gws, mamba::kGemmWorkspace, stream) ||
+      !mamba::gemm_bf16(a->hidden, H, W_in + (size_t)D * H * 2, nullptr, z, D, M, D, H, gws, mamba::kGemmWorkspace,
+                        stream))
+    return MAMBA_ERR_CUDA;
+  if (mamba::launch_conv_silu(IoType::BF16, x, a->conv_w, a->conv_b, u, a->batch, a->seqlen, D, stream) !=
+      cudaSuccess)
+    return MAMBA_ERR_CUDA;
+  if (!mamba::gemm_bf16(u, D, a->W_x, nullptr, xdbl, XD, M, XD, D, gws, mamba::kGemmWorkspace, stream) ||
+      !mamba::gemm_bf16(xdbl, XD, a->W_dt, a->b_dt, dt_raw, D, M, D, R, gws, mamba::kGemmWorkspace, stream))
+    return MAMBA_ERR_CUDA;
+
+  // the scan, B and C read in place from the x_proj output
+  mamba_scan_args sa;
+  std::memset(&sa, 0, sizeof(sa));
+  sa.batch = a->batch;
+  sa.seqlen = a->seqlen;
+  sa.d_inner = D;
+  sa.d_state = a->d_state;
+  sa.d_conv = a->d_conv;
+  sa.io = MAMBA_BF16;
+  sa.x = x;
+  sa.z = z;
+  sa.dt_raw = dt_raw;
+  sa.Bm = xdbl + (size_t)R * 2;
+  sa.Cm = xdbl + (size_t)(R + 16) * 2;
+  sa.A_log = a->A_log;
+  sa.Dskip = a->Dskip;
+  sa.conv_w = a->conv_w;
+  sa.conv_b = a->conv_b;
+  sa.y = y;
+  sa.final_h = a->final_h;
+  sa.final_conv_state = a->final_conv_state;
+  sa.workspace = wsp + ws.scan;
+  sa.workspace_bytes = ws.scan_ws.total;
+  st = launch_forward(&sa, pl, ws.scan_ws, stream, XD);
+  if (st != MAMBA_OK) return st;
+
+  // out_proj
+  if (!mamba::gemm_bf16(y, D, a->W_out, nullptr, a->out, H, M, H, D, gws, mamba::kGemmWorkspace, stream))
     return MAMBA_ERR_CUDA;
   return MAMBA_OK;
 }

@@ -44,20 +44,20 @@ static cudaError_t launch_summary_t(const CUtensorMap* m, const ScanParams& p, d
 }
 
 template <typename IO>
-static cudaError_t launch_widen_t(const void* Bm, const void* Cm, float* bc, long rows, cudaStream_t s) {
+static cudaError_t launch_widen_t(const void* Bm, const void* Cm, float* bc, long rows, int ld, cudaStream_t s) {
   const long n = rows * 8;
   long blocks = (n + 255) / 256;
   if (blocks > 148L * 16) blocks = 148L * 16;
   if (blocks < 1) blocks = 1;
   bc_widen_kernel<IO><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const IO*>(Bm), static_cast<const IO*>(Cm),
-                                                        bc, rows);
+                                                        bc, rows, ld);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bc_widen(IoType io, const void* Bm, const void* Cm, float* bc, long rows,
+cudaError_t launch_bc_widen(IoType io, const void* Bm, const void* Cm, float* bc, long rows, int ld,
                             cudaStream_t stream) {
-  return io == IoType::BF16 ? launch_widen_t<__nv_bfloat16>(Bm, Cm, bc, rows, stream)
-                            : launch_widen_t<float>(Bm, Cm, bc, rows, stream);
+  return io == IoType::BF16 ? launch_widen_t<__nv_bfloat16>(Bm, Cm, bc, rows, ld, stream)
+                            : launch_widen_t<float>(Bm, Cm, bc, rows, ld, stream);
 }
 
 cudaError_t launch_scan(IoType io, const CUtensorMap maps[4], const ScanParams& p, dim3 grid,
@@ -172,6 +172,83 @@ cudaError_t launch_io_to_f32(IoType io, const void* src, float* dst, long n, cud
         static_cast<const __nv_bfloat16*>(src), dst, n);
   else
     io_to_f32_kernel<float><<<grid_for(n, 256), 256, 0, stream>>>(static_cast<const float*>(src), dst, n);
+  return cudaGetLastError();
+}
+
+// u = silu(conv(x)) for the layer's x_proj (B, L, D), the conv's inputs
+// before t = 0 zero.  A thread owns one 16-byte vector of channels (8 in
+// bf16) over a run of kConvRun tokens of one batch row: its conv taps stay in
+// registers and the window of the last three inputs slides along, so every x
+// is read once (plus three before the run) and every u written once, with
+// 16-byte accesses (a warp covers 512 contiguous bytes of a row).  The
+// arithmetic is the scan's own (conv4, silu), so u equals the scan's internal
+// u before its rounding to the I/O dtype.
+constexpr int kConvRun = 32;
+
+template <typename IO>
+__global__ void __launch_bounds__(128) conv_silu_kernel(const IO* __restrict__ x, const float* __restrict__ conv_w,
+                                                        const float* __restrict__ conv_b, IO* __restrict__ u,
+                                                        int L, int D) {
+  constexpr int kV = 16 / sizeof(IO);  // channels per 16-byte vector
+  const int c0 = (blockIdx.x * blockDim.x + threadIdx.x) * kV;
+  if (c0 >= D) return;
+  const int b = blockIdx.z;
+  const int t0 = blockIdx.y * kConvRun;
+  const int t1 = min(t0 + kConvRun, L);
+  float4 w[kV];
+  float bias[kV];
+#pragma unroll
+  for (int v = 0; v < kV; ++v) {
+    w[v] = __ldg(reinterpret_cast<const float4*>(conv_w + (size_t)(c0 + v) * 4));
+    bias[v] = conv_b ? __ldg(conv_b + c0 + v) : 0.0f;
+  }
+  const IO* xr = x + (size_t)b * L * D + c0;
+  IO* ur = u + (size_t)b * L * D + c0;
+  float m3[kV], m2[kV], m1[kV];
+  {
+    IO in[3][kV];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const int t = t0 - 3 + k;
+      if (t >= 0) {
+        *reinterpret_cast<uint4*>(&in[k][0]) = __ldg(reinterpret_cast<const uint4*>(xr + (size_t)t * D));
+      } else {
+#pragma unroll
+        for (int v = 0; v < kV; ++v) in[k][v] = from_f32<IO>(0.0f);
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < kV; ++v) {
+      m3[v] = to_f32(in[0][v]);
+      m2[v] = to_f32(in[1][v]);
+      m1[v] = to_f32(in[2][v]);
+    }
+  }
+  for (int t = t0; t < t1; ++t) {
+    IO in[kV], out[kV];
+    *reinterpret_cast<uint4*>(in) = __ldg(reinterpret_cast<const uint4*>(xr + (size_t)t * D));
+#pragma unroll
+    for (int v = 0; v < kV; ++v) {
+      const float x0 = to_f32(in[v]);
+      out[v] = from_f32<IO>(silu(conv4(w[v], bias[v], m3[v], m2[v], m1[v], x0)));
+      m3[v] = m2[v];
+      m2[v] = m1[v];
+      m1[v] = x0;
+    }
+    *reinterpret_cast<uint4*>(ur + (size_t)t * D) = *reinterpret_cast<const uint4*>(out);
+  }
+}
+
+cudaError_t launch_conv_silu(IoType io, const void* x, const float* conv_w, const float* conv_b, void* u, int B,
+                             int L, int D, cudaStream_t stream) {
+  const int kV = io == IoType::BF16 ? 8 : 4;
+  const dim3 grid((unsigned)((D / kV + 127) / 128), (unsigned)((L + kConvRun - 1) / kConvRun), (unsigned)B);
+  if (io == IoType::BF16)
+    conv_silu_kernel<__nv_bfloat16><<<grid, 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), conv_w, conv_b,
+                                                              static_cast<__nv_bfloat16*>(u), L, D);
+  else
+    conv_silu_kernel<float><<<grid, 128, 0, stream>>>(static_cast<const float*>(x), conv_w, conv_b,
+                                                      static_cast<float*>(u), L, D);
   return cudaGetLastError();
 }
 

@@ -17,9 +17,13 @@ enum class IoType { F32, BF16 };
 size_t scan_smem_bytes(IoType io);
 size_t summary_smem_bytes(IoType io);
 
-// B (rows, 16), C (rows, 16) in the I/O dtype -> bc (rows, 32) fp32.
-cudaError_t launch_bc_widen(IoType io, const void* Bm, const void* Cm, float* bc, long rows,
+// B, C rows (16 values each, `ld` elements apart) in the I/O dtype -> bc
+// (rows, 32) fp32.
+cudaError_t launch_bc_widen(IoType io, const void* Bm, const void* Cm, float* bc, long rows, int ld,
                             cudaStream_t stream);
+// u = silu(conv(x)), (B, L, D) in the I/O dtype, zero conv inputs before t = 0.
+cudaError_t launch_conv_silu(IoType io, const void* x, const float* conv_w, const float* conv_b, void* u, int B,
+                             int L, int D, cudaStream_t stream);
 // maps: x, z, dt_raw, bc (3-D tiled tensor maps).
 cudaError_t launch_scan(IoType io, const CUtensorMap maps[4], const ScanParams& p, dim3 grid,
                         cudaStream_t stream);

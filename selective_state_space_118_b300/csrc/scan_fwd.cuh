@@ -68,15 +68,18 @@ __device__ __forceinline__ float input_at(const ScanParams& p, int b, long tau, 
 // token rows (64 bytes per token read in bf16).  One TMA box carries both
 // rows; one 128-bit shared load gives a lane the B and C values of one state
 // pair as two aligned register pairs.
+// ld: elements from one token's row of B (and of C) to the next (16 when
+// they are (B, L, 16) tensors; more when they are columns of a wider
+// projection output).
 template <typename IO>
 __global__ void __launch_bounds__(256) bc_widen_kernel(const IO* __restrict__ Bm, const IO* __restrict__ Cm,
-                                                       float* __restrict__ bc, long rows) {
+                                                       float* __restrict__ bc, long rows, int ld) {
   const long n = rows * 8;  // 8 pair quads per row
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
     const long r = i >> 3;
     const int k = (int)(i & 7);
-    const IO* b = Bm + r * kN + 2 * k;
-    const IO* c = Cm + r * kN + 2 * k;
+    const IO* b = Bm + r * ld + 2 * k;
+    const IO* c = Cm + r * ld + 2 * k;
     *reinterpret_cast<float4*>(bc + r * kBC + 4 * k) =
         make_float4(to_f32(b[0]), to_f32(b[1]), to_f32(c[0]), to_f32(c[1]));
   }

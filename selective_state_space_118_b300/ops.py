@@ -27,7 +27,8 @@ D_STATE, D_CONV = 16, 4
 # the functions the public header declares (checked by the tests)
 EXPORTED = ("mamba_scan_workspace_size", "mamba_scan_default_chunks", "mamba_scan_plan", "mamba_scan_fwd",
             "mamba_step", "mamba_last_error", "mamba_status_string", "mamba_abi_version",
-            "mamba_scan_fwd_noalloc", "mamba_scan_bwd_workspace_size", "mamba_scan_bwd")
+            "mamba_scan_fwd_noalloc", "mamba_scan_bwd_workspace_size", "mamba_scan_bwd",
+            "mamba_layer_workspace_size", "mamba_layer_fwd")
 MAMBA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _vp = ctypes.c_void_p
@@ -55,6 +56,16 @@ class BwdArgs(ctypes.Structure):
                 ("dconv_b", _vp), ("dh0", _vp), ("dconv_state0", _vp), ("workspace", _vp),
                 ("workspace_bytes", ctypes.c_size_t), ("n_chunks", ctypes.c_int),
                 ("flags", ctypes.c_uint32), ("wait_timeout_ns", ctypes.c_uint64)]
+
+
+class LayerArgs(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("seqlen", ctypes.c_int), ("d_model", ctypes.c_int),
+                ("d_inner", ctypes.c_int), ("dt_rank", ctypes.c_int), ("d_state", ctypes.c_int),
+                ("d_conv", ctypes.c_int), ("io", ctypes.c_int),
+                ("hidden", _vp), ("W_in", _vp), ("conv_w", _vp), ("conv_b", _vp), ("W_x", _vp),
+                ("W_dt", _vp), ("b_dt", _vp), ("A_log", _vp), ("Dskip", _vp), ("W_out", _vp),
+                ("out", _vp), ("u_out", _vp), ("final_h", _vp), ("final_conv_state", _vp),
+                ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("n_chunks", ctypes.c_int)]
 
 
 class StepArgs(ctypes.Structure):
@@ -107,6 +118,10 @@ def load_library(path: str = LIB_PATH):
         lib.mamba_scan_bwd_workspace_size.restype = ctypes.c_size_t
         lib.mamba_scan_bwd.argtypes = [ctypes.POINTER(BwdArgs), _vp]
         lib.mamba_scan_bwd.restype = ctypes.c_int
+        lib.mamba_layer_workspace_size.argtypes = [ctypes.c_int] * 7
+        lib.mamba_layer_workspace_size.restype = ctypes.c_size_t
+        lib.mamba_layer_fwd.argtypes = [ctypes.POINTER(LayerArgs), _vp]
+        lib.mamba_layer_fwd.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -248,6 +263,44 @@ def mamba_scan_bwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=N
     if st != MAMBA_OK:
         raise MambaError(st, "mamba_scan_bwd")
     return g
+
+
+def mamba_layer_workspace_size(batch: int, seqlen: int, d_model: int, d_inner: int, dt_rank: int,
+                               n_chunks: int = 0, with_u_out: bool = False) -> int:
+    return int(load_library().mamba_layer_workspace_size(batch, seqlen, d_model, d_inner, dt_rank, n_chunks,
+                                                         int(with_u_out)))
+
+
+def mamba_layer_fwd(hidden, W_in, conv_w, conv_b, W_x, W_dt, b_dt, A_log, Dskip, W_out, *, out=None,
+                    u_out=None, final_h=None, final_conv_state=None, workspace=None, n_chunks: int = 0,
+                    stream=None):
+    """The whole Mamba layer (C ABI ``mamba_layer_fwd``): hidden (B,L,H) bf16;
+    W_in (2D,H), W_x (R+32,D), W_dt (D,R), b_dt (D), W_out (H,D) bf16;
+    conv_w (D,4), conv_b (D), A_log (D,16), Dskip (D) fp32.  Returns out
+    (B,L,H) bf16 (u_out, final_h, final_conv_state are filled when given)."""
+    lib = load_library()
+    B, L, H = hidden.shape
+    D = A_log.shape[0]
+    R = W_dt.shape[1]
+    if out is None:
+        out = torch.empty_like(hidden)
+    ws_bytes = mamba_layer_workspace_size(B, L, H, D, R, n_chunks, u_out is not None)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, device=hidden.device, dtype=torch.uint8)
+    a = LayerArgs(batch=B, seqlen=L, d_model=H, d_inner=D, dt_rank=R, d_state=A_log.shape[-1],
+                  d_conv=conv_w.shape[-1], io=_io_code(hidden), hidden=_ptr(hidden), W_in=_ptr(W_in),
+                  conv_w=_ptr(conv_w), conv_b=_ptr(conv_b), W_x=_ptr(W_x), W_dt=_ptr(W_dt), b_dt=_ptr(b_dt),
+                  A_log=_ptr(A_log), Dskip=_ptr(Dskip), W_out=_ptr(W_out), out=_ptr(out), u_out=_ptr(u_out),
+                  final_h=_ptr(final_h), final_conv_state=_ptr(final_conv_state), workspace=_ptr(workspace),
+                  workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
+                  n_chunks=n_chunks)
+    for t in (W_in, W_x, W_dt, b_dt, W_out, out, u_out, final_conv_state):
+        if t is not None and t.dtype != torch.bfloat16:
+            raise TypeError("the layer's activations and projection weights are bf16")
+    st = lib.mamba_layer_fwd(ctypes.byref(a), _stream(stream))
+    if st != MAMBA_OK:
+        raise MambaError(st, "mamba_layer_fwd")
+    return out
 
 
 def mamba_step(h, conv_state, x_t, z_t, dt_raw_t, B_t, C_t, A_log, Dskip, conv_w, conv_b=None,

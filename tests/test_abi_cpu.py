@@ -55,7 +55,8 @@ def _c_layout(tmp_path, struct, fields):
 
 @pytest.mark.parametrize("struct,cls", [("mamba_scan_args", ops.ScanArgs),
                                         ("mamba_step_args", ops.StepArgs),
-                                        ("mamba_scan_bwd_args", ops.BwdArgs)])
+                                        ("mamba_scan_bwd_args", ops.BwdArgs),
+                                        ("mamba_layer_args", ops.LayerArgs)])
 def test_ctypes_structs_match_c_layout(tmp_path, struct, cls):
     fields = [f for f, _ in cls._fields_]
     c = _c_layout(tmp_path, struct, fields)
@@ -133,6 +134,29 @@ def test_bwd_argument_checks(lib):
         ops.MAMBA_ERR_UNSUPPORTED
     assert lib.mamba_scan_bwd(ctypes.byref(ops.BwdArgs(**full)), None) == ops.MAMBA_ERR_WORKSPACE
     assert lib.mamba_scan_bwd(None, None) == ops.MAMBA_ERR_INVALID_ARG
+
+
+def test_layer_argument_checks(lib):
+    base = dict(batch=1, seqlen=8, d_model=64, d_inner=32, dt_rank=8, d_state=16, d_conv=4, io=ops.MAMBA_BF16)
+    assert lib.mamba_layer_fwd(ctypes.byref(ops.LayerArgs(**base)), None) == ops.MAMBA_ERR_INVALID_ARG
+    full = dict(base, hidden=FAKE, W_in=FAKE, conv_w=FAKE, W_x=FAKE, W_dt=FAKE, A_log=FAKE, Dskip=FAKE,
+                W_out=FAKE, out=FAKE)
+    for kw, status in ((dict(io=ops.MAMBA_F32), ops.MAMBA_ERR_UNSUPPORTED),
+                       (dict(dt_rank=12), ops.MAMBA_ERR_UNSUPPORTED),
+                       (dict(d_model=60), ops.MAMBA_ERR_UNSUPPORTED),
+                       (dict(d_inner=24), ops.MAMBA_ERR_UNSUPPORTED),
+                       (dict(seqlen=0), ops.MAMBA_ERR_INVALID_ARG),
+                       (dict(W_x=FAKE + 2), ops.MAMBA_ERR_INVALID_ARG),
+                       (dict(), ops.MAMBA_ERR_WORKSPACE)):
+        assert lib.mamba_layer_fwd(ctypes.byref(ops.LayerArgs(**dict(full, **kw))), None) == status, kw
+    # intermediates (x, z, u, x_proj output, dt_raw, y), the scan's workspace, 32 MiB GEMM scratch
+    B, L, H, D, R = 1, 4096, 64, 32, 8
+    r = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    scan = ops.mamba_scan_workspace_size(B, L, D, 1)
+    assert ops.mamba_layer_workspace_size(B, L, H, D, R, 1, False) == \
+        5 * r(B * L * D * 2) + r(B * L * (R + 32) * 2) + scan + (32 << 20)
+    assert ops.mamba_layer_workspace_size(B, L, H, D, R, 1, True) == \
+        4 * r(B * L * D * 2) + r(B * L * (R + 32) * 2) + scan + (32 << 20)
 
 
 def test_bwd_workspace(lib):

@@ -1,0 +1,132 @@
+"""Pins of the layer oracle (oracle.layer) against things fixed outside it:
+torch's own bf16 rounding and conv1d, and a closed form of the whole layer.
+
+Closed form: with the x half of in_proj zero, the conv sees only its bias,
+so u = silu(conv_b) for every token; then the x_proj output, dt, B and C are
+the same for every token, the layer is time-invariant with constant input,
+and from h0 = 0 each state is a geometric series:
+  h_t[n] = dt B_n u (1 - a_n^(t+1)) / (1 - a_n),   a_n = exp(dt A_n)
+  y_t = (sum_n C_n h_t[n] + D u) silu(z_t),   out_t = y_t W_out^T
+(every stored value rounded to bf16 as the layer stores it).  y alone is
+symmetric in B and C here; the final state (proportional to B) is not.  This pins the
+order of in_proj's halves, the x_proj slices (dt input, B, C), the dt_proj
+bias, x_proj reading u (not x) and the out_proj orientation; a last test
+plants each of those mistakes in a copy of the oracle and checks a pin
+rejects it.
+"""
+import inspect
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+N = 16
+
+
+def bf16(a):
+    return oracle.bf16_round(a)
+
+
+def problem(B=2, L=40, H=24, D=32, R=8, seed=0, zero_x=False):
+    rng = np.random.default_rng(seed)
+    p = dict(hidden=bf16(rng.normal(size=(B, L, H))),
+             W_in=bf16(rng.normal(scale=H ** -0.5, size=(2 * D, H))),
+             conv_w=rng.uniform(-0.5, 0.5, size=(D, 4)),
+             conv_b=rng.normal(scale=0.5, size=D),
+             W_x=bf16(rng.normal(scale=D ** -0.5, size=(R + 32, D))),
+             W_dt=bf16(rng.normal(scale=R ** -0.5, size=(D, R))),
+             b_dt=bf16(rng.uniform(-4.0, -2.5, size=D)),
+             A_log=np.log(np.arange(1, N + 1, dtype=float))[None, :].repeat(D, 0),
+             Dskip=rng.normal(size=D),
+             W_out=bf16(rng.normal(scale=D ** -0.5, size=(H, D))))
+    if zero_x:
+        p["W_in"][:D] = 0.0
+    return p
+
+
+def test_bf16_round_matches_torch():
+    rng = np.random.default_rng(1)
+    v = np.concatenate([rng.normal(size=10000) * 10.0 ** rng.integers(-6, 6, size=10000),
+                        # exact ties between two bf16 values, both parities
+                        (np.arange(1, 200) * 2 + 1) * 2.0 ** -8 + 1.0])
+    ref = torch.tensor(v, dtype=torch.float64).to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle.bf16_round(v), ref)
+
+
+def test_u_matches_torch_conv1d():
+    p = problem(seed=2)
+    r = oracle.layer(**p)
+    x = torch.tensor(r["x"]).permute(0, 2, 1)  # (B, D, L)
+    w = torch.tensor(p["conv_w"]).unsqueeze(1)  # (D, 1, 4)
+    pre = torch.nn.functional.conv1d(x, w, torch.tensor(p["conv_b"]), padding=3, groups=x.shape[1])
+    pre = pre[:, :, :x.shape[2]].permute(0, 2, 1)
+    u = torch.nn.functional.silu(pre).numpy()
+    # both sides round to bf16; the fp64 sums may differ in the last bits,
+    # which can move a value across a rounding boundary: allow one bf16 ulp
+    np.testing.assert_allclose(r["u"], u, rtol=2.0 ** -7, atol=1e-30)
+
+
+def closed_form(p):
+    h, Win = p["hidden"], p["W_in"]
+    D = Win.shape[0] // 2
+    R = p["W_dt"].shape[1]
+    c = p["conv_b"]
+    us = c / (1.0 + np.exp(-c))                          # the scan's own u (fp64)
+    u0 = bf16(us)                                        # x_proj's input (stored bf16)
+    xd = bf16(u0 @ p["W_x"].T)
+    dt_in, Bv, Cv = xd[:R], xd[R:R + 16], xd[R + 16:R + 32]
+    dt_raw = bf16(dt_in @ p["W_dt"].T + p["b_dt"])       # (D,)
+    dt = np.log1p(np.exp(dt_raw))
+    A = -np.exp(p["A_log"])                              # (D, 16)
+    a = np.exp(dt[:, None] * A)
+    L = h.shape[1]
+    t = np.arange(L)[:, None, None]
+    hs = (dt * us)[None, :, None] * Bv[None, None, :] * (1.0 - a[None] ** (t + 1)) / (1.0 - a[None])
+    z = bf16(h @ Win[D:].T)                              # (B, L, D)
+    ss = np.einsum("tdn,n->td", hs, Cv)[None] + p["Dskip"] * us
+    y = bf16(ss * (z / (1.0 + np.exp(-z))))
+    final_h = np.broadcast_to(hs[-1], (h.shape[0],) + hs[-1].shape)  # (B, D, 16)
+    return y, bf16(y @ p["W_out"].T), final_h
+
+
+def test_layer_closed_form():
+    p = problem(seed=3, zero_x=True)
+    r = oracle.layer(**p)
+    y, out, fh = closed_form(p)
+    np.testing.assert_allclose(r["y"], y, rtol=2.0 ** -7, atol=1e-12)
+    np.testing.assert_allclose(r["final_h"], fh, rtol=1e-10, atol=1e-14)
+    rms = np.sqrt(np.mean(out ** 2))
+    assert np.abs(r["out"] - out).max() <= 1e-2 * rms
+
+
+MUTANTS = [
+    ("in_proj halves swapped", "x = bf16_round(h @ Win[:D].T)\n    z = bf16_round(h @ Win[D:].T)",
+     "x = bf16_round(h @ Win[D:].T)\n    z = bf16_round(h @ Win[:D].T)"),
+    ("B and C slices swapped", "xdbl[..., R:R + 16], xdbl[..., R + 16:R + 32]",
+     "xdbl[..., R + 16:R + 32], xdbl[..., R:R + 16]"),
+    ("dt_proj bias dropped", "bias = 0.0 if b_dt is None else f64(b_dt)", "bias = 0.0"),
+    ("x_proj reads x", "xdbl = bf16_round(u @ f64(W_x).T)", "xdbl = bf16_round(x @ f64(W_x).T)"),
+    ("dt input read from the C columns", "dt_in, Bm, Cm = xdbl[..., :R],", "dt_in, Bm, Cm = xdbl[..., 32:R + 32],"),
+]
+
+
+@pytest.mark.parametrize("what,old,new", MUTANTS)
+def test_pins_reject_planted_mistakes(what, old, new):
+    src = inspect.getsource(oracle.layer)
+    assert old in src, what
+    ns = dict(vars(oracle))
+    exec(src.replace(old, new), ns)
+    bad = ns["layer"]
+    p = problem(seed=3, zero_x=True)
+    caught = False
+    try:
+        r = bad(**p)
+        y, out, fh = closed_form(p)
+        rms = np.sqrt(np.mean(out ** 2))
+        caught = (r["out"].shape != out.shape or np.abs(r["out"] - out).max() > 1e-2 * rms
+                  or not np.allclose(r["final_h"], fh, rtol=1e-10, atol=1e-14))
+    except (ValueError, IndexError):
+        caught = True
+    assert caught, what
