@@ -18,6 +18,8 @@ scan_chunked(...)  the same scan evaluated chunk by chunk with a carried,
 step(...)          one decode token, state updated in place
 scan_bwd(...)      gradients of sum(y*dy) (+ final-state terms) w.r.t. every
                    input of scan(...)
+ssd(...)           Mamba-2's scan: heads of P channels sharing one scalar
+                   decay per token, an N x P state per head
 layer(...)         the whole Mamba layer: the projections (numpy matmuls in
                    fp64) around scan(...), with every stored intermediate
                    rounded to bf16 where the library stores it
@@ -65,6 +67,8 @@ def _bind(path: str):
     lib.oracle_step_f64.restype = None
     lib.oracle_scan_bwd_f64.argtypes = [i, i, i, i, i] + [_P] * 25
     lib.oracle_scan_bwd_f64.restype = None
+    lib.oracle_ssd_f64.argtypes = [i] * 6 + [_P] * 10
+    lib.oracle_ssd_f64.restype = None
     return lib
 
 
@@ -255,3 +259,18 @@ def layer(hidden, W_in, conv_w, conv_b, W_x, W_dt, b_dt, A_log, Dskip, W_out, li
     y = bf16_round(y)
     out = bf16_round(y @ f64(W_out).T)
     return dict(out=out, x=x, z=z, u=u, xdbl=xdbl, dt_raw=dt_raw, y=y, final_h=fh, final_conv_state=fcs)
+
+
+def ssd(x, dt_raw, A_log, Bm, Cm, Dskip, z=None, h0=None, lib=None):
+    """Mamba-2's scan (mamba_oracle.c: oracle_ssd_f64, which states it and its
+    page).  x, z (B,L,H,P); dt_raw (B,L,H); A_log, Dskip (H); Bm, Cm
+    (B,L,G,N); h0 (B,H,N,P).  Returns (y (B,L,H,P), final_S (B,H,N,P))."""
+    lib = _load(lib)
+    x, z, dt_raw, A_log, Bm, Cm, Dskip, h0 = map(f64, (x, z, dt_raw, A_log, Bm, Cm, Dskip, h0))
+    B, L, H, P = x.shape
+    G, N = Bm.shape[2], Bm.shape[3]
+    y = np.zeros((B, L, H, P))
+    fs = np.zeros((B, H, N, P))
+    lib.oracle_ssd_f64(B, L, H, P, G, N, _ptr(x), _ptr(z), _ptr(dt_raw), _ptr(A_log), _ptr(Bm), _ptr(Cm),
+                       _ptr(Dskip), _ptr(h0), _ptr(y), _ptr(fs))
+    return y, fs

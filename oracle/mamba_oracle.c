@@ -406,3 +406,56 @@ void oracle_scan_bwd_f64(int batch, int seqlen, int d_inner, int d_state, int d_
         }
     free(hs); free(u); free(pre); free(dt); free(yss); free(din); free(lam);
 }
+
+/*
+ * Mamba-2's structure ("Jamba -- SSM-Transformer Hibrido", ai-engineering.academy,
+ * section "Mamba-3: a linha de base de SSM puro em 2026", items 1 and 2: Mamba-2
+ * reduced the state matrix to a scaled identity and discretises with Euler's
+ * method): the channels come in heads of P that share one scalar decay
+ * exp(dt*A_h) per token, dt and A being per head, and one state matrix of
+ * N x P per head.  For batch row b, head h (group g = h / (H / G) of the B and
+ * C rows), t = 0..L-1:
+ *   dt       = softplus(dt_raw[b,t,h])            (beta 1, threshold 20)
+ *   S[n][p]  = exp(dt * A_h) * S[n][p] + dt * B[b,t,g,n] * x[b,t,h,p]
+ *   y[p]     = (sum_n C[b,t,g,n] * S[n][p] + D_h * x[b,t,h,p]) * silu(z[b,t,h,p])
+ * with A_h = -exp(A_log[h]), S starting at h0[b,h] (or zero), the gate only
+ * when z is given.  Layouts: x, z, y (B,L,H,P); dt_raw (B,L,H); Bm, Cm
+ * (B,L,G,N); A_log, Dskip (H); h0, final_S (B,H,N,P).  Plain sequential fp64.
+ */
+void oracle_ssd_f64(int batch, int seqlen, int heads, int head_dim, int groups, int d_state,
+                    const double *x, const double *z, const double *dt_raw, const double *A_log,
+                    const double *Bm, const double *Cm, const double *Dskip, const double *h0,
+                    double *y, double *final_S)
+{
+    int B = batch, L = seqlen, H = heads, P = head_dim, G = groups, N = d_state;
+    int hpg = H / G;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            int g = h / hpg;
+            double *S = (double *)malloc((size_t)N * P * sizeof(double));
+            for (int i = 0; i < N * P; ++i)
+                S[i] = h0 ? h0[((size_t)b * H + h) * N * P + i] : 0.0;
+            double A = -exp(A_log[h]);
+            for (int t = 0; t < L; ++t) {
+                double dt = softplus(dt_raw[((size_t)b * L + t) * H + h]);
+                double a = exp(dt * A);
+                const double *xr = x + (((size_t)b * L + t) * H + h) * P;
+                const double *Br = Bm + (((size_t)b * L + t) * G + g) * N;
+                const double *Cr = Cm + (((size_t)b * L + t) * G + g) * N;
+                for (int n = 0; n < N; ++n)
+                    for (int p = 0; p < P; ++p)
+                        S[n * P + p] = a * S[n * P + p] + dt * Br[n] * xr[p];
+                for (int p = 0; p < P; ++p) {
+                    double acc = 0.0;
+                    for (int n = 0; n < N; ++n) acc += Cr[n] * S[n * P + p];
+                    double v = acc + Dskip[h] * xr[p];
+                    if (z) v *= silu(z[(((size_t)b * L + t) * H + h) * P + p]);
+                    y[(((size_t)b * L + t) * H + h) * P + p] = v;
+                }
+            }
+            if (final_S)
+                for (int i = 0; i < N * P; ++i) final_S[((size_t)b * H + h) * N * P + i] = S[i];
+            free(S);
+        }
+}
