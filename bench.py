@@ -493,6 +493,68 @@ def bench_layer(w, steps, warmup, local, n_chunks_req=0, d_model=4096, dt_rank=2
     return res
 
 
+def ssd_algorithmic_bytes(B, L, H, G):
+    """Minimum HBM bytes of one Mamba-2 scan call (bf16): x and z read and y
+    written once, dt per (token, head), B and C rows per (token, group)."""
+    return 3 * B * L * H * 64 * 2 + B * L * H * 2 + 2 * B * L * G * D_STATE * 2
+
+
+def bench_ssd(w, steps, warmup, local, heads=None, groups=1):
+    """Mamba-2's chunked scan (mamba2_scan_fwd) on the workload's batch and
+    length, its d_inner cut into heads of 64 channels (Jamba shape: 128
+    heads), one group of B and C rows, with the gate; seeded inputs of the
+    scan workload's distributions (dt log-uniform per (token, head))."""
+    from selective_state_space_118_b300 import ops
+    dev = torch.device("cuda", local)
+    B, L = w.batch, w.seqlen
+    H = heads or w.d_inner // 64
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 3000)
+    bf = torch.bfloat16
+    x = torch.randn((B, L, H, 64), generator=g, device=dev).to(bf)
+    z = torch.randn((B, L, H, 64), generator=g, device=dev).to(bf)
+    u = torch.rand((B, L, H), generator=g, device=dev)
+    dt_raw = torch.log(torch.expm1(torch.exp(math.log(1e-3) + u * (math.log(1e-1) - math.log(1e-3))))).to(bf)
+    Bm = (torch.randn((B, L, groups, D_STATE), generator=g, device=dev) * w.bc_std).to(bf)
+    Cm = (torch.randn((B, L, groups, D_STATE), generator=g, device=dev) * w.bc_std).to(bf)
+    A_log = torch.log(torch.arange(H, device=dev, dtype=torch.float32) % 16 + 1)
+    Dskip = torch.ones(H, device=dev)
+    y = torch.empty_like(x)
+    fs = torch.empty((B, H, D_STATE, 64), device=dev)
+    ws = torch.empty(ops.mamba2_scan_workspace_size(B, L, H), device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        ops.mamba2_scan_fwd(x, dt_raw, A_log, Bm, Cm, Dskip, z, None, y=y, final_state=fs, workspace=ws,
+                            stream=stream)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with ClockSampler(dev.index) as clk:
+        ev[0].record(stream)
+        for i in range(steps):
+            call()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    t = ev[0].elapsed_time(ev[steps]) / 1e3 / steps
+    alg = ssd_algorithmic_bytes(B, L, H, groups)
+    hbm, src = peaks()
+    res = {"metric": "mamba2 scan elements/s", "value": B * L * H * 64 / t, "unit": UNIT,
+           "config": {"workload": f"mamba2_scan_bf16_b{B}_l{L}_h{H}_p64_g{groups}_n16", "batch": B, "seqlen": L,
+                      "heads": H, "head_dim": 64, "groups": groups, "d_state": D_STATE, "chunk": 64},
+           "ms_per_call": t * 1e3, "ms_per_call_min": min(per),
+           "roofline": {"bound": "hbm", "achieved": alg / t / 1e9, "peak": hbm, "unit": "GB/s",
+                        "frac": alg / t / 1e9 / hbm, "peak_source": src, "algorithmic_bytes_per_call": alg,
+                        "note": "whole call (3 kernels); the per-chunk states it writes and reads back are "
+                                "not algorithmic bytes"},
+           "gpu_launches": 3 * steps, "clocks": clk.summary()}
+    del x, z, y, ws
+    return res
+
+
 def bench_decode(w, local, replays=3, layers=None, tokens=None):
     """28 layers x 256 tokens, one mamba_step per layer and token, replayed
     from one CUDA graph.  decode steps/s = tokens (for all 64 sequences
@@ -633,6 +695,8 @@ def main():
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--backward-only", action="store_true", help="the backward block alone (profiling)")
     ap.add_argument("--no-layer", action="store_true")
+    ap.add_argument("--no-ssd", action="store_true")
+    ap.add_argument("--ssd-only", action="store_true", help="the Mamba-2 scan block alone (profiling)")
     ap.add_argument("--layer-only", action="store_true", help="the layer block alone (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--n-chunks", type=int, default=0,
@@ -659,6 +723,11 @@ def main():
     w = workload_of(args)
     if args.backward_only:
         b = bench_backward(w, args.steps, args.warmup, local, args.n_chunks)
+        if rank == 0:
+            print(json.dumps(b), flush=True)
+        return
+    if args.ssd_only:
+        b = bench_ssd(w, args.steps, args.warmup, local)
         if rank == 0:
             print(json.dumps(b), flush=True)
         return
@@ -691,6 +760,9 @@ def main():
     if not args.no_decode:
         line["decode"] = bench_decode(inputs.DECODE, local, layers=args.decode_layers,
                                       tokens=args.decode_tokens)
+        torch.cuda.empty_cache()
+    if not args.no_ssd:
+        line["mamba2"] = bench_ssd(w, max(3, min(args.steps, 20)), 3, local)
         torch.cuda.empty_cache()
     if not args.no_layer:
         line["layer"] = bench_layer(w, max(3, min(args.steps, 20)), 3, local, args.n_chunks)

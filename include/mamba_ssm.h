@@ -297,6 +297,47 @@ size_t mamba_layer_workspace_size(int batch, int seqlen, int d_model, int d_inne
 mamba_status mamba_layer_fwd(const mamba_layer_args *args, void *stream);
 
 /*
+ * Mamba-2's scan ("Jamba -- SSM-Transformer Hibrido", section "Mamba-3: a
+ * linha de base de SSM puro em 2026", items 1-2: the state matrix a scaled
+ * identity, Euler discretisation), in its chunked matrix form on the tensor
+ * cores.  Channels come in heads of head_dim = 64 that share dt and A; each
+ * head keeps a 16 x 64 state S.  For batch row b, head h (group g = h /
+ * (heads / groups) of the B and C rows), t = 0..L-1:
+ *
+ *   dt      = softplus(dt_raw[b,t,h])
+ *   S[n][p] = exp(dt * A_h) S[n][p] + dt B[b,t,g,n] x[b,t,h,p],  A_h = -exp(A_log[h])
+ *   y[p]    = (sum_n C[b,t,g,n] S[n][p] + D_h x[b,t,h,p]) * silu(z[b,t,h,p])
+ *
+ * (the gate only when z is given; S starts at h0, or zero).
+ *
+ *   x, z, y           (B, L, heads, 64) bf16      (z may be NULL)
+ *   dt_raw            (B, L, heads) bf16
+ *   Bm, Cm            (B, L, groups, 16) bf16
+ *   A_log, Dskip      (heads) fp32
+ *   h0, final_state   (B, heads, 16, 64) fp32 or NULL
+ *   workspace         mamba2_scan_workspace_size() bytes, 256-byte aligned:
+ *                     two (B, heads, chunks, 16, 64) fp32 state arrays and the
+ *                     chunks' decay sums (chunks of 64 tokens)
+ *
+ * bf16 I/O only; head_dim 64 and d_state 16 only; heads % groups == 0.
+ * seqlen may be 0 (then final_state = h0, or zeros).
+ */
+typedef struct mamba2_scan_args {
+    int batch, seqlen, heads, head_dim, groups, d_state;
+    mamba_dtype io;
+    const void *x, *z, *dt_raw, *Bm, *Cm;
+    const float *A_log, *Dskip, *h0;
+    void *y;
+    float *final_state;
+    void *workspace;
+    size_t workspace_bytes;
+} mamba2_scan_args;
+
+size_t mamba2_scan_workspace_size(int batch, int seqlen, int heads);
+
+mamba_status mamba2_scan_fwd(const mamba2_scan_args *args, void *stream);
+
+/*
  * Decode: one token through the layer, state updated in place -- the
  * constant-memory recurrence of "Um SSM em uma pagina" (y_t needs only
  * h_{t-1} and x_t).  Bit for bit the same arithmetic as one token of

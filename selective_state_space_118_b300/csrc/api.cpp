@@ -646,6 +646,65 @@ mamba_status mamba_layer_fwd(const mamba_layer_args* a, void* stream_v) {
   return MAMBA_OK;
 }
 
+size_t mamba2_scan_workspace_size(int batch, int seqlen, int heads) {
+  if (batch <= 0 || seqlen <= 0 || heads <= 0) return 0;
+  const size_t nC = ((size_t)seqlen + 63) / 64, BH = (size_t)batch * heads;
+  return 2 * round256(BH * nC * 16 * 64 * sizeof(float)) + round256(BH * nC * sizeof(float));
+}
+
+mamba_status mamba2_scan_fwd(const mamba2_scan_args* a, void* stream_v) {
+  if (!a) return MAMBA_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
+  if (a->batch <= 0 || a->heads <= 0 || a->groups <= 0 || a->seqlen < 0) return MAMBA_ERR_INVALID_ARG;
+  if (a->io != MAMBA_BF16 || a->head_dim != 64 || a->d_state != MAMBA_D_STATE || a->heads % a->groups)
+    return MAMBA_ERR_UNSUPPORTED;
+  if (!a->A_log || !a->Dskip) return MAMBA_ERR_INVALID_ARG;
+  const void* al[] = {a->A_log, a->Dskip, a->h0, a->final_state, a->z};
+  for (const void* p : al)
+    if (p && !aligned16(p)) return MAMBA_ERR_INVALID_ARG;
+  const size_t BH = (size_t)a->batch * a->heads;
+  if (a->seqlen == 0) {
+    if (a->final_state && a->final_state != a->h0) {
+      cudaError_t e = a->h0 ? cudaMemcpyAsync(a->final_state, a->h0, BH * 16 * 64 * sizeof(float),
+                                              cudaMemcpyDeviceToDevice, stream)
+                            : cudaMemsetAsync(a->final_state, 0, BH * 16 * 64 * sizeof(float), stream);
+      if (e != cudaSuccess) return MAMBA_ERR_CUDA;
+    }
+    return MAMBA_OK;
+  }
+  const void* io[] = {a->x, a->dt_raw, a->Bm, a->Cm, a->y};
+  for (const void* p : io)
+    if (!p || !aligned16(p)) return MAMBA_ERR_INVALID_ARG;
+  const size_t need = mamba2_scan_workspace_size(a->batch, a->seqlen, a->heads);
+  if (!a->workspace || a->workspace_bytes < need) return MAMBA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return MAMBA_ERR_INVALID_ARG;
+  const int nC = (a->seqlen + 63) / 64;
+  char* w = static_cast<char*>(a->workspace);
+  const size_t st = round256(BH * nC * 16 * 64 * sizeof(float));
+  mamba::SsdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.batch = a->batch;
+  p.seqlen = a->seqlen;
+  p.heads = a->heads;
+  p.groups = a->groups;
+  p.n_chunks = nC;
+  p.x = a->x;
+  p.z = a->z;
+  p.dt_raw = a->dt_raw;
+  p.Bm = a->Bm;
+  p.Cm = a->Cm;
+  p.A_log = a->A_log;
+  p.Dskip = a->Dskip;
+  p.h0 = a->h0;
+  p.y = a->y;
+  p.final_state = a->final_state;
+  p.S_c = reinterpret_cast<float*>(w);
+  p.S_in = reinterpret_cast<float*>(w + st);
+  p.totals = reinterpret_cast<float*>(w + 2 * st);
+  if (mamba::launch_ssd(p, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+  return MAMBA_OK;
+}
+
 mamba_status mamba_step(const mamba_step_args* a, void* stream_v) {
   if (!a) return MAMBA_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);

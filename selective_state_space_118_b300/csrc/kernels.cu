@@ -5,6 +5,7 @@
 #include "launch.h"
 #include "scan_bwd.cuh"
 #include "scan_fwd.cuh"
+#include "ssd.cuh"
 #include "step.cuh"
 
 namespace mamba {
@@ -249,6 +250,18 @@ cudaError_t launch_conv_silu(IoType io, const void* x, const float* conv_w, cons
   else
     conv_silu_kernel<float><<<grid, 128, 0, stream>>>(static_cast<const float*>(x), conv_w, conv_b,
                                                       static_cast<float*>(u), L, D);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ssd(const SsdParams& p, cudaStream_t stream) {
+  const dim3 grid((unsigned)p.heads, (unsigned)p.n_chunks, (unsigned)p.batch);
+  ssd_states_kernel<<<grid, kSsdThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ssd_pass_kernel<<<dim3((unsigned)p.heads, (unsigned)p.batch), 256, 0, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ssd_output_kernel<<<grid, kSsdThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -64,6 +64,25 @@ struct BwdParams {
   uint64_t timeout_ns;
 };
 
+// Mamba-2's chunked scan (ssd.cuh): heads of 64 channels sharing one scalar
+// decay per token, 16 x 64 state per head, chunks of 64 tokens.
+struct SsdParams {
+  int batch, seqlen, heads, groups, n_chunks;
+  const void* x;          // (B, L, H, 64) bf16
+  const void* z;          // (B, L, H, 64) bf16 or null
+  const void* dt_raw;     // (B, L, H) bf16
+  const void* Bm;         // (B, L, G, 16) bf16
+  const void* Cm;
+  const float* A_log;     // (H)
+  const float* Dskip;     // (H)
+  const float* h0;        // (B, H, 16, 64) or null
+  void* y;                // (B, L, H, 64) bf16
+  float* final_state;     // (B, H, 16, 64) or null
+  float* S_c;             // (B, H, n_chunks, 16, 64): each chunk's end state from zero
+  float* S_in;            // (B, H, n_chunks, 16, 64): the state entering each chunk
+  float* totals;          // (B, H, n_chunks): sum of dt * A over each chunk
+};
+
 struct StepParams {
   int batch, d_inner;
   float* h;           // (B, D, 16)

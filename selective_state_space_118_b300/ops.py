@@ -28,7 +28,8 @@ D_STATE, D_CONV = 16, 4
 EXPORTED = ("mamba_scan_workspace_size", "mamba_scan_default_chunks", "mamba_scan_plan", "mamba_scan_fwd",
             "mamba_step", "mamba_last_error", "mamba_status_string", "mamba_abi_version",
             "mamba_scan_fwd_noalloc", "mamba_scan_bwd_workspace_size", "mamba_scan_bwd",
-            "mamba_layer_workspace_size", "mamba_layer_fwd")
+            "mamba_layer_workspace_size", "mamba_layer_fwd", "mamba2_scan_workspace_size",
+            "mamba2_scan_fwd")
 MAMBA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _vp = ctypes.c_void_p
@@ -66,6 +67,14 @@ class LayerArgs(ctypes.Structure):
                 ("W_dt", _vp), ("b_dt", _vp), ("A_log", _vp), ("Dskip", _vp), ("W_out", _vp),
                 ("out", _vp), ("u_out", _vp), ("final_h", _vp), ("final_conv_state", _vp),
                 ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("n_chunks", ctypes.c_int)]
+
+
+class Mamba2Args(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("seqlen", ctypes.c_int), ("heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("groups", ctypes.c_int), ("d_state", ctypes.c_int),
+                ("io", ctypes.c_int), ("x", _vp), ("z", _vp), ("dt_raw", _vp), ("Bm", _vp), ("Cm", _vp),
+                ("A_log", _vp), ("Dskip", _vp), ("h0", _vp), ("y", _vp), ("final_state", _vp),
+                ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class StepArgs(ctypes.Structure):
@@ -122,6 +131,10 @@ def load_library(path: str = LIB_PATH):
         lib.mamba_layer_workspace_size.restype = ctypes.c_size_t
         lib.mamba_layer_fwd.argtypes = [ctypes.POINTER(LayerArgs), _vp]
         lib.mamba_layer_fwd.restype = ctypes.c_int
+        lib.mamba2_scan_workspace_size.argtypes = [ctypes.c_int] * 3
+        lib.mamba2_scan_workspace_size.restype = ctypes.c_size_t
+        lib.mamba2_scan_fwd.argtypes = [ctypes.POINTER(Mamba2Args), _vp]
+        lib.mamba2_scan_fwd.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -301,6 +314,36 @@ def mamba_layer_fwd(hidden, W_in, conv_w, conv_b, W_x, W_dt, b_dt, A_log, Dskip,
     if st != MAMBA_OK:
         raise MambaError(st, "mamba_layer_fwd")
     return out
+
+
+def mamba2_scan_workspace_size(batch: int, seqlen: int, heads: int) -> int:
+    return int(load_library().mamba2_scan_workspace_size(batch, seqlen, heads))
+
+
+def mamba2_scan_fwd(x, dt_raw, A_log, Bm, Cm, Dskip, z=None, h0=None, *, y=None, final_state=None,
+                    workspace=None, stream=None):
+    """Mamba-2's chunked scan (C ABI ``mamba2_scan_fwd``): x, z (B,L,H,64),
+    dt_raw (B,L,H), Bm, Cm (B,L,G,16) bf16; A_log, Dskip (H) fp32; h0
+    (B,H,16,64) fp32.  Returns (y, final_state)."""
+    lib = load_library()
+    B, L, H, P = x.shape
+    G, N = Bm.shape[2], Bm.shape[3]
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None:
+        final_state = torch.empty((B, H, N, P), device=x.device, dtype=torch.float32)
+    ws_bytes = mamba2_scan_workspace_size(B, L, H)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, device=x.device, dtype=torch.uint8)
+    a = Mamba2Args(batch=B, seqlen=L, heads=H, head_dim=P, groups=G, d_state=N, io=_io_code(x), x=_ptr(x),
+                   z=_ptr(z), dt_raw=_ptr(dt_raw), Bm=_ptr(Bm), Cm=_ptr(Cm), A_log=_ptr(A_log),
+                   Dskip=_ptr(Dskip), h0=_ptr(h0), y=_ptr(y), final_state=_ptr(final_state),
+                   workspace=_ptr(workspace),
+                   workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
+    st = lib.mamba2_scan_fwd(ctypes.byref(a), _stream(stream))
+    if st != MAMBA_OK:
+        raise MambaError(st, "mamba2_scan_fwd")
+    return y, final_state
 
 
 def mamba_step(h, conv_state, x_t, z_t, dt_raw_t, B_t, C_t, A_log, Dskip, conv_w, conv_b=None,

@@ -24,7 +24,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mamba_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(mamba2?_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_binding_functions():
@@ -34,7 +34,7 @@ def test_header_declares_the_binding_functions():
 def test_library_exports_every_declared_symbol(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", ops.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
-    exported = set(re.findall(r"\bT (mamba_\w+)$", out, flags=re.M))
+    exported = set(re.findall(r"\bT (mamba2?_\w+)$", out, flags=re.M))
     missing = set(declared_functions()) - exported
     assert not missing, f"declared but not exported: {missing}"
     for name in declared_functions():
@@ -56,7 +56,8 @@ def _c_layout(tmp_path, struct, fields):
 @pytest.mark.parametrize("struct,cls", [("mamba_scan_args", ops.ScanArgs),
                                         ("mamba_step_args", ops.StepArgs),
                                         ("mamba_scan_bwd_args", ops.BwdArgs),
-                                        ("mamba_layer_args", ops.LayerArgs)])
+                                        ("mamba_layer_args", ops.LayerArgs),
+                                        ("mamba2_scan_args", ops.Mamba2Args)])
 def test_ctypes_structs_match_c_layout(tmp_path, struct, cls):
     fields = [f for f, _ in cls._fields_]
     c = _c_layout(tmp_path, struct, fields)
