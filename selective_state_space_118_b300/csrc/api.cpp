@@ -649,7 +649,8 @@ mamba_status mamba_layer_fwd(const mamba_layer_args* a, void* stream_v) {
 size_t mamba2_scan_workspace_size(int batch, int seqlen, int heads) {
   if (batch <= 0 || seqlen <= 0 || heads <= 0) return 0;
   const size_t nC = ((size_t)seqlen + 63) / 64, BH = (size_t)batch * heads;
-  return 2 * round256(BH * nC * 16 * 64 * sizeof(float)) + round256(BH * nC * sizeof(float));
+  return 2 * round256(BH * nC * 16 * 64 * sizeof(float)) + round256(BH * nC * sizeof(float)) +
+         round256(BH * nC * 64 * 2 * sizeof(float));
 }
 
 mamba_status mamba2_scan_fwd(const mamba2_scan_args* a, void* stream_v) {
@@ -701,6 +702,7 @@ mamba_status mamba2_scan_fwd(const mamba2_scan_args* a, void* stream_v) {
   p.S_c = reinterpret_cast<float*>(w);
   p.S_in = reinterpret_cast<float*>(w + st);
   p.totals = reinterpret_cast<float*>(w + 2 * st);
+  p.cum = reinterpret_cast<float*>(w + 2 * st + round256(BH * nC * sizeof(float)));
   if (mamba::launch_ssd(p, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
   return MAMBA_OK;
 }

@@ -86,13 +86,20 @@ struct SsdTile {
   __nv_bfloat16 x[kSsdQ][kXs];
   __nv_bfloat16 B[kSsdQ][kBs];
   __nv_bfloat16 C[kSsdQ][kBs];
-  float acum[kSsdQ];  // inclusive cumulative sum of dt * A within the chunk
+  float acum[kSsdQ];  // inclusive cumulative sum of dt * A (base 2) within the chunk
   float dt[kSsdQ];
 };
 
+// Offset of value (n, p) of a chunk state in the sliced layout: slice
+// q = 2 n + p / 32 of (batch row, head) bh, chunk c.
+__device__ __forceinline__ size_t ssd_slice(size_t bh, int n, int p, int c, int n_chunks) {
+  return ((bh * 32 + (size_t)(2 * n + p / 32)) * n_chunks + c) * 32 + (p % 32);
+}
+
 // Loads x (and C when with_c) of chunk c of head h, batch row b, computes dt
 // and the cumulative decay exponents.  Ends with a block barrier.
-__device__ __forceinline__ void ssd_load_tile(const SsdParams& p, SsdTile& s, int b, int h, int c, bool with_c) {
+__device__ __forceinline__ void ssd_load_tile(const SsdParams& p, SsdTile& s, int b, int h, int c, bool with_c,
+                                              bool from_cum = false) {
   const int tid = threadIdx.x;
   const int t0 = c * kSsdQ;
   const int H = p.heads, G = p.groups, L = p.seqlen;
@@ -119,6 +126,15 @@ __device__ __forceinline__ void ssd_load_tile(const SsdParams& p, SsdTile& s, in
     }
     *reinterpret_cast<uint4*>(&s.B[r][q * 8]) = vb;
     if (with_c) *reinterpret_cast<uint4*>(&s.C[r][q * 8]) = vc;
+  }
+  if (from_cum) {  // dt and the decay prefix as the states kernel computed them
+    if (tid < kSsdQ) {
+      const float2 v = reinterpret_cast<const float2*>(p.cum)[(((size_t)b * H + h) * p.n_chunks + c) * kSsdQ + tid];
+      s.acum[tid] = v.x;
+      s.dt[tid] = v.y;
+    }
+    __syncthreads();
+    return;
   }
   // dt and dt * A
   const float A2 = a2_from_log(p.A_log[h]);  // A log2(e)
@@ -158,8 +174,11 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_states_kernel(const __grid_co
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float last = s.acum[kSsdQ - 1];
   if (tid < kSsdQ) wj[tid] = __fmul_rn(ex2_approx(__fsub_rn(last, s.acum[tid])), s.dt[tid]);
-  const size_t chunk = ((size_t)b * p.heads + h) * p.n_chunks + c;
+  const size_t bh = (size_t)b * p.heads + h;
+  const size_t chunk = bh * p.n_chunks + c;
   if (tid == 0) p.totals[chunk] = last;
+  if (tid < kSsdQ)  // the output kernel's copy of the chunk's dt and decay prefix
+    reinterpret_cast<float2*>(p.cum)[chunk * kSsdQ + tid] = make_float2(s.acum[tid], s.dt[tid]);
   __syncthreads();
 
   const int g = lane >> 2, t = lane & 3;
@@ -188,71 +207,114 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_states_kernel(const __grid_co
       mma_16816(acc[nt], alo, bx[0], bx[1]);
     }
   }
-  float* out = p.S_c + chunk * kSsdN * kSsdP;
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
     const int col = warp * 16 + nt * 8 + 2 * t;
-    *reinterpret_cast<float2*>(out + (size_t)g * kSsdP + col) = make_float2(acc[nt][0], acc[nt][1]);
-    *reinterpret_cast<float2*>(out + (size_t)(g + 8) * kSsdP + col) = make_float2(acc[nt][2], acc[nt][3]);
+    *reinterpret_cast<float2*>(p.S_c + ssd_slice(bh, g, col, c, p.n_chunks)) = make_float2(acc[nt][0], acc[nt][1]);
+    *reinterpret_cast<float2*>(p.S_c + ssd_slice(bh, g + 8, col, c, p.n_chunks)) =
+        make_float2(acc[nt][2], acc[nt][3]);
   }
 }
 
 // ---------------------------------------------------------------- state passing
-// Per (batch row, head), in chunk order: S_in[0] = h0 (or 0),
-// S_in[c + 1] = 2^(totals[c]) S_in[c] + S_c[c]; the last one is the final
-// state.  fp32; each thread owns 4 of the 1024 values, and keeps the next
-// kPassAhead chunks' loads in flight.  grid (H, B), 256 threads.
-constexpr int kPassAhead = 8;
+// The state entering chunk c is a composition of affine maps, one per earlier
+// chunk: S -> 2^(total_k) S + S_c[k].  Per (batch row, head, slice of 32
+// state values) one CTA of 256 threads takes 256 chunks at a time, thread =
+// chunk: an inclusive scan of the maps over the warp (shuffles), then over
+// the warps (their totals in shared memory, in order), applied to the state
+// entering the block of chunks (the carry, starting at h0); each thread
+// stores the state after the previous chunk.  fp32 throughout; the order of
+// the fp32 operations differs from a serial loop, the values agree to
+// rounding.  grid (32, H, B), 256 threads.
+constexpr int kPassThreads = 256;
 
-constexpr int kPassTotals = 1024;  // chunk decay factors staged in shared memory at a time
-
-__global__ void __launch_bounds__(256) ssd_pass_kernel(const __grid_constant__ SsdParams p) {
-  __shared__ float fac[kPassTotals];
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int tid = threadIdx.x;
+__global__ void __launch_bounds__(kPassThreads) ssd_pass_kernel(const __grid_constant__ SsdParams p) {
+  __shared__ float wa[kPassThreads / 32];
+  __shared__ float wsum[kPassThreads / 32][33];
+  __shared__ float after[kPassThreads][33];
+  __shared__ float carry[32];
+  const int q = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t bh = (size_t)b * p.heads + h;
   const int nC = p.n_chunks;
-  float4 S = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (p.h0) S = *reinterpret_cast<const float4*>(p.h0 + bh * kSsdN * kSsdP + 4 * tid);
-  const float4* src = reinterpret_cast<const float4*>(p.S_c + bh * nC * kSsdN * kSsdP) + tid;
-  float4* dst = reinterpret_cast<float4*>(p.S_in + bh * nC * kSsdN * kSsdP) + tid;
-  const float* tot = p.totals + bh * nC;
-  constexpr int kStride = kSsdN * kSsdP / 4;  // float4s per chunk state
-  float4 ahead[kPassAhead];
+  const int n = q / 2, p0 = 32 * (q % 2);  // this slice: state row n, columns p0 .. p0 + 31
+  const float* src = p.S_c + (bh * 32 + q) * (size_t)nC * 32;
+  float* dst = p.S_in + (bh * 32 + q) * (size_t)nC * 32;
+  if (tid < 32) carry[tid] = p.h0 ? p.h0[bh * kSsdN * kSsdP + n * kSsdP + p0 + tid] : 0.0f;
+  __syncthreads();
+  for (int c0 = 0; c0 < nC; c0 += kPassThreads) {
+    const int c = c0 + tid;
+    const bool valid = c < nC;
+    float a = 1.0f, v[32];
+    if (valid) {
+      a = ex2_approx(__ldg(p.totals + bh * nC + c));
+      const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)c * 32);
 #pragma unroll
-  for (int k = 0; k < kPassAhead; ++k)
-    if (k < nC) ahead[k] = __ldcs(src + (size_t)k * kStride);
-  for (int c0 = 0; c0 < nC; c0 += kPassAhead) {
-    if (c0 % kPassTotals == 0) {  // the next block of decay factors 2^(total)
-      __syncthreads();
-      for (int i = tid; i < kPassTotals && c0 + i < nC; i += 256) fac[i] = ex2_approx(__ldg(tot + c0 + i));
-      __syncthreads();
-    }
-#pragma unroll
-    for (int k = 0; k < kPassAhead; ++k) {
-      const int c = c0 + k;
-      if (c < nC) {
-        __stcs(dst + (size_t)c * kStride, S);
-        const float a = fac[c % kPassTotals];
-        const float4 v = ahead[k];
-        if (c + kPassAhead < nC) ahead[k] = __ldcs(src + (size_t)(c + kPassAhead) * kStride);
-        S.x = __fmaf_rn(a, S.x, v.x);
-        S.y = __fmaf_rn(a, S.y, v.y);
-        S.z = __fmaf_rn(a, S.z, v.z);
-        S.w = __fmaf_rn(a, S.w, v.w);
+      for (int k = 0; k < 8; ++k) {
+        const float4 x4 = __ldcs(s4 + k);
+        v[4 * k] = x4.x;
+        v[4 * k + 1] = x4.y;
+        v[4 * k + 2] = x4.z;
+        v[4 * k + 3] = x4.w;
       }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] = 0.0f;
     }
+    // over the warp: (a, v) <- (a, v) o (a_up, v_up) = (a a_up, a v_up + v)
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float a_up = __shfl_up_sync(0xffffffffu, a, off);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float u = __shfl_up_sync(0xffffffffu, v[k], off);
+        if (lane >= off) v[k] = __fmaf_rn(a, u, v[k]);
+      }
+      if (lane >= off) a = __fmul_rn(a, a_up);
+    }
+    if (lane == 31) {
+      wa[warp] = a;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) wsum[warp][k] = v[k];
+    }
+    __syncthreads();
+    // the earlier warps' maps, in order, then this thread's
+    float pa = 1.0f, pv[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) pv[k] = 0.0f;
+    for (int w = 0; w < warp; ++w) {
+      const float aw = wa[w];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) pv[k] = __fmaf_rn(aw, pv[k], wsum[w][k]);
+      pa = __fmul_rn(pa, aw);
+    }
+    // state after chunk c = (a, v) o (pa, pv) applied to the carry
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      after[tid][k] = __fmaf_rn(__fmul_rn(a, pa), carry[k], __fmaf_rn(a, pv[k], v[k]));
+    __syncthreads();
+    if (valid) {
+      float4* d4 = reinterpret_cast<float4*>(dst + (size_t)c * 32);
+      const float* prev = tid == 0 ? carry : after[tid - 1];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        __stcs(d4 + k, make_float4(prev[4 * k], prev[4 * k + 1], prev[4 * k + 2], prev[4 * k + 3]));
+    }
+    __syncthreads();
+    const int last = min(kPassThreads, nC - c0) - 1;
+    if (tid < 32) carry[tid] = after[last][tid];
+    __syncthreads();
   }
-  if (p.final_state) *reinterpret_cast<float4*>(p.final_state + bh * kSsdN * kSsdP + 4 * tid) = S;
+  if (p.final_state && tid < 32) p.final_state[bh * kSsdN * kSsdP + n * kSsdP + p0 + tid] = carry[tid];
 }
 
 // ---------------------------------------------------------------- output
 // grid (H, n_chunks, B), 128 threads; warp w produces chunk rows 16w .. 16w + 15.
 struct SsdOutSmem {
-  SsdTile t;
+  SsdTile t;                       // x is overwritten by y at the end (each thread its own values)
+  __nv_bfloat16 z[kSsdQ][kXs];
   __nv_bfloat16 s_hi[kSsdN][kXs];  // the entering state split into two bf16 terms
   __nv_bfloat16 s_lo[kSsdN][kXs];
-  float y[kSsdQ][kSsdP + 4];       // fp32 staging for the gated, vectorised store
 };
 
 __global__ void __launch_bounds__(kSsdThreads) ssd_output_kernel(const __grid_constant__ SsdParams p) {
@@ -261,21 +323,32 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_output_kernel(const __grid_co
   const int h = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t chunk = ((size_t)b * p.heads + h) * p.n_chunks + c;
-  {  // the entering state, fp32 -> hi + lo bf16 (s = hi + lo to ~16 bits)
-    const float4* src = reinterpret_cast<const float4*>(p.S_in + chunk * kSsdN * kSsdP);
+  const size_t bh = (size_t)b * p.heads + h;
+  {  // the entering state (32 slices of 32 values), fp32 -> hi + lo bf16 pairs
     for (int i = tid; i < kSsdN * kSsdP / 4; i += kSsdThreads) {
-      const float4 v = src[i];
-      const int n = (4 * i) / kSsdP, q = (4 * i) % kSsdP;
-      const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat16 hi = __float2bfloat16_rn(vv[e]);
-        sm.s_hi[n][q + e] = hi;
-        sm.s_lo[n][q + e] = __float2bfloat16_rn(__fsub_rn(vv[e], __bfloat162float(hi)));
-      }
+      const int e = 4 * i, q = e / 32, n = q / 2, col = 32 * (q % 2) + e % 32;
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(p.S_in + ssd_slice(bh, n, col, c, p.n_chunks)));
+      uint32_t h01, l01, h23, l23;
+      split_bf16(v.x, v.y, h01, l01);
+      split_bf16(v.z, v.w, h23, l23);
+      *reinterpret_cast<uint2*>(&sm.s_hi[n][col]) = make_uint2(h01, h23);
+      *reinterpret_cast<uint2*>(&sm.s_lo[n][col]) = make_uint2(l01, l23);
     }
   }
-  ssd_load_tile(p, s, b, h, c, true);
+  ssd_load_tile(p, s, b, h, c, true, true);
+  // z (for the gate), coalesced like x
+  if (p.z) {
+    const int L = p.seqlen;
+    for (int i = tid; i < kSsdQ * 8; i += kSsdThreads) {
+      const int r = i >> 3, qq = i & 7;
+      const int tt = c * kSsdQ + r;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (tt < L) v = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.z) +
+                                                          (((size_t)b * L + tt) * p.heads + h) * kSsdP) + qq);
+      *reinterpret_cast<uint4*>(&sm.z[r][qq * 8]) = v;
+    }
+  }
+  __syncthreads();
 
   const int g = lane >> 2, t = lane & 3;
   const int i0 = warp * 16 + g, i1 = i0 + 8;  // this thread's two rows
@@ -339,46 +412,42 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_output_kernel(const __grid_co
     mma_16816(Yo[2 * np], ca, bl_[0], bl_[1]);
     mma_16816(Yo[2 * np + 1], ca, bl_[2], bl_[3]);
   }
-  // y = Y + 2^(acum_i) Yo + D x, staged in fp32
+  // y = (Y + 2^(acum_i) Yo + D x) silu(z), written over this thread's own x
+  // values once every warp is done reading x
+  __syncthreads();
   const float e0 = ex2_approx(s.acum[i0]), e1 = ex2_approx(s.acum[i1]);
   const float Dh = p.Dskip[h];
+  const bool gate = p.z != nullptr;
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
     const int col = nt * 8 + 2 * t;
-    const float2 x0 = unpack_bf16(*reinterpret_cast<const uint32_t*>(&s.x[i0][col]));
-    const float2 x1 = unpack_bf16(*reinterpret_cast<const uint32_t*>(&s.x[i1][col]));
-    sm.y[i0][col] = __fmaf_rn(Dh, x0.x, __fmaf_rn(e0, Yo[nt][0], Y[nt][0]));
-    sm.y[i0][col + 1] = __fmaf_rn(Dh, x0.y, __fmaf_rn(e0, Yo[nt][1], Y[nt][1]));
-    sm.y[i1][col] = __fmaf_rn(Dh, x1.x, __fmaf_rn(e1, Yo[nt][2], Y[nt][2]));
-    sm.y[i1][col + 1] = __fmaf_rn(Dh, x1.y, __fmaf_rn(e1, Yo[nt][3], Y[nt][3]));
+    uint32_t* w0 = reinterpret_cast<uint32_t*>(&s.x[i0][col]);
+    uint32_t* w1 = reinterpret_cast<uint32_t*>(&s.x[i1][col]);
+    const float2 x0 = unpack_bf16(*w0), x1 = unpack_bf16(*w1);
+    float y00 = __fmaf_rn(Dh, x0.x, __fmaf_rn(e0, Yo[nt][0], Y[nt][0]));
+    float y01 = __fmaf_rn(Dh, x0.y, __fmaf_rn(e0, Yo[nt][1], Y[nt][1]));
+    float y10 = __fmaf_rn(Dh, x1.x, __fmaf_rn(e1, Yo[nt][2], Y[nt][2]));
+    float y11 = __fmaf_rn(Dh, x1.y, __fmaf_rn(e1, Yo[nt][3], Y[nt][3]));
+    if (gate) {
+      const float2 z0 = unpack_bf16(*reinterpret_cast<const uint32_t*>(&sm.z[i0][col]));
+      const float2 z1 = unpack_bf16(*reinterpret_cast<const uint32_t*>(&sm.z[i1][col]));
+      y00 = __fmul_rn(y00, silu(z0.x));
+      y01 = __fmul_rn(y01, silu(z0.y));
+      y10 = __fmul_rn(y10, silu(z1.x));
+      y11 = __fmul_rn(y11, silu(z1.y));
+    }
+    *w0 = pack_bf16(y00, y01);
+    *w1 = pack_bf16(y10, y11);
   }
   __syncthreads();
-  // gate and store: 8 channels (16 bytes) per access
+  // store: 8 channels (16 bytes) per access
   const int H = p.heads, L = p.seqlen;
   for (int i = tid; i < kSsdQ * 8; i += kSsdThreads) {
     const int r = i >> 3, q = i & 7;
     const int tt = c * kSsdQ + r;
-    if (tt >= L) continue;
-    const size_t o = (((size_t)b * L + tt) * H + h) * kSsdP + q * 8;
-    float v[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = sm.y[r][q * 8 + e];
-    if (p.z) {
-      const uint4 zz = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.z) + o));
-      const uint32_t zw[4] = {zz.x, zz.y, zz.z, zz.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 zf = unpack_bf16(zw[e]);
-        v[2 * e] = __fmul_rn(v[2 * e], silu(zf.x));
-        v[2 * e + 1] = __fmul_rn(v[2 * e + 1], silu(zf.y));
-      }
-    }
-    uint4 out;
-    out.x = pack_bf16(v[0], v[1]);
-    out.y = pack_bf16(v[2], v[3]);
-    out.z = pack_bf16(v[4], v[5]);
-    out.w = pack_bf16(v[6], v[7]);
-    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + o) = out;
+    if (tt < L)
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + (((size_t)b * L + tt) * H + h) * kSsdP + q * 8) =
+          *reinterpret_cast<const uint4*>(&s.x[r][q * 8]);
   }
 }
 
