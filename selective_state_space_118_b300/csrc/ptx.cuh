@@ -139,6 +139,16 @@ __device__ __forceinline__ void st_global_if(bool pred, __nv_bfloat16* p, __nv_b
                "h"(__bfloat16_as_ushort(v)), "r"((unsigned)pred));
 }
 
+// ---------------------------------------------------------------- cp.async
+// 16 bytes global -> shared, asynchronous (L2 only); src_bytes 0 writes 16
+// zero bytes and reads nothing (src must still be a valid address).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool read) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(read ? 16 : 0)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ---------------------------------------------------------------- MUFU
 // 2^x, flushing subnormal inputs/results to zero.
 __device__ __forceinline__ float ex2_approx(float x) {

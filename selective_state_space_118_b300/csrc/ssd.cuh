@@ -96,60 +96,61 @@ __device__ __forceinline__ size_t ssd_slice(size_t bh, int n, int p, int c, int 
   return ((bh * 32 + (size_t)(2 * n + p / 32)) * n_chunks + c) * 32 + (p % 32);
 }
 
-// Loads x (and C when with_c) of chunk c of head h, batch row b, computes dt
-// and the cumulative decay exponents.  Ends with a block barrier.
+// Loads x, B (and C and z when given) of chunk c of head h, batch row b into
+// shared memory with asynchronous 16-byte copies (zero past the sequence's
+// end), and dt with the decay prefix: computed here (from_cum false), or read
+// from the states kernel's copy.  `more`, run while the copies fly, lets the
+// caller put its own loads in flight too.  Ends with a block barrier.
+template <typename More>
 __device__ __forceinline__ void ssd_load_tile(const SsdParams& p, SsdTile& s, int b, int h, int c, bool with_c,
-                                              bool from_cum = false) {
+                                              bool from_cum, __nv_bfloat16 (*zt)[kXs], More more) {
   const int tid = threadIdx.x;
   const int t0 = c * kSsdQ;
   const int H = p.heads, G = p.groups, L = p.seqlen;
   const int g = h / (H / G);
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  // x: 64 rows of 128 bytes = 8 uint4 each
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(p.x);
+  const __nv_bfloat16* zb = static_cast<const __nv_bfloat16*>(p.z);
+  // x (and z): 64 rows of 128 bytes = 8 pieces of 16 bytes each
   for (int i = tid; i < kSsdQ * 8; i += kSsdThreads) {
     const int r = i >> 3, q = i & 7;
     const int t = t0 + r;
-    uint4 v = zero;
-    if (t < L) v = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.x) +
-                                                        (((size_t)b * L + t) * H + h) * kSsdP) + q);
-    *reinterpret_cast<uint4*>(&s.x[r][q * 8]) = v;
+    const bool in = t < L;
+    const size_t o = (((size_t)b * L + (in ? t : 0)) * H + h) * kSsdP + q * 8;
+    cp_async16(smem_u32(&s.x[r][q * 8]), xb + o, in);
+    if (zt) cp_async16(smem_u32(&zt[r][q * 8]), zb + o, in);
   }
-  // B (and C): 64 rows of 32 bytes = 2 uint4 each
+  // B (and C): 64 rows of 32 bytes = 2 pieces each
+  const __nv_bfloat16* Bb = static_cast<const __nv_bfloat16*>(p.Bm);
+  const __nv_bfloat16* Cb = static_cast<const __nv_bfloat16*>(p.Cm);
   for (int i = tid; i < kSsdQ * 2; i += kSsdThreads) {
     const int r = i >> 1, q = i & 1;
     const int t = t0 + r;
-    uint4 vb = zero, vc = zero;
-    if (t < L) {
-      const size_t o = (((size_t)b * L + t) * G + g) * kSsdN;
-      vb = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.Bm) + o) + q);
-      if (with_c) vc = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.Cm) + o) + q);
-    }
-    *reinterpret_cast<uint4*>(&s.B[r][q * 8]) = vb;
-    if (with_c) *reinterpret_cast<uint4*>(&s.C[r][q * 8]) = vc;
+    const bool in = t < L;
+    const size_t o = (((size_t)b * L + (in ? t : 0)) * G + g) * kSsdN + q * 8;
+    cp_async16(smem_u32(&s.B[r][q * 8]), Bb + o, in);
+    if (with_c) cp_async16(smem_u32(&s.C[r][q * 8]), Cb + o, in);
   }
+  more();
   if (from_cum) {  // dt and the decay prefix as the states kernel computed them
     if (tid < kSsdQ) {
       const float2 v = reinterpret_cast<const float2*>(p.cum)[(((size_t)b * H + h) * p.n_chunks + c) * kSsdQ + tid];
       s.acum[tid] = v.x;
       s.dt[tid] = v.y;
     }
+    cp_async_wait_all();
     __syncthreads();
     return;
   }
-  // dt and dt * A
-  const float A2 = a2_from_log(p.A_log[h]);  // A log2(e)
-  float dA = 0.0f;
+  // dt and dt * A, then the inclusive prefix sum over the 64 tokens: two
+  // warps, then warp 1 adds warp 0's total
   if (tid < kSsdQ) {
+    const float A2 = a2_from_log(p.A_log[h]);  // A log2(e)
     const int t = t0 + tid;
     float dt = 0.0f;
     if (t < L) dt = softplus(to_f32(static_cast<const __nv_bfloat16*>(p.dt_raw)[((size_t)b * L + t) * H + h]));
     s.dt[tid] = dt;
-    dA = __fmul_rn(dt, A2);  // in base 2
-  }
-  // inclusive prefix sum over the 64 tokens: two warps, then warp 1 adds warp 0's total
-  if (tid < kSsdQ) {
+    float v = __fmul_rn(dt, A2);  // in base 2
     const int lane = tid & 31;
-    float v = dA;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float u = __shfl_up_sync(0xffffffffu, v, o);
@@ -157,6 +158,7 @@ __device__ __forceinline__ void ssd_load_tile(const SsdParams& p, SsdTile& s, in
     }
     s.acum[tid] = v;
   }
+  cp_async_wait_all();
   __syncthreads();
   if (tid >= 32 && tid < kSsdQ) s.acum[tid] = __fadd_rn(s.acum[tid], s.acum[31]);
   __syncthreads();
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_states_kernel(const __grid_co
   __shared__ __align__(128) SsdTile s;
   __shared__ float wj[kSsdQ];
   const int h = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
-  ssd_load_tile(p, s, b, h, c, false);
+  ssd_load_tile(p, s, b, h, c, false, false, nullptr, [] {});
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float last = s.acum[kSsdQ - 1];
   if (tid < kSsdQ) wj[tid] = __fmul_rn(ex2_approx(__fsub_rn(last, s.acum[tid])), s.dt[tid]);
@@ -219,19 +221,32 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_states_kernel(const __grid_co
 // ---------------------------------------------------------------- state passing
 // The state entering chunk c is a composition of affine maps, one per earlier
 // chunk: S -> 2^(total_k) S + S_c[k].  Per (batch row, head, slice of 32
-// state values) one CTA of 256 threads takes 256 chunks at a time, thread =
-// chunk: an inclusive scan of the maps over the warp (shuffles), then over
-// the warps (their totals in shared memory, in order), applied to the state
-// entering the block of chunks (the carry, starting at h0); each thread
-// stores the state after the previous chunk.  fp32 throughout; the order of
-// the fp32 operations differs from a serial loop, the values agree to
-// rounding.  grid (32, H, B), 256 threads.
+// state values) one CTA of 256 threads takes 1024 chunks at a time, four
+// consecutive ones per thread: each thread composes its four maps, an
+// exclusive scan of those compositions runs over the warp (shuffles) and over
+// the warps (their totals in shared memory, in order), the result is applied
+// to the state entering the block of chunks (the carry, starting at h0), and
+// each thread walks its four chunks storing the state entering each.  fp32
+// throughout; the order of the fp32 operations differs from a serial loop,
+// the values agree to rounding.  grid (32, H, B), 256 threads.
 constexpr int kPassThreads = 256;
+constexpr int kPassPer = 4;
+
+__device__ __forceinline__ void ssd_load_slice(const float* src, float (&v)[32]) {
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float4 x4 = __ldcg(s4 + k);
+    v[4 * k] = x4.x;
+    v[4 * k + 1] = x4.y;
+    v[4 * k + 2] = x4.z;
+    v[4 * k + 3] = x4.w;
+  }
+}
 
 __global__ void __launch_bounds__(kPassThreads) ssd_pass_kernel(const __grid_constant__ SsdParams p) {
   __shared__ float wa[kPassThreads / 32];
   __shared__ float wsum[kPassThreads / 32][33];
-  __shared__ float after[kPassThreads][33];
   __shared__ float carry[32];
   const int q = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -240,28 +255,28 @@ __global__ void __launch_bounds__(kPassThreads) ssd_pass_kernel(const __grid_con
   const int n = q / 2, p0 = 32 * (q % 2);  // this slice: state row n, columns p0 .. p0 + 31
   const float* src = p.S_c + (bh * 32 + q) * (size_t)nC * 32;
   float* dst = p.S_in + (bh * 32 + q) * (size_t)nC * 32;
+  const float* tot = p.totals + bh * nC;
   if (tid < 32) carry[tid] = p.h0 ? p.h0[bh * kSsdN * kSsdP + n * kSsdP + p0 + tid] : 0.0f;
   __syncthreads();
-  for (int c0 = 0; c0 < nC; c0 += kPassThreads) {
-    const int c = c0 + tid;
-    const bool valid = c < nC;
+  for (int c0 = 0; c0 < nC; c0 += kPassThreads * kPassPer) {
+    const int cb = c0 + tid * kPassPer;  // this thread's first chunk
+    // this thread's chunks composed: (a, v) = f_cb+3 o ... o f_cb
     float a = 1.0f, v[32];
-    if (valid) {
-      a = ex2_approx(__ldg(p.totals + bh * nC + c));
-      const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)c * 32);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float4 x4 = __ldcs(s4 + k);
-        v[4 * k] = x4.x;
-        v[4 * k + 1] = x4.y;
-        v[4 * k + 2] = x4.z;
-        v[4 * k + 3] = x4.w;
+    for (int k = 0; k < 32; ++k) v[k] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kPassPer; ++j) {
+      const int c = cb + j;
+      if (c < nC) {
+        const float aj = ex2_approx(__ldg(tot + c));
+        float sj[32];
+        ssd_load_slice(src + (size_t)c * 32, sj);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = __fmaf_rn(aj, v[k], sj[k]);
+        a = __fmul_rn(aj, a);
       }
-    } else {
-#pragma unroll
-      for (int k = 0; k < 32; ++k) v[k] = 0.0f;
     }
-    // over the warp: (a, v) <- (a, v) o (a_up, v_up) = (a a_up, a v_up + v)
+    // inclusive over the warp: (a, v) <- (a, v) o (a_up, v_up) = (a a_up, a v_up + v)
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const float a_up = __shfl_up_sync(0xffffffffu, a, off);
@@ -277,32 +292,50 @@ __global__ void __launch_bounds__(kPassThreads) ssd_pass_kernel(const __grid_con
 #pragma unroll
       for (int k = 0; k < 32; ++k) wsum[warp][k] = v[k];
     }
-    __syncthreads();
-    // the earlier warps' maps, in order, then this thread's
-    float pa = 1.0f, pv[32];
+    // exclusive: the lane before's inclusive (lane 0: the identity)
+    a = __shfl_up_sync(0xffffffffu, a, 1);
 #pragma unroll
-    for (int k = 0; k < 32; ++k) pv[k] = 0.0f;
+    for (int k = 0; k < 32; ++k) v[k] = __shfl_up_sync(0xffffffffu, v[k], 1);
+    if (lane == 0) {
+      a = 1.0f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] = 0.0f;
+    }
+    __syncthreads();
+    // the earlier warps' maps in order, then this thread's exclusive map,
+    // applied to the carry: the state entering this thread's first chunk
+    float pa = 1.0f, S[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) S[k] = 0.0f;
     for (int w = 0; w < warp; ++w) {
       const float aw = wa[w];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) pv[k] = __fmaf_rn(aw, pv[k], wsum[w][k]);
+      for (int k = 0; k < 32; ++k) S[k] = __fmaf_rn(aw, S[k], wsum[w][k]);
       pa = __fmul_rn(pa, aw);
     }
-    // state after chunk c = (a, v) o (pa, pv) applied to the carry
 #pragma unroll
-    for (int k = 0; k < 32; ++k)
-      after[tid][k] = __fmaf_rn(__fmul_rn(a, pa), carry[k], __fmaf_rn(a, pv[k], v[k]));
-    __syncthreads();
-    if (valid) {
-      float4* d4 = reinterpret_cast<float4*>(dst + (size_t)c * 32);
-      const float* prev = tid == 0 ? carry : after[tid - 1];
+    for (int k = 0; k < 32; ++k) S[k] = __fmaf_rn(a, __fmaf_rn(pa, carry[k], S[k]), v[k]);
+    // walk this thread's chunks
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        __stcs(d4 + k, make_float4(prev[4 * k], prev[4 * k + 1], prev[4 * k + 2], prev[4 * k + 3]));
+    for (int j = 0; j < kPassPer; ++j) {
+      const int c = cb + j;
+      if (c < nC) {
+        float4* d4 = reinterpret_cast<float4*>(dst + (size_t)c * 32);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) __stcs(d4 + k, make_float4(S[4 * k], S[4 * k + 1], S[4 * k + 2], S[4 * k + 3]));
+        const float aj = ex2_approx(__ldg(tot + c));
+        float sj[32];
+        ssd_load_slice(src + (size_t)c * 32, sj);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) S[k] = __fmaf_rn(aj, S[k], sj[k]);
+      }
     }
-    __syncthreads();
-    const int last = min(kPassThreads, nC - c0) - 1;
-    if (tid < 32) carry[tid] = after[last][tid];
+    __syncthreads();  // everyone has read the carry
+    const int last = (min(nC - c0, kPassThreads * kPassPer) - 1) / kPassPer;
+    if (tid == last) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) carry[k] = S[k];
+    }
     __syncthreads();
   }
   if (p.final_state && tid < 32) p.final_state[bh * kSsdN * kSsdP + n * kSsdP + p0 + tid] = carry[tid];
@@ -315,6 +348,7 @@ struct SsdOutSmem {
   __nv_bfloat16 z[kSsdQ][kXs];
   __nv_bfloat16 s_hi[kSsdN][kXs];  // the entering state split into two bf16 terms
   __nv_bfloat16 s_lo[kSsdN][kXs];
+  float fdt[kSsdThreads / 32][kSsdQ];  // per warp: 2^(ref - acum_j) dt_j
 };
 
 __global__ void __launch_bounds__(kSsdThreads) ssd_output_kernel(const __grid_constant__ SsdParams p) {
@@ -324,31 +358,25 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_output_kernel(const __grid_co
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t chunk = ((size_t)b * p.heads + h) * p.n_chunks + c;
   const size_t bh = (size_t)b * p.heads + h;
-  {  // the entering state (32 slices of 32 values), fp32 -> hi + lo bf16 pairs
-    for (int i = tid; i < kSsdN * kSsdP / 4; i += kSsdThreads) {
-      const int e = 4 * i, q = e / 32, n = q / 2, col = 32 * (q % 2) + e % 32;
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(p.S_in + ssd_slice(bh, n, col, c, p.n_chunks)));
+  // tiles by asynchronous copies; meanwhile the entering state (32 slices of
+  // 32 values), fp32 -> hi + lo bf16 pairs
+  ssd_load_tile(p, s, b, h, c, true, true, p.z ? sm.z : nullptr, [&] {
+    float4 v[kSsdN * kSsdP / 4 / kSsdThreads];
+#pragma unroll
+    for (int k = 0; k < kSsdN * kSsdP / 4 / kSsdThreads; ++k) {
+      const int e = 4 * (tid + k * kSsdThreads), q = e / 32, n = q / 2, col = 32 * (q % 2) + e % 32;
+      v[k] = __ldcs(reinterpret_cast<const float4*>(p.S_in + ssd_slice(bh, n, col, c, p.n_chunks)));
+    }
+#pragma unroll
+    for (int k = 0; k < kSsdN * kSsdP / 4 / kSsdThreads; ++k) {
+      const int e = 4 * (tid + k * kSsdThreads), q = e / 32, n = q / 2, col = 32 * (q % 2) + e % 32;
       uint32_t h01, l01, h23, l23;
-      split_bf16(v.x, v.y, h01, l01);
-      split_bf16(v.z, v.w, h23, l23);
+      split_bf16(v[k].x, v[k].y, h01, l01);
+      split_bf16(v[k].z, v[k].w, h23, l23);
       *reinterpret_cast<uint2*>(&sm.s_hi[n][col]) = make_uint2(h01, h23);
       *reinterpret_cast<uint2*>(&sm.s_lo[n][col]) = make_uint2(l01, l23);
     }
-  }
-  ssd_load_tile(p, s, b, h, c, true, true);
-  // z (for the gate), coalesced like x
-  if (p.z) {
-    const int L = p.seqlen;
-    for (int i = tid; i < kSsdQ * 8; i += kSsdThreads) {
-      const int r = i >> 3, qq = i & 7;
-      const int tt = c * kSsdQ + r;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (tt < L) v = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.z) +
-                                                          (((size_t)b * L + tt) * p.heads + h) * kSsdP) + qq);
-      *reinterpret_cast<uint4*>(&sm.z[r][qq * 8]) = v;
-    }
-  }
-  __syncthreads();
+  });
 
   const int g = lane >> 2, t = lane & 3;
   const int i0 = warp * 16 + g, i1 = i0 + 8;  // this thread's two rows
@@ -359,6 +387,21 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_output_kernel(const __grid_co
     ldsm_x4(ca, smem_u32(&s.C[warp * 16 + (m & 1) * 8 + r][(m >> 1) * 8]));
   }
   // G = C B^T over the columns j <= this warp's last row, masked and scaled
+  // by the decay 2^(acum_i - acum_j) dt_j.  Where the warp's 16 rows span a
+  // decay of at most 2^60 (ref: acum at its first row), the factor splits
+  // as 2^(acum_i - ref) * 2^(ref - acum_j): one exponential per row and one
+  // per column (shared through fdt) instead of one per pair; neither factor
+  // overflows, and a product that underflows is one far below fp32's
+  // precision of the sum.  Otherwise each pair takes its own exponential.
+  const float ref = s.acum[warp * 16];
+  const bool split = __fsub_rn(ref, s.acum[warp * 16 + 15]) <= 60.0f;  // the same for the whole warp
+  if (split) {
+    for (int j = lane; j < warp * 16 + 16; j += 32)
+      sm.fdt[warp][j] = __fmul_rn(ex2_approx(__fsub_rn(ref, s.acum[j])), s.dt[j]);
+    __syncwarp();
+  }
+  const float a0 = s.acum[i0], a1 = s.acum[i1];
+  const float r0 = ex2_approx(__fsub_rn(a0, ref)), r1 = ex2_approx(__fsub_rn(a1, ref));
   float G[8][4];
 #pragma unroll
   for (int jt = 0; jt < 8; ++jt) {
@@ -367,13 +410,21 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_output_kernel(const __grid_co
       uint32_t bb[2];
       ldsm_x2(bb, smem_u32(&s.B[jt * 8 + (lane & 7)][(lane >> 3 & 1) * 8]));
       mma_16816(G[jt], ca, bb[0], bb[1]);
-      const float a0 = s.acum[i0], a1 = s.acum[i1];
+      const int j0 = jt * 8 + 2 * t;
+      if (split) {
+        const float2 f = *reinterpret_cast<const float2*>(&sm.fdt[warp][j0]);
+        G[jt][0] = j0 <= i0 ? __fmul_rn(__fmul_rn(G[jt][0], r0), f.x) : 0.0f;
+        G[jt][1] = j0 + 1 <= i0 ? __fmul_rn(__fmul_rn(G[jt][1], r0), f.y) : 0.0f;
+        G[jt][2] = j0 <= i1 ? __fmul_rn(__fmul_rn(G[jt][2], r1), f.x) : 0.0f;
+        G[jt][3] = j0 + 1 <= i1 ? __fmul_rn(__fmul_rn(G[jt][3], r1), f.y) : 0.0f;
+      } else {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int j = jt * 8 + 2 * t + e;
-        const float aj = s.acum[j], dtj = s.dt[j];
-        G[jt][e] = j <= i0 ? __fmul_rn(G[jt][e], __fmul_rn(ex2_approx(__fsub_rn(a0, aj)), dtj)) : 0.0f;
-        G[jt][2 + e] = j <= i1 ? __fmul_rn(G[jt][2 + e], __fmul_rn(ex2_approx(__fsub_rn(a1, aj)), dtj)) : 0.0f;
+        for (int e = 0; e < 2; ++e) {
+          const int j = j0 + e;
+          const float aj = s.acum[j], dtj = s.dt[j];
+          G[jt][e] = j <= i0 ? __fmul_rn(G[jt][e], __fmul_rn(ex2_approx(__fsub_rn(a0, aj)), dtj)) : 0.0f;
+          G[jt][2 + e] = j <= i1 ? __fmul_rn(G[jt][2 + e], __fmul_rn(ex2_approx(__fsub_rn(a1, aj)), dtj)) : 0.0f;
+        }
       }
     }
   }

@@ -76,3 +76,16 @@ def test_ssd_seqlen_zero_and_errors():
     with pytest.raises(ops.MambaError) as e:
         ops.mamba2_scan_fwd(x, p["dt_raw"], p["A_log"], p["Bm"], p["Cm"], p["Dskip"])
     assert e.value.status == ops.MAMBA_ERR_UNSUPPORTED
+
+
+def test_ssd_large_dt_fast_decay():
+    """dt up to ~5 with A down to -16: a 16-token row block spans far more
+    than 2^60 of decay, so the output kernel takes its exact per-pair decay
+    path (the split path covers the other cases above)."""
+    p = case(2, 300, 4, 2, seed=11, dt_lo=0.5, dt_hi=5.0)
+    p["A_log"] = torch.log(torch.tensor([1.0, 4.0, 10.0, 16.0], device="cuda"))
+    y, fs = run(p)
+    torch.cuda.synchronize()
+    yr, fsr = oracle.ssd(**p)
+    assert_close(y, yr, "bf16", "large dt y")
+    assert_close(fs, fsr, "bf16", "large dt final state", fp32_output=True)
