@@ -221,30 +221,19 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_states_kernel(const __grid_co
 // ---------------------------------------------------------------- state passing
 // The state entering chunk c is a composition of affine maps, one per earlier
 // chunk: S -> 2^(total_k) S + S_c[k].  Per (batch row, head, slice of 32
-// state values) one CTA of 256 threads takes 1024 chunks at a time, four
-// consecutive ones per thread: each thread composes its four maps, an
-// exclusive scan of those compositions runs over the warp (shuffles) and over
-// the warps (their totals in shared memory, in order), the result is applied
-// to the state entering the block of chunks (the carry, starting at h0), and
-// each thread walks its four chunks storing the state entering each.  fp32
-// throughout; the order of the fp32 operations differs from a serial loop,
-// the values agree to rounding.  grid (32, H, B), 256 threads.
+// state values) one CTA of 256 threads takes 256 chunks at a time, thread =
+// chunk: an exclusive scan of the maps over the warp (shuffles) and over the
+// warps (their totals in shared memory, in order), applied to the state
+// entering the block of chunks (the carry, starting at h0), gives the state
+// entering each chunk.  Each thread copies its chunk's slice into its own
+// row of shared memory asynchronously and, once it has read it, starts the
+// copy of its chunk in the next block, which then flies during the scan.
+// fp32 throughout; the order of the fp32 operations differs from a serial
+// loop, the values agree to rounding.  grid (32, H, B), 256 threads.
 constexpr int kPassThreads = 256;
-constexpr int kPassPer = 4;
-
-__device__ __forceinline__ void ssd_load_slice(const float* src, float (&v)[32]) {
-  const float4* s4 = reinterpret_cast<const float4*>(src);
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float4 x4 = __ldcg(s4 + k);
-    v[4 * k] = x4.x;
-    v[4 * k + 1] = x4.y;
-    v[4 * k + 2] = x4.z;
-    v[4 * k + 3] = x4.w;
-  }
-}
 
 __global__ void __launch_bounds__(kPassThreads) ssd_pass_kernel(const __grid_constant__ SsdParams p) {
+  __shared__ __align__(16) float stage[kPassThreads][32];
   __shared__ float wa[kPassThreads / 32];
   __shared__ float wsum[kPassThreads / 32][33];
   __shared__ float carry[32];
@@ -256,26 +245,26 @@ __global__ void __launch_bounds__(kPassThreads) ssd_pass_kernel(const __grid_con
   const float* src = p.S_c + (bh * 32 + q) * (size_t)nC * 32;
   float* dst = p.S_in + (bh * 32 + q) * (size_t)nC * 32;
   const float* tot = p.totals + bh * nC;
+  const uint32_t row = smem_u32(&stage[tid][0]);
+  auto fetch = [&](int c) {  // this thread's slice of chunk c (zeros past the end)
+    const bool in = c < nC;
+    const float* s = src + (size_t)(in ? c : 0) * 32;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) cp_async16(row + 16 * k, s + 4 * k, in);
+  };
   if (tid < 32) carry[tid] = p.h0 ? p.h0[bh * kSsdN * kSsdP + n * kSsdP + p0 + tid] : 0.0f;
+  fetch(tid);
+  float a_next = tid < nC ? ex2_approx(__ldg(tot + tid)) : 1.0f;
   __syncthreads();
-  for (int c0 = 0; c0 < nC; c0 += kPassThreads * kPassPer) {
-    const int cb = c0 + tid * kPassPer;  // this thread's first chunk
-    // this thread's chunks composed: (a, v) = f_cb+3 o ... o f_cb
-    float a = 1.0f, v[32];
+  for (int c0 = 0; c0 < nC; c0 += kPassThreads) {
+    const int c = c0 + tid;
+    cp_async_wait_all();
+    float a = a_next, v[32];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) v[k] = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kPassPer; ++j) {
-      const int c = cb + j;
-      if (c < nC) {
-        const float aj = ex2_approx(__ldg(tot + c));
-        float sj[32];
-        ssd_load_slice(src + (size_t)c * 32, sj);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = __fmaf_rn(aj, v[k], sj[k]);
-        a = __fmul_rn(aj, a);
-      }
-    }
+    for (int k = 0; k < 32; ++k) v[k] = stage[tid][k];
+    const float a_own = a;
+    fetch(c + kPassThreads);  // the next block's copy flies during the scan
+    a_next = c + kPassThreads < nC ? ex2_approx(__ldg(tot + c + kPassThreads)) : 1.0f;
     // inclusive over the warp: (a, v) <- (a, v) o (a_up, v_up) = (a a_up, a v_up + v)
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -303,7 +292,7 @@ __global__ void __launch_bounds__(kPassThreads) ssd_pass_kernel(const __grid_con
     }
     __syncthreads();
     // the earlier warps' maps in order, then this thread's exclusive map,
-    // applied to the carry: the state entering this thread's first chunk
+    // applied to the carry: the state entering chunk c
     float pa = 1.0f, S[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) S[k] = 0.0f;
@@ -315,29 +304,26 @@ __global__ void __launch_bounds__(kPassThreads) ssd_pass_kernel(const __grid_con
     }
 #pragma unroll
     for (int k = 0; k < 32; ++k) S[k] = __fmaf_rn(a, __fmaf_rn(pa, carry[k], S[k]), v[k]);
-    // walk this thread's chunks
+    if (c < nC) {
+      float4* d4 = reinterpret_cast<float4*>(dst + (size_t)c * 32);
 #pragma unroll
-    for (int j = 0; j < kPassPer; ++j) {
-      const int c = cb + j;
-      if (c < nC) {
-        float4* d4 = reinterpret_cast<float4*>(dst + (size_t)c * 32);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) __stcs(d4 + k, make_float4(S[4 * k], S[4 * k + 1], S[4 * k + 2], S[4 * k + 3]));
-        const float aj = ex2_approx(__ldg(tot + c));
-        float sj[32];
-        ssd_load_slice(src + (size_t)c * 32, sj);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) S[k] = __fmaf_rn(aj, S[k], sj[k]);
-      }
+      for (int k = 0; k < 8; ++k) __stcs(d4 + k, make_float4(S[4 * k], S[4 * k + 1], S[4 * k + 2], S[4 * k + 3]));
     }
-    __syncthreads();  // everyone has read the carry
-    const int last = (min(nC - c0, kPassThreads * kPassPer) - 1) / kPassPer;
-    if (tid == last) {
+    __syncthreads();  // everyone has read the carry and the warp totals
+    if (c == min(nC, c0 + kPassThreads) - 1) {  // the block's last chunk: the new carry
+      const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)c * 32);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) carry[k] = S[k];
+      for (int k = 0; k < 8; ++k) {
+        const float4 x4 = __ldcg(s4 + k);
+        carry[4 * k] = __fmaf_rn(a_own, S[4 * k], x4.x);
+        carry[4 * k + 1] = __fmaf_rn(a_own, S[4 * k + 1], x4.y);
+        carry[4 * k + 2] = __fmaf_rn(a_own, S[4 * k + 2], x4.z);
+        carry[4 * k + 3] = __fmaf_rn(a_own, S[4 * k + 3], x4.w);
+      }
     }
     __syncthreads();
   }
+  cp_async_wait_all();  // the last, unused copy lands before the block ends
   if (p.final_state && tid < 32) p.final_state[bh * kSsdN * kSsdP + n * kSsdP + p0 + tid] = carry[tid];
 }
 
