@@ -258,7 +258,7 @@ cudaError_t launch_ssd(const SsdParams& p, cudaStream_t stream) {
   ssd_states_kernel<<<grid, kSsdThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  ssd_pass_kernel<<<dim3(32u, (unsigned)p.heads, (unsigned)p.batch), kPassThreads, 0, stream>>>(p);
+  ssd_pass_kernel<<<dim3(32u / kPassSlices, (unsigned)p.heads, (unsigned)p.batch), 32 * kPassSlices, 0, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ssd_output_kernel<<<grid, kSsdThreads, 0, stream>>>(p);

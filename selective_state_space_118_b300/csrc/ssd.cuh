@@ -219,112 +219,50 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_states_kernel(const __grid_co
 }
 
 // ---------------------------------------------------------------- state passing
-// The state entering chunk c is a composition of affine maps, one per earlier
-// chunk: S -> 2^(total_k) S + S_c[k].  Per (batch row, head, slice of 32
-// state values) one CTA of 256 threads takes 256 chunks at a time, thread =
-// chunk: an exclusive scan of the maps over the warp (shuffles) and over the
-// warps (their totals in shared memory, in order), applied to the state
-// entering the block of chunks (the carry, starting at h0), gives the state
-// entering each chunk.  Each thread copies its chunk's slice into its own
-// row of shared memory asynchronously and, once it has read it, starts the
-// copy of its chunk in the next block, which then flies during the scan.
-// fp32 throughout; the order of the fp32 operations differs from a serial
-// loop, the values agree to rounding.  grid (32, H, B), 256 threads.
-constexpr int kPassThreads = 256;
+// The state entering chunk c: S_in[0] = h0 (or 0), S_in[c + 1] = 2^(total_c)
+// S_in[c] + S_c[c], in fp32.  One thread per state value walks the chunks in
+// order; a warp holds one slice (32 values), so each step's loads and stores
+// are 128 contiguous bytes, and each thread keeps kPassAhead chunks' loads in
+// flight (the chain itself is one fma per chunk).  The chunks' decay factors
+// 2^(total) are staged in shared memory, kPassBlock at a time.
+// grid (32 / kPassSlices, H, B), 32 * kPassSlices threads.
+constexpr int kPassSlices = 4;
+constexpr int kPassAhead = 16;
+constexpr int kPassBlock = 512;
 
-__global__ void __launch_bounds__(kPassThreads) ssd_pass_kernel(const __grid_constant__ SsdParams p) {
-  __shared__ __align__(16) float stage[kPassThreads][32];
-  __shared__ float wa[kPassThreads / 32];
-  __shared__ float wsum[kPassThreads / 32][33];
-  __shared__ float carry[32];
-  const int q = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__global__ void __launch_bounds__(32 * kPassSlices) ssd_pass_kernel(const __grid_constant__ SsdParams p) {
+  __shared__ float fac[kPassBlock];
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int q = blockIdx.x * kPassSlices + (tid >> 5);  // this warp's slice
   const size_t bh = (size_t)b * p.heads + h;
   const int nC = p.n_chunks;
-  const int n = q / 2, p0 = 32 * (q % 2);  // this slice: state row n, columns p0 .. p0 + 31
-  const float* src = p.S_c + (bh * 32 + q) * (size_t)nC * 32;
-  float* dst = p.S_in + (bh * 32 + q) * (size_t)nC * 32;
+  const int n = q / 2, col = 32 * (q % 2) + lane;  // this thread's state value (row n, column col)
+  const float* src = p.S_c + (bh * 32 + q) * (size_t)nC * 32 + lane;
+  float* dst = p.S_in + (bh * 32 + q) * (size_t)nC * 32 + lane;
   const float* tot = p.totals + bh * nC;
-  const uint32_t row = smem_u32(&stage[tid][0]);
-  auto fetch = [&](int c) {  // this thread's slice of chunk c (zeros past the end)
-    const bool in = c < nC;
-    const float* s = src + (size_t)(in ? c : 0) * 32;
+  float S = p.h0 ? p.h0[bh * kSsdN * kSsdP + n * kSsdP + col] : 0.0f;
+  float ahead[kPassAhead];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) cp_async16(row + 16 * k, s + 4 * k, in);
-  };
-  if (tid < 32) carry[tid] = p.h0 ? p.h0[bh * kSsdN * kSsdP + n * kSsdP + p0 + tid] : 0.0f;
-  fetch(tid);
-  float a_next = tid < nC ? ex2_approx(__ldg(tot + tid)) : 1.0f;
-  __syncthreads();
-  for (int c0 = 0; c0 < nC; c0 += kPassThreads) {
-    const int c = c0 + tid;
-    cp_async_wait_all();
-    float a = a_next, v[32];
-#pragma unroll
-    for (int k = 0; k < 32; ++k) v[k] = stage[tid][k];
-    const float a_own = a;
-    fetch(c + kPassThreads);  // the next block's copy flies during the scan
-    a_next = c + kPassThreads < nC ? ex2_approx(__ldg(tot + c + kPassThreads)) : 1.0f;
-    // inclusive over the warp: (a, v) <- (a, v) o (a_up, v_up) = (a a_up, a v_up + v)
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float a_up = __shfl_up_sync(0xffffffffu, a, off);
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float u = __shfl_up_sync(0xffffffffu, v[k], off);
-        if (lane >= off) v[k] = __fmaf_rn(a, u, v[k]);
-      }
-      if (lane >= off) a = __fmul_rn(a, a_up);
-    }
-    if (lane == 31) {
-      wa[warp] = a;
-#pragma unroll
-      for (int k = 0; k < 32; ++k) wsum[warp][k] = v[k];
-    }
-    // exclusive: the lane before's inclusive (lane 0: the identity)
-    a = __shfl_up_sync(0xffffffffu, a, 1);
-#pragma unroll
-    for (int k = 0; k < 32; ++k) v[k] = __shfl_up_sync(0xffffffffu, v[k], 1);
-    if (lane == 0) {
-      a = 1.0f;
-#pragma unroll
-      for (int k = 0; k < 32; ++k) v[k] = 0.0f;
-    }
-    __syncthreads();
-    // the earlier warps' maps in order, then this thread's exclusive map,
-    // applied to the carry: the state entering chunk c
-    float pa = 1.0f, S[32];
-#pragma unroll
-    for (int k = 0; k < 32; ++k) S[k] = 0.0f;
-    for (int w = 0; w < warp; ++w) {
-      const float aw = wa[w];
-#pragma unroll
-      for (int k = 0; k < 32; ++k) S[k] = __fmaf_rn(aw, S[k], wsum[w][k]);
-      pa = __fmul_rn(pa, aw);
+  for (int k = 0; k < kPassAhead; ++k) ahead[k] = k < nC ? __ldcs(src + (size_t)k * 32) : 0.0f;
+  for (int c0 = 0; c0 < nC; c0 += kPassAhead) {
+    if (c0 % kPassBlock == 0) {  // the next block of decay factors
+      __syncthreads();
+      for (int i = tid; i < kPassBlock && c0 + i < nC; i += 32 * kPassSlices) fac[i] = ex2_approx(__ldg(tot + c0 + i));
+      __syncthreads();
     }
 #pragma unroll
-    for (int k = 0; k < 32; ++k) S[k] = __fmaf_rn(a, __fmaf_rn(pa, carry[k], S[k]), v[k]);
-    if (c < nC) {
-      float4* d4 = reinterpret_cast<float4*>(dst + (size_t)c * 32);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) __stcs(d4 + k, make_float4(S[4 * k], S[4 * k + 1], S[4 * k + 2], S[4 * k + 3]));
-    }
-    __syncthreads();  // everyone has read the carry and the warp totals
-    if (c == min(nC, c0 + kPassThreads) - 1) {  // the block's last chunk: the new carry
-      const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)c * 32);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float4 x4 = __ldcg(s4 + k);
-        carry[4 * k] = __fmaf_rn(a_own, S[4 * k], x4.x);
-        carry[4 * k + 1] = __fmaf_rn(a_own, S[4 * k + 1], x4.y);
-        carry[4 * k + 2] = __fmaf_rn(a_own, S[4 * k + 2], x4.z);
-        carry[4 * k + 3] = __fmaf_rn(a_own, S[4 * k + 3], x4.w);
+    for (int k = 0; k < kPassAhead; ++k) {
+      const int c = c0 + k;
+      if (c < nC) {
+        __stcs(dst + (size_t)c * 32, S);
+        const float v = ahead[k];
+        if (c + kPassAhead < nC) ahead[k] = __ldcs(src + (size_t)(c + kPassAhead) * 32);
+        S = __fmaf_rn(fac[c % kPassBlock], S, v);
       }
     }
-    __syncthreads();
   }
-  cp_async_wait_all();  // the last, unused copy lands before the block ends
-  if (p.final_state && tid < 32) p.final_state[bh * kSsdN * kSsdP + n * kSsdP + p0 + tid] = carry[tid];
+  if (p.final_state) p.final_state[bh * kSsdN * kSsdP + n * kSsdP + col] = S;
 }
 
 // ---------------------------------------------------------------- output
