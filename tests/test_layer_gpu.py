@@ -24,7 +24,7 @@ import pytest
 import torch
 
 import oracle
-from parity import assert_close, errors
+from parity import assert_close, errors, sample_channels
 from selective_state_space_118_b300 import ops
 
 pytestmark = pytest.mark.gpu
@@ -142,3 +142,40 @@ def test_layer_u_out_optional_and_rejects_bad_arguments():
     with pytest.raises(ops.MambaError) as e:
         run(p, workspace=torch.empty(256, dtype=torch.uint8, device="cuda"))
     assert e.value.status == ops.MAMBA_ERR_WORKSPACE
+
+
+def test_layer_fullsize_stagewise_sampled():
+    """The benchmark's layer (1 x 32768 tokens, d_model 4096, d_inner 8192,
+    dt_rank 256), stage by stage on samples: every GEMM on 48 sampled token
+    rows (rows are independent), the conv + SiLU and the scan on 8 sampled
+    channels (independent given B and C), each from the GPU's own inputs of
+    that stage."""
+    B, L, H, D, R = 1, 32768, 4096, 8192, 256
+    p = weights(B, L, H, D, R, seed=77)
+    u = torch.empty(B, L, D, device="cuda", dtype=torch.bfloat16)
+    ws = torch.empty(ops.mamba_layer_workspace_size(B, L, H, D, R, 0, True), device="cuda", dtype=torch.uint8)
+    out = run(p, u_out=u, workspace=ws)
+    torch.cuda.synchronize()
+    v = workspace_views(ws, B, L, D, R)
+    f = oracle.f64
+    rows = torch.tensor(np.unique(np.linspace(0, L - 1, 48).round().astype(np.int64)), device="cuda")
+    h = f(p["hidden"][0, rows])
+    Win = f(p["W_in"])
+    ulp_close(v["x"][0, rows], oracle.bf16_round(h @ Win[:D].T), "full size in_proj x")
+    ulp_close(v["z"][0, rows], oracle.bf16_round(h @ Win[D:].T), "full size in_proj z")
+    ulp_close(v["xdbl"][0, rows], oracle.bf16_round(f(u[0, rows]) @ f(p["W_x"]).T), "full size x_proj")
+    xd = f(v["xdbl"][0, rows])
+    ulp_close(v["dt_raw"][0, rows], oracle.bf16_round(xd[:, :R] @ f(p["W_dt"]).T + f(p["b_dt"])), "full size dt_proj")
+    ulp_close(out[0, rows], oracle.bf16_round(f(v["y"][0, rows]) @ f(p["W_out"]).T), "full size out_proj")
+    chans = sample_channels(D, 8)
+    ci = torch.as_tensor(chans, device="cuda")
+    x = f(v["x"][:, :, ci])
+    cw, cb = f(p["conv_w"])[chans], f(p["conv_b"])[chans]
+    xp = np.concatenate([np.zeros((B, 3, len(chans))), x], axis=1)
+    pre = cb + sum(cw[:, k] * xp[:, k:k + L] for k in range(4))
+    ulp_close(u[:, :, ci], oracle.bf16_round(pre / (1.0 + np.exp(-pre))), "full size conv+SiLU")
+    xdbl = f(v["xdbl"])
+    yr, _, _ = oracle.scan(x, f(v["z"][:, :, ci]), f(v["dt_raw"][:, :, ci]),
+                           np.ascontiguousarray(xdbl[..., R:R + 16]), np.ascontiguousarray(xdbl[..., R + 16:]),
+                           f(p["A_log"])[chans], f(p["Dskip"])[chans], cw, cb)
+    assert_close(v["y"][:, :, ci], yr, "bf16", "full size scan (sampled channels)")

@@ -89,3 +89,20 @@ def test_ssd_large_dt_fast_decay():
     yr, fsr = oracle.ssd(**p)
     assert_close(y, yr, "bf16", "large dt y")
     assert_close(fs, fsr, "bf16", "large dt final state", fp32_output=True)
+
+
+def test_ssd_fullsize_sampled_heads():
+    """The benchmark's configuration (1 x 32768 tokens, 128 heads of 64, one
+    group, the gate), in the launch configuration bench.py times: 6 sampled
+    heads against the oracle (heads are independent given B and C)."""
+    p = case(1, 32768, 128, 1, seed=3)
+    y, fs = run(p)
+    torch.cuda.synchronize()
+    heads = [0, 1, 37, 64, 100, 127]
+    idx = torch.tensor(heads, device="cuda")
+    sub = dict(p, x=p["x"][:, :, idx].contiguous(), z=p["z"][:, :, idx].contiguous(),
+               dt_raw=p["dt_raw"][:, :, idx].contiguous(), A_log=p["A_log"][idx].contiguous(),
+               Dskip=p["Dskip"][idx].contiguous(), h0=p["h0"][:, idx].contiguous())
+    yr, fsr = oracle.ssd(**sub)
+    assert_close(y[:, :, idx], yr, "bf16", "full size y (sampled heads)")
+    assert_close(fs[:, idx], fsr, "bf16", "full size final state (sampled heads)", fp32_output=True)
