@@ -52,7 +52,6 @@ namespace mamba {
 constexpr int kSub = 4;             // tokens per register sub-tile
 constexpr int kSubs = kT / kSub;    // sub-tiles per tile
 constexpr int kParamStride = 24;    // floats per channel of the parameter partials
-constexpr int kBwdMinBlocks = 1;    // resident reverse-sweep CTAs per SM the register budget must allow
 
 template <typename IO>
 struct BwdStage {
@@ -365,7 +364,7 @@ __device__ __forceinline__ void issue_bwd_tile(BwdSmem<IO>& sm, int s, const CUt
 // ---------------------------------------------------------------- reverse sweep
 // grid (n_groups, batch, n_chunks), 32 threads.
 template <typename IO>
-__global__ void __launch_bounds__(kLanes, kBwdMinBlocks)
+__global__ void __launch_bounds__(kLanes)
     scan_bwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
                     const __grid_constant__ CUtensorMap tm_dt, const __grid_constant__ CUtensorMap tm_dy,
                     const __grid_constant__ CUtensorMap tm_bc, const __grid_constant__ BwdParams p) {

@@ -280,7 +280,6 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_output_kernel(const __grid_co
   SsdTile& s = sm.t;
   const int h = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const size_t chunk = ((size_t)b * p.heads + h) * p.n_chunks + c;
   const size_t bh = (size_t)b * p.heads + h;
   // tiles by asynchronous copies; meanwhile the entering state (32 slices of
   // 32 values), fp32 -> hi + lo bf16 pairs
