@@ -2,14 +2,21 @@
 """Benchmark of the selective-scan library on synthetic Jamba-shaped inputs.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                [--workload NAME] [--no-decode] [--no-e2e] [--no-cpu-baseline]
+                [--workload NAME] [--seqlen L] [--n-chunks K]
+                [--no-e2e] [--no-cpu-baseline] [--no-decode] [--no-ssd]
+                [--no-layer] [--no-backward]
+                [--no-prefill | --backward-only | --layer-only | --ssd-only]
 
 A step is one prefill pass of the layer (conv, SiLU, softplus, discretised
 scan, D skip, SiLU(z) gate; final h and conv state) over the workload's whole
 batch, through the C ABI, inputs resident in HBM (larger than L2).  Prints
 one JSON line on rank 0.  Under torchrun every rank runs an independent
 replica (the scan has no cross-device exchange): value = elements all ranks
-processed / max-over-ranks time.
+processed / max-over-ranks time.  The line also carries, unless switched
+off, the end-to-end number (host copies in the timed region), the decode
+block, Mamba-2's scan, the whole layer and the backward, each with its own
+timing, roofline and clocks; the --*-only switches print one block alone
+(profiling).
 
 --impl reference times the fp64 CPU oracle (the definition the library is
 checked against) on the host cores, on a bounded sample of the same workload.
