@@ -95,6 +95,9 @@ typedef enum { MAMBA_F32 = 0, MAMBA_BF16 = 1 } mamba_dtype;
  *                     agree with the sequential pass to rounding)
  *   flags             0, or MAMBA_FLAG_TEST_* (tests only)
  *   wait_timeout_ns   limit of every device-side wait (0: 1 second)
+ *   tile_states       NULL, or (B, ceil(L/16), D, 16) fp32: the state entering
+ *                     every 16-token tile is stored there (B*L*D*4 bytes,
+ *                     rounded up to whole tiles), for mamba_scan_bwd
  *
  * seqlen may be 0 (then only final_h/final_conv_state are written: copies of
  * h0/conv_state0, or zeros).  batch and d_inner must be > 0.
@@ -115,6 +118,9 @@ typedef struct mamba_scan_args {
     int n_chunks;
     uint32_t flags;
     uint64_t wait_timeout_ns;
+    float *tile_states;   /* NULL, or (B, ceil(L / 16), D, 16) fp32 output: the
+                             state entering every 16-token tile, for a later
+                             mamba_scan_bwd of the same inputs */
 } mamba_scan_args;
 
 /* Bytes of workspace mamba_scan_fwd needs for these sizes and n_chunks
@@ -195,6 +201,12 @@ mamba_status mamba_scan_fwd_noalloc(const mamba_scan_args *args, void *stream);
  *                     right is computed first, the way the forward computes
  *                     its carries, with time reversed
  *   wait_timeout_ns   limit of every device-side wait (0: 1 second)
+ *   tile_states       NULL: the forward is recomputed inside the call, storing
+ *                     the tile states in the workspace.  Or the tile_states
+ *                     output of a mamba_scan_fwd of the same inputs (any
+ *                     n_chunks): the recomputation is skipped; the gradients
+ *                     are the same bits (the states are computed the same way
+ *                     in both passes)
  *
  * Every output is overwritten.  Results are deterministic (fixed summation
  * orders, no atomics).  seqlen may be 0: then dh0 = dfinal_h,
@@ -222,6 +234,9 @@ typedef struct mamba_scan_bwd_args {
     int n_chunks;
     uint32_t flags;
     uint64_t wait_timeout_ns;
+    const float *tile_states;  /* NULL, or the tile states a mamba_scan_fwd of the
+                                  same inputs wrote: the forward is then not
+                                  recomputed */
 } mamba_scan_bwd_args;
 
 /* Bytes of workspace mamba_scan_bwd needs (0 only for invalid sizes or

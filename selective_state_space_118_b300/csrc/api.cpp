@@ -315,7 +315,7 @@ mamba_status launch_forward(const mamba_scan_args* a, const Plan& pl, const Work
       !encode3d(&maps[4], bc, MAMBA_F32, 32, a->seqlen, a->batch, 32))
     return MAMBA_ERR_CUDA;
 
-  const mamba::ScanParams p = fwd_params(a, pl, ws, nullptr);
+  const mamba::ScanParams p = fwd_params(a, pl, ws, a->tile_states);
   const IoType io = a->io == MAMBA_BF16 ? IoType::BF16 : IoType::F32;
 
   if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, bc_ld, stream) != cudaSuccess)
@@ -378,7 +378,7 @@ mamba_status mamba_scan_fwd(const mamba_scan_args* a, void* stream_v) {
   if (a->seqlen < 0 || a->n_chunks < 0) return MAMBA_ERR_INVALID_ARG;
   if (!a->A_log || !a->Dskip || !a->conv_w) return MAMBA_ERR_INVALID_ARG;
   const void* aligned_ptrs[] = {a->A_log, a->Dskip, a->conv_w, a->conv_b, a->h0, a->conv_state0,
-                                a->final_h, a->final_conv_state};
+                                a->final_h, a->final_conv_state, a->tile_states};
   for (const void* p : aligned_ptrs)
     if (p && !aligned16(p)) return MAMBA_ERR_INVALID_ARG;
 
@@ -428,7 +428,7 @@ mamba_status mamba_scan_bwd(const mamba_scan_bwd_args* a, void* stream_v) {
     return MAMBA_ERR_INVALID_ARG;
   const void* aligned_ptrs[] = {a->A_log, a->Dskip, a->conv_w, a->conv_b, a->h0, a->conv_state0,
                                 a->dfinal_h, a->dfinal_conv_state, a->dA_log, a->dDskip, a->dconv_w,
-                                a->dconv_b, a->dh0, a->dconv_state0};
+                                a->dconv_b, a->dh0, a->dconv_state0, a->tile_states};
   for (const void* p : aligned_ptrs)
     if (p && !aligned16(p)) return MAMBA_ERR_INVALID_ARG;
   const size_t B = a->batch, D = a->d_inner;
@@ -466,7 +466,9 @@ mamba_status mamba_scan_bwd(const mamba_scan_bwd_args* a, void* stream_v) {
   if (!a->workspace || a->workspace_bytes < ws.total) return MAMBA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return MAMBA_ERR_INVALID_ARG;
   char* wsp = static_cast<char*>(a->workspace);
-  float* ckpt = reinterpret_cast<float*>(wsp + ws.ckpt);
+  // the tile states: the caller's (from its forward call), or recomputed here
+  const bool recompute = a->tile_states == nullptr;
+  float* ckpt = recompute ? reinterpret_cast<float*>(wsp + ws.ckpt) : const_cast<float*>(a->tile_states);
   const uint64_t timeout = a->wait_timeout_ns ? a->wait_timeout_ns : kDefaultTimeoutNs;
 
   // The forward pass again, storing the state entering every tile (no y).
@@ -532,9 +534,10 @@ mamba_status mamba_scan_bwd(const mamba_scan_bwd_args* a, void* stream_v) {
   p.dconv_state0 = a->dconv_state0;
   p.timeout_ns = timeout;
 
-  // 1. B/C rows widened; 2. chunked mode: the forward's chunk carries and the
-  // adjoint carries (one launch); 3. the states-only forward pass; 4. the
-  // reverse sweep; 5. the edge fix-up and the fixed-order sums
+  // 1. B/C rows widened; 2. chunked mode: the forward's chunk carries (when
+  // the forward is recomputed) and the adjoint carries, in one launch; 3. the
+  // states-only forward pass (when recomputed); 4. the reverse sweep; 5. the
+  // edge fix-up and the fixed-order sums
   if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, 16, stream) != cudaSuccess)
     return MAMBA_ERR_CUDA;
   if (pl.n_chunks > 1) {
@@ -542,15 +545,18 @@ mamba_status mamba_scan_bwd(const mamba_scan_bwd_args* a, void* stream_v) {
     p.counters = reinterpret_cast<unsigned*>(wsp + ws.counters);
     p.edge_dx = reinterpret_cast<float*>(wsp + ws.edge_dx);
     p.edge_dpre = reinterpret_cast<float*>(wsp + ws.edge_dpre);
-    if (cudaMemsetAsync(fp.counters, 0, ws.fwd.counters_bytes, stream) != cudaSuccess ||
+    if ((recompute && cudaMemsetAsync(fp.counters, 0, ws.fwd.counters_bytes, stream) != cudaSuccess) ||
         cudaMemsetAsync(p.counters, 0, ws.counters_bytes, stream) != cudaSuccess)
       return MAMBA_ERR_CUDA;
     const unsigned n_each = (unsigned)((size_t)(pl.n_chunks - 1) * p.n_groups * B);
-    if (mamba::launch_carries(io, maps, fp, p, n_each, n_each, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+    if (mamba::launch_carries(io, maps, fp, p, recompute ? n_each : 0u, n_each, stream) != cudaSuccess)
+      return MAMBA_ERR_CUDA;
   }
-  const CUtensorMap fmaps[4] = {maps[0], maps[1], maps[2], maps[4]};  // x, z (unused), dt_raw, bc
   dim3 grid((unsigned)p.n_groups, (unsigned)B, (unsigned)pl.n_chunks);
-  if (mamba::launch_scan(io, fmaps, fp, grid, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+  if (recompute) {
+    const CUtensorMap fmaps[4] = {maps[0], maps[1], maps[2], maps[4]};  // x, z (unused), dt_raw, bc
+    if (mamba::launch_scan(io, fmaps, fp, grid, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+  }
   if (mamba::launch_bwd(io, maps, p, grid, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
   if (mamba::launch_bwd_finish(io, p, a->dB, a->dC, a->dA_log, a->dDskip, a->dconv_w, a->dconv_b, stream) !=
       cudaSuccess)

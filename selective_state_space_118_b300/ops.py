@@ -43,7 +43,8 @@ class ScanArgs(ctypes.Structure):
                 ("h0", _vp), ("conv_state0", _vp), ("y", _vp), ("final_h", _vp),
                 ("final_conv_state", _vp), ("workspace", _vp),
                 ("workspace_bytes", ctypes.c_size_t), ("n_chunks", ctypes.c_int),
-                ("flags", ctypes.c_uint32), ("wait_timeout_ns", ctypes.c_uint64)]
+                ("flags", ctypes.c_uint32), ("wait_timeout_ns", ctypes.c_uint64),
+                ("tile_states", _vp)]
 
 
 class BwdArgs(ctypes.Structure):
@@ -56,7 +57,8 @@ class BwdArgs(ctypes.Structure):
                 ("dB", _vp), ("dC", _vp), ("dA_log", _vp), ("dDskip", _vp), ("dconv_w", _vp),
                 ("dconv_b", _vp), ("dh0", _vp), ("dconv_state0", _vp), ("workspace", _vp),
                 ("workspace_bytes", ctypes.c_size_t), ("n_chunks", ctypes.c_int),
-                ("flags", ctypes.c_uint32), ("wait_timeout_ns", ctypes.c_uint64)]
+                ("flags", ctypes.c_uint32), ("wait_timeout_ns", ctypes.c_uint64),
+                ("tile_states", _vp)]
 
 
 class LayerArgs(ctypes.Structure):
@@ -187,12 +189,15 @@ def mamba_scan_plan(batch: int, seqlen: int, d_inner: int, n_chunks: int = 0) ->
 def mamba_scan_fwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=None,
                    conv_state0=None, *, y=None, final_h=None, final_conv_state=None,
                    workspace=None, n_chunks: int = 0, flags: int = 0,
-                   wait_timeout_ns: int = 0, return_state: bool = True, stream=None):
+                   wait_timeout_ns: int = 0, return_state: bool = True, tile_states=None,
+                   stream=None):
     """Prefill scan (C ABI ``mamba_scan_fwd``).  x, z, dt_raw (B,L,D) and
     Bm, Cm (B,L,16) in fp32 or bf16; A_log (D,16), Dskip (D), conv_w (D,4),
     conv_b (D) fp32; h0 (B,D,16) fp32; conv_state0 (B,3,D) in the I/O dtype.
     Returns (y, final_h, final_conv_state) (the last two None when
-    return_state is False and they were not passed)."""
+    return_state is False and they were not passed).  tile_states: an fp32
+    tensor of tile_states_shape(B, L, D) that receives the state entering
+    every 16-token tile, for mamba_scan_bwd."""
     lib = load_library()
     B, L, D = x.shape
     dev = x.device
@@ -213,7 +218,8 @@ def mamba_scan_fwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=N
                  final_h=_ptr(final_h), final_conv_state=_ptr(final_conv_state),
                  workspace=_ptr(workspace),
                  workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
-                 n_chunks=n_chunks, flags=flags, wait_timeout_ns=wait_timeout_ns)
+                 n_chunks=n_chunks, flags=flags, wait_timeout_ns=wait_timeout_ns,
+                 tile_states=_ptr(tile_states))
     for t in (z, dt_raw, Bm, Cm, conv_state0, y, final_conv_state):
         if t is not None and t.dtype != x.dtype:
             raise TypeError("x, z, dt_raw, Bm, Cm, conv_state0, y and final_conv_state share one dtype")
@@ -231,15 +237,22 @@ BWD_OUTPUTS = ("dx", "dz", "ddt_raw", "dB", "dC", "dA_log", "dDskip", "dconv_w",
                "dconv_state0")
 
 
+def tile_states_shape(batch: int, seqlen: int, d_inner: int) -> tuple:
+    """Shape of the tile states mamba_scan_fwd can store for mamba_scan_bwd."""
+    return (batch, (seqlen + 15) // 16, d_inner, D_STATE)
+
+
 def mamba_scan_bwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=None,
                    conv_state0=None, *, dy, dfinal_h=None, dfinal_conv_state=None,
                    out=None, workspace=None, n_chunks: int = 0, wait_timeout_ns: int = 0,
-                   stream=None) -> dict:
+                   tile_states=None, stream=None) -> dict:
     """Backward of the prefill scan (C ABI ``mamba_scan_bwd``): the gradients
     of l given dy = dl/dy (B,L,D) and optionally dl/dfinal_h (B,D,16) fp32 and
     dl/dfinal_conv_state (B,3,D).  Returns a dict keyed by BWD_OUTPUTS: dx,
     dz, ddt_raw in the I/O dtype, everything else fp32 (dconv_b only when
-    conv_b is given).  `out` may hold preallocated outputs by the same keys."""
+    conv_b is given).  `out` may hold preallocated outputs by the same keys.
+    tile_states: the tile states of a mamba_scan_fwd of the same inputs
+    (skips the forward recomputation)."""
     lib = load_library()
     B, L, D = x.shape
     dev = x.device
@@ -271,7 +284,8 @@ def mamba_scan_bwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=N
                 **{k: _ptr(g[k]) for k in BWD_OUTPUTS},
                 workspace=_ptr(workspace),
                 workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
-                n_chunks=n_chunks, flags=0, wait_timeout_ns=wait_timeout_ns)
+                n_chunks=n_chunks, flags=0, wait_timeout_ns=wait_timeout_ns,
+                tile_states=_ptr(tile_states))
     st = lib.mamba_scan_bwd(ctypes.byref(a), _stream(stream))
     if st != MAMBA_OK:
         raise MambaError(st, "mamba_scan_bwd")

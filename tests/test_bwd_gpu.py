@@ -202,3 +202,23 @@ def test_bwd_fullsize_sampled_channels():
     out = run_gpu(inp)
     chans = sample_channels(w.d_inner, 12)
     check(inp, out, "full size", channels=chans, skip=("dB", "dC", "dconv_b"))
+
+
+@pytest.mark.parametrize("io,n_chunks", [("bf16", 0), ("f32", 1), ("bf16", 4)])
+def test_bwd_from_forward_tile_states_is_bitwise_the_same(io, n_chunks):
+    """A forward call that stores the tile states, then a backward given them
+    (no recomputation), equals a backward that recomputes them, bit for bit:
+    both passes compute the states with the same operations."""
+    inp = make_case(2, 700, 48, io, seed=51)
+    B, L, D = inp["x"].shape
+    ts = torch.empty(ops.tile_states_shape(B, L, D), device="cuda")
+    ops.mamba_scan_fwd(inp["x"], inp["z"], inp["dt_raw"], inp["Bm"], inp["Cm"], inp["A_log"], inp["Dskip"],
+                       inp["conv_w"], inp["conv_b"], inp["h0"], inp["conv_state0"], n_chunks=n_chunks,
+                       tile_states=ts)
+    a = run_gpu(inp, n_chunks=n_chunks)
+    a = {k: (v.clone() if v is not None else None) for k, v in a.items()}
+    b = run_gpu(inp, n_chunks=n_chunks, tile_states=ts)
+    torch.cuda.synchronize()
+    for k in ops.BWD_OUTPUTS:
+        if a[k] is not None:
+            assert torch.equal(a[k], b[k]), k
