@@ -203,10 +203,11 @@ mamba_status mamba_scan_fwd_noalloc(const mamba_scan_args *args, void *stream);
  *   wait_timeout_ns   limit of every device-side wait (0: 1 second)
  *   tile_states       NULL: the forward is recomputed inside the call, storing
  *                     the tile states in the workspace.  Or the tile_states
- *                     output of a mamba_scan_fwd of the same inputs (any
- *                     n_chunks): the recomputation is skipped; the gradients
- *                     are the same bits (the states are computed the same way
- *                     in both passes)
+ *                     output of a mamba_scan_fwd of the same inputs: the
+ *                     recomputation is skipped.  When that call had the same
+ *                     n_chunks, the gradients are the same bits as with NULL
+ *                     (the states are computed the same way in both passes);
+ *                     with another n_chunks they differ by rounding only
  *
  * Every output is overwritten.  Results are deterministic (fixed summation
  * orders, no atomics).  seqlen may be 0: then dh0 = dfinal_h,

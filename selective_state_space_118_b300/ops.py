@@ -201,6 +201,7 @@ def mamba_scan_fwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=N
     lib = load_library()
     B, L, D = x.shape
     dev = x.device
+    _check_tile_states(tile_states, B, L, D)
     if y is None:
         y = torch.empty_like(x)
     if return_state:
@@ -242,6 +243,15 @@ def tile_states_shape(batch: int, seqlen: int, d_inner: int) -> tuple:
     return (batch, (seqlen + 15) // 16, d_inner, D_STATE)
 
 
+def _check_tile_states(t, batch: int, seqlen: int, d_inner: int) -> None:
+    """The C ABI takes a bare pointer: the buffer's size is checked here."""
+    if t is None:
+        return
+    shape = tile_states_shape(batch, seqlen, d_inner)
+    if t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != shape:
+        raise ValueError(f"tile_states must be a contiguous float32 tensor of shape {shape}")
+
+
 def mamba_scan_bwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=None,
                    conv_state0=None, *, dy, dfinal_h=None, dfinal_conv_state=None,
                    out=None, workspace=None, n_chunks: int = 0, wait_timeout_ns: int = 0,
@@ -252,10 +262,12 @@ def mamba_scan_bwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=N
     dz, ddt_raw in the I/O dtype, everything else fp32 (dconv_b only when
     conv_b is given).  `out` may hold preallocated outputs by the same keys.
     tile_states: the tile states of a mamba_scan_fwd of the same inputs
-    (skips the forward recomputation)."""
+    (skips the forward recomputation; with the same n_chunks as that call,
+    the gradients are the same bits as without it)."""
     lib = load_library()
     B, L, D = x.shape
     dev = x.device
+    _check_tile_states(tile_states, B, L, D)
     f32 = torch.float32
     shapes = {"dx": ((B, L, D), x.dtype), "dz": ((B, L, D), x.dtype), "ddt_raw": ((B, L, D), x.dtype),
               "dB": ((B, L, D_STATE), f32), "dC": ((B, L, D_STATE), f32),

@@ -8,6 +8,7 @@ import re
 import subprocess
 
 import pytest
+import torch
 
 from selective_state_space_118_b300 import build, ops
 
@@ -211,3 +212,28 @@ def test_workspace_plan(lib):
     assert big["n_chunks"] > 1 and big["chunk_len"] * big["n_chunks"] >= 32768
     # many sequences fill it: one pass
     assert ops.mamba_scan_default_chunks(64, 4096, 8192) == 1
+
+
+def test_tile_states_checks(lib):
+    """A misaligned tile-state pointer is refused by both calls; the binding
+    refuses a buffer of the wrong shape or dtype before calling the C ABI
+    (which cannot see a pointer's extent)."""
+    scan = dict(A_log=FAKE, Dskip=FAKE, conv_w=FAKE, x=FAKE, z=FAKE, dt_raw=FAKE, Bm=FAKE, Cm=FAKE, y=FAKE)
+    a = _args(**dict(scan, tile_states=FAKE + 4))
+    assert lib.mamba_scan_fwd(ctypes.byref(a), None) == ops.MAMBA_ERR_INVALID_ARG
+    bwd = dict(batch=1, seqlen=8, d_inner=16, d_state=16, d_conv=4, io=ops.MAMBA_BF16, A_log=FAKE, Dskip=FAKE,
+               conv_w=FAKE, dA_log=FAKE, dDskip=FAKE, dconv_w=FAKE, x=FAKE, z=FAKE, dt_raw=FAKE, Bm=FAKE,
+               Cm=FAKE, dy=FAKE, dx=FAKE, dz=FAKE, ddt_raw=FAKE, dB=FAKE, dC=FAKE)
+    assert lib.mamba_scan_bwd(ctypes.byref(ops.BwdArgs(**dict(bwd, tile_states=FAKE + 8))), None) == \
+        ops.MAMBA_ERR_INVALID_ARG
+    assert ops.tile_states_shape(2, 33, 64) == (2, 3, 64, 16)
+    B, L, D = 1, 40, 32
+    x = torch.zeros(B, L, D, dtype=torch.bfloat16)
+    bc = torch.zeros(B, L, 16, dtype=torch.bfloat16)
+    p = (torch.zeros(D, 16), torch.ones(D), torch.zeros(D, 4))
+    for bad in (torch.zeros(B, 2, D, 16), torch.zeros(B, 3, D, 16, dtype=torch.float64),
+                torch.zeros(B, D, 3, 16).transpose(1, 2)):
+        with pytest.raises(ValueError):
+            ops.mamba_scan_fwd(x, x, x, bc, bc, *p, tile_states=bad)
+        with pytest.raises(ValueError):
+            ops.mamba_scan_bwd(x, x, x, bc, bc, *p, dy=x, tile_states=bad)
