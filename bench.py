@@ -384,6 +384,7 @@ def bench_backward(w, steps, warmup, local, n_chunks_req=0):
     hbm, src = peaks()
     n_chunks = ops.mamba_scan_plan(B, L, D, n_chunks_req)["n_chunks"]
     launches = 7 if n_chunks > 1 else 5
+    reuse = bench_tile_state_reuse(ops, inp, dy, out, ws, n_chunks_req, stream, steps, warmup, dev)
     res = {"metric": "backward elements/s", "value": B * L * D / t, "unit": UNIT,
            "config": {"workload": w.name, "batch": B, "seqlen": L, "d_inner": D, "n_chunks": n_chunks,
                       "dy": "seeded N(0,1) in the I/O dtype"},
@@ -393,9 +394,54 @@ def bench_backward(w, steps, warmup, local, n_chunks_req=0):
                         "algorithmic_bytes_per_call": alg,
                         "note": "instruction-issue bound (forward recomputed from tile checkpoints, "
                                 "then the reverse sweep); the HBM fraction is context"},
-           "gpu_launches": launches * steps, "clocks": clk.summary()}
+           "gpu_launches": launches * steps, "clocks": clk.summary(), "tile_state_reuse": reuse}
     del inp, dy, ws, out
     return res
+
+
+def bench_tile_state_reuse(ops, inp, dy, out, ws, n_chunks_req, stream, steps, warmup, dev):
+    """A training step's two scan calls when the forward stores its tile
+    states and the backward reuses them (no recomputed forward inside the
+    backward): each call timed alone, in ms per call (CUDA events, the same
+    workload and plan as the backward above)."""
+    x = inp["x"]
+    B, L, D = x.shape
+    ts = torch.empty(ops.tile_states_shape(B, L, D), device=dev)
+    y = torch.empty_like(x)
+    nbytes = ops.mamba_scan_workspace_size(B, L, D, n_chunks_req)
+    fws = torch.empty(max(nbytes, 256), device=dev, dtype=torch.uint8)
+    args = (x, inp["z"], inp["dt_raw"], inp["Bm"], inp["Cm"], inp["A_log"], inp["Dskip"], inp["conv_w"],
+            inp["conv_b"])
+
+    def fwd(tiles):
+        ops.mamba_scan_fwd(*args, y=y, workspace=fws, n_chunks=n_chunks_req, return_state=False,
+                           tile_states=tiles, stream=stream)
+
+    def bwd():
+        ops.mamba_scan_bwd(*args, dy=dy, out=out, workspace=ws, n_chunks=n_chunks_req, tile_states=ts,
+                           stream=stream)
+
+    def per_call(fn):
+        for _ in range(warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        assert ops.mamba_last_error(stream) == ops.MAMBA_OK
+        return e0.elapsed_time(e1) / steps
+
+    fwd_plain = per_call(lambda: fwd(None))
+    fwd_tiles = per_call(lambda: fwd(ts))
+    bwd_given = per_call(bwd)
+    del ts, y, fws
+    return {"fwd_ms": fwd_plain, "fwd_storing_tile_states_ms": fwd_tiles,
+            "bwd_given_tile_states_ms": bwd_given,
+            "note": "tile states (B, L/16, D, 16) fp32 written by the forward and read by the backward, "
+                    "which then skips its states-only forward pass"}
 
 
 def oracle_bwd_sample_rate(w, target_s: float):
