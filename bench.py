@@ -661,8 +661,9 @@ def bench_decode(w, local, replays=3, layers=None, tokens=None):
             "ms_per_token": t * 1e3 / w.steps,
             "roofline": {"bound": "hbm", "achieved": alg / per_launch / 1e9, "peak": hbm,
                          "unit": "GB/s", "frac": alg / per_launch / 1e9 / hbm,
-                         "traffic": None, "peak_source": src,
-                         "note": "per-launch time = graph replay time / launches (gaps included)"},
+                         "traffic": measured_traffic(w.name), "peak_source": src,
+                         "note": "per-launch time = graph replay time / launches (gaps included); "
+                                 "traffic: ncu DRAM bytes of one step_kernel launch"},
             "gpu_launches": launches * replays, "clocks": clk.summary()}
 
 
