@@ -163,6 +163,43 @@ def _ptr(t):
     return t.data_ptr()
 
 
+def _check_args(specs, check_shapes: bool = True) -> None:
+    """Dtype, shape and device of every tensor argument given.  The C ABI
+    takes bare pointers and cannot see a buffer's extent, so a tensor smaller
+    than the sizes passed with it would be read or written out of bounds;
+    this is checked here, before any device access.  specs: (name, tensor or
+    None, expected shape, expected dtype).  check_shapes is False for sizes
+    the library does not support: it refuses those itself before touching
+    memory.  A missing required tensor is the library's to refuse too."""
+    dev = None
+    for name, t, shape, dtype in specs:
+        if t is None:
+            continue
+        if t.dtype != dtype:
+            raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+        if check_shapes and tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the other tensors on {dev}")
+
+
+def _scan_specs(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b, h0, conv_state0):
+    """The inputs shared by the prefill scan and its backward."""
+    B, L, D = x.shape
+    io, f32 = x.dtype, torch.float32
+    return [("x", x, (B, L, D), io), ("z", z, (B, L, D), io), ("dt_raw", dt_raw, (B, L, D), io),
+            ("Bm", Bm, (B, L, D_STATE), io), ("Cm", Cm, (B, L, D_STATE), io),
+            ("A_log", A_log, (D, D_STATE), f32), ("Dskip", Dskip, (D,), f32),
+            ("conv_w", conv_w, (D, D_CONV), f32), ("conv_b", conv_b, (D,), f32),
+            ("h0", h0, (B, D, D_STATE), f32), ("conv_state0", conv_state0, (B, D_CONV - 1, D), io)]
+
+
+def _scan_sizes_supported(A_log, conv_w) -> bool:
+    return A_log.shape[-1] == D_STATE and conv_w.shape[-1] == D_CONV
+
+
 def _stream(stream) -> int:
     s = torch.cuda.current_stream() if stream is None else stream
     return s.cuda_stream
@@ -202,6 +239,10 @@ def mamba_scan_fwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=N
     B, L, D = x.shape
     dev = x.device
     _check_tile_states(tile_states, B, L, D)
+    _check_args(_scan_specs(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b, h0, conv_state0)
+                + [("y", y, (B, L, D), x.dtype), ("final_h", final_h, (B, D, D_STATE), torch.float32),
+                   ("final_conv_state", final_conv_state, (B, D_CONV - 1, D), x.dtype)],
+                _scan_sizes_supported(A_log, conv_w))
     if y is None:
         y = torch.empty_like(x)
     if return_state:
@@ -221,9 +262,6 @@ def mamba_scan_fwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=N
                  workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
                  n_chunks=n_chunks, flags=flags, wait_timeout_ns=wait_timeout_ns,
                  tile_states=_ptr(tile_states))
-    for t in (z, dt_raw, Bm, Cm, conv_state0, y, final_conv_state):
-        if t is not None and t.dtype != x.dtype:
-            raise TypeError("x, z, dt_raw, Bm, Cm, conv_state0, y and final_conv_state share one dtype")
     st = lib.mamba_scan_fwd(ctypes.byref(a), _stream(stream))
     if st != MAMBA_OK:
         raise MambaError(st, "mamba_scan_fwd")
@@ -281,10 +319,11 @@ def mamba_scan_bwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=N
             continue
         if g.get(k) is None:
             g[k] = torch.empty(shape, device=dev, dtype=dtype)
-    for t in (z, dt_raw, Bm, Cm, conv_state0, dy, dfinal_conv_state, g["dx"], g["dz"], g["ddt_raw"]):
-        if t is not None and t.dtype != x.dtype:
-            raise TypeError("x, z, dt_raw, Bm, Cm, conv_state0, dy, dfinal_conv_state, dx, dz and "
-                            "ddt_raw share one dtype")
+    _check_args(_scan_specs(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b, h0, conv_state0)
+                + [("dy", dy, (B, L, D), x.dtype), ("dfinal_h", dfinal_h, (B, D, D_STATE), f32),
+                   ("dfinal_conv_state", dfinal_conv_state, (B, D_CONV - 1, D), x.dtype)]
+                + [(k, g[k], shape, dtype) for k, (shape, dtype) in shapes.items()],
+                _scan_sizes_supported(A_log, conv_w))
     ws_bytes = mamba_scan_bwd_workspace_size(B, L, D, n_chunks)
     if ws_bytes and workspace is None:
         workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
@@ -321,6 +360,15 @@ def mamba_layer_fwd(hidden, W_in, conv_w, conv_b, W_x, W_dt, b_dt, A_log, Dskip,
     B, L, H = hidden.shape
     D = A_log.shape[0]
     R = W_dt.shape[1]
+    bf, f32 = torch.bfloat16, torch.float32
+    _check_args([("hidden", hidden, (B, L, H), bf), ("W_in", W_in, (2 * D, H), bf),
+                 ("conv_w", conv_w, (D, D_CONV), f32), ("conv_b", conv_b, (D,), f32),
+                 ("W_x", W_x, (R + 2 * D_STATE, D), bf), ("W_dt", W_dt, (D, R), bf), ("b_dt", b_dt, (D,), bf),
+                 ("A_log", A_log, (D, D_STATE), f32), ("Dskip", Dskip, (D,), f32), ("W_out", W_out, (H, D), bf),
+                 ("out", out, (B, L, H), bf), ("u_out", u_out, (B, L, D), bf),
+                 ("final_h", final_h, (B, D, D_STATE), f32),
+                 ("final_conv_state", final_conv_state, (B, D_CONV - 1, D), bf)],
+                _scan_sizes_supported(A_log, conv_w) and R % 8 == 0)
     if out is None:
         out = torch.empty_like(hidden)
     ws_bytes = mamba_layer_workspace_size(B, L, H, D, R, n_chunks, u_out is not None)
@@ -333,9 +381,6 @@ def mamba_layer_fwd(hidden, W_in, conv_w, conv_b, W_x, W_dt, b_dt, A_log, Dskip,
                   final_h=_ptr(final_h), final_conv_state=_ptr(final_conv_state), workspace=_ptr(workspace),
                   workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
                   n_chunks=n_chunks)
-    for t in (W_in, W_x, W_dt, b_dt, W_out, out, u_out, final_conv_state):
-        if t is not None and t.dtype != torch.bfloat16:
-            raise TypeError("the layer's activations and projection weights are bf16")
     st = lib.mamba_layer_fwd(ctypes.byref(a), _stream(stream))
     if st != MAMBA_OK:
         raise MambaError(st, "mamba_layer_fwd")
@@ -354,6 +399,12 @@ def mamba2_scan_fwd(x, dt_raw, A_log, Bm, Cm, Dskip, z=None, h0=None, *, y=None,
     lib = load_library()
     B, L, H, P = x.shape
     G, N = Bm.shape[2], Bm.shape[3]
+    io, f32 = x.dtype, torch.float32
+    _check_args([("x", x, (B, L, H, P), io), ("dt_raw", dt_raw, (B, L, H), io), ("A_log", A_log, (H,), f32),
+                 ("Bm", Bm, (B, L, G, N), io), ("Cm", Cm, (B, L, G, N), io), ("Dskip", Dskip, (H,), f32),
+                 ("z", z, (B, L, H, P), io), ("h0", h0, (B, H, N, P), f32), ("y", y, (B, L, H, P), io),
+                 ("final_state", final_state, (B, H, N, P), f32)],
+                P == 64 and N == D_STATE)
     if y is None:
         y = torch.empty_like(x)
     if final_state is None:
@@ -378,6 +429,13 @@ def mamba_step(h, conv_state, x_t, z_t, dt_raw_t, B_t, C_t, A_log, Dskip, conv_w
     conv_state (B,3,D) are updated in place; returns y_t (B,D)."""
     lib = load_library()
     B, D = x_t.shape
+    io, f32 = x_t.dtype, torch.float32
+    _check_args([("h", h, (B, D, D_STATE), f32), ("conv_state", conv_state, (B, D_CONV - 1, D), io),
+                 ("x_t", x_t, (B, D), io), ("z_t", z_t, (B, D), io), ("dt_raw_t", dt_raw_t, (B, D), io),
+                 ("B_t", B_t, (B, D_STATE), io), ("C_t", C_t, (B, D_STATE), io),
+                 ("A_log", A_log, (D, D_STATE), f32), ("Dskip", Dskip, (D,), f32),
+                 ("conv_w", conv_w, (D, D_CONV), f32), ("conv_b", conv_b, (D,), f32), ("y_t", y_t, (B, D), io)],
+                _scan_sizes_supported(A_log, conv_w))
     if y_t is None:
         y_t = torch.empty_like(x_t)
     a = StepArgs(batch=B, d_inner=D, d_state=A_log.shape[-1], d_conv=conv_w.shape[-1],
@@ -412,6 +470,10 @@ def mamba_scan_fwd_noalloc(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=No
     Calls that may overlap on the GPU share that scratch and race."""
     lib = load_library()
     B, L, D = x.shape
+    _check_args(_scan_specs(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b, h0, conv_state0)
+                + [("y", y, (B, L, D), x.dtype), ("final_h", final_h, (B, D, D_STATE), torch.float32),
+                   ("final_conv_state", final_conv_state, (B, D_CONV - 1, D), x.dtype)],
+                _scan_sizes_supported(A_log, conv_w))
     a = ScanArgs(batch=B, seqlen=L, d_inner=D, d_state=A_log.shape[-1], d_conv=conv_w.shape[-1],
                  io=_io_code(x), x=_ptr(x), z=_ptr(z), dt_raw=_ptr(dt_raw), Bm=_ptr(Bm),
                  Cm=_ptr(Cm), A_log=_ptr(A_log), Dskip=_ptr(Dskip), conv_w=_ptr(conv_w),

@@ -237,3 +237,112 @@ def test_tile_states_checks(lib):
             ops.mamba_scan_fwd(x, x, x, bc, bc, *p, tile_states=bad)
         with pytest.raises(ValueError):
             ops.mamba_scan_bwd(x, x, x, bc, bc, *p, dy=x, tile_states=bad)
+
+
+CUDA_MSG = "must be on a CUDA device"  # what a CPU tensor meets once every check before it passed
+
+
+def _scan_cpu(B=1, L=40, D=32, io=torch.bfloat16, N=16, K=4):
+    a = dict(x=torch.zeros(B, L, D, dtype=io), z=torch.zeros(B, L, D, dtype=io), dt_raw=torch.zeros(B, L, D, dtype=io),
+             Bm=torch.zeros(B, L, 16, dtype=io), Cm=torch.zeros(B, L, 16, dtype=io), A_log=torch.zeros(D, N),
+             Dskip=torch.ones(D), conv_w=torch.zeros(D, K), conv_b=torch.zeros(D), h0=torch.zeros(B, D, 16),
+             conv_state0=torch.zeros(B, 3, D, dtype=io))
+    return a
+
+
+@pytest.mark.parametrize("fn", ["fwd", "bwd", "noalloc"])
+def test_scan_bindings_check_shapes_before_any_device_access(fn):
+    """Every tensor's shape and dtype is checked against the sizes passed to
+    the C ABI (which sees bare pointers), before any device access."""
+    def call(**kw):
+        a = dict(_scan_cpu(), **kw)
+        args = [a[k] for k in ("x", "z", "dt_raw", "Bm", "Cm", "A_log", "Dskip", "conv_w", "conv_b", "h0",
+                               "conv_state0")]
+        extra = {k: a[k] for k in a if k not in ("x", "z", "dt_raw", "Bm", "Cm", "A_log", "Dskip", "conv_w",
+                                                  "conv_b", "h0", "conv_state0")}
+        if fn == "fwd":
+            return ops.mamba_scan_fwd(*args, **extra)
+        if fn == "bwd":
+            extra.setdefault("dy", torch.zeros(1, 40, 32, dtype=torch.bfloat16))
+            return ops.mamba_scan_bwd(*args, **extra)
+        extra.setdefault("y", torch.zeros(1, 40, 32, dtype=torch.bfloat16))
+        return ops.mamba_scan_fwd_noalloc(*args, **extra)
+
+    with pytest.raises(ValueError, match=CUDA_MSG):
+        call()  # consistent arguments pass every check
+    bad = [dict(z=torch.zeros(1, 39, 32, dtype=torch.bfloat16)), dict(Bm=torch.zeros(1, 40, 8, dtype=torch.bfloat16)),
+           dict(Dskip=torch.ones(16)), dict(conv_b=torch.zeros(31)), dict(h0=torch.zeros(1, 32, 8)),
+           dict(conv_state0=torch.zeros(1, 4, 32, dtype=torch.bfloat16))]
+    if fn == "bwd":
+        bad += [dict(dy=torch.zeros(1, 40, 16, dtype=torch.bfloat16)), dict(dfinal_h=torch.zeros(1, 16, 16)),
+                dict(out={"dB": torch.zeros(1, 40, 8)})]
+    elif fn == "fwd":
+        bad += [dict(y=torch.zeros(1, 20, 32, dtype=torch.bfloat16)), dict(final_h=torch.zeros(1, 32, 4))]
+    else:
+        bad += [dict(y=torch.zeros(1, 20, 32, dtype=torch.bfloat16))]
+    for kw in bad:
+        with pytest.raises(ValueError, match=next(iter(kw)) if "out" not in kw else "dB"):
+            call(**kw)
+    for kw in (dict(A_log=torch.zeros(32, 16, dtype=torch.bfloat16)), dict(z=torch.zeros(1, 40, 32))):
+        with pytest.raises(TypeError):
+            call(**kw)
+    # an unsupported state size is the library's to refuse: no shape check
+    with pytest.raises(ValueError, match=CUDA_MSG):
+        call(A_log=torch.zeros(32, 8))
+
+
+def test_step_layer_mamba2_bindings_check_shapes():
+    B, D = 2, 32
+    bf = torch.bfloat16
+    st = dict(h=torch.zeros(B, D, 16), conv_state=torch.zeros(B, 3, D, dtype=bf), x_t=torch.zeros(B, D, dtype=bf),
+              z_t=torch.zeros(B, D, dtype=bf), dt_raw_t=torch.zeros(B, D, dtype=bf), B_t=torch.zeros(B, 16, dtype=bf),
+              C_t=torch.zeros(B, 16, dtype=bf), A_log=torch.zeros(D, 16), Dskip=torch.ones(D),
+              conv_w=torch.zeros(D, 4))
+
+    def step(**kw):
+        return ops.mamba_step(**dict(st, **kw))
+
+    with pytest.raises(ValueError, match=CUDA_MSG):
+        step()
+    for kw in (dict(h=torch.zeros(B, D, 8)), dict(conv_state=torch.zeros(B, 2, D, dtype=bf)),
+               dict(C_t=torch.zeros(1, 16, dtype=bf)), dict(y_t=torch.zeros(B, D + 1, dtype=bf))):
+        with pytest.raises(ValueError, match=next(iter(kw))):
+            step(**kw)
+    with pytest.raises(ValueError, match=CUDA_MSG):
+        step(A_log=torch.zeros(D, 8))  # unsupported: left to the library
+
+    Bt, L, H, Di, R = 1, 16, 64, 32, 8
+    lw = dict(hidden=torch.zeros(Bt, L, H, dtype=bf), W_in=torch.zeros(2 * Di, H, dtype=bf), conv_w=torch.zeros(Di, 4),
+              conv_b=torch.zeros(Di), W_x=torch.zeros(R + 32, Di, dtype=bf), W_dt=torch.zeros(Di, R, dtype=bf),
+              b_dt=torch.zeros(Di, dtype=bf), A_log=torch.zeros(Di, 16), Dskip=torch.ones(Di),
+              W_out=torch.zeros(H, Di, dtype=bf))
+
+    def layer(**kw):
+        return ops.mamba_layer_fwd(**dict(lw, **kw))
+
+    with pytest.raises(ValueError, match=CUDA_MSG):
+        layer()
+    for kw in (dict(W_in=torch.zeros(Di, H, dtype=bf)), dict(W_x=torch.zeros(R + 16, Di, dtype=bf)),
+               dict(W_out=torch.zeros(Di, H, dtype=bf)), dict(u_out=torch.zeros(Bt, L, H, dtype=bf))):
+        with pytest.raises(ValueError, match=next(iter(kw))):
+            layer(**kw)
+    with pytest.raises(TypeError, match="b_dt"):
+        layer(b_dt=torch.zeros(Di))
+    with pytest.raises(ValueError, match=CUDA_MSG):
+        layer(W_dt=torch.zeros(Di, 6, dtype=bf))  # dt_rank 6: unsupported, left to the library
+
+    Hh, G = 4, 2
+    m2 = dict(x=torch.zeros(Bt, L, Hh, 64, dtype=bf), dt_raw=torch.zeros(Bt, L, Hh, dtype=bf), A_log=torch.zeros(Hh),
+              Bm=torch.zeros(Bt, L, G, 16, dtype=bf), Cm=torch.zeros(Bt, L, G, 16, dtype=bf), Dskip=torch.ones(Hh))
+
+    def mamba2(**kw):
+        return ops.mamba2_scan_fwd(**dict(m2, **kw))
+
+    with pytest.raises(ValueError, match=CUDA_MSG):
+        mamba2()
+    for kw in (dict(dt_raw=torch.zeros(Bt, L, G, dtype=bf)), dict(Cm=torch.zeros(Bt, L, 1, 16, dtype=bf)),
+               dict(h0=torch.zeros(Bt, Hh, 64, 16)), dict(z=torch.zeros(Bt, L, Hh, 32, dtype=bf))):
+        with pytest.raises(ValueError, match=next(iter(kw))):
+            mamba2(**kw)
+    with pytest.raises(ValueError, match=CUDA_MSG):
+        mamba2(x=torch.zeros(Bt, L, Hh, 32, dtype=bf))  # head_dim 32: unsupported, left to the library
