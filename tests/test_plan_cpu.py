@@ -1,0 +1,86 @@
+"""The host-side work plan and workspace sizes of the prefill scan and its
+backward, over many sizes (hypothesis), without a GPU: the plan covers the
+sequence in whole 16-token tiles, its carry pieces cover a chunk, an explicit
+chunk count is honoured as a bound, and the workspace sizes equal the
+documented layouts summed here independently."""
+import pytest
+from hypothesis import given, settings, strategies as st
+
+from selective_state_space_118_b300 import ops
+
+T = 16  # tokens per tile
+
+
+def r256(v):
+    return (v + 255) // 256 * 256
+
+
+def fwd_workspace(B, L, D, n):
+    """B/C rows widened to fp32 (B, L, 32); in chunked mode the carries
+    (B, n, D, 16) and the counters (a ticket and one flag per (row, group,
+    chunk))."""
+    total = r256(B * L * 32 * 4)
+    if n <= 1:
+        return total
+    counters = r256(total + B * n * D * 16 * 4)
+    return r256(counters + (1 + B * -(-D // 32) * n) * 4)  # groups of 32 channels, rounded up
+
+
+def bwd_workspace(B, L, D, n):
+    """The forward's workspace, the tile states (B, tiles, D, 16), chunked:
+    the adjoint carries and their counters; the per-group dB | dC sums, the
+    per-chunk parameter partials (B n, D, 24) and, chunked, the conv edge
+    buffers (B, n, 3, D) twice."""
+    G = -(-D // 32)
+    o = fwd_workspace(B, L, D, n)
+    o = r256(o + B * (-(-L // T)) * D * 16 * 4)
+    if n > 1:
+        o = r256(o + B * n * D * 16 * 4)
+        o = r256(o + (1 + B * G * n) * 4)
+    o = r256(o + G * B * L * 32 * 4)
+    o = r256(o + B * n * D * 24 * 4)
+    if n > 1:
+        o = r256(o + B * n * 3 * D * 4)
+        o = r256(o + B * n * 3 * D * 4)
+    return o
+
+
+sizes = st.tuples(st.integers(1, 4), st.integers(1, 300_000), st.integers(1, 1024).map(lambda k: 16 * k),
+                  st.integers(0, 80))
+
+
+@settings(max_examples=300, deadline=None)
+@given(sizes)
+def test_plan_invariants(s):
+    B, L, D, n_req = s
+    pl = ops.mamba_scan_plan(B, L, D, n_req)
+    n, C, m, P = pl["n_chunks"], pl["chunk_len"], pl["pieces"], pl["piece_len"]
+    tiles = -(-L // T)
+    assert n >= 1 and C % T == 0
+    assert n * C >= tiles * T and (n - 1) * C < L  # every chunk holds tokens, the chunks cover L
+    if n_req == 1 or tiles == 1:
+        assert n == 1
+    if n_req >= 1:
+        assert n <= n_req
+    else:
+        assert n <= 64 and n == ops.mamba_scan_default_chunks(B, L, D)
+    if n > 1:
+        assert P % T == 0 and 0 < P <= 256
+        assert m * P >= C > (m - 1) * P  # the carry pieces cover one chunk
+    else:
+        assert (m, P) == (0, 0) and C == tiles * T
+
+
+@settings(max_examples=300, deadline=None)
+@given(sizes)
+def test_workspace_sizes_follow_the_layouts(s):
+    B, L, D, n_req = s
+    n = ops.mamba_scan_plan(B, L, D, n_req)["n_chunks"]
+    assert ops.mamba_scan_workspace_size(B, L, D, n_req) == fwd_workspace(B, L, D, n)
+    assert ops.mamba_scan_bwd_workspace_size(B, L, D, n_req) == bwd_workspace(B, L, D, n)
+
+
+@pytest.mark.parametrize("args", [(0, 10, 16, 0), (1, 0, 16, 0), (1, 10, 0, 0), (1, 10, 24, 0), (1, 10, 16, -1)])
+def test_sizes_without_a_plan(args):
+    assert ops.mamba_scan_workspace_size(*args) == 0
+    assert ops.mamba_scan_bwd_workspace_size(*args) == 0
