@@ -84,3 +84,27 @@ def test_workspace_sizes_follow_the_layouts(s):
 def test_sizes_without_a_plan(args):
     assert ops.mamba_scan_workspace_size(*args) == 0
     assert ops.mamba_scan_bwd_workspace_size(*args) == 0
+
+
+@settings(max_examples=200, deadline=None)
+@given(sizes, st.integers(1, 64).map(lambda k: 8 * k), st.booleans())
+def test_layer_workspace_follows_its_layout(s, R, with_u_out):
+    """x, z, u (unless the caller takes u), the x_proj output (rows, R + 32),
+    dt_raw and y, all bf16; then the scan's workspace; then 32 MiB of GEMM
+    scratch."""
+    B, L, D, n_req = s
+    H = 2 * D
+    act = r256(B * L * D * 2)
+    n = ops.mamba_scan_plan(B, L, D, n_req)["n_chunks"]
+    want = (4 if with_u_out else 5) * act + r256(B * L * (R + 32) * 2) + fwd_workspace(B, L, D, n) + (32 << 20)
+    assert ops.mamba_layer_workspace_size(B, L, H, D, R, n_req, with_u_out) == want
+
+
+@settings(max_examples=200, deadline=None)
+@given(st.integers(1, 8), st.integers(1, 300_000), st.integers(1, 256))
+def test_mamba2_workspace_follows_its_layout(B, L, H):
+    """Per (row, head, 64-token chunk): the chunk's end state and entering
+    state (16 x 64 fp32 each), its decay sum, and per token the dt and decay
+    prefix (64 x 2 fp32)."""
+    k = B * H * -(-L // 64)
+    assert ops.mamba2_scan_workspace_size(B, L, H) == 2 * r256(k * 16 * 64 * 4) + r256(k * 4) + r256(k * 64 * 2 * 4)
