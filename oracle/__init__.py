@@ -1,7 +1,7 @@
 """fp64 CPU oracle of the Mamba selective-scan layer -- TEST INFRASTRUCTURE.
 
-Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
-``bench.py`` may import this package.  The library under
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg and
+reference arm of ``bench.py`` may import this package.  The library under
 ``selective_state_space_118_b300`` never imports it, and it imports nothing
 from the library: the two share no code.
 
