@@ -27,6 +27,7 @@ import numpy as np
 import pytest
 import torch
 import torch.nn.functional as F
+from hypothesis import given, settings, strategies as st
 
 import oracle
 
@@ -339,3 +340,22 @@ def test_pin(pin):
 @pytest.mark.parametrize("chunk", [1, 5, 16, 37, 64, 100])
 def test_chunked_equals_sequential(chunk):
     pin_chunked_equals_sequential(chunk)
+
+
+
+@settings(max_examples=60, deadline=None)
+@given(st.integers(1, 2), st.integers(1, 20), st.integers(1, 3), st.integers(1, 16), st.integers(2, 4),
+       st.booleans(), st.booleans(), st.integers(0, 2 ** 31 - 1))
+def test_brute_force_closed_form_over_shapes(B, L, D, N, K, with_state, with_bias, seed):
+    """The closed form of the recurrence on random small shapes: every
+    sequence length from 1 (conv state only), every state and conv width the
+    oracle accepts, with and without initial states and conv bias."""
+    c = rand_case(B=B, L=L, D=D, N=N, K=K, seed=seed, with_state=with_state)
+    if not with_bias:
+        c["conv_b"] = None
+    y, fh, fcs = run(c)
+    yb, fhb = brute_force(c)
+    assert relerr(y, yb) < 1e-11
+    assert relerr(fh, fhb) < 1e-11
+    prev = c["conv_state0"] if with_state else np.zeros((B, K - 1, D))
+    np.testing.assert_array_equal(fcs, np.concatenate([prev, c["x"]], axis=1)[:, -(K - 1):])
