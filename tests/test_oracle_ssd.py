@@ -11,6 +11,7 @@ than its recurrence.
 """
 import numpy as np
 import pytest
+from hypothesis import given, settings, strategies as st
 
 import oracle
 
@@ -109,3 +110,17 @@ def test_dual_form_rejects_planted_mistakes(tmp_path, what, old, new):
     y, fs = oracle.ssd(**p, lib=lib)
     yr, fsr = dual_form(p)
     assert not (np.allclose(y, yr, rtol=1e-8, atol=1e-10) and np.allclose(fs, fsr, rtol=1e-8, atol=1e-10)), what
+
+
+@settings(max_examples=60, deadline=None)
+@given(st.integers(1, 2), st.integers(1, 40), st.integers(1, 3), st.integers(1, 3), st.integers(1, 5),
+       st.integers(1, 8), st.booleans(), st.booleans(), st.integers(0, 2 ** 31 - 1))
+def test_dual_form_over_shapes(B, L, G, hpg, P, N, gate, state, seed):
+    """The quadratic form on random small shapes: any number of groups and
+    heads per group, head and state widths, with and without gate and
+    initial state."""
+    p = problem(B=B, L=L, H=G * hpg, P=P, G=G, N=N, seed=seed, gate=gate, state=state)
+    y, fs = oracle.ssd(**p)
+    yr, fsr = dual_form(p)
+    np.testing.assert_allclose(y, yr, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(fs, fsr, rtol=1e-9, atol=1e-11)
