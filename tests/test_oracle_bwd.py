@@ -9,6 +9,7 @@ plausible mistakes in a copy of the backward and checks that the finite
 differences reject each."""
 import numpy as np
 import pytest
+from hypothesis import given, settings, strategies as st
 
 import oracle
 
@@ -73,6 +74,25 @@ def test_backward_matches_finite_differences(B, L, D, big_dt):
     p, w = problem(B, L, D, seed=10 * L + D, big_dt=big_dt)
     ok, msg = fd_check(p, w)
     assert ok, msg
+
+
+
+@settings(max_examples=40, deadline=None)
+@given(st.integers(1, 2), st.integers(1, 40), st.integers(1, 4), st.booleans(), st.integers(0, 2 ** 31 - 1))
+def test_backward_matches_a_directional_derivative(B, L, D, big_dt, seed):
+    """On random shapes (longer sequences than the per-coordinate check
+    reaches): the loss's central difference along one random direction in
+    all inputs at once equals the gradients' inner product with it."""
+    p, w = problem(B, L, D, seed=seed, big_dt=big_dt)
+    g = oracle.scan_bwd(**p, **w)
+    rng = np.random.default_rng(seed + 1)
+    v = {k: rng.normal(size=p[k].shape) for k in NAMES_IN}
+    eps = 1e-6
+    plus = {k: p[k] + eps * v[k] for k in NAMES_IN}
+    minus = {k: p[k] - eps * v[k] for k in NAMES_IN}
+    fd = (loss(plus, w) - loss(minus, w)) / (2 * eps)
+    an = sum(float(np.sum(g[GRAD_OF[k]] * v[k])) for k in NAMES_IN)
+    assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (fd, an)
 
 
 MUTANTS = [
