@@ -19,6 +19,7 @@ import inspect
 import numpy as np
 import pytest
 import torch
+from hypothesis import given, settings, strategies as st
 
 import oracle
 
@@ -99,6 +100,21 @@ def test_layer_closed_form():
     np.testing.assert_allclose(r["final_h"], fh, rtol=1e-10, atol=1e-14)
     rms = np.sqrt(np.mean(out ** 2))
     assert np.abs(r["out"] - out).max() <= 1e-2 * rms
+
+
+
+@settings(max_examples=30, deadline=None, derandomize=True)
+@given(st.integers(1, 2), st.integers(1, 60), st.integers(1, 6).map(lambda k: 8 * k),
+       st.integers(1, 6).map(lambda k: 8 * k), st.integers(1, 4).map(lambda k: 4 * k), st.integers(0, 2 ** 31 - 1))
+def test_layer_closed_form_over_shapes(B, L, H, D, R, seed):
+    """The geometric-series closed form on random small layer shapes."""
+    p = problem(B=B, L=L, H=H, D=D, R=R, seed=seed, zero_x=True)
+    r = oracle.layer(**p)
+    y, out, fh = closed_form(p)
+    np.testing.assert_allclose(r["y"], y, rtol=2.0 ** -7, atol=1e-12)
+    np.testing.assert_allclose(r["final_h"], fh, rtol=1e-10, atol=1e-14)
+    rms = np.sqrt(np.mean(out ** 2))
+    assert np.abs(r["out"] - out).max() <= 1e-2 * rms + 1e-300
 
 
 MUTANTS = [
