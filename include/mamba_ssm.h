@@ -16,9 +16,9 @@
  *   h_n  = exp(dt*A_n) * h_n + dt*B[b,t,n]*u  (n = 0..15; h starts at h0 or 0)
  *   y    = (sum_n C[b,t,n]*h_n + D[c]*u) * silu(z[b,t,c])
  *
- * The projections around the scan (in_proj producing x and z, x_proj
- * producing B, C and the dt input, dt_proj, out_proj) are not part of this
- * library: the caller passes their results.
+ * The scan calls take the results of the projections around the scan
+ * (in_proj producing x and z, x_proj producing B, C and the dt input,
+ * dt_proj) from the caller; mamba_layer_fwd below runs the projections too.
  *
  * Conventions for every call below.
  *  - All tensor pointers are DEVICE pointers (CUDA global memory), row-major
@@ -170,10 +170,10 @@ mamba_status mamba_scan_fwd_noalloc(const mamba_scan_args *args, void *stream);
  * dl/dfinal_h and dl/dfinal_conv_state -- the chain rule through the
  * recurrence stated at the top of this file (for training the layer of
  * "实现 > Mamba 层"; the pages train it end to end but print no backward, so
- * this is the plain reverse-mode derivative of that forward).  The forward
- * pass is recomputed inside the call (it stores the state entering every
- * 16-token tile in the workspace); nothing from an earlier forward call is
- * needed.
+ * this is the plain reverse-mode derivative of that forward).  Unless
+ * tile_states is given, the forward pass is recomputed inside the call (it
+ * stores the state entering every 16-token tile in the workspace), so
+ * nothing from an earlier forward call is needed.
  *
  *   x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b, h0, conv_state0
  *                     the forward's inputs, as for mamba_scan_fwd
@@ -332,8 +332,9 @@ mamba_status mamba_layer_fwd(const mamba_layer_args *args, void *stream);
  *   A_log, Dskip      (heads) fp32
  *   h0, final_state   (B, heads, 16, 64) fp32 or NULL
  *   workspace         mamba2_scan_workspace_size() bytes, 256-byte aligned:
- *                     two (B, heads, chunks, 16, 64) fp32 state arrays and the
- *                     chunks' decay sums (chunks of 64 tokens)
+ *                     per (batch row, head, chunk of 64 tokens) the chunk's
+ *                     end state and entering state (16 x 64 fp32 each), its
+ *                     decay sum, and per token its dt and decay prefix
  *
  * bf16 I/O only; head_dim 64 and d_state 16 only; heads % groups == 0.
  * seqlen may be 0 (then final_state = h0, or zeros).
