@@ -64,6 +64,20 @@ typedef enum { MAMBA_F32 = 0, MAMBA_BF16 = 1 } mamba_dtype;
  * mamba_last_error().  Never set in normal use. */
 #define MAMBA_FLAG_TEST_STALL_FIRST_LOAD 0x1u
 
+/* Flag for mamba_scan_args.flags and mamba_scan_bwd_args.flags: exact chunk
+ * carries.  In chunked mode (n_chunks > 1) the carry entering a chunk is
+ * normally gathered by walking the previous chunk backwards until every
+ * state has decayed below 2^-32 on its way to the boundary; what lies
+ * further back is then dropped.  The dropped part is at most 2^-32 times the
+ * size of the state where the walk stopped, far below fp32 rounding for
+ * states of comparable size along the sequence; it can only show when a
+ * state >= ~1e5 times larger than the state at the boundary was hidden from
+ * y (zero C, D and gate) while it decayed.  With this flag every walk covers
+ * its whole chunk and folds in the carry before it: the result then equals
+ * the sequential recurrence up to rounding for any inputs, at the cost of a
+ * carry pass as long as the main pass.  No effect with n_chunks = 1. */
+#define MAMBA_FLAG_EXACT_CARRY 0x2u
+
 /*
  * Prefill: the scan over a whole sequence (MambaBlock.forward minus the
  * projections).
@@ -93,7 +107,8 @@ typedef enum { MAMBA_F32 = 0, MAMBA_BF16 = 1 } mamba_dtype;
  *                     the chunks before it, computed by a first pass over the
  *                     earlier chunks cut into pieces (two passes; results
  *                     agree with the sequential pass to rounding)
- *   flags             0, or MAMBA_FLAG_TEST_* (tests only)
+ *   flags             0, MAMBA_FLAG_EXACT_CARRY, or MAMBA_FLAG_TEST_* (tests
+ *                     only)
  *   wait_timeout_ns   limit of every device-side wait (0: 1 second)
  *   tile_states       NULL, or (B, ceil(L/16), D, 16) fp32: the state entering
  *                     every 16-token tile is stored there (B*L*D*4 bytes,
@@ -151,9 +166,11 @@ mamba_status mamba_scan_fwd(const mamba_scan_args *args, void *stream);
  *  - Calls whose mamba_scan_workspace_size() exceeds that size are rejected
  *    with MAMBA_ERR_WORKSPACE before anything runs (one sequential pass fits
  *    up to batch * seqlen = 262,144 tokens).
- *  - The first call on a device looks the array's device address up (once,
- *    with that device current); make that first call before any stream
- *    capture.
+ *  - The array's device address belongs to the CUDA context the library's
+ *    kernels are loaded into.  The first call in a context (the first on a
+ *    device; again after cudaDeviceReset, or from a thread with another
+ *    context of its own current) looks it up and remembers it for that
+ *    context; make that first call before any stream capture.
  *  - All calls share the one array: calls that may overlap on the GPU (two
  *    streams, or two threads) race and corrupt each other's results; order
  *    them on one stream.  The array keeps the last call's contents; every
@@ -200,6 +217,8 @@ mamba_status mamba_scan_fwd_noalloc(const mamba_scan_args *args, void *stream);
  *                     chunked mode the adjoint entering each chunk from the
  *                     right is computed first, the way the forward computes
  *                     its carries, with time reversed
+ *   flags             0 or MAMBA_FLAG_EXACT_CARRY (both the forward's carries
+ *                     and the adjoint carries then walk whole chunks)
  *   wait_timeout_ns   limit of every device-side wait (0: 1 second)
  *   tile_states       NULL: the forward is recomputed inside the call, storing
  *                     the tile states in the workspace.  Or the tile_states

@@ -71,13 +71,30 @@ struct Machine {
   int summary_per_sm;
 };
 
-Machine machine() {
+Machine query_machine() {
   Machine m{sm_count(), 16, 20};
   int a = 0, b = 0;
   mamba::scan_occupancy(IoType::BF16, &a, &b);
   if (a > 0) m.main_per_sm = a;
   if (b > 0) m.summary_per_sm = b;
   return m;
+}
+
+// The machine of the current device, queried once per device (the plan is
+// made on every call; the occupancy queries behind it cost host time).
+Machine machine() {
+  constexpr int kMaxDev = 64;
+  static Machine cache[kMaxDev];
+  static bool have[kMaxDev] = {};
+  static std::mutex mu;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return query_machine();
+  std::lock_guard<std::mutex> lock(mu);
+  if (!have[dev]) {
+    cache[dev] = query_machine();
+    have[dev] = true;
+  }
+  return cache[dev];
 }
 
 // Modelled time of a kernel pass that runs `items` one-warp CTAs of `tiles`
@@ -494,6 +511,7 @@ mamba_status mamba_scan_bwd(const mamba_scan_bwd_args* a, void* stream_v) {
   fa.workspace = a->workspace;
   fa.workspace_bytes = a->workspace_bytes;
   fa.wait_timeout_ns = timeout;
+  fa.flags = a->flags & MAMBA_FLAG_EXACT_CARRY;
   const mamba::ScanParams fp = fwd_params(&fa, pl, ws.fwd, ckpt);
 
   float* bc = reinterpret_cast<float*>(wsp + ws.fwd.bc);
@@ -532,6 +550,7 @@ mamba_status mamba_scan_bwd(const mamba_scan_bwd_args* a, void* stream_v) {
   p.part_param = reinterpret_cast<float*>(wsp + ws.part_param);
   p.dh0 = a->dh0;
   p.dconv_state0 = a->dconv_state0;
+  p.flags = a->flags & MAMBA_FLAG_EXACT_CARRY;
   p.timeout_ns = timeout;
 
   // 1. B/C rows widened; 2. chunked mode: the forward's chunk carries (when

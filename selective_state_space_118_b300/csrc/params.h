@@ -9,6 +9,10 @@ namespace mamba {
 // Tokens per tile: the unit of the TMA ring and of every chunk and piece.
 constexpr int kTileTokens = 16;
 
+// Bits of ScanParams::flags / BwdParams::flags (the public MAMBA_FLAG_*).
+constexpr uint32_t kFlagTestStallFirstLoad = 1u;
+constexpr uint32_t kFlagExactCarry = 2u;  // chunk-carry walks never drop decayed terms
+
 struct ScanParams {
   int batch, seqlen, d_inner;
   int n_groups;     // ceil(d_inner / 32): one CTA (warp) per group of 32 channels
@@ -61,6 +65,7 @@ struct BwdParams {
   float* edge_dpre;                 // (B, n_chunks, 3, D): d(conv output) of its first 3 tokens
   float* dh0;                       // (B, D, 16) or null
   float* dconv_state0;              // (B, 3, D) fp32 or null
+  uint32_t flags;                   // kFlagExactCarry or 0
   uint64_t timeout_ns;
 };
 

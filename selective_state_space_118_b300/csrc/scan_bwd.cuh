@@ -600,6 +600,7 @@ __device__ __forceinline__ void acarry_warp(const CUtensorMap& tm_z, const CUten
 #pragma unroll
   for (int k = 0; k < 8; ++k) wgt.h[k] = make_float2(1.0f, 1.0f);
   float s_before = 0.0f, sdt = 0.0f;
+  const bool exact = (p.flags & kFlagExactCarry) != 0;  // walk the whole chunk, drop nothing
 
   bool ok = true, done = false;
   int k = 0;
@@ -639,7 +640,7 @@ __device__ __forceinline__ void acarry_warp(const CUtensorMap& tm_z, const CUten
       state16_zero(zero);
       state16_fold(wgt, ch.a2, sdt, zero);
       s_before = __fadd_rn(s_before, sdt);
-      if (__all_sync(0xffffffffu, !active || __fmul_rn(a2max, s_before) < kCarryDropLog2)) {
+      if (!exact && __all_sync(0xffffffffu, !active || __fmul_rn(a2max, s_before) < kCarryDropLog2)) {
         done = true;
         ++k;
         break;

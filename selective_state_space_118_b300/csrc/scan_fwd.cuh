@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kLanes)
   }
   __syncwarp();
 
-  const bool stall_test = (p.flags & 1u) != 0;
+  const bool stall_test = (p.flags & kFlagTestStallFirstLoad) != 0;
   constexpr uint32_t kBytes = (kY ? 3 : 2) * kT * kLanes * sizeof(IO) + kT * kBC * sizeof(float);
   if (lane == 0) {
     for (int k = 0; k < kStages && k < n_tiles; ++k) {
@@ -414,6 +414,7 @@ __device__ __forceinline__ void carry_warp(const CUtensorMap& tm_x, const CUtens
 #pragma unroll
   for (int k = 0; k < 8; ++k) wgt.h[k] = make_float2(1.0f, 1.0f);
   float s_after = 0.0f;  // dt summed from the current piece's end to the boundary
+  const bool exact = (p.flags & kFlagExactCarry) != 0;  // walk the whole chunk, drop nothing
 
   bool ok = true, done = false;
   int k = 0;
@@ -447,7 +448,7 @@ __device__ __forceinline__ void carry_warp(const CUtensorMap& tm_x, const CUtens
       state16_zero(zero);
       state16_fold(wgt, ch.a2, sdt, zero);
       s_after = __fadd_rn(s_after, sdt);
-      if (__all_sync(0xffffffffu, !active || __fmul_rn(a2max, s_after) < kCarryDropLog2)) {
+      if (!exact && __all_sync(0xffffffffu, !active || __fmul_rn(a2max, s_after) < kCarryDropLog2)) {
         done = true;
         ++k;
         break;

@@ -87,6 +87,31 @@ def _dt_raw(g, shape, device, lo=1e-3, hi=1e-1):
     return torch.log(torch.expm1(dt))
 
 
+# dt_raw ranges of the wide-range draw (one per 16-token block): every value
+# below the softplus's small-argument bound; the full range across the
+# threshold 20; a narrow band around the small-argument bound (-2.08); and
+# values past the threshold only or near it.
+WIDE_DT_RANGES = ((-9.0, -2.2), (-30.0, 30.0), (-2.3, -1.85), (12.0, 30.0))
+
+
+def wide_dt_raw(batch: int, seqlen: int, d_inner: int, io: str, seed: int, device="cpu") -> torch.Tensor:
+    """dt_raw (B, L, D) in the I/O dtype spanning [-30, 30]: each block of 16
+    consecutive tokens draws uniformly from one of WIDE_DT_RANGES, the range
+    chosen at random per block, so that some 16-token tiles lie entirely in
+    one region and others mix all of them."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    blocks = (seqlen + 15) // 16
+    mode = torch.randint(0, len(WIDE_DT_RANGES), (batch, blocks), generator=g, device=dev)
+    lo = torch.tensor([r[0] for r in WIDE_DT_RANGES], device=dev)[mode]
+    hi = torch.tensor([r[1] for r in WIDE_DT_RANGES], device=dev)[mode]
+    lo = lo.repeat_interleave(16, dim=1)[:, :seqlen, None]
+    hi = hi.repeat_interleave(16, dim=1)[:, :seqlen, None]
+    r = torch.rand((batch, seqlen, d_inner), generator=g, device=dev, dtype=torch.float32)
+    return (lo + r * (hi - lo)).to(torch_dtype(io))
+
+
 def layer_params(d_inner: int, g: torch.Generator, device) -> dict:
     """Per-layer parameters (fp32): A_log, D, conv_w, conv_b."""
     n = torch.arange(D_STATE, device=device, dtype=torch.float32)

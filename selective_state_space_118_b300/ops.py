@@ -22,6 +22,7 @@ MAMBA_OK, MAMBA_ERR_INVALID_ARG, MAMBA_ERR_UNSUPPORTED, MAMBA_ERR_CUDA, MAMBA_ER
     MAMBA_ERR_WORKSPACE = range(6)
 MAMBA_F32, MAMBA_BF16 = 0, 1
 MAMBA_FLAG_TEST_STALL_FIRST_LOAD = 0x1
+MAMBA_FLAG_EXACT_CARRY = 0x2
 D_STATE, D_CONV = 16, 4
 
 # the functions the public header declares (checked by the tests)
@@ -205,6 +206,17 @@ def _stream(stream) -> int:
     return s.cuda_stream
 
 
+def _launch(fn, args, stream, dev: torch.device) -> int:
+    """Calls the C entry point with `dev` (the tensors' device) as the current
+    device: the library launches on the current device and takes its
+    per-device resources from it.  A stream given must belong to `dev`."""
+    if stream is not None and stream.device != dev:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {dev}")
+    with torch.cuda.device(dev):
+        s = torch.cuda.current_stream(dev) if stream is None else stream
+        return fn(ctypes.byref(args), s.cuda_stream)
+
+
 def mamba_scan_workspace_size(batch: int, seqlen: int, d_inner: int, n_chunks: int = 0) -> int:
     return int(load_library().mamba_scan_workspace_size(batch, seqlen, d_inner, n_chunks))
 
@@ -262,7 +274,7 @@ def mamba_scan_fwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=N
                  workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
                  n_chunks=n_chunks, flags=flags, wait_timeout_ns=wait_timeout_ns,
                  tile_states=_ptr(tile_states))
-    st = lib.mamba_scan_fwd(ctypes.byref(a), _stream(stream))
+    st = _launch(lib.mamba_scan_fwd, a, stream, dev)
     if st != MAMBA_OK:
         raise MambaError(st, "mamba_scan_fwd")
     return y, final_h, final_conv_state
@@ -292,7 +304,7 @@ def _check_tile_states(t, batch: int, seqlen: int, d_inner: int) -> None:
 
 def mamba_scan_bwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=None,
                    conv_state0=None, *, dy, dfinal_h=None, dfinal_conv_state=None,
-                   out=None, workspace=None, n_chunks: int = 0, wait_timeout_ns: int = 0,
+                   out=None, workspace=None, n_chunks: int = 0, flags: int = 0, wait_timeout_ns: int = 0,
                    tile_states=None, stream=None) -> dict:
     """Backward of the prefill scan (C ABI ``mamba_scan_bwd``): the gradients
     of l given dy = dl/dy (B,L,D) and optionally dl/dfinal_h (B,D,16) fp32 and
@@ -335,9 +347,9 @@ def mamba_scan_bwd(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=None, h0=N
                 **{k: _ptr(g[k]) for k in BWD_OUTPUTS},
                 workspace=_ptr(workspace),
                 workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
-                n_chunks=n_chunks, flags=0, wait_timeout_ns=wait_timeout_ns,
+                n_chunks=n_chunks, flags=flags, wait_timeout_ns=wait_timeout_ns,
                 tile_states=_ptr(tile_states))
-    st = lib.mamba_scan_bwd(ctypes.byref(a), _stream(stream))
+    st = _launch(lib.mamba_scan_bwd, a, stream, dev)
     if st != MAMBA_OK:
         raise MambaError(st, "mamba_scan_bwd")
     return g
@@ -381,7 +393,7 @@ def mamba_layer_fwd(hidden, W_in, conv_w, conv_b, W_x, W_dt, b_dt, A_log, Dskip,
                   final_h=_ptr(final_h), final_conv_state=_ptr(final_conv_state), workspace=_ptr(workspace),
                   workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
                   n_chunks=n_chunks)
-    st = lib.mamba_layer_fwd(ctypes.byref(a), _stream(stream))
+    st = _launch(lib.mamba_layer_fwd, a, stream, hidden.device)
     if st != MAMBA_OK:
         raise MambaError(st, "mamba_layer_fwd")
     return out
@@ -417,7 +429,7 @@ def mamba2_scan_fwd(x, dt_raw, A_log, Bm, Cm, Dskip, z=None, h0=None, *, y=None,
                    Dskip=_ptr(Dskip), h0=_ptr(h0), y=_ptr(y), final_state=_ptr(final_state),
                    workspace=_ptr(workspace),
                    workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
-    st = lib.mamba2_scan_fwd(ctypes.byref(a), _stream(stream))
+    st = _launch(lib.mamba2_scan_fwd, a, stream, x.device)
     if st != MAMBA_OK:
         raise MambaError(st, "mamba2_scan_fwd")
     return y, final_state
@@ -443,7 +455,7 @@ def mamba_step(h, conv_state, x_t, z_t, dt_raw_t, B_t, C_t, A_log, Dskip, conv_w
                  z_t=_ptr(z_t), dt_raw_t=_ptr(dt_raw_t), B_t=_ptr(B_t), C_t=_ptr(C_t),
                  A_log=_ptr(A_log), Dskip=_ptr(Dskip), conv_w=_ptr(conv_w), conv_b=_ptr(conv_b),
                  y_t=_ptr(y_t))
-    st = lib.mamba_step(ctypes.byref(a), _stream(stream))
+    st = _launch(lib.mamba_step, a, stream, x_t.device)
     if st != MAMBA_OK:
         raise MambaError(st, "mamba_step")
     return y_t
@@ -480,7 +492,7 @@ def mamba_scan_fwd_noalloc(x, z, dt_raw, Bm, Cm, A_log, Dskip, conv_w, conv_b=No
                  conv_b=_ptr(conv_b), h0=_ptr(h0), conv_state0=_ptr(conv_state0), y=_ptr(y),
                  final_h=_ptr(final_h), final_conv_state=_ptr(final_conv_state),
                  workspace=None, workspace_bytes=0, n_chunks=n_chunks, flags=0, wait_timeout_ns=0)
-    st = lib.mamba_scan_fwd_noalloc(ctypes.byref(a), _stream(stream))
+    st = _launch(lib.mamba_scan_fwd_noalloc, a, stream, x.device)
     if st != MAMBA_OK:
         raise MambaError(st, "mamba_scan_fwd_noalloc")
     return y, final_h, final_conv_state

@@ -22,13 +22,16 @@ def _check_line(d, n_gpus):
               "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
         assert k in d, k
     assert d["n_gpus"] == n_gpus and d["value"] > 0 and d["higher_is_better"] is True
-    assert d["config"]["workload"] == "jamba_prefill_bf16_b1_l32768_d8192"
+    assert d["config"]["workload"] == "prefill_256k_bf16_b1_l262144_d8192"
+    assert d["config"]["calls_per_step"] == 64
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
-    # the time of one step is the whole workload at the measured rate
-    elems = d["config"]["batch"] * d["config"]["seqlen"] * d["config"]["d_inner"]
-    assert d["ms_per_step"] == pytest.approx(elems / d["value"] * 1e3)
+    # a step is the bounded sample actually timed: ms_per_step is its time
+    # and the value its rate, so steps x ms_per_step is the time really spent
+    assert 0 < d["elements_per_step"] < d["config"]["batch"] * d["config"]["seqlen"] * d["config"]["d_inner"]
+    assert d["ms_per_step"] == pytest.approx(d["elements_per_step"] / d["value"] * 1e3)
+    assert d["ms_per_step"] < 60e3
 
 
 @pytest.mark.timeout(300)

@@ -222,3 +222,29 @@ def test_bwd_from_forward_tile_states_is_bitwise_the_same(io, n_chunks):
     for k in ops.BWD_OUTPUTS:
         if a[k] is not None:
             assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("io,n_chunks", [("f32", 1), ("f32", 3), ("bf16", 3)])
+def test_bwd_softplus_regions(io, n_chunks):
+    """dt_raw across [-30, 30]: the softplus derivative (sigmoid below the
+    threshold, 1 above it) and the three regions of softplus itself, in
+    the recomputed forward, the adjoint walk and the reverse sweep."""
+    B, L, D = 2, 700, 48
+    inp = make_case(B, L, D, io, seed=97)
+    inp["dt_raw"] = inputs.wide_dt_raw(B, L, D, io, seed=98, device="cuda")
+    g = run_gpu(inp, n_chunks=n_chunks)
+    check(inp, g, f"wide dt {io} nc{n_chunks}")
+
+
+def test_bwd_exact_carry_flag():
+    """MAMBA_FLAG_EXACT_CARRY in the backward: both carry walks cover whole
+    chunks; the gradients match the oracle and the one-pass backward."""
+    B, L, D = 1, 8192, 32
+    inp = make_case(B, L, D, "f32", seed=99)
+    g = run_gpu(inp, n_chunks=4, flags=ops.MAMBA_FLAG_EXACT_CARRY)
+    check(inp, g, "exact carries")
+    g1 = run_gpu(inp, n_chunks=1)
+    torch.cuda.synchronize()
+    for k in ("dh0", "dA_log", "dB", "dx"):
+        assert_close(g[k], g1[k].double().cpu().numpy(), "f32", f"exact chunked vs one pass {k}",
+                     fp32_output=True)

@@ -183,3 +183,82 @@ def test_chunk_carries_against_oracle(case):
         assert_close(outs[0], oracle_like(y1), "f32", f"{case}: chunked vs one pass, y")
     assert_close(outs[1], oracle_like(fh1), "f32", f"{case}: chunked vs one pass, h", fp32_output=True)
     assert torch.equal(outs[2], fcs1)
+
+
+def _tile_regions(dt_raw):
+    """Per 16-token tile of every batch row (over all channels): whether all of
+    it lies below the softplus's small-argument bound, and whether it holds
+    values above the threshold 20 and values in between."""
+    v = dt_raw.float().cpu()
+    B, L, D = v.shape
+    tiles = [(b, t) for b in range(B) for t in range(0, L, 16)]
+    small = sum(bool((v[b, t:t + 16] < -2.08).all()) for b, t in tiles)
+    mixed = sum(bool((v[b, t:t + 16] > 20).any() and ((v[b, t:t + 16] > -2.08) & (v[b, t:t + 16] < 20)).any()
+                     and (v[b, t:t + 16] < -2.08).any()) for b, t in tiles)
+    return small, mixed
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("n_chunks", [1, 3])
+def test_softplus_regions_against_oracle(io, n_chunks):
+    """dt_raw across [-30, 30]: softplus's small-argument polynomial, its
+    log2 region (up to the threshold) and the identity above 20, in tiles
+    that lie wholly in the small region (the fast path) and tiles that mix
+    all three (the per-value path), one pass and chunked (the carry walk
+    takes the same two paths)."""
+    B, L, D = 2, 1000, 64
+    inp = inputs.scan_inputs(B, L, D, io, seed=71, device="cuda", with_state=True)
+    inp["dt_raw"] = inputs.wide_dt_raw(B, L, D, io, seed=72, device="cuda")
+    small, mixed = _tile_regions(inp["dt_raw"])
+    assert small >= 5 and mixed >= 5, (small, mixed)
+    check_against_oracle(inp, run_gpu(inp, n_chunks=n_chunks), f"wide dt {io} nc{n_chunks}")
+
+
+def _large_range_case(seed):
+    return inputs.scan_inputs(1, 8192, 64, "f32", seed=seed, device="cuda", with_state=True)
+
+
+@pytest.mark.parametrize("case", ["h0_x1e6", "first_chunk_x_x1e3"])
+def test_chunked_carry_large_dynamic_range(case):
+    """Chunked mode (4 chunks, the carry walks stop early on these decays)
+    with an initial state a million times the inputs' scale, or the first
+    chunk's inputs a thousand times the later ones': against the oracle at
+    the fp32 bound, and against the one-pass scan."""
+    inp = _large_range_case(81)
+    if case == "h0_x1e6":
+        inp["h0"] = inp["h0"] * 1e6
+    else:
+        inp["x"][:, :2048] *= 1e3
+    plan = ops.mamba_scan_plan(1, 8192, 64, 4)
+    assert plan["n_chunks"] == 4 and plan["pieces"] > 1
+    outs = [t.clone() for t in run_gpu(inp, n_chunks=4)]
+    check_against_oracle(inp, outs, f"carries {case}")
+    y1, fh1, fcs1 = run_gpu(inp, n_chunks=1)
+    torch.cuda.synchronize()
+    assert_close(outs[0], oracle_like(y1), "f32", f"{case}: chunked vs one pass, y")
+    assert_close(outs[1], oracle_like(fh1), "f32", f"{case}: chunked vs one pass, h", fp32_output=True)
+
+
+def test_exact_carry_flag_with_hidden_large_state():
+    """A state 1e8 times the inputs' scale built up early in chunk 0 and hidden
+    from y there (gate input z = 0 over chunk 0), decaying towards the
+    boundary: the default carry walk stops where every state has decayed
+    below 2^-32 and drops what lies before, which here is still visible in
+    the next chunk's y.  With MAMBA_FLAG_EXACT_CARRY the walks cover whole
+    chunks and the chunked scan matches the oracle at the fp32 bound."""
+    B, L, D = 1, 8192, 32
+    inp = inputs.scan_inputs(B, L, D, "f32", seed=83, device="cuda", with_state=True)
+    inp["A_log"] = torch.zeros_like(inp["A_log"])  # A = -1: every state decays at the same rate
+    # dt = 0.02 on every token: the walk over chunk 0 stops after five pieces,
+    # at token 768, and drops tokens 0..767
+    inp["dt_raw"] = torch.full_like(inp["dt_raw"], float(np.log(np.expm1(0.02))))
+    inp["x"][:, 700:768] *= 1e8
+    inp["z"][:, :2048] = 0.0
+    plan = ops.mamba_scan_plan(B, L, D, 4)
+    assert plan["n_chunks"] == 4 and plan["piece_len"] == 256
+    y, fh, fcs = run_gpu(inp, n_chunks=4, flags=ops.MAMBA_FLAG_EXACT_CARRY)
+    check_against_oracle(inp, (y, fh, fcs), "exact carries, hidden large state")
+    y1, fh1, _ = run_gpu(inp, n_chunks=1)
+    torch.cuda.synchronize()
+    assert_close(y, oracle_like(y1), "f32", "exact chunked vs one pass, y")
+    assert_close(fh, oracle_like(fh1), "f32", "exact chunked vs one pass, h", fp32_output=True)

@@ -73,3 +73,34 @@ def test_step_rejects_bad_arguments():
         ops.mamba_step(h, cs, v, v, v, bc, bc, A, torch.zeros(D, device="cuda"),
                        torch.zeros(D, 4, device="cuda"))
     assert e.value.status == ops.MAMBA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_steps_wide_softplus_range(io):
+    """dt_raw across [-30, 30] (softplus's three regions): steps against the
+    oracle, and bit for bit equal to a one-pass scan of the same tokens (the
+    scan's per-tile fast path and per-value path give softplus's bits)."""
+    B, L, D = 2, 96, 48
+    inp = inputs.scan_inputs(B, L, D, io, seed=91, device="cuda", with_state=True)
+    inp["dt_raw"] = inputs.wide_dt_raw(B, L, D, io, seed=92, device="cuda")
+    y, fh, fcs = ops.mamba_scan_fwd(inp["x"], inp["z"], inp["dt_raw"], inp["Bm"], inp["Cm"],
+                                    inp["A_log"], inp["Dskip"], inp["conv_w"], inp["conv_b"],
+                                    inp["h0"], inp["conv_state0"], n_chunks=1)
+    st = dict(h=inp["h0"].clone(), conv_state=inp["conv_state0"].clone(), A_log=inp["A_log"],
+              Dskip=inp["Dskip"], conv_w=inp["conv_w"], conv_b=inp["conv_b"])
+    tok = {"x_t": inp["x"].transpose(0, 1).contiguous(), "z_t": inp["z"].transpose(0, 1).contiguous(),
+           "dt_raw_t": inp["dt_raw"].transpose(0, 1).contiguous(),
+           "B_t": inp["Bm"].transpose(0, 1).contiguous(), "C_t": inp["Cm"].transpose(0, 1).contiguous()}
+    h_ref, cs_ref = oracle.f64(inp["h0"]), oracle.f64(inp["conv_state0"])
+    ys = []
+    for t in range(L):
+        ys.append(step(st, tok, t))
+        yr, h_ref, cs_ref = oracle.step(h_ref, cs_ref, tok["x_t"][t], tok["z_t"][t], tok["dt_raw_t"][t],
+                                        tok["B_t"][t], tok["C_t"][t], st["A_log"], st["Dskip"],
+                                        st["conv_w"], st["conv_b"])
+        torch.cuda.synchronize()
+        assert_close(ys[-1], yr, io, f"y step {t}")
+    assert_close(st["h"], h_ref, io, "h", fp32_output=True)
+    assert torch.equal(torch.stack(ys, 1), y)
+    assert torch.equal(st["h"], fh)
+    assert torch.equal(st["conv_state"], fcs)

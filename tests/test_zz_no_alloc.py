@@ -1,16 +1,18 @@
 """mamba_scan_fwd_noalloc, the prefill entry point for callers that cannot
 allocate device memory (for example a plugin whose host framework owns all
 device memory through its own pool, or a path that must not take
-cudaMalloc's implicit synchronisation).  It must give the same results as
-mamba_scan_fwd, which takes a caller-allocated workspace, on consecutive
-calls that share its fixed scratch array, and must refuse sizes that do not
-fit that array.  This file is collected last on purpose."""
+cudaMalloc's implicit synchronisation).  It runs the same kernels with the
+same plan as mamba_scan_fwd, which takes a caller-allocated workspace, so
+its results must be the same bits, on consecutive calls that share its fixed
+scratch array (whatever an earlier call left there), and must refuse sizes
+that do not fit that array.  This file is collected last on purpose."""
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
-from parity import assert_close
+from parity import assert_close, oracle_scan
 from selective_state_space_118_b300 import inputs, ops
 
 pytestmark = pytest.mark.gpu
@@ -28,23 +30,32 @@ def _args(inp):
             inp["conv_w"], inp["conv_b"], inp.get("h0"), inp.get("conv_state0"))
 
 
-def _compare(io, got, ref, what):
-    for g, r, name, fp32 in zip(got, ref, ("y", "final_h", "final_conv_state"), (False, True, False)):
-        torch.cuda.synchronize()
-        assert_close(g, r.double().cpu().numpy(), io, f"{what} {name}", fp32_output=fp32)
-
-
-def test_noalloc_matches_workspace_entry_point_on_two_calls():
-    # call 1: a chunked plan (carries live in the scratch); call 2: one pass
-    cases = [(inputs.scan_inputs(2, 2048, 1024, "bf16", seed=61, device="cuda", with_state=True), 0),
+def test_noalloc_equals_workspace_entry_point_on_consecutive_calls():
+    # two chunked calls of different sizes back to back (the second starts on
+    # the counters and carries the first left in the scratch), then a
+    # one-pass call; every call must give mamba_scan_fwd's bits
+    cases = [(inputs.scan_inputs(2, 2048, 1024, "bf16", seed=61, device="cuda", with_state=True), 4),
+             (inputs.scan_inputs(1, 3000, 256, "f32", seed=63, device="cuda", with_state=True), 3),
              (inputs.scan_inputs(1, 700, 48, "f32", seed=62, device="cuda", with_state=True), 1)]
     for i, (inp, n_chunks) in enumerate(cases):
-        io = "bf16" if inp["x"].dtype == torch.bfloat16 else "f32"
+        B, L, D = inp["x"].shape
+        assert ops.mamba_scan_plan(B, L, D, n_chunks)["n_chunks"] == n_chunks
         ref = ops.mamba_scan_fwd(*_args(inp), n_chunks=n_chunks)
-        out = _outputs_like(inp)
-        got = ops.mamba_scan_fwd_noalloc(*_args(inp), n_chunks=n_chunks, **out)
-        _compare(io, got, ref, f"call {i + 1}")
+        got = ops.mamba_scan_fwd_noalloc(*_args(inp), n_chunks=n_chunks, **_outputs_like(inp))
+        torch.cuda.synchronize()
+        for g, r, name in zip(got, ref, ("y", "final_h", "final_conv_state")):
+            assert torch.equal(g, r), f"call {i + 1}: {name} differs from mamba_scan_fwd"
         assert ops.mamba_last_error() == ops.MAMBA_OK
+
+
+def test_noalloc_against_oracle():
+    inp = inputs.scan_inputs(1, 1500, 64, "f32", seed=64, device="cuda", with_state=True)
+    y, fh, fcs = ops.mamba_scan_fwd_noalloc(*_args(inp), n_chunks=3, **_outputs_like(inp))
+    torch.cuda.synchronize()
+    yr, fhr, fcsr = oracle_scan(inp)
+    assert_close(y, yr, "f32", "noalloc y")
+    assert_close(fh, fhr, "f32", "noalloc final_h", fp32_output=True)
+    np.testing.assert_array_equal(fcs.double().cpu().numpy(), fcsr)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
