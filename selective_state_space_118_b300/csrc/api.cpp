@@ -123,6 +123,13 @@ constexpr int kPieceTiles = 16;
 // A = -1): used only to size the plan.
 constexpr int kCarryTilesEstimate = 64;
 
+// Relative costs of the plan's model: a main-pass tile and a carry-walk tile
+// (16 tokens x 32 channels each) and one hop of a carry chain, in units of
+// ~1,800 issued warp-instructions.
+constexpr double kMainTileCost = 1.0;
+constexpr double kCarryTileCost = 0.7;
+constexpr double kChainHopCost = 1.5;
+
 // The plan depends only on the sizes (not on the I/O dtype), so that the
 // workspace queries, which take no dtype, agree with the call.
 Plan make_plan(int batch, int seqlen, int d_inner, int n_chunks_req) {
@@ -139,14 +146,17 @@ Plan make_plan(int batch, int seqlen, int d_inner, int n_chunks_req) {
     const int n_eff = (tiles + C - 1) / C;
     const int P = C < kPieceTiles ? C : kPieceTiles;
     const int m = (C + P - 1) / P;
-    // Chunks shorter than the expected walk make every boundary wait for the
-    // previous one: the carries of a group then form one serial chain.
+    // Chunks shorter than the expected walk make every boundary walk its
+    // whole chunk and then wait for the previous boundary's carry: the walks
+    // run side by side, the folds one after another (a chain of hops of
+    // about a tile's time each).
     double t_carry = 0.0;
-    if (n_eff > 1)
-      t_carry = C >= kCarryTilesEstimate
-                    ? pass_time(groups * (n_eff - 1), kCarryTilesEstimate, 0.7, mc.sms, mc.summary_per_sm)
-                    : pass_time(groups, (n_eff - 1) * C, 0.7, mc.sms, mc.summary_per_sm);
-    const double t = pass_time(groups * n_eff, C, 1.0, mc.sms, mc.main_per_sm) + t_carry;
+    if (n_eff > 1) {
+      const int walk = C < kCarryTilesEstimate ? C : kCarryTilesEstimate;
+      t_carry = pass_time(groups * (n_eff - 1), walk, kCarryTileCost, mc.sms, mc.summary_per_sm);
+      if (C < kCarryTilesEstimate) t_carry += kChainHopCost * (n_eff - 1);
+    }
+    const double t = pass_time(groups * n_eff, C, kMainTileCost, mc.sms, mc.main_per_sm) + t_carry;
     if (best < 0.0 || t < best - 1e-9) {
       best = t;
       pl = Plan{n_eff, C, n_eff > 1 ? m : 1, n_eff > 1 ? P : C};

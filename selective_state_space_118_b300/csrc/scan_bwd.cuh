@@ -85,6 +85,30 @@ struct ACarrySmem {
   unsigned ticket;
 };
 
+// One tile of an adjoint-carry piece, walked backwards from its last row
+// (rows tokens): R <- dA (C dyss + R) on the first kPairs state pairs (the
+// later ones, whose decay to the boundary is already below the drop bound,
+// stay as they are: zero within the piece), and the dt sum.
+template <typename IO, int kPairs>
+__device__ __forceinline__ void adjoint_tile(const ACarryStage<IO>& S, int rows, int lane, bool active,
+                                             const Channel& ch, State16& rr, float& sdt) {
+#pragma unroll(kScanUnroll)
+  for (int r = rows - 1; r >= 0; --r) {
+    const float dt = softplus(to_f32(S.dt[r][lane]));
+    const float dyv = active ? to_f32(S.dy[r][lane]) : 0.0f;
+    const float dyss = __fmul_rn(dyv, silu(to_f32(S.z[r][lane])));
+    const float2 d2 = make_float2(dt, dt), y2 = make_float2(dyss, dyss);
+#pragma unroll
+    for (int kk = 0; kk < kPairs; ++kk) {
+      const float4 q = *reinterpret_cast<const float4*>(&S.bc[r][4 * kk]);
+      const float2 xa = __fmul2_rn(d2, ch.a2[kk]);
+      const float2 dA = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
+      rr.h[kk] = __fmul2_rn(__ffma2_rn(make_float2(q.z, q.w), y2, rr.h[kk]), dA);
+    }
+    sdt = __fadd_rn(sdt, dt);
+  }
+}
+
 // softplus(v) (the forward's bits) and its derivative sigmoid(v), which is 1
 // above the threshold where softplus(v) = v.
 __device__ __forceinline__ void softplus_grad(float v, float& sp, float& sig) {
@@ -601,6 +625,7 @@ __device__ __forceinline__ void acarry_warp(const CUtensorMap& tm_z, const CUten
   for (int k = 0; k < 8; ++k) wgt.h[k] = make_float2(1.0f, 1.0f);
   float s_before = 0.0f, sdt = 0.0f;
   const bool exact = (p.flags & kFlagExactCarry) != 0;  // walk the whole chunk, drop nothing
+  int n_pairs = 8;  // leading state pairs the current piece advances
 
   bool ok = true, done = false;
   int k = 0;
@@ -614,22 +639,14 @@ __device__ __forceinline__ void acarry_warp(const CUtensorMap& tm_z, const CUten
     bool mine = mbar_wait_bounded(smem_u32(&sm.full[s]), (k / kStages) & 1, p.timeout_ns);
     ok = __all_sync(0xffffffffu, mine);
     if (!ok) break;
-#pragma unroll(kScanUnroll)
-    for (int r = rows - 1; r >= 0; --r) {
-      const float dt = softplus(to_f32(S.dt[r][lane]));
-      const float dyv = active ? to_f32(S.dy[r][lane]) : 0.0f;
-      const float dyss = __fmul_rn(dyv, silu(to_f32(S.z[r][lane])));
-      const float2 d2 = make_float2(dt, dt), y2 = make_float2(dyss, dyss);
-      float4 Q[8];
-      load_quads(&S.bc[r][0], Q);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const float2 xa = __fmul2_rn(d2, ch.a2[kk]);
-        const float2 dA = make_float2(ex2_approx(xa.x), ex2_approx(xa.y));
-        rr.h[kk] = __fmul2_rn(__ffma2_rn(make_float2(Q[kk].z, Q[kk].w), y2, rr.h[kk]), dA);
-      }
-      sdt = __fadd_rn(sdt, dt);
-    }
+    if (n_pairs <= 1)
+      adjoint_tile<IO, 1>(S, rows, lane, active, ch, rr, sdt);
+    else if (n_pairs <= 2)
+      adjoint_tile<IO, 2>(S, rows, lane, active, ch, rr, sdt);
+    else if (n_pairs <= 4)
+      adjoint_tile<IO, 4>(S, rows, lane, active, ch, rr, sdt);
+    else
+      adjoint_tile<IO, 8>(S, rows, lane, active, ch, rr, sdt);
     __syncwarp();
     if (lane == 0 && k + kStages < n_tiles)
       issue_acarry_tile<IO>(sm, s, &tm_z, &tm_dt, &tm_dy, &tm_bc, c0, wk.tile_of(k + kStages), b);
@@ -650,6 +667,9 @@ __device__ __forceinline__ void acarry_warp(const CUtensorMap& tm_z, const CUten
         left = wk.piece_len(q);
         state16_zero(rr);
         sdt = 0.0f;
+        // state pairs whose weight to the boundary fell below the drop bound
+        // contribute nothing from here on: the piece advances the others only
+        if (!exact) n_pairs = live_pairs(wgt, active);
       }
     }
   }

@@ -2,16 +2,19 @@
 //
 // Work decomposition.  A CTA is one warp.  Lane i owns channel c0 + i of a
 // group of 32 channels of one batch row, with all 16 of its fp32 states in
-// registers, and walks one chunk of the sequence in tiles of 32 tokens.  Each
-// tile of x, z, dt_raw (32 tokens x 32 channels, I/O dtype) and of the token
-// rows of B and C (32 x 32 fp32, widened and interleaved beforehand by
+// registers, and walks one chunk of the sequence in tiles of 16 tokens.  Each
+// tile of x, z, dt_raw (16 tokens x 32 channels, I/O dtype) and of the token
+// rows of B and C (16 x 32 fp32, widened and interleaved beforehand by
 // bc_widen_kernel) is brought into shared memory by TMA bulk-tensor copies
 // through a ring of two mbarrier-tracked stages, so every input byte is read
 // from HBM once.  B and C are the same for every channel: all lanes read the
 // same row, so their 128-bit shared loads are broadcasts.  Nothing is
 // exchanged between lanes; the only serial dependence is each state's
 // recurrence, and a lane has 16 independent ones plus all the per-token
-// exponentials, which do not depend on the state, to overlap with it.
+// exponentials, which do not depend on the state, to overlap with it.  In
+// tiles whose dt_raw all lie in softplus's small region (the common case),
+// the per-token scalar work of two consecutive tokens runs as packed f32x2
+// operations.
 //
 // The conv's three earlier inputs travel in registers from token to token
 // (loaded from x, or conv_state0, at the chunk start).  y is stored straight
@@ -23,7 +26,9 @@
 // scan_carry_kernel (described with it below): one warp per chunk boundary
 // and channel group walks the previous chunk backwards in pieces and stops
 // where the decay to the boundary makes earlier tokens negligible (below
-// 2^-32 for every state), or else chains onto the previous boundary's carry.
+// 2^-32 for every state), or else chains onto the previous boundary's carry;
+// on the way, each piece advances only the state pairs whose decay to the
+// boundary is not yet below that bound.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -41,6 +46,11 @@ constexpr int kT = kTileTokens;
 constexpr int kBC = 2 * kN;  // widened B and C per token
 constexpr int kStages = 2;   // TMA ring depth
 constexpr int kScanUnroll = 4;  // tokens unrolled in the tile loops
+
+// The chunk-carry walks drop terms whose weight to the boundary is below
+// 2^-32 of their own size.
+constexpr float kCarryDropLog2 = -32.0f;
+constexpr float kCarryDropWeight = 2.3283064365386963e-10f;  // 2^-32
 
 // Sticky device error word (MAMBA_ERR_* code of the first failure).
 __device__ unsigned int g_mamba_error;
@@ -134,37 +144,93 @@ __device__ __forceinline__ float softplus_sel(float v) {
   return kSmall ? softplus_small_raw(v) : softplus(v);
 }
 
-// One tile of the main pass, `rows` tokens, straight-line per token; y is
-// stored where wy holds.  kFull: rows == kT, the loop is unrolled completely.
-// kY false: the states alone (z, the read-out and y are skipped).
+// One token r of a tile of the main pass; y is stored where wy holds.  kY
+// false: the states alone (z, the read-out and y are skipped).
+template <typename IO, bool kSmall, bool kY>
+__device__ __forceinline__ void main_token(const MainStage<IO>& S, int r, int lane, bool wy, const Channel& ch,
+                                           State16& st, float& xm3, float& xm2, float& xm1, IO* ytile, int D) {
+  const float xv = to_f32(S.x[r][lane]);
+  const float u = silu(conv4(ch.w, ch.bias, xm3, xm2, xm1, xv));
+  xm3 = xm2;
+  xm2 = xm1;
+  xm1 = xv;
+  const float dt = softplus_sel<kSmall>(to_f32(S.dt[r][lane]));
+  float4 Q[8];
+  load_quads(&S.bc[r][0], Q);
+  Drive16 d;
+  drive16_q(d, ch.a2, dt, __fmul_rn(dt, u), Q);
+  state16_apply(st, d);
+  if (kY) {
+    const float gz = silu(to_f32(S.z[r][lane]));
+    const float yv = gate_out(state16_readout_q(st, Q), ch.Dc, u, gz);
+    st_global_if(wy, ytile + (size_t)r * D, from_f32<IO>(yv));
+  }
+}
+
+// Tokens r and r+1, both with dt_raw in softplus's small region: the
+// per-token scalar work (conv, SiLU, softplus, dt*u, SiLU(z), gate) of the
+// two tokens runs as packed f32x2 operations, the same operations as
+// main_token's on each (the same bits), in about half the instructions.
+template <typename IO, bool kY>
+__device__ __forceinline__ void main_token_pair(const MainStage<IO>& S, int r, int lane, bool wy,
+                                                const Channel& ch, State16& st, float& xm3, float& xm2, float& xm1,
+                                                IO* ytile, int D) {
+  const float x0 = to_f32(S.x[r][lane]);
+  const float x1 = to_f32(S.x[r + 1][lane]);
+  const float2 u = silu_x2(conv4_x2(ch.w, ch.bias, xm3, xm2, xm1, x0, x1));
+  xm3 = xm1;
+  xm2 = x0;
+  xm1 = x1;
+  const float2 dt = softplus_small_raw_x2(make_float2(to_f32(S.dt[r][lane]), to_f32(S.dt[r + 1][lane])));
+  const float2 dtu = __fmul2_rn(dt, u);
+  float2 ss = make_float2(0.0f, 0.0f);
+  {
+    float4 Q[8];
+    load_quads(&S.bc[r][0], Q);
+    Drive16 d;
+    drive16_q(d, ch.a2, dt.x, dtu.x, Q);
+    state16_apply(st, d);
+    if (kY) ss.x = state16_readout_q(st, Q);
+  }
+  {
+    float4 Q[8];
+    load_quads(&S.bc[r + 1][0], Q);
+    Drive16 d;
+    drive16_q(d, ch.a2, dt.y, dtu.y, Q);
+    state16_apply(st, d);
+    if (kY) ss.y = state16_readout_q(st, Q);
+  }
+  if (kY) {
+    const float2 gz = silu_x2(make_float2(to_f32(S.z[r][lane]), to_f32(S.z[r + 1][lane])));
+    const float2 yv = gate_out_x2(ss, ch.Dc, u, gz);
+    st_global_if(wy, ytile + (size_t)r * D, from_f32<IO>(yv.x));
+    st_global_if(wy, ytile + (size_t)(r + 1) * D, from_f32<IO>(yv.y));
+  }
+}
+
+// One tile of the main pass, `rows` tokens, straight-line per token (per
+// token pair in small-dt tiles).  kFull: rows == kT, unrolled completely.
 template <typename IO, bool kSmall, bool kFull, bool kY>
 __device__ __forceinline__ void main_tile(const MainStage<IO>& S, int rows, int lane, bool wy,
                                           const Channel& ch, State16& st, float& xm3, float& xm2, float& xm1,
                                           IO* ytile, int D) {
   if (kFull) rows = kT;
+  if (kSmall) {
+    int r = 0;
+#pragma unroll(kFull ? kT / 2 : kScanUnroll / 2)
+    for (; r + 1 < rows; r += 2)
+      main_token_pair<IO, kY>(S, r, lane, wy, ch, st, xm3, xm2, xm1, ytile, D);
+    if (!kFull && r < rows) main_token<IO, true, kY>(S, r, lane, wy, ch, st, xm3, xm2, xm1, ytile, D);
+  } else {
 #pragma unroll(kFull ? kT : kScanUnroll)
-  for (int r = 0; r < rows; ++r) {
-    const float xv = to_f32(S.x[r][lane]);
-    const float u = silu(conv4(ch.w, ch.bias, xm3, xm2, xm1, xv));
-    xm3 = xm2;
-    xm2 = xm1;
-    xm1 = xv;
-    const float dt = softplus_sel<kSmall>(to_f32(S.dt[r][lane]));
-    float4 Q[8];
-    load_quads(&S.bc[r][0], Q);
-    Drive16 d;
-    drive16_q(d, ch.a2, dt, __fmul_rn(dt, u), Q);
-    state16_apply(st, d);
-    if (kY) {
-      const float gz = silu(to_f32(S.z[r][lane]));
-      const float yv = gate_out(state16_readout_q(st, Q), ch.Dc, u, gz);
-      st_global_if(wy, ytile + (size_t)r * D, from_f32<IO>(yv));
-    }
+    for (int r = 0; r < rows; ++r) main_token<IO, false, kY>(S, r, lane, wy, ch, st, xm3, xm2, xm1, ytile, D);
   }
 }
 
-// One full tile of a carry piece (state and dt sum only).
-template <typename IO, bool kSmall>
+// One full tile of a carry piece (state and dt sum only), advancing the
+// first kPairs state pairs (the later ones, whose decay to the boundary is
+// already below the drop bound, stay as they are: zero within the piece).
+template <typename IO, bool kSmall, int kPairs>
 __device__ __forceinline__ void summary_tile(const SummaryStage<IO>& S, int lane, const Channel& ch, State16& st,
                                              float& sdt, float& xm3, float& xm2, float& xm1) {
 #pragma unroll(kScanUnroll)
@@ -175,13 +241,42 @@ __device__ __forceinline__ void summary_tile(const SummaryStage<IO>& S, int lane
     xm2 = xm1;
     xm1 = xv;
     const float dt = softplus_sel<kSmall>(to_f32(S.dt[r][lane]));
-    float4 Q[8];
-    load_quads(&S.bc[r][0], Q);
-    Drive16 d;
-    drive16_q(d, ch.a2, dt, __fmul_rn(dt, u), Q);
-    state16_apply(st, d);
+    const float2 d2 = make_float2(dt, dt);
+    const float dtu = __fmul_rn(dt, u);
+    const float2 u2 = make_float2(dtu, dtu);
+#pragma unroll
+    for (int k = 0; k < kPairs; ++k) {  // the operations of drive16_q and state16_apply, pair by pair
+      const float4 q = *reinterpret_cast<const float4*>(&S.bc[r][4 * k]);
+      const float2 x = __fmul2_rn(d2, ch.a2[k]);
+      const float2 dA = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+      st.h[k] = __ffma2_rn(dA, st.h[k], __fmul2_rn(u2, make_float2(q.x, q.y)));
+    }
     sdt = __fadd_rn(sdt, dt);
   }
+}
+
+template <typename IO, bool kSmall>
+__device__ __forceinline__ void summary_tile_n(int n_pairs, const SummaryStage<IO>& S, int lane, const Channel& ch,
+                                               State16& st, float& sdt, float& xm3, float& xm2, float& xm1) {
+  if (n_pairs <= 1)
+    summary_tile<IO, kSmall, 1>(S, lane, ch, st, sdt, xm3, xm2, xm1);
+  else if (n_pairs <= 2)
+    summary_tile<IO, kSmall, 2>(S, lane, ch, st, sdt, xm3, xm2, xm1);
+  else if (n_pairs <= 4)
+    summary_tile<IO, kSmall, 4>(S, lane, ch, st, sdt, xm3, xm2, xm1);
+  else
+    summary_tile<IO, kSmall, 8>(S, lane, ch, st, sdt, xm3, xm2, xm1);
+}
+
+// Number of leading state pairs whose weight to the boundary (wgt, over the
+// active lanes) is still at or above the drop bound: 1 + the last such pair,
+// 0 when none is.
+__device__ __forceinline__ int live_pairs(const State16& wgt, bool active) {
+  int last = -1;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (fmaxf(wgt.h[k].x, wgt.h[k].y) >= kCarryDropWeight) last = k;
+  return __reduce_max_sync(0xffffffffu, active ? last + 1 : 0);
 }
 
 // ---------------------------------------------------------------- main pass
@@ -325,7 +420,6 @@ __global__ void __launch_bounds__(kLanes)
 // decay, the common case, costs a few pieces per boundary; no decay at all
 // costs one pass over the earlier chunks and a chain of waits, no more than a
 // full two-pass scan.
-constexpr float kCarryDropLog2 = -32.0f;
 
 template <typename IO>
 struct CarrySmem {
@@ -415,6 +509,7 @@ __device__ __forceinline__ void carry_warp(const CUtensorMap& tm_x, const CUtens
   for (int k = 0; k < 8; ++k) wgt.h[k] = make_float2(1.0f, 1.0f);
   float s_after = 0.0f;  // dt summed from the current piece's end to the boundary
   const bool exact = (p.flags & kFlagExactCarry) != 0;  // walk the whole chunk, drop nothing
+  int n_pairs = 8;  // leading state pairs the current piece advances
 
   bool ok = true, done = false;
   int k = 0;
@@ -435,9 +530,9 @@ __device__ __forceinline__ void carry_warp(const CUtensorMap& tm_x, const CUtens
     ok = __all_sync(0xffffffffu, mine);
     if (!ok) break;
     if (small_dt_tile<IO>(S.dt, kT, lane, active))
-      summary_tile<IO, true>(S, lane, ch, st, sdt, xm3, xm2, xm1);
+      summary_tile_n<IO, true>(n_pairs, S, lane, ch, st, sdt, xm3, xm2, xm1);
     else
-      summary_tile<IO, false>(S, lane, ch, st, sdt, xm3, xm2, xm1);
+      summary_tile_n<IO, false>(n_pairs, S, lane, ch, st, sdt, xm3, xm2, xm1);
     __syncwarp();
     if (lane == 0 && k + kStages < n_tiles)
       issue_carry_tile<IO>(sm, s, &tm_x, &tm_dt, &tm_bc, c0, wk.tile_of(k + kStages), b);
@@ -458,6 +553,9 @@ __device__ __forceinline__ void carry_warp(const CUtensorMap& tm_x, const CUtens
         left = wk.piece_len(q);
         state16_zero(st);
         sdt = 0.0f;
+        // state pairs whose weight to the boundary fell below the drop bound
+        // contribute nothing from here on: the piece advances the others only
+        if (!exact) n_pairs = live_pairs(wgt, active);
         const long t0 = (long)wk.tile_of(k + 1) * kT;
         xm3 = input_at<IO>(p, b, t0 - 3, cl);
         xm2 = input_at<IO>(p, b, t0 - 2, cl);

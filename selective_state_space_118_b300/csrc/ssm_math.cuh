@@ -65,11 +65,17 @@ __device__ __forceinline__ float softplus_e(float v) { return ex2_approx(__fmul_
 
 // P evaluated in Estrin's scheme (depth 4 instead of Horner's 6):
 // P = (1 + a1 e) + e^2 ((a2 + a3 e) + e^2 (a4 + a5 e)).
+constexpr float kLp1 = -0.49999988079071045f;  // coefficients a1..a5 of P (fit_log1p.py)
+constexpr float kLp2 = 0.3333229124546051f;
+constexpr float kLp3 = -0.24963703751564026f;
+constexpr float kLp4 = 0.19420583546161652f;
+constexpr float kLp5 = -0.12255968898534775f;
+
 __device__ __forceinline__ float softplus_small(float e) {
   const float e2 = __fmul_rn(e, e);
-  const float q0 = __fmaf_rn(e, -0.49999988079071045f, 1.0f);
-  const float q1 = __fmaf_rn(e, -0.24963703751564026f, 0.3333229124546051f);
-  const float q2 = __fmaf_rn(e, -0.12255968898534775f, 0.19420583546161652f);
+  const float q0 = __fmaf_rn(e, kLp1, 1.0f);
+  const float q1 = __fmaf_rn(e, kLp3, kLp2);
+  const float q2 = __fmaf_rn(e, kLp5, kLp4);
   const float p = __fmaf_rn(__fmaf_rn(q2, e2, q1), e2, q0);
   return __fmul_rn(e, p);
 }
@@ -91,6 +97,28 @@ constexpr float kSoftplusSmallRaw = -2.08f;
 // softplus(v) for v < kSoftplusSmallRaw (the caller guarantees it).
 __device__ __forceinline__ float softplus_small_raw(float v) { return softplus_small(softplus_e(v)); }
 
+// The same three functions on two values at once with packed f32x2
+// operations: each lane of a packed operation performs the scalar
+// operation above, in the same order, so the results are the same bits.
+__device__ __forceinline__ float2 silu_x2(float2 v) {
+  const float2 m = __fmul2_rn(v, make_float2(-kLog2e, -kLog2e));
+  const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f), make_float2(ex2_approx(m.x), ex2_approx(m.y)));
+  return __fmul2_rn(v, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
+
+// softplus of two raw values both below kSoftplusSmallRaw (the caller
+// guarantees it): softplus_small(softplus_e(v)) on each.
+__device__ __forceinline__ float2 softplus_small_raw_x2(float2 v) {
+  const float2 m = __fmul2_rn(v, make_float2(kLog2e, kLog2e));
+  const float2 e = make_float2(ex2_approx(m.x), ex2_approx(m.y));
+  const float2 e2 = __fmul2_rn(e, e);
+  const float2 q0 = __ffma2_rn(e, make_float2(kLp1, kLp1), make_float2(1.0f, 1.0f));
+  const float2 q1 = __ffma2_rn(e, make_float2(kLp3, kLp3), make_float2(kLp2, kLp2));
+  const float2 q2 = __ffma2_rn(e, make_float2(kLp5, kLp5), make_float2(kLp4, kLp4));
+  const float2 p = __ffma2_rn(__ffma2_rn(q2, e2, q1), e2, q0);
+  return __fmul2_rn(e, p);
+}
+
 // ---------------------------------------------------------------- conv
 // Causal depthwise cross-correlation of width 4: w.w multiplies the current
 // input (PyTorch Conv1d with padding 3, first L outputs kept).
@@ -100,6 +128,20 @@ __device__ __forceinline__ float conv4(float4 w, float bias, float xm3, float xm
   a = __fmaf_rn(w.y, xm2, a);
   a = __fmaf_rn(w.z, xm1, a);
   return __fmaf_rn(w.w, x0, a);
+}
+
+// conv4 for two consecutive tokens t, t+1 (inputs x[t-3..t+1]).
+__device__ __forceinline__ float2 conv4_x2(float4 w, float bias, float xm3, float xm2, float xm1, float x0,
+                                           float x1) {
+  float2 a = __ffma2_rn(make_float2(w.x, w.x), make_float2(xm3, xm2), make_float2(bias, bias));
+  a = __ffma2_rn(make_float2(w.y, w.y), make_float2(xm2, xm1), a);
+  a = __ffma2_rn(make_float2(w.z, w.z), make_float2(xm1, x0), a);
+  return __ffma2_rn(make_float2(w.w, w.w), make_float2(x0, x1), a);
+}
+
+// gate_out for two tokens.
+__device__ __forceinline__ float2 gate_out_x2(float2 S, float Dc, float2 u, float2 gz) {
+  return __fmul2_rn(__ffma2_rn(make_float2(Dc, Dc), u, S), gz);
 }
 
 // ---------------------------------------------------------------- parameters

@@ -19,11 +19,11 @@ def load_fit():
 
 def header_coefficients():
     src = open(os.path.join(CSRC, "ssm_math.cuh")).read()
-    body = src[src.index("float softplus_small(float e)"):src.index("constexpr float kSoftplusSmallE")]
-    vals = [float(v) for v in re.findall(r"(-?\d+\.\d+(?:e-?\d+)?)f", body)]
-    # Estrin's terms in source order: (c1, c0), (c3, c2), (c5, c4)
-    c1, c0, c3, c2, c5, c4 = vals[0], vals[1], vals[2], vals[3], vals[4], vals[5]
-    return np.array([c0, c1, c2, c3, c4, c5], dtype=np.float32)
+    named = {int(k): float(v) for k, v in re.findall(r"constexpr float kLp(\d) = (-?\d+\.\d+(?:e-?\d+)?)f;", src)}
+    assert sorted(named) == [1, 2, 3, 4, 5], named
+    # the constant term is the 1 of Estrin's first term (1 + a1 e)
+    assert "__fmaf_rn(e, kLp1, 1.0f)" in src
+    return np.array([1.0] + [named[k] for k in range(1, 6)], dtype=np.float32)
 
 
 def test_header_holds_the_fitted_coefficients():
