@@ -23,7 +23,11 @@ ssd(...)           Mamba-2's scan: heads of P channels sharing one scalar
 layer(...)         the whole Mamba layer: the projections (numpy matmuls in
                    fp64) around scan(...), with every stored intermediate
                    rounded to bf16 where the library stores it
-build()            compile ``liboracle.so`` next to this file
+m3_scan(...)       the complex-valued scan (Mamba-3's state update, Euler or
+                   exponential-trapezoidal; ``mamba3_oracle.c``)
+m3_core(...)       its bare recurrence on one row, given u and dt directly
+build()            compile ``liboracle.so`` and ``liboracle_m3.so`` next to
+                   this file
 """
 from __future__ import annotations
 
@@ -37,23 +41,31 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "mamba_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_SRC_M3 = os.path.join(_HERE, "mamba3_oracle.c")
+_LIB_M3_PATH = os.path.join(_HERE, "liboracle_m3.so")
 _lib = None
+_lib_m3 = None
 _lock = threading.Lock()
 
 _P = ctypes.POINTER(ctypes.c_double)
 
 
-def build(force: bool = False) -> str:
-    """Compile mamba_oracle.c into liboracle.so (gcc, -O2, OpenMP)."""
-    if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
-        return _LIB_PATH
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+def _compile(src: str, lib: str, force: bool) -> str:
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= os.path.getmtime(src):
+        return lib
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99",
-           "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
+           "-Wall", "-Wextra", "-o", tmp, src, "-lm"]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    os.replace(tmp, lib)
+    return lib
+
+
+def build(force: bool = False) -> str:
+    """Compile mamba_oracle.c into liboracle.so and mamba3_oracle.c into
+    liboracle_m3.so (gcc, -O2, OpenMP)."""
+    _compile(_SRC_M3, _LIB_M3_PATH, force)
+    return _compile(_SRC, _LIB_PATH, force)
 
 
 def _bind(path: str):
@@ -274,3 +286,71 @@ def ssd(x, dt_raw, A_log, Bm, Cm, Dskip, z=None, h0=None, lib=None):
     lib.oracle_ssd_f64(B, L, H, P, G, N, _ptr(x), _ptr(z), _ptr(dt_raw), _ptr(A_log), _ptr(Bm), _ptr(Cm),
                        _ptr(Dskip), _ptr(h0), _ptr(y), _ptr(fs))
     return y, fs
+
+
+# ---------------------------------------------------------------- complex scan
+def _bind_m3(path: str):
+    lib = ctypes.CDLL(path)
+    i = ctypes.c_int
+    lib.oracle_m3_scan_f64.argtypes = [i] * 5 + [_P] * 13 + [i] + [_P] * 4 + [i]
+    lib.oracle_m3_scan_f64.restype = None
+    lib.oracle_m3_core_f64.argtypes = [i, i] + [_P] * 6 + [i] + [_P] * 3
+    lib.oracle_m3_core_f64.restype = None
+    return lib
+
+
+def _load_m3(lib=None):
+    global _lib_m3
+    if lib is not None:
+        return _bind_m3(lib) if isinstance(lib, str) else lib
+    with _lock:
+        if _lib_m3 is None:
+            build()
+            _lib_m3 = _bind_m3(_LIB_M3_PATH)
+    return _lib_m3
+
+
+def source_m3() -> str:
+    with open(_SRC_M3) as f:
+        return f.read()
+
+
+def m3_scan(x, z, dt_raw, Bm, Cm, A_log, theta, Dskip, conv_w, conv_b=None, h0=None,
+            conv_state0=None, v0=None, trapezoidal: bool = False, n_threads: int = 0, lib=None):
+    """The complex-valued scan (mamba3_oracle.c).  Shapes: x, z, dt_raw (B,L,D);
+    Bm, Cm (B,L,2M) as (re, im) pairs; A_log, theta (D,M); Dskip (D,);
+    conv_w (D,K); conv_b (D,) or None; h0, v0 (B,D,2M) or None; conv_state0
+    (B,K-1,D) or None.  Returns (y (B,L,D), final_h (B,D,2M),
+    final_conv_state (B,K-1,D), final_v (B,D,2M))."""
+    lib = _load_m3(lib)
+    x, z, dt_raw, Bm, Cm = map(f64, (x, z, dt_raw, Bm, Cm))
+    A_log, theta, Dskip, conv_w, conv_b, h0, conv_state0, v0 = map(
+        f64, (A_log, theta, Dskip, conv_w, conv_b, h0, conv_state0, v0))
+    B, L, D = x.shape
+    M = A_log.shape[1]
+    K = conv_w.shape[1]
+    assert Bm.shape[-1] == 2 * M and theta.shape == A_log.shape
+    y = np.zeros((B, L, D))
+    fh = np.zeros((B, D, 2 * M))
+    fv = np.zeros((B, D, 2 * M))
+    fcs = np.zeros((B, max(K - 1, 0), D))
+    lib.oracle_m3_scan_f64(B, L, D, M, K, _ptr(x), _ptr(z), _ptr(dt_raw), _ptr(Bm), _ptr(Cm),
+                           _ptr(A_log), _ptr(theta), _ptr(Dskip), _ptr(conv_w), _ptr(conv_b),
+                           _ptr(h0), _ptr(conv_state0), _ptr(v0), int(trapezoidal), _ptr(y),
+                           _ptr(fh), _ptr(fcs), _ptr(fv), int(n_threads))
+    return y, fh, fcs, fv
+
+
+def m3_core(u, dt, Bm, Cm, A_log, theta, h0=None, v0=None, trapezoidal: bool = False, lib=None):
+    """The bare complex recurrence of one row: u, dt (L,); Bm, Cm (L,2M);
+    A_log, theta (M,); h0, v0 (2M,) or None.  Returns (ys (L,) = Re(C h)
+    after each token, final h (2M,), final v (2M,))."""
+    lib = _load_m3(lib)
+    u, dt, Bm, Cm, A_log, theta = map(f64, (u, dt, Bm, Cm, A_log, theta))
+    L, M = u.shape[0], A_log.shape[0]
+    h = np.zeros(2 * M) if h0 is None else f64(h0).copy()
+    v = np.zeros(2 * M) if v0 is None else f64(v0).copy()
+    ys = np.zeros(L)
+    lib.oracle_m3_core_f64(L, M, _ptr(u), _ptr(dt), _ptr(Bm), _ptr(Cm), _ptr(A_log), _ptr(theta),
+                           int(trapezoidal), _ptr(h), _ptr(v), _ptr(ys))
+    return ys, h, v

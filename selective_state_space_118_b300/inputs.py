@@ -147,6 +147,21 @@ def scan_inputs(batch: int, seqlen: int, d_inner: int, io: str, seed: int,
     return out
 
 
+def complex_scan_inputs(batch: int, seqlen: int, d_inner: int, io: str, seed: int,
+                        bc_std: float = 1.0, device="cpu", with_state: bool = False,
+                        h_std: float = 0.1) -> dict:
+    """Inputs of one call of the complex-valued scan: those of scan_inputs
+    (B and C rows of 16 reals read as 8 complex numbers, (re, im) pairs; h0
+    (B,D,16) likewise), with 8 modes per channel: A_log[c, n] = log(n + 1)
+    and rotation frequencies theta[c, n] = pi * n, n = 0..7."""
+    out = scan_inputs(batch, seqlen, d_inner, io, seed, bc_std, device, with_state, h_std)
+    modes = D_STATE // 2
+    n = torch.arange(modes, device=out["A_log"].device, dtype=torch.float32)
+    out["A_log"] = torch.log(n + 1.0).expand(d_inner, modes).contiguous()
+    out["theta"] = (math.pi * n).expand(d_inner, modes).contiguous()
+    return out
+
+
 def workload_inputs(w: ScanWorkload, device="cpu", **kw) -> dict:
     return scan_inputs(w.batch, w.seqlen, w.d_inner, w.io, w.seed, w.bc_std, device, **kw)
 
