@@ -4,8 +4,9 @@
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                 [--workload NAME] [--seqlen L] [--n-chunks K]
                 [--no-e2e] [--no-cpu-baseline] [--no-decode] [--no-ssd]
-                [--no-layer] [--no-backward] [--no-extra-prefill]
-                [--no-prefill | --prefill-only | --backward-only | --layer-only | --ssd-only]
+                [--no-layer] [--no-backward] [--no-complex] [--no-extra-prefill]
+                [--no-prefill | --prefill-only | --backward-only | --layer-only | --ssd-only |
+                 --complex-only]
 
 A step is one prefill of the layer's scan (conv, SiLU, softplus, discretised
 scan, D skip, SiLU(z) gate; final h and conv state) over the workload's whole
@@ -711,6 +712,59 @@ def bench_ssd(w, steps, warmup, local, heads=None, groups=1):
     return res
 
 
+def bench_complex(w, steps, warmup, local, trapezoidal, n_chunks_req=0):
+    """The complex-valued scan (mamba3_scan_fwd, Mamba-3's state update) on the
+    workload's shapes and distributions (8 complex modes per channel, A_log =
+    log(n+1), theta = pi n): elements/s and its HBM roofline."""
+    from selective_state_space_118_b300 import ops
+    dev = torch.device("cuda", local)
+    inp = inputs.complex_scan_inputs(w.batch, w.seqlen, w.d_inner, w.io, w.seed, w.bc_std, device=dev)
+    B, L, D = w.batch, w.seqlen, w.d_inner
+    es = 2 if w.io == "bf16" else 4
+    y = torch.empty_like(inp["x"])
+    fh = torch.empty(B, D, D_STATE, device=dev)
+    fv = torch.empty(B, D, D_STATE, device=dev)
+    fcs = torch.empty(B, D_CONV - 1, D, device=dev, dtype=inp["x"].dtype)
+    ws = torch.empty(max(ops.mamba3_scan_workspace_size(B, L, D, n_chunks_req), 256), device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        ops.mamba3_scan_fwd(inp["x"], inp["z"], inp["dt_raw"], inp["Bm"], inp["Cm"], inp["A_log"], inp["theta"],
+                            inp["Dskip"], inp["conv_w"], inp["conv_b"], trapezoidal=trapezoidal, y=y, final_h=fh,
+                            final_conv_state=fcs, final_v=fv, workspace=ws, n_chunks=n_chunks_req, stream=stream)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    assert ops.mamba_last_error(stream) == ops.MAMBA_OK
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with ClockSampler(dev.index) as clk:
+        ev[0].record(stream)
+        for i in range(steps):
+            call()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+    assert ops.mamba_last_error(stream) == ops.MAMBA_OK
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    t = ev[0].elapsed_time(ev[steps]) / 1e3 / steps
+    # the real scan's minimum bytes plus theta and the state input out (fp32)
+    alg = scan_algorithmic_bytes(B, L, D, es) + D * 8 * 4 + B * D * D_STATE * 4
+    hbm, src = peaks()
+    ws_big = ops.mamba3_scan_workspace_size(B, L, D, n_chunks_req) > ops.mamba3_scan_workspace_size(B, L, D, 1)
+    res = {"metric": "complex scan elements/s", "value": B * L * D / t, "unit": UNIT,
+           "config": {"workload": f"{w.name}_complex8", "batch": B, "seqlen": L, "d_inner": D, "modes": 8,
+                      "discretization": "trapezoidal" if trapezoidal else "euler", "chunked": ws_big,
+                      "theta": "pi * n", "A_log": "log(n + 1)"},
+           "ms_per_call": t * 1e3, "ms_per_call_min": min(per),
+           "roofline": {"bound": "hbm", "achieved": alg / t / 1e9, "peak": hbm, "unit": "GB/s",
+                        "frac": alg / t / 1e9 / hbm, "peak_source": src, "algorithmic_bytes_per_call": alg,
+                        "note": "MUFU-bound in practice: per element 8 ex2 + 8 sin + 8 cos for the modes' "
+                                "decays and turns, plus the SiLUs and softplus"},
+           "gpu_launches": (4 if ws_big else 2) * steps, "clocks": clk.summary()}
+    del inp, y, ws
+    return res
+
+
 def bench_decode(w, local, replays=3, layers=None, tokens=None):
     """28 layers x 256 tokens, one mamba_step per layer and token, replayed
     from one CUDA graph.  decode steps/s = tokens (for all 64 sequences
@@ -941,6 +995,9 @@ def main():
     ap.add_argument("--backward-only", action="store_true", help="the backward block alone (profiling)")
     ap.add_argument("--no-layer", action="store_true")
     ap.add_argument("--no-ssd", action="store_true")
+    ap.add_argument("--no-complex", action="store_true")
+    ap.add_argument("--complex-only", action="store_true",
+                    help="the complex-valued scan blocks alone (profiling)")
     ap.add_argument("--no-extra-prefill", action="store_true",
                     help="skip the secondary prefill blocks (one-call 256k, 32k workload)")
     ap.add_argument("--ssd-only", action="store_true", help="the Mamba-2 scan block alone (profiling)")
@@ -979,6 +1036,12 @@ def main():
         return
     if args.ssd_only:
         b = bench_ssd(w32, args.steps, args.warmup, local)
+        if rank == 0:
+            print(json.dumps(b), flush=True)
+        return
+    if args.complex_only:
+        b = {rule: bench_complex(w32, args.steps, args.warmup, local, rule == "trapezoidal", args.n_chunks)
+             for rule in ("euler", "trapezoidal")}
         if rank == 0:
             print(json.dumps(b), flush=True)
         return
@@ -1038,6 +1101,10 @@ def main():
         torch.cuda.empty_cache()
     if not args.no_ssd:
         line["mamba2"] = bench_ssd(w32, max(3, min(args.steps, 20)), 3, local)
+        torch.cuda.empty_cache()
+    if not args.no_complex:
+        line["complex"] = {rule: bench_complex(w32, max(3, min(args.steps, 20)), 3, local, rule == "trapezoidal")
+                           for rule in ("euler", "trapezoidal")}
         torch.cuda.empty_cache()
     if not args.no_layer:
         line["layer"] = bench_layer(w32, max(3, min(args.steps, 20)), 3, local, args.n_chunks)

@@ -374,6 +374,87 @@ size_t mamba2_scan_workspace_size(int batch, int seqlen, int heads);
 mamba_status mamba2_scan_fwd(const mamba2_scan_args *args, void *stream);
 
 /*
+ * The complex-valued scan: Mamba-3's state update, from the lesson
+ * "Jamba -- SSM-Transformer Hibrido", section "Mamba-3: a linha de base de
+ * SSM puro em 2026", item 2 (a complex-valued state, equal to a
+ * data-dependent rotary embedding of the state) and item 1 (the
+ * exponential-trapezoidal discretization).  The pages print no formula;
+ * this library reads them as the Mamba layer of mamba_scan_fwd with its
+ * diagonal state made complex.  Per channel c, M = 8 complex modes
+ * (d_state = 16 real numbers, the real scan's state size):
+ *
+ *   u        = silu(conv(x)),  dt = softplus(dt_raw)      (as mamba_scan_fwd)
+ *   lambda_n = -exp(A_log[c,n]) + i theta[c,n]
+ *   alpha_n  = exp(dt lambda_n)       (decay, and a turn by the angle dt theta_n)
+ *   v_n      = (Bm[b,t,2n] + i Bm[b,t,2n+1]) u                (state input)
+ *   EULER:        h_n = alpha_n h_n + dt v_n
+ *   TRAPEZOIDAL:  h_n = alpha_n (h_n + dt/2 vprev_n) + dt/2 v_n,  vprev = v
+ *   y        = (Re(sum_n (Cm[b,t,2n] + i Cm[b,t,2n+1]) h_n) + D[c] u) silu(z)
+ *
+ * The trapezoidal rule weights the state inputs at both ends of the step
+ * (the earlier one carried through the step's decay and turn); it reduces
+ * to Euler's rule when the earlier end's weight is moved to the later end.
+ *
+ *   x, z, dt_raw      (B, L, D) io
+ *   Bm, Cm            (B, L, 16) io       8 complex numbers as (re, im) pairs
+ *   A_log, theta      (D, 8) fp32
+ *   Dskip, conv_w, conv_b, conv_state0, final_conv_state, y   as for
+ *                     mamba_scan_fwd
+ *   h0, final_h       (B, D, 16) fp32 or NULL     complex state, (re, im)
+ *                                                 pairs; final_h may alias h0
+ *   v0, final_v       (B, D, 16) fp32 or NULL     the state input v of the
+ *                     token before the first one (trapezoidal; NULL: zero)
+ *                     and of the last token, so that a sequence split into
+ *                     calls carrying (final_h, final_conv_state, final_v)
+ *                     into (h0, conv_state0, v0) equals one call; final_v
+ *                     may alias v0
+ *   workspace         at least mamba3_scan_workspace_size() bytes, 256-byte
+ *                     aligned, contents need not be initialised
+ *   n_chunks          0: the library picks; 1: one sequential pass; k > 1:
+ *                     k chunks in parallel, each chunk's entering state
+ *                     computed exactly (no term is dropped): every chunk but
+ *                     the last is first run from a zero state, and those end
+ *                     states are folded in chunk order
+ *   discretization    MAMBA3_EULER or MAMBA3_TRAPEZOIDAL
+ *   wait_timeout_ns   limit of every device-side wait (0: 1 second)
+ *
+ * d_state must be 16, d_conv 4, d_inner a multiple of 16.  seqlen may be 0
+ * (the final states are then copies of the initial ones, or zeros).
+ * Precision: the turn dt theta is reduced to [-pi, pi] exactly (its whole
+ * revolutions removed with the product's rounding error kept), but it
+ * carries dt's own fp32 rounding (a few 1e-8 of dt): a mode turning by
+ * thousands of radians per token loses the fp32 accuracy of its angle.
+ */
+#define MAMBA3_EULER 0
+#define MAMBA3_TRAPEZOIDAL 1
+
+typedef struct mamba3_scan_args {
+    int batch, seqlen, d_inner, d_state, d_conv;
+    mamba_dtype io;
+    const void *x, *z, *dt_raw;
+    const void *Bm, *Cm;
+    const float *A_log, *theta, *Dskip, *conv_w, *conv_b;
+    const float *h0;
+    const void *conv_state0;
+    const float *v0;
+    void *y;
+    float *final_h;
+    void *final_conv_state;
+    float *final_v;
+    void *workspace;
+    size_t workspace_bytes;
+    int n_chunks;
+    int discretization;
+    uint64_t wait_timeout_ns;
+} mamba3_scan_args;
+
+/* Bytes of workspace mamba3_scan_fwd needs (0 only for invalid sizes or
+ * seqlen 0). */
+size_t mamba3_scan_workspace_size(int batch, int seqlen, int d_inner, int n_chunks);
+
+mamba_status mamba3_scan_fwd(const mamba3_scan_args *args, void *stream);
+
+/*
  * Decode: one token through the layer, state updated in place -- the
  * constant-memory recurrence of "Um SSM em uma pagina" (y_t needs only
  * h_{t-1} and x_t).  Bit for bit the same arithmetic as one token of

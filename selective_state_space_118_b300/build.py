@@ -11,7 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmamba_ssm.so")
 SOURCES = ["kernels.cu", "api.cpp", "noalloc.cu", "gemm.cpp"]
-HEADERS = ["ptx.cuh", "ssm_math.cuh", "scan_fwd.cuh", "scan_bwd.cuh", "step.cuh", "params.h", "launch.h", "gemm.h", "ssd.cuh"]
+HEADERS = ["ptx.cuh", "ssm_math.cuh", "scan_fwd.cuh", "scan_bwd.cuh", "scan_complex.cuh", "step.cuh", "params.h", "launch.h", "gemm.h", "ssd.cuh"]
 PUBLIC_HEADER = os.path.join(os.path.dirname(HERE), "include", "mamba_ssm.h")
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

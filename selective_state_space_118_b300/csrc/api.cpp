@@ -358,6 +358,40 @@ mamba_status launch_forward(const mamba_scan_args* a, const Plan& pl, const Work
   return MAMBA_OK;
 }
 
+// The complex scan's plan: chunks of whole tiles, as many as fill the GPU
+// with about 16 one-warp CTAs per SM (its chunked mode recomputes every chunk
+// but the last once as a summary, so no more chunks than that), at most 64.
+Plan complex_plan(int batch, int seqlen, int d_inner, int n_chunks_req) {
+  const int tiles = (seqlen + kT - 1) / kT;
+  int n = n_chunks_req;
+  if (n <= 0) {
+    const long groups = (long)batch * ((d_inner + kLanes - 1) / kLanes);
+    const long target = 16L * sm_count();
+    n = (int)((target + groups - 1) / groups);
+    if (n > 64) n = 64;
+  }
+  if (n > tiles) n = tiles;
+  if (n < 1) n = 1;
+  const int C = (tiles + n - 1) / n;
+  return Plan{(tiles + C - 1) / C, C, 1, C};
+}
+
+struct ComplexWorkspace {
+  size_t bc, hloc, sdt, carry, total;
+};
+
+ComplexWorkspace complex_workspace_layout(int batch, int seqlen, int d_inner, const Plan& pl) {
+  ComplexWorkspace w{0, 0, 0, 0, 0};
+  const size_t B = batch, L = seqlen, D = d_inner, n = pl.n_chunks;
+  w.total = round256(B * L * 32 * sizeof(float));
+  if (n <= 1) return w;
+  w.hloc = w.total;
+  w.sdt = round256(w.hloc + B * n * D * 16 * sizeof(float));
+  w.carry = round256(w.sdt + B * n * D * sizeof(float));
+  w.total = round256(w.carry + B * n * D * 16 * sizeof(float));
+  return w;
+}
+
 }  // namespace
 
 extern "C" {
@@ -772,6 +806,92 @@ mamba_status mamba_step(const mamba_step_args* a, void* stream_v) {
   p.y_t = a->y_t;
   const IoType io = a->io == MAMBA_BF16 ? IoType::BF16 : IoType::F32;
   if (mamba::launch_step(io, p, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+  return MAMBA_OK;
+}
+
+size_t mamba3_scan_workspace_size(int batch, int seqlen, int d_inner, int n_chunks) {
+  if (batch <= 0 || seqlen <= 0 || d_inner <= 0 || d_inner % 16 || n_chunks < 0) return 0;
+  return complex_workspace_layout(batch, seqlen, d_inner, complex_plan(batch, seqlen, d_inner, n_chunks)).total;
+}
+
+mamba_status mamba3_scan_fwd(const mamba3_scan_args* a, void* stream_v) {
+  if (!a) return MAMBA_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
+  mamba_status st = check_common(a->batch, a->d_inner, a->d_state, a->d_conv, a->io);
+  if (st != MAMBA_OK) return st;
+  if (a->seqlen < 0 || a->n_chunks < 0) return MAMBA_ERR_INVALID_ARG;
+  if (a->discretization != MAMBA3_EULER && a->discretization != MAMBA3_TRAPEZOIDAL) return MAMBA_ERR_UNSUPPORTED;
+  if (!a->A_log || !a->theta || !a->Dskip || !a->conv_w) return MAMBA_ERR_INVALID_ARG;
+  const void* aligned_ptrs[] = {a->A_log, a->theta, a->Dskip, a->conv_w, a->conv_b, a->h0, a->conv_state0,
+                                a->v0, a->final_h, a->final_v, a->final_conv_state};
+  for (const void* p : aligned_ptrs)
+    if (p && !aligned16(p)) return MAMBA_ERR_INVALID_ARG;
+  const size_t B = a->batch, D = a->d_inner, es = esize(a->io);
+  if (a->seqlen == 0) {
+    // nothing to scan: the final states are the initial ones
+    const void* src[] = {a->h0, a->v0, a->conv_state0};
+    void* dst[] = {a->final_h, a->final_v, a->final_conv_state};
+    const size_t bytes[] = {B * D * 16 * sizeof(float), B * D * 16 * sizeof(float), B * 3 * D * es};
+    for (int i = 0; i < 3; ++i) {
+      if (!dst[i] || dst[i] == src[i]) continue;
+      cudaError_t e = src[i] ? cudaMemcpyAsync(dst[i], src[i], bytes[i], cudaMemcpyDeviceToDevice, stream)
+                             : cudaMemsetAsync(dst[i], 0, bytes[i], stream);
+      if (e != cudaSuccess) return MAMBA_ERR_CUDA;
+    }
+    return MAMBA_OK;
+  }
+  const void* io_ptrs[] = {a->x, a->z, a->dt_raw, a->Bm, a->Cm, a->y};
+  for (const void* p : io_ptrs)
+    if (!p || !aligned16(p)) return MAMBA_ERR_INVALID_ARG;
+  if ((long long)a->seqlen * (long long)D > (1LL << 40)) return MAMBA_ERR_UNSUPPORTED;
+
+  const Plan pl = complex_plan(a->batch, a->seqlen, a->d_inner, a->n_chunks);
+  const ComplexWorkspace ws = complex_workspace_layout(a->batch, a->seqlen, a->d_inner, pl);
+  if (!a->workspace || a->workspace_bytes < ws.total) return MAMBA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return MAMBA_ERR_INVALID_ARG;
+  char* wsp = static_cast<char*>(a->workspace);
+  float* bc = reinterpret_cast<float*>(wsp + ws.bc);
+
+  CUtensorMap maps[4];  // x, z, dt_raw, bc
+  if (!encode3d(&maps[0], a->x, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
+      !encode3d(&maps[1], a->z, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
+      !encode3d(&maps[2], a->dt_raw, a->io, a->d_inner, a->seqlen, a->batch, kLanes) ||
+      !encode3d(&maps[3], bc, MAMBA_F32, 32, a->seqlen, a->batch, 32))
+    return MAMBA_ERR_CUDA;
+
+  mamba::ComplexParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.batch = a->batch;
+  p.seqlen = a->seqlen;
+  p.d_inner = a->d_inner;
+  p.n_groups = (a->d_inner + kLanes - 1) / kLanes;
+  p.chunk_tiles = pl.chunk_tiles;
+  p.n_chunks = pl.n_chunks;
+  p.A_log = a->A_log;
+  p.theta = a->theta;
+  p.Dskip = a->Dskip;
+  p.conv_w = a->conv_w;
+  p.conv_b = a->conv_b;
+  p.h0 = a->h0;
+  p.conv_state0 = a->conv_state0;
+  p.v0 = a->v0;
+  p.x = a->x;
+  p.y = a->y;
+  p.final_h = a->final_h;
+  p.final_v = a->final_v;
+  p.final_conv_state = a->final_conv_state;
+  p.bc = bc;
+  p.timeout_ns = a->wait_timeout_ns ? a->wait_timeout_ns : kDefaultTimeoutNs;
+  if (pl.n_chunks > 1) {
+    p.hloc = reinterpret_cast<float*>(wsp + ws.hloc);
+    p.sdt = reinterpret_cast<float*>(wsp + ws.sdt);
+    p.carry = reinterpret_cast<float*>(wsp + ws.carry);
+  }
+  const IoType io = a->io == MAMBA_BF16 ? IoType::BF16 : IoType::F32;
+  if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, 16, stream) != cudaSuccess)
+    return MAMBA_ERR_CUDA;
+  if (mamba::launch_complex(io, a->discretization == MAMBA3_TRAPEZOIDAL, maps, p, stream) != cudaSuccess)
+    return MAMBA_ERR_CUDA;
   return MAMBA_OK;
 }
 

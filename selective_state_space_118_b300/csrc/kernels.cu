@@ -4,6 +4,7 @@
 
 #include "launch.h"
 #include "scan_bwd.cuh"
+#include "scan_complex.cuh"
 #include "scan_fwd.cuh"
 #include "ssd.cuh"
 #include "step.cuh"
@@ -71,6 +72,39 @@ cudaError_t launch_summary(IoType io, const CUtensorMap maps[3], const ScanParam
                            cudaStream_t stream) {
   return io == IoType::BF16 ? launch_summary_t<__nv_bfloat16>(maps, p, grid, stream)
                             : launch_summary_t<float>(maps, p, grid, stream);
+}
+
+// ---------------------------------------------------------------- complex scan
+template <typename IO, bool kTrap, bool kSummary>
+static cudaError_t launch_complex_pass(const CUtensorMap* m, const ComplexParams& p, dim3 grid, cudaStream_t s) {
+  const size_t smem = sizeof(MainSmem<IO>) + 128;
+  cudaError_t e = cudaFuncSetAttribute(complex_scan_kernel<IO, kTrap, kSummary>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  complex_scan_kernel<IO, kTrap, kSummary><<<grid, kLanes, smem, s>>>(m[0], m[1], m[2], m[3], p);
+  return cudaGetLastError();
+}
+
+template <typename IO, bool kTrap>
+static cudaError_t launch_complex_t(const CUtensorMap* m, const ComplexParams& p, cudaStream_t s) {
+  if (p.n_chunks > 1) {
+    cudaError_t e =
+        launch_complex_pass<IO, kTrap, true>(m, p, dim3((unsigned)p.n_groups, (unsigned)p.batch, (unsigned)(p.n_chunks - 1)), s);
+    if (e != cudaSuccess) return e;
+    const long n = (long)p.batch * p.d_inner;
+    complex_fold_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return launch_complex_pass<IO, kTrap, false>(m, p, dim3((unsigned)p.n_groups, (unsigned)p.batch, (unsigned)p.n_chunks), s);
+}
+
+cudaError_t launch_complex(IoType io, bool trapezoidal, const CUtensorMap maps[4], const ComplexParams& p,
+                           cudaStream_t stream) {
+  if (io == IoType::BF16)
+    return trapezoidal ? launch_complex_t<__nv_bfloat16, true>(maps, p, stream)
+                       : launch_complex_t<__nv_bfloat16, false>(maps, p, stream);
+  return trapezoidal ? launch_complex_t<float, true>(maps, p, stream) : launch_complex_t<float, false>(maps, p, stream);
 }
 
 // Launched with programmatic stream serialization: the kernel may be

@@ -31,6 +31,10 @@ cudaError_t launch_scan(IoType io, const CUtensorMap maps[4], const ScanParams& 
 cudaError_t launch_summary(IoType io, const CUtensorMap maps[3], const ScanParams& p, dim3 grid,
                            cudaStream_t stream);
 cudaError_t launch_step(IoType io, const StepParams& p, cudaStream_t stream);
+// The complex-valued scan: in chunked mode the summaries, the fold and the
+// main pass; otherwise the main pass.  maps: x, z, dt_raw, bc.
+cudaError_t launch_complex(IoType io, bool trapezoidal, const CUtensorMap maps[4], const ComplexParams& p,
+                           cudaStream_t stream);
 
 // Backward.  maps: x, z, dt_raw, dy, bc.  launch_carries runs the forward's
 // chunk carries (n_fwd warps) and the adjoint carries (n_adj warps) in one

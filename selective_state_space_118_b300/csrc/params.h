@@ -93,6 +93,33 @@ struct SsdParams {
   float* cum;             // (B, H, n_chunks, 64, 2): per token, the prefix sum of dt * A and dt
 };
 
+// The complex-valued scan (scan_complex.cuh): 8 complex modes per channel,
+// states and state inputs as 16 fp32 numbers (re, im pairs) per channel.
+struct ComplexParams {
+  int batch, seqlen, d_inner;
+  int n_groups;     // ceil(d_inner / 32)
+  int chunk_tiles;  // tiles of kTileTokens tokens per chunk
+  int n_chunks;
+  const float* A_log;        // (D, 8)
+  const float* theta;        // (D, 8)
+  const float* Dskip;
+  const float* conv_w;
+  const float* conv_b;       // may be null
+  const float* h0;           // (B, D, 16) or null
+  const void* conv_state0;   // (B, 3, D) or null
+  const float* v0;           // (B, D, 16) or null: the state input before the first token
+  const void* x;             // plain pointer to x, for the conv inputs before a chunk
+  void* y;
+  float* final_h;            // may be null
+  float* final_v;            // may be null
+  void* final_conv_state;    // may be null
+  const float* bc;           // widened B/C rows (B, L, 32): per mode (Re B, Im B, Re C, Im C)
+  float* hloc;               // chunked: (B, n_chunks, D, 16) each chunk's end state from zero
+  float* sdt;                // chunked: (B, n_chunks, D) each chunk's dt sum
+  float* carry;              // chunked: (B, n_chunks, D, 16) the state entering each chunk
+  uint64_t timeout_ns;
+};
+
 struct StepParams {
   int batch, d_inner;
   float* h;           // (B, D, 16)

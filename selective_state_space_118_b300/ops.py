@@ -30,7 +30,8 @@ EXPORTED = ("mamba_scan_workspace_size", "mamba_scan_default_chunks", "mamba_sca
             "mamba_step", "mamba_last_error", "mamba_status_string", "mamba_abi_version",
             "mamba_scan_fwd_noalloc", "mamba_scan_bwd_workspace_size", "mamba_scan_bwd",
             "mamba_layer_workspace_size", "mamba_layer_fwd", "mamba2_scan_workspace_size",
-            "mamba2_scan_fwd")
+            "mamba2_scan_fwd", "mamba3_scan_workspace_size", "mamba3_scan_fwd")
+MAMBA3_EULER, MAMBA3_TRAPEZOIDAL = 0, 1
 MAMBA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _vp = ctypes.c_void_p
@@ -78,6 +79,17 @@ class Mamba2Args(ctypes.Structure):
                 ("io", ctypes.c_int), ("x", _vp), ("z", _vp), ("dt_raw", _vp), ("Bm", _vp), ("Cm", _vp),
                 ("A_log", _vp), ("Dskip", _vp), ("h0", _vp), ("y", _vp), ("final_state", _vp),
                 ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class Mamba3Args(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("seqlen", ctypes.c_int), ("d_inner", ctypes.c_int),
+                ("d_state", ctypes.c_int), ("d_conv", ctypes.c_int), ("io", ctypes.c_int),
+                ("x", _vp), ("z", _vp), ("dt_raw", _vp), ("Bm", _vp), ("Cm", _vp),
+                ("A_log", _vp), ("theta", _vp), ("Dskip", _vp), ("conv_w", _vp), ("conv_b", _vp),
+                ("h0", _vp), ("conv_state0", _vp), ("v0", _vp), ("y", _vp), ("final_h", _vp),
+                ("final_conv_state", _vp), ("final_v", _vp), ("workspace", _vp),
+                ("workspace_bytes", ctypes.c_size_t), ("n_chunks", ctypes.c_int),
+                ("discretization", ctypes.c_int), ("wait_timeout_ns", ctypes.c_uint64)]
 
 
 class StepArgs(ctypes.Structure):
@@ -138,6 +150,10 @@ def load_library(path: str = LIB_PATH):
         lib.mamba2_scan_workspace_size.restype = ctypes.c_size_t
         lib.mamba2_scan_fwd.argtypes = [ctypes.POINTER(Mamba2Args), _vp]
         lib.mamba2_scan_fwd.restype = ctypes.c_int
+        lib.mamba3_scan_workspace_size.argtypes = [ctypes.c_int] * 4
+        lib.mamba3_scan_workspace_size.restype = ctypes.c_size_t
+        lib.mamba3_scan_fwd.argtypes = [ctypes.POINTER(Mamba3Args), _vp]
+        lib.mamba3_scan_fwd.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -433,6 +449,58 @@ def mamba2_scan_fwd(x, dt_raw, A_log, Bm, Cm, Dskip, z=None, h0=None, *, y=None,
     if st != MAMBA_OK:
         raise MambaError(st, "mamba2_scan_fwd")
     return y, final_state
+
+
+def mamba3_scan_workspace_size(batch: int, seqlen: int, d_inner: int, n_chunks: int = 0) -> int:
+    return int(load_library().mamba3_scan_workspace_size(batch, seqlen, d_inner, n_chunks))
+
+
+def mamba3_scan_fwd(x, z, dt_raw, Bm, Cm, A_log, theta, Dskip, conv_w, conv_b=None, h0=None,
+                    conv_state0=None, v0=None, *, trapezoidal: bool = False, y=None, final_h=None,
+                    final_conv_state=None, final_v=None, workspace=None, n_chunks: int = 0,
+                    wait_timeout_ns: int = 0, return_state: bool = True, stream=None):
+    """The complex-valued scan (C ABI ``mamba3_scan_fwd``): x, z, dt_raw
+    (B,L,D) and Bm, Cm (B,L,16: 8 complex numbers as (re, im) pairs) in fp32
+    or bf16; A_log, theta (D,8), Dskip (D), conv_w (D,4), conv_b (D) fp32;
+    h0, v0 (B,D,16) fp32; conv_state0 (B,3,D) in the I/O dtype.  Returns
+    (y, final_h, final_conv_state, final_v) (the last three None when
+    return_state is False and they were not passed)."""
+    lib = load_library()
+    B, L, D = x.shape
+    dev = x.device
+    f32 = torch.float32
+    modes = D_STATE // 2
+    specs = _scan_specs(x, z, dt_raw, Bm, Cm, None, Dskip, conv_w, conv_b, h0, conv_state0)
+    specs += [("A_log", A_log, (D, modes), f32), ("theta", theta, (D, modes), f32),
+              ("v0", v0, (B, D, D_STATE), f32), ("y", y, (B, L, D), x.dtype),
+              ("final_h", final_h, (B, D, D_STATE), f32), ("final_v", final_v, (B, D, D_STATE), f32),
+              ("final_conv_state", final_conv_state, (B, D_CONV - 1, D), x.dtype)]
+    _check_args(specs, A_log.shape[-1] == modes and conv_w.shape[-1] == D_CONV)
+    if y is None:
+        y = torch.empty_like(x)
+    if return_state:
+        if final_h is None:
+            final_h = torch.empty((B, D, D_STATE), device=dev, dtype=f32)
+        if final_v is None:
+            final_v = torch.empty((B, D, D_STATE), device=dev, dtype=f32)
+        if final_conv_state is None:
+            final_conv_state = torch.empty((B, D_CONV - 1, D), device=dev, dtype=x.dtype)
+    ws_bytes = mamba3_scan_workspace_size(B, L, D, n_chunks)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+    a = Mamba3Args(batch=B, seqlen=L, d_inner=D, d_state=2 * A_log.shape[-1], d_conv=conv_w.shape[-1],
+                   io=_io_code(x), x=_ptr(x), z=_ptr(z), dt_raw=_ptr(dt_raw), Bm=_ptr(Bm), Cm=_ptr(Cm),
+                   A_log=_ptr(A_log), theta=_ptr(theta), Dskip=_ptr(Dskip), conv_w=_ptr(conv_w),
+                   conv_b=_ptr(conv_b), h0=_ptr(h0), conv_state0=_ptr(conv_state0), v0=_ptr(v0), y=_ptr(y),
+                   final_h=_ptr(final_h), final_conv_state=_ptr(final_conv_state), final_v=_ptr(final_v),
+                   workspace=_ptr(workspace),
+                   workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
+                   n_chunks=n_chunks, discretization=MAMBA3_TRAPEZOIDAL if trapezoidal else MAMBA3_EULER,
+                   wait_timeout_ns=wait_timeout_ns)
+    st = _launch(lib.mamba3_scan_fwd, a, stream, dev)
+    if st != MAMBA_OK:
+        raise MambaError(st, "mamba3_scan_fwd")
+    return y, final_h, final_conv_state, final_v
 
 
 def mamba_step(h, conv_state, x_t, z_t, dt_raw_t, B_t, C_t, A_log, Dskip, conv_w, conv_b=None,

@@ -25,7 +25,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mamba2?_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(mamba[23]?_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_binding_functions():
@@ -35,7 +35,7 @@ def test_header_declares_the_binding_functions():
 def test_library_exports_every_declared_symbol(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", ops.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
-    exported = set(re.findall(r"\bT (mamba2?_\w+)$", out, flags=re.M))
+    exported = set(re.findall(r"\bT (mamba[23]?_\w+)$", out, flags=re.M))
     missing = set(declared_functions()) - exported
     assert not missing, f"declared but not exported: {missing}"
     for name in declared_functions():
@@ -58,7 +58,8 @@ def _c_layout(tmp_path, struct, fields):
                                         ("mamba_step_args", ops.StepArgs),
                                         ("mamba_scan_bwd_args", ops.BwdArgs),
                                         ("mamba_layer_args", ops.LayerArgs),
-                                        ("mamba2_scan_args", ops.Mamba2Args)])
+                                        ("mamba2_scan_args", ops.Mamba2Args),
+                                        ("mamba3_scan_args", ops.Mamba3Args)])
 def test_ctypes_structs_match_c_layout(tmp_path, struct, cls):
     fields = [f for f, _ in cls._fields_]
     c = _c_layout(tmp_path, struct, fields)
@@ -346,3 +347,42 @@ def test_step_layer_mamba2_bindings_check_shapes():
             mamba2(**kw)
     with pytest.raises(ValueError, match=CUDA_MSG):
         mamba2(x=torch.zeros(Bt, L, Hh, 32, dtype=bf))  # head_dim 32: unsupported, left to the library
+
+
+def test_complex_scan_argument_checks(lib):
+    """mamba3_scan_fwd refuses missing or misaligned pointers, an unknown
+    discretization, unsupported sizes and a short workspace before anything
+    runs (no GPU needed: the pointers are never dereferenced)."""
+    full = dict(batch=1, seqlen=64, d_inner=32, d_state=16, d_conv=4, io=ops.MAMBA_BF16, x=FAKE, z=FAKE,
+                dt_raw=FAKE, Bm=FAKE, Cm=FAKE, A_log=FAKE, theta=FAKE, Dskip=FAKE, conv_w=FAKE, y=FAKE)
+
+    def call(**kw):
+        return lib.mamba3_scan_fwd(ctypes.byref(ops.Mamba3Args(**dict(full, **kw))), None)
+    assert lib.mamba3_scan_fwd(None, None) == ops.MAMBA_ERR_INVALID_ARG
+    for k in ("x", "z", "dt_raw", "Bm", "Cm", "A_log", "theta", "Dskip", "conv_w", "y"):
+        assert call(**{k: 0}) == ops.MAMBA_ERR_INVALID_ARG, k
+        assert call(**{k: FAKE + 4}) == ops.MAMBA_ERR_INVALID_ARG, k
+    for k in ("h0", "v0", "final_h", "final_v", "conv_b", "conv_state0", "final_conv_state"):
+        assert call(**{k: FAKE + 8}) == ops.MAMBA_ERR_INVALID_ARG, k
+    assert call(discretization=2) == ops.MAMBA_ERR_UNSUPPORTED
+    assert call(d_state=8) == ops.MAMBA_ERR_UNSUPPORTED
+    assert call(d_inner=24) == ops.MAMBA_ERR_UNSUPPORTED
+    assert call(seqlen=-1) == ops.MAMBA_ERR_INVALID_ARG
+    assert call() == ops.MAMBA_ERR_WORKSPACE
+    need = ops.mamba3_scan_workspace_size(1, 64, 32, 0)
+    assert call(workspace=FAKE, workspace_bytes=need - 1) == ops.MAMBA_ERR_WORKSPACE
+
+
+def test_complex_scan_workspace(lib):
+    def r256(v):
+        return (v + 255) // 256 * 256
+    # one pass: B and C widened to fp32 (B, L, 32)
+    assert ops.mamba3_scan_workspace_size(2, 1000, 64, 1) == r256(2 * 1000 * 32 * 4)
+    # chunked: plus the chunks' end states from zero, their dt sums and the
+    # entering states (B, n, D, 16), (B, n, D), (B, n, D, 16)
+    B, L, D, n = 1, 4096, 64, 4
+    need = B * L * 32 * 4 + B * n * D * 16 * 4 + B * n * D * 4 + B * n * D * 16 * 4
+    ws = ops.mamba3_scan_workspace_size(B, L, D, n)
+    assert need <= ws <= need + 4 * 256
+    assert ops.mamba3_scan_workspace_size(1, 0, 64, 0) == 0
+    assert ops.mamba3_scan_workspace_size(1, 64, 24, 0) == 0
