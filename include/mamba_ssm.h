@@ -455,6 +455,40 @@ size_t mamba3_scan_workspace_size(int batch, int seqlen, int d_inner, int n_chun
 mamba_status mamba3_scan_fwd(const mamba3_scan_args *args, void *stream);
 
 /*
+ * A linear map on the tensor cores, for the projections around the scan
+ * (in_proj, x_proj, dt_proj, out_proj of "【大模型】- Jamba 混合
+ * SSM-Transformer", section "实现 > Mamba 层", each an nn.Linear):
+ *
+ *   C = A W^T (+ bias)      row-major; fp32 accumulation, bf16 result
+ *
+ *   M, N, K           C is M x N; A is M x K; W is N x K (the nn.Linear weight
+ *                     layout, rows K elements apart); M may be 0
+ *   A, lda            bf16, rows lda >= K elements apart
+ *   W                 bf16
+ *   bias              (N) bf16 or NULL
+ *   C, ldc            bf16 output, rows ldc >= N elements apart
+ *   wait_timeout_ns   limit of every device-side wait (0: 1 second)
+ *
+ * K must be a multiple of 64 and lda, ldc multiples of 8
+ * (MAMBA_ERR_UNSUPPORTED otherwise); pointers 16-byte aligned.  The
+ * product runs in hand-written tcgen05 code: 128 x 256 output tiles, the
+ * accumulator in tensor memory, operands brought into shared memory by TMA.
+ */
+typedef struct mamba_linear_args {
+    long M;
+    int N, K;
+    const void *A;
+    int lda;
+    const void *W;
+    const void *bias;
+    void *C;
+    int ldc;
+    uint64_t wait_timeout_ns;
+} mamba_linear_args;
+
+mamba_status mamba_linear_fwd(const mamba_linear_args *args, void *stream);
+
+/*
  * Decode: one token through the layer, state updated in place -- the
  * constant-memory recurrence of "Um SSM em uma pagina" (y_t needs only
  * h_{t-1} and x_t).  Bit for bit the same arithmetic as one token of

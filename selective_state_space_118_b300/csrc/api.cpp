@@ -282,6 +282,21 @@ bool encode3d(CUtensorMap* m, const void* base, mamba_dtype io, int inner, int L
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over a row-major bf16 matrix of `rows` rows of `inner` elements,
+// rows `ld` elements apart, read in boxes of 64 elements (128 bytes) x
+// box_rows rows with the 128-byte swizzle (the tensor-core GEMM's operands).
+bool encode2d_sw128(CUtensorMap* m, const void* base, int inner, long rows, long ld, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 mamba_status check_common(int batch, int d_inner, int d_state, int d_conv, mamba_dtype io) {
   if (batch <= 0 || d_inner <= 0) return MAMBA_ERR_INVALID_ARG;
   if (io != MAMBA_F32 && io != MAMBA_BF16) return MAMBA_ERR_UNSUPPORTED;
@@ -891,6 +906,32 @@ mamba_status mamba3_scan_fwd(const mamba3_scan_args* a, void* stream_v) {
   if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, 16, stream) != cudaSuccess)
     return MAMBA_ERR_CUDA;
   if (mamba::launch_complex(io, a->discretization == MAMBA3_TRAPEZOIDAL, maps, p, stream) != cudaSuccess)
+    return MAMBA_ERR_CUDA;
+  return MAMBA_OK;
+}
+
+mamba_status mamba_linear_fwd(const mamba_linear_args* a, void* stream_v) {
+  if (!a) return MAMBA_ERR_INVALID_ARG;
+  if (a->M < 0 || a->N <= 0 || a->K <= 0 || a->lda < a->K || a->ldc < a->N) return MAMBA_ERR_INVALID_ARG;
+  if (a->M == 0) return MAMBA_OK;  // nothing to compute (an empty A or C may have no address)
+  if (!a->A || !a->W || !a->C) return MAMBA_ERR_INVALID_ARG;
+  const void* al[] = {a->A, a->W, a->C, a->bias};
+  for (const void* p : al)
+    if (p && !aligned16(p)) return MAMBA_ERR_INVALID_ARG;
+  if (a->K % 64 || a->lda % 8 || a->ldc % 8) return MAMBA_ERR_UNSUPPORTED;
+  CUtensorMap ma, mw;
+  if (!encode2d_sw128(&ma, a->A, a->K, a->M, a->lda, 128) || !encode2d_sw128(&mw, a->W, a->K, a->N, a->K, 256))
+    return MAMBA_ERR_CUDA;
+  mamba::GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.M = a->M;
+  p.N = a->N;
+  p.K = a->K;
+  p.ldc = a->ldc;
+  p.C = a->C;
+  p.bias = a->bias;
+  p.timeout_ns = a->wait_timeout_ns ? a->wait_timeout_ns : kDefaultTimeoutNs;
+  if (mamba::launch_gemm_tc(ma, mw, p, reinterpret_cast<cudaStream_t>(stream_v)) != cudaSuccess)
     return MAMBA_ERR_CUDA;
   return MAMBA_OK;
 }

@@ -2,6 +2,7 @@
 // chunk carries, decode step and the sticky error word) and its launchers.
 #include <cuda_bf16.h>
 
+#include "gemm_tc.cuh"
 #include "launch.h"
 #include "scan_bwd.cuh"
 #include "scan_complex.cuh"
@@ -72,6 +73,19 @@ cudaError_t launch_summary(IoType io, const CUtensorMap maps[3], const ScanParam
                            cudaStream_t stream) {
   return io == IoType::BF16 ? launch_summary_t<__nv_bfloat16>(maps, p, grid, stream)
                             : launch_summary_t<float>(maps, p, grid, stream);
+}
+
+// ---------------------------------------------------------------- tensor-core GEMM
+cudaError_t launch_gemm_tc(const CUtensorMap& a, const CUtensorMap& w, const GemmParams& p, cudaStream_t s) {
+  const size_t smem = sizeof(GemmSmem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long tiles = ((p.M + kGemmBM - 1) / kGemmBM) * (long)((p.N + kGemmBN - 1) / kGemmBN);
+  const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
+  gemm_tc_kernel<<<grid, kGemmThreads, smem, s>>>(a, w, p);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- complex scan

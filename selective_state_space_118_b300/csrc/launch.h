@@ -54,6 +54,10 @@ cudaError_t launch_io_to_f32(IoType io, const void* src, float* dst, long n, cud
 // that; scan_occupancy sets the same attribute).
 void scan_occupancy(IoType io, int* main_per_sm, int* summary_per_sm);
 
+// C = A W^T [+ bias] on the tensor cores (gemm_tc.cuh).  a: A (K x M, box
+// 64 x 128), w: W (K x N, box 64 x 256), both bf16 with the 128-byte swizzle.
+cudaError_t launch_gemm_tc(const CUtensorMap& a, const CUtensorMap& w, const GemmParams& p, cudaStream_t s);
+
 // Reads and clears the sticky device error word of the current device
 // (synchronises the stream first).
 cudaError_t take_device_error(unsigned* code, cudaStream_t stream);

@@ -120,6 +120,17 @@ struct ComplexParams {
   uint64_t timeout_ns;
 };
 
+// The tensor-core GEMM (gemm_tc.cuh): row-major C (M x N, bf16, rows ldc
+// elements apart) = A W^T [+ bias]; A and W are read through tensor maps.
+struct GemmParams {
+  long M;
+  int N, K;
+  int ldc;
+  void* C;             // bf16
+  const void* bias;    // (N) bf16 or null
+  uint64_t timeout_ns;
+};
+
 struct StepParams {
   int batch, d_inner;
   float* h;           // (B, D, 16)

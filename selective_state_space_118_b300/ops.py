@@ -30,7 +30,7 @@ EXPORTED = ("mamba_scan_workspace_size", "mamba_scan_default_chunks", "mamba_sca
             "mamba_step", "mamba_last_error", "mamba_status_string", "mamba_abi_version",
             "mamba_scan_fwd_noalloc", "mamba_scan_bwd_workspace_size", "mamba_scan_bwd",
             "mamba_layer_workspace_size", "mamba_layer_fwd", "mamba2_scan_workspace_size",
-            "mamba2_scan_fwd", "mamba3_scan_workspace_size", "mamba3_scan_fwd")
+            "mamba2_scan_fwd", "mamba3_scan_workspace_size", "mamba3_scan_fwd", "mamba_linear_fwd")
 MAMBA3_EULER, MAMBA3_TRAPEZOIDAL = 0, 1
 MAMBA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -90,6 +90,11 @@ class Mamba3Args(ctypes.Structure):
                 ("final_conv_state", _vp), ("final_v", _vp), ("workspace", _vp),
                 ("workspace_bytes", ctypes.c_size_t), ("n_chunks", ctypes.c_int),
                 ("discretization", ctypes.c_int), ("wait_timeout_ns", ctypes.c_uint64)]
+
+
+class LinearArgs(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_long), ("N", ctypes.c_int), ("K", ctypes.c_int), ("A", _vp), ("lda", ctypes.c_int),
+                ("W", _vp), ("bias", _vp), ("C", _vp), ("ldc", ctypes.c_int), ("wait_timeout_ns", ctypes.c_uint64)]
 
 
 class StepArgs(ctypes.Structure):
@@ -154,6 +159,8 @@ def load_library(path: str = LIB_PATH):
         lib.mamba3_scan_workspace_size.restype = ctypes.c_size_t
         lib.mamba3_scan_fwd.argtypes = [ctypes.POINTER(Mamba3Args), _vp]
         lib.mamba3_scan_fwd.restype = ctypes.c_int
+        lib.mamba_linear_fwd.argtypes = [ctypes.POINTER(LinearArgs), _vp]
+        lib.mamba_linear_fwd.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -501,6 +508,33 @@ def mamba3_scan_fwd(x, z, dt_raw, Bm, Cm, A_log, theta, Dskip, conv_w, conv_b=No
     if st != MAMBA_OK:
         raise MambaError(st, "mamba3_scan_fwd")
     return y, final_h, final_conv_state, final_v
+
+
+def mamba_linear_fwd(A, W, bias=None, *, out=None, wait_timeout_ns: int = 0, stream=None):
+    """C = A W^T (+ bias) on the tensor cores (C ABI ``mamba_linear_fwd``):
+    A (..., K), W (N, K), bias (N) bf16; returns C (..., N) bf16.  A's rows
+    may be a strided view (rows lda apart) of a wider matrix."""
+    lib = load_library()
+    K = A.shape[-1]
+    N = W.shape[0]
+    bf = torch.bfloat16
+    A2 = A.reshape(-1, K) if A.is_contiguous() else A
+    if A2.dim() != 2 or A2.stride(1) != 1:
+        raise ValueError("A must be a row-major matrix (rows may be strided)")
+    M = A2.shape[0]
+    _check_args([("A", A2, (M, K), bf), ("W", W, (N, K), bf), ("bias", bias, (N,), bf)])
+    if out is None:
+        out = torch.empty(A.shape[:-1] + (N,), device=A.device, dtype=bf)
+    C2 = out.reshape(-1, N) if out.is_contiguous() else out
+    _check_args([("out", C2, (M, N), bf)])
+    if not (A2.is_cuda and W.is_cuda and C2.is_cuda) or not W.is_contiguous():
+        raise ValueError("tensors must be on a CUDA device and W contiguous")
+    a = LinearArgs(M=M, N=N, K=K, A=A2.data_ptr(), lda=A2.stride(0), W=W.data_ptr(), bias=_ptr(bias),
+                   C=C2.data_ptr(), ldc=C2.stride(0), wait_timeout_ns=wait_timeout_ns)
+    st = _launch(lib.mamba_linear_fwd, a, stream, A.device)
+    if st != MAMBA_OK:
+        raise MambaError(st, "mamba_linear_fwd")
+    return out
 
 
 def mamba_step(h, conv_state, x_t, z_t, dt_raw_t, B_t, C_t, A_log, Dskip, conv_w, conv_b=None,

@@ -59,7 +59,8 @@ def _c_layout(tmp_path, struct, fields):
                                         ("mamba_scan_bwd_args", ops.BwdArgs),
                                         ("mamba_layer_args", ops.LayerArgs),
                                         ("mamba2_scan_args", ops.Mamba2Args),
-                                        ("mamba3_scan_args", ops.Mamba3Args)])
+                                        ("mamba3_scan_args", ops.Mamba3Args),
+                                        ("mamba_linear_args", ops.LinearArgs)])
 def test_ctypes_structs_match_c_layout(tmp_path, struct, cls):
     fields = [f for f, _ in cls._fields_]
     c = _c_layout(tmp_path, struct, fields)
@@ -386,3 +387,22 @@ def test_complex_scan_workspace(lib):
     assert need <= ws <= need + 4 * 256
     assert ops.mamba3_scan_workspace_size(1, 0, 64, 0) == 0
     assert ops.mamba3_scan_workspace_size(1, 64, 24, 0) == 0
+
+
+def test_linear_argument_checks(lib):
+    full = dict(M=256, N=256, K=128, A=FAKE, lda=128, W=FAKE, C=FAKE, ldc=256)
+
+    def call(**kw):
+        return lib.mamba_linear_fwd(ctypes.byref(ops.LinearArgs(**dict(full, **kw))), None)
+    assert lib.mamba_linear_fwd(None, None) == ops.MAMBA_ERR_INVALID_ARG
+    for k in ("A", "W", "C"):
+        assert call(**{k: 0}) == ops.MAMBA_ERR_INVALID_ARG, k
+        assert call(**{k: FAKE + 8}) == ops.MAMBA_ERR_INVALID_ARG, k
+    assert call(bias=FAKE + 2) == ops.MAMBA_ERR_INVALID_ARG
+    assert call(K=96, lda=96) == ops.MAMBA_ERR_UNSUPPORTED
+    assert call(lda=132) == ops.MAMBA_ERR_UNSUPPORTED
+    assert call(ldc=260) == ops.MAMBA_ERR_UNSUPPORTED
+    assert call(lda=64) == ops.MAMBA_ERR_INVALID_ARG
+    assert call(ldc=128) == ops.MAMBA_ERR_INVALID_ARG
+    assert call(M=-1) == ops.MAMBA_ERR_INVALID_ARG
+    assert call(M=0) == ops.MAMBA_OK  # nothing to do, nothing touched
