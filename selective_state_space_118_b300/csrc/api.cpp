@@ -285,16 +285,21 @@ bool encode3d(CUtensorMap* m, const void* base, mamba_dtype io, int inner, int L
 // 2-D map over a row-major bf16 matrix of `rows` rows of `inner` elements,
 // rows `ld` elements apart, read in boxes of 64 elements (128 bytes) x
 // box_rows rows with the 128-byte swizzle (the tensor-core GEMM's operands).
-bool encode2d_sw128(CUtensorMap* m, const void* base, int inner, long rows, long ld, int box_rows) {
+bool encode2d_bf16(CUtensorMap* m, const void* base, int inner, long rows, long ld, int box_inner, int box_rows,
+                   CUtensorMapSwizzle swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode2d_sw128(CUtensorMap* m, const void* base, int inner, long rows, long ld, int box_rows) {
+  return encode2d_bf16(m, base, inner, rows, ld, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 mamba_status check_common(int batch, int d_inner, int d_state, int d_conv, mamba_dtype io) {
@@ -919,19 +924,25 @@ mamba_status mamba_linear_fwd(const mamba_linear_args* a, void* stream_v) {
   for (const void* p : al)
     if (p && !aligned16(p)) return MAMBA_ERR_INVALID_ARG;
   if (a->K % 64 || a->lda % 8 || a->ldc % 8) return MAMBA_ERR_UNSUPPORTED;
-  CUtensorMap ma, mw;
-  if (!encode2d_sw128(&ma, a->A, a->K, a->M, a->lda, 128) || !encode2d_sw128(&mw, a->W, a->K, a->N, a->K, 256))
+  // the N extent cut evenly into tiles of at most 256 columns, each a
+  // multiple of 32 (the W box is as many rows)
+  const int tiles_n = (a->N + 255) / 256;
+  const int bn = ((a->N + tiles_n - 1) / tiles_n + 31) / 32 * 32;
+  CUtensorMap ma, mw, mc;
+  if (!encode2d_sw128(&ma, a->A, a->K, a->M, a->lda, 128) || !encode2d_sw128(&mw, a->W, a->K, a->N, a->K, bn / 2) ||
+      !encode2d_bf16(&mc, a->C, a->N, a->M, a->ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return MAMBA_ERR_CUDA;
   mamba::GemmParams p;
   std::memset(&p, 0, sizeof(p));
   p.M = a->M;
   p.N = a->N;
   p.K = a->K;
+  p.bn = bn;
   p.ldc = a->ldc;
   p.C = a->C;
   p.bias = a->bias;
   p.timeout_ns = a->wait_timeout_ns ? a->wait_timeout_ns : kDefaultTimeoutNs;
-  if (mamba::launch_gemm_tc(ma, mw, p, reinterpret_cast<cudaStream_t>(stream_v)) != cudaSuccess)
+  if (mamba::launch_gemm_tc(ma, mw, mc, p, reinterpret_cast<cudaStream_t>(stream_v)) != cudaSuccess)
     return MAMBA_ERR_CUDA;
   return MAMBA_OK;
 }

@@ -2,21 +2,29 @@
 // row-major C (M x N) = A (M x K) * W^T (W: N x K, the nn.Linear weight
 // layout) [+ bias (N)], fp32 accumulation in tensor memory, bf16 out.
 //
-// Work decomposition.  Output tiles of 128 x 256, taken by a persistent grid
-// (one CTA per SM) in row-block order, so that the CTAs running at once share
-// A's row block and walk W, which stays in L2.  Per CTA, six warps with fixed
+// Work decomposition.  Output tiles of 256 x bn (bn: the N extent divided
+// evenly into tiles of at most 256, rounded up to 32), each taken by a
+// cluster of two CTAs (one per SM; a persistent grid) that compute its two
+// 128-row halves: each CTA loads its own rows of A and half of W's bn rows,
+// multicast to both, so that a W tile crosses from L2 once per pair.  Tiles
+// are taken in row-block order, so that the clusters running at once share
+// A's rows and walk W, which stays in L2.  Per CTA, six warps with fixed
 // roles:
 //   warp 0     the producer: one lane issues the TMA loads of A and W tiles
 //              (64 columns of K, 128 B rows, 128-byte swizzle) into a ring of
-//              4 shared-memory stages, each released by the MMA that read it;
+//              4 shared-memory stages, each released when the MMAs of both
+//              CTAs have read it;
 //   warp 1     owns the tensor memory (512 columns: two accumulators of 256)
 //              and one lane issues the MMAs: per stage four 128 x 256 x 16
-//              tcgen05.mma, then a commit that frees the stage; per tile a
-//              commit that hands the accumulator to the epilogue;
+//              tcgen05.mma, then a commit that frees the stage (arriving in
+//              both CTAs); per tile a commit that hands the accumulator to
+//              the epilogue;
 //   warps 2-5  the epilogue: each reads its 32 TMEM lanes (tile rows) 32
-//              columns at a time, adds the bias, rounds to bf16 and stores
-//              64 contiguous bytes per row, then frees the accumulator; the
-//              next tile's MMAs run meanwhile in the other accumulator.
+//              columns at a time, adds the bias, rounds to bf16, writes the
+//              32 x 32 chunk into one of two staging buffers of its own and
+//              stores it with one TMA store; the accumulator is freed after
+//              its last load, and the next tile's MMAs run meanwhile in the
+//              other accumulator.
 // Every wait on an mbarrier is bounded (wait_timeout_ns); a wait that gives
 // up records MAMBA_ERR_TIMEOUT and its role stops, the others give up in
 // turn, and the tensor memory is always released.
@@ -42,6 +50,9 @@ constexpr uint32_t kGemmTmemCols = 2 * kGemmBN;
 struct GemmSmem {
   __nv_bfloat16 a[kGemmStages][kGemmBM * kGemmBK];  // 16 KB per stage
   __nv_bfloat16 b[kGemmStages][kGemmBN * kGemmBK];  // 32 KB per stage
+  // per epilogue warp, two staging buffers of 32 rows x 32 columns (64-byte
+  // rows, 64-byte swizzle) for the TMA stores of C
+  __nv_bfloat16 cst[4][2][32 * 32];
   uint64_t full[kGemmStages];
   uint64_t empty[kGemmStages];
   uint64_t acc_full[2];
@@ -65,8 +76,9 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and
 // B bf16 (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N / 8 at
 // bits 17-22, M / 16 at bits 24-28.
-constexpr uint32_t kGemmIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kGemmBN >> 3) << 17) |
-                                ((uint32_t)(kGemmBM >> 4) << 24);
+__device__ __forceinline__ uint32_t gemm_idesc(int bn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(kGemmBM >> 4) << 24);
+}
 
 __device__ __forceinline__ uint32_t smem_pad1024(const void* base) {
   return (1024u - (smem_u32(base) & 1023u)) & 1023u;
@@ -79,19 +91,24 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
-                   const __grid_constant__ GemmParams p) {
+                   const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ GemmParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   GemmSmem& sm = *reinterpret_cast<GemmSmem*>(smem_raw + smem_pad1024(smem_raw));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int tiles_n = (p.N + kGemmBN - 1) / kGemmBN;
-  const long tiles = ((p.M + kGemmBM - 1) / kGemmBM) * (long)tiles_n;
+  const int bn = p.bn;  // the N tile: a multiple of 32, at most kGemmBN
+  const int tiles_n = (p.N + bn - 1) / bn;
+  // the CTA pair of a cluster takes the two 128-row halves of 256-row tiles
+  const uint32_t rank = cluster_ctarank();
+  const long tiles = ((p.M + 2 * kGemmBM - 1) / (2 * kGemmBM)) * (long)tiles_n;
+  const long first = cluster_id_x(), step = cluster_count_x();
   const int nk = p.K / kGemmBK;
+  const uint32_t idesc = gemm_idesc(bn);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGemmStages; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
-      mbar_init(smem_u32(&sm.empty[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), 2);  // the MMAs of both CTAs of the pair
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&sm.acc_full[b]), 1);
@@ -100,13 +117,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_mbar_init();
     prefetch_tensormap(&tm_a);
     prefetch_tensormap(&tm_w);
+    prefetch_tensormap(&tm_c);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&sm.tmem_base), kGemmTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before either multicasts
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   bool ok = true;
@@ -114,27 +132,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     if (lane == 0) {  // producer
       uint32_t it = 0;
-      for (long t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        const int m0 = (int)(t / tiles_n) * kGemmBM;
-        const int n0 = (int)(t % tiles_n) * kGemmBN;
+      for (long t = first; t < tiles && ok; t += step) {
+        const int m0 = (int)(t / tiles_n) * 2 * kGemmBM + (int)rank * kGemmBM;
+        const int n0 = (int)(t % tiles_n) * bn;
+        const int half = bn / 2;  // the W rows this CTA loads for both
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = (int)(it % kGemmStages);
           const uint32_t ph = (it / kGemmStages) & 1u;
+          // stage s is free in both CTAs (its empty barrier counts both MMAs)
           if (!mbar_wait_bounded(smem_u32(&sm.empty[s]), ph ^ 1u, p.timeout_ns)) {
             ok = false;
             break;
           }
           const uint32_t bar = smem_u32(&sm.full[s]);
-          mbar_arrive_expect_tx(bar, (kGemmBM + kGemmBN) * kGemmBK * 2);
+          mbar_arrive_expect_tx(bar, (kGemmBM + bn) * kGemmBK * 2);  // own A, both halves of W
           tma_load_2d(smem_u32(&sm.a[s][0]), &tm_a, kb * kGemmBK, m0, bar);
-          tma_load_2d(smem_u32(&sm.b[s][0]), &tm_w, kb * kGemmBK, n0, bar);
+          tma_load_2d_mc(smem_u32(&sm.b[s][(size_t)rank * half * kGemmBK]), &tm_w, kb * kGemmBK, n0 + (int)rank * half,
+                         bar, 0x3);
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
       uint32_t it = 0, i = 0;
-      for (long t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++i) {
+      for (long t = first; t < tiles && ok; t += step, ++i) {
         const uint32_t buf = i & 1u;
         if (!mbar_wait_bounded(smem_u32(&sm.acc_empty[buf]), ((i >> 1) & 1u) ^ 1u, p.timeout_ns)) {
           ok = false;
@@ -153,8 +174,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint64_t bd = smem_desc_k128(smem_u32(&sm.b[s][0]));
 #pragma unroll
           for (int kk = 0; kk < kGemmBK / 16; ++kk)  // 16 elements = 32 bytes further along the row
-            tc_mma_f16(d, ad + 2 * kk, bd + 2 * kk, kGemmIdesc, (kb | kk) != 0);
-          tc_commit(smem_u32(&sm.empty[s]));
+            tc_mma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+          tc_commit_mc(smem_u32(&sm.empty[s]), 0x3);  // frees stage s in both CTAs
         }
         if (!ok) break;
         tc_commit(smem_u32(&sm.acc_full[buf]));
@@ -162,8 +183,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {  // epilogue, warps 2..5: warp w reads TMEM lanes 32 (w % 4) .. + 31
     const int q = warp & 3;
-    uint32_t i = 0;
-    for (long t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+    const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(p.bias);
+    uint32_t i = 0, sb = 0;
+    for (long t = first; t < tiles; t += step, ++i) {
       const uint32_t buf = i & 1u;
       const bool mine = mbar_wait_bounded(smem_u32(&sm.acc_full[buf]), (i >> 1) & 1u, p.timeout_ns);
       if (!__all_sync(0xffffffffu, mine)) {
@@ -171,42 +193,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after();
-      const long row = (t / tiles_n) * kGemmBM + 32 * q + lane;
-      const int n0 = (int)(t % tiles_n) * kGemmBN;
-      __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(p.C) + row * (long)p.ldc;
-      const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(p.bias);
+      const int m0 = (int)(t / tiles_n) * 2 * kGemmBM + (int)rank * kGemmBM;
+      const int n0 = (int)(t % tiles_n) * bn;
+      const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + buf * kGemmBN;
+      const int chunks = min(bn, p.N - n0 + 31) / 32;  // 32-column chunks holding valid columns
 #pragma unroll 1
-      for (int c = 0; c < kGemmBN / 32; ++c) {
-        const int col0 = n0 + 32 * c;
-        if (col0 >= p.N) break;  // warp-uniform
+      for (int c = 0; c < chunks; ++c) {
         uint32_t r[32];
-        tmem_ld_32cols(tmem + ((uint32_t)(32 * q) << 16) + buf * kGemmBN + 32 * c, r);
-        float v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-        if (bias) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (col0 + j < p.N) v[j] = __fadd_rn(v[j], __bfloat162float(bias[col0 + j]));
+        tmem_ld_32cols(tbase + 32 * c, r);
+        if (c == chunks - 1) {  // the accumulator is in registers: hand it back to the MMAs
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[buf]));
         }
-        if (row < p.M) {
-          if (col0 + 32 <= p.N) {
+        const int col0 = n0 + 32 * c;
+        uint32_t pk[16];
 #pragma unroll
-            for (int g = 0; g < 4; ++g)
-              reinterpret_cast<uint4*>(crow + col0)[g] =
-                  make_uint4(pack2_bf16(v[8 * g], v[8 * g + 1]), pack2_bf16(v[8 * g + 2], v[8 * g + 3]),
-                             pack2_bf16(v[8 * g + 4], v[8 * g + 5]), pack2_bf16(v[8 * g + 6], v[8 * g + 7]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j < p.N) crow[col0 + j] = __float2bfloat16_rn(v[j]);
+        for (int g = 0; g < 16; ++g) {
+          float lo = __uint_as_float(r[2 * g]), hi = __uint_as_float(r[2 * g + 1]);
+          if (bias) {
+            if (col0 + 2 * g < p.N) lo = __fadd_rn(lo, __bfloat162float(bias[col0 + 2 * g]));
+            if (col0 + 2 * g + 1 < p.N) hi = __fadd_rn(hi, __bfloat162float(bias[col0 + 2 * g + 1]));
           }
+          pk[g] = pack2_bf16(lo, hi);
         }
+        // this lane's row of the chunk into the staging buffer (64-byte
+        // swizzle: the 16-byte piece j of row r sits at piece j ^ ((r / 2) % 4)),
+        // then one TMA store of the 32 x 32 chunk (clipped at the matrix edge)
+        const uint32_t st = smem_u32(&sm.cst[q][sb][0]);
+        if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done reading
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          st_shared_v4(st + lane * 64 + 16 * (j ^ ((lane >> 1) & 3)), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
+                       pk[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tm_c, col0, m0 + 32 * q, st);
+          bulk_commit();
+        }
+        sb ^= 1u;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[buf]));
     }
+    if (lane == 0) bulk_wait_all();  // every store has left shared memory before the CTA ends
   }
 
   if (!ok) report_error(4u);  // MAMBA_ERR_TIMEOUT
@@ -217,6 +247,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kGemmTmemCols);
   }
+  cluster_sync();  // the peer's last arrivals on this CTA's barriers have landed
 }
 
 }  // namespace mamba

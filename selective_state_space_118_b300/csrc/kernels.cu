@@ -76,16 +76,29 @@ cudaError_t launch_summary(IoType io, const CUtensorMap maps[3], const ScanParam
 }
 
 // ---------------------------------------------------------------- tensor-core GEMM
-cudaError_t launch_gemm_tc(const CUtensorMap& a, const CUtensorMap& w, const GemmParams& p, cudaStream_t s) {
+cudaError_t launch_gemm_tc(const CUtensorMap& a, const CUtensorMap& w, const CUtensorMap& c, const GemmParams& p,
+                           cudaStream_t s) {
   const size_t smem = sizeof(GemmSmem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long tiles = ((p.M + kGemmBM - 1) / kGemmBM) * (long)((p.N + kGemmBN - 1) / kGemmBN);
-  const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
-  gemm_tc_kernel<<<grid, kGemmThreads, smem, s>>>(a, w, p);
-  return cudaGetLastError();
+  // clusters of two CTAs, one 256-row tile each at a time
+  const long tiles = ((p.M + 2 * kGemmBM - 1) / (2 * kGemmBM)) * (long)((p.N + p.bn - 1) / p.bn);
+  const long clusters = tiles < sms / 2 ? tiles : sms / 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * clusters));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, a, w, c, p);
 }
 
 // ---------------------------------------------------------------- complex scan

@@ -55,8 +55,10 @@ cudaError_t launch_io_to_f32(IoType io, const void* src, float* dst, long n, cud
 void scan_occupancy(IoType io, int* main_per_sm, int* summary_per_sm);
 
 // C = A W^T [+ bias] on the tensor cores (gemm_tc.cuh).  a: A (K x M, box
-// 64 x 128), w: W (K x N, box 64 x 256), both bf16 with the 128-byte swizzle.
-cudaError_t launch_gemm_tc(const CUtensorMap& a, const CUtensorMap& w, const GemmParams& p, cudaStream_t s);
+// 64 x 128), w: W (K x N, box 64 x bn/2), both bf16 with the 128-byte swizzle;
+// c: C (N x M, box 32 x 32, 64-byte swizzle) for the stores.
+cudaError_t launch_gemm_tc(const CUtensorMap& a, const CUtensorMap& w, const CUtensorMap& c, const GemmParams& p,
+                           cudaStream_t s);
 
 // Reads and clears the sticky device error word of the current device
 // (synchronises the stream first).

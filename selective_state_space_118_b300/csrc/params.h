@@ -125,6 +125,7 @@ struct ComplexParams {
 struct GemmParams {
   long M;
   int N, K;
+  int bn;              // columns of an output tile (a multiple of 32, at most 256)
   int ldc;
   void* C;             // bf16
   const void* bias;    // (N) bf16 or null
