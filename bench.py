@@ -634,6 +634,7 @@ def bench_layer(w, steps, warmup, local, n_chunks_req=0, d_model=4096, dt_rank=2
     t = ev[0].elapsed_time(ev[steps]) / 1e3 / steps
     flops = 2 * B * L * (H * 2 * D + D * (R + 32) + R * D + D * H)
     burst, sustained, src = bf16_peaks()
+    gemms = compare_gemms(ops, B * L, H, D, R, dev, stream, max(3, steps))
     n_chunks = ops.mamba_scan_plan(B, L, D, n_chunks_req)["n_chunks"]
     res = {"metric": "layer tokens/s", "value": B * L / t, "unit": "tokens/s",
            "config": {"workload": f"mamba_layer_bf16_b{B}_l{L}_h{H}_d{D}_r{R}", "batch": B, "seqlen": L,
@@ -644,10 +645,47 @@ def bench_layer(w, steps, warmup, local, n_chunks_req=0, d_model=4096, dt_rank=2
                         "frac": flops / t / 1e12 / sustained, "peak_source": f"{src} (sustained: a long step)",
                         "flops_per_call": flops,
                         "note": "projection FLOPs over the whole layer call (the scan and conv included in "
-                                "the time); the GEMMs are cuBLASLt"},
-           "gpu_launches": (2 if n_chunks == 1 else 3) + 1, "library_gemms_per_call": 5, "clocks": clk.summary()}
+                                "the time); the GEMMs are the library's tcgen05 GEMM"},
+           "gemms": gemms,
+           "gpu_launches": ((2 if n_chunks == 1 else 3) + 1 + 5) * steps, "clocks": clk.summary()}
     del p, ws, out
     return res
+
+
+def compare_gemms(ops, M, H, D, R, dev, stream, reps):
+    """The layer's five projection shapes timed alone through the library's
+    tcgen05 GEMM (mamba_linear_fwd) and through cuBLAS (torch's linear, for
+    comparison only), ms per GEMM and TFLOP/s, on seeded operands."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    bf = torch.bfloat16
+    out = {}
+    # (name, M, N, K, bias)
+    for name, N, K, bias in (("in_proj_x", D, H, False), ("in_proj_z", D, H, False), ("x_proj", R + 32, D, False),
+                             ("dt_proj", D, R, True), ("out_proj", H, D, False)):
+        A = torch.randn((M, K), generator=g, device=dev).to(bf)
+        W = (torch.randn((N, K), generator=g, device=dev) * K ** -0.5).to(bf)
+        b = torch.randn((N,), generator=g, device=dev).to(bf) if bias else None
+        C = torch.empty((M, N), device=dev, dtype=bf)
+        res = {}
+        for impl, fn in (("tcgen05", lambda: ops.mamba_linear_fwd(A, W, b, out=C, stream=stream)),
+                         ("cublas", lambda: torch.nn.functional.linear(A, W, b, out=C))):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(torch.cuda.current_stream(dev))
+            for _ in range(reps):
+                fn()
+            e1.record(torch.cuda.current_stream(dev))
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1) / reps
+            res[impl] = {"ms": ms, "tflops": 2 * M * N * K / ms / 1e9}
+        res["shape"] = [M, N, K]
+        res["tcgen05_vs_cublas_time"] = res["cublas"]["ms"] / res["tcgen05"]["ms"]
+        out[name] = res
+        del A, W, C
+    return out
 
 
 def ssd_algorithmic_bytes(B, L, H, G):

@@ -282,8 +282,8 @@ mamba_status mamba_scan_bwd(const mamba_scan_bwd_args *args, void *stream);
  *   out     = y W_out^T                (out_proj: W_out (d_model, D))
  *
  * Every stored intermediate (x, z, u, the x_proj output, dt_raw, y) and out
- * is bf16; the GEMMs accumulate in fp32 (cuBLASLt, the one part of the
- * library not written here), the scan as for mamba_scan_fwd.  The pages'
+ * is bf16; the GEMMs accumulate in fp32 on the tensor cores (the
+ * tcgen05 GEMM of mamba_linear_fwd), the scan as for mamba_scan_fwd.  The pages'
  * x_proj yields no C; here it yields dt input, B and C, as in the layer the
  * pages describe in prose.
  *
@@ -297,14 +297,10 @@ mamba_status mamba_scan_bwd(const mamba_scan_bwd_args *args, void *stream);
  *                     (e.g. to keep for the backward of x_proj)
  *   final_h, final_conv_state   as for the scan (may be NULL)
  *   workspace         at least mamba_layer_workspace_size() bytes, 256-byte
- *                     aligned: the intermediates, the scan's workspace and
- *                     32 MiB of GEMM scratch
+ *                     aligned: the intermediates and the scan's workspace
  *   n_chunks          the scan's, as for mamba_scan_fwd
  *
- * d_model and dt_rank must be multiples of 8, d_inner of 16.  The first call
- * creates one cuBLASLt handle for the process (kept until exit); GEMM
- * algorithms are chosen once per shape.  MAMBA_ERR_CUDA if cuBLASLt refuses
- * a GEMM.
+ * d_model and dt_rank must be multiples of 8, d_inner of 16.
  */
 typedef struct mamba_layer_args {
     int batch, seqlen, d_model, d_inner, dt_rank, d_state, d_conv;

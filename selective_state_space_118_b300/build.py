@@ -10,15 +10,15 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmamba_ssm.so")
-SOURCES = ["kernels.cu", "api.cpp", "noalloc.cu", "gemm.cpp"]
-HEADERS = ["ptx.cuh", "ssm_math.cuh", "scan_fwd.cuh", "scan_bwd.cuh", "scan_complex.cuh", "step.cuh", "params.h", "launch.h", "gemm.h", "ssd.cuh"]
+SOURCES = ["kernels.cu", "api.cpp", "noalloc.cu"]
+HEADERS = ["ptx.cuh", "ssm_math.cuh", "scan_fwd.cuh", "scan_bwd.cuh", "scan_complex.cuh", "step.cuh", "params.h", "launch.h", "gemm_tc.cuh", "ssd.cuh"]
 PUBLIC_HEADER = os.path.join(os.path.dirname(HERE), "include", "mamba_ssm.h")
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-cudart", "shared",
          "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
-LIBS = ["-lcublasLt"]
+LIBS = []
 
 
 def _stale() -> bool:

@@ -9,7 +9,6 @@
 #include <mutex>
 
 #include "../../include/mamba_ssm.h"
-#include "gemm.h"
 #include "launch.h"
 
 using mamba::IoType;
@@ -230,9 +229,9 @@ BwdWorkspace bwd_workspace_layout(int batch, int seqlen, int d_inner, const Plan
 
 // The layer's workspace: x, z, u (unless the caller takes u), the x_proj
 // output (B, L, dt_rank + 32), dt_raw and y, then the scan's workspace, then
-// cuBLASLt's scratch.
+// nothing else (the GEMMs need no scratch).
 struct LayerWorkspace {
-  size_t x, z, u, xdbl, dt_raw, y, scan, gemm, total;
+  size_t x, z, u, xdbl, dt_raw, y, scan, total;
   Workspace scan_ws;
 };
 
@@ -260,8 +259,6 @@ LayerWorkspace layer_workspace_layout(int batch, int seqlen, int d_inner, int dt
   w.scan = o;
   w.scan_ws = workspace_layout(batch, seqlen, d_inner, pl);
   o += w.scan_ws.total;
-  w.gemm = o;
-  o += mamba::kGemmWorkspace;
   w.total = o;
   return w;
 }
@@ -300,6 +297,31 @@ bool encode2d_bf16(CUtensorMap* m, const void* base, int inner, long rows, long 
 
 bool encode2d_sw128(CUtensorMap* m, const void* base, int inner, long rows, long ld, int box_rows) {
   return encode2d_bf16(m, base, inner, rows, ld, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// C = A W^T [+ bias] on the tensor cores (checked arguments: K, lda, ldc
+// multiples of 8, 16-byte aligned pointers, M > 0).  The N extent is cut
+// evenly into tiles of at most 256 columns, each a multiple of 32; a CTA pair
+// loads half of a W tile each (the W box is bn / 2 rows).
+mamba_status tc_linear(const void* A, long lda, const void* W, const void* bias, void* C, long ldc, long M, int N,
+                       int K, uint64_t timeout_ns, cudaStream_t stream) {
+  const int tiles_n = (N + 255) / 256;
+  const int bn = ((N + tiles_n - 1) / tiles_n + 31) / 32 * 32;
+  CUtensorMap ma, mw, mc;
+  if (!encode2d_sw128(&ma, A, K, M, lda, 128) || !encode2d_sw128(&mw, W, K, N, K, bn / 2) ||
+      !encode2d_bf16(&mc, C, N, M, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return MAMBA_ERR_CUDA;
+  mamba::GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.bn = bn;
+  p.ldc = (int)ldc;
+  p.C = C;
+  p.bias = bias;
+  p.timeout_ns = timeout_ns;
+  return mamba::launch_gemm_tc(ma, mw, mc, p, stream) == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
 
 mamba_status check_common(int batch, int d_inner, int d_state, int d_conv, mamba_dtype io) {
@@ -687,21 +709,20 @@ mamba_status mamba_layer_fwd(const mamba_layer_args* a, void* stream_v) {
   char* xdbl = wsp + ws.xdbl;
   void* dt_raw = wsp + ws.dt_raw;
   void* y = wsp + ws.y;
-  void* gws = wsp + ws.gemm;
+  const uint64_t timeout = kDefaultTimeoutNs;
   const char* W_in = static_cast<const char*>(a->W_in);
 
   // in_proj (two halves: x and z, each contiguous), conv + SiLU, x_proj
   // (dt input | B | C per token), dt_proj with its bias
-  if (!mamba::gemm_bf16(a->hidden, H, W_in, nullptr, x, D, M, D, H, gws, mamba::kGemmWorkspace, stream) ||
-      !mamba::gemm_bf16(a->hidden, H, W_in + (size_t)D * H * 2, nullptr, z, D, M, D, H, gws, mamba::kGemmWorkspace,
-                        stream))
-    return MAMBA_ERR_CUDA;
+  if ((st = tc_linear(a->hidden, H, W_in, nullptr, x, D, M, D, H, timeout, stream)) != MAMBA_OK ||
+      (st = tc_linear(a->hidden, H, W_in + (size_t)D * H * 2, nullptr, z, D, M, D, H, timeout, stream)) != MAMBA_OK)
+    return st;
   if (mamba::launch_conv_silu(IoType::BF16, x, a->conv_w, a->conv_b, u, a->batch, a->seqlen, D, stream) !=
       cudaSuccess)
     return MAMBA_ERR_CUDA;
-  if (!mamba::gemm_bf16(u, D, a->W_x, nullptr, xdbl, XD, M, XD, D, gws, mamba::kGemmWorkspace, stream) ||
-      !mamba::gemm_bf16(xdbl, XD, a->W_dt, a->b_dt, dt_raw, D, M, D, R, gws, mamba::kGemmWorkspace, stream))
-    return MAMBA_ERR_CUDA;
+  if ((st = tc_linear(u, D, a->W_x, nullptr, xdbl, XD, M, XD, D, timeout, stream)) != MAMBA_OK ||
+      (st = tc_linear(xdbl, XD, a->W_dt, a->b_dt, dt_raw, D, M, D, R, timeout, stream)) != MAMBA_OK)
+    return st;
 
   // the scan, B and C read in place from the x_proj output
   mamba_scan_args sa;
@@ -730,8 +751,7 @@ mamba_status mamba_layer_fwd(const mamba_layer_args* a, void* stream_v) {
   if (st != MAMBA_OK) return st;
 
   // out_proj
-  if (!mamba::gemm_bf16(y, D, a->W_out, nullptr, a->out, H, M, H, D, gws, mamba::kGemmWorkspace, stream))
-    return MAMBA_ERR_CUDA;
+  if ((st = tc_linear(y, D, a->W_out, nullptr, a->out, H, M, H, D, timeout, stream)) != MAMBA_OK) return st;
   return MAMBA_OK;
 }
 
@@ -923,28 +943,9 @@ mamba_status mamba_linear_fwd(const mamba_linear_args* a, void* stream_v) {
   const void* al[] = {a->A, a->W, a->C, a->bias};
   for (const void* p : al)
     if (p && !aligned16(p)) return MAMBA_ERR_INVALID_ARG;
-  if (a->K % 64 || a->lda % 8 || a->ldc % 8) return MAMBA_ERR_UNSUPPORTED;
-  // the N extent cut evenly into tiles of at most 256 columns, each a
-  // multiple of 32 (the W box is as many rows)
-  const int tiles_n = (a->N + 255) / 256;
-  const int bn = ((a->N + tiles_n - 1) / tiles_n + 31) / 32 * 32;
-  CUtensorMap ma, mw, mc;
-  if (!encode2d_sw128(&ma, a->A, a->K, a->M, a->lda, 128) || !encode2d_sw128(&mw, a->W, a->K, a->N, a->K, bn / 2) ||
-      !encode2d_bf16(&mc, a->C, a->N, a->M, a->ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
-    return MAMBA_ERR_CUDA;
-  mamba::GemmParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.M = a->M;
-  p.N = a->N;
-  p.K = a->K;
-  p.bn = bn;
-  p.ldc = a->ldc;
-  p.C = a->C;
-  p.bias = a->bias;
-  p.timeout_ns = a->wait_timeout_ns ? a->wait_timeout_ns : kDefaultTimeoutNs;
-  if (mamba::launch_gemm_tc(ma, mw, mc, p, reinterpret_cast<cudaStream_t>(stream_v)) != cudaSuccess)
-    return MAMBA_ERR_CUDA;
-  return MAMBA_OK;
+  if (a->K % 8 || a->lda % 8 || a->ldc % 8) return MAMBA_ERR_UNSUPPORTED;
+  return tc_linear(a->A, a->lda, a->W, a->bias, a->C, a->ldc, a->M, a->N, a->K,
+                   a->wait_timeout_ns ? a->wait_timeout_ns : kDefaultTimeoutNs, reinterpret_cast<cudaStream_t>(stream_v));
 }
 
 mamba_status mamba_last_error(void* stream_v) {

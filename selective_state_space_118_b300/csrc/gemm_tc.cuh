@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t rank = cluster_ctarank();
   const long tiles = ((p.M + 2 * kGemmBM - 1) / (2 * kGemmBM)) * (long)tiles_n;
   const long first = cluster_id_x(), step = cluster_count_x();
-  const int nk = p.K / kGemmBK;
+  const int nk = (p.K + kGemmBK - 1) / kGemmBK;  // the loads fill zeros past K
   const uint32_t idesc = gemm_idesc(bn);
 
   if (threadIdx.x == 0) {
@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {  // producer
+      const uint64_t keep = l2_policy_evict_last();  // W: read by every row block
       uint32_t it = 0;
       for (long t = first; t < tiles && ok; t += step) {
         const int m0 = (int)(t / tiles_n) * 2 * kGemmBM + (int)rank * kGemmBM;
@@ -146,9 +147,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           const uint32_t bar = smem_u32(&sm.full[s]);
           mbar_arrive_expect_tx(bar, (kGemmBM + bn) * kGemmBK * 2);  // own A, both halves of W
-          tma_load_2d(smem_u32(&sm.a[s][0]), &tm_a, kb * kGemmBK, m0, bar);
+          tma_load_2d(smem_u32(&sm.a[s][0]), &tm_a, kb * kGemmBK, m0, bar);  // A: reused by the row block's tiles
           tma_load_2d_mc(smem_u32(&sm.b[s][(size_t)rank * half * kGemmBK]), &tm_w, kb * kGemmBK, n0 + (int)rank * half,
-                         bar, 0x3);
+                         bar, 0x3, keep);
         }
       }
     }
@@ -184,6 +185,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {  // epilogue, warps 2..5: warp w reads TMEM lanes 32 (w % 4) .. + 31
     const int q = warp & 3;
     const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(p.bias);
+    const uint64_t out_policy = l2_policy_evict_first();  // C: written once
     uint32_t i = 0, sb = 0;
     for (long t = first; t < tiles; t += step, ++i) {
       const uint32_t buf = i & 1u;
@@ -207,13 +209,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[buf]));
         }
         const int col0 = n0 + 32 * c;
+        // the chunk's 32 bias values (the same for every lane: broadcast
+        // loads), four 16-byte vectors where the chunk lies inside N
+        uint32_t bw[16];
+#pragma unroll
+        for (int g = 0; g < 16; ++g) bw[g] = 0u;
+        if (bias) {
+          if (col0 + 32 <= p.N) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint4 b4 = __ldg(reinterpret_cast<const uint4*>(bias + col0) + v);
+              bw[4 * v] = b4.x;
+              bw[4 * v + 1] = b4.y;
+              bw[4 * v + 2] = b4.z;
+              bw[4 * v + 3] = b4.w;
+            }
+          } else {
+#pragma unroll
+            for (int g = 0; g < 16; ++g) {
+              const uint32_t lo = col0 + 2 * g < p.N ? __bfloat16_as_ushort(bias[col0 + 2 * g]) : 0u;
+              const uint32_t hi = col0 + 2 * g + 1 < p.N ? __bfloat16_as_ushort(bias[col0 + 2 * g + 1]) : 0u;
+              bw[g] = lo | (hi << 16);
+            }
+          }
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int g = 0; g < 16; ++g) {
           float lo = __uint_as_float(r[2 * g]), hi = __uint_as_float(r[2 * g + 1]);
           if (bias) {
-            if (col0 + 2 * g < p.N) lo = __fadd_rn(lo, __bfloat162float(bias[col0 + 2 * g]));
-            if (col0 + 2 * g + 1 < p.N) hi = __fadd_rn(hi, __bfloat162float(bias[col0 + 2 * g + 1]));
+            lo = __fadd_rn(lo, __uint_as_float(bw[g] << 16));
+            hi = __fadd_rn(hi, __uint_as_float(bw[g] & 0xffff0000u));
           }
           pk[g] = pack2_bf16(lo, hi);
         }
@@ -230,7 +256,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tm_c, col0, m0 + 32 * q, st);
+          tma_store_2d(&tm_c, col0, m0 + 32 * q, st, out_policy);
           bulk_commit();
         }
         sb ^= 1u;

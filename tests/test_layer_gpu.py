@@ -1,4 +1,4 @@
-"""The whole layer (mamba_layer_fwd: cuBLASLt projections around the scan)
+"""The whole layer (mamba_layer_fwd: tensor-core projections around the scan)
 on the GPU against the fp64 layer oracle, which rounds every stored
 intermediate to bf16 where the library stores it.
 

@@ -52,6 +52,8 @@ SHAPES = [
     (1000, 1000, 256, True, None, None),   # a column tail not a multiple of 32
     (517, 256, 320, False, 384, 264),      # strided A and C (views of wider matrices)
     (4096, 4096, 1024, True, None, None),  # many tiles per CTA: both accumulators, the stage ring wraps
+    (700, 512, 96, True, None, None),      # K not a multiple of 64: the last K block is zero-filled
+    (257, 320, 32, False, 288, None),      # K = 32 read from a wider row (dt_proj's input layout)
 ]
 
 
@@ -82,7 +84,7 @@ def test_linear_empty_and_refusals():
     A, W, b, _ = case(0, 256, 64, seed=1)
     C = ops.mamba_linear_fwd(A, W, b)
     assert C.shape == (0, 256)
-    A, W, b, _ = case(64, 256, 96, seed=2)
+    A, W, b, _ = case(64, 256, 36, seed=2)
     with pytest.raises(ops.MambaError) as e:
         ops.mamba_linear_fwd(A, W, b)
     assert e.value.status == ops.MAMBA_ERR_UNSUPPORTED
