@@ -755,11 +755,27 @@ mamba_status mamba_layer_fwd(const mamba_layer_args* a, void* stream_v) {
   return MAMBA_OK;
 }
 
+constexpr int kSsdChunk = 128;  // tokens per chunk of Mamba-2's scan
+
 size_t mamba2_scan_workspace_size(int batch, int seqlen, int heads) {
   if (batch <= 0 || seqlen <= 0 || heads <= 0) return 0;
-  const size_t nC = ((size_t)seqlen + 63) / 64, BH = (size_t)batch * heads;
+  const size_t nC = ((size_t)seqlen + kSsdChunk - 1) / kSsdChunk, BH = (size_t)batch * heads;
   return 2 * round256(BH * nC * 16 * 64 * sizeof(float)) + round256(BH * nC * sizeof(float)) +
-         round256(BH * nC * 64 * 2 * sizeof(float));
+         round256(BH * nC * kSsdChunk * 2 * sizeof(float));
+}
+
+// 4-D map over a bf16 tensor (B, L, R, inner), rows of `inner` elements, read
+// or written in boxes of inner x 1 x 128 tokens x 1 with the given swizzle.
+bool encode4d_tokens(CUtensorMap* m, const void* base, int inner, int R, int L, int B, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)R, (cuuint64_t)L, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * 2 * R, (cuuint64_t)inner * 2 * R * L};
+  cuuint32_t box[4] = {(cuuint32_t)inner, 1, (cuuint32_t)kSsdChunk, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 mamba_status mamba2_scan_fwd(const mamba2_scan_args* a, void* stream_v) {
@@ -788,7 +804,7 @@ mamba_status mamba2_scan_fwd(const mamba2_scan_args* a, void* stream_v) {
   const size_t need = mamba2_scan_workspace_size(a->batch, a->seqlen, a->heads);
   if (!a->workspace || a->workspace_bytes < need) return MAMBA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return MAMBA_ERR_INVALID_ARG;
-  const int nC = (a->seqlen + 63) / 64;
+  const int nC = (a->seqlen + kSsdChunk - 1) / kSsdChunk;
   char* w = static_cast<char*>(a->workspace);
   const size_t st = round256(BH * nC * 16 * 64 * sizeof(float));
   mamba::SsdParams p;
@@ -812,7 +828,16 @@ mamba_status mamba2_scan_fwd(const mamba2_scan_args* a, void* stream_v) {
   p.S_in = reinterpret_cast<float*>(w + st);
   p.totals = reinterpret_cast<float*>(w + 2 * st);
   p.cum = reinterpret_cast<float*>(w + 2 * st + round256(BH * nC * sizeof(float)));
-  if (mamba::launch_ssd(p, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+  p.timeout_ns = kDefaultTimeoutNs;
+  CUtensorMap maps[5];  // x, z, B, C, y
+  const int H = a->heads, G = a->groups, L = a->seqlen, Bt = a->batch;
+  if (!encode4d_tokens(&maps[0], a->x, 64, H, L, Bt, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode4d_tokens(&maps[1], a->z ? a->z : a->x, 64, H, L, Bt, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode4d_tokens(&maps[2], a->Bm, 16, G, L, Bt, CU_TENSOR_MAP_SWIZZLE_32B) ||
+      !encode4d_tokens(&maps[3], a->Cm, 16, G, L, Bt, CU_TENSOR_MAP_SWIZZLE_32B) ||
+      !encode4d_tokens(&maps[4], a->y, 64, H, L, Bt, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MAMBA_ERR_CUDA;
+  if (mamba::launch_ssd(maps, p, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
   return MAMBA_OK;
 }
 

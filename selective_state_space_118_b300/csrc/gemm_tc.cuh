@@ -63,22 +63,12 @@ struct GemmSmem {
 // Shared-memory matrix descriptor of a K-major tile written by TMA with the
 // 128-byte swizzle: rows of 128 bytes, 8-row swizzle atoms 1024 bytes apart
 // (the stride byte offset); the leading byte offset is unused in this mode.
-__device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);  // start address, 16-byte units
-  d |= (uint64_t)1 << 16;                   // leading byte offset (unused)
-  d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset
-  d |= (uint64_t)1 << 46;                   // descriptor version
-  d |= (uint64_t)2 << 61;                   // 128-byte swizzle
-  return d;
-}
+__device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) { return umma_desc(saddr, 1024, 2); }
 
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and
 // B bf16 (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N / 8 at
 // bits 17-22, M / 16 at bits 24-28.
-__device__ __forceinline__ uint32_t gemm_idesc(int bn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(kGemmBM >> 4) << 24);
-}
+__device__ __forceinline__ uint32_t gemm_idesc(int bn) { return umma_idesc_bf16(kGemmBM, bn, false); }
 
 __device__ __forceinline__ uint32_t smem_pad1024(const void* base) {
   return (1024u - (smem_u32(base) & 1023u)) & 1023u;

@@ -314,7 +314,7 @@ cudaError_t launch_conv_silu(IoType io, const void* x, const float* conv_w, cons
   return cudaGetLastError();
 }
 
-cudaError_t launch_ssd(const SsdParams& p, cudaStream_t stream) {
+cudaError_t launch_ssd(const CUtensorMap maps[5], const SsdParams& p, cudaStream_t stream) {
   const dim3 grid((unsigned)p.heads, (unsigned)p.n_chunks, (unsigned)p.batch);
   ssd_states_kernel<<<grid, kSsdThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
@@ -322,7 +322,10 @@ cudaError_t launch_ssd(const SsdParams& p, cudaStream_t stream) {
   ssd_pass_kernel<<<dim3(32u / kPassSlices, (unsigned)p.heads, (unsigned)p.batch), 32 * kPassSlices, 0, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  ssd_output_kernel<<<grid, kSsdThreads, 0, stream>>>(p);
+  const size_t smem = sizeof(SsdTcSmem) + 1024;
+  e = cudaFuncSetAttribute(ssd_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  ssd_output_kernel<<<grid, kSsdOutThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
   return cudaGetLastError();
 }
 

@@ -45,8 +45,9 @@ cudaError_t launch_carries(IoType io, const CUtensorMap maps[5], const ScanParam
                            unsigned n_fwd, unsigned n_adj, cudaStream_t stream);
 cudaError_t launch_bwd_finish(IoType io, const BwdParams& p, float* dB, float* dC, float* dA_log, float* dD,
                               float* dconv_w, float* dconv_b, cudaStream_t stream);
-// Mamba-2's chunked scan: chunk end states, state passing, output.
-cudaError_t launch_ssd(const SsdParams& p, cudaStream_t stream);
+// Mamba-2's chunked scan: chunk end states, state passing, output.  maps
+// (4-D, for the output kernel): x, z, B, C, y.
+cudaError_t launch_ssd(const CUtensorMap maps[5], const SsdParams& p, cudaStream_t stream);
 cudaError_t launch_io_to_f32(IoType io, const void* src, float* dst, long n, cudaStream_t stream);
 
 // Resident CTAs per SM of the main and summary kernels (0 when no device

@@ -70,7 +70,7 @@ struct BwdParams {
 };
 
 // Mamba-2's chunked scan (ssd.cuh): heads of 64 channels sharing one scalar
-// decay per token, 16 x 64 state per head, chunks of 64 tokens.
+// decay per token, 16 x 64 state per head, chunks of 128 tokens.
 struct SsdParams {
   int batch, seqlen, heads, groups, n_chunks;
   const void* x;          // (B, L, H, 64) bf16
@@ -90,7 +90,8 @@ struct SsdParams {
   float* S_c;             // each chunk's end state from zero
   float* S_in;            // the state entering each chunk
   float* totals;          // (B, H, n_chunks): sum of dt * A (base 2) over each chunk
-  float* cum;             // (B, H, n_chunks, 64, 2): per token, the prefix sum of dt * A and dt
+  float* cum;             // (B, H, n_chunks, 128, 2): per token, the prefix sum of dt * A and dt
+  uint64_t timeout_ns;
 };
 
 // The complex-valued scan (scan_complex.cuh): 8 complex modes per channel,

@@ -5,17 +5,19 @@
 // state matrix is a scaled identity, discretised with Euler's method.  Heads of
 // P = 64 channels share dt and A, so the decay from token s to token t,
 // exp(A (cum_t - cum_s)), is one number per (t, s) for the whole head, and
-// within a chunk of Q = 64 tokens the scan is a pair of small matrix products:
+// within a chunk of Q = 128 tokens the scan is a few small matrix products:
 //   Y_diag = (mask(t >= s) * exp(A (cum_t - cum_s)) * dt_s * (C B^T)) X
 //   Y_off  = exp(A cum_t) (C S_in)          (S_in: the state entering the chunk)
 //   S_end  = (exp(A (cum_last - cum_s)) dt_s B_s)^T X + exp(A cum_last) S_in
-// Three kernels: ssd_states_kernel (each chunk's end state from zero),
-// ssd_pass_kernel (the states entering the chunks, serially per head, in
-// fp32), ssd_output_kernel (Y_diag + Y_off + D x, gated).  The products use
-// warp-level mma (m16n8k16, bf16 operands, fp32 accumulation): with d_state 16
-// the path does ~200 tensor FLOPs per element against 6-8 bytes of traffic,
-// HBM-bound, so warp-level mma keeps up and lets the first product's
-// accumulators feed the second as operands without leaving registers.
+// Three kernels: ssd_states_kernel (each chunk's end state from zero, a
+// 16 x 64 product: warp-level mma m16n8k16, 16 rows being below the
+// 5th-generation MMA's smallest M), ssd_pass_kernel (the states entering the
+// chunks, serially per head, in fp32) and ssd_output_kernel (Y_diag + Y_off +
+// D x, gated) on tcgen05: its three products are 128-row MMAs with the
+// accumulators in tensor memory and the tiles brought in by TMA.  fp32
+// quantities entering a product (the decay-weighted B rows and C B^T
+// entries, the entering state) go in as two bf16 terms (hi + lo, ~16
+// significant bits).
 #pragma once
 #include <cuda_bf16.h>
 
@@ -23,14 +25,15 @@
 
 #include "params.h"
 #include "ptx.cuh"
+#include "scan_fwd.cuh"
 #include "ssm_math.cuh"
 
 namespace mamba {
 
-constexpr int kSsdQ = 64;          // tokens per chunk
+constexpr int kSsdQ = 128;         // tokens per chunk
 constexpr int kSsdP = 64;          // channels per head
 constexpr int kSsdN = 16;          // d_state
-constexpr int kSsdThreads = 128;   // 4 warps: 16 chunk rows each
+constexpr int kSsdThreads = 128;   // 4 warps
 constexpr int kXs = kSsdP + 8;     // padded bf16 row of x / state tiles (144 B: ldmatrix rows conflict-free)
 constexpr int kBs = kSsdN + 8;     // padded bf16 row of B / C tiles (48 B)
 
@@ -141,8 +144,8 @@ __device__ __forceinline__ void ssd_load_tile(const SsdParams& p, SsdTile& s, in
     __syncthreads();
     return;
   }
-  // dt and dt * A, then the inclusive prefix sum over the 64 tokens: two
-  // warps, then warp 1 adds warp 0's total
+  // dt and dt * A, then the inclusive prefix sum over the chunk's tokens:
+  // per warp, then each warp adds the totals of the warps before it
   if (tid < kSsdQ) {
     const float A2 = a2_from_log(p.A_log[h]);  // A log2(e)
     const int t = t0 + tid;
@@ -160,13 +163,18 @@ __device__ __forceinline__ void ssd_load_tile(const SsdParams& p, SsdTile& s, in
   }
   cp_async_wait_all();
   __syncthreads();
-  if (tid >= 32 && tid < kSsdQ) s.acum[tid] = __fadd_rn(s.acum[tid], s.acum[31]);
+  const int w = tid >> 5;
+  float off = 0.0f;  // the earlier warps' totals, read before any is updated
+  if (tid < kSsdQ)
+    for (int k = 0; k < w; ++k) off = __fadd_rn(off, s.acum[32 * k + 31]);
+  __syncthreads();
+  if (tid < kSsdQ && w > 0) s.acum[tid] = __fadd_rn(s.acum[tid], off);
   __syncthreads();
 }
 
 // ---------------------------------------------------------------- chunk end states
 // S_c[n][p] = sum_j 2^(acum_last - acum_j) dt_j B_j[n] x_j[p]: a 16 x 64 product
-// over the 64 tokens; warp w computes columns 16w .. 16w + 15.
+// over the chunk's tokens; warp w computes columns 16w .. 16w + 15.
 // grid (H, n_chunks, B), 128 threads.
 __global__ void __launch_bounds__(kSsdThreads) ssd_states_kernel(const __grid_constant__ SsdParams p) {
   __shared__ __align__(128) SsdTile s;
@@ -266,162 +274,240 @@ __global__ void __launch_bounds__(32 * kPassSlices) ssd_pass_kernel(const __grid
 }
 
 // ---------------------------------------------------------------- output
-// grid (H, n_chunks, B), 128 threads; warp w produces chunk rows 16w .. 16w + 15.
-struct SsdOutSmem {
-  SsdTile t;                       // x is overwritten by y at the end (each thread its own values)
-  __nv_bfloat16 z[kSsdQ][kXs];
-  __nv_bfloat16 s_hi[kSsdN][kXs];  // the entering state split into two bf16 terms
-  __nv_bfloat16 s_lo[kSsdN][kXs];
-  float fdt[kSsdThreads / 32][kSsdQ];  // per warp: 2^(ref - acum_j) dt_j
+// One CTA (8 warps) per (head, chunk, batch row): thread t serves chunk row
+// i = t % 128 (TMEM lane i) and half t / 128 of that row's columns.  Tiles by TMA: x and z (128 tokens x 64 channels, 128-byte
+// swizzle: the K = token dimension's rows of 128 bytes, an MN-major operand),
+// B and C (128 tokens x 16 states, 32-byte swizzle, K-major).  Three MMA
+// groups, issued by one thread, accumulators in tensor memory:
+//   G  = C B^T              128 x 128, K = 16          (TMEM columns 0..127)
+//   Yo = C (S_hi + S_lo)    128 x 64,  K = 16 twice    (columns 128..191)
+//   Y  = (G_hi + G_lo) X    128 x 64,  K = 128 twice   (columns 192..255)
+// Between them each thread reads its row of G, masks it to s <= t, scales it
+// by the decay 2^(acum_i - acum_j) dt_j and writes it, as hi + lo bf16 terms,
+// into shared memory in the K-major 128-byte-swizzled layout of an A
+// operand.  The epilogue: y = Y + 2^(acum_i) Yo + D x, times silu(z), written
+// over the thread's row of the x tile and stored by TMA.
+constexpr int kSsdTmemCols = 256;
+constexpr int kSsdOutThreads = 256;
+
+struct SsdTcSmem {
+  __nv_bfloat16 x[kSsdQ * kSsdP];        // 16 KB, then y
+  __nv_bfloat16 z[kSsdQ * kSsdP];        // 16 KB
+  __nv_bfloat16 ghi[2][kSsdQ * 64];      // G's columns 0..63 and 64..127: rows of 128 bytes
+  __nv_bfloat16 glo[2][kSsdQ * 64];
+  __nv_bfloat16 shi[kSsdN * kSsdP];      // S_in: rows n of 64 channels (128 bytes)
+  __nv_bfloat16 slo[kSsdN * kSsdP];
+  __nv_bfloat16 c[kSsdQ * kSsdN];        // rows of 32 bytes
+  __nv_bfloat16 b[kSsdQ * kSsdN];
+  float acum[kSsdQ];
+  float dt[kSsdQ];
+  float fdt[kSsdQ];                      // 2^(ref - acum_j) dt_j
+  uint64_t bar_tile, bar_mma1, bar_mma2;
+  uint32_t tmem_base;
 };
 
-__global__ void __launch_bounds__(kSsdThreads) ssd_output_kernel(const __grid_constant__ SsdParams p) {
-  __shared__ __align__(128) SsdOutSmem sm;
-  SsdTile& s = sm.t;
-  const int h = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const size_t bh = (size_t)b * p.heads + h;
-  // tiles by asynchronous copies; meanwhile the entering state (32 slices of
-  // 32 values), fp32 -> hi + lo bf16 pairs
-  ssd_load_tile(p, s, b, h, c, true, true, p.z ? sm.z : nullptr, [&] {
-    float4 v[kSsdN * kSsdP / 4 / kSsdThreads];
-#pragma unroll
-    for (int k = 0; k < kSsdN * kSsdP / 4 / kSsdThreads; ++k) {
-      const int e = 4 * (tid + k * kSsdThreads), q = e / 32, n = q / 2, col = 32 * (q % 2) + e % 32;
-      v[k] = __ldcs(reinterpret_cast<const float4*>(p.S_in + ssd_slice(bh, n, col, c, p.n_chunks)));
-    }
-#pragma unroll
-    for (int k = 0; k < kSsdN * kSsdP / 4 / kSsdThreads; ++k) {
-      const int e = 4 * (tid + k * kSsdThreads), q = e / 32, n = q / 2, col = 32 * (q % 2) + e % 32;
-      uint32_t h01, l01, h23, l23;
-      split_bf16(v[k].x, v[k].y, h01, l01);
-      split_bf16(v[k].z, v[k].w, h23, l23);
-      *reinterpret_cast<uint2*>(&sm.s_hi[n][col]) = make_uint2(h01, h23);
-      *reinterpret_cast<uint2*>(&sm.s_lo[n][col]) = make_uint2(l01, l23);
-    }
-  });
+// 16-byte piece `piece` of row `row` in a 128-byte-swizzled tile of 128-byte rows.
+__device__ __forceinline__ uint32_t sw128(uint32_t base, int row, int piece) {
+  return base + row * 128 + ((piece ^ (row & 7)) << 4);
+}
 
-  const int g = lane >> 2, t = lane & 3;
-  const int i0 = warp * 16 + g, i1 = i0 + 8;  // this thread's two rows
-  // C rows of this warp as the A operand (16 rows x 16 states)
-  uint32_t ca[4];
-  {
-    const int r = lane & 7, m = lane >> 3;  // matrix m: rows (m & 1) * 8, states (m >> 1) * 8
-    ldsm_x4(ca, smem_u32(&s.C[warp * 16 + (m & 1) * 8 + r][(m >> 1) * 8]));
+__global__ void __launch_bounds__(kSsdOutThreads, 2)
+    ssd_output_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
+                      const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
+                      const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ SsdParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  SsdTcSmem& sm = *reinterpret_cast<SsdTcSmem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+  const int h = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int H = p.heads, G = p.groups;
+  const int g = h / (H / G);
+  const int t0 = c * kSsdQ;
+  const size_t bh = (size_t)b * H + h;
+  const bool gate = p.z != nullptr;
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&sm.bar_tile), 1);
+    mbar_init(smem_u32(&sm.bar_mma1), 1);
+    mbar_init(smem_u32(&sm.bar_mma2), 1);
+    fence_mbar_init();
   }
-  // G = C B^T over the columns j <= this warp's last row, masked and scaled
-  // by the decay 2^(acum_i - acum_j) dt_j.  Where the warp's 16 rows span a
-  // decay of at most 2^60 (ref: acum at its first row), the factor splits
-  // as 2^(acum_i - ref) * 2^(ref - acum_j): one exponential per row and one
-  // per column (shared through fdt) instead of one per pair; neither factor
-  // overflows, and a product that underflows is one far below fp32's
-  // precision of the sum.  Otherwise each pair takes its own exponential.
-  const float ref = s.acum[warp * 16];
-  const bool split = __fsub_rn(ref, s.acum[warp * 16 + 15]) <= 60.0f;  // the same for the whole warp
-  if (split) {
-    for (int j = lane; j < warp * 16 + 16; j += 32)
-      sm.fdt[warp][j] = __fmul_rn(ex2_approx(__fsub_rn(ref, s.acum[j])), s.dt[j]);
-    __syncwarp();
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&sm.tmem_base), kSsdTmemCols);
+    tmem_relinquish();
   }
-  const float a0 = s.acum[i0], a1 = s.acum[i1];
-  const float r0 = ex2_approx(__fsub_rn(a0, ref)), r1 = ex2_approx(__fsub_rn(a1, ref));
-  float G[8][4];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  if (tid == 0) {
+    const uint32_t bar = smem_u32(&sm.bar_tile);
+    mbar_arrive_expect_tx(bar, (gate ? 2 : 1) * kSsdQ * kSsdP * 2 + 2 * kSsdQ * kSsdN * 2);
+    tma_load_4d(smem_u32(sm.x), &tm_x, 0, h, t0, b, bar);
+    if (gate) tma_load_4d(smem_u32(sm.z), &tm_z, 0, h, t0, b, bar);
+    tma_load_4d(smem_u32(sm.b), &tm_b, 0, g, t0, b, bar);
+    tma_load_4d(smem_u32(sm.c), &tm_c, 0, g, t0, b, bar);
+  }
+  // while the tiles fly: dt and the decay prefix (the states kernel's), and
+  // the entering state as hi + lo bf16 terms in the MN-major layout (row n:
+  // 64 channels, 8 channels per 16-byte piece, 128-byte swizzle)
+  if (tid < kSsdQ) {
+    const float2 v = reinterpret_cast<const float2*>(p.cum)[(bh * p.n_chunks + c) * kSsdQ + tid];
+    sm.acum[tid] = v.x;
+    sm.dt[tid] = v.y;
+    const int n = tid >> 3, piece = tid & 7;  // 16 rows x 8 pieces: one per thread
+    const float* src = p.S_in + ssd_slice(bh, n, piece * 8, c, p.n_chunks);
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(src));
+    const float4 d = __ldcs(reinterpret_cast<const float4*>(src) + 1);
+    uint32_t hi[4], lo[4];
+    split_bf16(a.x, a.y, hi[0], lo[0]);
+    split_bf16(a.z, a.w, hi[1], lo[1]);
+    split_bf16(d.x, d.y, hi[2], lo[2]);
+    split_bf16(d.z, d.w, hi[3], lo[3]);
+    st_shared_v4(sw128(smem_u32(sm.shi), n, piece), hi[0], hi[1], hi[2], hi[3]);
+    st_shared_v4(sw128(smem_u32(sm.slo), n, piece), lo[0], lo[1], lo[2], lo[3]);
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  const float ref = sm.acum[0];
+  const bool split = __fsub_rn(ref, sm.acum[kSsdQ - 1]) <= 60.0f;  // the whole chunk's decay span
+  if (split && tid < kSsdQ) sm.fdt[tid] = __fmul_rn(ex2_approx(__fsub_rn(ref, sm.acum[tid])), sm.dt[tid]);
+
+  bool ok = true;
+  if (tid == 0) {  // G = C B^T and Yo = C S_in
+    ok = mbar_wait_bounded(smem_u32(&sm.bar_tile), 0, p.timeout_ns);
+    if (ok) {
+      tc_fence_after();
+      const uint64_t cd = umma_desc(smem_u32(sm.c), 256, 6);
+      tc_mma_f16(tmem, cd, umma_desc(smem_u32(sm.b), 256, 6), umma_idesc_bf16(128, 128, false), false);
+      const uint32_t io = umma_idesc_bf16(128, 64, true);
+      tc_mma_f16(tmem + 128, cd, umma_desc(smem_u32(sm.shi), 1024, 2), io, false);
+      tc_mma_f16(tmem + 128, cd, umma_desc(smem_u32(sm.slo), 1024, 2), io, true);
+      tc_commit(smem_u32(&sm.bar_mma1));
+    }
+  }
+  ok = __syncthreads_and(ok);
+  if (ok) {
+    ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&sm.bar_mma1), 0, p.timeout_ns));
+    ok = __syncthreads_and(ok);
+  }
+  const int i = tid & (kSsdQ - 1);  // this thread's row
+  const int hf = tid >> 7;           // and half of the row's columns
+  const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
+  if (ok) {
+    tc_fence_after();
+    const float ai = sm.acum[i];
+    const float ri = ex2_approx(__fsub_rn(ai, ref));
+#pragma unroll 1
+    for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {  // 32 columns j of G at a time
+      uint32_t r[32];
+      tmem_ld_32cols(tmem + lanes + 32 * cb, r);
+      uint32_t hi[16], lo[16];
 #pragma unroll
-  for (int jt = 0; jt < 8; ++jt) {
-    G[jt][0] = G[jt][1] = G[jt][2] = G[jt][3] = 0.0f;
-    if (jt <= 2 * warp + 1) {
-      uint32_t bb[2];
-      ldsm_x2(bb, smem_u32(&s.B[jt * 8 + (lane & 7)][(lane >> 3 & 1) * 8]));
-      mma_16816(G[jt], ca, bb[0], bb[1]);
-      const int j0 = jt * 8 + 2 * t;
-      if (split) {
-        const float2 f = *reinterpret_cast<const float2*>(&sm.fdt[warp][j0]);
-        G[jt][0] = j0 <= i0 ? __fmul_rn(__fmul_rn(G[jt][0], r0), f.x) : 0.0f;
-        G[jt][1] = j0 + 1 <= i0 ? __fmul_rn(__fmul_rn(G[jt][1], r0), f.y) : 0.0f;
-        G[jt][2] = j0 <= i1 ? __fmul_rn(__fmul_rn(G[jt][2], r1), f.x) : 0.0f;
-        G[jt][3] = j0 + 1 <= i1 ? __fmul_rn(__fmul_rn(G[jt][3], r1), f.y) : 0.0f;
-      } else {
+      for (int e = 0; e < 16; ++e) {
+        float v2[2];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int j = j0 + e;
-          const float aj = s.acum[j], dtj = s.dt[j];
-          G[jt][e] = j <= i0 ? __fmul_rn(G[jt][e], __fmul_rn(ex2_approx(__fsub_rn(a0, aj)), dtj)) : 0.0f;
-          G[jt][2 + e] = j <= i1 ? __fmul_rn(G[jt][2 + e], __fmul_rn(ex2_approx(__fsub_rn(a1, aj)), dtj)) : 0.0f;
+        for (int u = 0; u < 2; ++u) {
+          const int j = 32 * cb + 2 * e + u;
+          float f;
+          if (split)
+            f = __fmul_rn(ri, sm.fdt[j]);
+          else
+            f = __fmul_rn(ex2_approx(__fsub_rn(ai, sm.acum[j])), sm.dt[j]);
+          v2[u] = j <= i ? __fmul_rn(__uint_as_float(r[2 * e + u]), f) : 0.0f;
+        }
+        split_bf16(v2[0], v2[1], hi[e], lo[e]);
+      }
+      // columns 32cb .. 32cb + 31: K block cb / 2, pieces 4 (cb % 2) .. + 3
+      const int kb = cb >> 1;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int piece = 4 * (cb & 1) + q;
+        st_shared_v4(sw128(smem_u32(sm.ghi[kb]), i, piece), hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+        st_shared_v4(sw128(smem_u32(sm.glo[kb]), i, piece), lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+      }
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0 && ok) {  // Y = G X: the hi terms, then the lo terms, 16 tokens of K per MMA
+    const uint32_t iy = umma_idesc_bf16(128, 64, true);
+    bool acc = false;
+#pragma unroll 1
+    for (int part = 0; part < 2; ++part) {
+      for (int kb = 0; kb < 2; ++kb) {
+        const uint32_t gbase = smem_u32(part == 0 ? sm.ghi[kb] : sm.glo[kb]);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t ad = umma_desc(gbase + 32 * ks, 1024, 2);                         // 16 columns of G
+          const uint64_t bd = umma_desc(smem_u32(sm.x) + (kb * 64 + ks * 16) * 128, 1024, 2);  // 16 rows of x
+          tc_mma_f16(tmem + 192, ad, bd, iy, acc);
+          acc = true;
         }
       }
     }
+    tc_commit(smem_u32(&sm.bar_mma2));
   }
-  // Y = G X (k blocks up to the diagonal) and C S_in (hi and lo parts)
-  float Y[8][4], Yo[8][4];
+  if (ok) {
+    ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&sm.bar_mma2), 0, p.timeout_ns));
+    ok = __syncthreads_and(ok);
+  }
+  if (ok) {
+    tc_fence_after();
+    const float ei = ex2_approx(sm.acum[i]);
+    const float Dh = p.Dskip[h];
+    {
+      const int half = hf;  // channels 32 half .. + 31
+      uint32_t yv[32], yo[32];
+      tmem_ld_32cols(tmem + lanes + 192 + 32 * half, yv);
+      tmem_ld_32cols(tmem + lanes + 128 + 32 * half, yo);
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt) Y[nt][0] = Y[nt][1] = Y[nt][2] = Y[nt][3] = Yo[nt][0] = Yo[nt][1] = Yo[nt][2] =
-      Yo[nt][3] = 0.0f;
+      for (int q = 0; q < 4; ++q) {
+        const int piece = 4 * half + q;
+        const uint32_t xa = sw128(smem_u32(sm.x), i, piece);
+        uint4 xv = *reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned char*>(sm.x) + (xa - smem_u32(sm.x)));
+        uint4 zv = make_uint4(0, 0, 0, 0);
+        if (gate)
+          zv = *reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned char*>(sm.z) +
+                                               (sw128(smem_u32(sm.z), i, piece) - smem_u32(sm.z)));
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+        const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
+        uint32_t out[4];
 #pragma unroll
-  for (int kb = 0; kb < kSsdQ / 16; ++kb) {
-    if (kb <= warp) {
-      // the accumulators of G, as A operands (hi + lo bf16 terms)
-      uint32_t ah[4], al[4];
-      split_bf16(G[2 * kb][0], G[2 * kb][1], ah[0], al[0]);
-      split_bf16(G[2 * kb][2], G[2 * kb][3], ah[1], al[1]);
-      split_bf16(G[2 * kb + 1][0], G[2 * kb + 1][1], ah[2], al[2]);
-      split_bf16(G[2 * kb + 1][2], G[2 * kb + 1][3], ah[3], al[3]);
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {  // two 8-column tiles per transposing load
-        uint32_t bx[4];
-        ldsm_x4_trans(bx, smem_u32(&s.x[kb * 16 + (lane & 15)][np * 16 + (lane >> 4) * 8]));
-        mma_16816(Y[2 * np], ah, bx[0], bx[1]);
-        mma_16816(Y[2 * np + 1], ah, bx[2], bx[3]);
-        mma_16816(Y[2 * np], al, bx[0], bx[1]);
-        mma_16816(Y[2 * np + 1], al, bx[2], bx[3]);
+        for (int e = 0; e < 4; ++e) {
+          const int k = 8 * q + 2 * e;  // column within the half
+          const float2 xx = unpack_bf16(xw[e]);
+          float y0 = __fmaf_rn(Dh, xx.x, __fmaf_rn(ei, __uint_as_float(yo[k]), __uint_as_float(yv[k])));
+          float y1 = __fmaf_rn(Dh, xx.y, __fmaf_rn(ei, __uint_as_float(yo[k + 1]), __uint_as_float(yv[k + 1])));
+          if (gate) {
+            const float2 zz = unpack_bf16(zw[e]);
+            y0 = __fmul_rn(y0, silu(zz.x));
+            y1 = __fmul_rn(y1, silu(zz.y));
+          }
+          out[e] = pack_bf16(y0, y1);
+        }
+        st_shared_v4(xa, out[0], out[1], out[2], out[3]);
       }
     }
   }
-#pragma unroll
-  for (int np = 0; np < 4; ++np) {
-    uint32_t bh_[4], bl_[4];
-    ldsm_x4_trans(bh_, smem_u32(&sm.s_hi[lane & 15][np * 16 + (lane >> 4) * 8]));
-    ldsm_x4_trans(bl_, smem_u32(&sm.s_lo[lane & 15][np * 16 + (lane >> 4) * 8]));
-    mma_16816(Yo[2 * np], ca, bh_[0], bh_[1]);
-    mma_16816(Yo[2 * np + 1], ca, bh_[2], bh_[3]);
-    mma_16816(Yo[2 * np], ca, bl_[0], bl_[1]);
-    mma_16816(Yo[2 * np + 1], ca, bl_[2], bl_[3]);
-  }
-  // y = (Y + 2^(acum_i) Yo + D x) silu(z), written over this thread's own x
-  // values once every warp is done reading x
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
-  const float e0 = ex2_approx(s.acum[i0]), e1 = ex2_approx(s.acum[i1]);
-  const float Dh = p.Dskip[h];
-  const bool gate = p.z != nullptr;
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    const int col = nt * 8 + 2 * t;
-    uint32_t* w0 = reinterpret_cast<uint32_t*>(&s.x[i0][col]);
-    uint32_t* w1 = reinterpret_cast<uint32_t*>(&s.x[i1][col]);
-    const float2 x0 = unpack_bf16(*w0), x1 = unpack_bf16(*w1);
-    float y00 = __fmaf_rn(Dh, x0.x, __fmaf_rn(e0, Yo[nt][0], Y[nt][0]));
-    float y01 = __fmaf_rn(Dh, x0.y, __fmaf_rn(e0, Yo[nt][1], Y[nt][1]));
-    float y10 = __fmaf_rn(Dh, x1.x, __fmaf_rn(e1, Yo[nt][2], Y[nt][2]));
-    float y11 = __fmaf_rn(Dh, x1.y, __fmaf_rn(e1, Yo[nt][3], Y[nt][3]));
-    if (gate) {
-      const float2 z0 = unpack_bf16(*reinterpret_cast<const uint32_t*>(&sm.z[i0][col]));
-      const float2 z1 = unpack_bf16(*reinterpret_cast<const uint32_t*>(&sm.z[i1][col]));
-      y00 = __fmul_rn(y00, silu(z0.x));
-      y01 = __fmul_rn(y01, silu(z0.y));
-      y10 = __fmul_rn(y10, silu(z1.x));
-      y11 = __fmul_rn(y11, silu(z1.y));
+  if (tid == 0) {
+    if (ok) {
+      tma_store_4d(&tm_y, 0, h, t0, b, smem_u32(sm.x));
+      bulk_commit();
+      bulk_wait_all();
+    } else {
+      report_error(4u);  // MAMBA_ERR_TIMEOUT
     }
-    *w0 = pack_bf16(y00, y01);
-    *w1 = pack_bf16(y10, y11);
   }
   __syncthreads();
-  // store: 8 channels (16 bytes) per access
-  const int H = p.heads, L = p.seqlen;
-  for (int i = tid; i < kSsdQ * 8; i += kSsdThreads) {
-    const int r = i >> 3, q = i & 7;
-    const int tt = c * kSsdQ + r;
-    if (tt < L)
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + (((size_t)b * L + tt) * H + h) * kSsdP + q * 8) =
-          *reinterpret_cast<const uint4*>(&s.x[r][q * 8]);
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kSsdTmemCols);
   }
 }
 

@@ -102,8 +102,8 @@ def test_layer_workspace_follows_its_layout(s, R, with_u_out):
 @settings(max_examples=200, deadline=None, derandomize=True)
 @given(st.integers(1, 8), st.integers(1, 300_000), st.integers(1, 256))
 def test_mamba2_workspace_follows_its_layout(B, L, H):
-    """Per (row, head, 64-token chunk): the chunk's end state and entering
+    """Per (row, head, 128-token chunk): the chunk's end state and entering
     state (16 x 64 fp32 each), its decay sum, and per token the dt and decay
-    prefix (64 x 2 fp32)."""
-    k = B * H * -(-L // 64)
-    assert ops.mamba2_scan_workspace_size(B, L, H) == 2 * r256(k * 16 * 64 * 4) + r256(k * 4) + r256(k * 64 * 2 * 4)
+    prefix (128 x 2 fp32)."""
+    k = B * H * -(-L // 128)
+    assert ops.mamba2_scan_workspace_size(B, L, H) == 2 * r256(k * 16 * 64 * 4) + r256(k * 4) + r256(k * 128 * 2 * 4)
