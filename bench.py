@@ -739,7 +739,7 @@ def bench_ssd(w, steps, warmup, local, heads=None, groups=1):
     hbm, src = peaks()
     res = {"metric": "mamba2 scan elements/s", "value": B * L * H * 64 / t, "unit": UNIT,
            "config": {"workload": f"mamba2_scan_bf16_b{B}_l{L}_h{H}_p64_g{groups}_n16", "batch": B, "seqlen": L,
-                      "heads": H, "head_dim": 64, "groups": groups, "d_state": D_STATE, "chunk": 64},
+                      "heads": H, "head_dim": 64, "groups": groups, "d_state": D_STATE, "chunk": 128},
            "ms_per_call": t * 1e3, "ms_per_call_min": min(per),
            "roofline": {"bound": "hbm", "achieved": alg / t / 1e9, "peak": hbm, "unit": "GB/s",
                         "frac": alg / t / 1e9 / hbm, "peak_source": src, "algorithmic_bytes_per_call": alg,

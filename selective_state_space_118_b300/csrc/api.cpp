@@ -765,13 +765,14 @@ size_t mamba2_scan_workspace_size(int batch, int seqlen, int heads) {
 }
 
 // 4-D map over a bf16 tensor (B, L, R, inner), rows of `inner` elements, read
-// or written in boxes of inner x 1 x 128 tokens x 1 with the given swizzle.
-bool encode4d_tokens(CUtensorMap* m, const void* base, int inner, int R, int L, int B, CUtensorMapSwizzle swizzle) {
+// or written in boxes of inner x 1 x `rows` tokens x 1 with the given swizzle.
+bool encode4d_tokens(CUtensorMap* m, const void* base, int inner, int R, int L, int B, CUtensorMapSwizzle swizzle,
+                     int rows = kSsdChunk) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)R, (cuuint64_t)L, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * 2 * R, (cuuint64_t)inner * 2 * R * L};
-  cuuint32_t box[4] = {(cuuint32_t)inner, 1, (cuuint32_t)kSsdChunk, 1};
+  cuuint32_t box[4] = {(cuuint32_t)inner, 1, (cuuint32_t)rows, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -829,13 +830,13 @@ mamba_status mamba2_scan_fwd(const mamba2_scan_args* a, void* stream_v) {
   p.totals = reinterpret_cast<float*>(w + 2 * st);
   p.cum = reinterpret_cast<float*>(w + 2 * st + round256(BH * nC * sizeof(float)));
   p.timeout_ns = kDefaultTimeoutNs;
-  CUtensorMap maps[5];  // x, z, B, C, y
+  CUtensorMap maps[5];  // x, z, B, C, y (y stored 32 tokens at a time)
   const int H = a->heads, G = a->groups, L = a->seqlen, Bt = a->batch;
   if (!encode4d_tokens(&maps[0], a->x, 64, H, L, Bt, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode4d_tokens(&maps[1], a->z ? a->z : a->x, 64, H, L, Bt, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode4d_tokens(&maps[2], a->Bm, 16, G, L, Bt, CU_TENSOR_MAP_SWIZZLE_32B) ||
       !encode4d_tokens(&maps[3], a->Cm, 16, G, L, Bt, CU_TENSOR_MAP_SWIZZLE_32B) ||
-      !encode4d_tokens(&maps[4], a->y, 64, H, L, Bt, CU_TENSOR_MAP_SWIZZLE_128B))
+      !encode4d_tokens(&maps[4], a->y, 64, H, L, Bt, CU_TENSOR_MAP_SWIZZLE_128B, 32))
     return MAMBA_ERR_CUDA;
   if (mamba::launch_ssd(maps, p, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
   return MAMBA_OK;

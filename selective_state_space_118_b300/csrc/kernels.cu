@@ -322,10 +322,15 @@ cudaError_t launch_ssd(const CUtensorMap maps[5], const SsdParams& p, cudaStream
   ssd_pass_kernel<<<dim3(32u / kPassSlices, (unsigned)p.heads, (unsigned)p.batch), 32 * kPassSlices, 0, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t smem = sizeof(SsdTcSmem) + 1024;
+  const size_t smem = sizeof(SsdOutSmem) + 1024;
   e = cudaFuncSetAttribute(ssd_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  ssd_output_kernel<<<grid, kSsdOutThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long tiles = (long)p.heads * p.n_chunks * p.batch;  // one CTA per SM, persistent
+  if (tiles >= (1L << 31)) return cudaErrorInvalidValue;
+  ssd_output_kernel<<<(unsigned)(tiles < sms ? tiles : sms), kSsdOutThreads, smem, stream>>>(maps[0], maps[1], maps[2],
+                                                                                           maps[3], maps[4], p);
   return cudaGetLastError();
 }
 

@@ -88,7 +88,7 @@ struct SsdParams {
   // laid out (B, H, 32, n_chunks, 32) so that one slice of every chunk is
   // contiguous
   float* S_c;             // each chunk's end state from zero
-  float* S_in;            // the state entering each chunk
+  float* S_in;            // the state entering each chunk: (B, H, n_chunks, 16, 64), one chunk's contiguous
   float* totals;          // (B, H, n_chunks): sum of dt * A (base 2) over each chunk
   float* cum;             // (B, H, n_chunks, 128, 2): per token, the prefix sum of dt * A and dt
   uint64_t timeout_ns;

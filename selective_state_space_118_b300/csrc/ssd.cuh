@@ -13,8 +13,9 @@
 // 16 x 64 product: warp-level mma m16n8k16, 16 rows being below the
 // 5th-generation MMA's smallest M), ssd_pass_kernel (the states entering the
 // chunks, serially per head, in fp32) and ssd_output_kernel (Y_diag + Y_off +
-// D x, gated) on tcgen05: its three products are 128-row MMAs with the
-// accumulators in tensor memory and the tiles brought in by TMA.  fp32
+// D x, gated) on tcgen05: a persistent, warp-specialised pipeline whose three
+// products are 128-row MMAs with the accumulators in tensor memory and the
+// tiles brought in by TMA.  fp32
 // quantities entering a product (the decay-weighted B rows and C B^T
 // entries, the entering state) go in as two bf16 terms (hi + lo, ~16
 // significant bits).
@@ -230,7 +231,8 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_states_kernel(const __grid_co
 // The state entering chunk c: S_in[0] = h0 (or 0), S_in[c + 1] = 2^(total_c)
 // S_in[c] + S_c[c], in fp32.  One thread per state value walks the chunks in
 // order; a warp holds one slice (32 values), so each step's loads and stores
-// are 128 contiguous bytes, and each thread keeps kPassAhead chunks' loads in
+// are 128 contiguous bytes (S_in is written one chunk's state contiguous, for
+// the output kernel's bulk copy), and each thread keeps kPassAhead chunks' loads in
 // flight (the chain itself is one fma per chunk).  The chunks' decay factors
 // 2^(total) are staged in shared memory, kPassBlock at a time.
 // grid (32 / kPassSlices, H, B), 32 * kPassSlices threads.
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(32 * kPassSlices) ssd_pass_kernel(const __grid
   const int nC = p.n_chunks;
   const int n = q / 2, col = 32 * (q % 2) + lane;  // this thread's state value (row n, column col)
   const float* src = p.S_c + (bh * 32 + q) * (size_t)nC * 32 + lane;
-  float* dst = p.S_in + (bh * 32 + q) * (size_t)nC * 32 + lane;
+  float* dst = p.S_in + (bh * nC * 32 + q) * 32 + lane;  // S_in: each chunk's 16 x 64 state contiguous
   const float* tot = p.totals + bh * nC;
   float S = p.h0 ? p.h0[bh * kSsdN * kSsdP + n * kSsdP + col] : 0.0f;
   float ahead[kPassAhead];
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(32 * kPassSlices) ssd_pass_kernel(const __grid
     for (int k = 0; k < kPassAhead; ++k) {
       const int c = c0 + k;
       if (c < nC) {
-        __stcs(dst + (size_t)c * 32, S);
+        __stcs(dst + (size_t)c * kSsdN * kSsdP, S);
         const float v = ahead[k];
         if (c + kPassAhead < nC) ahead[k] = __ldcs(src + (size_t)(c + kPassAhead) * 32);
         S = __fmaf_rn(fac[c % kPassBlock], S, v);
@@ -274,64 +276,163 @@ __global__ void __launch_bounds__(32 * kPassSlices) ssd_pass_kernel(const __grid
 }
 
 // ---------------------------------------------------------------- output
-// One CTA (8 warps) per (head, chunk, batch row): thread t serves chunk row
-// i = t % 128 (TMEM lane i) and half t / 128 of that row's columns.  Tiles by TMA: x and z (128 tokens x 64 channels, 128-byte
-// swizzle: the K = token dimension's rows of 128 bytes, an MN-major operand),
-// B and C (128 tokens x 16 states, 32-byte swizzle, K-major).  Three MMA
-// groups, issued by one thread, accumulators in tensor memory:
-//   G  = C B^T              128 x 128, K = 16          (TMEM columns 0..127)
-//   Yo = C (S_hi + S_lo)    128 x 64,  K = 16 twice    (columns 128..191)
-//   Y  = (G_hi + G_lo) X    128 x 64,  K = 128 twice   (columns 192..255)
-// Between them each thread reads its row of G, masks it to s <= t, scales it
-// by the decay 2^(acum_i - acum_j) dt_j and writes it, as hi + lo bf16 terms,
-// into shared memory in the K-major 128-byte-swizzled layout of an A
-// operand.  The epilogue: y = Y + 2^(acum_i) Yo + D x, times silu(z), written
-// over the thread's row of the x tile and stored by TMA.
-constexpr int kSsdTmemCols = 256;
-constexpr int kSsdOutThreads = 256;
+// A persistent kernel, one CTA per SM, walking tiles t = (head, chunk, batch
+// row) with the head fastest (the SMs at work at one time share a chunk's B
+// and C rows and read its x, z rows whole).  Warp roles, linked by mbarriers:
+//   warp 0      loads tile k into stage k % 4 by TMA: x (128 tokens x 64
+//               channels, 128-byte swizzle), B, C (128 x 16, 32-byte
+//               swizzle), the entering state (fp32, 4 KB) and the chunk's
+//               (decay prefix, dt) pairs by bulk copies; z, read only by the
+//               epilogue, into a ring of its own of two tiles;
+//   warp 1      issues the MMAs into tensor-memory buffer k % 4 (128
+//               columns each), each as soon as its inputs are ready:
+//               G = C B^T (128 x 128, K = 16); then Y = G' X (128 x 64), the
+//               hi and lo terms accumulated,
+//               two halves of K = 64, each once the converter has written its
+//               half of G', over columns 0..63; Yo = C (S_hi + S_lo)
+//               (128 x 64, K = 16) over columns 64..127 with the second half;
+//   warps 4-11  warp w reads rows 32 (w % 4) .. + 31 of G and columns
+//               64 h .. + 63 (h = (w - 4) / 4, the K half), masks them to
+//               s <= t, scales them by the decay 2^(acum_i - acum_j) dt_j and
+//               writes them as hi + lo bf16 terms (G' = G_hi + G_lo, ~16
+//               significant bits) into half h of the K-major operand of the Y
+//               product; the h = 1 warps also write the entering state, as
+//               hi + lo terms, into the MN-major operand of the Yo product;
+//   warps 12-15 y = Y + 2^(acum_i) Yo + D x, times silu(z) (through tanh),
+//               written over the stage's x rows and stored by TMA (32 rows
+//               per warp), which frees the stage.
+// The decay factor of an entry is taken relative to the first token of its
+// 32-column group, 2^(acum_i - acum_r) * (2^(acum_r - acum_j) dt_j): both
+// factors stay in range while the decay across the 32 tokens is at most
+// 2^60; beyond that (very fast decay) the entry's factor is computed whole.
+// The all-zero 32 x 32 blocks above the diagonal are written once.
+constexpr int kSsdStages = 4;
+constexpr int kSsdOutThreads = 512;
+constexpr int kSsdAcc = 4;  // tensor-memory accumulator buffers of 128 columns
+constexpr int kSsdTmemCols = 128 * kSsdAcc;
 
-struct SsdTcSmem {
-  __nv_bfloat16 x[kSsdQ * kSsdP];        // 16 KB, then y
-  __nv_bfloat16 z[kSsdQ * kSsdP];        // 16 KB
-  __nv_bfloat16 ghi[2][kSsdQ * 64];      // G's columns 0..63 and 64..127: rows of 128 bytes
+struct SsdStage {
+  __nv_bfloat16 x[kSsdQ * kSsdP];  // 16 KB, rows of 128 bytes; then y
+  __nv_bfloat16 b[kSsdQ * kSsdN];  // rows of 32 bytes
+  __nv_bfloat16 c[kSsdQ * kSsdN];
+  float s[kSsdN * kSsdP];          // the entering state, row n of 64 channels
+  float2 cum[kSsdQ];               // (decay prefix, dt) per token
+};
+static_assert(sizeof(SsdStage) % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled tiles");
+
+struct SsdOutSmem {
+  SsdStage st[kSsdStages];
+  __nv_bfloat16 z[2][kSsdQ * kSsdP];  // the gate's ring
+  __nv_bfloat16 ghi[2][kSsdQ * 64];   // G' in two 64-column K halves, rows of 128 bytes
   __nv_bfloat16 glo[2][kSsdQ * 64];
-  __nv_bfloat16 shi[kSsdN * kSsdP];      // S_in: rows n of 64 channels (128 bytes)
+  __nv_bfloat16 shi[kSsdN * kSsdP];  // the entering state: rows n of 64 channels
   __nv_bfloat16 slo[kSsdN * kSsdP];
-  __nv_bfloat16 c[kSsdQ * kSsdN];        // rows of 32 bytes
-  __nv_bfloat16 b[kSsdQ * kSsdN];
-  float acum[kSsdQ];
-  float dt[kSsdQ];
-  float fdt[kSsdQ];                      // 2^(ref - acum_j) dt_j
-  uint64_t bar_tile, bar_mma1, bar_mma2;
+  float fdt[8][64];                  // per converter warp: 2^(acum_r - acum_j) dt_j for its columns
+  uint64_t full[kSsdStages], empty[kSsdStages];
+  uint64_t gfull[kSsdAcc], tmem_empty[kSsdAcc], yfull[kSsdAcc];
+  uint64_t gop_full[2], gop_empty[2];
+  uint64_t zfull[2], zempty[2];
   uint32_t tmem_base;
 };
 
-// 16-byte piece `piece` of row `row` in a 128-byte-swizzled tile of 128-byte rows.
+// 16-byte piece `piece` of row `row` in a 128-byte-swizzled tile of 128-byte
+// rows (the tile 1024-byte aligned).
 __device__ __forceinline__ uint32_t sw128(uint32_t base, int row, int piece) {
   return base + row * 128 + ((piece ^ (row & 7)) << 4);
 }
 
-__global__ void __launch_bounds__(kSsdOutThreads, 2)
+struct SsdTileId {
+  int h, c, b;
+};
+
+// (the host keeps the tile count below 2^31)
+__device__ __forceinline__ SsdTileId ssd_tile(uint32_t t, uint32_t H, uint32_t nC) {
+  SsdTileId id;
+  const uint32_t hc = t / H;
+  id.h = (int)(t - hc * H);
+  id.b = (int)(hc / nC);
+  id.c = (int)(hc - (uint32_t)id.b * nC);
+  return id;
+}
+
+// silu(z) = z sigmoid(z) = h + h tanh(h), h = z / 2: one MUFU operation per
+// value (tanh.approx, relative error about 2^-11, which moves silu by at most
+// about |h| 2^-11 -- below a bf16 output's half ulp relative to the gated
+// output's scale).
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float2 silu_tanh_x2(float2 z) {
+  const float2 h = __fmul2_rn(z, make_float2(0.5f, 0.5f));
+  return __ffma2_rn(h, make_float2(tanh_approx(h.x), tanh_approx(h.y)), h);
+}
+
+// v (two fp32 values) as hi + lo bf16 pairs, packed arithmetic.
+__device__ __forceinline__ void split_bf16_x2(float2 v, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(v.x, v.y);
+  const float2 h = unpack_bf16(hi);
+  const float2 d = __ffma2_rn(h, make_float2(-1.0f, -1.0f), v);  // v - h, exactly rounded
+  lo = pack_bf16(d.x, d.y);
+}
+
+// The Y half kh of tile kk (and, with the second half, Yo): MMAs into d.
+__device__ __forceinline__ void ssd_issue_y(const SsdOutSmem& sm, const SsdStage& st, uint32_t d, int kh) {
+  const uint32_t iy = umma_idesc_bf16(128, 64, true);  // B operand (x rows, S rows) MN-major
+#pragma unroll
+  for (int part = 0; part < 2; ++part)
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const uint32_t gb = smem_u32(part == 0 ? sm.ghi[kh] : sm.glo[kh]);
+      const uint64_t ad = umma_desc(gb + 32 * ks, 1024, 2);                                // 16 columns of G'
+      const uint64_t bd = umma_desc(smem_u32(st.x) + (kh * 64 + ks * 16) * 128, 1024, 2);  // 16 rows of x
+      tc_mma_f16(d, ad, bd, iy, kh > 0 || part > 0 || ks > 0);
+    }
+  if (kh == 1) {
+    const uint64_t cd = umma_desc(smem_u32(st.c), 256, 6);
+    tc_mma_f16(d + 64, cd, umma_desc(smem_u32(sm.shi), 1024, 2), iy, false);
+    tc_mma_f16(d + 64, cd, umma_desc(smem_u32(sm.slo), 1024, 2), iy, true);
+  }
+}
+
+__global__ void __launch_bounds__(kSsdOutThreads, 1)
     ssd_output_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
                       const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
                       const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ SsdParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  SsdTcSmem& sm = *reinterpret_cast<SsdTcSmem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
-  const int h = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int H = p.heads, G = p.groups;
-  const int g = h / (H / G);
-  const int t0 = c * kSsdQ;
-  const size_t bh = (size_t)b * H + h;
+  SsdOutSmem& sm = *reinterpret_cast<SsdOutSmem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = p.heads, nC = p.n_chunks, L = p.seqlen;
+  const uint32_t tiles = (uint32_t)H * nC * p.batch;
+  const uint32_t n_mine = (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;  // this CTA's tiles
   const bool gate = p.z != nullptr;
 
   if (tid == 0) {
-    mbar_init(smem_u32(&sm.bar_tile), 1);
-    mbar_init(smem_u32(&sm.bar_mma1), 1);
-    mbar_init(smem_u32(&sm.bar_mma2), 1);
+    for (int s = 0; s < kSsdStages; ++s) {
+      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), 4);  // one arrival per epilogue warp
+    }
+    for (int a = 0; a < kSsdAcc; ++a) {
+      mbar_init(smem_u32(&sm.gfull[a]), 1);
+      mbar_init(smem_u32(&sm.tmem_empty[a]), 4);
+      mbar_init(smem_u32(&sm.yfull[a]), 1);
+    }
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(smem_u32(&sm.gop_full[h]), 4);  // one arrival per converter warp of the half
+      mbar_init(smem_u32(&sm.gop_empty[h]), 1);
+      mbar_init(smem_u32(&sm.zfull[h]), 1);
+      mbar_init(smem_u32(&sm.zempty[h]), 4);  // one arrival per epilogue warp
+    }
     fence_mbar_init();
+    prefetch_tensormap(&tm_x);
+    prefetch_tensormap(&tm_z);
+    prefetch_tensormap(&tm_b);
+    prefetch_tensormap(&tm_c);
+    prefetch_tensormap(&tm_y);
   }
-  if (warp == 0) {
+  if (warp == 1) {
     tmem_alloc(smem_u32(&sm.tmem_base), kSsdTmemCols);
     tmem_relinquish();
   }
@@ -339,172 +440,274 @@ __global__ void __launch_bounds__(kSsdOutThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  if (tid == 0) {
-    const uint32_t bar = smem_u32(&sm.bar_tile);
-    mbar_arrive_expect_tx(bar, (gate ? 2 : 1) * kSsdQ * kSsdP * 2 + 2 * kSsdQ * kSsdN * 2);
-    tma_load_4d(smem_u32(sm.x), &tm_x, 0, h, t0, b, bar);
-    if (gate) tma_load_4d(smem_u32(sm.z), &tm_z, 0, h, t0, b, bar);
-    tma_load_4d(smem_u32(sm.b), &tm_b, 0, g, t0, b, bar);
-    tma_load_4d(smem_u32(sm.c), &tm_c, 0, g, t0, b, bar);
-  }
-  // while the tiles fly: dt and the decay prefix (the states kernel's), and
-  // the entering state as hi + lo bf16 terms in the MN-major layout (row n:
-  // 64 channels, 8 channels per 16-byte piece, 128-byte swizzle)
-  if (tid < kSsdQ) {
-    const float2 v = reinterpret_cast<const float2*>(p.cum)[(bh * p.n_chunks + c) * kSsdQ + tid];
-    sm.acum[tid] = v.x;
-    sm.dt[tid] = v.y;
-    const int n = tid >> 3, piece = tid & 7;  // 16 rows x 8 pieces: one per thread
-    const float* src = p.S_in + ssd_slice(bh, n, piece * 8, c, p.n_chunks);
-    const float4 a = __ldcs(reinterpret_cast<const float4*>(src));
-    const float4 d = __ldcs(reinterpret_cast<const float4*>(src) + 1);
-    uint32_t hi[4], lo[4];
-    split_bf16(a.x, a.y, hi[0], lo[0]);
-    split_bf16(a.z, a.w, hi[1], lo[1]);
-    split_bf16(d.x, d.y, hi[2], lo[2]);
-    split_bf16(d.z, d.w, hi[3], lo[3]);
-    st_shared_v4(sw128(smem_u32(sm.shi), n, piece), hi[0], hi[1], hi[2], hi[3]);
-    st_shared_v4(sw128(smem_u32(sm.slo), n, piece), lo[0], lo[1], lo[2], lo[3]);
-  }
-  fence_proxy_async_smem();
-  __syncthreads();
-  const float ref = sm.acum[0];
-  const bool split = __fsub_rn(ref, sm.acum[kSsdQ - 1]) <= 60.0f;  // the whole chunk's decay span
-  if (split && tid < kSsdQ) sm.fdt[tid] = __fmul_rn(ex2_approx(__fsub_rn(ref, sm.acum[tid])), sm.dt[tid]);
-
   bool ok = true;
-  if (tid == 0) {  // G = C B^T and Yo = C S_in
-    ok = mbar_wait_bounded(smem_u32(&sm.bar_tile), 0, p.timeout_ns);
-    if (ok) {
-      tc_fence_after();
-      const uint64_t cd = umma_desc(smem_u32(sm.c), 256, 6);
-      tc_mma_f16(tmem, cd, umma_desc(smem_u32(sm.b), 256, 6), umma_idesc_bf16(128, 128, false), false);
-      const uint32_t io = umma_idesc_bf16(128, 64, true);
-      tc_mma_f16(tmem + 128, cd, umma_desc(smem_u32(sm.shi), 1024, 2), io, false);
-      tc_mma_f16(tmem + 128, cd, umma_desc(smem_u32(sm.slo), 1024, 2), io, true);
-      tc_commit(smem_u32(&sm.bar_mma1));
-    }
-  }
-  ok = __syncthreads_and(ok);
-  if (ok) {
-    ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&sm.bar_mma1), 0, p.timeout_ns));
-    ok = __syncthreads_and(ok);
-  }
-  const int i = tid & (kSsdQ - 1);  // this thread's row
-  const int hf = tid >> 7;           // and half of the row's columns
-  const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
-  if (ok) {
-    tc_fence_after();
-    const float ai = sm.acum[i];
-    const float ri = ex2_approx(__fsub_rn(ai, ref));
-#pragma unroll 1
-    for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {  // 32 columns j of G at a time
-      uint32_t r[32];
-      tmem_ld_32cols(tmem + lanes + 32 * cb, r);
-      uint32_t hi[16], lo[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        float v2[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int j = 32 * cb + 2 * e + u;
-          float f;
-          if (split)
-            f = __fmul_rn(ri, sm.fdt[j]);
-          else
-            f = __fmul_rn(ex2_approx(__fsub_rn(ai, sm.acum[j])), sm.dt[j]);
-          v2[u] = j <= i ? __fmul_rn(__uint_as_float(r[2 * e + u]), f) : 0.0f;
-        }
-        split_bf16(v2[0], v2[1], hi[e], lo[e]);
-      }
-      // columns 32cb .. 32cb + 31: K block cb / 2, pieces 4 (cb % 2) .. + 3
-      const int kb = cb >> 1;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int piece = 4 * (cb & 1) + q;
-        st_shared_v4(sw128(smem_u32(sm.ghi[kb]), i, piece), hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
-        st_shared_v4(sw128(smem_u32(sm.glo[kb]), i, piece), lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
-      }
-    }
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (tid == 0 && ok) {  // Y = G X: the hi terms, then the lo terms, 16 tokens of K per MMA
-    const uint32_t iy = umma_idesc_bf16(128, 64, true);
-    bool acc = false;
-#pragma unroll 1
-    for (int part = 0; part < 2; ++part) {
-      for (int kb = 0; kb < 2; ++kb) {
-        const uint32_t gbase = smem_u32(part == 0 ? sm.ghi[kb] : sm.glo[kb]);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t ad = umma_desc(gbase + 32 * ks, 1024, 2);                         // 16 columns of G
-          const uint64_t bd = umma_desc(smem_u32(sm.x) + (kb * 64 + ks * 16) * 128, 1024, 2);  // 16 rows of x
-          tc_mma_f16(tmem + 192, ad, bd, iy, acc);
-          acc = true;
-        }
-      }
-    }
-    tc_commit(smem_u32(&sm.bar_mma2));
-  }
-  if (ok) {
-    ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&sm.bar_mma2), 0, p.timeout_ns));
-    ok = __syncthreads_and(ok);
-  }
-  if (ok) {
-    tc_fence_after();
-    const float ei = ex2_approx(sm.acum[i]);
-    const float Dh = p.Dskip[h];
-    {
-      const int half = hf;  // channels 32 half .. + 31
-      uint32_t yv[32], yo[32];
-      tmem_ld_32cols(tmem + lanes + 192 + 32 * half, yv);
-      tmem_ld_32cols(tmem + lanes + 128 + 32 * half, yo);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int piece = 4 * half + q;
-        const uint32_t xa = sw128(smem_u32(sm.x), i, piece);
-        uint4 xv = *reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned char*>(sm.x) + (xa - smem_u32(sm.x)));
-        uint4 zv = make_uint4(0, 0, 0, 0);
-        if (gate)
-          zv = *reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned char*>(sm.z) +
-                                               (sw128(smem_u32(sm.z), i, piece) - smem_u32(sm.z)));
-        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-        const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
-        uint32_t out[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int k = 8 * q + 2 * e;  // column within the half
-          const float2 xx = unpack_bf16(xw[e]);
-          float y0 = __fmaf_rn(Dh, xx.x, __fmaf_rn(ei, __uint_as_float(yo[k]), __uint_as_float(yv[k])));
-          float y1 = __fmaf_rn(Dh, xx.y, __fmaf_rn(ei, __uint_as_float(yo[k + 1]), __uint_as_float(yv[k + 1])));
-          if (gate) {
-            const float2 zz = unpack_bf16(zw[e]);
-            y0 = __fmul_rn(y0, silu(zz.x));
-            y1 = __fmul_rn(y1, silu(zz.y));
-          }
-          out[e] = pack_bf16(y0, y1);
-        }
-        st_shared_v4(xa, out[0], out[1], out[2], out[3]);
-      }
-    }
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  if (tid == 0) {
-    if (ok) {
-      tma_store_4d(&tm_y, 0, h, t0, b, smem_u32(sm.x));
-      bulk_commit();
-      bulk_wait_all();
-    } else {
-      report_error(4u);  // MAMBA_ERR_TIMEOUT
-    }
-  }
-  __syncthreads();
+
   if (warp == 0) {
+    if (lane == 0) {  // producer: the stages, and the gate's ring (one tile behind at most)
+      const uint32_t bytes = kSsdQ * kSsdP * 2 + 2 * kSsdQ * kSsdN * 2 + kSsdN * kSsdP * 4 + kSsdQ * 8;
+      uint32_t k = 0, kz = 0;
+      uint64_t idle_since = globaltimer_ns();
+      while (k < n_mine || (gate && kz < n_mine)) {
+        bool moved = false;
+        if (k < n_mine && mbar_test_wait(smem_u32(&sm.empty[k % kSsdStages]), ((k / kSsdStages) & 1u) ^ 1u)) {
+          const int s = (int)(k % kSsdStages);
+          const SsdTileId id = ssd_tile(blockIdx.x + k * gridDim.x, H, nC);
+          const int g = id.h / (H / p.groups), t0 = id.c * kSsdQ;
+          const size_t chunk = ((size_t)id.b * H + id.h) * nC + id.c;
+          SsdStage& st = sm.st[s];
+          const uint32_t bar = smem_u32(&sm.full[s]);
+          if (gate) tma_prefetch_4d(&tm_z, 0, id.h, t0, id.b);  // into L2, for the gate's ring
+          mbar_arrive_expect_tx(bar, bytes);
+          tma_load_4d(smem_u32(st.x), &tm_x, 0, id.h, t0, id.b, bar);
+          tma_load_4d(smem_u32(st.b), &tm_b, 0, g, t0, id.b, bar);
+          tma_load_4d(smem_u32(st.c), &tm_c, 0, g, t0, id.b, bar);
+          bulk_load(smem_u32(st.s), p.S_in + chunk * (kSsdN * kSsdP), kSsdN * kSsdP * 4, bar);
+          bulk_load(smem_u32(st.cum), p.cum + chunk * (2 * kSsdQ), kSsdQ * 8, bar);
+          ++k;
+          moved = true;
+        }
+        if (gate && kz < k && mbar_test_wait(smem_u32(&sm.zempty[kz & 1u]), ((kz >> 1) & 1u) ^ 1u)) {
+          const SsdTileId id = ssd_tile(blockIdx.x + kz * gridDim.x, H, nC);
+          const uint32_t bar = smem_u32(&sm.zfull[kz & 1u]);
+          mbar_arrive_expect_tx(bar, kSsdQ * kSsdP * 2);
+          tma_load_4d(smem_u32(sm.z[kz & 1u]), &tm_z, 0, id.h, id.c * kSsdQ, id.b, bar);
+          ++kz;
+          moved = true;
+        }
+        if (moved) {
+          idle_since = globaltimer_ns();
+        } else {
+          if (globaltimer_ns() - idle_since > p.timeout_ns) {
+            ok = false;
+            break;
+          }
+          __nanosleep(32);
+        }
+      }
+      // the copies issued last have landed before the CTA may end
+      for (uint32_t j = k > kSsdStages ? k - kSsdStages : 0; j < k; ++j)
+        if (!mbar_wait_bounded(smem_u32(&sm.full[j % kSsdStages]), (j / kSsdStages) & 1u, p.timeout_ns)) ok = false;
+      for (uint32_t j = kz > 2 ? kz - 2 : 0; j < kz; ++j)
+        if (!mbar_wait_bounded(smem_u32(&sm.zfull[j & 1u]), (j >> 1) & 1u, p.timeout_ns)) ok = false;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer: G of tile kg, Y halves of tiles ky0, ky1, each as soon as it may go
+      const uint32_t ig = umma_idesc_bf16(128, 128, false);  // G = C B^T: both K-major
+      uint32_t kg = 0, ky0 = 0, ky1 = 0;
+      uint64_t idle_since = globaltimer_ns();
+      while (ky1 < n_mine) {
+        bool moved = false;
+        if (kg < n_mine && mbar_test_wait(smem_u32(&sm.full[kg % kSsdStages]), (kg / kSsdStages) & 1u) &&
+            mbar_test_wait(smem_u32(&sm.tmem_empty[kg % kSsdAcc]), ((kg / kSsdAcc) & 1u) ^ 1u)) {
+          tc_fence_after();
+          const SsdStage& st = sm.st[kg % kSsdStages];
+          tc_mma_f16(tmem + (kg % kSsdAcc) * 128, umma_desc(smem_u32(st.c), 256, 6),
+                     umma_desc(smem_u32(st.b), 256, 6), ig, false);
+          tc_commit(smem_u32(&sm.gfull[kg % kSsdAcc]));
+          ++kg;
+          moved = true;
+        }
+        if (ky0 < kg && mbar_test_wait(smem_u32(&sm.gop_full[0]), ky0 & 1u)) {
+          tc_fence_after();
+          ssd_issue_y(sm, sm.st[ky0 % kSsdStages], tmem + (ky0 % kSsdAcc) * 128, 0);
+          tc_commit(smem_u32(&sm.gop_empty[0]));
+          ++ky0;
+          moved = true;
+        }
+        if (ky1 < ky0 && mbar_test_wait(smem_u32(&sm.gop_full[1]), ky1 & 1u)) {
+          tc_fence_after();
+          ssd_issue_y(sm, sm.st[ky1 % kSsdStages], tmem + (ky1 % kSsdAcc) * 128, 1);
+          tc_commit(smem_u32(&sm.gop_empty[1]));
+          tc_commit(smem_u32(&sm.yfull[ky1 % kSsdAcc]));
+          ++ky1;
+          moved = true;
+        }
+        if (moved) {
+          idle_since = globaltimer_ns();
+        } else {
+          if (globaltimer_ns() - idle_since > p.timeout_ns) {
+            ok = false;
+            break;
+          }
+          __nanosleep(20);
+        }
+      }
+    }
+  } else if (warp >= 4 && warp < 12) {  // G -> operand
+    const int q4 = warp & 3, kh = (warp - 4) >> 2, cw = warp - 4;
+    const int i = 32 * q4 + lane;  // this thread's row (token of the chunk)
+    const uint32_t lanes = (uint32_t)(32 * q4) << 16;
+    const uint32_t ghi = smem_u32(sm.ghi[kh]), glo = smem_u32(sm.glo[kh]);
+    // the blocks above the diagonal, zero for every tile
+#pragma unroll
+    for (int gq = 0; gq < 2; ++gq)
+      if (64 * kh + 32 * gq > 32 * q4)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          st_shared_v4(sw128(ghi, i, 4 * gq + q), 0u, 0u, 0u, 0u);
+          st_shared_v4(sw128(glo, i, 4 * gq + q), 0u, 0u, 0u, 0u);
+        }
+    float* fd = sm.fdt[cw];
+    for (uint32_t k = 0; k < n_mine; ++k) {
+      const int s = (int)(k % kSsdStages);
+      const uint32_t a = k % kSsdAcc;
+      const bool mine = mbar_wait_bounded(smem_u32(&sm.full[s]), (k / kSsdStages) & 1u, p.timeout_ns) &&
+                        mbar_wait_bounded(smem_u32(&sm.gfull[a]), (k / kSsdAcc) & 1u, p.timeout_ns) &&
+                        mbar_wait_bounded(smem_u32(&sm.gop_empty[kh]), (k & 1u) ^ 1u, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, mine)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const SsdStage& st = sm.st[s];
+      const float ai = st.cum[i].x;
+#pragma unroll
+      for (int gq = 0; gq < 2; ++gq) {
+        const int col0 = 64 * kh + 32 * gq;  // the group's first column (token r)
+        if (col0 > 32 * q4) continue;        // above the diagonal for the whole warp: zero, written once
+        const float ar = st.cum[col0].x;
+        const bool fast = __fsub_rn(ar, st.cum[col0 + 31].x) <= 60.0f;  // the group's decay span
+        {
+          const float2 v = st.cum[col0 + lane];
+          fd[32 * gq + lane] = __fmul_rn(ex2_approx(__fsub_rn(ar, v.x)), v.y);
+        }
+        __syncwarp();
+        const float ri = ex2_approx(__fsub_rn(ai, ar));
+        const float2 ri2 = make_float2(ri, ri);
+        uint32_t graw[32];
+        tmem_ld_32cols(tmem + lanes + a * 128 + col0, graw);
+        const bool diag = col0 == 32 * q4;
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          float2 f01, f23;
+          if (fast) {
+            const float4 fv = *reinterpret_cast<const float4*>(fd + 32 * gq + 4 * e4);
+            f01 = __fmul2_rn(ri2, make_float2(fv.x, fv.y));
+            f23 = __fmul2_rn(ri2, make_float2(fv.z, fv.w));
+          } else {
+            float f[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float2 v = st.cum[col0 + 4 * e4 + u];
+              f[u] = __fmul_rn(ex2_approx(__fsub_rn(ai, v.x)), v.y);
+            }
+            f01 = make_float2(f[0], f[1]);
+            f23 = make_float2(f[2], f[3]);
+          }
+          float2 v01 = __fmul2_rn(make_float2(__uint_as_float(graw[4 * e4]), __uint_as_float(graw[4 * e4 + 1])), f01);
+          float2 v23 =
+              __fmul2_rn(make_float2(__uint_as_float(graw[4 * e4 + 2]), __uint_as_float(graw[4 * e4 + 3])), f23);
+          if (diag) {
+            const int j = col0 + 4 * e4;
+            if (j > i) v01.x = 0.0f;
+            if (j + 1 > i) v01.y = 0.0f;
+            if (j + 2 > i) v23.x = 0.0f;
+            if (j + 3 > i) v23.y = 0.0f;
+          }
+          split_bf16_x2(v01, hi[2 * e4], lo[2 * e4]);
+          split_bf16_x2(v23, hi[2 * e4 + 1], lo[2 * e4 + 1]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int piece = 4 * gq + q;
+          st_shared_v4(sw128(ghi, i, piece), hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+          st_shared_v4(sw128(glo, i, piece), lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+        }
+        __syncwarp();  // fd is read before the next group overwrites it
+      }
+      if (kh == 1) {  // the entering state: row n, 8 channels (one 16-byte piece) per thread
+        const int n = i >> 3, piece = i & 7;
+        const float4 v0 = *reinterpret_cast<const float4*>(st.s + n * kSsdP + 8 * piece);
+        const float4 v1 = *reinterpret_cast<const float4*>(st.s + n * kSsdP + 8 * piece + 4);
+        uint32_t h[4], l[4];
+        split_bf16_x2(make_float2(v0.x, v0.y), h[0], l[0]);
+        split_bf16_x2(make_float2(v0.z, v0.w), h[1], l[1]);
+        split_bf16_x2(make_float2(v1.x, v1.y), h[2], l[2]);
+        split_bf16_x2(make_float2(v1.z, v1.w), h[3], l[3]);
+        st_shared_v4(sw128(smem_u32(sm.shi), n, piece), h[0], h[1], h[2], h[3]);
+        st_shared_v4(sw128(smem_u32(sm.slo), n, piece), l[0], l[1], l[2], l[3]);
+      }
+      fence_proxy_async_smem();  // the operands, visible to the tensor core
+      tc_fence_before();         // and G's columns read out before they are overwritten
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.gop_full[kh]));
+    }
+  } else if (warp >= 12) {  // epilogue
+    const int q4 = warp & 3;
+    const int i = 32 * q4 + lane;
+    const uint32_t lanes = (uint32_t)(32 * q4) << 16;
+    for (uint32_t k = 0; k < n_mine; ++k) {
+      const int s = (int)(k % kSsdStages);
+      const uint32_t a = k % kSsdAcc;
+      const SsdTileId id = ssd_tile(blockIdx.x + k * gridDim.x, H, nC);
+      const float Dh = __ldg(p.Dskip + id.h);  // in flight while the accumulators are waited for
+      const bool mine = mbar_wait_bounded(smem_u32(&sm.yfull[a]), (k / kSsdAcc) & 1u, p.timeout_ns) &&
+                        mbar_wait_bounded(smem_u32(&sm.full[s]), (k / kSsdStages) & 1u, p.timeout_ns) &&
+                        (!gate || mbar_wait_bounded(smem_u32(&sm.zfull[k & 1u]), (k >> 1) & 1u, p.timeout_ns));
+      if (!__all_sync(0xffffffffu, mine)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      SsdStage& st = sm.st[s];
+      const float ei = ex2_approx(st.cum[i].x);
+      const float2 ei2 = make_float2(ei, ei), Dh2 = make_float2(Dh, Dh);
+      const uint32_t xb = smem_u32(st.x), zb = smem_u32(sm.z[k & 1u]);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {  // 16 channels at a time
+        uint32_t yv[16], yo[16];
+        tmem_ld_16cols(tmem + lanes + a * 128 + 16 * r, yv);
+        tmem_ld_16cols(tmem + lanes + a * 128 + 64 + 16 * r, yo);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t xa = sw128(xb, i, 2 * r + q);
+          uint4 xv;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(xv.x), "=r"(xv.y), "=r"(xv.z), "=r"(xv.w)
+                       : "r"(xa));
+          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+          uint4 zv = make_uint4(0u, 0u, 0u, 0u);
+          if (gate)
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(zv.x), "=r"(zv.y), "=r"(zv.z), "=r"(zv.w)
+                         : "r"(sw128(zb, i, 2 * r + q)));
+          const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
+          uint32_t out[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int kk = 8 * q + 2 * e;
+            float2 y2 = __ffma2_rn(ei2, make_float2(__uint_as_float(yo[kk]), __uint_as_float(yo[kk + 1])),
+                                   make_float2(__uint_as_float(yv[kk]), __uint_as_float(yv[kk + 1])));
+            y2 = __ffma2_rn(Dh2, unpack_bf16(xw[e]), y2);
+            if (gate) y2 = __fmul2_rn(y2, silu_tanh_x2(unpack_bf16(zw[e])));
+            out[e] = pack_bf16(y2.x, y2.y);
+          }
+          st_shared_v4(xa, out[0], out[1], out[2], out[3]);
+        }
+      }
+      tc_fence_before();  // the accumulators are read: tensor-memory buffer a is free
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&sm.tmem_empty[a]));
+        if (gate) mbar_arrive(smem_u32(&sm.zempty[k & 1u]));  // this warp's rows of z are read
+        if (id.c * kSsdQ + 32 * q4 < L) {  // rows past the sequence's end are clipped (or all of them)
+          tma_store_4d(&tm_y, 0, id.h, id.c * kSsdQ + 32 * q4, id.b, xb + 32 * q4 * 128);
+          bulk_commit();
+          bulk_wait_read<0>();  // the rows have left shared memory: this warp's share of the stage is free
+        }
+        mbar_arrive(smem_u32(&sm.empty[s]));
+      }
+      __syncwarp();
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+
+  if (!ok) report_error(4u);  // MAMBA_ERR_TIMEOUT
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kSsdTmemCols);
