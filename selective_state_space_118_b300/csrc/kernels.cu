@@ -315,20 +315,26 @@ cudaError_t launch_conv_silu(IoType io, const void* x, const float* conv_w, cons
 }
 
 cudaError_t launch_ssd(const CUtensorMap maps[5], const SsdParams& p, cudaStream_t stream) {
-  const dim3 grid((unsigned)p.heads, (unsigned)p.n_chunks, (unsigned)p.batch);
-  ssd_states_kernel<<<grid, kSsdThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  const long tiles = (long)p.heads * p.n_chunks * p.batch;  // persistent kernels walk the tiles
+  if (tiles >= (1L << 31)) return cudaErrorInvalidValue;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const size_t st_smem = sizeof(StSmem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(ssd_states_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st_smem);
   if (e != cudaSuccess) return e;
-  ssd_pass_kernel<<<dim3(32u / kPassSlices, (unsigned)p.heads, (unsigned)p.batch), 32 * kPassSlices, 0, stream>>>(p);
+  ssd_states_kernel<<<(unsigned)(tiles < 2L * sms ? tiles : 2L * sms), kStThreads, st_smem, stream>>>(maps[0], maps[2],
+                                                                                                     p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t pass_smem = sizeof(PassSmem) + 128;
+  e = cudaFuncSetAttribute(ssd_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pass_smem);
+  if (e != cudaSuccess) return e;
+  ssd_pass_kernel<<<dim3(2u, (unsigned)p.heads, (unsigned)p.batch), kPassThreads, pass_smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(SsdOutSmem) + 1024;
   e = cudaFuncSetAttribute(ssd_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long tiles = (long)p.heads * p.n_chunks * p.batch;  // one CTA per SM, persistent
-  if (tiles >= (1L << 31)) return cudaErrorInvalidValue;
   ssd_output_kernel<<<(unsigned)(tiles < sms ? tiles : sms), kSsdOutThreads, smem, stream>>>(maps[0], maps[1], maps[2],
                                                                                            maps[3], maps[4], p);
   return cudaGetLastError();

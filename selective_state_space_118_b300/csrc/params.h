@@ -83,12 +83,9 @@ struct SsdParams {
   const float* h0;        // (B, H, 16, 64) or null
   void* y;                // (B, L, H, 64) bf16
   float* final_state;     // (B, H, 16, 64) or null
-  // chunk states: each 16 x 64 matrix cut into 32 slices of 32 values
-  // (slice q = 2 n + p / 32 holds state row n, columns 32 (q % 2) .. + 31),
-  // laid out (B, H, 32, n_chunks, 32) so that one slice of every chunk is
-  // contiguous
+  // chunk states, (B, H, n_chunks, 16, 64): one chunk's 16 x 64 state contiguous
   float* S_c;             // each chunk's end state from zero
-  float* S_in;            // the state entering each chunk: (B, H, n_chunks, 16, 64), one chunk's contiguous
+  float* S_in;            // the state entering each chunk
   float* totals;          // (B, H, n_chunks): sum of dt * A (base 2) over each chunk
   float* cum;             // (B, H, n_chunks, 128, 2): per token, the prefix sum of dt * A and dt
   uint64_t timeout_ns;

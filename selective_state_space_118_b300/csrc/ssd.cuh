@@ -9,16 +9,14 @@
 //   Y_diag = (mask(t >= s) * exp(A (cum_t - cum_s)) * dt_s * (C B^T)) X
 //   Y_off  = exp(A cum_t) (C S_in)          (S_in: the state entering the chunk)
 //   S_end  = (exp(A (cum_last - cum_s)) dt_s B_s)^T X + exp(A cum_last) S_in
-// Three kernels: ssd_states_kernel (each chunk's end state from zero, a
-// 16 x 64 product: warp-level mma m16n8k16, 16 rows being below the
-// 5th-generation MMA's smallest M), ssd_pass_kernel (the states entering the
-// chunks, serially per head, in fp32) and ssd_output_kernel (Y_diag + Y_off +
-// D x, gated) on tcgen05: a persistent, warp-specialised pipeline whose three
-// products are 128-row MMAs with the accumulators in tensor memory and the
-// tiles brought in by TMA.  fp32
-// quantities entering a product (the decay-weighted B rows and C B^T
-// entries, the entering state) go in as two bf16 terms (hi + lo, ~16
-// significant bits).
+// Three kernels: ssd_states_kernel (each chunk's end state from zero, the
+// transposed 64 x 16 product on tcgen05), ssd_pass_kernel (the states
+// entering the chunks, serially per head, in fp32) and ssd_output_kernel
+// (Y_diag + Y_off + D x, gated) on tcgen05.  The first and the last are
+// persistent, warp-specialised pipelines: tiles brought in by TMA, 128- or
+// 64-row MMAs with the accumulators in tensor memory.  fp32 quantities
+// entering a product (the decay-weighted B rows and C B^T entries, the
+// entering state) go in as two bf16 terms (hi + lo, ~16 significant bits).
 #pragma once
 #include <cuda_bf16.h>
 
@@ -34,37 +32,6 @@ namespace mamba {
 constexpr int kSsdQ = 128;         // tokens per chunk
 constexpr int kSsdP = 64;          // channels per head
 constexpr int kSsdN = 16;          // d_state
-constexpr int kSsdThreads = 128;   // 4 warps
-constexpr int kXs = kSsdP + 8;     // padded bf16 row of x / state tiles (144 B: ldmatrix rows conflict-free)
-constexpr int kBs = kSsdN + 8;     // padded bf16 row of B / C tiles (48 B)
-
-__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x2_trans(uint32_t (&r)[2], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
-}
 
 // two floats as a bf16 pair (lo in the low half: the smaller column)
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -76,203 +43,411 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
 
-// fp32 pair (a, b) as hi + lo bf16 pairs: hi = bf16(v), lo = bf16(v - hi), so
-// that hi + lo carries ~16 significant bits into a bf16 tensor-core product.
-__device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
-  hi = pack_bf16(a, b);
-  const float2 h = unpack_bf16(hi);
-  lo = pack_bf16(__fsub_rn(a, h.x), __fsub_rn(b, h.y));
+// 16-byte piece `piece` of row `row` in a 128-byte-swizzled tile of 128-byte
+// rows (the tile 1024-byte aligned).
+__device__ __forceinline__ uint32_t sw128(uint32_t base, int row, int piece) {
+  return base + row * 128 + ((piece ^ (row & 7)) << 4);
 }
 
-// A chunk's inputs in shared memory (rows past the sequence's end are zero,
-// with dt = 0: no decay and no input there).
-struct SsdTile {
-  __nv_bfloat16 x[kSsdQ][kXs];
-  __nv_bfloat16 B[kSsdQ][kBs];
-  __nv_bfloat16 C[kSsdQ][kBs];
-  float acum[kSsdQ];  // inclusive cumulative sum of dt * A (base 2) within the chunk
-  float dt[kSsdQ];
+struct SsdTileId {
+  int h, c, b;
 };
 
-// Offset of value (n, p) of a chunk state in the sliced layout: slice
-// q = 2 n + p / 32 of (batch row, head) bh, chunk c.
-__device__ __forceinline__ size_t ssd_slice(size_t bh, int n, int p, int c, int n_chunks) {
-  return ((bh * 32 + (size_t)(2 * n + p / 32)) * n_chunks + c) * 32 + (p % 32);
+// (the host keeps the tile count below 2^31)
+__device__ __forceinline__ SsdTileId ssd_tile(uint32_t t, uint32_t H, uint32_t nC) {
+  SsdTileId id;
+  const uint32_t hc = t / H;
+  id.h = (int)(t - hc * H);
+  id.b = (int)(hc / nC);
+  id.c = (int)(hc - (uint32_t)id.b * nC);
+  return id;
 }
 
-// Loads x, B (and C and z when given) of chunk c of head h, batch row b into
-// shared memory with asynchronous 16-byte copies (zero past the sequence's
-// end), and dt with the decay prefix: computed here (from_cum false), or read
-// from the states kernel's copy.  `more`, run while the copies fly, lets the
-// caller put its own loads in flight too.  Ends with a block barrier.
-template <typename More>
-__device__ __forceinline__ void ssd_load_tile(const SsdParams& p, SsdTile& s, int b, int h, int c, bool with_c,
-                                              bool from_cum, __nv_bfloat16 (*zt)[kXs], More more) {
-  const int tid = threadIdx.x;
-  const int t0 = c * kSsdQ;
-  const int H = p.heads, G = p.groups, L = p.seqlen;
-  const int g = h / (H / G);
-  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(p.x);
-  const __nv_bfloat16* zb = static_cast<const __nv_bfloat16*>(p.z);
-  // x (and z): 64 rows of 128 bytes = 8 pieces of 16 bytes each
-  for (int i = tid; i < kSsdQ * 8; i += kSsdThreads) {
-    const int r = i >> 3, q = i & 7;
-    const int t = t0 + r;
-    const bool in = t < L;
-    const size_t o = (((size_t)b * L + (in ? t : 0)) * H + h) * kSsdP + q * 8;
-    cp_async16(smem_u32(&s.x[r][q * 8]), xb + o, in);
-    if (zt) cp_async16(smem_u32(&zt[r][q * 8]), zb + o, in);
-  }
-  // B (and C): 64 rows of 32 bytes = 2 pieces each
-  const __nv_bfloat16* Bb = static_cast<const __nv_bfloat16*>(p.Bm);
-  const __nv_bfloat16* Cb = static_cast<const __nv_bfloat16*>(p.Cm);
-  for (int i = tid; i < kSsdQ * 2; i += kSsdThreads) {
-    const int r = i >> 1, q = i & 1;
-    const int t = t0 + r;
-    const bool in = t < L;
-    const size_t o = (((size_t)b * L + (in ? t : 0)) * G + g) * kSsdN + q * 8;
-    cp_async16(smem_u32(&s.B[r][q * 8]), Bb + o, in);
-    if (with_c) cp_async16(smem_u32(&s.C[r][q * 8]), Cb + o, in);
-  }
-  more();
-  if (from_cum) {  // dt and the decay prefix as the states kernel computed them
-    if (tid < kSsdQ) {
-      const float2 v = reinterpret_cast<const float2*>(p.cum)[(((size_t)b * H + h) * p.n_chunks + c) * kSsdQ + tid];
-      s.acum[tid] = v.x;
-      s.dt[tid] = v.y;
-    }
-    cp_async_wait_all();
-    __syncthreads();
-    return;
-  }
-  // dt and dt * A, then the inclusive prefix sum over the chunk's tokens:
-  // per warp, then each warp adds the totals of the warps before it
-  if (tid < kSsdQ) {
-    const float A2 = a2_from_log(p.A_log[h]);  // A log2(e)
-    const int t = t0 + tid;
-    float dt = 0.0f;
-    if (t < L) dt = softplus(to_f32(static_cast<const __nv_bfloat16*>(p.dt_raw)[((size_t)b * L + t) * H + h]));
-    s.dt[tid] = dt;
-    float v = __fmul_rn(dt, A2);  // in base 2
-    const int lane = tid & 31;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float u = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v = __fadd_rn(v, u);
-    }
-    s.acum[tid] = v;
-  }
-  cp_async_wait_all();
-  __syncthreads();
-  const int w = tid >> 5;
-  float off = 0.0f;  // the earlier warps' totals, read before any is updated
-  if (tid < kSsdQ)
-    for (int k = 0; k < w; ++k) off = __fadd_rn(off, s.acum[32 * k + 31]);
-  __syncthreads();
-  if (tid < kSsdQ && w > 0) s.acum[tid] = __fadd_rn(s.acum[tid], off);
-  __syncthreads();
+// v (two fp32 values) as hi + lo bf16 pairs, packed arithmetic.
+__device__ __forceinline__ void split_bf16_x2(float2 v, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(v.x, v.y);
+  const float2 h = unpack_bf16(hi);
+  const float2 d = __ffma2_rn(h, make_float2(-1.0f, -1.0f), v);  // v - h, exactly rounded
+  lo = pack_bf16(d.x, d.y);
 }
 
 // ---------------------------------------------------------------- chunk end states
-// S_c[n][p] = sum_j 2^(acum_last - acum_j) dt_j B_j[n] x_j[p]: a 16 x 64 product
-// over the chunk's tokens; warp w computes columns 16w .. 16w + 15.
-// grid (H, n_chunks, B), 128 threads.
-__global__ void __launch_bounds__(kSsdThreads) ssd_states_kernel(const __grid_constant__ SsdParams p) {
-  __shared__ __align__(128) SsdTile s;
-  __shared__ float wj[kSsdQ];
-  const int h = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
-  ssd_load_tile(p, s, b, h, c, false, false, nullptr, [] {});
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float last = s.acum[kSsdQ - 1];
-  if (tid < kSsdQ) wj[tid] = __fmul_rn(ex2_approx(__fsub_rn(last, s.acum[tid])), s.dt[tid]);
-  const size_t bh = (size_t)b * p.heads + h;
-  const size_t chunk = bh * p.n_chunks + c;
-  if (tid == 0) p.totals[chunk] = last;
-  if (tid < kSsdQ)  // the output kernel's copy of the chunk's dt and decay prefix
-    reinterpret_cast<float2*>(p.cum)[chunk * kSsdQ + tid] = make_float2(s.acum[tid], s.dt[tid]);
-  __syncthreads();
+// S_c[n][p] = sum_j 2^(acum_last - acum_j) dt_j B_j[n] x_j[p], each chunk's end
+// state from zero, as the transposed product S_c^T = X^T (w o B): M = 64
+// channels, N = 16 states, K = 128 tokens on tcgen05 (M = 64: accumulator row
+// m in tensor-memory lane 32 (m / 16) + m % 16), the weights w_j =
+// 2^(acum_last - acum_j) dt_j applied to the B rows, which enter as hi + lo
+// bf16 terms.  A persistent kernel, two CTAs per SM, tiles (head, chunk,
+// batch row) with the head fastest:
+//   warp 0      loads x (128 tokens x 64 channels, 128-byte swizzle: the
+//               MN-major A operand) and B (128 x 16, 32-byte swizzle) of tile
+//               k into stage k % 3 by TMA;
+//   warp 1      issues the 16 MMAs of tile k into accumulator k % 4 once its
+//               weighted-B operand is written, freeing the stage;
+//   warps 4-11  two groups of four warps, group g taking the tiles k with
+//               k % 2 = g (the per-tile work is a chain of dependent steps:
+//               two chains in flight per CTA).  Thread j = token j:
+//               softplus(dt), the chunk's decay prefix (warp scans, then the
+//               earlier warps' totals), the weight, w_j B_j as hi + lo into
+//               the K-major operand, the chunk's (prefix, dt) pairs and total
+//               for the later kernels; then the accumulator of the group's
+//               previous tile out of tensor memory into S_c.
+constexpr int kStStages = 3;
+constexpr int kStGroups = 2;
+constexpr int kStThreads = 128 + 128 * kStGroups;
+constexpr int kStBufs = 2 * kStGroups;  // weighted-B operands and accumulators (16 columns each)
 
-  const int g = lane >> 2, t = lane & 3;
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-  for (int kb = 0; kb < kSsdQ / 16; ++kb) {
-    // A = (w o B)^T (16 states x 16 tokens): B^T through a transposing load
-    uint32_t a[4];
-    {
-      const int r = lane & 7, m = lane >> 3;  // matrix m: states (m & 1) * 8, tokens (m >> 1) * 8
-      ldsm_x4_trans(a, smem_u32(&s.B[kb * 16 + (m >> 1) * 8 + r][(m & 1) * 8]));
+struct StStage {
+  __nv_bfloat16 x[kSsdQ * kSsdP];  // rows of 128 bytes
+  __nv_bfloat16 b[kSsdQ * kSsdN];  // rows of 32 bytes
+  unsigned char pad[3072];         // keeps the next stage's x 1024-byte aligned
+};
+static_assert(sizeof(StStage) % 1024 == 0, "stage alignment");
+
+struct StSmem {
+  StStage st[kStStages];
+  __nv_bfloat16 whi[kStBufs][2][kSsdN * 64];  // [buffer][K half]: rows n of 64 tokens (128 bytes)
+  __nv_bfloat16 wlo[kStBufs][2][kSsdN * 64];
+  float wsum[kStGroups][4];                   // per group: its warps' dt A totals
+  uint64_t full[kStStages], empty[kStStages];
+  uint64_t wb_full[kStBufs], wb_empty[kStBufs], acc_full[kStBufs], acc_empty[kStBufs];
+  uint32_t tmem_base;
+};
+
+// The 128 threads of compute group g (named barrier 1 + g) agree on a predicate.
+__device__ __forceinline__ bool group_all(int g, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(1 + g)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void group_sync(int g) { asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory"); }
+
+// 32-byte-swizzled tile of 32-byte rows: 16-byte chunk c of row r.
+__device__ __forceinline__ uint32_t sw32(uint32_t base, int r, int c) {
+  return base + r * 32 + ((c ^ ((r >> 2) & 1)) << 4);
+}
+
+__global__ void __launch_bounds__(kStThreads, 2)
+    ssd_states_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
+                      const __grid_constant__ SsdParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  StSmem& sm = *reinterpret_cast<StSmem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = p.heads, nC = p.n_chunks, L = p.seqlen;
+  const uint32_t tiles = (uint32_t)H * nC * p.batch;
+  const uint32_t n_mine = (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStStages; ++s) {
+      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), 1);
     }
-    // w o B in fp32, as two bf16 terms (hi + lo) so that the product keeps ~16 bits
-    uint32_t ahi[4], alo[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int k = kb * 16 + (q >> 1) * 8 + 2 * t;  // tokens of this register's pair
-      const float2 v = unpack_bf16(a[q]);
-      split_bf16(__fmul_rn(v.x, wj[k]), __fmul_rn(v.y, wj[k + 1]), ahi[q], alo[q]);
+    for (int w = 0; w < kStBufs; ++w) {
+      mbar_init(smem_u32(&sm.wb_full[w]), 4);  // one arrival per warp of the group
+      mbar_init(smem_u32(&sm.wb_empty[w]), 1);
+      mbar_init(smem_u32(&sm.acc_full[w]), 1);
+      mbar_init(smem_u32(&sm.acc_empty[w]), 4);
     }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      uint32_t bx[2];
-      ldsm_x2_trans(bx, smem_u32(&s.x[kb * 16 + (lane & 15)][warp * 16 + nt * 8]));
-      mma_16816(acc[nt], ahi, bx[0], bx[1]);
-      mma_16816(acc[nt], alo, bx[0], bx[1]);
-    }
+    fence_mbar_init();
+    prefetch_tensormap(&tm_x);
+    prefetch_tensormap(&tm_b);
   }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 16 * kStBufs);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  bool ok = true;
+
+  if (warp == 0) {
+    if (lane == 0) {  // producer
+      uint32_t k = 0;
+      for (; k < n_mine; ++k) {
+        const int s = (int)(k % kStStages);
+        if (!mbar_wait_bounded(smem_u32(&sm.empty[s]), ((k / kStStages) & 1u) ^ 1u, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        const SsdTileId id = ssd_tile(blockIdx.x + k * gridDim.x, H, nC);
+        const int g = id.h / (H / p.groups), t0 = id.c * kSsdQ;
+        const uint32_t bar = smem_u32(&sm.full[s]);
+        mbar_arrive_expect_tx(bar, kSsdQ * kSsdP * 2 + kSsdQ * kSsdN * 2);
+        tma_load_4d(smem_u32(sm.st[s].x), &tm_x, 0, id.h, t0, id.b, bar);
+        tma_load_4d(smem_u32(sm.st[s].b), &tm_b, 0, g, t0, id.b, bar);
+      }
+      for (uint32_t j = k > kStStages ? k - kStStages : 0; j < k; ++j)
+        if (!mbar_wait_bounded(smem_u32(&sm.full[j % kStStages]), (j / kStStages) & 1u, p.timeout_ns)) ok = false;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      const uint32_t idesc = umma_idesc_bf16(64, 16, false) | (1u << 15);  // A (x^T) MN-major, B K-major
+      for (uint32_t k = 0; k < n_mine; ++k) {
+        const int s = (int)(k % kStStages);
+        const uint32_t w = k % kStBufs, ph = (k / kStBufs) & 1u;
+        if (!mbar_wait_bounded(smem_u32(&sm.wb_full[w]), ph, p.timeout_ns) ||
+            !mbar_wait_bounded(smem_u32(&sm.full[s]), (k / kStStages) & 1u, p.timeout_ns) ||
+            !mbar_wait_bounded(smem_u32(&sm.acc_empty[w]), ph ^ 1u, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + w * 16;
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    const int col = warp * 16 + nt * 8 + 2 * t;
-    *reinterpret_cast<float2*>(p.S_c + ssd_slice(bh, g, col, c, p.n_chunks)) = make_float2(acc[nt][0], acc[nt][1]);
-    *reinterpret_cast<float2*>(p.S_c + ssd_slice(bh, g + 8, col, c, p.n_chunks)) =
-        make_float2(acc[nt][2], acc[nt][3]);
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t ad = umma_desc(smem_u32(sm.st[s].x) + (kh * 64 + ks * 16) * 128, 1024, 2);  // 16 tokens
+              const uint32_t wb = smem_u32(part == 0 ? sm.whi[w][kh] : sm.wlo[w][kh]);
+              tc_mma_f16(d, ad, umma_desc(wb + 32 * ks, 1024, 2), idesc, (part | kh | ks) != 0);
+            }
+        tc_commit(smem_u32(&sm.acc_full[w]));
+        tc_commit(smem_u32(&sm.wb_empty[w]));
+        tc_commit(smem_u32(&sm.empty[s]));
+      }
+    }
+  } else if (warp >= 4) {  // compute groups
+    const int grp = (warp - 4) >> 2, cw = warp & 3;
+    const int j = 32 * cw + lane;  // token of the chunk
+    const unsigned short* dtr16 = static_cast<const unsigned short*>(p.dt_raw);
+    // this thread's dt_raw (bf16 bits, converted at use) and the head's
+    // A_log of tile k: plain loads, no select on their values (which would
+    // wait for them here); tokens past the sequence's end read the last one
+    // and are masked at use
+    auto inputs_of = [&](uint32_t k) -> uint2 {
+      const SsdTileId id = ssd_tile(blockIdx.x + (k < n_mine ? k : 0) * gridDim.x, H, nC);
+      const int t = min(id.c * kSsdQ + j, L - 1);
+      return make_uint2((uint32_t)__ldg(dtr16 + ((size_t)id.b * L + t) * H + id.h),
+                        __float_as_uint(__ldg(p.A_log + id.h)));
+    };
+    // the accumulator of tile kk out of tensor memory into S_c: lanes 0..15
+    // of warp q hold channels 16 q .. + 15, 16 states each
+    auto drain = [&](uint32_t kk) -> bool {
+      const uint32_t w = kk % kStBufs;
+      if (!group_all(grp, mbar_wait_bounded(smem_u32(&sm.acc_full[w]), (kk / kStBufs) & 1u, p.timeout_ns)))
+        return false;
+      tc_fence_after();
+      uint32_t r[16];
+      tmem_ld_16cols(tmem + ((uint32_t)(32 * cw) << 16) + w * 16, r);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.acc_empty[w]));
+      if (lane < 16) {
+        const SsdTileId id = ssd_tile(blockIdx.x + kk * gridDim.x, H, nC);
+        const int col = 16 * cw + lane;  // channel
+        float* dst = p.S_c + (((size_t)id.b * H + id.h) * nC + id.c) * (kSsdN * kSsdP) + col;
+#pragma unroll
+        for (int n = 0; n < kSsdN; ++n) dst[n * kSsdP] = __uint_as_float(r[n]);
+      }
+      return true;
+    };
+    uint2 in = inputs_of(grp);
+    uint32_t k = grp;
+    for (; k < n_mine; k += kStGroups) {
+      const int s = (int)(k % kStStages);
+      const uint32_t w = k % kStBufs;
+      const SsdTileId id = ssd_tile(blockIdx.x + k * gridDim.x, H, nC);
+      const uint2 in_next = inputs_of(k + kStGroups);  // in flight through this tile
+      const bool mine = mbar_wait_bounded(smem_u32(&sm.full[s]), (k / kStStages) & 1u, p.timeout_ns) &&
+                        mbar_wait_bounded(smem_u32(&sm.wb_empty[w]), ((k / kStBufs) & 1u) ^ 1u, p.timeout_ns);
+      if (!group_all(grp, mine)) {
+        ok = false;
+        break;
+      }
+      // dt and the inclusive prefix of dt A (base 2) over the chunk: per
+      // warp, then each warp adds the totals of the warps before it
+      const float A2 = a2_from_log(__uint_as_float(in.y));
+      const int t = id.c * kSsdQ + j;
+      const float dt = t < L ? softplus(__uint_as_float(in.x << 16)) : 0.0f;
+      float v = __fmul_rn(dt, A2);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v = __fadd_rn(v, u);
+      }
+      if (lane == 31) sm.wsum[grp][cw] = v;
+      group_sync(grp);
+      float off = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 3; ++q)
+        if (q < cw) off = __fadd_rn(off, sm.wsum[grp][q]);
+      const float acum = cw > 0 ? __fadd_rn(v, off) : v;
+      // the last token's prefix, by the same sums in the same order as its
+      // own: warp 3's scan plus the totals of warps 0..2
+      float last = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 3; ++q) last = __fadd_rn(last, sm.wsum[grp][q]);
+      last = __fadd_rn(sm.wsum[grp][3], last);
+      const float wj = __fmul_rn(ex2_approx(__fsub_rn(last, acum)), dt);
+      const size_t chunk = ((size_t)id.b * H + id.h) * nC + id.c;
+      reinterpret_cast<float2*>(p.cum)[chunk * kSsdQ + j] = make_float2(acum, dt);
+      if (j == kSsdQ - 1) p.totals[chunk] = acum;
+      // w_j B_j (16 states) as hi + lo into the K-major operand: row n, token j
+      {
+        const StStage& st = sm.st[s];
+        uint4 b0, b1;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(b0.x), "=r"(b0.y), "=r"(b0.z), "=r"(b0.w)
+                     : "r"(sw32(smem_u32(st.b), j, 0)));
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(b1.x), "=r"(b1.y), "=r"(b1.z), "=r"(b1.w)
+                     : "r"(sw32(smem_u32(st.b), j, 1)));
+        const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const int kh = j >> 6, jj = j & 63;
+        const uint32_t hb = smem_u32(sm.whi[w][kh]), lb = smem_u32(sm.wlo[w][kh]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float2 bv = unpack_bf16(bw[e]);
+          uint32_t hi, lo;
+          split_bf16_x2(__fmul2_rn(bv, make_float2(wj, wj)), hi, lo);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int n = 2 * e + u;
+            const uint32_t off16 = sw128(0, n, jj >> 3) + (jj & 7) * 2;
+            const uint16_t hv = (uint16_t)(u ? hi >> 16 : hi & 0xffffu);
+            const uint16_t lv = (uint16_t)(u ? lo >> 16 : lo & 0xffffu);
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(hb + off16), "h"(hv) : "memory");
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(lb + off16), "h"(lv) : "memory");
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.wb_full[w]));
+      in = in_next;
+      if (k >= (uint32_t)kStGroups && !drain(k - kStGroups)) {  // the group's previous tile
+        ok = false;
+        break;
+      }
+    }
+    if (ok && k >= (uint32_t)kStGroups && !drain(k - kStGroups)) ok = false;  // the group's last tile
+  }
+
+  if (!ok) report_error(4u);  // MAMBA_ERR_TIMEOUT
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 16 * kStBufs);
   }
 }
 
 // ---------------------------------------------------------------- state passing
 // The state entering chunk c: S_in[0] = h0 (or 0), S_in[c + 1] = 2^(total_c)
-// S_in[c] + S_c[c], in fp32.  One thread per state value walks the chunks in
-// order; a warp holds one slice (32 values), so each step's loads and stores
-// are 128 contiguous bytes (S_in is written one chunk's state contiguous, for
-// the output kernel's bulk copy), and each thread keeps kPassAhead chunks' loads in
-// flight (the chain itself is one fma per chunk).  The chunks' decay factors
-// 2^(total) are staged in shared memory, kPassBlock at a time.
-// grid (32 / kPassSlices, H, B), 32 * kPassSlices threads.
-constexpr int kPassSlices = 4;
-constexpr int kPassAhead = 16;
-constexpr int kPassBlock = 512;
+// S_in[c] + S_c[c], in fp32.  Two CTAs per (batch row, head), each walking
+// the chunks in order over half of the head's 16 x 64 state, one thread per
+// value.  The halves of S_c come in by bulk copies, kPassRing chunks ahead
+// (the per-SM limit on outstanding cache misses would hold plain loads to a
+// fraction of the bandwidth), and S_in leaves by bulk stores from a staging
+// ring, kPassGroup chunks per step; the chain itself is one fma per value and
+// chunk.  The chunks' decay factors 2^(total) are staged in shared memory,
+// kPassBlock at a time.
+constexpr int kPassThreads = kSsdN * kSsdP / 2;
+constexpr int kPassRing = 32;
+constexpr int kPassGroup = 4;                 // chunks per step (one barrier, one bulk group)
+constexpr int kPassStage = 3 * kPassGroup;    // staging slots: three steps' worth
+constexpr int kPassBlock = 1024;
 
-__global__ void __launch_bounds__(32 * kPassSlices) ssd_pass_kernel(const __grid_constant__ SsdParams p) {
-  __shared__ float fac[kPassBlock];
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int q = blockIdx.x * kPassSlices + (tid >> 5);  // this warp's slice
+struct PassSmem {
+  float ring[kPassRing][kPassThreads];
+  float out[kPassStage][kPassThreads];
+  float fac[kPassBlock];
+  uint64_t full[kPassRing];
+};
+
+__global__ void __launch_bounds__(kPassThreads) ssd_pass_kernel(const __grid_constant__ SsdParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  PassSmem& sm = *reinterpret_cast<PassSmem*>(smem_raw + smem_pad128(smem_raw));
+  const int half = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x;
   const size_t bh = (size_t)b * p.heads + h;
   const int nC = p.n_chunks;
-  const int n = q / 2, col = 32 * (q % 2) + lane;  // this thread's state value (row n, column col)
-  const float* src = p.S_c + (bh * 32 + q) * (size_t)nC * 32 + lane;
-  float* dst = p.S_in + (bh * nC * 32 + q) * 32 + lane;  // S_in: each chunk's 16 x 64 state contiguous
+  constexpr int kStep = kSsdN * kSsdP;  // floats per chunk state
+  constexpr uint32_t kBytes = kPassThreads * 4;
+  const float* src = p.S_c + bh * nC * kStep + half * kPassThreads;
+  float* dst = p.S_in + bh * nC * kStep + half * kPassThreads;
   const float* tot = p.totals + bh * nC;
-  float S = p.h0 ? p.h0[bh * kSsdN * kSsdP + n * kSsdP + col] : 0.0f;
-  float ahead[kPassAhead];
-#pragma unroll
-  for (int k = 0; k < kPassAhead; ++k) ahead[k] = k < nC ? __ldcs(src + (size_t)k * 32) : 0.0f;
-  for (int c0 = 0; c0 < nC; c0 += kPassAhead) {
-    if (c0 % kPassBlock == 0) {  // the next block of decay factors
-      __syncthreads();
-      for (int i = tid; i < kPassBlock && c0 + i < nC; i += 32 * kPassSlices) fac[i] = ex2_approx(__ldg(tot + c0 + i));
-      __syncthreads();
-    }
-#pragma unroll
-    for (int k = 0; k < kPassAhead; ++k) {
-      const int c = c0 + k;
-      if (c < nC) {
-        __stcs(dst + (size_t)c * kSsdN * kSsdP, S);
-        const float v = ahead[k];
-        if (c + kPassAhead < nC) ahead[k] = __ldcs(src + (size_t)(c + kPassAhead) * 32);
-        S = __fmaf_rn(fac[c % kPassBlock], S, v);
-      }
+  if (tid == 0) {
+    for (int r = 0; r < kPassRing; ++r) mbar_init(smem_u32(&sm.full[r]), 1);
+    fence_mbar_init();
+    for (int c = 0; c < kPassRing && c < nC; ++c) {
+      mbar_arrive_expect_tx(smem_u32(&sm.full[c]), kBytes);
+      bulk_load(smem_u32(sm.ring[c]), src + (size_t)c * kStep, kBytes, smem_u32(&sm.full[c]));
     }
   }
-  if (p.final_state) p.final_state[bh * kSsdN * kSsdP + n * kSsdP + col] = S;
+  __syncthreads();
+  float S = p.h0 ? p.h0[bh * kStep + half * kPassThreads + tid] : 0.0f;
+  bool ok = true;
+  int c0 = 0;
+  for (int step = 0; c0 < nC; ++step, c0 += kPassGroup) {
+    if (c0 % kPassBlock == 0) {  // the next block of decay factors (the last block's reads are behind a barrier)
+      for (int i = tid; i < kPassBlock && c0 + i < nC; i += kPassThreads) sm.fac[i] = ex2_approx(__ldg(tot + c0 + i));
+      __syncthreads();
+    }
+    bool mine = true;
+#pragma unroll
+    for (int u = 0; u < kPassGroup; ++u) {
+      const int c = c0 + u;
+      if (c < nC) mine = mine && mbar_wait_bounded(smem_u32(&sm.full[c % kPassRing]), (c / kPassRing) & 1u, p.timeout_ns);
+    }
+    if (!__syncthreads_and(mine)) {
+      ok = false;
+      break;
+    }
+    const int o0 = (step % 3) * kPassGroup;
+#pragma unroll
+    for (int u = 0; u < kPassGroup; ++u) {
+      const int c = c0 + u;
+      if (c < nC) {
+        const float v = sm.ring[c % kPassRing][tid];
+        sm.out[o0 + u][tid] = S;
+        S = __fmaf_rn(sm.fac[c % kPassBlock], S, v);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();  // the ring slots are read and the staging slots written by every thread
+    if (tid == 0) {
+#pragma unroll
+      for (int u = 0; u < kPassGroup; ++u) {
+        const int c = c0 + u;
+        if (c < nC) bulk_store(dst + (size_t)c * kStep, smem_u32(sm.out[o0 + u]), kBytes);
+      }
+      bulk_commit();
+#pragma unroll
+      for (int u = 0; u < kPassGroup; ++u) {
+        const int c = c0 + u;
+        if (c + kPassRing < nC) {
+          mbar_arrive_expect_tx(smem_u32(&sm.full[c % kPassRing]), kBytes);
+          bulk_load(smem_u32(sm.ring[c % kPassRing]), src + (size_t)(c + kPassRing) * kStep, kBytes,
+                    smem_u32(&sm.full[c % kPassRing]));
+        }
+      }
+      // the stores of the step before have left shared memory: their staging
+      // slots are written two steps on, after the next step's barrier
+      bulk_wait_read<1>();
+    }
+  }
+  if (tid == 0) {
+    bulk_wait_all();
+    if (!ok) report_error(4u);  // MAMBA_ERR_TIMEOUT
+    // every load issued has landed before the CTA may end: chunks below
+    // min(nC, c0 + kPassRing), the last of each ring slot
+    const int issued = min(nC, c0 + kPassRing);
+    for (int cc = issued > kPassRing ? issued - kPassRing : 0; cc < issued; ++cc)
+      mbar_wait_bounded(smem_u32(&sm.full[cc % kPassRing]), (cc / kPassRing) & 1u, p.timeout_ns);
+  }
+  if (ok && p.final_state) p.final_state[bh * kStep + half * kPassThreads + tid] = S;
 }
 
 // ---------------------------------------------------------------- output
@@ -335,26 +510,6 @@ struct SsdOutSmem {
   uint32_t tmem_base;
 };
 
-// 16-byte piece `piece` of row `row` in a 128-byte-swizzled tile of 128-byte
-// rows (the tile 1024-byte aligned).
-__device__ __forceinline__ uint32_t sw128(uint32_t base, int row, int piece) {
-  return base + row * 128 + ((piece ^ (row & 7)) << 4);
-}
-
-struct SsdTileId {
-  int h, c, b;
-};
-
-// (the host keeps the tile count below 2^31)
-__device__ __forceinline__ SsdTileId ssd_tile(uint32_t t, uint32_t H, uint32_t nC) {
-  SsdTileId id;
-  const uint32_t hc = t / H;
-  id.h = (int)(t - hc * H);
-  id.b = (int)(hc / nC);
-  id.c = (int)(hc - (uint32_t)id.b * nC);
-  return id;
-}
-
 // silu(z) = z sigmoid(z) = h + h tanh(h), h = z / 2: one MUFU operation per
 // value (tanh.approx, relative error about 2^-11, which moves silu by at most
 // about |h| 2^-11 -- below a bf16 output's half ulp relative to the gated
@@ -368,14 +523,6 @@ __device__ __forceinline__ float tanh_approx(float x) {
 __device__ __forceinline__ float2 silu_tanh_x2(float2 z) {
   const float2 h = __fmul2_rn(z, make_float2(0.5f, 0.5f));
   return __ffma2_rn(h, make_float2(tanh_approx(h.x), tanh_approx(h.y)), h);
-}
-
-// v (two fp32 values) as hi + lo bf16 pairs, packed arithmetic.
-__device__ __forceinline__ void split_bf16_x2(float2 v, uint32_t& hi, uint32_t& lo) {
-  hi = pack_bf16(v.x, v.y);
-  const float2 h = unpack_bf16(hi);
-  const float2 d = __ffma2_rn(h, make_float2(-1.0f, -1.0f), v);  // v - h, exactly rounded
-  lo = pack_bf16(d.x, d.y);
 }
 
 // The Y half kh of tile kk (and, with the second half, Yo): MMAs into d.
