@@ -639,11 +639,27 @@ __global__ void __launch_bounds__(kSsdOutThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer: G of tile kg, Y halves of tiles ky0, ky1, each as soon as it may go
+      // (polled without sleeping, the Y halves first: they gate the epilogue)
       const uint32_t ig = umma_idesc_bf16(128, 128, false);  // G = C B^T: both K-major
       uint32_t kg = 0, ky0 = 0, ky1 = 0;
       uint64_t idle_since = globaltimer_ns();
       while (ky1 < n_mine) {
         bool moved = false;
+        if (ky1 < ky0 && mbar_test_wait(smem_u32(&sm.gop_full[1]), ky1 & 1u)) {
+          tc_fence_after();
+          ssd_issue_y(sm, sm.st[ky1 % kSsdStages], tmem + (ky1 % kSsdAcc) * 128, 1);
+          tc_commit(smem_u32(&sm.gop_empty[1]));
+          tc_commit(smem_u32(&sm.yfull[ky1 % kSsdAcc]));
+          ++ky1;
+          moved = true;
+        }
+        if (ky0 < kg && mbar_test_wait(smem_u32(&sm.gop_full[0]), ky0 & 1u)) {
+          tc_fence_after();
+          ssd_issue_y(sm, sm.st[ky0 % kSsdStages], tmem + (ky0 % kSsdAcc) * 128, 0);
+          tc_commit(smem_u32(&sm.gop_empty[0]));
+          ++ky0;
+          moved = true;
+        }
         if (kg < n_mine && mbar_test_wait(smem_u32(&sm.full[kg % kSsdStages]), (kg / kSsdStages) & 1u) &&
             mbar_test_wait(smem_u32(&sm.tmem_empty[kg % kSsdAcc]), ((kg / kSsdAcc) & 1u) ^ 1u)) {
           tc_fence_after();
@@ -654,21 +670,6 @@ __global__ void __launch_bounds__(kSsdOutThreads, 1)
           ++kg;
           moved = true;
         }
-        if (ky0 < kg && mbar_test_wait(smem_u32(&sm.gop_full[0]), ky0 & 1u)) {
-          tc_fence_after();
-          ssd_issue_y(sm, sm.st[ky0 % kSsdStages], tmem + (ky0 % kSsdAcc) * 128, 0);
-          tc_commit(smem_u32(&sm.gop_empty[0]));
-          ++ky0;
-          moved = true;
-        }
-        if (ky1 < ky0 && mbar_test_wait(smem_u32(&sm.gop_full[1]), ky1 & 1u)) {
-          tc_fence_after();
-          ssd_issue_y(sm, sm.st[ky1 % kSsdStages], tmem + (ky1 % kSsdAcc) * 128, 1);
-          tc_commit(smem_u32(&sm.gop_empty[1]));
-          tc_commit(smem_u32(&sm.yfull[ky1 % kSsdAcc]));
-          ++ky1;
-          moved = true;
-        }
         if (moved) {
           idle_since = globaltimer_ns();
         } else {
@@ -676,7 +677,6 @@ __global__ void __launch_bounds__(kSsdOutThreads, 1)
             ok = false;
             break;
           }
-          __nanosleep(20);
         }
       }
     }
