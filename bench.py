@@ -304,6 +304,34 @@ def compute_roofline(elems_per_s, elems_per_step, t_step_s):
                     "16 decays per element need 16 MUFU slots for 8 bytes"}
 
 
+# The backward's instruction mix, measured by ncu on the reverse-sweep kernel
+# (L = 4096, the Jamba width): warp-instructions per warp-token (one warp, its
+# 32 channels, one token) and the MUFU share of them.
+BWD_WARP_INSTR_PER_WARP_TOKEN = 457
+BWD_MUFU_SHARE = 0.12
+
+
+def bwd_compute_floor(elems, t_s):
+    """Two floors of the backward at its measured instruction mix: issue (one
+    warp-instruction per scheduler per clock, four schedulers per SM) and the
+    MUFU's (its instructions at 16 per clock per SM, the reciprocal's rate;
+    ex2 runs at twice that)."""
+    sms, mhz = 148, 2032.0
+    try:
+        props = torch.cuda.get_device_properties(torch.cuda.current_device())
+        sms = props.multi_processor_count
+    except Exception:
+        pass
+    per_elem = BWD_WARP_INSTR_PER_WARP_TOKEN / 32.0  # warp-instructions per element
+    issue_s = elems * per_elem / (4 * sms * mhz * 1e6)
+    mufu_s = elems * per_elem * BWD_MUFU_SHARE * 32 / (16 * sms * mhz * 1e6)
+    return {"what": "issue and MUFU floors at the measured instruction mix",
+            "warp_instructions_per_warp_token": BWD_WARP_INSTR_PER_WARP_TOKEN, "mufu_share": BWD_MUFU_SHARE,
+            "issue_floor_ms": issue_s * 1e3, "issue_frac": issue_s / t_s,
+            "mufu_floor_ms": mufu_s * 1e3, "mufu_frac": mufu_s / t_s,
+            "sm_clock_mhz_assumed": mhz}
+
+
 def bench_prefill(w, steps, warmup, world, local, n_chunks_req=0, inp=None, slices=None):
     from selective_state_space_118_b300 import ops
     dev = torch.device("cuda", local)
@@ -496,6 +524,7 @@ def bench_backward(w, steps, warmup, local, n_chunks_req=0):
            "roofline": {"bound": "issue", "hbm_achieved": alg / t / 1e9, "hbm_peak": hbm, "unit": "GB/s",
                         "hbm_frac": alg / t / 1e9 / hbm, "peak_source": src,
                         "algorithmic_bytes_per_call": alg,
+                        "compute": bwd_compute_floor(B * L * D, t),
                         "note": "instruction-issue bound (forward recomputed from tile checkpoints, "
                                 "then the reverse sweep); the HBM fraction is context"},
            "gpu_launches": launches * steps, "clocks": clk.summary(), "tile_state_reuse": reuse}
