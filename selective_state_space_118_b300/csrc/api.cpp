@@ -389,11 +389,13 @@ mamba_status launch_forward(const mamba_scan_args* a, const Plan& pl, const Work
 
   if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, bc_ld, stream) != cudaSuccess)
     return MAMBA_ERR_CUDA;
-  if (pl.n_chunks > 1) {
+  if (pl.n_chunks > 1) {  // carries and main pass in one launch, the carry tasks first
     if (cudaMemsetAsync(p.counters, 0, ws.counters_bytes, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
-    const CUtensorMap smaps[3] = {maps[0], maps[2], maps[4]};  // x, dt_raw, B/C rows
-    dim3 g1((unsigned)((size_t)(pl.n_chunks - 1) * p.n_groups * B));
-    if (mamba::launch_summary(io, smaps, p, g1, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+    const size_t per = (size_t)p.n_groups * B;
+    const size_t ctas = (2 * (size_t)pl.n_chunks - 1) * per;
+    if (ctas >= (1u << 31)) return MAMBA_ERR_UNSUPPORTED;
+    if (mamba::launch_scan_fused(io, maps, p, (unsigned)ctas, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+    return MAMBA_OK;
   }
   dim3 g2((unsigned)p.n_groups, (unsigned)B, (unsigned)pl.n_chunks);
   if (mamba::launch_scan(io, maps, p, g2, stream) != cudaSuccess) return MAMBA_ERR_CUDA;

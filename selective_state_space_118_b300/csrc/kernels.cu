@@ -36,6 +36,27 @@ static cudaError_t launch_scan_t(const CUtensorMap* m, const ScanParams& p, dim3
   return p.y != nullptr ? launch_scan_y<IO, true>(m, p, grid, s) : launch_scan_y<IO, false>(m, p, grid, s);
 }
 
+template <typename IO, bool kY>
+static cudaError_t launch_fused_y(const CUtensorMap* m, const ScanParams& p, unsigned ctas, cudaStream_t s) {
+  const size_t smem = fused_smem_bytes<IO>() + 128;
+  cudaError_t e = cudaFuncSetAttribute(scan_fused_kernel<IO, kY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  scan_fused_kernel<IO, kY><<<ctas, kLanes, smem, s>>>(m[0], m[1], m[2], m[3], p);
+  return cudaGetLastError();
+}
+
+template <typename IO>
+static cudaError_t launch_fused_t(const CUtensorMap* m, const ScanParams& p, unsigned ctas, cudaStream_t s) {
+  return p.y != nullptr ? launch_fused_y<IO, true>(m, p, ctas, s) : launch_fused_y<IO, false>(m, p, ctas, s);
+}
+
+cudaError_t launch_scan_fused(IoType io, const CUtensorMap maps[4], const ScanParams& p, unsigned ctas,
+                              cudaStream_t stream) {
+  return io == IoType::BF16 ? launch_fused_t<__nv_bfloat16>(maps, p, ctas, stream)
+                            : launch_fused_t<float>(maps, p, ctas, stream);
+}
+
 template <typename IO>
 static cudaError_t launch_summary_t(const CUtensorMap* m, const ScanParams& p, dim3 grid, cudaStream_t s) {
   const size_t smem = sizeof(CarrySmem<IO>) + 128;

@@ -25,6 +25,10 @@ cudaError_t launch_bc_widen(IoType io, const void* Bm, const void* Cm, float* bc
 cudaError_t launch_conv_silu(IoType io, const void* x, const float* conv_w, const float* conv_b, void* u, int B,
                              int L, int D, cudaStream_t stream);
 // maps: x, z, dt_raw, bc (3-D tiled tensor maps).
+// The chunked mode's carry pass and main pass as one launch of `ctas`
+// one-warp CTAs (the carry tasks first, by ticket; maps: x, z, dt_raw, bc).
+cudaError_t launch_scan_fused(IoType io, const CUtensorMap maps[4], const ScanParams& p, unsigned ctas,
+                              cudaStream_t stream);
 cudaError_t launch_scan(IoType io, const CUtensorMap maps[4], const ScanParams& p, dim3 grid,
                         cudaStream_t stream);
 // maps: x, dt_raw, and the B half of bc.

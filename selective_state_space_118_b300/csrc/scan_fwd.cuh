@@ -280,21 +280,16 @@ __device__ __forceinline__ int live_pairs(const State16& wgt, bool active) {
 }
 
 // ---------------------------------------------------------------- main pass
-// grid (n_groups, batch, n_chunks), 32 threads.  kY false: no y (and no z):
-// the pass only stores the states entering every tile (p.ckpt), for the
-// backward.
+// One warp per (channel group g, batch row b, chunk j).  kY false: no y (and
+// no z): the pass only stores the states entering every tile (p.ckpt), for
+// the backward.  wait_carry: the carry entering chunk j is published during
+// this launch (the fused kernel below); wait (bounded) for its flag first.
 template <typename IO, bool kY>
-__global__ void __launch_bounds__(kLanes)
-    scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
-                    const __grid_constant__ CUtensorMap tm_dt, const __grid_constant__ CUtensorMap tm_bc,
-                    const __grid_constant__ ScanParams p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  MainSmem<IO>& sm = *reinterpret_cast<MainSmem<IO>*>(smem_raw + smem_pad128(smem_raw));
-
+__device__ __forceinline__ void main_warp(const CUtensorMap& tm_x, const CUtensorMap& tm_z, const CUtensorMap& tm_dt,
+                                          const CUtensorMap& tm_bc, const ScanParams& p, MainSmem<IO>& sm, int g,
+                                          int b, int j, bool wait_carry) {
   const int lane = threadIdx.x;
-  const int c0 = blockIdx.x * kLanes;
-  const int b = blockIdx.y;
-  const int j = blockIdx.z;
+  const int c0 = g * kLanes;
   const int D = p.d_inner;
   const int c = c0 + lane;
   const bool active = c < D;
@@ -331,7 +326,33 @@ __global__ void __launch_bounds__(kLanes)
   Channel ch;
   load_channel(ch, p.A_log, p.conv_w, p.conv_b, p.Dskip, cl);
   State16 st;
-  if (j > 0)
+  if (j > 0 && wait_carry) {
+    bool have = true;
+    if (lane == 0) {
+      const unsigned* ready = p.counters + 1 + (size_t)b * p.n_groups * p.n_chunks + (size_t)g * p.n_chunks;
+      const uint64_t t_start = globaltimer_ns();
+      while (atomicAdd(const_cast<unsigned*>(ready + j), 0u) == 0u) {
+        if (globaltimer_ns() - t_start > p.timeout_ns) {
+          have = false;
+          break;
+        }
+      }
+    }
+    have = __shfl_sync(0xffffffffu, have, 0);
+    __threadfence();
+    if (!have) {
+      if (lane == 0) report_error(4u);  // MAMBA_ERR_TIMEOUT
+      state16_zero(st);
+    } else {
+      const float4* src = reinterpret_cast<const float4*>(p.carry + (((size_t)b * p.n_chunks + j) * D + cl) * kN);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {  // from L2: written by another SM during this launch
+        const float4 v = __ldcg(src + kk);
+        st.h[2 * kk] = make_float2(v.x, v.y);
+        st.h[2 * kk + 1] = make_float2(v.z, v.w);
+      }
+    }
+  } else if (j > 0)
     state16_load(st, p.carry + (((size_t)b * p.n_chunks + j) * D + cl) * kN);
   else if (p.h0)
     state16_load(st, p.h0 + ((size_t)b * D + cl) * kN);
@@ -402,6 +423,18 @@ __global__ void __launch_bounds__(kLanes)
   if (j == p.n_chunks - 1 && p.final_h && active) state16_store(st, p.final_h + ((size_t)b * D + c) * kN);
 }
 
+// grid (n_groups, batch, n_chunks), 32 threads: the carries were computed by
+// an earlier launch.
+template <typename IO, bool kY>
+__global__ void __launch_bounds__(kLanes)
+    scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
+                    const __grid_constant__ CUtensorMap tm_dt, const __grid_constant__ CUtensorMap tm_bc,
+                    const __grid_constant__ ScanParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  main_warp<IO, kY>(tm_x, tm_z, tm_dt, tm_bc, p, *reinterpret_cast<MainSmem<IO>*>(smem_raw + smem_pad128(smem_raw)),
+                    blockIdx.x, blockIdx.y, blockIdx.z, false);
+}
+
 // ---------------------------------------------------------------- chunk carries
 // One warp per (chunk boundary j = 1..n_chunks-1, channel group, batch row),
 // assigned in launch order from a ticket counter, so that the warp of
@@ -462,10 +495,10 @@ __device__ __forceinline__ void issue_carry_tile(CarrySmem<IO>& sm, int s, const
 // that runs it beside the adjoint carries).
 template <typename IO>
 __device__ __forceinline__ void carry_warp(const CUtensorMap& tm_x, const CUtensorMap& tm_dt, const CUtensorMap& tm_bc,
-                                           const ScanParams& p, CarrySmem<IO>& sm) {
+                                           const ScanParams& p, CarrySmem<IO>& sm, long ticket_in = -1) {
   const int lane = threadIdx.x;
   if (lane == 0) {
-    sm.ticket = atomicAdd(p.counters, 1u);
+    sm.ticket = ticket_in >= 0 ? (unsigned)ticket_in : atomicAdd(p.counters, 1u);
     for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&sm.full[s]), 1);
     fence_mbar_init();
     prefetch_tensormap(&tm_x);
@@ -621,6 +654,41 @@ __global__ void __launch_bounds__(kLanes)
                       const __grid_constant__ CUtensorMap tm_bc, const __grid_constant__ ScanParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   carry_warp<IO>(tm_x, tm_dt, tm_bc, p, *reinterpret_cast<CarrySmem<IO>*>(smem_raw + smem_pad128(smem_raw)));
+}
+
+// ---------------------------------------------------------------- carries and main pass in one launch
+// The chunked mode's two passes as one launch of (n_chunks - 1) * n_groups *
+// batch carry warps and n_chunks * n_groups * batch main warps.  Each CTA
+// takes a ticket at its start: the carry tasks come first (in the carry
+// kernel's order), then the main tasks chunk by chunk.  The main warp of
+// chunk j > 0 waits (bounded) for carry_j's flag; its carry warp took an
+// earlier ticket, so it is resident or done, and chunk 0's main warps and the
+// carries run side by side instead of one pass after the other.
+template <typename IO>
+constexpr size_t fused_smem_bytes() {
+  return sizeof(MainSmem<IO>) > sizeof(CarrySmem<IO>) ? sizeof(MainSmem<IO>) : sizeof(CarrySmem<IO>);
+}
+
+template <typename IO, bool kY>
+__global__ void __launch_bounds__(kLanes)
+    scan_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
+                      const __grid_constant__ CUtensorMap tm_dt, const __grid_constant__ CUtensorMap tm_bc,
+                      const __grid_constant__ ScanParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* base = smem_raw + smem_pad128(smem_raw);
+  unsigned ticket = 0;
+  if (threadIdx.x == 0) ticket = atomicAdd(p.counters, 1u);
+  ticket = __shfl_sync(0xffffffffu, ticket, 0);
+  const unsigned per = (unsigned)p.n_groups * (unsigned)p.batch;
+  const unsigned n_carry = (unsigned)(p.n_chunks - 1) * per;
+  if (ticket < n_carry) {
+    carry_warp<IO>(tm_x, tm_dt, tm_bc, p, *reinterpret_cast<CarrySmem<IO>*>(base), (long)ticket);
+  } else {
+    const unsigned t = ticket - n_carry;
+    const int j = (int)(t / per), gb = (int)(t % per);
+    main_warp<IO, kY>(tm_x, tm_z, tm_dt, tm_bc, p, *reinterpret_cast<MainSmem<IO>*>(base), gb % p.n_groups,
+                      gb / p.n_groups, j, true);
+  }
 }
 
 }  // namespace mamba
