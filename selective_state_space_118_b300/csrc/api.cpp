@@ -871,6 +871,7 @@ mamba_status mamba_step(const mamba_step_args* a, void* stream_v) {
   p.Dskip = a->Dskip;
   p.conv_w = a->conv_w;
   p.conv_b = a->conv_b;
+  p.timeout_ns = kDefaultTimeoutNs;
   p.y_t = a->y_t;
   const IoType io = a->io == MAMBA_BF16 ? IoType::BF16 : IoType::F32;
   if (mamba::launch_step(io, p, stream) != cudaSuccess) return MAMBA_ERR_CUDA;

@@ -144,6 +144,7 @@ struct StepParams {
   const float* conv_w;
   const float* conv_b;  // may be null
   void* y_t;          // (B, D)
+  uint64_t timeout_ns;  // limit of the wait for a block of h
 };
 
 }  // namespace mamba

@@ -12,13 +12,15 @@
 // meet through one exchange in the fixed order of state16_readout.  The arithmetic is ssm_math.cuh's, in the
 // same order as one token of scan_fwd_kernel, so a sequence of steps
 // reproduces a single-pass scan bit for bit.  h is 128 of the ~144 bytes
-// moved per channel and row; many small threads (one row each) keep more
-// bytes in flight per SM than fewer threads with several rows.
+// moved per channel and row: a CTA's block of h (64 channels of one row,
+// 4 KB contiguous) comes in by one bulk copy and leaves by one bulk store,
+// which keeps more bytes in flight per SM than per-lane loads do.
 #pragma once
 #include <cuda_bf16.h>
 
 #include "params.h"
 #include "ptx.cuh"
+#include "scan_fwd.cuh"
 #include "ssm_math.cuh"
 
 namespace mamba {
@@ -30,28 +32,6 @@ constexpr int kStepChannels = kStepThreads / kLPC;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-// kLS consecutive fp32 values of h.
-__device__ __forceinline__ void load_h(const float* p, float4 (&v)[kLS / 4]) {
-  if constexpr (kLS == 8) {
-    asm volatile("ld.global.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=f"(v[0].x), "=f"(v[0].y), "=f"(v[0].z), "=f"(v[0].w), "=f"(v[1].x), "=f"(v[1].y),
-                   "=f"(v[1].z), "=f"(v[1].w)
-                 : "l"(p));
-  } else {
-    v[0] = *reinterpret_cast<const float4*>(p);
-  }
-}
-
-__device__ __forceinline__ void store_h(float* p, const float4 (&v)[kLS / 4]) {
-  if constexpr (kLS == 8) {
-    asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v[0].x), "f"(v[0].y),
-                 "f"(v[0].z), "f"(v[0].w), "f"(v[1].x), "f"(v[1].y), "f"(v[1].z), "f"(v[1].w)
-                 : "memory");
-  } else {
-    *reinterpret_cast<float4*>(p) = v[0];
-  }
-}
 
 // kLS consecutive I/O values (part of a B or C row) as fp32.
 __device__ __forceinline__ void load_part(const float* p, float4 (&v)[kLS / 4]) {
@@ -74,18 +54,29 @@ __device__ __forceinline__ void load_part(const __nv_bfloat16* p, float4 (&v)[kL
 // consecutive threads = one channel of one batch row.
 template <typename IO>
 __global__ void __launch_bounds__(kStepThreads) step_kernel(const __grid_constant__ StepParams p) {
+  __shared__ __align__(128) float hs[kStepChannels * kN];
+  __shared__ __align__(8) uint64_t hbar;
   griddep_wait();
   griddep_launch_dependents();
   const int D = p.d_inner;
   const int q = threadIdx.x % kLPC;
-  const int c = blockIdx.x * kStepChannels + threadIdx.x / kLPC;
+  const int c0 = blockIdx.x * kStepChannels;
+  const int c = c0 + threadIdx.x / kLPC;
   const int b = blockIdx.y;
   const bool valid = c < D;  // the lanes of a channel share it
   const int cl = valid ? c : D - 1;
   const size_t ch = (size_t)b * D + cl;
+  const uint32_t hbytes = (uint32_t)min(kStepChannels, D - c0) * kN * 4;  // this block's channels of h
+  float* hblk = p.h + ((size_t)b * D + c0) * kN;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&hbar), 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(smem_u32(&hbar), hbytes);
+    bulk_load(smem_u32(hs), hblk, hbytes, smem_u32(&hbar));
+  }
+  __syncthreads();
 
   float4 hv[kLS / 4], Bv[kLS / 4], Cv[kLS / 4];
-  load_h(p.h + ch * kN + kLS * q, hv);
   const IO* cs = reinterpret_cast<const IO*>(p.conv_state) + (size_t)b * 3 * D + cl;
   const IO r0 = cs[0], r1 = cs[D], r2 = cs[2 * (size_t)D];
   const IO rx = __ldg(reinterpret_cast<const IO*>(p.x_t) + ch);
@@ -98,6 +89,15 @@ __global__ void __launch_bounds__(kStepThreads) step_kernel(const __grid_constan
   const float4 w = __ldg(reinterpret_cast<const float4*>(p.conv_w + (size_t)cl * 4));
   const float bias = p.conv_b ? __ldg(p.conv_b + cl) : 0.0f;
   const float Dc = __ldg(p.Dskip + cl);
+  if (!__syncthreads_and(mbar_wait_bounded(smem_u32(&hbar), 0, p.timeout_ns))) {
+    if (threadIdx.x == 0) report_error(4u);  // MAMBA_ERR_TIMEOUT
+    return;
+  }
+  {
+    const float4* hp4 = reinterpret_cast<const float4*>(hs + (threadIdx.x / kLPC) * kN + kLS * q);
+#pragma unroll
+    for (int k = 0; k < kLS / 4; ++k) hv[k] = hp4[k];
+  }
 
   const float u = silu(conv4(w, bias, to_f32(r0), to_f32(r1), to_f32(r2), to_f32(rx)));
   const float dt = softplus(dr);
@@ -124,8 +124,18 @@ __global__ void __launch_bounds__(kStepThreads) step_kernel(const __grid_constan
   const float2 pr = readout_half(hp, Cv);
   const float2 po = make_float2(__shfl_xor_sync(0xffffffffu, pr.x, 1), __shfl_xor_sync(0xffffffffu, pr.y, 1));
   const float ss = q == 0 ? readout_join(pr, po) : readout_join(po, pr);
+  {
+    float4* hp4 = reinterpret_cast<float4*>(hs + (threadIdx.x / kLPC) * kN + kLS * q);
+#pragma unroll
+    for (int k = 0; k < kLS / 4; ++k) hp4[k] = hv[k];
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bulk_store(hblk, smem_u32(hs), hbytes);
+    bulk_commit();
+  }
   if (valid) {
-    store_h(p.h + ch * kN + kLS * q, hv);
     if (q == 0) {
       reinterpret_cast<IO*>(p.y_t)[ch] = from_f32<IO>(gate_out(ss, Dc, u, gz));
       IO* csw = reinterpret_cast<IO*>(p.conv_state) + (size_t)b * 3 * D + c;
@@ -134,6 +144,7 @@ __global__ void __launch_bounds__(kStepThreads) step_kernel(const __grid_constan
       csw[2 * (size_t)D] = rx;
     }
   }
+  if (threadIdx.x == 0) bulk_wait_read<0>();  // the block of h has left shared memory
 }
 
 }  // namespace mamba
