@@ -269,9 +269,9 @@ def prefill_step(ops, inp, out, ws, stream, slices, n_chunks=0):
 
 
 def scan_launches(ops, B, L, D, n_chunks_req):
-    """Kernels one mamba_scan_fwd launches: B/C widening, the chunk carries
-    (chunked mode) and the main pass."""
-    return 2 if ops.mamba_scan_plan(B, L, D, n_chunks_req)["n_chunks"] == 1 else 3
+    """Kernels one mamba_scan_fwd launches: B/C widening, then the main pass
+    (one chunk) or the chunk carries and the main pass in one launch."""
+    return 2
 
 
 def mufu_peak():
@@ -1130,7 +1130,7 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": measured_traffic(w.name), "peak_source": src,
                          "kernel": f"mamba_scan_fwd x {res['calls_per_step']} calls per step "
-                                   f"(bc_widen + scan_carry + scan_fwd each), CUDA events around the step",
+                                   f"(bc_widen + scan_fused each), CUDA events around the step",
                          "algorithmic_bytes_per_step": res["alg_bytes"],
                          "compute": compute_roofline(res["elems"] / t_step, res["elems"], t_step)},
             "gpu_launches": res["launches_per_step"] * args.steps,

@@ -16,10 +16,6 @@ size_t scan_smem_bytes(IoType io) {
   return (io == IoType::BF16 ? sizeof(MainSmem<__nv_bfloat16>) : sizeof(MainSmem<float>)) + 128;
 }
 
-size_t summary_smem_bytes(IoType io) {
-  return (io == IoType::BF16 ? sizeof(CarrySmem<__nv_bfloat16>) : sizeof(CarrySmem<float>)) + 128;
-}
-
 template <typename IO, bool kY>
 static cudaError_t launch_scan_y(const CUtensorMap* m, const ScanParams& p, dim3 grid, cudaStream_t s) {
   const size_t smem = sizeof(MainSmem<IO>) + 128;
@@ -58,16 +54,6 @@ cudaError_t launch_scan_fused(IoType io, const CUtensorMap maps[4], const ScanPa
 }
 
 template <typename IO>
-static cudaError_t launch_summary_t(const CUtensorMap* m, const ScanParams& p, dim3 grid, cudaStream_t s) {
-  const size_t smem = sizeof(CarrySmem<IO>) + 128;
-  cudaError_t e = cudaFuncSetAttribute(scan_carry_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
-  scan_carry_kernel<IO><<<grid, kLanes, smem, s>>>(m[0], m[1], m[2], p);
-  return cudaGetLastError();
-}
-
-template <typename IO>
 static cudaError_t launch_widen_t(const void* Bm, const void* Cm, float* bc, long rows, int ld, cudaStream_t s) {
   const long n = rows * 8;
   long blocks = (n + 255) / 256;
@@ -88,12 +74,6 @@ cudaError_t launch_scan(IoType io, const CUtensorMap maps[4], const ScanParams& 
                         cudaStream_t stream) {
   return io == IoType::BF16 ? launch_scan_t<__nv_bfloat16>(maps, p, grid, stream)
                             : launch_scan_t<float>(maps, p, grid, stream);
-}
-
-cudaError_t launch_summary(IoType io, const CUtensorMap maps[3], const ScanParams& p, dim3 grid,
-                           cudaStream_t stream) {
-  return io == IoType::BF16 ? launch_summary_t<__nv_bfloat16>(maps, p, grid, stream)
-                            : launch_summary_t<float>(maps, p, grid, stream);
 }
 
 // ---------------------------------------------------------------- tensor-core GEMM
@@ -179,13 +159,13 @@ void scan_occupancy(IoType io, int* main_per_sm, int* summary_per_sm) {
   if (io == IoType::BF16) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, scan_fwd_kernel<__nv_bfloat16, true>, kLanes,
                                                       sizeof(MainSmem<__nv_bfloat16>) + 128) != cudaSuccess) a = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, scan_carry_kernel<__nv_bfloat16>, kLanes,
-                                                      sizeof(CarrySmem<__nv_bfloat16>) + 128) != cudaSuccess) b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, scan_fused_kernel<__nv_bfloat16, true>, kLanes,
+                                                      fused_smem_bytes<__nv_bfloat16>() + 128) != cudaSuccess) b = 0;
   } else {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, scan_fwd_kernel<float, true>, kLanes,
                                                       sizeof(MainSmem<float>) + 128) != cudaSuccess) a = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, scan_carry_kernel<float>, kLanes,
-                                                      sizeof(CarrySmem<float>) + 128) != cudaSuccess) b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, scan_fused_kernel<float, true>, kLanes,
+                                                      fused_smem_bytes<float>() + 128) != cudaSuccess) b = 0;
   }
   *main_per_sm = a;
   *summary_per_sm = b;

@@ -15,7 +15,6 @@ enum class IoType { F32, BF16 };
 
 // Dynamic shared memory of the prefill kernels for an I/O type.
 size_t scan_smem_bytes(IoType io);
-size_t summary_smem_bytes(IoType io);
 
 // B, C rows (16 values each, `ld` elements apart) in the I/O dtype -> bc
 // (rows, 32) fp32.
@@ -32,8 +31,6 @@ cudaError_t launch_scan_fused(IoType io, const CUtensorMap maps[4], const ScanPa
 cudaError_t launch_scan(IoType io, const CUtensorMap maps[4], const ScanParams& p, dim3 grid,
                         cudaStream_t stream);
 // maps: x, dt_raw, and the B half of bc.
-cudaError_t launch_summary(IoType io, const CUtensorMap maps[3], const ScanParams& p, dim3 grid,
-                           cudaStream_t stream);
 cudaError_t launch_step(IoType io, const StepParams& p, cudaStream_t stream);
 // The complex-valued scan: in chunked mode the summaries, the fold and the
 // main pass; otherwise the main pass.  maps: x, z, dt_raw, bc.
@@ -54,9 +51,9 @@ cudaError_t launch_bwd_finish(IoType io, const BwdParams& p, float* dB, float* d
 cudaError_t launch_ssd(const CUtensorMap maps[5], const SsdParams& p, cudaStream_t stream);
 cudaError_t launch_io_to_f32(IoType io, const void* src, float* dst, long n, cudaStream_t stream);
 
-// Resident CTAs per SM of the main and summary kernels (0 when no device
-// answers); the dynamic shared memory has to be allowed first (launch_* do
-// that; scan_occupancy sets the same attribute).
+// Resident CTAs per SM of the main-pass kernel and of the fused carry and
+// main-pass kernel (0 when no device answers); both need less dynamic shared
+// memory than the default limit.
 void scan_occupancy(IoType io, int* main_per_sm, int* summary_per_sm);
 
 // C = A W^T [+ bias] on the tensor cores (gemm_tc.cuh).  a: A (K x M, box

@@ -491,8 +491,8 @@ __device__ __forceinline__ void issue_carry_tile(CarrySmem<IO>& sm, int s, const
   tma_load_3d(smem_u32(&sm.stage[s].bc[0][0]), tbc, 0, tt, b, bar);
 }
 
-// One warp of the carry pass (the kernel below, or the backward's launch
-// that runs it beside the adjoint carries).
+// One warp of the carry pass (in the fused launch below, or in the
+// backward's launch that runs it beside the adjoint carries).
 template <typename IO>
 __device__ __forceinline__ void carry_warp(const CUtensorMap& tm_x, const CUtensorMap& tm_dt, const CUtensorMap& tm_bc,
                                            const ScanParams& p, CarrySmem<IO>& sm, long ticket_in = -1) {
@@ -645,15 +645,6 @@ __device__ __forceinline__ void carry_warp(const CUtensorMap& tm_x, const CUtens
   __threadfence();
   __syncwarp();
   if (lane == 0) atomicExch(ready + j, 1u);
-}
-
-// grid ((n_chunks - 1) * n_groups * batch), 32 threads.
-template <typename IO>
-__global__ void __launch_bounds__(kLanes)
-    scan_carry_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dt,
-                      const __grid_constant__ CUtensorMap tm_bc, const __grid_constant__ ScanParams p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  carry_warp<IO>(tm_x, tm_dt, tm_bc, p, *reinterpret_cast<CarrySmem<IO>*>(smem_raw + smem_pad128(smem_raw)));
 }
 
 // ---------------------------------------------------------------- carries and main pass in one launch
