@@ -498,6 +498,11 @@ mamba_status mamba_linear_fwd(const mamba_linear_args *args, void *stream);
  *   B_t, C_t          (B, 16) io          (16-byte aligned, like h)
  *   A_log, Dskip, conv_w, conv_b   as for the scan
  *   y_t               (B, D) io           output
+ *
+ * h moves in blocks of 64 channels of one row (4 KB) by bulk copies into
+ * and out of shared memory; the one device-side wait (for a block to land)
+ * gives up after 1 second and reports MAMBA_ERR_TIMEOUT through
+ * mamba_last_error, leaving that block's h and y unwritten.
  */
 typedef struct mamba_step_args {
     int batch, d_inner, d_state, d_conv;
