@@ -454,42 +454,50 @@ __global__ void __launch_bounds__(kPassThreads) ssd_pass_kernel(const __grid_con
 // A persistent kernel, one CTA per SM, walking tiles t = (head, chunk, batch
 // row) with the head fastest (the SMs at work at one time share a chunk's B
 // and C rows and read its x, z rows whole).  Warp roles, linked by mbarriers:
-//   warp 0      loads tile k into stage k % 4 by TMA: x (128 tokens x 64
+//   warp 0      loads tile k into stage k % 5 by TMA: x (128 tokens x 64
 //               channels, 128-byte swizzle), B, C (128 x 16, 32-byte
 //               swizzle), the entering state (fp32, 4 KB) and the chunk's
 //               (decay prefix, dt) pairs by bulk copies; z, read only by the
-//               epilogue, into a ring of its own of two tiles;
-//   warp 1      issues the MMAs into tensor-memory buffer k % 4 (128
-//               columns each), each as soon as its inputs are ready:
-//               G = C B^T (128 x 128, K = 16); then Y = G' X (128 x 64), the
-//               hi and lo terms accumulated,
-//               two halves of K = 64, each once the converter has written its
-//               half of G', over columns 0..63; Yo = C (S_hi + S_lo)
-//               (128 x 64, K = 16) over columns 64..127 with the second half;
+//               epilogue, into a ring of its own of three tiles;
+//   warp 1      issues the MMAs, each as soon as its inputs are ready:
+//               G = C B^T (128 x 128, K = 16) into score buffer k % 2 of
+//               tensor memory; then Y = G' X (128 x 64), G' read from tensor
+//               memory (hi and lo terms accumulated), in two halves of K =
+//               64, each once the converter has written its half of G', into
+//               accumulator buffer k % 4 (64 columns); with the second half
+//               the entering state's term (e C) S_in (K = 16, e_i =
+//               2^(acum_i); hi + lo products) accumulated into the same Y;
 //   warps 4-11  warp w reads rows 32 (w % 4) .. + 31 of G and columns
 //               64 h .. + 63 (h = (w - 4) / 4, the K half), masks them to
 //               s <= t, scales them by the decay 2^(acum_i - acum_j) dt_j and
-//               writes them as hi + lo bf16 terms (G' = G_hi + G_lo, ~16
-//               significant bits) into half h of the K-major operand of the Y
-//               product; the h = 1 warps also write the entering state, as
-//               hi + lo terms, into the MN-major operand of the Yo product;
-//   warps 12-15 y = Y + 2^(acum_i) Yo + D x, times silu(z) (through tanh),
-//               written over the stage's x rows and stored by TMA (32 rows
-//               per warp), which frees the stage.
+//               writes them back in place as hi + lo bf16 terms (G' = G_hi +
+//               G_lo, ~16 significant bits: each 32-column group's 32 fp32
+//               columns become 16 columns of hi pairs and 16 of lo pairs), the
+//               A operand of the Y product; the h = 1 warps also write the
+//               entering state (hi + lo, MN-major) into shared memory, and
+//               the rows e_i C_i (hi + lo) over the stage's B and C tiles,
+//               dead once G is formed;
+//   warps 12-15 y = Y + D x, times silu(z) (through tanh), written over the
+//               stage's x rows and stored by TMA (32 rows per warp), which
+//               frees the stage.
+// Tensor memory holds two score buffers (2 x 128 columns) and four
+// accumulator buffers (4 x 64): a score buffer is free again once the Y
+// product has read it, so G of tile k + 2 needs only tile k's Y product, and
+// the epilogue runs up to four tiles behind the MMAs.
 // The decay factor of an entry is taken relative to the first token of its
 // 32-column group, 2^(acum_i - acum_r) * (2^(acum_r - acum_j) dt_j): both
 // factors stay in range while the decay across the 32 tokens is at most
 // 2^60; beyond that (very fast decay) the entry's factor is computed whole.
-// The all-zero 32 x 32 blocks above the diagonal are written once.
-constexpr int kSsdStages = 4;
+constexpr int kSsdStages = 5;
+constexpr int kSsdZ = 3;  // the gate's ring
+constexpr int kSsdAcc = 4;
 constexpr int kSsdOutThreads = 512;
-constexpr int kSsdAcc = 4;  // tensor-memory accumulator buffers of 128 columns
-constexpr int kSsdTmemCols = 128 * kSsdAcc;
+constexpr int kSsdTmemCols = 512;  // score buffers at columns 0, 128; accumulators at 256 + 64 j
 
 struct SsdStage {
   __nv_bfloat16 x[kSsdQ * kSsdP];  // 16 KB, rows of 128 bytes; then y
-  __nv_bfloat16 b[kSsdQ * kSsdN];  // rows of 32 bytes
-  __nv_bfloat16 c[kSsdQ * kSsdN];
+  __nv_bfloat16 b[kSsdQ * kSsdN];  // rows of 32 bytes; then the e C rows' hi terms
+  __nv_bfloat16 c[kSsdQ * kSsdN];  // then their lo terms
   float s[kSsdN * kSsdP];          // the entering state, row n of 64 channels
   float2 cum[kSsdQ];               // (decay prefix, dt) per token
 };
@@ -497,16 +505,15 @@ static_assert(sizeof(SsdStage) % 1024 == 0, "stages keep the 1024-byte alignment
 
 struct SsdOutSmem {
   SsdStage st[kSsdStages];
-  __nv_bfloat16 z[2][kSsdQ * kSsdP];  // the gate's ring
-  __nv_bfloat16 ghi[2][kSsdQ * 64];   // G' in two 64-column K halves, rows of 128 bytes
-  __nv_bfloat16 glo[2][kSsdQ * 64];
-  __nv_bfloat16 shi[kSsdN * kSsdP];  // the entering state: rows n of 64 channels
-  __nv_bfloat16 slo[kSsdN * kSsdP];
-  float fdt[8][64];                  // per converter warp: 2^(acum_r - acum_j) dt_j for its columns
+  __nv_bfloat16 z[kSsdZ][kSsdQ * kSsdP];  // the gate's ring
+  __nv_bfloat16 shi[2][kSsdN * kSsdP];    // the entering state: rows n of 64 channels
+  __nv_bfloat16 slo[2][kSsdN * kSsdP];
+  float fdt[8][64];                       // per converter warp: 2^(acum_r - acum_j) dt_j for its columns
   uint64_t full[kSsdStages], empty[kSsdStages];
-  uint64_t gfull[kSsdAcc], tmem_empty[kSsdAcc], yfull[kSsdAcc];
-  uint64_t gop_full[2], gop_empty[2];
-  uint64_t zfull[2], zempty[2];
+  uint64_t zfull[kSsdZ], zempty[kSsdZ];
+  uint64_t gfull[2], aempty[2];  // score buffers: G formed; read by the Y product
+  uint64_t opfull[2][2];         // [score buffer][K half]: G' written
+  uint64_t yfull[kSsdAcc], yempty[kSsdAcc];  // accumulator buffers
   uint32_t tmem_base;
 };
 
@@ -525,22 +532,25 @@ __device__ __forceinline__ float2 silu_tanh_x2(float2 z) {
   return __ffma2_rn(h, make_float2(tanh_approx(h.x), tanh_approx(h.y)), h);
 }
 
-// The Y half kh of tile kk (and, with the second half, Yo): MMAs into d.
-__device__ __forceinline__ void ssd_issue_y(const SsdOutSmem& sm, const SsdStage& st, uint32_t d, int kh) {
+// The Y half kh of a tile (and, with the second half, the entering state's
+// term): MMAs with G' from score buffer column ga into accumulator column dy.
+__device__ __forceinline__ void ssd_issue_y(const SsdOutSmem& sm, const SsdStage& st, uint32_t ga, uint32_t dy,
+                                            int kh, int sb) {
   const uint32_t iy = umma_idesc_bf16(128, 64, true);  // B operand (x rows, S rows) MN-major
 #pragma unroll
-  for (int part = 0; part < 2; ++part)
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const uint32_t gb = smem_u32(part == 0 ? sm.ghi[kh] : sm.glo[kh]);
-      const uint64_t ad = umma_desc(gb + 32 * ks, 1024, 2);                                // 16 columns of G'
-      const uint64_t bd = umma_desc(smem_u32(st.x) + (kh * 64 + ks * 16) * 128, 1024, 2);  // 16 rows of x
-      tc_mma_f16(d, ad, bd, iy, kh > 0 || part > 0 || ks > 0);
-    }
-  if (kh == 1) {
-    const uint64_t cd = umma_desc(smem_u32(st.c), 256, 6);
-    tc_mma_f16(d + 64, cd, umma_desc(smem_u32(sm.shi), 1024, 2), iy, false);
-    tc_mma_f16(d + 64, cd, umma_desc(smem_u32(sm.slo), 1024, 2), iy, true);
+  for (int ks = 0; ks < 4; ++ks) {
+    // 16 columns of G': group ks / 2 of the half, its hi pairs at +0, lo at +16
+    const uint32_t a = ga + 64 * kh + 32 * (ks >> 1) + 8 * (ks & 1);
+    const uint64_t bd = umma_desc(smem_u32(st.x) + (kh * 64 + ks * 16) * 128, 1024, 2);  // 16 rows of x
+    tc_mma_f16_ta(dy, a, bd, iy, kh > 0 || ks > 0);
+    tc_mma_f16_ta(dy, a + 16, bd, iy, true);
+  }
+  if (kh == 1) {  // + (e C) S_in: (e C)_hi S_hi + (e C)_hi S_lo + (e C)_lo S_hi
+    const uint64_t ehi = umma_desc(smem_u32(st.b), 256, 6), elo = umma_desc(smem_u32(st.c), 256, 6);
+    const uint64_t shi = umma_desc(smem_u32(sm.shi[sb]), 1024, 2), slo = umma_desc(smem_u32(sm.slo[sb]), 1024, 2);
+    tc_mma_f16(dy, ehi, shi, iy, true);
+    tc_mma_f16(dy, ehi, slo, iy, true);
+    tc_mma_f16(dy, elo, shi, iy, true);
   }
 }
 
@@ -561,16 +571,19 @@ __global__ void __launch_bounds__(kSsdOutThreads, 1)
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), 4);  // one arrival per epilogue warp
     }
-    for (int a = 0; a < kSsdAcc; ++a) {
-      mbar_init(smem_u32(&sm.gfull[a]), 1);
-      mbar_init(smem_u32(&sm.tmem_empty[a]), 4);
-      mbar_init(smem_u32(&sm.yfull[a]), 1);
+    for (int z = 0; z < kSsdZ; ++z) {
+      mbar_init(smem_u32(&sm.zfull[z]), 1);
+      mbar_init(smem_u32(&sm.zempty[z]), 4);
     }
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(smem_u32(&sm.gop_full[h]), 4);  // one arrival per converter warp of the half
-      mbar_init(smem_u32(&sm.gop_empty[h]), 1);
-      mbar_init(smem_u32(&sm.zfull[h]), 1);
-      mbar_init(smem_u32(&sm.zempty[h]), 4);  // one arrival per epilogue warp
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&sm.gfull[a]), 1);
+      mbar_init(smem_u32(&sm.aempty[a]), 1);
+      mbar_init(smem_u32(&sm.opfull[a][0]), 4);  // one arrival per converter warp of the half
+      mbar_init(smem_u32(&sm.opfull[a][1]), 4);
+    }
+    for (int e = 0; e < kSsdAcc; ++e) {
+      mbar_init(smem_u32(&sm.yfull[e]), 1);
+      mbar_init(smem_u32(&sm.yempty[e]), 4);
     }
     fence_mbar_init();
     prefetch_tensormap(&tm_x);
@@ -590,7 +603,7 @@ __global__ void __launch_bounds__(kSsdOutThreads, 1)
   bool ok = true;
 
   if (warp == 0) {
-    if (lane == 0) {  // producer: the stages, and the gate's ring (one tile behind at most)
+    if (lane == 0) {  // producer: the stages, and the gate's ring
       const uint32_t bytes = kSsdQ * kSsdP * 2 + 2 * kSsdQ * kSsdN * 2 + kSsdN * kSsdP * 4 + kSsdQ * 8;
       uint32_t k = 0, kz = 0;
       uint64_t idle_since = globaltimer_ns();
@@ -613,11 +626,11 @@ __global__ void __launch_bounds__(kSsdOutThreads, 1)
           ++k;
           moved = true;
         }
-        if (gate && kz < k && mbar_test_wait(smem_u32(&sm.zempty[kz & 1u]), ((kz >> 1) & 1u) ^ 1u)) {
+        if (gate && kz < k && mbar_test_wait(smem_u32(&sm.zempty[kz % kSsdZ]), ((kz / kSsdZ) & 1u) ^ 1u)) {
           const SsdTileId id = ssd_tile(blockIdx.x + kz * gridDim.x, H, nC);
-          const uint32_t bar = smem_u32(&sm.zfull[kz & 1u]);
+          const uint32_t bar = smem_u32(&sm.zfull[kz % kSsdZ]);
           mbar_arrive_expect_tx(bar, kSsdQ * kSsdP * 2);
-          tma_load_4d(smem_u32(sm.z[kz & 1u]), &tm_z, 0, id.h, id.c * kSsdQ, id.b, bar);
+          tma_load_4d(smem_u32(sm.z[kz % kSsdZ]), &tm_z, 0, id.h, id.c * kSsdQ, id.b, bar);
           ++kz;
           moved = true;
         }
@@ -628,14 +641,13 @@ __global__ void __launch_bounds__(kSsdOutThreads, 1)
             ok = false;
             break;
           }
-          __nanosleep(32);
         }
       }
       // the copies issued last have landed before the CTA may end
       for (uint32_t j = k > kSsdStages ? k - kSsdStages : 0; j < k; ++j)
         if (!mbar_wait_bounded(smem_u32(&sm.full[j % kSsdStages]), (j / kSsdStages) & 1u, p.timeout_ns)) ok = false;
-      for (uint32_t j = kz > 2 ? kz - 2 : 0; j < kz; ++j)
-        if (!mbar_wait_bounded(smem_u32(&sm.zfull[j & 1u]), (j >> 1) & 1u, p.timeout_ns)) ok = false;
+      for (uint32_t j = kz > kSsdZ ? kz - kSsdZ : 0; j < kz; ++j)
+        if (!mbar_wait_bounded(smem_u32(&sm.zfull[j % kSsdZ]), (j / kSsdZ) & 1u, p.timeout_ns)) ok = false;
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer: G of tile kg, Y halves of tiles ky0, ky1, each as soon as it may go
@@ -645,28 +657,30 @@ __global__ void __launch_bounds__(kSsdOutThreads, 1)
       uint64_t idle_since = globaltimer_ns();
       while (ky1 < n_mine) {
         bool moved = false;
-        if (ky1 < ky0 && mbar_test_wait(smem_u32(&sm.gop_full[1]), ky1 & 1u)) {
+        if (ky1 < ky0 && mbar_test_wait(smem_u32(&sm.opfull[ky1 & 1u][1]), (ky1 >> 1) & 1u)) {
           tc_fence_after();
-          ssd_issue_y(sm, sm.st[ky1 % kSsdStages], tmem + (ky1 % kSsdAcc) * 128, 1);
-          tc_commit(smem_u32(&sm.gop_empty[1]));
-          tc_commit(smem_u32(&sm.yfull[ky1 % kSsdAcc]));
+          const uint32_t a = ky1 & 1u, e = ky1 % kSsdAcc;
+          ssd_issue_y(sm, sm.st[ky1 % kSsdStages], tmem + 128 * a, tmem + 256 + 64 * e, 1, (int)a);
+          tc_commit(smem_u32(&sm.aempty[a]));
+          tc_commit(smem_u32(&sm.yfull[e]));
           ++ky1;
           moved = true;
         }
-        if (ky0 < kg && mbar_test_wait(smem_u32(&sm.gop_full[0]), ky0 & 1u)) {
+        if (ky0 < kg && mbar_test_wait(smem_u32(&sm.opfull[ky0 & 1u][0]), (ky0 >> 1) & 1u) &&
+            mbar_test_wait(smem_u32(&sm.yempty[ky0 % kSsdAcc]), ((ky0 / kSsdAcc) & 1u) ^ 1u)) {
           tc_fence_after();
-          ssd_issue_y(sm, sm.st[ky0 % kSsdStages], tmem + (ky0 % kSsdAcc) * 128, 0);
-          tc_commit(smem_u32(&sm.gop_empty[0]));
+          const uint32_t a = ky0 & 1u, e = ky0 % kSsdAcc;
+          ssd_issue_y(sm, sm.st[ky0 % kSsdStages], tmem + 128 * a, tmem + 256 + 64 * e, 0, (int)a);
           ++ky0;
           moved = true;
         }
         if (kg < n_mine && mbar_test_wait(smem_u32(&sm.full[kg % kSsdStages]), (kg / kSsdStages) & 1u) &&
-            mbar_test_wait(smem_u32(&sm.tmem_empty[kg % kSsdAcc]), ((kg / kSsdAcc) & 1u) ^ 1u)) {
+            mbar_test_wait(smem_u32(&sm.aempty[kg & 1u]), ((kg >> 1) & 1u) ^ 1u)) {
           tc_fence_after();
           const SsdStage& st = sm.st[kg % kSsdStages];
-          tc_mma_f16(tmem + (kg % kSsdAcc) * 128, umma_desc(smem_u32(st.c), 256, 6),
-                     umma_desc(smem_u32(st.b), 256, 6), ig, false);
-          tc_commit(smem_u32(&sm.gfull[kg % kSsdAcc]));
+          tc_mma_f16(tmem + 128 * (kg & 1u), umma_desc(smem_u32(st.c), 256, 6), umma_desc(smem_u32(st.b), 256, 6),
+                     ig, false);
+          tc_commit(smem_u32(&sm.gfull[kg & 1u]));
           ++kg;
           moved = true;
         }
@@ -680,88 +694,81 @@ __global__ void __launch_bounds__(kSsdOutThreads, 1)
         }
       }
     }
-  } else if (warp >= 4 && warp < 12) {  // G -> operand
+  } else if (warp >= 4 && warp < 12) {  // G -> G' in place
     const int q4 = warp & 3, kh = (warp - 4) >> 2, cw = warp - 4;
     const int i = 32 * q4 + lane;  // this thread's row (token of the chunk)
     const uint32_t lanes = (uint32_t)(32 * q4) << 16;
-    const uint32_t ghi = smem_u32(sm.ghi[kh]), glo = smem_u32(sm.glo[kh]);
-    // the blocks above the diagonal, zero for every tile
-#pragma unroll
-    for (int gq = 0; gq < 2; ++gq)
-      if (64 * kh + 32 * gq > 32 * q4)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          st_shared_v4(sw128(ghi, i, 4 * gq + q), 0u, 0u, 0u, 0u);
-          st_shared_v4(sw128(glo, i, 4 * gq + q), 0u, 0u, 0u, 0u);
-        }
     float* fd = sm.fdt[cw];
     for (uint32_t k = 0; k < n_mine; ++k) {
       const int s = (int)(k % kSsdStages);
-      const uint32_t a = k % kSsdAcc;
+      const uint32_t a = k & 1u;
+      // G formed in score buffer a (which also means tile k - 2's Y product,
+      // and with it its reads of the state operand's buffer a, are done)
       const bool mine = mbar_wait_bounded(smem_u32(&sm.full[s]), (k / kSsdStages) & 1u, p.timeout_ns) &&
-                        mbar_wait_bounded(smem_u32(&sm.gfull[a]), (k / kSsdAcc) & 1u, p.timeout_ns) &&
-                        mbar_wait_bounded(smem_u32(&sm.gop_empty[kh]), (k & 1u) ^ 1u, p.timeout_ns);
+                        mbar_wait_bounded(smem_u32(&sm.gfull[a]), (k >> 1) & 1u, p.timeout_ns);
       if (!__all_sync(0xffffffffu, mine)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const SsdStage& st = sm.st[s];
+      SsdStage& st = sm.st[s];
       const float ai = st.cum[i].x;
+      const uint32_t gbuf = tmem + lanes + 128 * a;
 #pragma unroll
       for (int gq = 0; gq < 2; ++gq) {
         const int col0 = 64 * kh + 32 * gq;  // the group's first column (token r)
-        if (col0 > 32 * q4) continue;        // above the diagonal for the whole warp: zero, written once
-        const float ar = st.cum[col0].x;
-        const bool fast = __fsub_rn(ar, st.cum[col0 + 31].x) <= 60.0f;  // the group's decay span
-        {
-          const float2 v = st.cum[col0 + lane];
-          fd[32 * gq + lane] = __fmul_rn(ex2_approx(__fsub_rn(ar, v.x)), v.y);
-        }
-        __syncwarp();
-        const float ri = ex2_approx(__fsub_rn(ai, ar));
-        const float2 ri2 = make_float2(ri, ri);
-        uint32_t graw[32];
-        tmem_ld_32cols(tmem + lanes + a * 128 + col0, graw);
-        const bool diag = col0 == 32 * q4;
         uint32_t hi[16], lo[16];
+        if (col0 > 32 * q4) {  // above the diagonal for the whole warp: zero
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          float2 f01, f23;
-          if (fast) {
-            const float4 fv = *reinterpret_cast<const float4*>(fd + 32 * gq + 4 * e4);
-            f01 = __fmul2_rn(ri2, make_float2(fv.x, fv.y));
-            f23 = __fmul2_rn(ri2, make_float2(fv.z, fv.w));
-          } else {
-            float f[4];
+          for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0u;
+        } else {
+          const float ar = st.cum[col0].x;
+          const bool fast = __fsub_rn(ar, st.cum[col0 + 31].x) <= 60.0f;  // the group's decay span
+          {
+            const float2 v = st.cum[col0 + lane];
+            fd[32 * gq + lane] = __fmul_rn(ex2_approx(__fsub_rn(ar, v.x)), v.y);
+          }
+          __syncwarp();
+          const float ri = ex2_approx(__fsub_rn(ai, ar));
+          const float2 ri2 = make_float2(ri, ri);
+          uint32_t graw[32];
+          tmem_ld_32cols(gbuf + col0, graw);
+          const bool diag = col0 == 32 * q4;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float2 v = st.cum[col0 + 4 * e4 + u];
-              f[u] = __fmul_rn(ex2_approx(__fsub_rn(ai, v.x)), v.y);
+          for (int e4 = 0; e4 < 8; ++e4) {
+            float2 f01, f23;
+            if (fast) {
+              const float4 fv = *reinterpret_cast<const float4*>(fd + 32 * gq + 4 * e4);
+              f01 = __fmul2_rn(ri2, make_float2(fv.x, fv.y));
+              f23 = __fmul2_rn(ri2, make_float2(fv.z, fv.w));
+            } else {
+              float f[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float2 v = st.cum[col0 + 4 * e4 + u];
+                f[u] = __fmul_rn(ex2_approx(__fsub_rn(ai, v.x)), v.y);
+              }
+              f01 = make_float2(f[0], f[1]);
+              f23 = make_float2(f[2], f[3]);
             }
-            f01 = make_float2(f[0], f[1]);
-            f23 = make_float2(f[2], f[3]);
+            float2 v01 = __fmul2_rn(make_float2(__uint_as_float(graw[4 * e4]), __uint_as_float(graw[4 * e4 + 1])), f01);
+            float2 v23 =
+                __fmul2_rn(make_float2(__uint_as_float(graw[4 * e4 + 2]), __uint_as_float(graw[4 * e4 + 3])), f23);
+            if (diag) {
+              const int j = col0 + 4 * e4;
+              if (j > i) v01.x = 0.0f;
+              if (j + 1 > i) v01.y = 0.0f;
+              if (j + 2 > i) v23.x = 0.0f;
+              if (j + 3 > i) v23.y = 0.0f;
+            }
+            split_bf16_x2(v01, hi[2 * e4], lo[2 * e4]);
+            split_bf16_x2(v23, hi[2 * e4 + 1], lo[2 * e4 + 1]);
           }
-          float2 v01 = __fmul2_rn(make_float2(__uint_as_float(graw[4 * e4]), __uint_as_float(graw[4 * e4 + 1])), f01);
-          float2 v23 =
-              __fmul2_rn(make_float2(__uint_as_float(graw[4 * e4 + 2]), __uint_as_float(graw[4 * e4 + 3])), f23);
-          if (diag) {
-            const int j = col0 + 4 * e4;
-            if (j > i) v01.x = 0.0f;
-            if (j + 1 > i) v01.y = 0.0f;
-            if (j + 2 > i) v23.x = 0.0f;
-            if (j + 3 > i) v23.y = 0.0f;
-          }
-          split_bf16_x2(v01, hi[2 * e4], lo[2 * e4]);
-          split_bf16_x2(v23, hi[2 * e4 + 1], lo[2 * e4 + 1]);
+          __syncwarp();  // fd is read before the next group overwrites it
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int piece = 4 * gq + q;
-          st_shared_v4(sw128(ghi, i, piece), hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
-          st_shared_v4(sw128(glo, i, piece), lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
-        }
-        __syncwarp();  // fd is read before the next group overwrites it
+        // in place: the group's 32 fp32 columns become 16 columns of hi pairs, 16 of lo pairs
+        tmem_st_16cols(gbuf + col0, hi);
+        tmem_st_16cols(gbuf + col0 + 16, lo);
       }
       if (kh == 1) {  // the entering state: row n, 8 channels (one 16-byte piece) per thread
         const int n = i >> 3, piece = i & 7;
@@ -772,13 +779,30 @@ __global__ void __launch_bounds__(kSsdOutThreads, 1)
         split_bf16_x2(make_float2(v0.z, v0.w), h[1], l[1]);
         split_bf16_x2(make_float2(v1.x, v1.y), h[2], l[2]);
         split_bf16_x2(make_float2(v1.z, v1.w), h[3], l[3]);
-        st_shared_v4(sw128(smem_u32(sm.shi), n, piece), h[0], h[1], h[2], h[3]);
-        st_shared_v4(sw128(smem_u32(sm.slo), n, piece), l[0], l[1], l[2], l[3]);
+        st_shared_v4(sw128(smem_u32(sm.shi[a]), n, piece), h[0], h[1], h[2], h[3]);
+        st_shared_v4(sw128(smem_u32(sm.slo[a]), n, piece), l[0], l[1], l[2], l[3]);
+        // row i of C times e_i = 2^(acum_i), as hi + lo over the stage's B
+        // and C tiles (read by the G product, which is done)
+        const float ei = ex2_approx(ai);
+        const float2 ei2 = make_float2(ei, ei);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint4 cv;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(cv.x), "=r"(cv.y), "=r"(cv.z), "=r"(cv.w)
+                       : "r"(sw32(smem_u32(st.c), i, q)));
+          const uint32_t cw4[4] = {cv.x, cv.y, cv.z, cv.w};
+          uint32_t eh[4], el[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split_bf16_x2(__fmul2_rn(unpack_bf16(cw4[e]), ei2), eh[e], el[e]);
+          st_shared_v4(sw32(smem_u32(st.b), i, q), eh[0], eh[1], eh[2], eh[3]);
+          st_shared_v4(sw32(smem_u32(st.c), i, q), el[0], el[1], el[2], el[3]);
+        }
       }
-      fence_proxy_async_smem();  // the operands, visible to the tensor core
-      tc_fence_before();         // and G's columns read out before they are overwritten
+      fence_proxy_async_smem();  // the shared-memory operands, visible to the tensor core
+      tc_fence_before();         // and G' in tensor memory, written, before the MMAs read it
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.gop_full[kh]));
+      if (lane == 0) mbar_arrive(smem_u32(&sm.opfull[a][kh]));
     }
   } else if (warp >= 12) {  // epilogue
     const int q4 = warp & 3;
@@ -786,26 +810,25 @@ __global__ void __launch_bounds__(kSsdOutThreads, 1)
     const uint32_t lanes = (uint32_t)(32 * q4) << 16;
     for (uint32_t k = 0; k < n_mine; ++k) {
       const int s = (int)(k % kSsdStages);
-      const uint32_t a = k % kSsdAcc;
+      const uint32_t e = k % kSsdAcc;
       const SsdTileId id = ssd_tile(blockIdx.x + k * gridDim.x, H, nC);
       const float Dh = __ldg(p.Dskip + id.h);  // in flight while the accumulators are waited for
-      const bool mine = mbar_wait_bounded(smem_u32(&sm.yfull[a]), (k / kSsdAcc) & 1u, p.timeout_ns) &&
+      const bool mine = mbar_wait_bounded(smem_u32(&sm.yfull[e]), (k / kSsdAcc) & 1u, p.timeout_ns) &&
                         mbar_wait_bounded(smem_u32(&sm.full[s]), (k / kSsdStages) & 1u, p.timeout_ns) &&
-                        (!gate || mbar_wait_bounded(smem_u32(&sm.zfull[k & 1u]), (k >> 1) & 1u, p.timeout_ns));
+                        (!gate || mbar_wait_bounded(smem_u32(&sm.zfull[k % kSsdZ]), (k / kSsdZ) & 1u, p.timeout_ns));
       if (!__all_sync(0xffffffffu, mine)) {
         ok = false;
         break;
       }
       tc_fence_after();
       SsdStage& st = sm.st[s];
-      const float ei = ex2_approx(st.cum[i].x);
-      const float2 ei2 = make_float2(ei, ei), Dh2 = make_float2(Dh, Dh);
-      const uint32_t xb = smem_u32(st.x), zb = smem_u32(sm.z[k & 1u]);
+      const float2 Dh2 = make_float2(Dh, Dh);
+      const uint32_t xb = smem_u32(st.x), zb = smem_u32(sm.z[k % kSsdZ]);
+      const uint32_t ybuf = tmem + lanes + 256 + 64 * e;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {  // 16 channels at a time
-        uint32_t yv[16], yo[16];
-        tmem_ld_16cols(tmem + lanes + a * 128 + 16 * r, yv);
-        tmem_ld_16cols(tmem + lanes + a * 128 + 64 + 16 * r, yo);
+        uint32_t yv[16];
+        tmem_ld_16cols(ybuf + 16 * r, yv);
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const uint32_t xa = sw128(xb, i, 2 * r + q);
@@ -822,23 +845,22 @@ __global__ void __launch_bounds__(kSsdOutThreads, 1)
           const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w};
           uint32_t out[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int kk = 8 * q + 2 * e;
-            float2 y2 = __ffma2_rn(ei2, make_float2(__uint_as_float(yo[kk]), __uint_as_float(yo[kk + 1])),
+          for (int u = 0; u < 4; ++u) {
+            const int kk = 8 * q + 2 * u;
+            float2 y2 = __ffma2_rn(Dh2, unpack_bf16(xw[u]),
                                    make_float2(__uint_as_float(yv[kk]), __uint_as_float(yv[kk + 1])));
-            y2 = __ffma2_rn(Dh2, unpack_bf16(xw[e]), y2);
-            if (gate) y2 = __fmul2_rn(y2, silu_tanh_x2(unpack_bf16(zw[e])));
-            out[e] = pack_bf16(y2.x, y2.y);
+            if (gate) y2 = __fmul2_rn(y2, silu_tanh_x2(unpack_bf16(zw[u])));
+            out[u] = pack_bf16(y2.x, y2.y);
           }
           st_shared_v4(xa, out[0], out[1], out[2], out[3]);
         }
       }
-      tc_fence_before();  // the accumulators are read: tensor-memory buffer a is free
+      tc_fence_before();  // the accumulator is read: accumulator buffer e is free
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(smem_u32(&sm.tmem_empty[a]));
-        if (gate) mbar_arrive(smem_u32(&sm.zempty[k & 1u]));  // this warp's rows of z are read
+        mbar_arrive(smem_u32(&sm.yempty[e]));
+        if (gate) mbar_arrive(smem_u32(&sm.zempty[k % kSsdZ]));  // this warp's rows of z are read
         if (id.c * kSsdQ + 32 * q4 < L) {  // rows past the sequence's end are clipped (or all of them)
           tma_store_4d(&tm_y, 0, id.h, id.c * kSsdQ + 32 * q4, id.b, xb + 32 * q4 * 128);
           bulk_commit();
