@@ -347,7 +347,7 @@ mamba_status mamba_layer_fwd(const mamba_layer_args *args, void *stream);
  *   A_log, Dskip      (heads) fp32
  *   h0, final_state   (B, heads, 16, 64) fp32 or NULL
  *   workspace         mamba2_scan_workspace_size() bytes, 256-byte aligned:
- *                     per (batch row, head, chunk of 64 tokens) the chunk's
+ *                     per (batch row, head, chunk of 128 tokens) the chunk's
  *                     end state and entering state (16 x 64 fp32 each), its
  *                     decay sum, and per token its dt and decay prefix
  *

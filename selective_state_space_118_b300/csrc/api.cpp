@@ -62,8 +62,9 @@ struct Plan {
 };
 
 // The machine as the plan sees it: SM count and resident one-warp CTAs per SM
-// of each prefill kernel with bf16 I/O (from the occupancy calculator;
-// typical B300 values when no device answers, e.g. in a build without a GPU).
+// of the main-pass kernel and of the fused carry-and-main kernel (which runs
+// the carry walks), bf16 I/O (from the occupancy calculator; typical B300
+// values when no device answers, e.g. in a build without a GPU).
 struct Machine {
   int sms;
   int main_per_sm;
@@ -124,7 +125,10 @@ constexpr int kCarryTilesEstimate = 64;
 
 // Relative costs of the plan's model: a main-pass tile and a carry-walk tile
 // (16 tokens x 32 channels each) and one hop of a carry chain, in units of
-// ~1,800 issued warp-instructions.
+// ~1,800 issued warp-instructions.  The model adds the two passes' times;
+// they share one launch and overlap in part, and a sweep of the chunk count
+// at 4,096 and 32,768 tokens (x 8,192 channels) found the model's choice
+// still the fastest.
 constexpr double kMainTileCost = 1.0;
 constexpr double kCarryTileCost = 0.7;
 constexpr double kChainHopCost = 1.5;

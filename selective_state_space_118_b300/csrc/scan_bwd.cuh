@@ -38,7 +38,7 @@
 // of linear recurrence as the state, run backwards:
 //   R_{t-1} = dA_t (C_t dyss_t + R_t),        R_{L-1} = dl/dfinal_h
 // (dyss does not depend on the state), so the adjoint-carry warps compute the
-// carries like the forward's scan_carry_kernel with time reversed: one warp
+// carries like the forward's carry walks with time reversed: one warp
 // per boundary walks the next chunk forwards in pieces, each piece scanned
 // backwards from zero, and stops once the decay from the boundary makes the
 // rest negligible (below 2^-32), or chains onto the next boundary's carry.

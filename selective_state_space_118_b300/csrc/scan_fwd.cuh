@@ -22,8 +22,9 @@
 //
 // Chunked mode.  At batch 1 the groups alone cannot fill the GPU, so the
 // sequence is cut into n_chunks chunks that run in parallel, each starting
-// from its carried-in state.  Those carries come from a first kernel,
-// scan_carry_kernel (described with it below): one warp per chunk boundary
+// from its carried-in state.  Those carries come from carry walks
+// (carry_warp, described with it below) that run in the same launch as the
+// main pass (scan_fused_kernel, at the end): one warp per chunk boundary
 // and channel group walks the previous chunk backwards in pieces and stops
 // where the decay to the boundary makes earlier tokens negligible (below
 // 2^-32 for every state), or else chains onto the previous boundary's carry;
