@@ -224,10 +224,15 @@ __global__ void __launch_bounds__(kLanes)
   CChannel ch;
   load_cchannel(ch, p, cl);
   const size_t sidx = ((size_t)b * D + cl) * 16;  // this channel's 16 numbers in (B, D, 16)
+  // In the chunked mode the fold (an earlier launch) copied h0 into the
+  // carry's chunk-0 slot and v0 into the unused last slot of hloc, so that
+  // no CTA of this launch reads h0 or v0, which the last chunk's final_h and
+  // final_v may alias.
+  const bool folded = !kSummary && p.n_chunks > 1;
   CState st, vp;
-  if (kSummary || (j == 0 && p.h0 == nullptr))
+  if (kSummary || (j == 0 && !folded && p.h0 == nullptr))
     cstate_zero(st);
-  else if (j == 0)
+  else if (j == 0 && !folded)
     cstate_load(st, p.h0 + sidx);
   else
     cstate_load(st, p.carry + (((size_t)b * p.n_chunks + j) * D + cl) * 16);
@@ -238,10 +243,12 @@ __global__ void __launch_bounds__(kLanes)
   float xm1 = cinput_at<IO>(p, b, (long)t_begin - 1, cl);
   if (kTrap) {  // the state input of the token before the chunk
     if (j == 0) {
-      if (p.v0)
-        cstate_load(vp, p.v0 + sidx);
-      else
+      if (p.v0 == nullptr)
         cstate_zero(vp);
+      else if (folded)
+        cstate_load(vp, p.hloc + (((size_t)b * p.n_chunks + p.n_chunks - 1) * D + cl) * 16);
+      else
+        cstate_load(vp, p.v0 + sidx);
     } else {
       const float xm4 = cinput_at<IO>(p, b, (long)t_begin - 4, cl);
       const float u = silu(conv4(ch.w, ch.bias, xm4, xm3, xm2, xm1));
@@ -339,6 +346,8 @@ __global__ void __launch_bounds__(kLanes)
 
 // The fold: one thread per (batch row, channel); h_in_{j+1} = W_j h_in_j +
 // hloc_j in chunk order, h_in_0 = h0 (or zero); W_j = exp(lambda S_j).
+// h_in_0 goes to the carry's chunk-0 slot and v0 to hloc's last slot (the
+// summary pass leaves it unused), from which the main pass reads them.
 __global__ void __launch_bounds__(256) complex_fold_kernel(const __grid_constant__ ComplexParams p) {
   const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long)p.batch * p.d_inner) return;
@@ -351,6 +360,12 @@ __global__ void __launch_bounds__(256) complex_fold_kernel(const __grid_constant
     cstate_load(h, p.h0 + ((size_t)b * D + c) * 16);
   else
     cstate_zero(h);
+  cstate_store(h, p.carry + ((size_t)b * p.n_chunks * D + c) * 16);
+  if (p.v0) {
+    CState v;
+    cstate_load(v, p.v0 + ((size_t)b * D + c) * 16);
+    cstate_store(v, p.hloc + (((size_t)b * p.n_chunks + p.n_chunks - 1) * D + c) * 16);
+  }
   for (int j = 0; j + 1 < p.n_chunks; ++j) {
     const size_t cj = ((size_t)b * p.n_chunks + j) * D + c;
     CState hl;

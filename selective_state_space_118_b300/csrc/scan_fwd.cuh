@@ -360,22 +360,22 @@ __device__ __forceinline__ void main_warp(const CUtensorMap& tm_x, const CUtenso
   else
     state16_zero(st);
 
-  // the conv's earlier inputs; chunk 0 also writes the final conv state (it
-  // is the one CTA of these channels that reads conv_state0, which the final
-  // state may alias: everything is read before anything is written)
+  // the conv's earlier inputs
   float xm3 = input_at<IO>(p, b, (long)t_begin - 3, cl);
   float xm2 = input_at<IO>(p, b, (long)t_begin - 2, cl);
   float xm1 = input_at<IO>(p, b, (long)t_begin - 1, cl);
-  if (j == 0 && p.final_conv_state != nullptr) {
-    const float f0 = input_at<IO>(p, b, (long)p.seqlen - 3, cl);
-    const float f1 = input_at<IO>(p, b, (long)p.seqlen - 2, cl);
-    const float f2 = input_at<IO>(p, b, (long)p.seqlen - 1, cl);
+  // final_h and final_conv_state may alias h0 and conv_state0.  In the one
+  // launch of the chunked mode their readers are chunk 0's main warp (here)
+  // and boundary 1's carry walk; each counts itself done on the group's
+  // chunk-0 flag, which the last chunk's warp awaits before it writes.
+  unsigned* const readers = wait_carry && p.n_chunks > 1
+                                ? p.counters + 1 + (size_t)b * p.n_groups * p.n_chunks + (size_t)g * p.n_chunks
+                                : nullptr;
+  if (readers != nullptr && j == 0) {
     __syncwarp();
-    if (active) {
-      IO* fcs = reinterpret_cast<IO*>(p.final_conv_state) + (size_t)b * 3 * D + c;
-      fcs[0] = from_f32<IO>(f0);
-      fcs[D] = from_f32<IO>(f1);
-      fcs[2 * (size_t)D] = from_f32<IO>(f2);
+    if (lane == 0) {
+      __threadfence();
+      atomicAdd(readers, 1u);
     }
   }
 
@@ -421,7 +421,36 @@ __device__ __forceinline__ void main_warp(const CUtensorMap& tm_x, const CUtenso
     }
     return;
   }
-  if (j == p.n_chunks - 1 && p.final_h && active) state16_store(st, p.final_h + ((size_t)b * D + c) * kN);
+  if (j == p.n_chunks - 1 && (p.final_h != nullptr || p.final_conv_state != nullptr)) {
+    if (readers != nullptr) {  // wait (bounded) until h0 and conv_state0 have been read
+      bool have = true;
+      if (lane == 0) {
+        const uint64_t t_start = globaltimer_ns();
+        while (atomicAdd(readers, 0u) < 2u) {
+          if (globaltimer_ns() - t_start > p.timeout_ns) {
+            have = false;
+            break;
+          }
+        }
+        if (!have) report_error(4u);  // MAMBA_ERR_TIMEOUT
+      }
+      __syncwarp();
+      __threadfence();
+    }
+    const float f0 = input_at<IO>(p, b, (long)p.seqlen - 3, cl);
+    const float f1 = input_at<IO>(p, b, (long)p.seqlen - 2, cl);
+    const float f2 = input_at<IO>(p, b, (long)p.seqlen - 1, cl);
+    __syncwarp();
+    if (active) {
+      if (p.final_h != nullptr) state16_store(st, p.final_h + ((size_t)b * D + c) * kN);
+      if (p.final_conv_state != nullptr) {
+        IO* fcs = reinterpret_cast<IO*>(p.final_conv_state) + (size_t)b * 3 * D + c;
+        fcs[0] = from_f32<IO>(f0);
+        fcs[D] = from_f32<IO>(f1);
+        fcs[2 * (size_t)D] = from_f32<IO>(f2);
+      }
+    }
+  }
 }
 
 // grid (n_groups, batch, n_chunks), 32 threads: the carries were computed by
@@ -645,7 +674,12 @@ __device__ __forceinline__ void carry_warp(const CUtensorMap& tm_x, const CUtens
   if (active) state16_store(acc, p.carry + (((size_t)b * p.n_chunks + j) * D + c) * kN);
   __threadfence();
   __syncwarp();
-  if (lane == 0) atomicExch(ready + j, 1u);
+  if (lane == 0) {
+    atomicExch(ready + j, 1u);
+    // boundary 1's walk is done reading h0 and conv_state0 (the final states
+    // may alias them): count it on the group's chunk-0 flag
+    if (j == 1) atomicAdd(ready, 1u);
+  }
 }
 
 // ---------------------------------------------------------------- carries and main pass in one launch

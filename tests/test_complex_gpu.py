@@ -134,6 +134,22 @@ def test_split_calls_equal_one_call_bitwise(rule, io):
 
 
 @pytest.mark.parametrize("rule", sorted(RULES))
+@pytest.mark.parametrize("n_chunks", [1, 3, 7])
+def test_final_states_may_alias_initial_states(rule, n_chunks):
+    """final_h, final_conv_state and final_v given the buffers of h0,
+    conv_state0 and v0 (the header allows it): the same bits as with separate
+    buffers, one pass and chunked."""
+    inp = make(2, 300, 64, "bf16", seed=631)
+    ref = [t.clone() for t in run_gpu(inp, RULES[rule], n_chunks=n_chunks)]
+    h, cs, v = inp["h0"].clone(), inp["conv_state0"].clone(), inp["v0"].clone()
+    out = run_gpu(dict(inp, h0=h, conv_state0=cs, v0=v), RULES[rule], final_h=h, final_conv_state=cs, final_v=v,
+                  n_chunks=n_chunks)
+    torch.cuda.synchronize()
+    assert torch.equal(out[0], ref[0])
+    assert torch.equal(h, ref[1]) and torch.equal(cs, ref[2]) and torch.equal(v, ref[3])
+
+
+@pytest.mark.parametrize("rule", sorted(RULES))
 def test_chunked_equals_one_pass_within_tolerance(rule):
     inp = make(1, 64 * 40 + 7, 32, "f32", seed=621)
     y1, fh1, fcs1, fv1 = [t.clone() for t in run_gpu(inp, RULES[rule], n_chunks=1)]

@@ -81,9 +81,14 @@ def test_seqlen_zero_returns_initial_state():
     assert torch.all(fh == 0) and torch.all(fcs == 0)
 
 
-@pytest.mark.parametrize("n_chunks", [1, 3])
-def test_final_state_may_alias_initial_state(n_chunks):
-    inp = inputs.scan_inputs(2, 300, 32, "bf16", seed=7, device="cuda", with_state=True)
+@pytest.mark.parametrize("L,n_chunks", [(300, 1), (300, 3), (1000, 9), (4096, 4)])
+def test_final_state_may_alias_initial_state(L, n_chunks):
+    """final_h and final_conv_state given the buffers of h0 and conv_state0:
+    the same bits as with separate buffers.  In the chunked launch chunk 0's
+    main warp and boundary 1's carry walk read h0 and conv_state0 while the
+    last chunk runs (walks of several pieces; at L = 4096 the walks stop
+    early on the decay)."""
+    inp = inputs.scan_inputs(2, L, 32, "bf16", seed=7, device="cuda", with_state=True)
     ref = [t.clone() for t in run_gpu(inp, n_chunks=n_chunks)]
     h, cs = inp["h0"].clone(), inp["conv_state0"].clone()
     inp2 = dict(inp, h0=h, conv_state0=cs)
@@ -249,13 +254,14 @@ def test_exact_carry_flag_with_hidden_large_state():
     B, L, D = 1, 8192, 32
     inp = inputs.scan_inputs(B, L, D, "f32", seed=83, device="cuda", with_state=True)
     inp["A_log"] = torch.zeros_like(inp["A_log"])  # A = -1: every state decays at the same rate
-    # dt = 0.02 on every token: the walk over chunk 0 stops after five pieces,
-    # at token 768, and drops tokens 0..767
+    # dt = 0.02 on every token: the walk over chunk 0 stops once the decay
+    # to the boundary passes 2^-32 (1,109 tokens), after 18 pieces of 64, at
+    # token 896, and drops tokens 0..895
     inp["dt_raw"] = torch.full_like(inp["dt_raw"], float(np.log(np.expm1(0.02))))
     inp["x"][:, 700:768] *= 1e8
     inp["z"][:, :2048] = 0.0
     plan = ops.mamba_scan_plan(B, L, D, 4)
-    assert plan["n_chunks"] == 4 and plan["piece_len"] == 256
+    assert plan["n_chunks"] == 4 and plan["piece_len"] == 64
     y, fh, fcs = run_gpu(inp, n_chunks=4, flags=ops.MAMBA_FLAG_EXACT_CARRY)
     check_against_oracle(inp, (y, fh, fcs), "exact carries, hidden large state")
     y1, fh1, _ = run_gpu(inp, n_chunks=1)
