@@ -405,6 +405,14 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// ---------------------------------------------------------------- flags
+// Relaxed load at GPU scope (the value in L2, never a stale L1 copy).
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------- dependent launch
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start while the previous kernel in the stream drains;
