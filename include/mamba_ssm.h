@@ -30,7 +30,10 @@
  *    default stream) and never synchronise.  Argument errors are reported
  *    before anything is launched; a launch failure returns MAMBA_ERR_CUDA.
  *  - d_state must be 16 and d_conv 4 (the layer's defaults); d_inner must be
- *    a multiple of 16.
+ *    a multiple of 8 for bf16 I/O and of 4 for fp32 (the channel rows are
+ *    read by bulk tensor copies, whose row stride must be a multiple of 16
+ *    bytes).  The size and plan queries, which take no dtype, accept any
+ *    multiple of 4.
  *  - A device-side wait that gives up (it cannot, in a healthy run) sets a
  *    sticky error word that mamba_last_error() reports.
  */
@@ -47,7 +50,7 @@ extern "C" {
 typedef enum {
     MAMBA_OK = 0,
     MAMBA_ERR_INVALID_ARG = 1,   /* null required pointer, bad size, misalignment */
-    MAMBA_ERR_UNSUPPORTED = 2,   /* d_state != 16, d_conv != 4, d_inner % 16, dtype */
+    MAMBA_ERR_UNSUPPORTED = 2,   /* d_state != 16, d_conv != 4, d_inner not a multiple of 8 (bf16) or 4 (fp32), dtype */
     MAMBA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
     MAMBA_ERR_TIMEOUT = 4,       /* a device-side wait gave up (sticky, see below) */
     MAMBA_ERR_WORKSPACE = 5      /* workspace missing or smaller than required */
@@ -300,7 +303,7 @@ mamba_status mamba_scan_bwd(const mamba_scan_bwd_args *args, void *stream);
  *                     aligned: the intermediates and the scan's workspace
  *   n_chunks          the scan's, as for mamba_scan_fwd
  *
- * d_model and dt_rank must be multiples of 8, d_inner of 16.
+ * d_model, dt_rank and d_inner must be multiples of 8.
  */
 typedef struct mamba_layer_args {
     int batch, seqlen, d_model, d_inner, dt_rank, d_state, d_conv;
@@ -414,7 +417,7 @@ mamba_status mamba2_scan_fwd(const mamba2_scan_args *args, void *stream);
  *   discretization    MAMBA3_EULER or MAMBA3_TRAPEZOIDAL
  *   wait_timeout_ns   limit of every device-side wait (0: 1 second)
  *
- * d_state must be 16, d_conv 4, d_inner a multiple of 16.  seqlen may be 0
+ * d_state must be 16, d_conv 4, d_inner as for mamba_scan_fwd.  seqlen may be 0
  * (the final states are then copies of the initial ones, or zeros).
  * Precision: the turn dt theta is reduced to [-pi, pi] exactly (its whole
  * revolutions removed with the product's rounding error kept), but it

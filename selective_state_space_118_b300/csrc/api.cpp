@@ -332,11 +332,17 @@ mamba_status tc_linear(const void* A, long lda, const void* W, const void* bias,
   return mamba::launch_gemm_tc(ma, mw, mc, p, stream) == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
 
+// The channel rows of the (B, L, D) tensors are read by bulk tensor copies,
+// whose row stride (D elements) must be a multiple of 16 bytes: d_inner a
+// multiple of 8 for bf16 and of 4 for fp32.  Groups of channels past D are
+// filled with zeros by the copies and masked in every kernel.
+int d_inner_multiple(mamba_dtype io) { return io == MAMBA_BF16 ? 8 : 4; }
+
 mamba_status check_common(int batch, int d_inner, int d_state, int d_conv, mamba_dtype io) {
   if (batch <= 0 || d_inner <= 0) return MAMBA_ERR_INVALID_ARG;
   if (io != MAMBA_F32 && io != MAMBA_BF16) return MAMBA_ERR_UNSUPPORTED;
   if (d_state != MAMBA_D_STATE || d_conv != MAMBA_D_CONV) return MAMBA_ERR_UNSUPPORTED;
-  if (d_inner % 16 != 0) return MAMBA_ERR_UNSUPPORTED;
+  if (d_inner % d_inner_multiple(io) != 0) return MAMBA_ERR_UNSUPPORTED;
   return MAMBA_OK;
 }
 
@@ -463,13 +469,13 @@ const char* mamba_status_string(mamba_status s) {
 }
 
 int mamba_scan_default_chunks(int batch, int seqlen, int d_inner) {
-  if (batch <= 0 || seqlen <= 0 || d_inner <= 0 || d_inner % 16) return 1;
+  if (batch <= 0 || seqlen <= 0 || d_inner <= 0 || d_inner % 4) return 1;
   return make_plan(batch, seqlen, d_inner, 0).n_chunks;
 }
 
 mamba_status mamba_scan_plan(int batch, int seqlen, int d_inner, int n_chunks, int out[4]) {
   if (!out || batch <= 0 || seqlen <= 0 || d_inner <= 0 || n_chunks < 0) return MAMBA_ERR_INVALID_ARG;
-  if (d_inner % 16) return MAMBA_ERR_UNSUPPORTED;
+  if (d_inner % 4) return MAMBA_ERR_UNSUPPORTED;
   const Plan pl = make_plan(batch, seqlen, d_inner, n_chunks);
   out[0] = pl.n_chunks;
   out[1] = pl.chunk_tiles * kT;
@@ -479,7 +485,7 @@ mamba_status mamba_scan_plan(int batch, int seqlen, int d_inner, int n_chunks, i
 }
 
 size_t mamba_scan_workspace_size(int batch, int seqlen, int d_inner, int n_chunks) {
-  if (batch <= 0 || seqlen <= 0 || d_inner <= 0 || d_inner % 16 || n_chunks < 0) return 0;
+  if (batch <= 0 || seqlen <= 0 || d_inner <= 0 || d_inner % 4 || n_chunks < 0) return 0;
   return workspace_layout(batch, seqlen, d_inner, make_plan(batch, seqlen, d_inner, n_chunks)).total;
 }
 
@@ -527,7 +533,7 @@ mamba_status mamba_scan_fwd(const mamba_scan_args* a, void* stream_v) {
 }
 
 size_t mamba_scan_bwd_workspace_size(int batch, int seqlen, int d_inner, int n_chunks) {
-  if (batch <= 0 || seqlen <= 0 || d_inner <= 0 || d_inner % 16 || n_chunks < 0) return 0;
+  if (batch <= 0 || seqlen <= 0 || d_inner <= 0 || d_inner % 4 || n_chunks < 0) return 0;
   return bwd_workspace_layout(batch, seqlen, d_inner, make_plan(batch, seqlen, d_inner, n_chunks)).total;
 }
 
@@ -681,7 +687,7 @@ mamba_status mamba_scan_bwd(const mamba_scan_bwd_args* a, void* stream_v) {
 
 size_t mamba_layer_workspace_size(int batch, int seqlen, int d_model, int d_inner, int dt_rank, int n_chunks,
                                   int with_u_out) {
-  if (batch <= 0 || seqlen <= 0 || d_model <= 0 || d_inner <= 0 || d_inner % 16 || dt_rank <= 0 ||
+  if (batch <= 0 || seqlen <= 0 || d_model <= 0 || d_inner <= 0 || d_inner % 4 || dt_rank <= 0 ||
       n_chunks < 0)
     return 0;
   return layer_workspace_layout(batch, seqlen, d_inner, dt_rank, make_plan(batch, seqlen, d_inner, n_chunks),
@@ -887,7 +893,7 @@ mamba_status mamba_step(const mamba_step_args* a, void* stream_v) {
 }
 
 size_t mamba3_scan_workspace_size(int batch, int seqlen, int d_inner, int n_chunks) {
-  if (batch <= 0 || seqlen <= 0 || d_inner <= 0 || d_inner % 16 || n_chunks < 0) return 0;
+  if (batch <= 0 || seqlen <= 0 || d_inner <= 0 || d_inner % 4 || n_chunks < 0) return 0;
   return complex_workspace_layout(batch, seqlen, d_inner, complex_plan(batch, seqlen, d_inner, n_chunks)).total;
 }
 

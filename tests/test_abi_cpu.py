@@ -88,7 +88,8 @@ FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced: checks f
 @pytest.mark.parametrize("kw,status", [
     (dict(d_state=8), ops.MAMBA_ERR_UNSUPPORTED),
     (dict(d_conv=3), ops.MAMBA_ERR_UNSUPPORTED),
-    (dict(d_inner=24), ops.MAMBA_ERR_UNSUPPORTED),
+    (dict(d_inner=20), ops.MAMBA_ERR_UNSUPPORTED),  # bf16 rows of 40 bytes: not a multiple of 16
+    (dict(d_inner=6, io=ops.MAMBA_F32), ops.MAMBA_ERR_UNSUPPORTED),  # fp32 rows of 24 bytes
     (dict(io=7), ops.MAMBA_ERR_UNSUPPORTED),
     (dict(batch=0), ops.MAMBA_ERR_INVALID_ARG),
     (dict(seqlen=-1), ops.MAMBA_ERR_INVALID_ARG),
@@ -134,7 +135,7 @@ def test_bwd_argument_checks(lib):
     for k in ("dconv_w", "dx", "dfinal_h"):
         assert lib.mamba_scan_bwd(ctypes.byref(ops.BwdArgs(**dict(full, **{k: FAKE + 4}))), None) == \
             ops.MAMBA_ERR_INVALID_ARG, k
-    assert lib.mamba_scan_bwd(ctypes.byref(ops.BwdArgs(**dict(full, d_inner=24))), None) == \
+    assert lib.mamba_scan_bwd(ctypes.byref(ops.BwdArgs(**dict(full, d_inner=20))), None) == \
         ops.MAMBA_ERR_UNSUPPORTED
     assert lib.mamba_scan_bwd(ctypes.byref(ops.BwdArgs(**full)), None) == ops.MAMBA_ERR_WORKSPACE
     assert lib.mamba_scan_bwd(None, None) == ops.MAMBA_ERR_INVALID_ARG
@@ -148,7 +149,7 @@ def test_layer_argument_checks(lib):
     for kw, status in ((dict(io=ops.MAMBA_F32), ops.MAMBA_ERR_UNSUPPORTED),
                        (dict(dt_rank=12), ops.MAMBA_ERR_UNSUPPORTED),
                        (dict(d_model=60), ops.MAMBA_ERR_UNSUPPORTED),
-                       (dict(d_inner=24), ops.MAMBA_ERR_UNSUPPORTED),
+                       (dict(d_inner=20), ops.MAMBA_ERR_UNSUPPORTED),
                        (dict(seqlen=0), ops.MAMBA_ERR_INVALID_ARG),
                        (dict(W_x=FAKE + 2), ops.MAMBA_ERR_INVALID_ARG),
                        (dict(), ops.MAMBA_ERR_WORKSPACE)):
@@ -367,7 +368,7 @@ def test_complex_scan_argument_checks(lib):
         assert call(**{k: FAKE + 8}) == ops.MAMBA_ERR_INVALID_ARG, k
     assert call(discretization=2) == ops.MAMBA_ERR_UNSUPPORTED
     assert call(d_state=8) == ops.MAMBA_ERR_UNSUPPORTED
-    assert call(d_inner=24) == ops.MAMBA_ERR_UNSUPPORTED
+    assert call(d_inner=20) == ops.MAMBA_ERR_UNSUPPORTED
     assert call(seqlen=-1) == ops.MAMBA_ERR_INVALID_ARG
     assert call() == ops.MAMBA_ERR_WORKSPACE
     need = ops.mamba3_scan_workspace_size(1, 64, 32, 0)
@@ -386,7 +387,8 @@ def test_complex_scan_workspace(lib):
     ws = ops.mamba3_scan_workspace_size(B, L, D, n)
     assert need <= ws <= need + 4 * 256
     assert ops.mamba3_scan_workspace_size(1, 0, 64, 0) == 0
-    assert ops.mamba3_scan_workspace_size(1, 64, 24, 0) == 0
+    assert ops.mamba3_scan_workspace_size(1, 64, 22, 0) == 0  # no I/O type takes rows of 22 channels
+    assert ops.mamba3_scan_workspace_size(1, 64, 24, 0) > 0
 
 
 def test_linear_argument_checks(lib):

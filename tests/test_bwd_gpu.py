@@ -125,6 +125,11 @@ CASES = [
     (1, 49, 16, "f32", True, True, True, 3),
     (3, 1000, 64, "f32", True, True, True, 5),
     (1, 4096, 32, "bf16", True, True, True, 0),
+    # widths that are not multiples of 16
+    (2, 300, 40, "bf16", True, True, True, 1),
+    (1, 337, 40, "bf16", True, True, True, 3),
+    (1, 300, 36, "f32", True, True, True, 1),
+    (2, 337, 36, "f32", True, False, True, 4),
 ]
 
 

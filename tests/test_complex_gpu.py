@@ -78,6 +78,9 @@ EDGE = [
     (2, 337, 32, "bf16", True, 5),
     (3, 1000, 64, "f32", True, 7),
     (1, 4096, 32, "bf16", True, 0),
+    # widths that are not multiples of 16
+    (2, 300, 40, "bf16", True, 1),
+    (1, 337, 36, "f32", True, 3),
 ]
 
 

@@ -106,6 +106,7 @@ def stage_checks(p, v, u, out, fh, what):
     (2, 300, 256, 512, 32, 0),
     (2, 300, 256, 512, 32, 3),
     (1, 1000, 128, 96, 16, 4),
+    (1, 300, 64, 40, 8, 3),         # d_inner not a multiple of 16
     (1, 384, 4096, 8192, 256, 0),   # Jamba widths: hidden 4096, expand 2, dt_rank 256
 ])
 def test_layer_against_oracle(B, L, H, D, R, n_chunks):

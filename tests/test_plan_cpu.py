@@ -45,7 +45,7 @@ def bwd_workspace(B, L, D, n):
     return o
 
 
-sizes = st.tuples(st.integers(1, 4), st.integers(1, 300_000), st.integers(1, 1024).map(lambda k: 16 * k),
+sizes = st.tuples(st.integers(1, 4), st.integers(1, 300_000), st.integers(1, 4096).map(lambda k: 4 * k),
                   st.integers(0, 80))
 
 
@@ -80,7 +80,7 @@ def test_workspace_sizes_follow_the_layouts(s):
     assert ops.mamba_scan_bwd_workspace_size(B, L, D, n_req) == bwd_workspace(B, L, D, n)
 
 
-@pytest.mark.parametrize("args", [(0, 10, 16, 0), (1, 0, 16, 0), (1, 10, 0, 0), (1, 10, 24, 0), (1, 10, 16, -1)])
+@pytest.mark.parametrize("args", [(0, 10, 16, 0), (1, 0, 16, 0), (1, 10, 0, 0), (1, 10, 22, 0), (1, 10, 16, -1)])
 def test_sizes_without_a_plan(args):
     assert ops.mamba_scan_workspace_size(*args) == 0
     assert ops.mamba_scan_bwd_workspace_size(*args) == 0

@@ -54,6 +54,13 @@ EDGE = [
     (1, 337, 16, "bf16", False, False, 6),
     (3, 1000, 64, "f32", True, True, 5),
     (1, 4096, 16, "bf16", True, True, 0),
+    # widths that are not multiples of 16: a last group of 8 (bf16) or 4 (fp32) channels
+    (2, 300, 40, "bf16", True, True, 1),
+    (2, 300, 40, "bf16", True, True, 3),
+    (1, 300, 36, "f32", True, True, 1),
+    (1, 337, 36, "f32", True, False, 4),
+    (2, 130, 8, "bf16", True, True, 2),
+    (1, 65, 4, "f32", True, True, 1),
 ]
 
 

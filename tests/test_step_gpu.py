@@ -18,10 +18,11 @@ def step(st, tok, t):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("L,D", [(1, 48), (37, 48), (130, 48), (37, 80), (130, 208)])
+@pytest.mark.parametrize("L,D", [(1, 48), (37, 48), (130, 48), (37, 80), (130, 208), (37, 40), (130, 72)])
 def test_steps_equal_single_pass_scan_bitwise(io, L, D):
     """D = 48: one partial block of 64 channels (the step moves h in blocks
-    of 64 channels of a row); 80, 208: full blocks and a partial one."""
+    of 64 channels of a row); 80, 208: full blocks and a partial one; 40, 72:
+    widths that are not multiples of 16 (a last scan group of 8 channels)."""
     B = 2
     inp = inputs.scan_inputs(B, L, D, io, seed=L, device="cuda", with_state=True)
     y, fh, fcs = ops.mamba_scan_fwd(inp["x"], inp["z"], inp["dt_raw"], inp["Bm"], inp["Cm"],
