@@ -223,16 +223,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
 #pragma unroll 1
       for (int c = h; c < chunks; c += kGemmEpiWarps / 4) {
-        uint32_t r[32];
-        tmem_ld_32cols(tbase + 32 * c, r);
-        if (c + kGemmEpiWarps / 4 >= chunks) {  // this warp's share is in registers: hand it back
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(acc_empty);
-        }
         const int col0 = n0 + 32 * c;
         // the chunk's 32 bias values (the same for every lane: broadcast
-        // loads), four 16-byte vectors where the chunk lies inside N
+        // loads), four 16-byte vectors where the chunk lies inside N, issued
+        // before the chunk's TMEM load so that the two latencies overlap
         uint32_t bw[16];
 #pragma unroll
         for (int g = 0; g < 16; ++g) bw[g] = 0u;
@@ -254,6 +248,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               bw[g] = lo | (hi << 16);
             }
           }
+        }
+        uint32_t r[32];
+        tmem_ld_32cols(tbase + 32 * c, r);
+        if (c + kGemmEpiWarps / 4 >= chunks) {  // this warp's share is in registers: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty);
         }
         uint32_t pk[16];
 #pragma unroll
