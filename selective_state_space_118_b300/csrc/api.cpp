@@ -401,16 +401,22 @@ mamba_status launch_forward(const mamba_scan_args* a, const Plan& pl, const Work
   const mamba::ScanParams p = fwd_params(a, pl, ws, a->tile_states);
   const IoType io = a->io == MAMBA_BF16 ? IoType::BF16 : IoType::F32;
 
-  if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, bc_ld, stream) != cudaSuccess)
-    return MAMBA_ERR_CUDA;
-  if (pl.n_chunks > 1) {  // carries and main pass in one launch, the carry tasks first
-    if (cudaMemsetAsync(p.counters, 0, ws.counters_bytes, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+  if (pl.n_chunks > 1) {
+    // carries and main pass in one launch, the carry tasks first; the B/C
+    // widening before it zeroes its counters, and both launch as programmatic
+    // dependents (each waits for the kernel before it, so that a sequence of
+    // calls overlaps one launch with the previous one's end)
     const size_t per = (size_t)p.n_groups * B;
     const size_t ctas = (2 * (size_t)pl.n_chunks - 1) * per;
     if (ctas >= (1u << 31)) return MAMBA_ERR_UNSUPPORTED;
+    if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, bc_ld, stream, p.counters,
+                               (int)(ws.counters_bytes / sizeof(unsigned)), true) != cudaSuccess)
+      return MAMBA_ERR_CUDA;
     if (mamba::launch_scan_fused(io, maps, p, (unsigned)ctas, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
     return MAMBA_OK;
   }
+  if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, bc_ld, stream) != cudaSuccess)
+    return MAMBA_ERR_CUDA;
   dim3 g2((unsigned)p.n_groups, (unsigned)B, (unsigned)pl.n_chunks);
   if (mamba::launch_scan(io, maps, p, g2, stream) != cudaSuccess) return MAMBA_ERR_CUDA;
   return MAMBA_OK;

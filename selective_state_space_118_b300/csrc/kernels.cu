@@ -32,14 +32,30 @@ static cudaError_t launch_scan_t(const CUtensorMap* m, const ScanParams& p, dim3
   return p.y != nullptr ? launch_scan_y<IO, true>(m, p, grid, s) : launch_scan_y<IO, false>(m, p, grid, s);
 }
 
+// Launch configuration of a programmatic dependent: the kernel may start
+// while the one before it in the stream drains, and waits for it
+// (griddepcontrol.wait) before reading anything.
+static void set_pdl(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[1]) {
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+}
+
 template <typename IO, bool kY>
 static cudaError_t launch_fused_y(const CUtensorMap* m, const ScanParams& p, unsigned ctas, cudaStream_t s) {
   const size_t smem = fused_smem_bytes<IO>() + 128;
   cudaError_t e = cudaFuncSetAttribute(scan_fused_kernel<IO, kY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  scan_fused_kernel<IO, kY><<<ctas, kLanes, smem, s>>>(m[0], m[1], m[2], m[3], p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kLanes);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  set_pdl(cfg, attr);
+  return cudaLaunchKernelEx(&cfg, scan_fused_kernel<IO, kY>, m[0], m[1], m[2], m[3], p);
 }
 
 template <typename IO>
@@ -54,20 +70,26 @@ cudaError_t launch_scan_fused(IoType io, const CUtensorMap maps[4], const ScanPa
 }
 
 template <typename IO>
-static cudaError_t launch_widen_t(const void* Bm, const void* Cm, float* bc, long rows, int ld, cudaStream_t s) {
+static cudaError_t launch_widen_t(const void* Bm, const void* Cm, float* bc, long rows, int ld, unsigned* counters,
+                                  int n_counters, bool pdl, cudaStream_t s) {
   const long n = rows * 8;
   long blocks = (n + 255) / 256;
   if (blocks > 148L * 16) blocks = 148L * 16;
   if (blocks < 1) blocks = 1;
-  bc_widen_kernel<IO><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const IO*>(Bm), static_cast<const IO*>(Cm),
-                                                        bc, rows, ld);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (pdl) set_pdl(cfg, attr);
+  return cudaLaunchKernelEx(&cfg, bc_widen_kernel<IO>, static_cast<const IO*>(Bm), static_cast<const IO*>(Cm), bc,
+                            rows, ld, counters, n_counters);
 }
 
 cudaError_t launch_bc_widen(IoType io, const void* Bm, const void* Cm, float* bc, long rows, int ld,
-                            cudaStream_t stream) {
-  return io == IoType::BF16 ? launch_widen_t<__nv_bfloat16>(Bm, Cm, bc, rows, ld, stream)
-                            : launch_widen_t<float>(Bm, Cm, bc, rows, ld, stream);
+                            cudaStream_t stream, unsigned* counters, int n_counters, bool pdl) {
+  return io == IoType::BF16 ? launch_widen_t<__nv_bfloat16>(Bm, Cm, bc, rows, ld, counters, n_counters, pdl, stream)
+                            : launch_widen_t<float>(Bm, Cm, bc, rows, ld, counters, n_counters, pdl, stream);
 }
 
 cudaError_t launch_scan(IoType io, const CUtensorMap maps[4], const ScanParams& p, dim3 grid,

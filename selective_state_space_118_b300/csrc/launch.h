@@ -17,15 +17,18 @@ enum class IoType { F32, BF16 };
 size_t scan_smem_bytes(IoType io);
 
 // B, C rows (16 values each, `ld` elements apart) in the I/O dtype -> bc
-// (rows, 32) fp32.
+// (rows, 32) fp32; also zeroes n_counters words at `counters` (when given).
+// pdl: launched as a programmatic dependent of the kernel before it.
 cudaError_t launch_bc_widen(IoType io, const void* Bm, const void* Cm, float* bc, long rows, int ld,
-                            cudaStream_t stream);
+                            cudaStream_t stream, unsigned* counters = nullptr, int n_counters = 0,
+                            bool pdl = false);
 // u = silu(conv(x)), (B, L, D) in the I/O dtype, zero conv inputs before t = 0.
 cudaError_t launch_conv_silu(IoType io, const void* x, const float* conv_w, const float* conv_b, void* u, int B,
                              int L, int D, cudaStream_t stream);
 // maps: x, z, dt_raw, bc (3-D tiled tensor maps).
 // The chunked mode's carry pass and main pass as one launch of `ctas`
-// one-warp CTAs (the carry tasks first, by ticket; maps: x, z, dt_raw, bc).
+// one-warp CTAs (the carry tasks first, by ticket; maps: x, z, dt_raw, bc),
+// a programmatic dependent of the B/C widening that zeroed its counters.
 cudaError_t launch_scan_fused(IoType io, const CUtensorMap maps[4], const ScanParams& p, unsigned ctas,
                               cudaStream_t stream);
 cudaError_t launch_scan(IoType io, const CUtensorMap maps[4], const ScanParams& p, dim3 grid,

@@ -82,9 +82,19 @@ __device__ __forceinline__ float input_at(const ScanParams& p, int b, long tau, 
 // ld: elements from one token's row of B (and of C) to the next (16 when
 // they are (B, L, 16) tensors; more when they are columns of a wider
 // projection output).
+//
+// Launched as a programmatic dependent (the forward's chunked mode) it waits
+// for the kernel before it (the previous call's scan, which reads bc) before
+// touching memory, then lets the scan after it launch; block 0 also zeroes
+// that scan's ticket counter and flags (n_counters words, when given).
 template <typename IO>
 __global__ void __launch_bounds__(256) bc_widen_kernel(const IO* __restrict__ Bm, const IO* __restrict__ Cm,
-                                                       float* __restrict__ bc, long rows, int ld) {
+                                                       float* __restrict__ bc, long rows, int ld,
+                                                       unsigned* __restrict__ counters, int n_counters) {
+  griddep_wait();
+  griddep_launch_dependents();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0u;
   const long n = rows * 8;  // 8 pair quads per row
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
     const long r = i >> 3;
@@ -708,6 +718,11 @@ __global__ void __launch_bounds__(kLanes)
                       const __grid_constant__ ScanParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* base = smem_raw + smem_pad128(smem_raw);
+  // a programmatic dependent of the B/C widening (which zeroed the counters):
+  // nothing is read before it has completed; the next call's widening may
+  // launch meanwhile (it waits for this launch in turn)
+  griddep_wait();
+  griddep_launch_dependents();
   unsigned ticket = 0;
   if (threadIdx.x == 0) ticket = atomicAdd(p.counters, 1u);
   ticket = __shfl_sync(0xffffffffu, ticket, 0);

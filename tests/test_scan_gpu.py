@@ -148,7 +148,7 @@ def test_timeout_is_reported_and_gpu_stays_usable():
 
 
 def test_rejects_bad_arguments_on_device():
-    inp = inputs.scan_inputs(1, 64, 24, "bf16", seed=19, device="cuda")
+    inp = inputs.scan_inputs(1, 64, 20, "bf16", seed=19, device="cuda")  # bf16 rows of 40 bytes
     with pytest.raises(ops.MambaError) as e:
         run_gpu(inp)
     assert e.value.status == ops.MAMBA_ERR_UNSUPPORTED
