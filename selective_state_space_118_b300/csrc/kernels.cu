@@ -345,22 +345,32 @@ cudaError_t launch_ssd(const CUtensorMap maps[5], const SsdParams& p, cudaStream
   const size_t st_smem = sizeof(StSmem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(ssd_states_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st_smem);
   if (e != cudaSuccess) return e;
-  ssd_states_kernel<<<(unsigned)(tiles < 2L * sms ? tiles : 2L * sms), kStThreads, st_smem, stream>>>(maps[0], maps[2],
-                                                                                                     p);
-  e = cudaGetLastError();
+  // the three launches are programmatic dependents, each of the kernel before
+  // it (whose results it waits for before touching memory)
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  set_pdl(cfg, attr);
+  cfg.stream = stream;
+  cfg.gridDim = dim3((unsigned)(tiles < 2L * sms ? tiles : 2L * sms));
+  cfg.blockDim = dim3(kStThreads);
+  cfg.dynamicSmemBytes = st_smem;
+  e = cudaLaunchKernelEx(&cfg, ssd_states_kernel, maps[0], maps[2], p);
   if (e != cudaSuccess) return e;
   const size_t pass_smem = sizeof(PassSmem) + 128;
   e = cudaFuncSetAttribute(ssd_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pass_smem);
   if (e != cudaSuccess) return e;
-  ssd_pass_kernel<<<dim3(2u, (unsigned)p.heads, (unsigned)p.batch), kPassThreads, pass_smem, stream>>>(p);
-  e = cudaGetLastError();
+  cfg.gridDim = dim3(2u, (unsigned)p.heads, (unsigned)p.batch);
+  cfg.blockDim = dim3(kPassThreads);
+  cfg.dynamicSmemBytes = pass_smem;
+  e = cudaLaunchKernelEx(&cfg, ssd_pass_kernel, p);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(SsdOutSmem) + 1024;
   e = cudaFuncSetAttribute(ssd_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  ssd_output_kernel<<<(unsigned)(tiles < sms ? tiles : sms), kSsdOutThreads, smem, stream>>>(maps[0], maps[1], maps[2],
-                                                                                           maps[3], maps[4], p);
-  return cudaGetLastError();
+  cfg.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms));
+  cfg.blockDim = dim3(kSsdOutThreads);
+  cfg.dynamicSmemBytes = smem;
+  return cudaLaunchKernelEx(&cfg, ssd_output_kernel, maps[0], maps[1], maps[2], maps[3], maps[4], p);
 }
 
 cudaError_t take_device_error(unsigned* code, cudaStream_t stream) {

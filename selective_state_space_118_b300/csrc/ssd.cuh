@@ -165,6 +165,11 @@ __global__ void __launch_bounds__(kStThreads, 2)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // a programmatic dependent: the kernel before it (the previous call's
+  // output kernel reads the chunk states and prefixes this one writes) has
+  // completed before any global memory is touched; the pass may launch now
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t tmem = sm.tmem_base;
   bool ok = true;
 
@@ -378,6 +383,8 @@ __global__ void __launch_bounds__(kPassThreads) ssd_pass_kernel(const __grid_con
   const float* src = p.S_c + bh * nC * kStep + half * kPassThreads;
   float* dst = p.S_in + bh * nC * kStep + half * kPassThreads;
   const float* tot = p.totals + bh * nC;
+  griddep_wait();  // the states kernel's chunk states are complete
+  griddep_launch_dependents();
   if (tid == 0) {
     for (int r = 0; r < kPassRing; ++r) mbar_init(smem_u32(&sm.full[r]), 1);
     fence_mbar_init();
@@ -599,6 +606,8 @@ __global__ void __launch_bounds__(kSsdOutThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_wait();  // the pass's entering states are complete
+  griddep_launch_dependents();
   const uint32_t tmem = sm.tmem_base;
   bool ok = true;
 
