@@ -122,16 +122,6 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// 3-D tiled store shared -> global (rows outside the tensor are clipped).
-// Coordinates are never negative here.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int c0, int c1, int c2,
-                                             uint32_t src) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2), "r"(src)
-               : "memory");
-}
-
 // 4-D tiled load global -> shared.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
                                             uint32_t bar) {
@@ -448,16 +438,6 @@ __device__ __forceinline__ void st_global_if(bool pred, __nv_bfloat16* p, __nv_b
   asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.global.b16 [%0], %1;\n\t}" ::"l"(p),
                "h"(__bfloat16_as_ushort(v)), "r"((unsigned)pred));
 }
-
-// ---------------------------------------------------------------- cp.async
-// 16 bytes global -> shared, asynchronous (L2 only); src_bytes 0 writes 16
-// zero bytes and reads nothing (src must still be a valid address).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool read) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(read ? 16 : 0)
-               : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // ---------------------------------------------------------------- MUFU
 // 2^x, flushing subnormal inputs/results to zero.

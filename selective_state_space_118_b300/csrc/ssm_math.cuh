@@ -203,29 +203,14 @@ __device__ __forceinline__ void state16_store(const State16& s, float* p) {
 }
 
 // The state-independent half of one token's update: the decays 2^(dt A2) and
-// the inputs dtu B of all 16 states (B[q] holds states 4q..4q+3).
+// the inputs dtu B of all 16 states.
 struct Drive16 {
   float2 dA[8];
   float2 bu[8];
 };
 
-__device__ __forceinline__ void drive16(Drive16& d, const float2 (&a2)[8], float dt, float dtu,
-                                        const float4 (&B)[4]) {
-  const float2 d2 = make_float2(dt, dt);
-  const float2 u2 = make_float2(dtu, dtu);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float2 x0 = __fmul2_rn(d2, a2[2 * q]);
-    const float2 x1 = __fmul2_rn(d2, a2[2 * q + 1]);
-    d.dA[2 * q] = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
-    d.dA[2 * q + 1] = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
-    d.bu[2 * q] = __fmul2_rn(u2, make_float2(B[q].x, B[q].y));
-    d.bu[2 * q + 1] = __fmul2_rn(u2, make_float2(B[q].z, B[q].w));
-  }
-}
-
-// The same from widened B/C rows in pair-quad layout: Q[k] = (B_2k, B_2k+1,
-// C_2k, C_2k+1); only the B halves are used here.
+// From widened B/C rows in pair-quad layout: Q[k] = (B_2k, B_2k+1, C_2k,
+// C_2k+1); only the B halves are used here.
 __device__ __forceinline__ void drive16_q(Drive16& d, const float2 (&a2)[8], float dt, float dtu,
                                           const float4 (&Q)[8]) {
   const float2 d2 = make_float2(dt, dt);
@@ -242,15 +227,6 @@ __device__ __forceinline__ void drive16_q(Drive16& d, const float2 (&a2)[8], flo
 __device__ __forceinline__ void state16_apply(State16& s, const Drive16& d) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) s.h[k] = __ffma2_rn(d.dA[k], s.h[k], d.bu[k]);
-}
-
-// h <- 2^(dt A2) h + dtu B on all 16 states (drive16 then state16_apply: the
-// same operations).
-__device__ __forceinline__ void state16_advance(State16& s, const float2 (&a2)[8], float dt, float dtu,
-                                                const float4 (&B)[4]) {
-  Drive16 d;
-  drive16(d, a2, dt, dtu, B);
-  state16_apply(s, d);
 }
 
 // Half of the read-out: the 8 states of pairs h[0..3] (C values C[0..1]) as
