@@ -410,12 +410,19 @@ mamba_status mamba2_scan_fwd(const mamba2_scan_args *args, void *stream);
  *   workspace         at least mamba3_scan_workspace_size() bytes, 256-byte
  *                     aligned, contents need not be initialised
  *   n_chunks          0: the library picks; 1: one sequential pass; k > 1:
- *                     k chunks in parallel, each chunk's entering state
- *                     computed exactly (no term is dropped): every chunk but
- *                     the last is first run from a zero state, and those end
- *                     states are folded in chunk order
+ *                     k chunks in parallel.  The state entering each chunk
+ *                     comes, as in mamba_scan_fwd, from a carry walk over
+ *                     the chunk before it in 64-token pieces that stops once
+ *                     every mode has decayed below 2^-32 from the piece's
+ *                     start to the chunk boundary (the terms before it, of
+ *                     weight below 2^-32 of their own size, are dropped), in
+ *                     one launch with the main pass.  With
+ *                     MAMBA_FLAG_EXACT_CARRY nothing is dropped: every chunk
+ *                     but the last is first run from a zero state and those
+ *                     end states are folded in chunk order (three launches)
  *   discretization    MAMBA3_EULER or MAMBA3_TRAPEZOIDAL
  *   wait_timeout_ns   limit of every device-side wait (0: 1 second)
+ *   flags             0 or MAMBA_FLAG_EXACT_CARRY
  *
  * d_state must be 16, d_conv 4, d_inner as for mamba_scan_fwd.  seqlen may be 0
  * (the final states are then copies of the initial ones, or zeros).
@@ -445,6 +452,7 @@ typedef struct mamba3_scan_args {
     int n_chunks;
     int discretization;
     uint64_t wait_timeout_ns;
+    unsigned flags;
 } mamba3_scan_args;
 
 /* Bytes of workspace mamba3_scan_fwd needs (0 only for invalid sizes or

@@ -437,22 +437,28 @@ Plan complex_plan(int batch, int seqlen, int d_inner, int n_chunks_req) {
   if (n > tiles) n = tiles;
   if (n < 1) n = 1;
   const int C = (tiles + n - 1) / n;
-  return Plan{(tiles + C - 1) / C, C, 1, C};
+  const int P = C < kPieceTiles ? C : kPieceTiles;  // carry pieces of the walked mode
+  return Plan{(tiles + C - 1) / C, C, (C + P - 1) / P, P};
 }
 
 struct ComplexWorkspace {
-  size_t bc, hloc, sdt, carry, total;
+  size_t bc, hloc, sdt, carry, counters, counters_bytes, total;
 };
 
 ComplexWorkspace complex_workspace_layout(int batch, int seqlen, int d_inner, const Plan& pl) {
-  ComplexWorkspace w{0, 0, 0, 0, 0};
+  ComplexWorkspace w{0, 0, 0, 0, 0, 0, 0};
   const size_t B = batch, L = seqlen, D = d_inner, n = pl.n_chunks;
+  const size_t G = (D + kLanes - 1) / kLanes;
   w.total = round256(B * L * 32 * sizeof(float));
   if (n <= 1) return w;
+  // the exact mode's chunk summaries, the entering states, and the walked
+  // mode's ticket and flags
   w.hloc = w.total;
   w.sdt = round256(w.hloc + B * n * D * 16 * sizeof(float));
   w.carry = round256(w.sdt + B * n * D * sizeof(float));
-  w.total = round256(w.carry + B * n * D * 16 * sizeof(float));
+  w.counters = round256(w.carry + B * n * D * 16 * sizeof(float));
+  w.counters_bytes = (1 + B * G * n) * sizeof(unsigned);
+  w.total = round256(w.counters + w.counters_bytes);
   return w;
 }
 
@@ -971,13 +977,21 @@ mamba_status mamba3_scan_fwd(const mamba3_scan_args* a, void* stream_v) {
   p.final_conv_state = a->final_conv_state;
   p.bc = bc;
   p.timeout_ns = a->wait_timeout_ns ? a->wait_timeout_ns : kDefaultTimeoutNs;
+  p.flags = a->flags & MAMBA_FLAG_EXACT_CARRY;
+  p.piece_tiles = pl.piece_tiles;
+  p.pieces = pl.pieces;
+  const bool walked = pl.n_chunks > 1 && p.flags == 0;
   if (pl.n_chunks > 1) {
     p.hloc = reinterpret_cast<float*>(wsp + ws.hloc);
     p.sdt = reinterpret_cast<float*>(wsp + ws.sdt);
     p.carry = reinterpret_cast<float*>(wsp + ws.carry);
+    p.counters = reinterpret_cast<unsigned*>(wsp + ws.counters);
+    if (walked && (size_t)(2 * pl.n_chunks - 1) * p.n_groups * B >= (1u << 31)) return MAMBA_ERR_UNSUPPORTED;
   }
   const IoType io = a->io == MAMBA_BF16 ? IoType::BF16 : IoType::F32;
-  if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, 16, stream) != cudaSuccess)
+  // the widening also zeroes the walked mode's ticket and flags
+  if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, 16, stream, walked ? p.counters : nullptr,
+                             walked ? (int)(ws.counters_bytes / sizeof(unsigned)) : 0) != cudaSuccess)
     return MAMBA_ERR_CUDA;
   if (mamba::launch_complex(io, a->discretization == MAMBA3_TRAPEZOIDAL, maps, p, stream) != cudaSuccess)
     return MAMBA_ERR_CUDA;

@@ -137,6 +137,15 @@ static cudaError_t launch_complex_pass(const CUtensorMap* m, const ComplexParams
 
 template <typename IO, bool kTrap>
 static cudaError_t launch_complex_t(const CUtensorMap* m, const ComplexParams& p, cudaStream_t s) {
+  if (p.n_chunks > 1 && (p.flags & kFlagExactCarry) == 0) {  // carry walks and main pass, one launch
+    const size_t smem = fused_smem_bytes<IO>() + 128;
+    cudaError_t e = cudaFuncSetAttribute(complex_fused_kernel<IO, kTrap>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const unsigned ctas = (unsigned)((2 * p.n_chunks - 1) * p.n_groups * p.batch);
+    complex_fused_kernel<IO, kTrap><<<ctas, kLanes, smem, s>>>(m[0], m[1], m[2], m[3], p);
+    return cudaGetLastError();
+  }
   if (p.n_chunks > 1) {
     cudaError_t e =
         launch_complex_pass<IO, kTrap, true>(m, p, dim3((unsigned)p.n_groups, (unsigned)p.batch, (unsigned)(p.n_chunks - 1)), s);

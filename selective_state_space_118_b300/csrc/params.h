@@ -112,9 +112,13 @@ struct ComplexParams {
   float* final_v;            // may be null
   void* final_conv_state;    // may be null
   const float* bc;           // widened B/C rows (B, L, 32): per mode (Re B, Im B, Re C, Im C)
-  float* hloc;               // chunked: (B, n_chunks, D, 16) each chunk's end state from zero
-  float* sdt;                // chunked: (B, n_chunks, D) each chunk's dt sum
+  float* hloc;               // exact chunked: (B, n_chunks, D, 16) each chunk's end state from zero
+  float* sdt;                // exact chunked: (B, n_chunks, D) each chunk's dt sum
   float* carry;              // chunked: (B, n_chunks, D, 16) the state entering each chunk
+  unsigned* counters;        // walked chunked mode: ticket, then per (row, group, chunk) a flag
+  int piece_tiles;           // walked chunked mode: tiles per carry piece
+  int pieces;                // pieces per chunk
+  unsigned flags;            // kFlagExactCarry: the exact three-pass chunked mode
   uint64_t timeout_ns;
 };
 

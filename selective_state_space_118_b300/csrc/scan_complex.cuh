@@ -174,22 +174,46 @@ __device__ __forceinline__ float cinput_at(const ComplexParams& p, int b, long t
   return to_f32(reinterpret_cast<const IO*>(p.conv_state0)[((size_t)b * 3 + (3 + tau)) * p.d_inner + c]);
 }
 
-// grid (n_groups, batch, chunks), 32 threads.  kSummary: chunks 0..n-2 from
-// a zero state, no z and no y; stores hloc_j and S_j.  Otherwise: the main
-// pass, every chunk from its entering state, y written.
-template <typename IO, bool kTrap, bool kSummary>
-__global__ void __launch_bounds__(kLanes)
-    complex_scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
-                        const __grid_constant__ CUtensorMap tm_dt, const __grid_constant__ CUtensorMap tm_bc,
-                        const __grid_constant__ ComplexParams p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  MainSmem<IO>& sm = *reinterpret_cast<MainSmem<IO>*>(smem_raw + smem_pad128(smem_raw));
-  constexpr bool kY = !kSummary;
+// The state input v of the token before t0 (trapezoidal rule): v0 (or zero)
+// before the first token, else B_{t0-1} u_{t0-1} from the inputs (xm3..xm1
+// are the inputs at t0-3..t0-1).
+template <typename IO>
+__device__ __forceinline__ void cvprev_at(CState& vp, const ComplexParams& p, const CChannel& ch, int b, int t0,
+                                          int cl, float xm3, float xm2, float xm1) {
+  if (t0 == 0) {
+    if (p.v0)
+      cstate_load(vp, p.v0 + ((size_t)b * p.d_inner + cl) * 16);
+    else
+      cstate_zero(vp);
+    return;
+  }
+  const float xm4 = cinput_at<IO>(p, b, (long)t0 - 4, cl);
+  const float u = silu(conv4(ch.w, ch.bias, xm4, xm3, xm2, xm1));
+  const float4* row = reinterpret_cast<const float4*>(p.bc + ((size_t)b * p.seqlen + t0 - 1) * kBC);
+#pragma unroll
+  for (int n = 0; n < kModes; ++n) {
+    const float4 q = __ldg(row + n);
+    vp.h[n] = make_float2(__fmul_rn(q.x, u), __fmul_rn(q.y, u));
+  }
+}
 
+// One chunk of one channel group (lane = channel) of one batch row.  kSummary
+// (the exact chunked mode's first pass): chunks 0..n-2 from a zero state, no
+// z and no y; stores hloc_j and S_j.  Otherwise the main pass: the chunk from
+// its entering state, y written.  fused (the walked chunked mode, one launch
+// with the carry walks): the state entering chunk j > 0 is awaited (bounded)
+// on its flag; chunk 0's warp and boundary 1's walk, the readers of h0, v0
+// and conv_state0, count themselves done on the group's chunk-0 flag, which
+// the last chunk's warp checks before it writes the final states that may
+// alias them.
+template <typename IO, bool kTrap, bool kSummary>
+__device__ __forceinline__ void complex_pass(const CUtensorMap& tm_x, const CUtensorMap& tm_z,
+                                             const CUtensorMap& tm_dt, const CUtensorMap& tm_bc,
+                                             const ComplexParams& p, MainSmem<IO>& sm, int g, int b, int j,
+                                             bool fused) {
+  constexpr bool kY = !kSummary;
   const int lane = threadIdx.x;
-  const int c0 = blockIdx.x * kLanes;
-  const int b = blockIdx.y;
-  const int j = blockIdx.z;
+  const int c0 = g * kLanes;
   const int D = p.d_inner;
   const int c = c0 + lane;
   const bool active = c < D;
@@ -224,43 +248,63 @@ __global__ void __launch_bounds__(kLanes)
   CChannel ch;
   load_cchannel(ch, p, cl);
   const size_t sidx = ((size_t)b * D + cl) * 16;  // this channel's 16 numbers in (B, D, 16)
-  // In the chunked mode the fold (an earlier launch) copied h0 into the
-  // carry's chunk-0 slot and v0 into the unused last slot of hloc, so that
-  // no CTA of this launch reads h0 or v0, which the last chunk's final_h and
-  // final_v may alias.
-  const bool folded = !kSummary && p.n_chunks > 1;
+  // In the exact chunked mode the fold (an earlier launch) copied h0 into the
+  // carry's chunk-0 slot and v0 into the unused last slot of hloc, so that no
+  // CTA of the main launch reads h0 or v0, which the last chunk's final_h
+  // and final_v may alias.
+  const bool folded = !kSummary && !fused && p.n_chunks > 1;
   CState st, vp;
-  if (kSummary || (j == 0 && !folded && p.h0 == nullptr))
+  if (fused && j > 0) {
+    bool have = true;
+    if (lane == 0) {
+      const unsigned* ready = p.counters + 1 + ((size_t)b * p.n_groups + g) * p.n_chunks;
+      const uint64_t t_start = globaltimer_ns();
+      while (atomicAdd(const_cast<unsigned*>(ready + j), 0u) == 0u) {
+        if (globaltimer_ns() - t_start > p.timeout_ns) {
+          have = false;
+          break;
+        }
+      }
+    }
+    have = __shfl_sync(0xffffffffu, have, 0);
+    __threadfence();
+    if (!have) {
+      if (lane == 0) report_error(4u);  // MAMBA_ERR_TIMEOUT
+      cstate_zero(st);
+    } else {
+      const float4* src = reinterpret_cast<const float4*>(p.carry + (((size_t)b * p.n_chunks + j) * D + cl) * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // from L2: written by another SM during this launch
+        const float4 v = __ldcg(src + q);
+        st.h[2 * q] = make_float2(v.x, v.y);
+        st.h[2 * q + 1] = make_float2(v.z, v.w);
+      }
+    }
+  } else if (kSummary || (j == 0 && !folded && p.h0 == nullptr)) {
     cstate_zero(st);
-  else if (j == 0 && !folded)
+  } else if (j == 0 && !folded) {
     cstate_load(st, p.h0 + sidx);
-  else
+  } else {
     cstate_load(st, p.carry + (((size_t)b * p.n_chunks + j) * D + cl) * 16);
+  }
 
   if (!kTrap) cstate_zero(vp);
   float xm3 = cinput_at<IO>(p, b, (long)t_begin - 3, cl);
   float xm2 = cinput_at<IO>(p, b, (long)t_begin - 2, cl);
   float xm1 = cinput_at<IO>(p, b, (long)t_begin - 1, cl);
   if (kTrap) {  // the state input of the token before the chunk
-    if (j == 0) {
+    if (j == 0 && folded) {
       if (p.v0 == nullptr)
         cstate_zero(vp);
-      else if (folded)
-        cstate_load(vp, p.hloc + (((size_t)b * p.n_chunks + p.n_chunks - 1) * D + cl) * 16);
       else
-        cstate_load(vp, p.v0 + sidx);
+        cstate_load(vp, p.hloc + (((size_t)b * p.n_chunks + p.n_chunks - 1) * D + cl) * 16);
     } else {
-      const float xm4 = cinput_at<IO>(p, b, (long)t_begin - 4, cl);
-      const float u = silu(conv4(ch.w, ch.bias, xm4, xm3, xm2, xm1));
-      const float4* row = reinterpret_cast<const float4*>(p.bc + ((size_t)b * p.seqlen + t_begin - 1) * kBC);
-#pragma unroll
-      for (int n = 0; n < kModes; ++n) {
-        const float4 q = __ldg(row + n);
-        vp.h[n] = make_float2(__fmul_rn(q.x, u), __fmul_rn(q.y, u));
-      }
+      cvprev_at<IO>(vp, p, ch, b, t_begin, cl, xm3, xm2, xm1);
     }
   }
-  if (kY && j == 0 && p.final_conv_state != nullptr) {
+  if (kY && !fused && j == 0 && p.final_conv_state != nullptr) {
+    // the one CTA of these channels in this launch that reads conv_state0,
+    // which the final conv state may alias: read before written
     const float f0 = cinput_at<IO>(p, b, (long)p.seqlen - 3, cl);
     const float f1 = cinput_at<IO>(p, b, (long)p.seqlen - 2, cl);
     const float f2 = cinput_at<IO>(p, b, (long)p.seqlen - 1, cl);
@@ -271,6 +315,20 @@ __global__ void __launch_bounds__(kLanes)
       fcs[D] = from_f32<IO>(f1);
       fcs[2 * (size_t)D] = from_f32<IO>(f2);
     }
+  }
+  if (fused && j == 0) {  // h0, v0 and conv_state0 read
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence();
+      atomicAdd(p.counters + 1 + ((size_t)b * p.n_groups + g) * p.n_chunks, 1u);
+    }
+  }
+  // the fused launch's last chunk writes the final conv state at its end
+  float f0 = 0.0f, f1 = 0.0f, f2 = 0.0f;
+  if (kY && fused && j == p.n_chunks - 1 && p.final_conv_state != nullptr) {
+    f0 = cinput_at<IO>(p, b, (long)p.seqlen - 3, cl);
+    f1 = cinput_at<IO>(p, b, (long)p.seqlen - 2, cl);
+    f2 = cinput_at<IO>(p, b, (long)p.seqlen - 1, cl);
   }
 
   const bool wy = kY && active;
@@ -322,11 +380,25 @@ __global__ void __launch_bounds__(kLanes)
     }
     return;
   }
+  const bool finals = !kSummary && j == p.n_chunks - 1;
+  if (finals && fused) {  // the readers of h0, v0 and conv_state0 are done (bounded)
+    if (lane == 0) {
+      const unsigned* readers = p.counters + 1 + ((size_t)b * p.n_groups + g) * p.n_chunks;
+      const uint64_t t_start = globaltimer_ns();
+      while (ld_relaxed_gpu(readers) < 2u) {
+        if (globaltimer_ns() - t_start > p.timeout_ns) {
+          report_error(4u);  // MAMBA_ERR_TIMEOUT
+          break;
+        }
+      }
+    }
+    __syncwarp();  // the other lanes' stores come after lane 0's check
+  }
   if (!active) return;
   if (kSummary) {
     cstate_store(st, p.hloc + (((size_t)b * p.n_chunks + j) * D + c) * 16);
     p.sdt[((size_t)b * p.n_chunks + j) * D + c] = sdt;
-  } else if (j == p.n_chunks - 1) {
+  } else if (finals) {
     if (p.final_h) cstate_store(st, p.final_h + sidx);
     if (p.final_v) {
       if (!kTrap) {  // Euler keeps no previous input: the last token's, from its inputs
@@ -341,6 +413,218 @@ __global__ void __launch_bounds__(kLanes)
       }
       cstate_store(vp, p.final_v + sidx);
     }
+    if (fused && p.final_conv_state != nullptr) {
+      IO* fcs = reinterpret_cast<IO*>(p.final_conv_state) + (size_t)b * 3 * D + c;
+      fcs[0] = from_f32<IO>(f0);
+      fcs[D] = from_f32<IO>(f1);
+      fcs[2 * (size_t)D] = from_f32<IO>(f2);
+    }
+  }
+}
+
+// grid (n_groups, batch, chunks), 32 threads: one pass, or a pass of the
+// exact chunked mode.
+template <typename IO, bool kTrap, bool kSummary>
+__global__ void __launch_bounds__(kLanes)
+    complex_scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
+                        const __grid_constant__ CUtensorMap tm_dt, const __grid_constant__ CUtensorMap tm_bc,
+                        const __grid_constant__ ComplexParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  complex_pass<IO, kTrap, kSummary>(tm_x, tm_z, tm_dt, tm_bc, p,
+                                    *reinterpret_cast<MainSmem<IO>*>(smem_raw + smem_pad128(smem_raw)), blockIdx.x,
+                                    blockIdx.y, blockIdx.z, false);
+}
+
+// The walked chunked mode's carry walk: one warp per (chunk boundary j =
+// 1..n_chunks-1, channel group, batch row), taken in ticket order, computes
+// the state entering chunk j from chunk j-1's tokens as the real scan's walk
+// does, with complex weights: chunk j-1's pieces are walked backwards, each
+// scanned forward from zero (hloc_q), and
+//   carry_j = sum_q W_q hloc_q + W_start carry_{j-1},
+// W_q = exp(lambda * (dt summed from the end of piece q to the boundary)),
+// the product of the alphas over those tokens.  The walk stops once every
+// mode of every lane has decayed below 2^-32 (|W| = 2^(A2 s) with the
+// slowest A2) from the current piece's start to the boundary; otherwise it
+// waits (bounded) for carry_{j-1}, published by boundary j-1's warp (an
+// earlier ticket), and folds it in.  Trapezoidal: each piece starts from the
+// state input of the token before it (from the inputs; v0 before token 0).
+template <typename IO, bool kTrap>
+__device__ __forceinline__ void ccarry_warp(const CUtensorMap& tm_x, const CUtensorMap& tm_dt,
+                                            const CUtensorMap& tm_bc, const ComplexParams& p, CarrySmem<IO>& sm,
+                                            unsigned ticket) {
+  const int lane = threadIdx.x;
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&sm.full[s]), 1);
+    fence_mbar_init();
+    prefetch_tensormap(&tm_x);
+    prefetch_tensormap(&tm_dt);
+    prefetch_tensormap(&tm_bc);
+  }
+  __syncwarp();
+  const int per = p.n_chunks - 1;
+  const int j = (int)(ticket % per) + 1;  // boundary: the state entering chunk j
+  const int gb = (int)(ticket / per);
+  const int g = gb % p.n_groups;
+  const int b = gb / p.n_groups;
+  const int D = p.d_inner;
+  const int c0 = g * kLanes;
+  const int c = c0 + lane;
+  const bool active = c < D;
+  const int cl = active ? c : D - 1;
+  unsigned* ready = p.counters + 1 + ((size_t)b * p.n_groups + g) * p.n_chunks;
+
+  PieceWalk wk;  // chunk j-1 is never the last chunk: whole tiles
+  wk.first_tile = (j - 1) * p.chunk_tiles;
+  wk.C = p.chunk_tiles;
+  wk.P = p.piece_tiles;
+  wk.m = p.pieces;
+  wk.len_last = p.chunk_tiles - (p.pieces - 1) * p.piece_tiles;
+  const int n_tiles = wk.C;
+  if (lane == 0)
+    for (int k = 0; k < kStages && k < n_tiles; ++k)
+      issue_carry_tile<IO>(sm, k, &tm_x, &tm_dt, &tm_bc, c0, wk.tile_of(k), b);
+
+  CChannel ch;
+  load_cchannel(ch, p, cl);
+  float a2max = ch.a2[0];  // the slowest decay of this channel
+#pragma unroll
+  for (int n = 1; n < kModes; ++n) a2max = fmaxf(a2max, ch.a2[n]);
+  CState acc, st, vp;
+  cstate_zero(acc);
+  cstate_zero(st);
+  float s_after = 0.0f;  // dt summed from the current piece's end to the boundary
+  float sdt = 0.0f;
+  int left = wk.piece_len(wk.piece_of(0));  // tiles left in the current piece
+  int t0 = wk.tile_of(0) * kT;
+  float xm3 = cinput_at<IO>(p, b, (long)t0 - 3, cl);
+  float xm2 = cinput_at<IO>(p, b, (long)t0 - 2, cl);
+  float xm1 = cinput_at<IO>(p, b, (long)t0 - 1, cl);
+  if (kTrap) cvprev_at<IO>(vp, p, ch, b, t0, cl, xm3, xm2, xm1);
+  else cstate_zero(vp);
+
+  bool ok = true, done = false;
+  int k = 0;
+  for (; k < n_tiles; ++k) {
+    const int s = k % kStages;
+    const SummaryStage<IO>& S = sm.stage[s];
+    const bool mine = mbar_wait_bounded(smem_u32(&sm.full[s]), (k / kStages) & 1, p.timeout_ns);
+    ok = __all_sync(0xffffffffu, mine);
+    if (!ok) break;
+#pragma unroll 2
+    for (int r = 0; r < kT; ++r) {
+      const float xv = to_f32(S.x[r][lane]);
+      const float u = silu(conv4(ch.w, ch.bias, xm3, xm2, xm1, xv));
+      xm3 = xm2;
+      xm2 = xm1;
+      xm1 = xv;
+      const float dt = softplus(to_f32(S.dt[r][lane]));
+      float4 Q[kModes];
+      load_quads(&S.bc[r][0], Q);
+      (void)ctoken<kTrap, false>(ch, st, vp, u, dt, Q);
+      sdt = __fadd_rn(sdt, dt);
+    }
+    __syncwarp();  // every lane is done with stage s
+    if (lane == 0 && k + kStages < n_tiles)
+      issue_carry_tile<IO>(sm, s, &tm_x, &tm_dt, &tm_bc, c0, wk.tile_of(k + kStages), b);
+    if (--left == 0) {  // piece done: acc += W hloc, W from the piece's end to the boundary
+#pragma unroll
+      for (int n = 0; n < kModes; ++n)
+        acc.h[n] = cmul_add(cexp_step(ch.a2[n], ch.tu[n], ch.tl[n], s_after), st.h[n], acc.h[n]);
+      s_after = __fadd_rn(s_after, sdt);
+      if ((p.flags & kFlagExactCarry) == 0 &&
+          __all_sync(0xffffffffu, !active || __fmul_rn(a2max, s_after) < kCarryDropLog2)) {
+        done = true;
+        ++k;
+        break;
+      }
+      if (k + 1 < n_tiles) {  // the next (earlier) piece, from zero
+        left = wk.piece_len(wk.piece_of(k + 1));
+        cstate_zero(st);
+        sdt = 0.0f;
+        t0 = wk.tile_of(k + 1) * kT;
+        xm3 = cinput_at<IO>(p, b, (long)t0 - 3, cl);
+        xm2 = cinput_at<IO>(p, b, (long)t0 - 2, cl);
+        xm1 = cinput_at<IO>(p, b, (long)t0 - 1, cl);
+        if (kTrap) cvprev_at<IO>(vp, p, ch, b, t0, cl, xm3, xm2, xm1);
+      }
+    }
+  }
+  if (lane == 0) {  // copies still in flight land before shared memory goes away
+    for (int kk = k; kk < n_tiles && kk < k + kStages; ++kk)
+      (void)mbar_wait_bounded(smem_u32(&sm.full[kk % kStages]), (kk / kStages) & 1, p.timeout_ns);
+  }
+  if (!ok && lane == 0) report_error(4u);  // MAMBA_ERR_TIMEOUT
+
+  if (ok && !done) {  // the whole chunk matters: fold in the state entering it
+    CState prev;
+    if (j - 1 == 0) {
+      if (p.h0)
+        cstate_load(prev, p.h0 + ((size_t)b * D + cl) * 16);
+      else
+        cstate_zero(prev);
+    } else {
+      bool have = true;
+      if (lane == 0) {
+        const uint64_t t_start = globaltimer_ns();
+        while (atomicAdd(ready + (j - 1), 0u) == 0u) {
+          if (globaltimer_ns() - t_start > p.timeout_ns) {
+            have = false;
+            break;
+          }
+        }
+      }
+      have = __shfl_sync(0xffffffffu, have, 0);
+      __threadfence();
+      if (!have) {
+        if (lane == 0) report_error(4u);
+        cstate_zero(prev);
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(p.carry + (((size_t)b * p.n_chunks + (j - 1)) * D + cl) * 16);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 v = __ldcg(src + q);
+          prev.h[2 * q] = make_float2(v.x, v.y);
+          prev.h[2 * q + 1] = make_float2(v.z, v.w);
+        }
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < kModes; ++n)
+      acc.h[n] = cmul_add(cexp_step(ch.a2[n], ch.tu[n], ch.tl[n], s_after), prev.h[n], acc.h[n]);
+  }
+
+  // publish carry_j (also after a failure, so that no later boundary waits in vain)
+  if (active) cstate_store(acc, p.carry + (((size_t)b * p.n_chunks + j) * D + c) * 16);
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) {
+    atomicExch(ready + j, 1u);
+    if (j == 1) atomicAdd(ready, 1u);  // boundary 1's walk is done with h0, v0 and conv_state0
+  }
+}
+
+// The walked chunked mode in one launch of (n_chunks - 1) * n_groups * batch
+// carry warps and n_chunks * n_groups * batch main warps, ticket-ordered as
+// the real scan's fused launch.
+template <typename IO, bool kTrap>
+__global__ void __launch_bounds__(kLanes)
+    complex_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_z,
+                         const __grid_constant__ CUtensorMap tm_dt, const __grid_constant__ CUtensorMap tm_bc,
+                         const __grid_constant__ ComplexParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* base = smem_raw + smem_pad128(smem_raw);
+  unsigned ticket = 0;
+  if (threadIdx.x == 0) ticket = atomicAdd(p.counters, 1u);
+  ticket = __shfl_sync(0xffffffffu, ticket, 0);
+  const unsigned per = (unsigned)p.n_groups * (unsigned)p.batch;
+  const unsigned n_carry = (unsigned)(p.n_chunks - 1) * per;
+  if (ticket < n_carry) {
+    ccarry_warp<IO, kTrap>(tm_x, tm_dt, tm_bc, p, *reinterpret_cast<CarrySmem<IO>*>(base), ticket);
+  } else {
+    const unsigned t = ticket - n_carry;
+    const int j = (int)(t / per), gb = (int)(t % per);
+    complex_pass<IO, kTrap, false>(tm_x, tm_z, tm_dt, tm_bc, p, *reinterpret_cast<MainSmem<IO>*>(base),
+                                   gb % p.n_groups, gb / p.n_groups, j, true);
   }
 }
 

@@ -89,7 +89,7 @@ class Mamba3Args(ctypes.Structure):
                 ("h0", _vp), ("conv_state0", _vp), ("v0", _vp), ("y", _vp), ("final_h", _vp),
                 ("final_conv_state", _vp), ("final_v", _vp), ("workspace", _vp),
                 ("workspace_bytes", ctypes.c_size_t), ("n_chunks", ctypes.c_int),
-                ("discretization", ctypes.c_int), ("wait_timeout_ns", ctypes.c_uint64)]
+                ("discretization", ctypes.c_int), ("wait_timeout_ns", ctypes.c_uint64), ("flags", ctypes.c_uint)]
 
 
 class LinearArgs(ctypes.Structure):
@@ -465,7 +465,7 @@ def mamba3_scan_workspace_size(batch: int, seqlen: int, d_inner: int, n_chunks: 
 def mamba3_scan_fwd(x, z, dt_raw, Bm, Cm, A_log, theta, Dskip, conv_w, conv_b=None, h0=None,
                     conv_state0=None, v0=None, *, trapezoidal: bool = False, y=None, final_h=None,
                     final_conv_state=None, final_v=None, workspace=None, n_chunks: int = 0,
-                    wait_timeout_ns: int = 0, return_state: bool = True, stream=None):
+                    wait_timeout_ns: int = 0, flags: int = 0, return_state: bool = True, stream=None):
     """The complex-valued scan (C ABI ``mamba3_scan_fwd``): x, z, dt_raw
     (B,L,D) and Bm, Cm (B,L,16: 8 complex numbers as (re, im) pairs) in fp32
     or bf16; A_log, theta (D,8), Dskip (D), conv_w (D,4), conv_b (D) fp32;
@@ -503,7 +503,7 @@ def mamba3_scan_fwd(x, z, dt_raw, Bm, Cm, A_log, theta, Dskip, conv_w, conv_b=No
                    workspace=_ptr(workspace),
                    workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
                    n_chunks=n_chunks, discretization=MAMBA3_TRAPEZOIDAL if trapezoidal else MAMBA3_EULER,
-                   wait_timeout_ns=wait_timeout_ns)
+                   wait_timeout_ns=wait_timeout_ns, flags=flags)
     st = _launch(lib.mamba3_scan_fwd, a, stream, dev)
     if st != MAMBA_OK:
         raise MambaError(st, "mamba3_scan_fwd")

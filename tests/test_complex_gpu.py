@@ -153,6 +153,22 @@ def test_final_states_may_alias_initial_states(rule, n_chunks):
 
 
 @pytest.mark.parametrize("rule", sorted(RULES))
+def test_exact_carry_flag_against_oracle(rule):
+    """MAMBA_FLAG_EXACT_CARRY: every chunk summarised and folded, nothing
+    dropped (three launches) -- against the oracle, and against the default
+    walked carries, which stop after ~1,100 tokens of these 2,048-token chunks
+    (the slowest mode's decay passes 2^-32) and drop what lies before."""
+    inp = make(1, 8192, 32, "f32", seed=651)
+    exact = [t.clone() for t in run_gpu(inp, RULES[rule], n_chunks=4, flags=ops.MAMBA_FLAG_EXACT_CARRY)]
+    check(inp, exact, RULES[rule], f"{rule} exact carries")
+    walked = run_gpu(inp, RULES[rule], n_chunks=4)
+    torch.cuda.synchronize()
+    assert_close(walked[0], exact[0].double().cpu().numpy(), "f32", "walked vs exact y")
+    assert_close(walked[1], exact[1].double().cpu().numpy(), "f32", "walked vs exact h", fp32_output=True)
+    assert torch.equal(walked[2], exact[2]) and torch.equal(walked[3], exact[3])
+
+
+@pytest.mark.parametrize("rule", sorted(RULES))
 def test_chunked_equals_one_pass_within_tolerance(rule):
     inp = make(1, 64 * 40 + 7, 32, "f32", seed=621)
     y1, fh1, fcs1, fv1 = [t.clone() for t in run_gpu(inp, RULES[rule], n_chunks=1)]
