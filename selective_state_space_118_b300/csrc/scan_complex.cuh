@@ -125,13 +125,15 @@ struct CState {
 // (read-out accumulated in a fixed order: (Re C Re h, Im C Im h) summed over
 // n as a packed pair, then the two parts subtracted).  vp: the previous
 // token's state input (trapezoidal only).
-template <bool kTrap, bool kRead>
+// NM < kModes: only modes 0..NM-1 advance (the carry walk's modes whose
+// weight to the boundary is still above the drop bound; the others stay).
+template <bool kTrap, bool kRead, int NM = kModes>
 __device__ __forceinline__ float ctoken(const CChannel& ch, CState& st, CState& vp, float u, float dt,
                                         const float4 (&Q)[kModes]) {
   const float hdt = __fmul_rn(0.5f, dt);
   float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-  for (int n = 0; n < kModes; ++n) {
+  for (int n = 0; n < NM; ++n) {
     const float2 al = cexp_step(ch.a2[n], ch.tu[n], ch.tl[n], dt);
     const float2 v = make_float2(__fmul_rn(Q[n].x, u), __fmul_rn(Q[n].y, u));
     if (kTrap) {
@@ -435,6 +437,25 @@ __global__ void __launch_bounds__(kLanes)
                                     blockIdx.y, blockIdx.z, false);
 }
 
+// One full tile of a carry piece: modes 0..NM-1 advanced, the dt summed.
+template <typename IO, bool kTrap, int NM>
+__device__ __forceinline__ void ccarry_tile(const SummaryStage<IO>& S, int lane, const CChannel& ch, CState& st,
+                                            CState& vp, float& sdt, float& xm3, float& xm2, float& xm1) {
+#pragma unroll 2
+  for (int r = 0; r < kT; ++r) {
+    const float xv = to_f32(S.x[r][lane]);
+    const float u = silu(conv4(ch.w, ch.bias, xm3, xm2, xm1, xv));
+    xm3 = xm2;
+    xm2 = xm1;
+    xm1 = xv;
+    const float dt = softplus(to_f32(S.dt[r][lane]));
+    float4 Q[kModes];
+    load_quads(&S.bc[r][0], Q);
+    (void)ctoken<kTrap, false, NM>(ch, st, vp, u, dt, Q);
+    sdt = __fadd_rn(sdt, dt);
+  }
+}
+
 // The walked chunked mode's carry walk: one warp per (chunk boundary j =
 // 1..n_chunks-1, channel group, batch row), taken in ticket order, computes
 // the state entering chunk j from chunk j-1's tokens as the real scan's walk
@@ -502,6 +523,7 @@ __device__ __forceinline__ void ccarry_warp(const CUtensorMap& tm_x, const CUten
   if (kTrap) cvprev_at<IO>(vp, p, ch, b, t0, cl, xm3, xm2, xm1);
   else cstate_zero(vp);
 
+  int n_modes = kModes;  // leading modes the current piece advances
   bool ok = true, done = false;
   int k = 0;
   for (; k < n_tiles; ++k) {
@@ -510,19 +532,14 @@ __device__ __forceinline__ void ccarry_warp(const CUtensorMap& tm_x, const CUten
     const bool mine = mbar_wait_bounded(smem_u32(&sm.full[s]), (k / kStages) & 1, p.timeout_ns);
     ok = __all_sync(0xffffffffu, mine);
     if (!ok) break;
-#pragma unroll 2
-    for (int r = 0; r < kT; ++r) {
-      const float xv = to_f32(S.x[r][lane]);
-      const float u = silu(conv4(ch.w, ch.bias, xm3, xm2, xm1, xv));
-      xm3 = xm2;
-      xm2 = xm1;
-      xm1 = xv;
-      const float dt = softplus(to_f32(S.dt[r][lane]));
-      float4 Q[kModes];
-      load_quads(&S.bc[r][0], Q);
-      (void)ctoken<kTrap, false>(ch, st, vp, u, dt, Q);
-      sdt = __fadd_rn(sdt, dt);
-    }
+    if (n_modes == 1)
+      ccarry_tile<IO, kTrap, 1>(S, lane, ch, st, vp, sdt, xm3, xm2, xm1);
+    else if (n_modes == 2)
+      ccarry_tile<IO, kTrap, 2>(S, lane, ch, st, vp, sdt, xm3, xm2, xm1);
+    else if (n_modes <= 4)
+      ccarry_tile<IO, kTrap, 4>(S, lane, ch, st, vp, sdt, xm3, xm2, xm1);
+    else
+      ccarry_tile<IO, kTrap, 8>(S, lane, ch, st, vp, sdt, xm3, xm2, xm1);
     __syncwarp();  // every lane is done with stage s
     if (lane == 0 && k + kStages < n_tiles)
       issue_carry_tile<IO>(sm, s, &tm_x, &tm_dt, &tm_bc, c0, wk.tile_of(k + kStages), b);
@@ -541,6 +558,16 @@ __device__ __forceinline__ void ccarry_warp(const CUtensorMap& tm_x, const CUten
         left = wk.piece_len(wk.piece_of(k + 1));
         cstate_zero(st);
         sdt = 0.0f;
+        // modes whose weight to the boundary fell below the drop bound add
+        // nothing from here on: the piece advances the leading ones up to
+        // the last mode still above it
+        if ((p.flags & kFlagExactCarry) == 0) {
+          int last = -1;
+#pragma unroll
+          for (int n = 0; n < kModes; ++n)
+            if (__fmul_rn(ch.a2[n], s_after) >= kCarryDropLog2) last = n;
+          n_modes = __reduce_max_sync(0xffffffffu, active ? last + 1 : 0);
+        }
         t0 = wk.tile_of(k + 1) * kT;
         xm3 = cinput_at<IO>(p, b, (long)t0 - 3, cl);
         xm2 = cinput_at<IO>(p, b, (long)t0 - 2, cl);
