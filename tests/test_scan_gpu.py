@@ -104,6 +104,34 @@ def test_final_state_may_alias_initial_state(L, n_chunks):
     assert torch.equal(y, ref[0]) and torch.equal(h, ref[1]) and torch.equal(cs, ref[2])
 
 
+def test_carried_calls_in_place_equal_separate_buffers():
+    """A sequence fed as chunked calls back to back (their launches overlap
+    the previous call's end), each call's final_h and final_conv_state
+    written over its own h0 and conv_state0 in place, as a serving loop
+    does: the same bits as with fresh buffers for every call."""
+    B, L, D, calls = 1, 16384, 256, 4
+    inp = inputs.scan_inputs(B, L, D, "bf16", seed=29, device="cuda", with_state=True)
+    step = L // calls
+
+    def part(i, h, cs):
+        q = dict(inp, h0=h, conv_state0=cs)
+        for k in ("x", "z", "dt_raw", "Bm", "Cm"):
+            q[k] = inp[k][:, i * step:(i + 1) * step]
+        return q
+
+    ys, h, cs = [], inp["h0"].clone(), inp["conv_state0"].clone()
+    for i in range(calls):
+        y, h, cs = run_gpu(part(i, h, cs), n_chunks=0)
+        ys.append(y)
+    h_in, cs_in = inp["h0"].clone(), inp["conv_state0"].clone()
+    ys_in = [run_gpu(part(i, h_in, cs_in), final_h=h_in, final_conv_state=cs_in, n_chunks=0)[0]
+             for i in range(calls)]
+    torch.cuda.synchronize()
+    assert ops.mamba_scan_plan(B, step, D, 0)["n_chunks"] > 1
+    assert all(torch.equal(a, b) for a, b in zip(ys, ys_in))
+    assert torch.equal(h_in, h) and torch.equal(cs_in, cs)
+
+
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_host_split_calls_equal_one_call_bitwise(io):
     """One sequential pass == the same sequence fed as several calls that carry
