@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -72,7 +73,7 @@ struct Machine {
 };
 
 Machine query_machine() {
-  Machine m{sm_count(), 16, 20};
+  Machine m{sm_count(), 16, 16};
   int a = 0, b = 0;
   mamba::scan_occupancy(IoType::BF16, &a, &b);
   if (a > 0) m.main_per_sm = a;
@@ -156,14 +157,31 @@ Plan make_plan(int batch, int seqlen, int d_inner, int n_chunks_req) {
     // Chunks shorter than the expected walk make every boundary walk its
     // whole chunk and then wait for the previous boundary's carry: the walks
     // run side by side, the folds one after another (a chain of hops of
-    // about a tile's time each).
-    double t_carry = 0.0;
-    if (n_eff > 1) {
-      const int walk = C < kCarryTilesEstimate ? C : kCarryTilesEstimate;
-      t_carry = pass_time(groups * (n_eff - 1), walk, kCarryTileCost, mc.sms, mc.summary_per_sm);
-      if (C < kCarryTilesEstimate) t_carry += kChainHopCost * (n_eff - 1);
+    // about a tile's time each).  Longer chunks: the walks stop early and the
+    // two kinds of warps are costed as passes of their own.
+    double t;
+    if (n_eff > 1 && C < kCarryTilesEstimate) {
+      // Walks over whole chunks: the one launch runs as two phases, all the
+      // walks (with chunk 0's main warps beside them), then the later
+      // chunks' main warps once their carries are in; each phase lasts a
+      // warp's duration (its C tiles, at the issue efficiency of the warps
+      // sharing a scheduler) per wave of resident slots, so shorter chunks
+      // shorten both phases until a phase spills into a second wave.
+      // Measured at 4,096 tokens x 8,192 channels, 8-12 chunks: 17.6, 16.1,
+      // 15.5, 16.9, 17.6 ms per 64 calls (this picks 10).
+      const long units = 4L * mc.sms;
+      const long slots = (long)mc.sms * mc.summary_per_sm;
+      const long walks = groups * (n_eff - 1);  // and as many later main warps
+      const double waves = (double)((walks + slots - 1) / slots);
+      const double w = (double)(walks < slots ? walks : slots) / units;
+      const double per_warp = std::ceil(w) / (0.25 + 0.2 * w);
+      t = (C + 0.5) * (kCarryTileCost + kMainTileCost) * per_warp * waves + kChainHopCost * (n_eff - 1);
+    } else {
+      double t_carry = 0.0;
+      if (n_eff > 1) t_carry = pass_time(groups * (n_eff - 1), kCarryTilesEstimate, kCarryTileCost, mc.sms,
+                                         mc.summary_per_sm);
+      t = pass_time(groups * n_eff, C, kMainTileCost, mc.sms, mc.main_per_sm) + t_carry;
     }
-    const double t = pass_time(groups * n_eff, C, kMainTileCost, mc.sms, mc.main_per_sm) + t_carry;
     if (best < 0.0 || t < best - 1e-9) {
       best = t;
       pl = Plan{n_eff, C, n_eff > 1 ? m : 1, n_eff > 1 ? P : C};
