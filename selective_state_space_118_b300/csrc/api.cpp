@@ -1009,7 +1009,7 @@ mamba_status mamba3_scan_fwd(const mamba3_scan_args* a, void* stream_v) {
   const IoType io = a->io == MAMBA_BF16 ? IoType::BF16 : IoType::F32;
   // the widening also zeroes the walked mode's ticket and flags
   if (mamba::launch_bc_widen(io, a->Bm, a->Cm, bc, (long)B * a->seqlen, 16, stream, walked ? p.counters : nullptr,
-                             walked ? (int)(ws.counters_bytes / sizeof(unsigned)) : 0) != cudaSuccess)
+                             walked ? (int)(ws.counters_bytes / sizeof(unsigned)) : 0, false, true) != cudaSuccess)
     return MAMBA_ERR_CUDA;
   if (mamba::launch_complex(io, a->discretization == MAMBA3_TRAPEZOIDAL, maps, p, stream) != cudaSuccess)
     return MAMBA_ERR_CUDA;

@@ -71,7 +71,7 @@ cudaError_t launch_scan_fused(IoType io, const CUtensorMap maps[4], const ScanPa
 
 template <typename IO>
 static cudaError_t launch_widen_t(const void* Bm, const void* Cm, float* bc, long rows, int ld, unsigned* counters,
-                                  int n_counters, bool pdl, cudaStream_t s) {
+                                  int n_counters, bool pdl, bool mode_pairs, cudaStream_t s) {
   const long n = rows * 8;
   long blocks = (n + 255) / 256;
   if (blocks > 148L * 16) blocks = 148L * 16;
@@ -82,14 +82,18 @@ static cudaError_t launch_widen_t(const void* Bm, const void* Cm, float* bc, lon
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   if (pdl) set_pdl(cfg, attr);
-  return cudaLaunchKernelEx(&cfg, bc_widen_kernel<IO>, static_cast<const IO*>(Bm), static_cast<const IO*>(Cm), bc,
-                            rows, ld, counters, n_counters);
+  if (mode_pairs)
+    return cudaLaunchKernelEx(&cfg, bc_widen_kernel<IO, true>, static_cast<const IO*>(Bm),
+                              static_cast<const IO*>(Cm), bc, rows, ld, counters, n_counters);
+  return cudaLaunchKernelEx(&cfg, bc_widen_kernel<IO, false>, static_cast<const IO*>(Bm), static_cast<const IO*>(Cm),
+                            bc, rows, ld, counters, n_counters);
 }
 
 cudaError_t launch_bc_widen(IoType io, const void* Bm, const void* Cm, float* bc, long rows, int ld,
-                            cudaStream_t stream, unsigned* counters, int n_counters, bool pdl) {
-  return io == IoType::BF16 ? launch_widen_t<__nv_bfloat16>(Bm, Cm, bc, rows, ld, counters, n_counters, pdl, stream)
-                            : launch_widen_t<float>(Bm, Cm, bc, rows, ld, counters, n_counters, pdl, stream);
+                            cudaStream_t stream, unsigned* counters, int n_counters, bool pdl, bool mode_pairs) {
+  return io == IoType::BF16
+             ? launch_widen_t<__nv_bfloat16>(Bm, Cm, bc, rows, ld, counters, n_counters, pdl, mode_pairs, stream)
+             : launch_widen_t<float>(Bm, Cm, bc, rows, ld, counters, n_counters, pdl, mode_pairs, stream);
 }
 
 cudaError_t launch_scan(IoType io, const CUtensorMap maps[4], const ScanParams& p, dim3 grid,

@@ -19,9 +19,10 @@ size_t scan_smem_bytes(IoType io);
 // B, C rows (16 values each, `ld` elements apart) in the I/O dtype -> bc
 // (rows, 32) fp32; also zeroes n_counters words at `counters` (when given).
 // pdl: launched as a programmatic dependent of the kernel before it.
+// mode_pairs: the complex scan's layout (quads across two modes).
 cudaError_t launch_bc_widen(IoType io, const void* Bm, const void* Cm, float* bc, long rows, int ld,
                             cudaStream_t stream, unsigned* counters = nullptr, int n_counters = 0,
-                            bool pdl = false);
+                            bool pdl = false, bool mode_pairs = false);
 // u = silu(conv(x)), (B, L, D) in the I/O dtype, zero conv inputs before t = 0.
 cudaError_t launch_conv_silu(IoType io, const void* x, const float* conv_w, const float* conv_b, void* u, int B,
                              int L, int D, cudaStream_t stream);

@@ -10,18 +10,22 @@
 //   Euler:        h_n = alpha_n h_n + dt v_n
 //   trapezoidal:  h_n = alpha_n (h_n + dt/2 vprev_n) + dt/2 v_n,  vprev = v
 //   y = (Re(sum_n C_n h_n) + D u) silu(z)
-// The turn dt theta_n is taken in whole turns first (t = dt theta_n / 2pi,
-// reduced to [-1/2, 1/2] by subtracting the nearest integer) and then fed to
-// the approximate sine and cosine, whose error bound holds on [-pi, pi].  So
-// that a turn of many revolutions per token keeps its fraction to fp32
-// precision, theta / 2pi is held as two fp32 parts (hi + lo) and the product
-// dt * hi carries its exact rounding error (an fma) into the fraction.
+// The approximate sine and cosine hold their error bound on [-pi, pi].  A
+// token whose dt keeps every turn dt theta_n of the channel within it (dt <=
+// pi / max |theta_n|, the common case) takes the angle as it is; any other
+// takes it in whole turns first (t = dt theta_n / 2pi, reduced to
+// [-1/2, 1/2] by subtracting the nearest integer).  So that a turn of many
+// revolutions per token keeps its fraction to fp32 precision, theta / 2pi is
+// then formed as two fp32 parts (hi + lo) and the product dt * hi carries its
+// exact rounding error (an fma) into the fraction.
 //
 // Decomposition: as the real scan's main pass -- a CTA is one warp, lane i
 // owns channel c0 + i with all 16 numbers of its state in registers, tiles of
 // 16 tokens of x, z, dt_raw and the widened B/C rows arrive by TMA through a
-// two-stage mbarrier ring.  The widened row of a token holds, per mode n,
-// the quad (Re B_n, Im B_n, Re C_n, Im C_n).
+// two-stage mbarrier ring.  The modes are advanced two at a time with packed
+// fp32 pair arithmetic: the state is held as (Re, Im) pairs across modes 2q,
+// 2q+1, and the widened row of a token holds, per mode pair q, the quads
+// (Re B_2q, Re B_2q+1, Im B_2q, Im B_2q+1) and (Re C_2q, ..., Im C_2q+1).
 //
 // Chunked mode (batch 1 needs it to fill the GPU): three exact passes, no
 // term dropped.  (1) Each chunk but the last runs the recurrence from a zero
@@ -45,8 +49,10 @@
 namespace mamba {
 
 constexpr int kModes = 8;
+constexpr int kPairs = kModes / 2;  // modes are advanced two at a time (packed fp32 pairs)
 constexpr float kInvTwoPi = 0.15915494309189533577f;
 constexpr float kTwoPi = 6.28318530717958647693f;
+constexpr float kPi = 3.14159265358979323846f;
 
 __device__ __forceinline__ float sin_approx(float x) {
   float y;
@@ -70,102 +76,173 @@ __device__ __forceinline__ void turns_of(float theta, float& hi, float& lo) {
   lo = __fmaf_rn(theta, kInvTwoPiLo, __fmaf_rn(theta, kInvTwoPi, -hi));
 }
 
-// The per-channel constants of one lane.
+// The turn s theta of one mode reduced to [-pi, pi]: the turn count
+// t = s theta / 2pi = s (hi + lo) less its nearest integer, formed as
+// (t - rint(t)) + (the rounding error of t = s hi) + s lo.  Subtracting the
+// nearest integer is exact, so the fraction keeps fp32's relative precision
+// however many whole turns t holds.
+__device__ __forceinline__ float turn_angle(float theta, float s) {
+  float hi, lo;
+  turns_of(theta, hi, lo);
+  const float t = __fmul_rn(s, hi);
+  const float e = __fmaf_rn(s, hi, -t);
+  const float f = __fadd_rn(__fsub_rn(t, rintf(t)), __fmaf_rn(s, lo, e));
+  return __fmul_rn(f, kTwoPi);
+}
+
+// The per-channel constants of one lane, by mode pair: element 0 of pair q
+// belongs to mode 2q, element 1 to mode 2q + 1.
 struct CChannel {
-  float a2[kModes];  // A2 = -exp(A_log) log2(e)
-  float tu[kModes];  // theta / 2pi (turns per unit of dt), rounded to fp32 ...
-  float tl[kModes];  // ... and the rest: theta / 2pi = tu + tl to ~2^-48
+  float2 a2[kPairs];  // A2 = -exp(A_log) log2(e)
+  float2 th[kPairs];  // theta
+  float thr;          // steps s up to this keep every turn s theta within [-pi, pi]
   float4 w;
   float bias;
   float Dc;
 };
 
 __device__ __forceinline__ void load_cchannel(CChannel& ch, const ComplexParams& p, int c) {
+  float tmax = 0.0f;
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
     const float4 al = __ldg(reinterpret_cast<const float4*>(p.A_log + (size_t)c * kModes) + q);
     const float4 th = __ldg(reinterpret_cast<const float4*>(p.theta + (size_t)c * kModes) + q);
-    ch.a2[4 * q + 0] = a2_from_log(al.x);
-    ch.a2[4 * q + 1] = a2_from_log(al.y);
-    ch.a2[4 * q + 2] = a2_from_log(al.z);
-    ch.a2[4 * q + 3] = a2_from_log(al.w);
-    const float thv[4] = {th.x, th.y, th.z, th.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) turns_of(thv[i], ch.tu[4 * q + i], ch.tl[4 * q + i]);
+    ch.a2[2 * q] = make_float2(a2_from_log(al.x), a2_from_log(al.y));
+    ch.a2[2 * q + 1] = make_float2(a2_from_log(al.z), a2_from_log(al.w));
+    ch.th[2 * q] = make_float2(th.x, th.y);
+    ch.th[2 * q + 1] = make_float2(th.z, th.w);
+    tmax = fmaxf(tmax, fmaxf(fmaxf(fabsf(th.x), fabsf(th.y)), fmaxf(fabsf(th.z), fabsf(th.w))));
   }
+  // s <= fl(pi / tmax) keeps |fl(s theta)| within pi up to a rounding
+  ch.thr = tmax > 0.0f ? __fdiv_rn(kPi, tmax) : __int_as_float(0x7f800000);
   ch.w = __ldg(reinterpret_cast<const float4*>(p.conv_w + (size_t)c * 4));
   ch.bias = p.conv_b ? __ldg(p.conv_b + c) : 0.0f;
   ch.Dc = __ldg(p.Dskip + c);
 }
 
-// exp(s lambda) for a dt (or dt sum) s: magnitude 2^(s A2), turn
-// s theta / 2pi = s (tu + tl), whose fraction is formed as (t - rint(t)) +
-// (the rounding error of t = s tu) + s tl: the subtraction of the nearest
-// integer is exact, so the fraction keeps fp32's relative precision however
-// many whole turns t holds.
-__device__ __forceinline__ float2 cexp_step(float a2, float tu, float tl, float s) {
-  const float m = ex2_approx(__fmul_rn(s, a2));
-  const float t = __fmul_rn(s, tu);
-  const float e = __fmaf_rn(s, tu, -t);
-  const float f = __fadd_rn(__fsub_rn(t, rintf(t)), __fmaf_rn(s, tl, e));
-  const float r = __fmul_rn(f, kTwoPi);
-  return make_float2(__fmul_rn(m, cos_approx(r)), __fmul_rn(m, sin_approx(r)));
+// exp(s lambda) for the first NP mode pairs at a step s (a dt or a dt sum):
+// magnitude 2^(s A2), angle s theta -- taken as it is when s <= thr (every
+// turn within [-pi, pi]), else reduced by turn_angle -- as (re, im) pairs.
+template <int NP>
+__device__ __forceinline__ void calphas(const CChannel& ch, float s, float2 (&are)[NP], float2 (&aim)[NP]) {
+  const float2 s2 = make_float2(s, s);
+  float2 r[NP];
+  if (s <= ch.thr) {
+#pragma unroll
+    for (int q = 0; q < NP; ++q) r[q] = __fmul2_rn(s2, ch.th[q]);
+  } else {
+#pragma unroll
+    for (int q = 0; q < NP; ++q) r[q] = make_float2(turn_angle(ch.th[q].x, s), turn_angle(ch.th[q].y, s));
+  }
+#pragma unroll
+  for (int q = 0; q < NP; ++q) {
+    const float2 e = __fmul2_rn(s2, ch.a2[q]);
+    const float2 m = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+    are[q] = __fmul2_rn(m, make_float2(cos_approx(r[q].x), cos_approx(r[q].y)));
+    aim[q] = __fmul2_rn(m, make_float2(sin_approx(r[q].x), sin_approx(r[q].y)));
+  }
 }
 
-// (a + ib)(x + iy) + (bx' + i by')
-__device__ __forceinline__ float2 cmul_add(float2 a, float2 g, float2 add) {
-  return make_float2(__fmaf_rn(a.x, g.x, __fmaf_rn(-a.y, g.y, add.x)), __fmaf_rn(a.x, g.y, __fmaf_rn(a.y, g.x, add.y)));
+// (are + i aim)(gre + i gim) + (addre + i addim) for a mode pair, into
+// (gre, gim): re = are gre + (-aim gim + addre), im = are gim + (aim gre + addim).
+__device__ __forceinline__ void cmad2(float2 are, float2 aim, float2& gre, float2& gim, float2 addre,
+                                      float2 addim) {
+  const float2 re = __ffma2_rn(are, gre, __ffma2_rn(make_float2(-aim.x, -aim.y), gim, addre));
+  const float2 im = __ffma2_rn(are, gim, __ffma2_rn(aim, gre, addim));
+  gre = re;
+  gim = im;
 }
 
+// A complex state (or state input) of one lane, by mode pair.  In memory it
+// is (re, im) per mode in mode order, 16 floats.
 struct CState {
-  float2 h[kModes];
+  float2 re[kPairs];
+  float2 im[kPairs];
 };
 
+// Four floats (re_2q, im_2q, re_2q+1, im_2q+1) of memory into pair q.
+__device__ __forceinline__ void cstate_set(CState& s, int q, float4 v) {
+  s.re[q] = make_float2(v.x, v.z);
+  s.im[q] = make_float2(v.y, v.w);
+}
+
 // One token of one lane: the state advanced, and Re(sum_n C_n h_n) returned
-// (read-out accumulated in a fixed order: (Re C Re h, Im C Im h) summed over
-// n as a packed pair, then the two parts subtracted).  vp: the previous
-// token's state input (trapezoidal only).
-// NM < kModes: only modes 0..NM-1 advance (the carry walk's modes whose
+// (per mode pair, Re C Re h and Im C Im h accumulated as packed pairs over
+// the pairs in order, then the halves summed and the two parts subtracted).
+// Q: the token's widened B/C row, per mode pair q the quads Q[2q] =
+// (Re B_2q, Re B_2q+1, Im B_2q, Im B_2q+1) and Q[2q+1] the same of C.
+// vp: the previous token's state input (trapezoidal only).
+// NP < kPairs: only pairs 0..NP-1 advance (the carry walk's modes whose
 // weight to the boundary is still above the drop bound; the others stay).
-template <bool kTrap, bool kRead, int NM = kModes>
+template <bool kTrap, bool kRead, int NP = kPairs>
 __device__ __forceinline__ float ctoken(const CChannel& ch, CState& st, CState& vp, float u, float dt,
                                         const float4 (&Q)[kModes]) {
-  const float hdt = __fmul_rn(0.5f, dt);
-  float2 acc = make_float2(0.0f, 0.0f);
+  float2 are[NP], aim[NP];
+  calphas<NP>(ch, dt, are, aim);
+  const float2 u2 = make_float2(u, u);
+  const float h = kTrap ? __fmul_rn(0.5f, dt) : dt;  // the input's weight: dt/2 (trapezoidal) or dt
+  const float2 h2 = make_float2(h, h);
+  float2 accre = make_float2(0.0f, 0.0f), accim = make_float2(0.0f, 0.0f);
 #pragma unroll
-  for (int n = 0; n < NM; ++n) {
-    const float2 al = cexp_step(ch.a2[n], ch.tu[n], ch.tl[n], dt);
-    const float2 v = make_float2(__fmul_rn(Q[n].x, u), __fmul_rn(Q[n].y, u));
+  for (int q = 0; q < NP; ++q) {
+    const float2 vre = __fmul2_rn(make_float2(Q[2 * q].x, Q[2 * q].y), u2);
+    const float2 vim = __fmul2_rn(make_float2(Q[2 * q].z, Q[2 * q].w), u2);
     if (kTrap) {
-      const float2 g = make_float2(__fmaf_rn(hdt, vp.h[n].x, st.h[n].x), __fmaf_rn(hdt, vp.h[n].y, st.h[n].y));
-      st.h[n] = cmul_add(al, g, make_float2(__fmul_rn(hdt, v.x), __fmul_rn(hdt, v.y)));
-      vp.h[n] = v;
-    } else {
-      st.h[n] = cmul_add(al, st.h[n], make_float2(__fmul_rn(dt, v.x), __fmul_rn(dt, v.y)));
+      st.re[q] = __ffma2_rn(h2, vp.re[q], st.re[q]);
+      st.im[q] = __ffma2_rn(h2, vp.im[q], st.im[q]);
+      vp.re[q] = vre;
+      vp.im[q] = vim;
     }
-    if (kRead) acc = __ffma2_rn(make_float2(Q[n].z, Q[n].w), st.h[n], acc);
+    cmad2(are[q], aim[q], st.re[q], st.im[q], __fmul2_rn(h2, vre), __fmul2_rn(h2, vim));
+    if (kRead) {
+      accre = __ffma2_rn(make_float2(Q[2 * q + 1].x, Q[2 * q + 1].y), st.re[q], accre);
+      accim = __ffma2_rn(make_float2(Q[2 * q + 1].z, Q[2 * q + 1].w), st.im[q], accim);
+    }
   }
-  return __fsub_rn(acc.x, acc.y);
+  return __fsub_rn(__fadd_rn(accre.x, accre.y), __fadd_rn(accim.x, accim.y));
+}
+
+// acc += exp(s lambda) h, every mode (a carry weight times a state).
+__device__ __forceinline__ void cstate_add_weighted(const CChannel& ch, float s, const CState& h, CState& acc) {
+  float2 are[kPairs], aim[kPairs];
+  calphas<kPairs>(ch, s, are, aim);
+#pragma unroll
+  for (int q = 0; q < kPairs; ++q) {
+    float2 re = h.re[q], im = h.im[q];
+    cmad2(are[q], aim[q], re, im, acc.re[q], acc.im[q]);
+    acc.re[q] = re;
+    acc.im[q] = im;
+  }
 }
 
 __device__ __forceinline__ void cstate_zero(CState& s) {
 #pragma unroll
-  for (int n = 0; n < kModes; ++n) s.h[n] = make_float2(0.0f, 0.0f);
+  for (int q = 0; q < kPairs; ++q) {
+    s.re[q] = make_float2(0.0f, 0.0f);
+    s.im[q] = make_float2(0.0f, 0.0f);
+  }
 }
 
 __device__ __forceinline__ void cstate_load(CState& s, const float* p) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float4 v = reinterpret_cast<const float4*>(p)[q];
-    s.h[2 * q] = make_float2(v.x, v.y);
-    s.h[2 * q + 1] = make_float2(v.z, v.w);
-  }
+  for (int q = 0; q < kPairs; ++q) cstate_set(s, q, reinterpret_cast<const float4*>(p)[q]);
 }
 
 __device__ __forceinline__ void cstate_store(const CState& s, float* p) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
-    reinterpret_cast<float4*>(p)[q] = make_float4(s.h[2 * q].x, s.h[2 * q].y, s.h[2 * q + 1].x, s.h[2 * q + 1].y);
+  for (int q = 0; q < kPairs; ++q)
+    reinterpret_cast<float4*>(p)[q] = make_float4(s.re[q].x, s.im[q].x, s.re[q].y, s.im[q].y);
+}
+
+// The state input v = B u of a token from its widened B/C row (global).
+__device__ __forceinline__ void cinput_from_row(CState& v, const float* row, float u) {
+  const float2 u2 = make_float2(u, u);
+#pragma unroll
+  for (int q = 0; q < kPairs; ++q) {
+    const float4 b = __ldg(reinterpret_cast<const float4*>(row) + 2 * q);
+    v.re[q] = __fmul2_rn(make_float2(b.x, b.y), u2);
+    v.im[q] = __fmul2_rn(make_float2(b.z, b.w), u2);
+  }
 }
 
 // Raw input of channel c at token tau (tau < 0: conv_state0, or zero).
@@ -191,12 +268,7 @@ __device__ __forceinline__ void cvprev_at(CState& vp, const ComplexParams& p, co
   }
   const float xm4 = cinput_at<IO>(p, b, (long)t0 - 4, cl);
   const float u = silu(conv4(ch.w, ch.bias, xm4, xm3, xm2, xm1));
-  const float4* row = reinterpret_cast<const float4*>(p.bc + ((size_t)b * p.seqlen + t0 - 1) * kBC);
-#pragma unroll
-  for (int n = 0; n < kModes; ++n) {
-    const float4 q = __ldg(row + n);
-    vp.h[n] = make_float2(__fmul_rn(q.x, u), __fmul_rn(q.y, u));
-  }
+  cinput_from_row(vp, p.bc + ((size_t)b * p.seqlen + t0 - 1) * kBC, u);
 }
 
 // One chunk of one channel group (lane = channel) of one batch row.  kSummary
@@ -208,6 +280,78 @@ __device__ __forceinline__ void cvprev_at(CState& vp, const ComplexParams& p, co
 // and conv_state0, count themselves done on the group's chunk-0 flag, which
 // the last chunk's warp checks before it writes the final states that may
 // alias them.
+// Token r of a staged tile (x, dt_raw, B/C rows; z when kY): the state
+// advanced, y stored where wy holds (kY), dt summed into sdt (kSum).
+// kSmall: the tile's dt_raw all lie in softplus's small region.
+template <typename IO, typename Stage, bool kTrap, bool kY, bool kSum, int NP, bool kSmall>
+__device__ __forceinline__ void ctoken_one(const Stage& S, int r, int lane, const CChannel& ch, CState& st,
+                                           CState& vp, float& sdt, float& xm3, float& xm2, float& xm1, bool wy,
+                                           IO* ytile, int D) {
+  const float xv = to_f32(S.x[r][lane]);
+  const float u = silu(conv4(ch.w, ch.bias, xm3, xm2, xm1, xv));
+  xm3 = xm2;
+  xm2 = xm1;
+  xm1 = xv;
+  const float dt = softplus_sel<kSmall>(to_f32(S.dt[r][lane]));
+  float4 Q[kModes];
+  load_quads(&S.bc[r][0], Q);
+  const float yss = ctoken<kTrap, kY, NP>(ch, st, vp, u, dt, Q);
+  if (kSum) sdt = __fadd_rn(sdt, dt);
+  if constexpr (kY) {
+    const float gz = silu(to_f32(S.z[r][lane]));
+    st_global_if(wy, ytile + (size_t)r * D, from_f32<IO>(gate_out(yss, ch.Dc, u, gz)));
+  }
+}
+
+// Tokens r and r+1 of a tile whose dt_raw all lie in softplus's small
+// region: as ctoken_one on each, with the per-token scalar work (conv, SiLU,
+// softplus, SiLU(z), gate) of the two as packed f32x2 operations -- the same
+// operations on each token, so the same bits.
+template <typename IO, typename Stage, bool kTrap, bool kY, bool kSum, int NP>
+__device__ __forceinline__ void ctoken_two(const Stage& S, int r, int lane, const CChannel& ch, CState& st,
+                                           CState& vp, float& sdt, float& xm3, float& xm2, float& xm1, bool wy,
+                                           IO* ytile, int D) {
+  const float x0 = to_f32(S.x[r][lane]);
+  const float x1 = to_f32(S.x[r + 1][lane]);
+  const float2 u = silu_x2(conv4_x2(ch.w, ch.bias, xm3, xm2, xm1, x0, x1));
+  xm3 = xm1;
+  xm2 = x0;
+  xm1 = x1;
+  const float2 dt = softplus_small_raw_x2(make_float2(to_f32(S.dt[r][lane]), to_f32(S.dt[r + 1][lane])));
+  float4 Q[kModes];
+  load_quads(&S.bc[r][0], Q);
+  const float y0 = ctoken<kTrap, kY, NP>(ch, st, vp, u.x, dt.x, Q);
+  load_quads(&S.bc[r + 1][0], Q);
+  const float y1 = ctoken<kTrap, kY, NP>(ch, st, vp, u.y, dt.y, Q);
+  if (kSum) sdt = __fadd_rn(__fadd_rn(sdt, dt.x), dt.y);
+  if constexpr (kY) {
+    const float2 gz = silu_x2(make_float2(to_f32(S.z[r][lane]), to_f32(S.z[r + 1][lane])));
+    const float2 yv = gate_out_x2(make_float2(y0, y1), ch.Dc, u, gz);
+    st_global_if(wy, ytile + (size_t)r * D, from_f32<IO>(yv.x));
+    st_global_if(wy, ytile + (size_t)(r + 1) * D, from_f32<IO>(yv.y));
+  }
+}
+
+// One staged tile of `rows` tokens, token pairs in tiles whose dt_raw all
+// lie in softplus's small region (checked over the warp's active lanes).
+template <typename IO, typename Stage, bool kTrap, bool kY, bool kSum, int NP>
+__device__ __forceinline__ void ctile(const Stage& S, int rows, int lane, bool active, const CChannel& ch,
+                                      CState& st, CState& vp, float& sdt, float& xm3, float& xm2, float& xm1,
+                                      bool wy, IO* ytile, int D) {
+  if (small_dt_tile<IO>(S.dt, rows, lane, active)) {
+    int r = 0;
+#pragma unroll 1
+    for (; r + 1 < rows; r += 2)
+      ctoken_two<IO, Stage, kTrap, kY, kSum, NP>(S, r, lane, ch, st, vp, sdt, xm3, xm2, xm1, wy, ytile, D);
+    if (r < rows)
+      ctoken_one<IO, Stage, kTrap, kY, kSum, NP, true>(S, r, lane, ch, st, vp, sdt, xm3, xm2, xm1, wy, ytile, D);
+  } else {
+#pragma unroll 2
+    for (int r = 0; r < rows; ++r)
+      ctoken_one<IO, Stage, kTrap, kY, kSum, NP, false>(S, r, lane, ch, st, vp, sdt, xm3, xm2, xm1, wy, ytile, D);
+  }
+}
+
 template <typename IO, bool kTrap, bool kSummary>
 __device__ __forceinline__ void complex_pass(const CUtensorMap& tm_x, const CUtensorMap& tm_z,
                                              const CUtensorMap& tm_dt, const CUtensorMap& tm_bc,
@@ -276,11 +420,7 @@ __device__ __forceinline__ void complex_pass(const CUtensorMap& tm_x, const CUte
     } else {
       const float4* src = reinterpret_cast<const float4*>(p.carry + (((size_t)b * p.n_chunks + j) * D + cl) * 16);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {  // from L2: written by another SM during this launch
-        const float4 v = __ldcg(src + q);
-        st.h[2 * q] = make_float2(v.x, v.y);
-        st.h[2 * q + 1] = make_float2(v.z, v.w);
-      }
+      for (int q = 0; q < kPairs; ++q) cstate_set(st, q, __ldcg(src + q));  // from L2: written by another SM during this launch
     }
   } else if (kSummary || (j == 0 && !folded && p.h0 == nullptr)) {
     cstate_zero(st);
@@ -346,23 +486,8 @@ __device__ __forceinline__ void complex_pass(const CUtensorMap& tm_x, const CUte
     ok = __all_sync(0xffffffffu, mine);
     if (!ok) break;
     IO* ytile = kY ? yrow + (size_t)k * kT * D : nullptr;
-#pragma unroll 2
-    for (int r = 0; r < rows; ++r) {
-      const float xv = to_f32(S.x[r][lane]);
-      const float u = silu(conv4(ch.w, ch.bias, xm3, xm2, xm1, xv));
-      xm3 = xm2;
-      xm2 = xm1;
-      xm1 = xv;
-      const float dt = softplus(to_f32(S.dt[r][lane]));
-      float4 Q[kModes];
-      load_quads(&S.bc[r][0], Q);
-      const float yss = ctoken<kTrap, kY>(ch, st, vp, u, dt, Q);
-      if (kSummary) sdt = __fadd_rn(sdt, dt);
-      if (kY) {
-        const float gz = silu(to_f32(S.z[r][lane]));
-        st_global_if(wy, ytile + (size_t)r * D, from_f32<IO>(gate_out(yss, ch.Dc, u, gz)));
-      }
-    }
+    ctile<IO, MainStage<IO>, kTrap, kY, kSummary, kPairs>(S, rows, lane, active, ch, st, vp, sdt, xm3, xm2, xm1,
+                                                          wy, ytile, D);
     __syncwarp();  // every lane is done with stage s
     if (lane == 0 && k + kStages < n_tiles) {
       const uint32_t bar = smem_u32(&sm.full[s]);
@@ -406,12 +531,7 @@ __device__ __forceinline__ void complex_pass(const CUtensorMap& tm_x, const CUte
       if (!kTrap) {  // Euler keeps no previous input: the last token's, from its inputs
         const float u =
             silu(conv4(ch.w, ch.bias, cinput_at<IO>(p, b, (long)p.seqlen - 4, c), xm3, xm2, xm1));
-        const float4* row = reinterpret_cast<const float4*>(p.bc + ((size_t)b * p.seqlen + p.seqlen - 1) * kBC);
-#pragma unroll
-        for (int n = 0; n < kModes; ++n) {
-          const float4 q = __ldg(row + n);
-          vp.h[n] = make_float2(__fmul_rn(q.x, u), __fmul_rn(q.y, u));
-        }
+        cinput_from_row(vp, p.bc + ((size_t)b * p.seqlen + p.seqlen - 1) * kBC, u);
       }
       cstate_store(vp, p.final_v + sidx);
     }
@@ -437,23 +557,13 @@ __global__ void __launch_bounds__(kLanes)
                                     blockIdx.y, blockIdx.z, false);
 }
 
-// One full tile of a carry piece: modes 0..NM-1 advanced, the dt summed.
-template <typename IO, bool kTrap, int NM>
-__device__ __forceinline__ void ccarry_tile(const SummaryStage<IO>& S, int lane, const CChannel& ch, CState& st,
-                                            CState& vp, float& sdt, float& xm3, float& xm2, float& xm1) {
-#pragma unroll 2
-  for (int r = 0; r < kT; ++r) {
-    const float xv = to_f32(S.x[r][lane]);
-    const float u = silu(conv4(ch.w, ch.bias, xm3, xm2, xm1, xv));
-    xm3 = xm2;
-    xm2 = xm1;
-    xm1 = xv;
-    const float dt = softplus(to_f32(S.dt[r][lane]));
-    float4 Q[kModes];
-    load_quads(&S.bc[r][0], Q);
-    (void)ctoken<kTrap, false, NM>(ch, st, vp, u, dt, Q);
-    sdt = __fadd_rn(sdt, dt);
-  }
+// One full tile of a carry piece: mode pairs 0..NP-1 advanced, the dt summed.
+template <typename IO, bool kTrap, int NP>
+__device__ __forceinline__ void ccarry_tile(const SummaryStage<IO>& S, int lane, bool active, const CChannel& ch,
+                                            CState& st, CState& vp, float& sdt, float& xm3, float& xm2,
+                                            float& xm1) {
+  ctile<IO, SummaryStage<IO>, kTrap, false, true, NP>(S, kT, lane, active, ch, st, vp, sdt, xm3, xm2, xm1, false,
+                                                      static_cast<IO*>(nullptr), 0);
 }
 
 // The walked chunked mode's carry walk: one warp per (chunk boundary j =
@@ -507,9 +617,9 @@ __device__ __forceinline__ void ccarry_warp(const CUtensorMap& tm_x, const CUten
 
   CChannel ch;
   load_cchannel(ch, p, cl);
-  float a2max = ch.a2[0];  // the slowest decay of this channel
+  float a2max = fmaxf(ch.a2[0].x, ch.a2[0].y);  // the slowest decay of this channel
 #pragma unroll
-  for (int n = 1; n < kModes; ++n) a2max = fmaxf(a2max, ch.a2[n]);
+  for (int q = 1; q < kPairs; ++q) a2max = fmaxf(a2max, fmaxf(ch.a2[q].x, ch.a2[q].y));
   CState acc, st, vp;
   cstate_zero(acc);
   cstate_zero(st);
@@ -523,7 +633,7 @@ __device__ __forceinline__ void ccarry_warp(const CUtensorMap& tm_x, const CUten
   if (kTrap) cvprev_at<IO>(vp, p, ch, b, t0, cl, xm3, xm2, xm1);
   else cstate_zero(vp);
 
-  int n_modes = kModes;  // leading modes the current piece advances
+  int n_pairs = kPairs;  // leading mode pairs the current piece advances
   bool ok = true, done = false;
   int k = 0;
   for (; k < n_tiles; ++k) {
@@ -532,21 +642,17 @@ __device__ __forceinline__ void ccarry_warp(const CUtensorMap& tm_x, const CUten
     const bool mine = mbar_wait_bounded(smem_u32(&sm.full[s]), (k / kStages) & 1, p.timeout_ns);
     ok = __all_sync(0xffffffffu, mine);
     if (!ok) break;
-    if (n_modes == 1)
-      ccarry_tile<IO, kTrap, 1>(S, lane, ch, st, vp, sdt, xm3, xm2, xm1);
-    else if (n_modes == 2)
-      ccarry_tile<IO, kTrap, 2>(S, lane, ch, st, vp, sdt, xm3, xm2, xm1);
-    else if (n_modes <= 4)
-      ccarry_tile<IO, kTrap, 4>(S, lane, ch, st, vp, sdt, xm3, xm2, xm1);
+    if (n_pairs == 1)
+      ccarry_tile<IO, kTrap, 1>(S, lane, active, ch, st, vp, sdt, xm3, xm2, xm1);
+    else if (n_pairs == 2)
+      ccarry_tile<IO, kTrap, 2>(S, lane, active, ch, st, vp, sdt, xm3, xm2, xm1);
     else
-      ccarry_tile<IO, kTrap, 8>(S, lane, ch, st, vp, sdt, xm3, xm2, xm1);
+      ccarry_tile<IO, kTrap, 4>(S, lane, active, ch, st, vp, sdt, xm3, xm2, xm1);
     __syncwarp();  // every lane is done with stage s
     if (lane == 0 && k + kStages < n_tiles)
       issue_carry_tile<IO>(sm, s, &tm_x, &tm_dt, &tm_bc, c0, wk.tile_of(k + kStages), b);
     if (--left == 0) {  // piece done: acc += W hloc, W from the piece's end to the boundary
-#pragma unroll
-      for (int n = 0; n < kModes; ++n)
-        acc.h[n] = cmul_add(cexp_step(ch.a2[n], ch.tu[n], ch.tl[n], s_after), st.h[n], acc.h[n]);
+      cstate_add_weighted(ch, s_after, st, acc);
       s_after = __fadd_rn(s_after, sdt);
       if ((p.flags & kFlagExactCarry) == 0 &&
           __all_sync(0xffffffffu, !active || __fmul_rn(a2max, s_after) < kCarryDropLog2)) {
@@ -559,14 +665,14 @@ __device__ __forceinline__ void ccarry_warp(const CUtensorMap& tm_x, const CUten
         cstate_zero(st);
         sdt = 0.0f;
         // modes whose weight to the boundary fell below the drop bound add
-        // nothing from here on: the piece advances the leading ones up to
-        // the last mode still above it
+        // nothing from here on: the piece advances the leading pairs up to
+        // the last pair with a mode still above it
         if ((p.flags & kFlagExactCarry) == 0) {
           int last = -1;
 #pragma unroll
-          for (int n = 0; n < kModes; ++n)
-            if (__fmul_rn(ch.a2[n], s_after) >= kCarryDropLog2) last = n;
-          n_modes = __reduce_max_sync(0xffffffffu, active ? last + 1 : 0);
+          for (int q = 0; q < kPairs; ++q)
+            if (__fmul_rn(fmaxf(ch.a2[q].x, ch.a2[q].y), s_after) >= kCarryDropLog2) last = q;
+          n_pairs = __reduce_max_sync(0xffffffffu, active ? last + 1 : 0);
         }
         t0 = wk.tile_of(k + 1) * kT;
         xm3 = cinput_at<IO>(p, b, (long)t0 - 3, cl);
@@ -608,16 +714,10 @@ __device__ __forceinline__ void ccarry_warp(const CUtensorMap& tm_x, const CUten
       } else {
         const float4* src = reinterpret_cast<const float4*>(p.carry + (((size_t)b * p.n_chunks + (j - 1)) * D + cl) * 16);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 v = __ldcg(src + q);
-          prev.h[2 * q] = make_float2(v.x, v.y);
-          prev.h[2 * q + 1] = make_float2(v.z, v.w);
-        }
+        for (int q = 0; q < kPairs; ++q) cstate_set(prev, q, __ldcg(src + q));
       }
     }
-#pragma unroll
-    for (int n = 0; n < kModes; ++n)
-      acc.h[n] = cmul_add(cexp_step(ch.a2[n], ch.tu[n], ch.tl[n], s_after), prev.h[n], acc.h[n]);
+    cstate_add_weighted(ch, s_after, prev, acc);
   }
 
   // publish carry_j (also after a failure, so that no later boundary waits in vain)
@@ -682,8 +782,8 @@ __global__ void __launch_bounds__(256) complex_fold_kernel(const __grid_constant
     CState hl;
     cstate_load(hl, p.hloc + cj * 16);
     const float S = p.sdt[cj];
-#pragma unroll
-    for (int n = 0; n < kModes; ++n) h.h[n] = cmul_add(cexp_step(ch.a2[n], ch.tu[n], ch.tl[n], S), h.h[n], hl.h[n]);
+    cstate_add_weighted(ch, S, h, hl);  // hl = W_j h_in_j + hloc_j
+    h = hl;
     cstate_store(h, p.carry + (((size_t)b * p.n_chunks + j + 1) * D + c) * 16);
   }
 }

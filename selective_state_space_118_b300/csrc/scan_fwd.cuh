@@ -83,11 +83,16 @@ __device__ __forceinline__ float input_at(const ScanParams& p, int b, long tau, 
 // they are (B, L, 16) tensors; more when they are columns of a wider
 // projection output).
 //
+// kModePairs (the complex scan, whose rows hold 8 complex numbers (re, im)):
+// per pair of modes q = 0..3 the quads bc[row][8q .. 8q+3] = (Re B_2q,
+// Re B_2q+1, Im B_2q, Im B_2q+1) and bc[row][8q+4 .. 8q+7] the same of C, so
+// that each quad gives a lane two aligned register pairs across two modes.
+//
 // Launched as a programmatic dependent (the forward's chunked mode) it waits
 // for the kernel before it (the previous call's scan, which reads bc) before
 // touching memory, then lets the scan after it launch; block 0 also zeroes
 // that scan's ticket counter and flags (n_counters words, when given).
-template <typename IO>
+template <typename IO, bool kModePairs>
 __global__ void __launch_bounds__(256) bc_widen_kernel(const IO* __restrict__ Bm, const IO* __restrict__ Cm,
                                                        float* __restrict__ bc, long rows, int ld,
                                                        unsigned* __restrict__ counters, int n_counters) {
@@ -95,14 +100,20 @@ __global__ void __launch_bounds__(256) bc_widen_kernel(const IO* __restrict__ Bm
   griddep_launch_dependents();
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0u;
-  const long n = rows * 8;  // 8 pair quads per row
+  const long n = rows * 8;  // 8 quads per row
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
     const long r = i >> 3;
     const int k = (int)(i & 7);
-    const IO* b = Bm + r * ld + 2 * k;
-    const IO* c = Cm + r * ld + 2 * k;
-    *reinterpret_cast<float4*>(bc + r * kBC + 4 * k) =
-        make_float4(to_f32(b[0]), to_f32(b[1]), to_f32(c[0]), to_f32(c[1]));
+    float4 v;
+    if (kModePairs) {
+      const IO* s = ((k & 1) ? Cm : Bm) + r * ld + 4 * (k >> 1);
+      v = make_float4(to_f32(s[0]), to_f32(s[2]), to_f32(s[1]), to_f32(s[3]));
+    } else {
+      const IO* b = Bm + r * ld + 2 * k;
+      const IO* c = Cm + r * ld + 2 * k;
+      v = make_float4(to_f32(b[0]), to_f32(b[1]), to_f32(c[0]), to_f32(c[1]));
+    }
+    *reinterpret_cast<float4*>(bc + r * kBC + 4 * k) = v;
   }
 }
 
