@@ -252,28 +252,59 @@ __device__ __forceinline__ void main_tile(const MainStage<IO>& S, int rows, int 
 // One full tile of a carry piece (state and dt sum only), advancing the
 // first kPairs state pairs (the later ones, whose decay to the boundary is
 // already below the drop bound, stay as they are: zero within the piece).
+// Tiles whose dt_raw all lie in softplus's small region (kSmall) take their
+// tokens two at a time, the per-token scalar work (conv, SiLU, softplus,
+// dt*u) of the two as packed f32x2 operations: the same operations on each
+// token, so the same bits.
 template <typename IO, bool kSmall, int kPairs>
 __device__ __forceinline__ void summary_tile(const SummaryStage<IO>& S, int lane, const Channel& ch, State16& st,
                                              float& sdt, float& xm3, float& xm2, float& xm1) {
-#pragma unroll(kScanUnroll)
-  for (int r = 0; r < kT; ++r) {
-    const float xv = to_f32(S.x[r][lane]);
-    const float u = silu(conv4(ch.w, ch.bias, xm3, xm2, xm1, xv));
-    xm3 = xm2;
-    xm2 = xm1;
-    xm1 = xv;
-    const float dt = softplus_sel<kSmall>(to_f32(S.dt[r][lane]));
-    const float2 d2 = make_float2(dt, dt);
-    const float dtu = __fmul_rn(dt, u);
-    const float2 u2 = make_float2(dtu, dtu);
+  if constexpr (kSmall) {
+#pragma unroll(kScanUnroll / 2)
+    for (int r = 0; r < kT; r += 2) {
+      const float x0 = to_f32(S.x[r][lane]);
+      const float x1 = to_f32(S.x[r + 1][lane]);
+      const float2 u = silu_x2(conv4_x2(ch.w, ch.bias, xm3, xm2, xm1, x0, x1));
+      xm3 = xm1;
+      xm2 = x0;
+      xm1 = x1;
+      const float2 dt = softplus_small_raw_x2(make_float2(to_f32(S.dt[r][lane]), to_f32(S.dt[r + 1][lane])));
+      const float2 dtu = __fmul2_rn(dt, u);
 #pragma unroll
-    for (int k = 0; k < kPairs; ++k) {  // the operations of drive16_q and state16_apply, pair by pair
-      const float4 q = *reinterpret_cast<const float4*>(&S.bc[r][4 * k]);
-      const float2 x = __fmul2_rn(d2, ch.a2[k]);
-      const float2 dA = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-      st.h[k] = __ffma2_rn(dA, st.h[k], __fmul2_rn(u2, make_float2(q.x, q.y)));
+      for (int i = 0; i < 2; ++i) {
+        const float2 d2 = i ? make_float2(dt.y, dt.y) : make_float2(dt.x, dt.x);
+        const float2 u2 = i ? make_float2(dtu.y, dtu.y) : make_float2(dtu.x, dtu.x);
+#pragma unroll
+        for (int k = 0; k < kPairs; ++k) {
+          const float4 q = *reinterpret_cast<const float4*>(&S.bc[r + i][4 * k]);
+          const float2 x = __fmul2_rn(d2, ch.a2[k]);
+          const float2 dA = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          st.h[k] = __ffma2_rn(dA, st.h[k], __fmul2_rn(u2, make_float2(q.x, q.y)));
+        }
+      }
+      sdt = __fadd_rn(__fadd_rn(sdt, dt.x), dt.y);
     }
-    sdt = __fadd_rn(sdt, dt);
+  } else {
+#pragma unroll(kScanUnroll)
+    for (int r = 0; r < kT; ++r) {
+      const float xv = to_f32(S.x[r][lane]);
+      const float u = silu(conv4(ch.w, ch.bias, xm3, xm2, xm1, xv));
+      xm3 = xm2;
+      xm2 = xm1;
+      xm1 = xv;
+      const float dt = softplus_sel<kSmall>(to_f32(S.dt[r][lane]));
+      const float2 d2 = make_float2(dt, dt);
+      const float dtu = __fmul_rn(dt, u);
+      const float2 u2 = make_float2(dtu, dtu);
+#pragma unroll
+      for (int k = 0; k < kPairs; ++k) {  // the operations of drive16_q and state16_apply, pair by pair
+        const float4 q = *reinterpret_cast<const float4*>(&S.bc[r][4 * k]);
+        const float2 x = __fmul2_rn(d2, ch.a2[k]);
+        const float2 dA = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        st.h[k] = __ffma2_rn(dA, st.h[k], __fmul2_rn(u2, make_float2(q.x, q.y)));
+      }
+      sdt = __fadd_rn(sdt, dt);
+    }
   }
 }
 
