@@ -293,15 +293,21 @@ def mufu_peak():
 MUFU_SLOTS_PER_ELEMENT = 16 + 3 + 2 * 2
 
 
-def compute_roofline(elems_per_s, elems_per_step, t_step_s):
+# The complex scan's: per mode (8 of them) the decay's ex2 and the turn's sin
+# and cos, plus the SiLUs' and softplus' three ex2 and two reciprocals.
+COMPLEX_MUFU_SLOTS_PER_ELEMENT = 8 * 3 + 3 + 2 * 2
+
+
+def compute_roofline(elems_per_s, elems_per_step, t_step_s, slots=MUFU_SLOTS_PER_ELEMENT,
+                     note="the exponentials alone bound the scan below the HBM roofline: "
+                          "16 decays per element need 16 MUFU slots for 8 bytes"):
     peak, how = mufu_peak()
-    achieved = elems_per_s * MUFU_SLOTS_PER_ELEMENT
+    achieved = elems_per_s * slots
     return {"bound": "alu", "what": "MUFU (special-function unit)", "achieved": achieved, "peak": peak,
             "unit": "MUFU slots/s", "frac": achieved / peak, "peak_source": how,
-            "slots_per_element": MUFU_SLOTS_PER_ELEMENT,
-            "floor_ms_per_step": elems_per_step * MUFU_SLOTS_PER_ELEMENT / peak * 1e3,
-            "note": "the exponentials alone bound the scan below the HBM roofline: "
-                    "16 decays per element need 16 MUFU slots for 8 bytes"}
+            "slots_per_element": slots,
+            "floor_ms_per_step": elems_per_step * slots / peak * 1e3,
+            "note": note}
 
 
 # The backward's instruction mix, measured by ncu on the reverse-sweep kernel
@@ -825,8 +831,11 @@ def bench_complex(w, steps, warmup, local, trapezoidal, n_chunks_req=0):
            "ms_per_call": t * 1e3, "ms_per_call_min": min(per),
            "roofline": {"bound": "hbm", "achieved": alg / t / 1e9, "peak": hbm, "unit": "GB/s",
                         "frac": alg / t / 1e9 / hbm, "peak_source": src, "algorithmic_bytes_per_call": alg,
-                        "note": "MUFU-bound in practice: per element 8 ex2 + 8 sin + 8 cos for the modes' "
-                                "decays and turns, plus the SiLUs and softplus"},
+                        "compute": compute_roofline(
+                            B * L * D / t, B * L * D, t, COMPLEX_MUFU_SLOTS_PER_ELEMENT,
+                            "per element 8 ex2 + 8 sin + 8 cos for the modes' decays and turns, plus the "
+                            "SiLUs and softplus; the kernel is issue- and latency-bound below this floor"),
+                        "note": "compute: the MUFU floor; bytes: far below the HBM roofline"},
            "gpu_launches": (4 if ws_big else 2) * steps, "clocks": clk.summary()}
     del inp, y, ws
     return res
