@@ -426,10 +426,13 @@ mamba_status mamba2_scan_fwd(const mamba2_scan_args *args, void *stream);
  *
  * d_state must be 16, d_conv 4, d_inner as for mamba_scan_fwd.  seqlen may be 0
  * (the final states are then copies of the initial ones, or zeros).
- * Precision: the turn dt theta is reduced to [-pi, pi] exactly (its whole
- * revolutions removed with the product's rounding error kept), but it
- * carries dt's own fp32 rounding (a few 1e-8 of dt): a mode turning by
- * thousands of radians per token loses the fp32 accuracy of its angle.
+ * Precision: a token whose dt keeps every turn dt theta_n of its channel
+ * within [-pi, pi] (dt <= pi / max_n |theta_n|) takes the angle as the fp32
+ * product dt theta_n (one rounding); any other has its turn reduced to
+ * [-pi, pi] exactly (its whole revolutions removed with the product's
+ * rounding error kept).  Either way the angle carries dt's own fp32
+ * rounding (a few 1e-8 of dt): a mode turning by thousands of radians per
+ * token loses the fp32 accuracy of its angle.
  */
 #define MAMBA3_EULER 0
 #define MAMBA3_TRAPEZOIDAL 1
