@@ -118,6 +118,25 @@ def test_fast_turns(rule):
 
 
 @pytest.mark.parametrize("rule", sorted(RULES))
+def test_fast_turns_in_small_dt_tiles(rule):
+    """dt log-uniform in [1e-3, 1e-1] (every tile in softplus's small region,
+    so the tokens go two at a time) with rotation frequencies up to +-200:
+    a token takes its angle dt theta directly only when dt <= pi / max|theta|
+    of its channel, so within one warp and one token pair some lanes take
+    the angle directly and others reduce whole turns (up to 20 radians per
+    token).  Chunked, so the carry walks take both paths too."""
+    B, L, D = 2, 700, 64
+    inp = make(B, L, D, "f32", seed=621)
+    g = torch.Generator(device="cuda").manual_seed(622)
+    inp["theta"] = (torch.rand(D, 8, device="cuda", generator=g) - 0.5) * 400.0
+    inp["theta"][::4] *= 0.05  # a quarter of the channels turn slowly: every token direct
+    dt = torch.exp(math.log(1e-3) + torch.rand(B, L, D, device="cuda", generator=g) * math.log(100.0))
+    inp["dt_raw"] = torch.log(torch.expm1(dt))
+    assert float(inp["dt_raw"].max()) < -2.08  # softplus's small region: token pairs
+    check(inp, run_gpu(inp, RULES[rule], n_chunks=3), RULES[rule], f"{rule} fast turns, small dt")
+
+
+@pytest.mark.parametrize("rule", sorted(RULES))
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_split_calls_equal_one_call_bitwise(rule, io):
     """One pass == the same sequence fed as calls that carry (final_h,
