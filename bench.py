@@ -475,33 +475,35 @@ def bench_e2e(w, inp, out, ws, steps, local, slices):
     bi = sum(h.numel() * h.element_size() for h in host.values())
     bo = y_host.numel() * y_host.element_size()
 
-    # the host link alone, outside the timed region: one step's uploads, then
-    # its downloads, as the same copies with nothing else running
-    def link(direction):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        st = up if direction == "h2d" else down
-        e0.record(st)
-        with torch.cuda.stream(st):
-            for i, (t0_, t1_) in enumerate(slices):
-                s = i % n_sets
-                l = t1_ - t0_
-                if direction == "h2d":
+    # the host link alone, outside the timed region: one step's uploads, its
+    # downloads, and both at once (on their two streams), as the same copies
+    # with nothing else running
+    def link(directions):
+        torch.cuda.synchronize(dev)
+        t0_wall = time.perf_counter()
+        for i, (t0_, t1_) in enumerate(slices):
+            s = i % n_sets
+            l = t1_ - t0_
+            if "h2d" in directions:
+                with torch.cuda.stream(up):
                     for k in names:
                         dev_slice(bufs[s][k], l).copy_(host[k] if one else host[k][:, t0_:t1_], non_blocking=True)
-                else:
+            if "d2h" in directions:
+                with torch.cuda.stream(down):
                     (y_host if one else y_host[:, t0_:t1_]).copy_(dev_slice(ybufs[s], l), non_blocking=True)
-        e1.record(st)
         torch.cuda.synchronize(dev)
-        return (bi if direction == "h2d" else bo) / (e0.elapsed_time(e1) / 1e3) / 1e9
-    h2d, d2h = link("h2d"), link("d2h")
+        moved = (bi if "h2d" in directions else 0) + (bo if "d2h" in directions else 0)
+        return moved / (time.perf_counter() - t0_wall) / 1e9
+    h2d, d2h, both = link(("h2d",)), link(("d2h",)), link(("h2d", "d2h"))
     res = {"t": t, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
            "steps": steps, "ms_per_step": t * 1e3 / steps,
            "pipelining": f"uploads / scans / downloads on three streams, two buffer sets, "
                          f"{len(slices)} call(s) per step",
-           "host_link": {"h2d_gbs": h2d, "d2h_gbs": d2h,
-                         "upload_floor_ms_per_step": bi / h2d / 1e6,
-                         "note": "one step's copies alone, each direction by itself, the same "
-                                 "pinned buffers and calls: the e2e step cannot beat the upload time"}}
+           "host_link": {"h2d_gbs": h2d, "d2h_gbs": d2h, "both_gbs": both,
+                         "floor_ms_per_step": (bi + bo) / both / 1e6,
+                         "note": "one step's copies alone (the same pinned buffers and calls), "
+                                 "each direction by itself and both at once; the two directions "
+                                 "share the link, so a step moving both cannot beat floor_ms_per_step"}}
     del host, y_host, bufs, ybufs
     return res
 
