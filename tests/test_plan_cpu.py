@@ -107,3 +107,18 @@ def test_mamba2_workspace_follows_its_layout(B, L, H):
     prefix (128 x 2 fp32)."""
     k = B * H * -(-L // 128)
     assert ops.mamba2_scan_workspace_size(B, L, H) == 2 * r256(k * 16 * 64 * 4) + r256(k * 4) + r256(k * 128 * 2 * 4)
+
+
+@pytest.mark.parametrize("L,n_best", [(4096, 10), (32768, 9), (262144, 9)])
+def test_default_plan_at_the_measured_shapes(L, n_best):
+    """At 8,192 channels, batch 1, on a 148-SM B300 (16 one-warp tasks per
+    SM), the default plan takes the chunk counts that measured fastest:
+    4,096-token calls 10 chunks (8-12 chunks: 17.6, 16.1, 15.5, 16.9, 17.6 ms
+    per 64 calls), 32k 9 (9-12: 1.28, 1.37-1.41, 1.32, 1.41 ms), 256k in
+    one call 9."""
+    import torch
+    if torch.cuda.is_available() and torch.cuda.get_device_properties(0).multi_processor_count != 148:
+        pytest.skip("the counts were measured on a 148-SM device")
+    pl = ops.mamba_scan_plan(1, L, 8192, 0)
+    assert pl["n_chunks"] == n_best
+    assert pl["piece_len"] == 64
